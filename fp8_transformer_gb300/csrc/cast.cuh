@@ -1,0 +1,114 @@
+// Output stage of the bandwidth-bound kernels: fp32 results -> fp32 / bf16 / E4M3 storage,
+// with the per-tensor amax and scale bookkeeping.
+#pragma once
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace te {
+
+struct CastState {
+  float scale = 1.0f;
+  float scale_inv = 1.0f;
+  int out_dtype = TE_BF16;
+  int fake_quant = 0;
+  int store = 1;
+};
+
+// Reads the scale (given, or derived from this call's amax); the first thread of the grid
+// publishes scale / scale_inv when the pass stores.
+__device__ __forceinline__ CastState cast_begin(const CastSpec& c) {
+  CastState s;
+  s.out_dtype = c.out_dtype;
+  s.fake_quant = c.fake_quant;
+  s.store = c.store;
+  if (c.out_dtype == TE_E4M3 || c.fake_quant) {
+    if (c.amax_in) s.scale = scale_from_amax(*c.amax_in);
+    else if (c.scale) s.scale = *c.scale;
+    s.scale_inv = 1.0f / s.scale;
+  }
+  if (c.store && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0 && threadIdx.y == 0) {
+    if (c.scale_out) *c.scale_out = s.scale;
+    if (c.scale_inv_out) *c.scale_inv_out = s.scale_inv;
+  }
+  return s;
+}
+
+// E4M3 round trip of one value: fp32(decode(E4M3(fp32(v * scale))) * scale_inv).
+__device__ __forceinline__ float fake_quant1(float v, float scale, float scale_inv) {
+  float2 d = unpack_e4m3x2(pack_e4m3x2(v * scale, 0.0f));
+  return d.x * scale_inv;
+}
+
+// Stores N (4 or 8) consecutive values at element index `idx` (a multiple of N) of `out`.
+template <int N>
+__device__ __forceinline__ void cast_store(void* out, int64_t idx, const float (&y)[N],
+                                           const CastState& cs) {
+  static_assert(N == 4 || N == 8, "vector of 4 or 8");
+  float v[N];
+#pragma unroll
+  for (int i = 0; i < N; ++i) v[i] = cs.fake_quant ? fake_quant1(y[i], cs.scale, cs.scale_inv) : y[i];
+  if (cs.out_dtype == TE_F32) {
+    float4* p = reinterpret_cast<float4*>(static_cast<float*>(out) + idx);
+    p[0] = make_float4(v[0], v[1], v[2], v[3]);
+    if constexpr (N == 8) p[1] = make_float4(v[4], v[5], v[6], v[7]);
+  } else if (cs.out_dtype == TE_BF16) {
+    uint16_t* base = static_cast<uint16_t*>(out) + idx;
+    if constexpr (N == 8) {
+      *reinterpret_cast<uint4*>(base) = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
+                                                   pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
+    } else {
+      *reinterpret_cast<uint2*>(base) = make_uint2(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]));
+    }
+  } else {  // E4M3 codes
+    const float s = cs.scale;
+    uint8_t* base = static_cast<uint8_t*>(out) + idx;
+    if constexpr (N == 8) {
+      *reinterpret_cast<uint2*>(base) = make_uint2(pack_e4m3x4(y[0] * s, y[1] * s, y[2] * s, y[3] * s),
+                                                   pack_e4m3x4(y[4] * s, y[5] * s, y[6] * s, y[7] * s));
+    } else {
+      *reinterpret_cast<uint32_t*>(base) = pack_e4m3x4(y[0] * s, y[1] * s, y[2] * s, y[3] * s);
+    }
+  }
+}
+
+// Loads 16 bytes of T (8 bf16 or 4 fp32) as fp32.
+template <typename T>
+struct Vec16;
+
+template <>
+struct Vec16<__nv_bfloat16> {
+  static constexpr int N = 8;
+  __device__ __forceinline__ static void load(const void* base, int64_t idx, float (&v)[8]) {
+    uint4 u = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(base) + idx));
+    v[0] = bf16_lo(u.x); v[1] = bf16_hi(u.x); v[2] = bf16_lo(u.y); v[3] = bf16_hi(u.y);
+    v[4] = bf16_lo(u.z); v[5] = bf16_hi(u.z); v[6] = bf16_lo(u.w); v[7] = bf16_hi(u.w);
+  }
+  // Unpacks with volatile moves so that the compiler re-expands a packed row on every pass
+  // instead of keeping all of its fp32 copies live (which would double the registers).
+  __device__ __forceinline__ static void unpack(const uint4& u, float (&v)[8]) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      asm volatile("shl.b32 %0, %1, 16;" : "=f"(v[2 * i]) : "r"(w[i]));
+      asm volatile("and.b32 %0, %1, 0xFFFF0000;" : "=f"(v[2 * i + 1]) : "r"(w[i]));
+    }
+  }
+};
+
+template <>
+struct Vec16<float> {
+  static constexpr int N = 4;
+  __device__ __forceinline__ static void load(const void* base, int64_t idx, float (&v)[4]) {
+    float4 u = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(base) + idx));
+    v[0] = u.x; v[1] = u.y; v[2] = u.z; v[3] = u.w;
+  }
+  __device__ __forceinline__ static void unpack(const uint4& u, float (&v)[4]) {
+    asm volatile("mov.b32 %0, %1;" : "=f"(v[0]) : "r"(u.x));
+    asm volatile("mov.b32 %0, %1;" : "=f"(v[1]) : "r"(u.y));
+    asm volatile("mov.b32 %0, %1;" : "=f"(v[2]) : "r"(u.z));
+    asm volatile("mov.b32 %0, %1;" : "=f"(v[3]) : "r"(u.w));
+  }
+};
+
+}  // namespace te

@@ -1,0 +1,138 @@
+// Device helpers shared by the kernels of the fused norm + feed-forward block (sm_103a).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "te_gb300.h"
+
+namespace te {
+
+constexpr float kE4M3Max = 448.0f;
+
+// ------------------------------------------------------------------ conversions ------------
+
+// Two fp32 -> two bf16 (round to nearest even), lo in the low half.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+__device__ __forceinline__ float round_bf16(float v) {
+  return __bfloat162float(__float2bfloat16_rn(v));
+}
+
+// Two fp32 -> two E4M3 bytes, round to nearest even, saturating to +-448 (satfinite).
+// `lo` lands in the low byte.
+__device__ __forceinline__ uint16_t pack_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Four fp32 -> four E4M3 bytes (element 0 in the lowest byte).
+__device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
+  return uint32_t(pack_e4m3x2(a, b)) | (uint32_t(pack_e4m3x2(c, d)) << 16);
+}
+
+// Two E4M3 bytes -> two exact fp32 values (via the exact E4M3 -> f16 conversion).
+__device__ __forceinline__ float2 unpack_e4m3x2(uint16_t v) {
+  uint32_t h2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(v));
+  __half2 h = *reinterpret_cast<__half2*>(&h2);
+  return __half22float2(h);
+}
+
+// ------------------------------------------------------------------ activations -----------
+// Written from their definitions; fp32 throughout.
+
+__device__ __forceinline__ float act_gelu(float h) {
+  const float k0 = 0.7978845608028654f;  // sqrt(2 / pi)
+  const float k1 = 0.044715f;
+  return 0.5f * h * (1.0f + tanhf(k0 * (h + k1 * h * h * h)));
+}
+
+__device__ __forceinline__ float act_silu(float z) { return z / (1.0f + expf(-z)); }
+
+__device__ __forceinline__ float act_relu(float h) { return h > 0.0f ? h : 0.0f; }
+
+// Non-gated activation by id (TE_IDENTITY, TE_RELU, TE_GELU, TE_SILU).
+__device__ __forceinline__ float act_apply(int act, float h) {
+  switch (act) {
+    case TE_RELU: return act_relu(h);
+    case TE_GELU: return act_gelu(h);
+    case TE_SILU: return act_silu(h);
+    default: return h;
+  }
+}
+
+// d/dh of the non-gated activations.
+__device__ __forceinline__ float dact_apply(int act, float h) {
+  switch (act) {
+    case TE_RELU: return h > 0.0f ? 1.0f : 0.0f;
+    case TE_GELU: {
+      const float k0 = 0.7978845608028654f;
+      const float k1 = 0.044715f;
+      float t = tanhf(k0 * (h + k1 * h * h * h));
+      return 0.5f * (1.0f + t) + 0.5f * h * (1.0f - t * t) * k0 * (1.0f + 3.0f * k1 * h * h);
+    }
+    case TE_SILU: {
+      float s = 1.0f / (1.0f + expf(-h));
+      return s * (1.0f + h * (1.0f - s));
+    }
+    default: return 1.0f;
+  }
+}
+
+// ------------------------------------------------------------------ scaling ---------------
+
+// scale = 448 / amax; 1 when amax is 0 or not finite; FLT_MAX when the quotient overflows.
+__device__ __forceinline__ float scale_from_amax(float amax) {
+  if (!(amax > 0.0f) || !isfinite(amax)) return 1.0f;
+  float s = kE4M3Max / amax;
+  if (!isfinite(s)) s = 3.4028234663852886e38f;
+  return s;
+}
+
+// ------------------------------------------------------------------ reductions ------------
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// amax of non-negative floats: their bit patterns order like the values.
+__device__ __forceinline__ void atomic_max_nonneg(float* addr, float v) {
+  if (v > 0.0f) atomicMax(reinterpret_cast<int*>(addr), __float_as_int(v));
+}
+
+// Block-wide max of a per-thread value, then one atomic per block (blockDim.x <= 1024).
+__device__ __forceinline__ void block_amax_commit(float v, float* amax) {
+  __shared__ float red[32];
+  v = warp_max(v);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  if (l == 0) red[w] = v;
+  __syncthreads();
+  if (w == 0) {
+    const int nw = (blockDim.x + 31) >> 5;
+    float m = l < nw ? red[l] : 0.0f;
+    m = warp_max(m);
+    if (l == 0 && amax) atomic_max_nonneg(amax, m);
+  }
+}
+
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+}  // namespace te

@@ -1,0 +1,227 @@
+// Bandwidth-bound kernels of the block: per-tensor quantize, activation, and the backward's
+// fused activation-gradient + bias-reduction + quantize.
+//
+// * quantize (TransformerEngine JAX "LayerNorm Dense" page, Description: the normalized output
+//   and the kernel are quantized before the GEMM): 16-byte vectors, grid-stride, amax by one
+//   integer atomic per block.
+// * act_lu ("Activation" page, Description: the forward rule's activation primitive, optional
+//   FP8 round trip): elementwise; the gated pair reads its gate and linear halves from the two
+//   column halves of the same row.
+// * dact_dbias ("LayerNorm MLP" page, Description, backward: tex.quantize_dact_dbias): each CTA
+//   owns a strip of 32 x 16-byte column vectors and a chunk of rows; every thread keeps its
+//   columns' sums in registers, the 8 warps of the CTA are combined through shared memory in a
+//   fixed order, and one partial row per chunk goes to the workspace.  A second kernel adds the
+//   partial rows in chunk order, so dbias is deterministic.
+#include "cast.cuh"
+#include "common.cuh"
+#include "kernels.h"
+
+namespace te {
+
+namespace {
+
+constexpr int kEwThreads = 256;
+
+unsigned ew_grid(int64_t vectors) {
+  const int64_t per_wave = int64_t(num_sms()) * 8;
+  const int64_t blocks = ceil_div(vectors, kEwThreads);
+  return unsigned(blocks < per_wave ? (blocks > 0 ? blocks : 1) : per_wave);
+}
+
+// ------------------------------------------------------------------ quantize --------------
+
+template <typename T>
+__global__ void __launch_bounds__(kEwThreads) quantize_kernel(QuantizeArgs a) {
+  using V = Vec16<T>;
+  constexpr int E = V::N;
+  const CastState cs = cast_begin(a.cast);
+  const int64_t nvec = a.n / E;
+  float amax = 0.0f;
+  for (int64_t v = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; v < nvec;
+       v += int64_t(gridDim.x) * blockDim.x) {
+    float x[E];
+    V::load(a.x, v * E, x);
+#pragma unroll
+    for (int e = 0; e < E; ++e) amax = fmaxf(amax, fabsf(x[e]));
+    if (cs.store) cast_store<E>(a.out, v * E, x, cs);
+  }
+  block_amax_commit(amax, a.cast.amax_out);
+}
+
+// ------------------------------------------------------------------ act_lu ----------------
+
+template <typename T>
+__global__ void __launch_bounds__(kEwThreads) act_lu_kernel(ActArgs a) {
+  using V = Vec16<T>;
+  constexpr int E = V::N;
+  const CastState cs = cast_begin(a.cast);
+  const bool gated = a.act == TE_SWIGLU;
+  const int64_t n_out = gated ? a.N_in / 2 : a.N_in;
+  const int64_t vec_per_row = n_out / E;
+  const int64_t nvec = a.M * vec_per_row;
+  float amax = 0.0f;
+  for (int64_t v = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; v < nvec;
+       v += int64_t(gridDim.x) * blockDim.x) {
+    const int64_t r = v / vec_per_row;
+    const int64_t c = (v - r * vec_per_row) * E;
+    float y[E];
+    if (gated) {
+      float g[E], l[E];
+      V::load(a.x, r * a.N_in + c, g);
+      V::load(a.x, r * a.N_in + n_out + c, l);
+#pragma unroll
+      for (int e = 0; e < E; ++e) y[e] = act_silu(g[e]) * l[e];
+    } else {
+      float h[E];
+      V::load(a.x, r * a.N_in + c, h);
+#pragma unroll
+      for (int e = 0; e < E; ++e) y[e] = act_apply(a.act, h[e]);
+    }
+#pragma unroll
+    for (int e = 0; e < E; ++e) amax = fmaxf(amax, fabsf(y[e]));
+    if (cs.store) cast_store<E>(a.out, r * n_out + c, y, cs);
+  }
+  block_amax_commit(amax, a.cast.amax_out);
+}
+
+// ------------------------------------------------------------------ dact + dbias ----------
+
+constexpr int kDactWarps = 8;
+constexpr int kDactRows = 128;  // rows per CTA (chunk)
+
+template <typename T>
+__global__ void __launch_bounds__(kDactWarps * 32) dact_dbias_kernel(DactArgs a) {
+  using V = Vec16<T>;
+  constexpr int E = V::N;
+  constexpr int W = 32 * E;  // strip width in columns
+  __shared__ float red[kDactWarps][2][W];
+  const CastState cs = cast_begin(a.cast);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const bool gated = a.act == TE_SWIGLU;
+  const int64_t n_out = gated ? a.N_in / 2 : a.N_in;
+  const int64_t col = (int64_t(blockIdx.x) * 32 + lane) * E;
+  const bool valid = col < n_out;
+  const int64_t r0 = int64_t(blockIdx.y) * kDactRows;
+  const int64_t r1 = r0 + kDactRows < a.M ? r0 + kDactRows : a.M;
+  float acc1[E], acc2[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) { acc1[e] = 0.0f; acc2[e] = 0.0f; }
+  float amax = 0.0f;
+  if (valid) {
+    for (int64_t r = r0 + warp; r < r1; r += kDactWarps) {
+      float dy[E];
+      V::load(a.dy, r * n_out + col, dy);
+      if (gated) {
+        float g[E], l[E], dg[E], dl[E];
+        V::load(a.x, r * a.N_in + col, g);
+        V::load(a.x, r * a.N_in + n_out + col, l);
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const float s = 1.0f / (1.0f + expf(-g[e]));
+          dg[e] = dy[e] * l[e] * (s * (1.0f + g[e] * (1.0f - s)));
+          dl[e] = dy[e] * (g[e] * s);
+          acc1[e] += dg[e];
+          acc2[e] += dl[e];
+          amax = fmaxf(amax, fmaxf(fabsf(dg[e]), fabsf(dl[e])));
+        }
+        if (cs.store) {
+          cast_store<E>(a.dx, r * a.N_in + col, dg, cs);
+          cast_store<E>(a.dx, r * a.N_in + n_out + col, dl, cs);
+        }
+      } else {
+        float h[E], d[E];
+        if (a.act != TE_IDENTITY) {
+          V::load(a.x, r * a.N_in + col, h);
+        } else {
+#pragma unroll
+          for (int e = 0; e < E; ++e) h[e] = 0.0f;
+        }
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          d[e] = a.act == TE_IDENTITY ? dy[e] : dy[e] * dact_apply(a.act, h[e]);
+          acc1[e] += d[e];
+          amax = fmaxf(amax, fabsf(d[e]));
+        }
+        if (cs.store && a.dx) cast_store<E>(a.dx, r * a.N_in + col, d, cs);
+      }
+    }
+  }
+  if (a.dbias) {
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      red[warp][0][lane * E + e] = acc1[e];
+      red[warp][1][lane * E + e] = acc2[e];
+    }
+    __syncthreads();
+    // 256 threads finish 2 * W column sums, each over the 8 warps in warp order.
+    const int halves = gated ? 2 : 1;
+    for (int t = threadIdx.x; t < halves * W; t += blockDim.x) {
+      const int hsel = t / W, j = t % W;
+      float s = 0.0f;
+#pragma unroll
+      for (int w = 0; w < kDactWarps; ++w) s += red[w][hsel][j];
+      const int64_t c = int64_t(blockIdx.x) * W + j;
+      if (c < n_out) a.partials[int64_t(blockIdx.y) * a.N_in + hsel * n_out + c] = s;
+    }
+  }
+  block_amax_commit(amax, a.cast.amax_out);
+}
+
+__global__ void colsum_partials_kernel(const float* partials, int chunks, int64_t n, float* out) {
+  const int64_t j = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (j >= n) return;
+  float s = 0.0f;
+  for (int c = 0; c < chunks; ++c) s += partials[int64_t(c) * n + j];
+  out[j] = s;
+}
+
+template <typename T>
+te_status launch_dact_t(const DactArgs& a, cudaStream_t s) {
+  constexpr int E = Vec16<T>::N;
+  const int64_t n_out = a.act == TE_SWIGLU ? a.N_in / 2 : a.N_in;
+  const int chunks = int(ceil_div(a.M, kDactRows));
+  dim3 grid(unsigned(ceil_div(n_out, 32 * E)), unsigned(chunks));
+  dact_dbias_kernel<T><<<grid, kDactWarps * 32, 0, s>>>(a);
+  if (a.dbias)
+    colsum_partials_kernel<<<unsigned(ceil_div(a.N_in, 256)), 256, 0, s>>>(a.partials, chunks,
+                                                                          a.N_in, a.dbias);
+  return cudaGetLastError() == cudaSuccess ? TE_OK : TE_ERR_CUDA;
+}
+
+}  // namespace
+
+te_status launch_quantize(const QuantizeArgs& a, cudaStream_t s) {
+  if (a.x_dtype == TE_BF16) {
+    quantize_kernel<__nv_bfloat16><<<ew_grid(a.n / 8), kEwThreads, 0, s>>>(a);
+  } else if (a.x_dtype == TE_F32) {
+    quantize_kernel<float><<<ew_grid(a.n / 4), kEwThreads, 0, s>>>(a);
+  } else {
+    return TE_ERR_UNSUPPORTED;
+  }
+  return cudaGetLastError() == cudaSuccess ? TE_OK : TE_ERR_CUDA;
+}
+
+te_status launch_act_lu(const ActArgs& a, cudaStream_t s) {
+  const int64_t n_out = a.act == TE_SWIGLU ? a.N_in / 2 : a.N_in;
+  if (a.x_dtype == TE_BF16) {
+    act_lu_kernel<__nv_bfloat16><<<ew_grid(a.M * n_out / 8), kEwThreads, 0, s>>>(a);
+  } else if (a.x_dtype == TE_F32) {
+    act_lu_kernel<float><<<ew_grid(a.M * n_out / 4), kEwThreads, 0, s>>>(a);
+  } else {
+    return TE_ERR_UNSUPPORTED;
+  }
+  return cudaGetLastError() == cudaSuccess ? TE_OK : TE_ERR_CUDA;
+}
+
+size_t dact_dbias_workspace(int64_t M, int64_t N_in) {
+  return size_t(ceil_div(M > 0 ? M : 1, kDactRows)) * size_t(N_in) * sizeof(float);
+}
+
+te_status launch_dact_dbias(const DactArgs& a, cudaStream_t s) {
+  if (a.M == 0) return TE_OK;
+  if (a.dtype == TE_BF16) return launch_dact_t<__nv_bfloat16>(a, s);
+  if (a.dtype == TE_F32) return launch_dact_t<float>(a, s);
+  return TE_ERR_UNSUPPORTED;
+}
+
+}  // namespace te

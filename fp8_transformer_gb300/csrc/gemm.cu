@@ -1,0 +1,694 @@
+// Tensor-core GEMM with fused epilogues for sm_103a: TMA -> shared-memory ring -> tcgen05.mma
+// into a double-buffered TMEM accumulator -> tcgen05.ld epilogue.
+//
+// It implements the two bias-carrying GEMMs of the TransformerEngine JAX "LayerNorm MLP" page
+// (Description, forward steps (2) and (4)) and the one GEMM of the "LayerNorm Dense" page, with
+// the activation and FP8 cast of step (3) fused into the first GEMM's epilogue.
+//
+// Structure (one CTA per SM, persistent over output tiles of 128 x 256 accumulator columns):
+//   warp 0     TMA producer: one elected thread fills a STAGES-deep ring of A/B tiles, each
+//              row of a tile 128 bytes of K in the 128-byte swizzled layout.
+//   warp 1     owns the TMEM allocation (512 columns = two 256-column fp32 accumulators) and
+//              issues tcgen05.mma from one thread; tcgen05.commit releases ring slots and
+//              hands a finished accumulator to the epilogue.
+//   warps 2-5  epilogue: tcgen05.ld 32 columns at a time, scale by the FP8 dequantization
+//              factor, add the bias, round the pre-activation, apply the activation (the gated
+//              pair's gate and linear halves sit in the two column halves of one accumulator
+//              tile), track amax, and store fp32 / bf16 / E4M3.
+// The epilogue of tile i overlaps the MMAs of tile i + 1.
+//
+// Every mbarrier wait is bounded in time.  On expiry the waiting thread records
+// TE_ERR_TIMEOUT in the device status word and raises a CTA-wide abort flag; every role
+// then leaves its loop, the producer waits (again bounded) for its own TMA copies still in
+// flight, the MMA thread waits for its own MMAs, and TMEM is freed before the CTA exits.
+#include <cuda.h>
+
+#include <cstring>
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace te {
+
+__device__ int g_device_status;
+
+namespace {
+
+constexpr int BM = 128;                 // accumulator rows per tile (TMEM lanes)
+constexpr int BN = 256;                 // accumulator columns per tile
+constexpr int STAGES = 4;
+constexpr int kRowBytes = 128;          // bytes of K per tile row per stage
+constexpr int A_STAGE = BM * kRowBytes; // 16 KB
+constexpr int B_STAGE = BN * kRowBytes; // 32 KB
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
+constexpr uint64_t kDrainLimitNs = 200000000ull;   // 0.2 s
+constexpr int kGroupM = 8;              // m-tiles per raster group (L2 reuse of B)
+
+// Element kinds: 0 = bf16 (kind::f16), 1 = E4M3 (kind::f8f6f4), 2 = fp32 as tf32 (kind::tf32).
+template <int KIND>
+struct Kind;
+template <> struct Kind<0> { static constexpr int esize = 2; static constexpr uint32_t fmt = 1; };
+template <> struct Kind<1> { static constexpr int esize = 1; static constexpr uint32_t fmt = 0; };
+template <> struct Kind<2> { static constexpr int esize = 4; static constexpr uint32_t fmt = 2; };
+
+struct GemmDev {
+  int64_t M, N, K;
+  int num_m, num_n, num_kb;
+  int gated;
+  int64_t F;        // gated: column offset of the linear half in B
+  int epilogue, act;
+  const float* a_scale_inv;
+  const float* b_scale_inv;
+  const void* bias;
+  int bias_dtype;
+  int h_dtype;
+  void* saved_h;
+  void* D;
+  int d_dtype;
+  const float* out_scale;
+  float* out_scale_inv;
+  float* amax_out;
+  int* status;
+};
+
+struct __align__(64) GemmParams {
+  CUtensorMap tmA;
+  CUtensorMap tmB;
+  GemmDev g;
+};
+
+// ------------------------------------------------------------------ PTX wrappers ----------
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Waits for the phase of `bar` with parity `parity`.  Returns false, without waiting further,
+// when the CTA's abort flag is raised (check_abort) or the time limit passes; the latter
+// records TE_ERR_TIMEOUT and raises the flag.
+__device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          uint64_t limit_ns, bool check_abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 31) == 0) {
+      if (check_abort && *abort_flag) return false;
+      if (global_ns() - t0 > limit_ns) {
+        atomicCAS(&g_device_status, 0, int(TE_ERR_TIMEOUT));
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm, uint32_t bar,
+                                            int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(bar), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor: 128-byte swizzle, descriptor version 1 (bits 46-48).
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return uint64_t((addr & 0x3FFFFu) >> 4) | (uint64_t((lbo >> 4) & 0x3FFFu) << 16) |
+         (uint64_t((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// Instruction descriptor: fp32 accumulator, A/B format, operand majors, N >> 3, M >> 4.
+template <int KIND>
+__host__ __device__ constexpr uint32_t instr_desc(int a_mn_major, int b_mn_major) {
+  return (1u << 4) | (Kind<KIND>::fmt << 7) | (Kind<KIND>::fmt << 10) |
+         (uint32_t(a_mn_major) << 15) | (uint32_t(b_mn_major) << 16) |
+         (uint32_t(BN >> 3) << 17) | (uint32_t(BM >> 4) << 24);
+}
+
+template <int KIND>
+__device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                     uint32_t accumulate) {
+  if constexpr (KIND == 0) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
+  } else if constexpr (KIND == 1) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
+  }
+}
+
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+
+// 32 lanes x 32 consecutive fp32 columns: thread t of the warp receives its TMEM lane's row.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+        "=r"(r[31])
+      : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_ld_wait() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// ------------------------------------------------------------------ tile order ------------
+
+struct Tile {
+  int m, n;
+};
+
+// Raster groups of kGroupM m-tiles: consecutive tiles share B columns within a group.
+__device__ __forceinline__ Tile tile_of(int t, int num_m, int num_n) {
+  const int group_size = kGroupM * num_n;
+  const int group = t / group_size;
+  const int first_m = group * kGroupM;
+  const int gm = min(num_m - first_m, kGroupM);
+  const int in_group = t - group * group_size;
+  return Tile{first_m + in_group % gm, in_group / gm};
+}
+
+// ------------------------------------------------------------------ epilogue stores -------
+
+__device__ __forceinline__ float load_bias(const void* bias, int dtype, int64_t j) {
+  if (dtype == TE_BF16) return __bfloat162float(static_cast<const __nv_bfloat16*>(bias)[j]);
+  return static_cast<const float*>(bias)[j];
+}
+
+// Stores `count` (16 or 32) values of one row segment starting at element `off`.
+__device__ __forceinline__ void store_seg(void* base, int64_t off, const float (&v)[32],
+                                          int count, int dtype, float scale) {
+  if (dtype == TE_F32) {
+    float4* p = reinterpret_cast<float4*>(static_cast<float*>(base) + off);
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (i * 4 < count) p[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+  } else if (dtype == TE_BF16) {
+    uint4* p = reinterpret_cast<uint4*>(static_cast<uint16_t*>(base) + off);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      if (i * 8 < count)
+        p[i] = make_uint4(pack_bf16x2(v[8 * i], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
+                          pack_bf16x2(v[8 * i + 4], v[8 * i + 5]),
+                          pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
+  } else {
+    uint4* p = reinterpret_cast<uint4*>(static_cast<uint8_t*>(base) + off);
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+      if (i * 16 < count) {
+        const float* w = v + 16 * i;
+        p[i] = make_uint4(pack_e4m3x4(w[0] * scale, w[1] * scale, w[2] * scale, w[3] * scale),
+                          pack_e4m3x4(w[4] * scale, w[5] * scale, w[6] * scale, w[7] * scale),
+                          pack_e4m3x4(w[8] * scale, w[9] * scale, w[10] * scale, w[11] * scale),
+                          pack_e4m3x4(w[12] * scale, w[13] * scale, w[14] * scale, w[15] * scale));
+      }
+  }
+}
+
+__device__ __forceinline__ void round_to(float (&v)[32], int dtype) {
+  if (dtype == TE_BF16) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = round_bf16(v[i]);
+  }
+}
+
+// ------------------------------------------------------------------ the kernel ------------
+
+template <int KIND, bool A_KMAJOR, bool B_KMAJOR>
+__global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ GemmParams p) {
+  constexpr int EPR = kRowBytes / Kind<KIND>::esize;  // K elements per 128-byte row
+  constexpr int MMA_K_BYTES = 32;                     // K bytes consumed by one tcgen05.mma
+  constexpr int MMA_K = MMA_K_BYTES / Kind<KIND>::esize;
+  constexpr uint32_t IDESC = instr_desc<KIND>(A_KMAJOR ? 0 : 1, B_KMAJOR ? 0 : 1);
+  const GemmDev& g = p.g;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* smA = smem;
+  uint8_t* smB = smem + STAGES * A_STAGE;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smB + STAGES * B_STAGE);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + STAGES;
+  uint64_t* tfull = bars + 2 * STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int num_tiles = g.num_m * g.num_n;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(smem_u32(&tfull[a]), 1);
+      mbar_init(smem_u32(&tempty[a]), 128);
+    }
+    mbar_init(smem_u32(drain), 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 0 && lane == 0) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tmA)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tmB)) : "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ----------------------------------------------------------- TMA producer -----------
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0, issued = 0, last_parity = 0;
+      for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+        const Tile tl = tile_of(t, g.num_m, g.num_n);
+        const int m0 = tl.m * BM;
+        bool ok = true;
+        for (int kb = 0; kb < g.num_kb; ++kb) {
+          if (!wait_bounded(smem_u32(&empty[stage]), phase ^ 1, abort_flag, kWaitLimitNs, true)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = smem_u32(&full[stage]);
+          mbar_expect_tx(fb, A_STAGE + B_STAGE);
+          const uint32_t a_dst = smem_u32(smA + stage * A_STAGE);
+          const uint32_t b_dst = smem_u32(smB + stage * B_STAGE);
+          const int k0 = kb * EPR;
+          if constexpr (A_KMAJOR) {
+            tma_load_2d(a_dst, &p.tmA, fb, k0, m0);
+          } else {
+#pragma unroll
+            for (int i = 0; i < BM / EPR; ++i)
+              tma_load_2d(a_dst + i * EPR * kRowBytes, &p.tmA, fb, m0 + i * EPR, k0);
+          }
+          if (!g.gated) {
+            const int n0 = tl.n * BN;
+            if constexpr (B_KMAJOR) {
+              tma_load_2d(b_dst, &p.tmB, fb, k0, n0);
+            } else {
+#pragma unroll
+              for (int i = 0; i < BN / EPR; ++i)
+                tma_load_2d(b_dst + i * EPR * kRowBytes, &p.tmB, fb, n0 + i * EPR, k0);
+            }
+          } else {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int c0 = int(h * g.F) + tl.n * (BN / 2);
+              const uint32_t dst = b_dst + h * (BN / 2) * kRowBytes;
+              if constexpr (B_KMAJOR) {
+                tma_load_2d(dst, &p.tmB, fb, k0, c0);
+              } else {
+#pragma unroll
+                for (int i = 0; i < (BN / 2) / EPR; ++i)
+                  tma_load_2d(dst + i * EPR * kRowBytes, &p.tmB, fb, c0 + i * EPR, k0);
+              }
+            }
+          }
+          issued |= 1u << stage;
+          last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+      }
+      // Own copies still in flight complete before the CTA may exit.
+      for (int s = 0; s < STAGES; ++s)
+        if (issued & (1u << s))
+          wait_bounded(smem_u32(&full[s]), (last_parity >> s) & 1, abort_flag, kDrainLimitNs, false);
+    }
+  } else if (warp == 1) {
+    // ----------------------------------------------------------- MMA issuer -------------
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int local = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++local) {
+        const int acc = local & 1;
+        const uint32_t acc_phase = (local >> 1) & 1;
+        if (!wait_bounded(smem_u32(&tempty[acc]), acc_phase ^ 1, abort_flag, kWaitLimitNs, true)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + uint32_t(acc * BN);
+        for (int kb = 0; kb < g.num_kb; ++kb) {
+          if (!wait_bounded(smem_u32(&full[stage]), phase, abort_flag, kWaitLimitNs, true)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_base = smem_u32(smA + stage * A_STAGE);
+          const uint32_t b_base = smem_u32(smB + stage * B_STAGE);
+#pragma unroll
+          for (int j = 0; j < kRowBytes / MMA_K_BYTES; ++j) {
+            const uint64_t ad =
+                A_KMAJOR ? smem_desc(a_base + j * MMA_K_BYTES, 16, 8 * kRowBytes)
+                         : smem_desc(a_base + j * MMA_K * kRowBytes, EPR * kRowBytes, 8 * kRowBytes);
+            const uint64_t bd =
+                B_KMAJOR ? smem_desc(b_base + j * MMA_K_BYTES, 16, 8 * kRowBytes)
+                         : smem_desc(b_base + j * MMA_K * kRowBytes, EPR * kRowBytes, 8 * kRowBytes);
+            umma<KIND>(d_tmem, ad, bd, IDESC, (kb | j) != 0 ? 1u : 0u);
+          }
+          umma_commit(smem_u32(&empty[stage]));
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        umma_commit(smem_u32(&tfull[acc]));
+      }
+      // Own MMAs complete before TMEM is released.
+      umma_commit(smem_u32(drain));
+      wait_bounded(smem_u32(drain), 0, abort_flag, kDrainLimitNs, false);
+    }
+  } else {
+    // ----------------------------------------------------------- epilogue ---------------
+    const int quad = warp & 3;  // TMEM lanes [32 * quad, 32 * quad + 32)
+    const int row_in_tile = quad * 32 + lane;
+    float alpha = 1.0f;
+    if (g.a_scale_inv) alpha *= *g.a_scale_inv;
+    if (g.b_scale_inv) alpha *= *g.b_scale_inv;
+    const float out_scale = (g.d_dtype == TE_E4M3 && g.out_scale) ? *g.out_scale : 1.0f;
+    if (blockIdx.x == 0 && threadIdx.x == 64 && g.out_scale_inv) *g.out_scale_inv = 1.0f / out_scale;
+    const int64_t ldd = g.gated ? g.F : g.N;
+    float amax = 0.0f;
+    int local = 0;
+    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++local) {
+      const int acc = local & 1;
+      const uint32_t acc_phase = (local >> 1) & 1;
+      const uint32_t tb = smem_u32(&tfull[acc]);
+      int ok = 1;
+      if (lane == 0) ok = wait_bounded(tb, acc_phase, abort_flag, kWaitLimitNs, true) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      // The phase has completed; every lane observes it before touching TMEM.
+      while (!mbar_try_wait(tb, acc_phase)) {
+      }
+      __syncwarp();
+      tc_fence_after();
+      const Tile tl = tile_of(t, g.num_m, g.num_n);
+      const int64_t row = int64_t(tl.m) * BM + row_in_tile;
+      const bool row_ok = row < g.M;
+      const uint32_t taddr = tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(acc * BN);
+      if (!g.gated) {
+        const int64_t n0 = int64_t(tl.n) * BN;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          const int64_t col0 = n0 + c * 32;
+          if (col0 >= g.N) break;
+          const int count = g.N - col0 >= 32 ? 32 : int(g.N - col0);
+          uint32_t r[32];
+          tmem_ld32(taddr + c * 32, r);
+          tmem_ld_wait();
+          float v[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            v[i] = __uint_as_float(r[i]) * alpha;
+            if (g.bias && i < count) v[i] += load_bias(g.bias, g.bias_dtype, col0 + i);
+          }
+          if (g.epilogue == EPI_BIAS_ACT) {
+            round_to(v, g.h_dtype);
+            if (g.saved_h && row_ok) store_seg(g.saved_h, row * g.N + col0, v, count, g.h_dtype, 1.0f);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = act_apply(g.act, v[i]);
+          }
+          if (row_ok) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (i < count) amax = fmaxf(amax, fabsf(v[i]));
+            store_seg(g.D, row * ldd + col0, v, count, g.d_dtype, out_scale);
+          }
+        }
+      } else {
+        const int64_t n0 = int64_t(tl.n) * (BN / 2);
+#pragma unroll 1
+        for (int c = 0; c < BN / 64; ++c) {
+          const int64_t col0 = n0 + c * 32;
+          if (col0 >= g.F) break;
+          const int count = g.F - col0 >= 32 ? 32 : int(g.F - col0);
+          uint32_t rg[32], rl[32];
+          tmem_ld32(taddr + c * 32, rg);
+          tmem_ld32(taddr + BN / 2 + c * 32, rl);
+          tmem_ld_wait();
+          float vg[32], vl[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            vg[i] = __uint_as_float(rg[i]) * alpha;
+            vl[i] = __uint_as_float(rl[i]) * alpha;
+            if (g.bias && i < count) {
+              vg[i] += load_bias(g.bias, g.bias_dtype, col0 + i);
+              vl[i] += load_bias(g.bias, g.bias_dtype, g.F + col0 + i);
+            }
+          }
+          round_to(vg, g.h_dtype);
+          round_to(vl, g.h_dtype);
+          if (g.saved_h && row_ok) {
+            store_seg(g.saved_h, row * g.N + col0, vg, count, g.h_dtype, 1.0f);
+            store_seg(g.saved_h, row * g.N + g.F + col0, vl, count, g.h_dtype, 1.0f);
+          }
+#pragma unroll
+          for (int i = 0; i < 32; ++i) vg[i] = act_silu(vg[i]) * vl[i];
+          if (row_ok) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (i < count) amax = fmaxf(amax, fabsf(vg[i]));
+            store_seg(g.D, row * ldd + col0, vg, count, g.d_dtype, out_scale);
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(smem_u32(&tempty[acc]));
+    }
+    amax = warp_max(amax);
+    if (lane == 0 && g.amax_out) atomic_max_nonneg(g.amax_out, amax);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "r"(kTmemCols)
+                 : "memory");
+  }
+}
+
+// ------------------------------------------------------------------ host side -------------
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+// 2-D tensor map over a row-major [outer, inner] matrix, 128-byte swizzled boxes.
+bool make_tmap(CUtensorMap* tm, const void* ptr, int ab_dtype, uint64_t inner, uint64_t outer,
+               uint32_t box_inner, uint32_t box_outer) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  CUtensorMapDataType dt = ab_dtype == TE_BF16   ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                           : ab_dtype == TE_E4M3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                                 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  const int esize = ab_dtype == TE_BF16 ? 2 : ab_dtype == TE_E4M3 ? 1 : 4;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner * esize};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(tm, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+constexpr size_t kSmemBytes = size_t(STAGES) * (A_STAGE + B_STAGE) + 1024 + 256;
+
+template <int KIND, bool AK, bool BK>
+te_status launch_t(GemmParams& prm, int grid, cudaStream_t s) {
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (!attr_set[dev & 63]) {
+    if (cudaFuncSetAttribute(gemm_kernel<KIND, AK, BK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(kSmemBytes)) != cudaSuccess)
+      return TE_ERR_CUDA;
+    attr_set[dev & 63] = true;
+  }
+  gemm_kernel<KIND, AK, BK><<<grid, kThreads, kSmemBytes, s>>>(prm);
+  return cudaGetLastError() == cudaSuccess ? TE_OK : TE_ERR_CUDA;
+}
+
+template <int KIND>
+te_status launch_kind(GemmParams& prm, int grid, bool ak, bool bk, cudaStream_t s) {
+  if (ak && bk) return launch_t<KIND, true, true>(prm, grid, s);
+  if (ak && !bk) return launch_t<KIND, true, false>(prm, grid, s);
+  if (!ak && bk) return launch_t<KIND, false, true>(prm, grid, s);
+  return launch_t<KIND, false, false>(prm, grid, s);
+}
+
+}  // namespace
+
+int num_sms() {
+  static int cached[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (!cached[dev & 63]) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cached[dev & 63] = n > 0 ? n : 1;
+  }
+  return cached[dev & 63];
+}
+
+int* device_status_ptr() {
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
+  return static_cast<int*>(p);
+}
+
+te_status read_and_clear_device_status(int32_t* out) {
+  int v = 0;
+  if (cudaDeviceSynchronize() != cudaSuccess) return TE_ERR_CUDA;
+  if (cudaMemcpyFromSymbol(&v, g_device_status, sizeof(int)) != cudaSuccess) return TE_ERR_CUDA;
+  const int zero = 0;
+  if (cudaMemcpyToSymbol(g_device_status, &zero, sizeof(int)) != cudaSuccess) return TE_ERR_CUDA;
+  if (out) *out = v;
+  return TE_OK;
+}
+
+te_status launch_gemm(const GemmArgs& a, cudaStream_t s) {
+  if (a.M == 0 || a.N == 0) return TE_OK;
+  const int kind = a.ab_dtype == TE_BF16 ? 0 : a.ab_dtype == TE_E4M3 ? 1 : 2;
+  const int esize = a.ab_dtype == TE_BF16 ? 2 : a.ab_dtype == TE_E4M3 ? 1 : 4;
+  const uint32_t epr = uint32_t(kRowBytes / esize);
+  const bool gated = a.epilogue == EPI_BIAS_GATED;
+  GemmParams prm;
+  memset(&prm, 0, sizeof(prm));
+  // A: op(A) is [M, K].
+  bool ok = a.a_kmajor ? make_tmap(&prm.tmA, a.A, a.ab_dtype, a.K, a.M, epr, BM)
+                       : make_tmap(&prm.tmA, a.A, a.ab_dtype, a.M, a.K, epr, epr);
+  // B: op(B) is [K, N].
+  ok = ok && (a.b_kmajor ? make_tmap(&prm.tmB, a.B, a.ab_dtype, a.K, a.N, epr, gated ? BN / 2 : BN)
+                         : make_tmap(&prm.tmB, a.B, a.ab_dtype, a.N, a.K, epr, epr));
+  if (!ok) return TE_ERR_CUDA;
+  GemmDev& g = prm.g;
+  g.M = a.M;
+  g.N = a.N;
+  g.K = a.K;
+  g.gated = gated ? 1 : 0;
+  g.F = gated ? a.N / 2 : 0;
+  g.num_m = int(ceil_div(a.M, BM));
+  g.num_n = int(gated ? ceil_div(a.N / 2, BN / 2) : ceil_div(a.N, BN));
+  g.num_kb = int(ceil_div(a.K, epr));
+  g.epilogue = a.epilogue;
+  g.act = a.act;
+  g.a_scale_inv = a.a_scale_inv;
+  g.b_scale_inv = a.b_scale_inv;
+  g.bias = a.bias;
+  g.bias_dtype = a.bias_dtype;
+  g.h_dtype = a.h_dtype;
+  g.saved_h = a.saved_h;
+  g.D = a.D;
+  g.d_dtype = a.cast.out_dtype;
+  g.out_scale = a.cast.scale;
+  g.out_scale_inv = a.cast.scale_inv_out;
+  g.amax_out = a.cast.amax_out;
+  const int64_t tiles = int64_t(g.num_m) * g.num_n;
+  const int grid = int(tiles < num_sms() ? tiles : num_sms());
+  if (kind == 0) return launch_kind<0>(prm, grid, a.a_kmajor, a.b_kmajor, s);
+  if (kind == 1) return launch_kind<1>(prm, grid, a.a_kmajor, a.b_kmajor, s);
+  return launch_kind<2>(prm, grid, a.a_kmajor, a.b_kmajor, s);
+}
+
+}  // namespace te

@@ -1,0 +1,120 @@
+// Internal launch interface between the C-ABI layer (api.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "te_gb300.h"
+
+namespace te {
+
+// Output stage shared by the bandwidth-bound kernels: how fp32 results become the stored
+// tensor, and which scalars the kernel reads or writes.
+struct CastSpec {
+  int out_dtype = TE_BF16;         // TE_F32 / TE_BF16 / TE_E4M3
+  int fake_quant = 0;              // quantize then dequantize into out_dtype (F32 / BF16)
+  const float* scale = nullptr;    // E4M3 scale to use (delayed scaling)
+  const float* amax_in = nullptr;  // current scaling: derive the scale from this amax
+  float* amax_out = nullptr;       // atomic max of |pre-cast value| (zeroed by the caller)
+  float* scale_out = nullptr;      // written with the scale used (current scaling)
+  float* scale_inv_out = nullptr;  // written with 1 / scale
+  int store = 1;                   // 0: amax pass of current scaling, nothing stored
+};
+
+struct NormFwdArgs {
+  const void* x = nullptr;
+  int x_dtype = TE_BF16;
+  int64_t M = 0, H = 0;
+  const void* gamma = nullptr;
+  const void* beta = nullptr;
+  int norm_type = TE_LAYERNORM;
+  int zero_centered_gamma = 0;
+  float eps = 1e-6f;
+  void* out = nullptr;
+  float* mu = nullptr;
+  float* rsigma = nullptr;
+  CastSpec cast;
+};
+te_status launch_norm_fwd(const NormFwdArgs& a, cudaStream_t s);
+
+struct NormBwdArgs {
+  const void* dz = nullptr;  // [M, H] upstream gradient, dtype
+  const void* x = nullptr;   // [M, H] forward input, dtype
+  const float* mu = nullptr;
+  const float* rsigma = nullptr;
+  const void* gamma = nullptr;
+  int dtype = TE_BF16;
+  int64_t M = 0, H = 0;
+  int norm_type = TE_LAYERNORM;
+  int zero_centered_gamma = 0;
+  void* dx = nullptr;        // [M, H] dtype
+  float* dgamma = nullptr;   // [H]
+  float* dbeta = nullptr;    // [H] or null
+  float* partials = nullptr; // workspace: [chunks, 2, H]
+};
+te_status launch_norm_bwd(const NormBwdArgs& a, cudaStream_t s);
+size_t norm_bwd_workspace(int64_t M, int64_t H);
+
+struct ActArgs {
+  const void* x = nullptr;
+  int x_dtype = TE_BF16;
+  int64_t M = 0, N_in = 0;
+  int act = TE_GELU;
+  void* out = nullptr;
+  CastSpec cast;
+};
+te_status launch_act_lu(const ActArgs& a, cudaStream_t s);
+
+struct DactArgs {
+  const void* dy = nullptr;
+  const void* x = nullptr;
+  int dtype = TE_BF16;
+  int64_t M = 0, N_in = 0;
+  int act = TE_GELU;
+  void* dx = nullptr;
+  float* dbias = nullptr;
+  float* partials = nullptr;  // workspace for the deterministic column reduction
+  CastSpec cast;
+};
+te_status launch_dact_dbias(const DactArgs& a, cudaStream_t s);
+size_t dact_dbias_workspace(int64_t M, int64_t N_in);
+
+struct QuantizeArgs {
+  const void* x = nullptr;
+  int x_dtype = TE_BF16;
+  int64_t n = 0;  // elements, multiple of 8
+  void* out = nullptr;
+  CastSpec cast;
+};
+te_status launch_quantize(const QuantizeArgs& a, cudaStream_t s);
+
+// Tensor-core GEMM D[M, N] = epilogue(alpha * op(A) op(B)).
+enum Epilogue { EPI_BIAS = 0, EPI_BIAS_ACT = 1, EPI_BIAS_GATED = 2 };
+
+struct GemmArgs {
+  const void* A = nullptr;
+  const void* B = nullptr;
+  int ab_dtype = TE_BF16;   // TE_BF16 / TE_E4M3 / TE_F32 (tf32)
+  int a_kmajor = 1;         // A stored [M, K] (1) or [K, M] (0)
+  int b_kmajor = 0;         // B stored [N, K] (1) or [K, N] (0)
+  int64_t M = 0, N = 0, K = 0;  // N = accumulator columns; gated: N = 2F
+  const float* a_scale_inv = nullptr;
+  const float* b_scale_inv = nullptr;
+  int epilogue = EPI_BIAS;
+  int act = TE_IDENTITY;
+  const void* bias = nullptr;   // [N]
+  int bias_dtype = TE_F32;
+  int h_dtype = TE_F32;         // dtype the pre-activation is rounded to (act epilogues)
+  void* saved_h = nullptr;      // [M, N] pre-activation, h_dtype
+  void* D = nullptr;            // [M, N] or [M, N/2] gated
+  CastSpec cast;                // output stage of D (amax / E4M3 of the activation)
+};
+te_status launch_gemm(const GemmArgs& g, cudaStream_t s);
+
+// Device status word (TE_OK or the first failure a kernel recorded).
+int* device_status_ptr();
+te_status read_and_clear_device_status(int32_t* out);
+
+int num_sms();
+
+}  // namespace te

@@ -1,0 +1,262 @@
+/*
+ * te_gb300.h -- C ABI of the fused normalization + feed-forward block for GB300 (sm_103a).
+ *
+ * The block is the one described by three TransformerEngine JAX pages:
+ *   "Activation"       (activation(x, activation_type, quantizer, act_params)),
+ *   "LayerNorm MLP"    (layernorm_mlp(x, gamma, beta, kernels, biases, norm_type, ...)),
+ *   "LayerNorm Dense"  (layernorm_dense(x, kernel, gamma, beta, bias, norm_type, ...)).
+ * Each entry point below names the page section that defines its operation.
+ *
+ * Conventions shared by every function:
+ *   - Pointers are device pointers unless a comment says "host".  Every tensor is dense and
+ *     row-major; leading batch/sequence dimensions are flattened into M rows (so the pages'
+ *     transpose_batch_sequence flag has no counterpart).  Weights are stored [in, out], e.g.
+ *     kernel1 is [H, F] (or [H, 2F] for a gated activation).
+ *   - Device pointers must be 16-byte aligned.  Row lengths (H, N, F) must be multiples of 16
+ *     elements for GEMM-carrying calls and multiples of 8 for the bandwidth-bound calls;
+ *     otherwise the call returns TE_ERR_UNSUPPORTED and launches nothing.
+ *   - The caller owns every buffer and the stream.  The library allocates no device memory;
+ *     scratch space comes from the caller's `workspace` (size from te_workspace_size).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).  Every call
+ *     is asynchronous on that stream and never synchronizes it.
+ *   - Host-detectable errors are returned synchronously before any launch.  Device-side
+ *     failures (a pipeline wait that timed out) are recorded in a device status word that
+ *     te_get_device_status reads after the caller synchronizes.
+ *   - FP8 is E4M3 (OCP "fn" variant), round to nearest even, saturating to +-448, with one fp32
+ *     scale per tensor: q = E4M3(fp32(v * scale)), dequantized value = fp32(decode(q) * scale_inv).
+ */
+#ifndef TE_GB300_H
+#define TE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  TE_OK = 0,
+  TE_ERR_INVALID_ARG = 1,  /* NULL required pointer, negative size, bad enum */
+  TE_ERR_UNSUPPORTED = 2,  /* alignment or shape this build does not handle */
+  TE_ERR_CUDA = 3,         /* a CUDA runtime call or kernel launch failed */
+  TE_ERR_TIMEOUT = 4,      /* a device pipeline wait gave up (device status word only) */
+  TE_ERR_WORKSPACE = 5     /* workspace missing or smaller than te_workspace_size() */
+} te_status;
+
+typedef enum { TE_F32 = 0, TE_BF16 = 1, TE_E4M3 = 2 } te_dtype;
+
+/* norm_type: "layernorm" or "rmsnorm" (LayerNorm MLP page, I/O Contract). */
+typedef enum { TE_LAYERNORM = 0, TE_RMSNORM = 1 } te_norm_type;
+
+/* activation_type (Activation page, I/O Contract): ("relu",), ("gelu",) (tanh form),
+ * ("silu",), and the gated pair ("silu", "linear") = SwiGLU.  TE_IDENTITY passes values
+ * through (used for the plain bias-gradient reduction). */
+typedef enum { TE_IDENTITY = 0, TE_RELU = 1, TE_GELU = 2, TE_SILU = 3, TE_SWIGLU = 4 } te_act_type;
+
+/* How a quantizer obtains its scale.
+ *   TE_SCALING_DELAYED: use *scale as given (e.g. from an earlier call's amax); one pass.
+ *   TE_SCALING_CURRENT: compute this call's amax first, then scale = 448 / amax (1 if amax is
+ *                       0 or not finite, FLT_MAX if the quotient overflows); two passes. */
+typedef enum { TE_SCALING_DELAYED = 0, TE_SCALING_CURRENT = 1 } te_scaling;
+
+/* One FP8 quantizer (the pages' Quantizer: the optional object that makes an output FP8).
+ * All three pointers are device fp32 scalars.
+ *   scale     DELAYED: read.  CURRENT: written (448 / amax).
+ *   scale_inv written: 1 / scale, the factor that dequantizes this tensor.
+ *   amax      written: max |v| over the fp32 values before the cast, for this call.
+ * A quantizer whose `scale` is NULL is disabled (that tensor is not quantized). */
+typedef struct {
+  float* scale;
+  float* scale_inv;
+  float* amax;
+  int32_t mode; /* te_scaling */
+} te_quantizer;
+
+/* The pages' QuantizerSet.  Passing NULL for a te_quantizer_set* is noop_quantizer_set. */
+typedef struct {
+  te_quantizer x;       /* normalized output (the first GEMM's A operand) */
+  te_quantizer kernel1; /* kernel1, or the LayerNorm-Dense kernel */
+  te_quantizer act;     /* activation output (the second GEMM's A operand) */
+  te_quantizer kernel2; /* kernel2 */
+  te_quantizer grad;    /* activation gradient dH in the backward pass */
+} te_quantizer_set;
+
+/* Operation ids for te_workspace_size. */
+typedef enum {
+  TE_OP_NORM_FWD = 0,
+  TE_OP_ACT_LU = 1,
+  TE_OP_DACT_DBIAS = 2,
+  TE_OP_LAYERNORM_DENSE_FWD = 3,
+  TE_OP_LAYERNORM_MLP_FWD = 4,
+  TE_OP_NORM_BWD = 5,
+  TE_OP_LAYERNORM_MLP_BWD = 6
+} te_op;
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char* te_status_string(te_status status);
+
+/* ABI version of this library (major * 100 + minor). */
+int te_version(void);
+
+/* Reads and clears the device status word of the current device.  Synchronizes the device.
+ * *device_status receives TE_OK, or the te_status a kernel recorded (e.g. TE_ERR_TIMEOUT). */
+te_status te_get_device_status(int32_t* device_status);
+
+/* Bytes of workspace a call needs.  dims = {M, H, F or N}; `dtype` is the activation dtype,
+ * `quantized` is nonzero when a quantizer set is passed, `kernel_dtype` the weights' storage
+ * dtype.  Unused dims may be 0.  Returns 0 for operations that need none. */
+size_t te_workspace_size(te_op op, int64_t M, int64_t H, int64_t F_or_N, te_dtype dtype,
+                         int quantized, te_dtype kernel_dtype, te_act_type act);
+
+/* ---------------------------------------------------------------------------------------
+ * te_norm_fwd -- LayerNorm or RMSNorm of each row (LayerNorm MLP page, Description, forward
+ * step (1), the tex.normalization_fwd primitive; I/O Contract: norm_type, zero_centered_gamma,
+ * epsilon).
+ *   x      [M, H] in x_dtype (TE_F32 or TE_BF16); gamma, beta [H] in x_dtype.
+ *   layernorm: y = (x - mean) / sqrt(var + epsilon) * g + beta, var the population variance.
+ *   rmsnorm:   y = x / sqrt(mean(x^2) + epsilon) * g; beta is ignored and may be NULL.
+ *   g = gamma, or 1 + gamma when zero_centered_gamma != 0.  All arithmetic is fp32.
+ *   out    [M, H] in out_dtype: TE_F32, TE_BF16, or TE_E4M3 (then q is required).
+ *   q      NULL, or the quantizer of y: amax of the fp32 y is written to q->amax (also
+ *          when out_dtype is not E4M3), and for E4M3 the codes use q's scale.
+ *   mu, rsigma  [M] fp32, optional (NULL = not written): the row mean (0 for rmsnorm) and
+ *          1 / sqrt(var + epsilon) (or 1 / sqrt(mean(x^2) + epsilon)).
+ * H must be a multiple of 8 (16-byte rows) and at most 8192.
+ */
+te_status te_norm_fwd(const void* x, te_dtype x_dtype, int64_t M, int64_t H, const void* gamma,
+                      const void* beta, te_norm_type norm_type, int zero_centered_gamma,
+                      float epsilon, const te_quantizer* q, void* out, te_dtype out_dtype,
+                      float* mu, float* rsigma, void* stream);
+
+/* ---------------------------------------------------------------------------------------
+ * te_act_lu -- activation with optional FP8 quantization (Activation page, Description: the
+ * forward rule runs the tex.act_lu primitive, quantizing when asked, and returns the values
+ * dequantized).
+ *   x      [M, N_in] in x_dtype (TE_F32 / TE_BF16).  For TE_SWIGLU, N_in = 2 * N_out and the
+ *          columns are [gate | linear]: out = silu(x[:, :N_out]) * x[:, N_out:].
+ *   out    [M, N_out] in out_dtype.
+ *   q      NULL: out = act(x) rounded to out_dtype (TE_F32 / TE_BF16).
+ *          non-NULL with out_dtype TE_E4M3: out holds the E4M3 codes.
+ *          non-NULL with out_dtype TE_F32 / TE_BF16: out holds the dequantized values
+ *          fp32(decode(q) * scale_inv), as the page's activation() returns them.
+ * N_out must be a multiple of 8.
+ */
+te_status te_act_lu(const void* x, te_dtype x_dtype, int64_t M, int64_t N_in, te_act_type act,
+                    const te_quantizer* q, void* out, te_dtype out_dtype, void* stream);
+
+/* ---------------------------------------------------------------------------------------
+ * te_dact_dbias_quantize -- the backward step that fuses the activation gradient, the bias
+ * gradient reduction and the FP8 cast (LayerNorm MLP page, Description, backward pass:
+ * tex.quantize_dact_dbias;
+ * Activation page, Description: tex.dact_lu).
+ *   dy        [M, N_out] in dtype: gradient w.r.t. the activation output.
+ *   x_preact  [M, N_in] in dtype: the activation input saved by the forward (ignored for
+ *             TE_IDENTITY, which makes dx = dy and dbias its column sums).
+ *   dx        [M, N_in] in dx_dtype: dy * act'(x_preact) computed in fp32, then rounded
+ *             (TE_F32 / TE_BF16) or quantized (TE_E4M3 with q).  Gated: [d_gate | d_linear].
+ *   dbias     [N_in] fp32 or NULL: column sums of the fp32 dx before any rounding, reduced
+ *             in a fixed order (deterministic).
+ *   workspace te_workspace_size(TE_OP_DACT_DBIAS, M, 0, N_in, ...) bytes, needed when dbias
+ *             is requested.
+ */
+te_status te_dact_dbias_quantize(const void* dy, const void* x_preact, te_dtype dtype, int64_t M,
+                                 int64_t N_in, te_act_type act, const te_quantizer* q, void* dx,
+                                 te_dtype dx_dtype, float* dbias, void* workspace,
+                                 size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------------------
+ * te_quantize -- per-tensor E4M3 cast of a [M, N] tensor (LayerNorm Dense page, Description:
+ * both the normalized output and the kernel are cast to FP8 before the GEMM).  x in x_dtype (TE_F32 / TE_BF16); out E4M3
+ * codes [M, N]; q required (DELAYED uses *scale, CURRENT computes it).  N multiple of 8.
+ */
+te_status te_quantize(const void* x, te_dtype x_dtype, int64_t M, int64_t N,
+                      const te_quantizer* q, void* out, void* stream);
+
+/* ---------------------------------------------------------------------------------------
+ * te_gemm -- D = alpha * op(A) @ op(B) + bias on the tensor cores (LayerNorm MLP page,
+ * Description, forward steps (2) and (4): the tex.gemm primitive with a bias).
+ *   op(A) is [M, K]: A stored [M, K] (a_trans = 0) or [K, M] (a_trans = 1).
+ *   op(B) is [K, N]: B stored [K, N] (b_trans = 0) or [N, K] (b_trans = 1).
+ *   ab_dtype      TE_BF16, TE_E4M3 or TE_F32 (computed as TF32); A and B share it.
+ *   a_scale_inv, b_scale_inv  device fp32 scalars or NULL (= 1); alpha is their product.
+ *   bias          [N] in bias_dtype (TE_F32 / TE_BF16) or NULL.
+ *   D             [M, N] in d_dtype (TE_F32 / TE_BF16).
+ * M >= 1; N and K multiples of 16.
+ */
+te_status te_gemm(const void* A, int a_trans, const void* B, int b_trans, te_dtype ab_dtype,
+                  int64_t M, int64_t N, int64_t K, const float* a_scale_inv,
+                  const float* b_scale_inv, const void* bias, te_dtype bias_dtype, void* D,
+                  te_dtype d_dtype, void* stream);
+
+/* ---------------------------------------------------------------------------------------
+ * te_layernorm_dense_fwd -- out = norm(x) @ kernel + bias (LayerNorm Dense page, Description
+ * and Signature: layernorm_dense(x, kernel, gamma, beta, bias, norm_type, zero_centered_gamma,
+ * epsilon, ..., quantizer_set)).
+ *   dtype         activation dtype of x, gamma, beta, bias and out (TE_F32 or TE_BF16).
+ *   x [M, H]; kernel [H, N] in kernel_dtype; bias [N] or NULL; out [M, N].
+ *   qset NULL (no quantization): the normalized output is stored in dtype, kernel_dtype must
+ *        equal dtype.  Non-NULL (FP8): qset->x and qset->kernel1 must be enabled; the
+ *        normalized output is written once, as E4M3.  kernel_dtype TE_E4M3 means the kernel is
+ *        already quantized and qset->kernel1.scale_inv holds its dequantization factor;
+ *        kernel_dtype == dtype means it is quantized in this call with qset->kernel1.
+ *   saved_ln_out  [M, H] (E4M3 with qset, else dtype) or NULL: keeps the GEMM operand.
+ *   mu, rsigma    [M] fp32 or NULL.
+ */
+te_status te_layernorm_dense_fwd(const void* x, const void* kernel, te_dtype kernel_dtype,
+                                 const void* gamma, const void* beta, const void* bias,
+                                 te_norm_type norm_type, int zero_centered_gamma, float epsilon,
+                                 const te_quantizer_set* qset, int64_t M, int64_t H, int64_t N,
+                                 te_dtype dtype, void* out, void* saved_ln_out, float* mu,
+                                 float* rsigma, void* workspace, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------------------
+ * te_layernorm_mlp_fwd -- norm -> GEMM1 + bias1 -> activation -> GEMM2 + bias2 (LayerNorm MLP
+ * page, Description steps (1)-(4); Signature: layernorm_mlp(x, gamma, beta, kernels, biases,
+ * norm_type, zero_centered_gamma, epsilon, ..., activation_type, quantizer_set)).
+ *   dtype       activation dtype of x, gamma, beta, biases, out (TE_F32 or TE_BF16).
+ *   x [M, H]; kernel1 [H, F'] with F' = 2F for TE_SWIGLU (columns [gate | linear]) else F;
+ *   kernel2 [F, H]; bias1 [F'] or NULL; bias2 [H] or NULL; out [M, H].
+ *   GEMM1's output plus bias1 is rounded to dtype before the activation; the activation and
+ *   the FP8 casts are fused into GEMM1's epilogue, bias2 into GEMM2's.
+ *   qset  NULL, or FP8 mode: qset->x, kernel1, act, kernel2 enabled; kernel_dtype TE_E4M3
+ *         means both kernels are pre-quantized (their scale_inv fields hold the factors),
+ *         kernel_dtype == dtype means they are quantized in this call.
+ *   saved_h      [M, F'] in dtype or NULL: GEMM1 output + bias1 (the activation input).
+ *   saved_ln_out [M, H] (E4M3 with qset, else dtype) or NULL.
+ *   mu, rsigma   [M] fp32 or NULL.
+ */
+te_status te_layernorm_mlp_fwd(const void* x, const void* gamma, const void* beta,
+                               const void* kernel1, const void* kernel2, te_dtype kernel_dtype,
+                               const void* bias1, const void* bias2, te_norm_type norm_type,
+                               int zero_centered_gamma, float epsilon, te_act_type act,
+                               const te_quantizer_set* qset, int64_t M, int64_t H, int64_t F,
+                               te_dtype dtype, void* out, void* saved_h, void* saved_ln_out,
+                               float* mu, float* rsigma, void* workspace, size_t ws_bytes,
+                               void* stream);
+
+/* ---------------------------------------------------------------------------------------
+ * te_norm_bwd -- gradients of te_norm_fwd (LayerNorm MLP page, Description: the backward pass
+ * yields the gradient of every parameter; LayerNorm Dense page, Description: gradients of x,
+ * gamma and beta).
+ *   dz [M, H] upstream gradient and x [M, H] the forward input, both in dtype; mu, rsigma [M]
+ *   from te_norm_fwd (mu unused for rmsnorm); gamma [H] in dtype.
+ *   With xhat = (x - mu) * rsigma (layernorm) or x * rsigma (rmsnorm), g the applied gain and
+ *   dxhat = dz * g:
+ *     layernorm: dx = rsigma * (dxhat - mean(dxhat) - xhat * mean(dxhat * xhat))
+ *     rmsnorm:   dx = rsigma * (dxhat - xhat * mean(dxhat * xhat))
+ *   dx [M, H] in dtype; dgamma [H] fp32 = sum over rows of dz * xhat; dbeta [H] fp32 = sum over
+ *   rows of dz (layernorm; may be NULL).  The column sums are reduced in a fixed order.
+ *   workspace: te_workspace_size(TE_OP_NORM_BWD, M, H, ...) bytes.  H multiple of 8, at most
+ *   8192 bf16 / 4096 fp32.
+ */
+te_status te_norm_bwd(const void* dz, const void* x, const float* mu, const float* rsigma,
+                      const void* gamma, te_dtype dtype, int64_t M, int64_t H,
+                      te_norm_type norm_type, int zero_centered_gamma, void* dx, float* dgamma,
+                      float* dbeta, void* workspace, size_t ws_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TE_GB300_H */

@@ -1,0 +1,67 @@
+"""The C-ABI library builds for sm_103a, loads, and exports every function include/*.h declares.
+
+CPU-only: no function that launches work is called.
+"""
+
+import glob
+import os
+import re
+
+import fp8_transformer_gb300 as te
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src = open(h).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        for m in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\**\s+(te_[a-z0-9_]+)\s*\(",
+                             src, flags=re.M):
+            names.add(m.group(1))
+    return names
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for fn in ("te_norm_fwd", "te_act_lu", "te_dact_dbias_quantize", "te_layernorm_dense_fwd",
+               "te_layernorm_mlp_fwd"):
+        assert fn in names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = te.lib()
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert set(te.EXPORTED) <= declared_functions()
+
+
+def test_host_only_calls():
+    assert te.version() == 100
+    assert te.status_string(0) == "TE_OK"
+    assert "timed out" in te.status_string(4)
+    b = te.binding
+    ws = te.workspace_size(b.TE_OP_LAYERNORM_MLP_FWD, 8192, 4096, 14336, b.TE_BF16, True,
+                           b.TE_BF16, b.TE_SWIGLU)
+    # ln (E4M3) + act (E4M3) + act staging (bf16) + E4M3 copies of both kernels
+    expect = 8192 * 4096 + 8192 * 14336 + 8192 * 14336 * 2 + 4096 * 28672 + 14336 * 4096
+    assert expect <= ws <= expect + 5 * 256
+    assert te.workspace_size(b.TE_OP_LAYERNORM_MLP_FWD, 8192, 4096, 14336, b.TE_BF16, True,
+                             b.TE_E4M3, b.TE_SWIGLU) < ws
+
+
+def test_invalid_arguments_rejected_before_launch():
+    lib = te.lib()
+    b = te.binding
+    # NULL x with M > 0, and a bad enum: both refused on the host, nothing launched
+    assert lib.te_norm_fwd(None, b.TE_BF16, 4, 128, None, None, 0, 0, 1e-5, None, None,
+                           b.TE_BF16, None, None, None) == b.TE_ERR_INVALID_ARG
+    assert lib.te_act_lu(None, b.TE_BF16, 0, 16, 99, None, None, b.TE_BF16,
+                         None) == b.TE_ERR_INVALID_ARG
+    # misaligned pointers and row lengths that are not whole 16-byte vectors
+    assert lib.te_quantize(8, b.TE_BF16, 1, 12, None, 16, None) == b.TE_ERR_INVALID_ARG
+    assert lib.te_gemm(16, 0, 32, 0, b.TE_BF16, 16, 24, 16, None, None, None, b.TE_F32, 64,
+                       b.TE_BF16, None) == b.TE_ERR_UNSUPPORTED
+    assert lib.te_gemm(18, 0, 32, 0, b.TE_BF16, 16, 32, 16, None, None, None, b.TE_F32, 64,
+                       b.TE_BF16, None) == b.TE_ERR_UNSUPPORTED

@@ -1,0 +1,225 @@
+"""Block-level parity: te_layernorm_dense_fwd and te_layernorm_mlp_fwd against the oracle.
+
+Small cases run every workload's recipe at shapes that span several 128 x 256 tiles with ragged
+tails, and are compared element by element.  Full-size cases run the exact benchmark
+configurations and compare a seeded sample of whole output rows (the block is row-local, so the
+oracle computes just those rows), plus properties that hold at any size.
+FP8 cases use fixed (delayed) power-of-two scales so both sides quantize with the same scale.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import fp8_transformer_gb300 as te
+from oracle import block as ob
+from oracle import numerics as nx
+from parity import (assert_e4m3_codes, assert_gemm_close, assert_reduction_close, codes, np64,
+                    rms)
+from workloads import make_inputs
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+MLP_SCALES = dict(x=32.0, w1=2048.0, act=16.0, w2=2048.0)
+
+
+def _qset(scales, mode="delayed"):
+    return te.QuantizerSet(x=te.Quantizer(scales["x"], mode), kernel1=te.Quantizer(scales["w1"]),
+                           act=te.Quantizer(scales["act"], mode),
+                           kernel2=te.Quantizer(scales["w2"]))
+
+
+def _fp8_oracle_scales(scales):
+    return {k: np.float32(v) for k, v in scales.items()}
+
+
+def run_mlp(inp, fp8=False, scales=MLP_SCALES, mode="delayed", rows=None):
+    M, H, F = inp["M"], inp["H"], inp["F"]
+    gated = inp["act"] == "swiglu"
+    dt = inp["x"].dtype
+    out = torch.empty(M, H, dtype=dt, device=DEV)
+    saved_h = torch.empty(M, 2 * F if gated else F, dtype=dt, device=DEV)
+    ln = torch.empty(M, H, dtype=torch.uint8 if fp8 else dt, device=DEV)
+    mu = torch.empty(M, dtype=torch.float32, device=DEV)
+    rs = torch.empty(M, dtype=torch.float32, device=DEV)
+    qs = _qset(scales, mode) if fp8 else None
+    te.te_layernorm_mlp_fwd(inp["x"], inp["gamma"], inp["beta"], inp["w1"], inp["w2"],
+                            inp.get("b1"), inp.get("b2"), out, norm_type=inp["norm"],
+                            zero_centered_gamma=inp["zero_centered_gamma"], epsilon=inp["eps"],
+                            activation_type=inp["act"], quantizer_set=qs, saved_h=saved_h,
+                            saved_ln_out=ln, mu=mu, rsigma=rs)
+    torch.cuda.synchronize()
+    return dict(out=out, h=saved_h, ln=ln, mu=mu, rsigma=rs, qs=qs)
+
+
+def oracle_mlp(inp, fp8=False, scales=MLP_SCALES, rows=None):
+    sel = slice(None) if rows is None else rows
+    x = np64(inp["x"])[sel]
+    return ob.layernorm_mlp_fwd(x, np64(inp["gamma"]), np64(inp["beta"]), np64(inp["w1"]),
+                                np64(inp["w2"]), None if inp.get("b1") is None else np64(inp["b1"]),
+                                None if inp.get("b2") is None else np64(inp["b2"]), inp["norm"],
+                                inp["zero_centered_gamma"], inp["eps"], inp["act"],
+                                "f32" if inp["dtype"] == "f32" else "bf16",
+                                fp8=_fp8_oracle_scales(scales) if fp8 else None)
+
+
+def check_mlp(inp, got, ref, fp8, rows=None):
+    sel = slice(None) if rows is None else rows
+    H = inp["H"]
+    F = inp["F"]
+    ln_ref = ref["ln"]
+    # normalized operand
+    if fp8:
+        assert_e4m3_codes(codes(got["ln"])[sel], ln_ref.codes, pre32=ln_ref.pre,
+                          scale=ln_ref.scale, what="ln e4m3")
+    else:
+        np.testing.assert_allclose(np64(got["ln"])[sel], ln_ref.value, rtol=2e-2,
+                                   atol=1e-3 * rms(ln_ref.value))
+    assert_reduction_close(np64(got["rsigma"])[sel], ref["rsigma"], what="rsigma")
+    # GEMM1 output (+ bias, rounded): contraction over H
+    a1 = ln_ref.value * ln_ref.inv()
+    w1 = ref["w1"].value * ref["w1"].inv()
+    assert_gemm_close(np64(got["h"])[sel], ref["h"].value, H, rms(a1), rms(w1), what="h")
+    # block output: contraction over F
+    a2 = ref["a"].value * ref["a"].inv()
+    w2 = ref["w2"].value * ref["w2"].inv()
+    assert_gemm_close(np64(got["out"])[sel], ref["out"].value, F, rms(a2), rms(w2), what="out")
+
+
+# -------------------------------------------------------------- small, element by element --
+
+SMALL = [
+    ("tiny_ln_mlp", {}),
+    ("gpt_ln_mlp", dict(M=300, H=512, F=784)),
+    ("llama_rms_mlp", dict(M=300, H=512, F=784)),
+]
+
+
+@pytest.mark.parametrize("name,shape", SMALL)
+def test_mlp_small(name, shape):
+    inp = make_inputs(name, device=DEV, **shape)
+    got = run_mlp(inp)
+    ref = oracle_mlp(inp)
+    check_mlp(inp, got, ref, fp8=False)
+
+
+@pytest.mark.parametrize("name,shape", SMALL[1:])
+def test_mlp_small_fp8(name, shape):
+    inp = make_inputs(name, device=DEV, **shape)
+    got = run_mlp(inp, fp8=True)
+    ref = oracle_mlp(inp, fp8=True)
+    check_mlp(inp, got, ref, fp8=True)
+    qs = got["qs"]
+    # amaxes of this call: normalized output and activation output
+    assert abs(qs.x.amax.item() - float(ref["ln"].amax)) <= 1e-5 * float(ref["ln"].amax)
+    assert abs(qs.act.amax.item() - float(ref["a"].amax)) <= 2e-2 * float(ref["a"].amax)
+    assert qs.act.scale_inv.item() == np.float32(1.0) / np.float32(MLP_SCALES["act"])
+
+
+@pytest.mark.parametrize("name,shape", SMALL[1:])
+def test_mlp_small_fp8_current_scaling(name, shape):
+    inp = make_inputs(name, device=DEV, **shape)
+    got = run_mlp(inp, fp8=True, mode="current")
+    qs = got["qs"]
+    ref = oracle_mlp(inp, fp8=True, scales=dict(MLP_SCALES, x=None, act=None))
+    # the scale is derived from this call's amax, in fp32, exactly as the recipe states
+    for q, r in ((qs.x, ref["ln"]), (qs.act, ref["a"])):
+        amax = np.float32(q.amax.item())
+        assert q.scale.item() == nx.compute_scale(amax)[0]
+        assert abs(float(amax) - float(r.amax)) <= 2e-2 * float(r.amax)
+    a2 = ref["a"].value * ref["a"].inv()
+    w2 = ref["w2"].value * ref["w2"].inv()
+    assert_gemm_close(got["out"], ref["out"].value, inp["F"], rms(a2), rms(w2), what="out")
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_ln_dense_small(fp8):
+    inp = make_inputs("qkv_ln_dense", device=DEV, M=300, H=512, N=784)
+    M, H, N = inp["M"], inp["H"], inp["N"]
+    out = torch.empty(M, N, dtype=torch.bfloat16, device=DEV)
+    ln = torch.empty(M, H, dtype=torch.uint8 if fp8 else torch.bfloat16, device=DEV)
+    scales = dict(x=64.0, kernel=4096.0)
+    qs = te.QuantizerSet(x=te.Quantizer(scales["x"]), kernel1=te.Quantizer(scales["kernel"])) if fp8 else None
+    te.te_layernorm_dense_fwd(inp["x"], inp["kernel"], inp["gamma"], inp["beta"], inp["bias"],
+                              out, epsilon=inp["eps"], quantizer_set=qs, saved_ln_out=ln)
+    torch.cuda.synchronize()
+    ref = ob.layernorm_dense_fwd(np64(inp["x"]), np64(inp["kernel"]), np64(inp["gamma"]),
+                                 np64(inp["beta"]), np64(inp["bias"]), "layernorm", False,
+                                 inp["eps"], "bf16",
+                                 fp8={k: np.float32(v) for k, v in scales.items()} if fp8 else None)
+    if fp8:
+        assert_e4m3_codes(ln, ref["ln"].codes, pre32=ref["ln"].pre, scale=ref["ln"].scale,
+                          what="ln e4m3")
+    a = ref["ln"].value * ref["ln"].inv()
+    w = ref["kernel"].value * ref["kernel"].inv()
+    assert_gemm_close(out, ref["out"].value, H, rms(a), rms(w), what="ln-dense out")
+
+
+def test_ln_dense_prequantized_kernel_matches_per_call_cast():
+    inp = make_inputs("qkv_ln_dense", device=DEV, M=256, H=256, N=512)
+    M, H, N = inp["M"], inp["H"], inp["N"]
+    qk = te.Quantizer(4096.0)
+    kq = torch.empty(H, N, dtype=torch.uint8, device=DEV)
+    te.te_quantize(inp["kernel"], qk, kq)
+    outs = []
+    for kernel in (inp["kernel"], kq):
+        out = torch.empty(M, N, dtype=torch.bfloat16, device=DEV)
+        qs = te.QuantizerSet(x=te.Quantizer(64.0), kernel1=te.Quantizer(4096.0))
+        te.te_layernorm_dense_fwd(inp["x"], kernel, inp["gamma"], inp["beta"], inp["bias"], out,
+                                  epsilon=inp["eps"], quantizer_set=qs)
+        outs.append(out)
+    assert torch.equal(outs[0], outs[1])
+
+
+def test_mlp_degenerate_inputs():
+    # one row, and an empty batch
+    for M in (1, 0):
+        inp = make_inputs("gpt_ln_mlp", device=DEV, M=max(M, 1), H=256, F=512)
+        x = inp["x"][:M]
+        out = torch.empty(M, 256, dtype=torch.bfloat16, device=DEV)
+        te.te_layernorm_mlp_fwd(x, inp["gamma"], inp["beta"], inp["w1"], inp["w2"], inp["b1"],
+                                inp["b2"], out, activation_type="gelu", epsilon=1e-6)
+        if M:
+            ref = ob.layernorm_mlp_fwd(np64(x), np64(inp["gamma"]), np64(inp["beta"]),
+                                       np64(inp["w1"]), np64(inp["w2"]), np64(inp["b1"]),
+                                       np64(inp["b2"]), "layernorm", False, 1e-6, "gelu", "bf16")
+            assert_gemm_close(out, ref["out"].value, 512, rms(ref["a"].value), rms(np64(inp["w2"])))
+
+
+# -------------------------------------------------------------- full size, sampled rows ----
+
+FULL = ["gpt_ln_mlp", "llama_rms_mlp"]
+
+
+@pytest.mark.parametrize("name", FULL)
+@pytest.mark.parametrize("fp8", [False, True])
+def test_mlp_full_size_sampled(name, fp8):
+    inp = make_inputs(name, device=DEV)
+    got = run_mlp(inp, fp8=fp8)
+    rng = np.random.default_rng(7)
+    rows = np.sort(rng.choice(inp["M"], size=48, replace=False))
+    rows[-1] = inp["M"] - 1  # include the last (tail) row
+    ref = oracle_mlp(inp, fp8=fp8, rows=rows)
+    check_mlp(inp, got, ref, fp8=fp8, rows=rows)
+    # properties over all rows: finite output, amax consistent with the stored codes
+    assert torch.isfinite(got["out"].float()).all()
+    if fp8:
+        qs = got["qs"]
+        deq_max = np.abs(nx.e4m3_decode(np.unique(codes(got["ln"])))).max() / MLP_SCALES["x"]
+        assert abs(deq_max - qs.x.amax.item()) <= qs.x.amax.item() / 16
+
+
+def test_ln_dense_full_size_sampled():
+    inp = make_inputs("qkv_ln_dense", device=DEV)
+    M, H, N = inp["M"], inp["H"], inp["N"]
+    out = torch.empty(M, N, dtype=torch.bfloat16, device=DEV)
+    te.te_layernorm_dense_fwd(inp["x"], inp["kernel"], inp["gamma"], inp["beta"], inp["bias"],
+                              out, epsilon=inp["eps"])
+    torch.cuda.synchronize()
+    rows = np.array([0, 1, 100, 5000, 8200, 12345, M - 1])  # rows 0 and 100 are the x8 rows
+    ref = ob.layernorm_dense_fwd(np64(inp["x"])[rows], np64(inp["kernel"]), np64(inp["gamma"]),
+                                 np64(inp["beta"]), np64(inp["bias"]), "layernorm", False,
+                                 inp["eps"], "bf16")
+    assert_gemm_close(np64(out)[rows], ref["out"].value, H, rms(ref["ln"].value),
+                      rms(np64(inp["kernel"])), what="qkv out")

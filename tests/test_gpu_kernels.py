@@ -1,0 +1,291 @@
+"""Kernel-level parity: each C-ABI call against the oracle on seeded inputs.
+
+Shapes span several tiles / vectors plus ragged tails and the degenerate cases (one row, empty
+input).  Inputs come from ``workloads.random_tensor``; nothing the oracle reads comes from the
+CUDA path.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import fp8_transformer_gb300 as te
+from oracle import block as ob
+from oracle import numerics as nx
+from parity import (assert_e4m3_codes, assert_elementwise_close, assert_gemm_close,
+                    assert_reduction_close, codes, np64, rms)
+from workloads import random_tensor
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+TDT = {"bf16": torch.bfloat16, "f32": torch.float32}
+
+
+def rt(shape, std=1.0, seed=0, dtype="bf16", mean=0.0):
+    return random_tensor(shape, std=std, device=DEV, seed=seed, dtype=dtype, mean=mean)
+
+
+# ------------------------------------------------------------------ quantize ---------------
+
+
+@pytest.mark.parametrize("M,N", [(1, 8), (37, 264), (1024, 4096)])
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("mode", ["delayed", "current"])
+def test_quantize_bit_exact(M, N, dtype, mode):
+    x = rt((M, N), std=3.0, seed=M + N, dtype=dtype)
+    q = te.Quantizer(scale=17.0, mode=mode)
+    out = torch.empty(M, N, dtype=torch.uint8, device=DEV)
+    te.te_quantize(x, q, out)
+    torch.cuda.synchronize()
+    xv = np64(x)
+    amax = nx.amax_of(xv)
+    assert q.amax.item() == amax  # order-free max: bit-exact
+    scale = np.float32(17.0) if mode == "delayed" else nx.compute_scale(amax)[0]
+    assert q.scale.item() == scale
+    assert q.scale_inv.item() == np.float32(1.0) / scale
+    assert_e4m3_codes(out, nx.quantize(xv, scale), what="quantize")
+
+
+def test_quantize_saturates_and_keeps_sign():
+    x = torch.tensor([[1000.0, -1000.0, 0.0, -0.0, 448.0, 464.0, 1e-3, -1e-3]], device=DEV)
+    q = te.Quantizer(scale=1.0)
+    out = torch.empty(1, 8, dtype=torch.uint8, device=DEV)
+    te.te_quantize(x, q, out)
+    assert_e4m3_codes(out, nx.quantize(np64(x), np.float32(1.0)), what="saturate")
+
+
+# ------------------------------------------------------------------ activation -------------
+
+
+@pytest.mark.parametrize("act", ["relu", "gelu", "silu", "swiglu"])
+@pytest.mark.parametrize("M,N", [(1, 16), (300, 1040)])
+def test_act_lu_bf16(act, M, N):
+    x = rt((M, N), std=2.0, seed=3)
+    n_out = N // 2 if act == "swiglu" else N
+    out = torch.empty(M, n_out, dtype=torch.bfloat16, device=DEV)
+    q = te.Quantizer(scale=1.0)  # records amax even without quantizing
+    te.te_act_lu(x, act, out)
+    ref = ob.act_fwd(np64(x), act)
+    assert_elementwise_close(out, nx.bf16_round(nx.to_f32(ref)), what=act)
+    if act == "relu":  # exact arithmetic: bit-exact
+        assert np.array_equal(np64(out), nx.bf16_round(ref))
+
+
+@pytest.mark.parametrize("act", ["gelu", "swiglu"])
+@pytest.mark.parametrize("mode", ["delayed", "current"])
+def test_act_lu_e4m3_and_dequantized(act, mode):
+    M, N = 257, 2048
+    x = rt((M, N), std=2.0, seed=4)
+    n_out = N // 2 if act == "swiglu" else N
+    q = te.Quantizer(scale=64.0, mode=mode)
+    out = torch.empty(M, n_out, dtype=torch.uint8, device=DEV)
+    te.te_act_lu(x, act, out, q=q)
+    torch.cuda.synchronize()
+    pre = nx.to_f32(ob.act_fwd(np64(x), act))
+    amax = q.amax.item()
+    assert abs(amax - nx.amax_of(pre)) <= 1e-6 * amax
+    scale = np.float32(64.0) if mode == "delayed" else np.float32(q.scale.item())
+    if mode == "current":
+        assert scale == nx.compute_scale(np.float32(amax))[0]
+    assert_e4m3_codes(out, nx.quantize(pre, scale), pre32=pre, scale=scale, what="act e4m3")
+    # dequantized output (the pages' activation() result) in bf16
+    deq = torch.empty(M, n_out, dtype=torch.bfloat16, device=DEV)
+    q2 = te.Quantizer(scale=64.0, mode=mode)
+    te.te_act_lu(x, act, deq, q=q2)
+    want = nx.bf16_round(nx.dequantize(codes(out), np.float32(1.0) / scale))
+    got = np64(deq)
+    mism = got != want
+    assert mism.mean() <= 1e-3  # only where the code itself flipped
+
+
+# ------------------------------------------------------------------ dact + dbias -----------
+
+
+@pytest.mark.parametrize("act", ["gelu", "relu", "silu", "swiglu", "identity"])
+@pytest.mark.parametrize("M,N_in", [(1, 16), (300, 528), (1000, 4096)])
+def test_dact_dbias_bf16(act, M, N_in):
+    n_out = N_in // 2 if act == "swiglu" else N_in
+    dy = rt((M, n_out), seed=5)
+    h = rt((M, N_in), std=2.0, seed=6)
+    dx = torch.empty(M, N_in, dtype=torch.bfloat16, device=DEV)
+    db = torch.empty(N_in, dtype=torch.float32, device=DEV)
+    te.te_dact_dbias_quantize(dy, h, act, dx, dbias=db)
+    ref = np64(dy) if act == "identity" else ob.act_bwd(np64(dy), np64(h), act)
+    assert_elementwise_close(dx, nx.bf16_round(nx.to_f32(ref)), what=f"d{act}")
+    assert_reduction_close(db, ob.colsum(nx.to_f32(ref)), what=f"dbias {act}")
+
+
+@pytest.mark.parametrize("mode", ["delayed", "current"])
+def test_dact_dbias_e4m3(mode):
+    M, N = 1000, 2048
+    dy = rt((M, N), seed=7)
+    h = rt((M, N), std=2.0, seed=8)
+    q = te.Quantizer(scale=32.0, mode=mode)
+    dx = torch.empty(M, N, dtype=torch.uint8, device=DEV)
+    db = torch.empty(N, dtype=torch.float32, device=DEV)
+    te.te_dact_dbias_quantize(dy, h, "gelu", dx, dbias=db, q=q)
+    torch.cuda.synchronize()
+    pre = nx.to_f32(ob.act_bwd(np64(dy), np64(h), "gelu"))
+    scale = np.float32(32.0) if mode == "delayed" else np.float32(q.scale.item())
+    assert_e4m3_codes(dx, nx.quantize(pre, scale), pre32=pre, scale=scale, what="dact e4m3")
+    assert_reduction_close(db, ob.colsum(pre), what="dbias")
+    assert abs(q.amax.item() - nx.amax_of(pre)) <= 1e-6 * nx.amax_of(pre)
+
+
+def test_dbias_deterministic():
+    M, N = 4096, 1024
+    dy, h = rt((M, N), seed=9), rt((M, N), seed=10)
+    outs = []
+    for _ in range(3):
+        dx = torch.empty(M, N, dtype=torch.bfloat16, device=DEV)
+        db = torch.empty(N, dtype=torch.float32, device=DEV)
+        te.te_dact_dbias_quantize(dy, h, "gelu", dx, dbias=db)
+        outs.append(db.cpu())
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])
+
+
+# ------------------------------------------------------------------ norm -------------------
+
+
+@pytest.mark.parametrize("norm", ["layernorm", "rmsnorm"])
+@pytest.mark.parametrize("M,H,dtype", [(1, 128, "f32"), (129, 136, "bf16"), (1000, 4096, "bf16"),
+                                       (70, 8192, "bf16"), (64, 128, "f32")])
+@pytest.mark.parametrize("zc", [False, True])
+def test_norm_fwd(norm, M, H, dtype, zc):
+    x = rt((M, H), std=2.0, seed=11, dtype=dtype, mean=0.5)
+    gamma = rt((H,), std=0.1, seed=12, dtype=dtype, mean=0.0 if zc else 1.0)
+    beta = rt((H,), std=0.1, seed=13, dtype=dtype)
+    out = torch.empty(M, H, dtype=TDT[dtype], device=DEV)
+    mu = torch.empty(M, dtype=torch.float32, device=DEV)
+    rs = torch.empty(M, dtype=torch.float32, device=DEV)
+    q = te.Quantizer()
+    te.te_norm_fwd(x, gamma, beta, norm, zc, 1e-5, out, q=q, mu=mu, rsigma=rs)
+    y, m_ref, r_ref = ob.norm_fwd(np64(x), np64(gamma), np64(beta), norm, zc, 1e-5)
+    want = nx.to_f32(y) if dtype == "f32" else nx.bf16_round(nx.to_f32(y))
+    assert_elementwise_close(out, want, what=f"{norm} y")
+    assert_reduction_close(rs, r_ref, what="rsigma")
+    if norm == "layernorm":
+        assert_reduction_close(mu, m_ref, what="mu")
+    torch.cuda.synchronize()
+    assert abs(q.amax.item() - nx.amax_of(nx.to_f32(y))) <= 1e-5 * nx.amax_of(nx.to_f32(y))
+
+
+@pytest.mark.parametrize("mode", ["delayed", "current"])
+def test_norm_fwd_e4m3(mode):
+    M, H = 1000, 4096
+    x = rt((M, H), seed=14)
+    gamma, beta = rt((H,), 0.1, 15, mean=1.0), rt((H,), 0.1, 16)
+    out = torch.empty(M, H, dtype=torch.uint8, device=DEV)
+    q = te.Quantizer(scale=64.0, mode=mode)
+    te.te_norm_fwd(x, gamma, beta, "layernorm", False, 1e-5, out, q=q)
+    torch.cuda.synchronize()
+    y, _, _ = ob.norm_fwd(np64(x), np64(gamma), np64(beta), "layernorm", False, 1e-5)
+    pre = nx.to_f32(y)
+    scale = np.float32(64.0) if mode == "delayed" else np.float32(q.scale.item())
+    if mode == "current":
+        assert scale == nx.compute_scale(np.float32(q.amax.item()))[0]
+    assert q.scale_inv.item() == np.float32(1.0) / scale
+    assert_e4m3_codes(out, nx.quantize(pre, scale), pre32=pre, scale=scale, what="norm e4m3")
+
+
+def test_norm_scale_identity_outlier_rows():
+    """LN(8x; eps) == LN(x; eps/64): rows scaled by 8 normalize to the unscaled rows' output."""
+    M, H = 64, 1024
+    x = rt((M, H), seed=17, dtype="f32")
+    x8 = x * 8.0
+    g, b = rt((H,), 0.1, 18, "f32", 1.0), rt((H,), 0.1, 19, "f32")
+    o1 = torch.empty(M, H, device=DEV)
+    o2 = torch.empty(M, H, device=DEV)
+    te.te_norm_fwd(x8, g, b, "layernorm", False, 1e-5, o1)
+    te.te_norm_fwd(x, g, b, "layernorm", False, 1e-5 / 64, o2)
+    assert torch.allclose(o1, o2, rtol=1e-5, atol=1e-5)
+
+
+@pytest.mark.parametrize("norm", ["layernorm", "rmsnorm"])
+@pytest.mark.parametrize("M,H", [(1, 128), (300, 1032), (2000, 4096)])
+def test_norm_bwd(norm, M, H):
+    x = rt((M, H), std=2.0, seed=20)
+    gamma = rt((H,), 0.1, 21, mean=1.0)
+    dz = rt((M, H), seed=22)
+    _, mu, rs = ob.norm_fwd(np64(x), np64(gamma), None if norm == "rmsnorm" else np.zeros(H),
+                            norm, False, 1e-5)
+    mu_t = torch.tensor(mu, dtype=torch.float32, device=DEV)
+    rs_t = torch.tensor(rs, dtype=torch.float32, device=DEV)
+    dx = torch.empty(M, H, dtype=torch.bfloat16, device=DEV)
+    dg = torch.empty(H, dtype=torch.float32, device=DEV)
+    db = torch.empty(H, dtype=torch.float32, device=DEV)
+    te.te_norm_bwd(dz, x, mu_t, rs_t, gamma, norm, False, dx, dg, db)
+    rdx, rdg, rdb = ob.norm_bwd(np64(dz), np64(x), np64(mu_t), np64(rs_t), np64(gamma), norm, False)
+    assert_elementwise_close(dx, nx.bf16_round(nx.to_f32(rdx)), what="dx", abs_rms=2e-3)
+    assert_reduction_close(dg, rdg, what="dgamma")
+    if norm == "layernorm":
+        assert_reduction_close(db, rdb, what="dbeta")
+
+
+# ------------------------------------------------------------------ GEMM -------------------
+
+
+@pytest.mark.parametrize("a_trans,b_trans", [(False, False), (False, True), (True, False),
+                                             (True, True)])
+@pytest.mark.parametrize("M,N,K", [(128, 256, 64), (300, 272, 96), (520, 784, 1040)])
+def test_gemm_bf16_layouts(a_trans, b_trans, M, N, K):
+    if a_trans and M % 16:
+        M += 16 - M % 16
+    A = rt((K, M) if a_trans else (M, K), seed=23)
+    B = rt((N, K) if b_trans else (K, N), seed=24)
+    bias = rt((N,), 0.5, 25)
+    out = torch.empty(M, N, dtype=torch.bfloat16, device=DEV)
+    te.te_gemm(A, B, out, a_trans=a_trans, b_trans=b_trans, bias=bias)
+    a = np64(A).T if a_trans else np64(A)
+    b = np64(B).T if b_trans else np64(B)
+    ref = ob.gemm(a, b, np64(bias))
+    assert_gemm_close(out, ref, K, rms(a), rms(b), what=f"gemm bf16 {a_trans}{b_trans}")
+
+
+@pytest.mark.parametrize("a_trans,b_trans", [(False, False), (False, True), (True, True)])
+def test_gemm_e4m3(a_trans, b_trans):
+    M, N, K = 384, 528, 640
+    Af = rt((K, M) if a_trans else (M, K), std=50.0, seed=26, dtype="f32")
+    Bf = rt((N, K) if b_trans else (K, N), std=50.0, seed=27, dtype="f32")
+    A = Af.clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8)
+    B = Bf.clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8)
+    sa = torch.tensor([1 / 64.0], device=DEV)
+    sb = torch.tensor([1 / 128.0], device=DEV)
+    out = torch.empty(M, N, dtype=torch.float32, device=DEV)
+    te.te_gemm(A, B, out, a_trans=a_trans, b_trans=b_trans, a_scale_inv=sa, b_scale_inv=sb)
+    a = nx.e4m3_decode(codes(A))
+    b = nx.e4m3_decode(codes(B))
+    a = a.T if a_trans else a
+    b = b.T if b_trans else b
+    ref = ob.gemm(a, b, None, alpha=ob.gemm_alpha(1 / 64.0, 1 / 128.0))
+    # fp8 products are exact in fp32 accumulation up to summation order
+    assert_gemm_close(out, ref, K, rms(a) / 64, rms(b) / 128, what="gemm e4m3")
+    err = np.abs(np64(out) - ref).max()
+    assert err <= 1e-5 * np.abs(ref).max() + 1e-6
+
+
+@pytest.mark.parametrize("b_trans", [False, True])
+def test_gemm_tf32(b_trans):
+    M, N, K = 200, 288, 160
+    A = rt((M, K), seed=28, dtype="f32")
+    B = rt((N, K) if b_trans else (K, N), seed=29, dtype="f32")
+    bias = rt((N,), 0.1, 30, dtype="f32")
+    out = torch.empty(M, N, dtype=torch.float32, device=DEV)
+    te.te_gemm(A, B, out, b_trans=b_trans, bias=bias)
+    b = np64(B).T if b_trans else np64(B)
+    ref = ob.gemm(np64(A), b, np64(bias))
+    assert_gemm_close(out, ref, K, rms(np64(A)), rms(b), what="gemm tf32")
+
+
+def test_gemm_rejects_bad_shapes():
+    A = torch.zeros(16, 24, dtype=torch.bfloat16, device=DEV)
+    B = torch.zeros(24, 16, dtype=torch.bfloat16, device=DEV)
+    out = torch.empty(16, 16, dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(te.TEError) as e:
+        te.te_gemm(A, B, out)  # K = 24 is not a multiple of 16
+    assert e.value.status == te.binding.TE_ERR_UNSUPPORTED
+
+
+def test_no_device_timeouts_recorded():
+    torch.cuda.synchronize()
+    assert te.get_device_status() == 0
