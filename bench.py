@@ -1,0 +1,397 @@
+#!/usr/bin/env python
+"""Throughput of the fused norm + feed-forward block forward on GB300.
+
+A step is one te_layernorm_mlp_fwd call (RMSNorm -> GEMM1 -> SwiGLU -> GEMM2, the whole
+forward hot path) over one batch of the Llama-style workload: tokens 8192, hidden 4096,
+ffn 14336 (W1 [4096, 28672], W2 [14336, 4096]), zero-centered gamma, no biases, synthetic
+seeded inputs.  The headline is the bf16 path; the FP8 (E4M3, delayed per-tensor scaling,
+weights cached in E4M3) path and the bandwidth-bound kernels are reported beside it.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+N > 1 runs under torchrun, one rank per GPU; every rank processes its own batch (the block is
+row-independent, so there is no data-path collective) and rank 0 prints one JSON line.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "llama_rms_mlp"
+METRIC = "fused LN-MLP fwd TFLOP/s (bf16, FP8) & % tensor peak; norm/dact GB/s % HBM"
+UNIT = "TFLOP/s"
+FLUSH_BYTES = 512 << 20  # > 129 MB L2
+ORACLE_ROWS_BASELINE = 256
+ORACLE_ROWS_REFERENCE = 32
+
+
+def mlp_flops(M, H, F, gated):
+    f1 = 2 * F if gated else F
+    return 2.0 * M * H * f1 + 2.0 * M * F * H
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return dict(hbm=float(p["hbm_gbs"]), bf16=float(p["bf16_tflops"]),
+                    bf16_sustained=float(p["bf16_tflops_sustained"]), source="measured")
+    except Exception:
+        return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return dict(sm_mhz=None, sm_max_mhz=None, reasons=["nvidia-smi unavailable"])
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.file.read().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.file.name)
+        return dict(sm_mhz=statistics.median(sm) if sm else None,
+                    sm_max_mhz=max(smax) if smax else None, reasons=sorted(reasons),
+                    samples=len(sm))
+
+
+def time_steps(step, K, flush, streams=None):
+    """Per-step CUDA-event durations (ms) on the current stream, L2 flushed before each step."""
+    import torch
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    for i in range(K):
+        if flush is not None:
+            flush()
+        starts[i].record()
+        step()
+        ends[i].record()
+    torch.cuda.synchronize()
+    return [s.elapsed_time(e) for s, e in zip(starts, ends)]
+
+
+def oracle_baseline(inp, rows, reps=1):
+    """The oracle's forward on the first `rows` rows of the batch, timed on the host cores."""
+    import numpy as np
+    from oracle import block as ob
+
+    f64 = lambda t: None if t is None else t.detach().cpu().double().numpy()
+    x = f64(inp["x"][:rows])
+    g, b, w1, w2 = (f64(inp[k]) for k in ("gamma", "beta", "w1", "w2"))
+    times = []
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        ob.layernorm_mlp_fwd(x, g, b, w1, w2, None, None, inp["norm"], inp["zero_centered_gamma"],
+                             inp["eps"], inp["act"], "bf16")
+        times.append(time.perf_counter() - t0)
+    flops = mlp_flops(rows, inp["H"], inp["F"], inp["act"] == "swiglu")
+    return flops, times
+
+
+def cores_used():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def run_reference(args, rank, world):
+    """The oracle as the reference arm: same metric and workload, a bounded row sample per step."""
+    if rank != 0:
+        return
+    import torch
+    from workloads import make_inputs
+    inp = make_inputs(WORKLOAD, device="cpu")
+    rows = ORACLE_ROWS_REFERENCE
+    for _ in range(args.warmup):
+        oracle_baseline(inp, rows)
+    flops, times = oracle_baseline(inp, rows, reps=args.steps)
+    ms = 1e3 * statistics.mean(times)
+    value = flops / (ms / 1e3) / 1e12
+    sample = f"{rows} of {inp['M']} token rows per step, full weights, fp64 numpy"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{WORKLOAD} M=8192 H=4096 F=14336 swiglu rmsnorm (oracle sample)",
+                   "parallelism": "replicas", "l2": "n/a (CPU)"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores_used(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, rank, world, local_rank):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import fp8_transformer_gb300 as te
+    from workloads import make_inputs
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    te.lib()
+    peaks = load_peaks()
+    inp = make_inputs(WORKLOAD, device=dev, seed=rank, M=args.tokens)
+    M, H, F = inp["M"], inp["H"], inp["F"]
+    gated = inp["act"] == "swiglu"
+    flops = mlp_flops(M, H, F, gated)
+    gemm1_flops = 2.0 * M * H * (2 * F if gated else F)
+    x, gamma, beta, w1, w2 = (inp[k] for k in ("x", "gamma", "beta", "w1", "w2"))
+    out = torch.empty(M, H, dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(te.workspace_size(te.binding.TE_OP_LAYERNORM_MLP_FWD, M, H, F,
+                                       te.binding.TE_BF16, True, te.binding.TE_BF16,
+                                       te.binding.TE_SWIGLU), dtype=torch.uint8, device=dev)
+    flush_buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = lambda: flush_buf.zero_()
+    common = dict(norm_type=inp["norm"], zero_centered_gamma=inp["zero_centered_gamma"],
+                  epsilon=inp["eps"], activation_type=("silu", "linear"), workspace=ws)
+
+    def step_bf16(xx=x, oo=out):
+        te.te_layernorm_mlp_fwd(xx, gamma, beta, w1, w2, None, None, oo, **common)
+
+    # FP8 steady state: weights cached in E4M3 with their own scales; x / act scales from a
+    # calibration call in current-scaling mode (delayed scaling with a history of one).
+    qw1, qw2 = te.Quantizer(1.0, "current", dev), te.Quantizer(1.0, "current", dev)
+    w1q = torch.empty_like(w1, dtype=torch.uint8)
+    w2q = torch.empty_like(w2, dtype=torch.uint8)
+    te.te_quantize(w1, qw1, w1q)
+    te.te_quantize(w2, qw2, w2q)
+    qx, qa = te.Quantizer(1.0, "current", dev), te.Quantizer(1.0, "current", dev)
+    calib = te.QuantizerSet(x=qx, kernel1=qw1, act=qa, kernel2=qw2)
+    te.te_layernorm_mlp_fwd(x, gamma, beta, w1q, w2q, None, None, out, quantizer_set=calib,
+                            **common)
+    torch.cuda.synchronize()
+    qx.mode = qa.mode = te.binding.TE_SCALING_DELAYED
+    qs = te.QuantizerSet(x=qx, kernel1=qw1, act=qa, kernel2=qw2)
+
+    def step_fp8():
+        te.te_layernorm_mlp_fwd(x, gamma, beta, w1q, w2q, None, None, out, quantizer_set=qs,
+                                **common)
+
+    def barrier():
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+
+    def max_over_ranks(v):
+        if world == 1:
+            return v
+        t = torch.tensor([v], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    for _ in range(args.warmup):
+        flush()
+        step_bf16()
+        flush()
+        step_fp8()
+    barrier()
+
+    # ---- headline: bf16 forward, K timed steps, library kernels profiled on the same stream
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    barrier()
+    t_wall = time.perf_counter()
+    te.profile_begin(64 * args.steps)
+    ms_bf16 = time_steps(step_bf16, args.steps, flush)
+    prof_bf16 = te.profile_end()
+    barrier()
+    wall_bf16 = time.perf_counter() - t_wall
+    te.profile_begin(64 * args.steps)
+    ms_fp8 = time_steps(step_fp8, args.steps, flush)
+    prof_fp8 = te.profile_end()
+    barrier()
+    clocks = sampler.stop() if sampler else None
+
+    ms_step = max_over_ranks(statistics.mean(ms_bf16))
+    ms_step_fp8 = max_over_ranks(statistics.mean(ms_fp8))
+    value = world * flops / (ms_step / 1e3) / 1e12
+    value_fp8 = world * flops / (ms_step_fp8 / 1e3) / 1e12
+    launches = sum(n for _, n in prof_bf16.values())
+    if args.kernels_only:
+        if rank == 0:
+            print(json.dumps({"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+                              "ms_per_step": ms_step, "fp8_ms_per_step": ms_step_fp8,
+                              "value_fp8": value_fp8, "tokens": M, "kernels_only": True,
+                              "profile_bf16": prof_bf16, "profile_fp8": prof_fp8}), flush=True)
+        return
+
+    # ---- end to end through the public call: pinned host input -> device -> host output
+    x_host = x.cpu().pin_memory()
+    out_host = torch.empty(M, H, dtype=torch.bfloat16).pin_memory()
+    x_dev = torch.empty_like(x)
+
+    def step_e2e():
+        x_dev.copy_(x_host, non_blocking=True)
+        step_bf16(x_dev, out)
+        out_host.copy_(out, non_blocking=True)
+
+    for _ in range(2):
+        step_e2e()
+    barrier()
+    ms_e2e = max_over_ranks(statistics.mean(time_steps(step_e2e, args.steps, flush)))
+    e2e_value = world * flops / (ms_e2e / 1e3) / 1e12
+
+    # ---- bandwidth-bound kernels: norm (this workload's shape) and dact+dbias+quantize
+    mu = torch.empty(M, dtype=torch.float32, device=dev)
+    rs = torch.empty(M, dtype=torch.float32, device=dev)
+    ln_out = torch.empty(M, H, dtype=torch.bfloat16, device=dev)
+    norm_step = lambda: te.te_norm_fwd(x, gamma, beta, inp["norm"], True, inp["eps"], ln_out,
+                                       mu=mu, rsigma=rs)
+    norm_bytes = M * H * (2 + 2) + H * 2 + M * 8
+    norm_step()
+    ms_norm = max_over_ranks(statistics.mean(time_steps(norm_step, args.steps, flush)))
+    Md, Nd = 16384, 16384  # the GPT workload's activation gradient
+    dyd = torch.randn(Md, Nd, device=dev, dtype=torch.bfloat16)
+    hd = torch.randn(Md, Nd, device=dev, dtype=torch.bfloat16)
+    dxd = torch.empty(Md, Nd, device=dev, dtype=torch.uint8)
+    dbd = torch.empty(Nd, device=dev, dtype=torch.float32)
+    qd = te.Quantizer(16.0, "delayed", dev)
+    wsd = torch.empty(te.workspace_size(te.binding.TE_OP_DACT_DBIAS, Md, 0, Nd), dtype=torch.uint8,
+                      device=dev)
+    dact_step = lambda: te.te_dact_dbias_quantize(dyd, hd, "gelu", dxd, dbias=dbd, q=qd,
+                                                  workspace=wsd)
+    dact_bytes = Md * Nd * (2 + 2 + 1) + Nd * 4
+    dact_step()
+    ms_dact = max_over_ranks(statistics.mean(time_steps(dact_step, args.steps, flush)))
+    barrier()
+
+    if rank != 0:
+        return
+
+    g1_ms, g1_n = prof_bf16["gemm_act"]
+    g1_avg = g1_ms / max(g1_n, 1)
+    achieved = gemm1_flops / (g1_avg / 1e3) / 1e12
+    g1f_ms, g1f_n = prof_fp8["gemm_act"]
+    achieved_fp8 = gemm1_flops / (g1f_ms / max(g1f_n, 1) / 1e3) / 1e12
+    fp8_peak = 2.0 * peaks["bf16"]  # nominal fp8 : bf16 dense ratio 4.5 : 2.25
+    cpu_flops, cpu_times = oracle_baseline(inp, ORACLE_ROWS_BASELINE)
+    cpu_value = cpu_flops / cpu_times[0] / 1e12
+    share = {k: round(v[0] / max(sum(t for t, _ in prof_bf16.values()), 1e-9), 4)
+             for k, v in prof_bf16.items() if v[1]}
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{WORKLOAD}: tokens {M}, hidden {H}, ffn {F}, rmsnorm "
+                               "(zero-centered gamma) -> SwiGLU MLP, no biases",
+                   "tokens_per_rank": M, "parallelism": "replicas (token-parallel, no collective)",
+                   "l2": f"flushed between steps ({FLUSH_BYTES >> 20} MiB write)"},
+        "tensor_frac_bf16": value / world / peaks["bf16"],
+        "fp8": {"value": value_fp8, "unit": UNIT, "ms_per_step": ms_step_fp8,
+                "frac": value_fp8 / world / fp8_peak,
+                "peak": fp8_peak, "peak_note": f"{peaks['source']} bf16 burst x nominal 2"},
+        "bandwidth_kernels": {
+            "norm_fwd": {"shape": [M, H], "GB/s": norm_bytes / (ms_norm / 1e3) / 1e9,
+                         "frac": norm_bytes / (ms_norm / 1e3) / 1e9 / peaks["hbm"],
+                         "ms": ms_norm, "bytes": norm_bytes},
+            "dact_dbias_quantize": {"shape": [Md, Nd], "GB/s": dact_bytes / (ms_dact / 1e3) / 1e9,
+                                    "frac": dact_bytes / (ms_dact / 1e3) / 1e9 / peaks["hbm"],
+                                    "ms": ms_dact, "bytes": dact_bytes}},
+        "clocks": clocks,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": x.numel() * 2,
+                "d2h_bytes_per_step": out.numel() * 2, "ms_per_step": ms_e2e},
+        "gpu_launches": launches,
+        "kernel_share": share,
+        "roofline": {"kernel": "gemm_act (GEMM1 + SwiGLU epilogue, bf16)", "bound": "tensor",
+                     "achieved": achieved, "peak": peaks["bf16"], "unit": "TFLOP/s",
+                     "frac": achieved / peaks["bf16"], "traffic": None,
+                     "peak_note": f"{peaks['source']} bf16 burst",
+                     "fp8_achieved": achieved_fp8, "fp8_frac": achieved_fp8 / fp8_peak},
+        "cpu_baseline": {"value": cpu_value, "unit": UNIT, "cores": cores_used(),
+                         "kind": "oracle",
+                         "sample": f"{ORACLE_ROWS_BASELINE} of {M} token rows, full weights, "
+                                   f"fp64 numpy, {cpu_times[0]:.1f} s"},
+        "wall_s_bf16_region": wall_bf16,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="override the token count (profiling runs on a smaller batch)")
+    ap.add_argument("--kernels-only", action="store_true",
+                    help="time the GPU steps only: no e2e, bandwidth kernels or CPU baseline")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if (args.impl == "ours" and torch.cuda.is_available()) else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local_rank)
+        dist.init_process_group(backend)
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank, world)
+        else:
+            run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -35,7 +35,10 @@ _DTYPE = {torch.float32: TE_F32, torch.bfloat16: TE_BF16, torch.uint8: TE_E4M3,
 
 EXPORTED = ["te_status_string", "te_version", "te_get_device_status", "te_workspace_size",
             "te_norm_fwd", "te_act_lu", "te_dact_dbias_quantize", "te_quantize", "te_gemm",
-            "te_layernorm_dense_fwd", "te_layernorm_mlp_fwd", "te_norm_bwd"]
+            "te_layernorm_dense_fwd", "te_layernorm_mlp_fwd", "te_norm_bwd",
+            "te_profile_begin", "te_profile_end"]
+KERNEL_KINDS = ["norm_fwd", "quantize", "act_lu", "dact_dbias", "gemm", "gemm_act", "norm_bwd",
+                "transpose"]
 
 
 class TEError(RuntimeError):
@@ -86,6 +89,8 @@ _SIGS = {
                                             _vp, _vp, _sz, _vp]),
     "te_norm_bwd": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, ctypes.c_int, _i64, _i64,
                                    ctypes.c_int, ctypes.c_int, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "te_profile_begin": (ctypes.c_int, [ctypes.c_int32]),
+    "te_profile_end": (ctypes.c_int, [ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_int32)]),
 }
 
 
@@ -314,3 +319,17 @@ def te_norm_bwd(dz, x, mu, rsigma, gamma, norm_type, zero_centered_gamma, dx, dg
                            _stream(stream))
     _check("te_norm_bwd", st)
     return dx
+
+
+def profile_begin(max_records: int = 4096):
+    """Start timing every library kernel launch with CUDA events on its launching stream."""
+    _check("te_profile_begin", lib().te_profile_begin(int(max_records)))
+
+
+def profile_end() -> dict:
+    """Stop timing; returns {kind: (total_ms, launches)} for the kernels launched since begin."""
+    n = len(KERNEL_KINDS)
+    ms = (ctypes.c_float * n)()
+    cnt = (ctypes.c_int32 * n)()
+    _check("te_profile_end", lib().te_profile_end(ms, cnt))
+    return {k: (float(ms[i]), int(cnt[i])) for i, k in enumerate(KERNEL_KINDS)}

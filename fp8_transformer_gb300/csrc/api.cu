@@ -88,6 +88,8 @@ te_status run_cast(const te_quantizer* q, int out_dtype, int fake_quant, cudaStr
 // Workspace layout of the composed forward passes (shared by te_workspace_size and the calls).
 struct FwdLayout {
   void* ln = nullptr;     // normalized output (when not saved by the caller)
+  void* kt1 = nullptr;    // fp32: kernel1 / the dense kernel transposed to [out, in]
+  void* kt2 = nullptr;    // fp32: kernel2 transposed
   void* kq1 = nullptr;    // E4M3 copy of kernel1 / the dense kernel
   void* kq2 = nullptr;    // E4M3 copy of kernel2
   void* a2 = nullptr;     // activation output, GEMM2 operand
@@ -101,6 +103,7 @@ FwdLayout dense_layout(void* ws, int64_t M, int64_t H, int64_t N, int dtype, boo
   FwdLayout L;
   if (!have_saved_ln) L.ln = c.take(size_t(M) * H * (quant ? 1 : esize(dtype)));
   if (quant && kernel_dtype != TE_E4M3) L.kq1 = c.take(size_t(H) * N);
+  if (!quant && dtype == TE_F32) L.kt1 = c.take(size_t(H) * N * 4);
   L.bytes = c.used;
   return L;
 }
@@ -118,6 +121,9 @@ FwdLayout mlp_layout(void* ws, int64_t M, int64_t H, int64_t F, int dtype, bool 
       L.kq1 = c.take(size_t(H) * F1);
       L.kq2 = c.take(size_t(F) * H);
     }
+  } else if (dtype == TE_F32) {
+    L.kt1 = c.take(size_t(H) * F1 * 4);
+    L.kt2 = c.take(size_t(F) * H * 4);
   }
   L.bytes = c.used;
   return L;
@@ -300,6 +306,8 @@ te_status te_gemm(const void* A, int a_trans, const void* B, int b_trans, te_dty
   if (M > 0 && (!A || !B || !D)) return TE_ERR_INVALID_ARG;
   if (N % 16 || K % 16) return TE_ERR_UNSUPPORTED;
   if (a_trans && M % 16) return TE_ERR_UNSUPPORTED;  // M is then a row length
+  // fp32 operands run as tf32, which the tensor cores take K-major only.
+  if (ab_dtype == TE_F32 && (a_trans || !b_trans)) return TE_ERR_UNSUPPORTED;
   if (!aligned16(A) || !aligned16(B) || !aligned16(D) || !opt_aligned16(bias) ||
       !aligned4(a_scale_inv) || !aligned4(b_scale_inv))
     return TE_ERR_UNSUPPORTED;
@@ -358,17 +366,23 @@ te_status te_layernorm_dense_fwd(const void* x, const void* kernel, te_dtype ker
                            quant ? &qset->x : nullptr, ln, ln_dtype, mu, rsigma, s);
   if (st != TE_OK) return st;
   const void* kop = kernel;
+  int b_kmajor = 0;
   if (quant && kernel_dtype != TE_E4M3) {
     st = quantize_into(kernel, dtype, H * N, &qset->kernel1, L.kq1, s);
     if (st != TE_OK) return st;
     kop = L.kq1;
+  } else if (!quant && dtype == TE_F32) {
+    st = launch_transpose_f32(static_cast<const float*>(kernel), H, N, static_cast<float*>(L.kt1), s);
+    if (st != TE_OK) return st;
+    kop = L.kt1;
+    b_kmajor = 1;
   }
   GemmArgs g;
   g.A = ln;
   g.B = kop;
   g.ab_dtype = quant ? TE_E4M3 : dtype;
   g.a_kmajor = 1;
-  g.b_kmajor = 0;
+  g.b_kmajor = b_kmajor;
   g.M = M;
   g.N = N;
   g.K = H;
@@ -426,6 +440,7 @@ te_status te_layernorm_mlp_fwd(const void* x, const void* gamma, const void* bet
   if (st != TE_OK) return st;
   const void* w1 = kernel1;
   const void* w2 = kernel2;
+  int b_kmajor = 0;
   if (quant && kernel_dtype != TE_E4M3) {
     st = quantize_into(kernel1, dtype, H * F1, &qset->kernel1, L.kq1, s);
     if (st != TE_OK) return st;
@@ -433,6 +448,14 @@ te_status te_layernorm_mlp_fwd(const void* x, const void* gamma, const void* bet
     if (st != TE_OK) return st;
     w1 = L.kq1;
     w2 = L.kq2;
+  } else if (!quant && dtype == TE_F32) {
+    st = launch_transpose_f32(static_cast<const float*>(kernel1), H, F1, static_cast<float*>(L.kt1), s);
+    if (st != TE_OK) return st;
+    st = launch_transpose_f32(static_cast<const float*>(kernel2), F, H, static_cast<float*>(L.kt2), s);
+    if (st != TE_OK) return st;
+    w1 = L.kt1;
+    w2 = L.kt2;
+    b_kmajor = 1;
   }
   // (2)+(3) GEMM1 + bias1 -> round -> activation [-> amax, E4M3], one kernel
   GemmArgs g1;
@@ -440,7 +463,7 @@ te_status te_layernorm_mlp_fwd(const void* x, const void* gamma, const void* bet
   g1.B = w1;
   g1.ab_dtype = quant ? TE_E4M3 : dtype;
   g1.a_kmajor = 1;
-  g1.b_kmajor = 0;
+  g1.b_kmajor = b_kmajor;
   g1.M = M;
   g1.N = F1;
   g1.K = H;
@@ -492,7 +515,7 @@ te_status te_layernorm_mlp_fwd(const void* x, const void* gamma, const void* bet
   g2.B = w2;
   g2.ab_dtype = quant ? TE_E4M3 : dtype;
   g2.a_kmajor = 1;
-  g2.b_kmajor = 0;
+  g2.b_kmajor = b_kmajor;
   g2.M = M;
   g2.N = H;
   g2.K = F;

@@ -49,17 +49,40 @@ __device__ __forceinline__ float2 unpack_e4m3x2(uint16_t v) {
 }
 
 // ------------------------------------------------------------------ activations -----------
-// Written from their definitions; fp32 throughout.
+// Written from their definitions, in fp32.  The tanh-form GELU uses the identity
+// 0.5 * (1 + tanh(u)) = 1 / (1 + exp(-2u)), which is the same function but avoids the
+// cancellation of 1 + tanh(u) for negative u; likewise 1 - tanh(u)^2 = 4 s(2u) s(-2u) with
+// s the logistic function, and 1 - s(z) = exp(-z) s(z).
+
+constexpr float kGeluK0 = 0.7978845608028654f;  // sqrt(2 / pi)
+constexpr float kGeluK1 = 0.044715f;
+
+__device__ __forceinline__ float gelu_u(float h) { return kGeluK0 * (h + kGeluK1 * h * h * h); }
 
 __device__ __forceinline__ float act_gelu(float h) {
-  const float k0 = 0.7978845608028654f;  // sqrt(2 / pi)
-  const float k1 = 0.044715f;
-  return 0.5f * h * (1.0f + tanhf(k0 * (h + k1 * h * h * h)));
+  return h / (1.0f + expf(-2.0f * gelu_u(h)));
 }
 
 __device__ __forceinline__ float act_silu(float z) { return z / (1.0f + expf(-z)); }
 
 __device__ __forceinline__ float act_relu(float h) { return h > 0.0f ? h : 0.0f; }
+
+// silu'(z) = s (1 + z (1 - s)), s = 1 / (1 + exp(-z)), with 1 - s = exp(-z) s.
+__device__ __forceinline__ float dsilu(float z) {
+  const float e = expf(-fmaxf(z, -80.0f));
+  const float s = 1.0f / (1.0f + e);
+  return s * (1.0f + z * (e * s));
+}
+
+// gelu'(h) = 0.5 (1 + t) + 0.5 h (1 - t^2) sqrt(2/pi) (1 + 3 * 0.044715 h^2), t = tanh(u),
+// evaluated as sp + 2 h sqrt(2/pi) (1 + 3 * 0.044715 h^2) sp sn with sp = s(2u), sn = s(-2u).
+__device__ __forceinline__ float dgelu(float h) {
+  const float u = gelu_u(h);
+  const float e = expf(-2.0f * fmaxf(u, -40.0f));
+  const float sp = 1.0f / (1.0f + e);
+  const float sn = e * sp;
+  return sp + 2.0f * h * kGeluK0 * (1.0f + 3.0f * kGeluK1 * h * h) * sp * sn;
+}
 
 // Non-gated activation by id (TE_IDENTITY, TE_RELU, TE_GELU, TE_SILU).
 __device__ __forceinline__ float act_apply(int act, float h) {
@@ -75,16 +98,8 @@ __device__ __forceinline__ float act_apply(int act, float h) {
 __device__ __forceinline__ float dact_apply(int act, float h) {
   switch (act) {
     case TE_RELU: return h > 0.0f ? 1.0f : 0.0f;
-    case TE_GELU: {
-      const float k0 = 0.7978845608028654f;
-      const float k1 = 0.044715f;
-      float t = tanhf(k0 * (h + k1 * h * h * h));
-      return 0.5f * (1.0f + t) + 0.5f * h * (1.0f - t * t) * k0 * (1.0f + 3.0f * k1 * h * h);
-    }
-    case TE_SILU: {
-      float s = 1.0f / (1.0f + expf(-h));
-      return s * (1.0f + h * (1.0f - s));
-    }
+    case TE_GELU: return dgelu(h);
+    case TE_SILU: return dsilu(h);
     default: return 1.0f;
   }
 }

@@ -117,9 +117,8 @@ __global__ void __launch_bounds__(kDactWarps * 32) dact_dbias_kernel(DactArgs a)
         V::load(a.x, r * a.N_in + n_out + col, l);
 #pragma unroll
         for (int e = 0; e < E; ++e) {
-          const float s = 1.0f / (1.0f + expf(-g[e]));
-          dg[e] = dy[e] * l[e] * (s * (1.0f + g[e] * (1.0f - s)));
-          dl[e] = dy[e] * (g[e] * s);
+          dg[e] = dy[e] * l[e] * dsilu(g[e]);
+          dl[e] = dy[e] * act_silu(g[e]);
           acc1[e] += dg[e];
           acc2[e] += dl[e];
           amax = fmaxf(amax, fmaxf(fabsf(dg[e]), fabsf(dl[e])));
@@ -188,9 +187,37 @@ te_status launch_dact_t(const DactArgs& a, cudaStream_t s) {
   return cudaGetLastError() == cudaSuccess ? TE_OK : TE_ERR_CUDA;
 }
 
+// ------------------------------------------------------------------ transpose -------------
+
+// dst[C, R] = src[R, C]^T through a 32 x 33 shared tile (coalesced on both sides).
+__global__ void __launch_bounds__(256) transpose_f32_kernel(const float* src, int64_t R, int64_t C,
+                                                            float* dst) {
+  __shared__ float tile[32][33];
+  const int64_t c0 = int64_t(blockIdx.x) * 32, r0 = int64_t(blockIdx.y) * 32;
+  for (int i = threadIdx.y; i < 32; i += 8) {
+    const int64_t r = r0 + i, c = c0 + threadIdx.x;
+    if (r < R && c < C) tile[i][threadIdx.x] = src[r * C + c];
+  }
+  __syncthreads();
+  for (int i = threadIdx.y; i < 32; i += 8) {
+    const int64_t c = c0 + i, r = r0 + threadIdx.x;
+    if (c < C && r < R) dst[c * R + r] = tile[threadIdx.x][i];
+  }
+}
+
 }  // namespace
 
+te_status launch_transpose_f32(const float* src, int64_t R, int64_t C, float* dst, cudaStream_t s) {
+  if (R == 0 || C == 0) return TE_OK;
+  if (ceil_div(R, 32) > 65535) return TE_ERR_UNSUPPORTED;
+  ProfileScope prof(TE_KERNEL_TRANSPOSE, s);
+  dim3 grid(unsigned(ceil_div(C, 32)), unsigned(ceil_div(R, 32)));
+  transpose_f32_kernel<<<grid, dim3(32, 8), 0, s>>>(src, R, C, dst);
+  return cudaGetLastError() == cudaSuccess ? TE_OK : TE_ERR_CUDA;
+}
+
 te_status launch_quantize(const QuantizeArgs& a, cudaStream_t s) {
+  ProfileScope prof(TE_KERNEL_QUANTIZE, s);
   if (a.x_dtype == TE_BF16) {
     quantize_kernel<__nv_bfloat16><<<ew_grid(a.n / 8), kEwThreads, 0, s>>>(a);
   } else if (a.x_dtype == TE_F32) {
@@ -202,6 +229,7 @@ te_status launch_quantize(const QuantizeArgs& a, cudaStream_t s) {
 }
 
 te_status launch_act_lu(const ActArgs& a, cudaStream_t s) {
+  ProfileScope prof(TE_KERNEL_ACT_LU, s);
   const int64_t n_out = a.act == TE_SWIGLU ? a.N_in / 2 : a.N_in;
   if (a.x_dtype == TE_BF16) {
     act_lu_kernel<__nv_bfloat16><<<ew_grid(a.M * n_out / 8), kEwThreads, 0, s>>>(a);
@@ -219,6 +247,7 @@ size_t dact_dbias_workspace(int64_t M, int64_t N_in) {
 
 te_status launch_dact_dbias(const DactArgs& a, cudaStream_t s) {
   if (a.M == 0) return TE_OK;
+  ProfileScope prof(TE_KERNEL_DACT_DBIAS, s);
   if (a.dtype == TE_BF16) return launch_dact_t<__nv_bfloat16>(a, s);
   if (a.dtype == TE_F32) return launch_dact_t<float>(a, s);
   return TE_ERR_UNSUPPORTED;

@@ -686,6 +686,7 @@ te_status launch_gemm(const GemmArgs& a, cudaStream_t s) {
   g.amax_out = a.cast.amax_out;
   const int64_t tiles = int64_t(g.num_m) * g.num_n;
   const int grid = int(tiles < num_sms() ? tiles : num_sms());
+  ProfileScope prof(a.epilogue == EPI_BIAS ? TE_KERNEL_GEMM : TE_KERNEL_GEMM_ACT, s);
   if (kind == 0) return launch_kind<0>(prm, grid, a.a_kmajor, a.b_kmajor, s);
   if (kind == 1) return launch_kind<1>(prm, grid, a.a_kmajor, a.b_kmajor, s);
   return launch_kind<2>(prm, grid, a.a_kmajor, a.b_kmajor, s);

@@ -88,6 +88,9 @@ struct QuantizeArgs {
 };
 te_status launch_quantize(const QuantizeArgs& a, cudaStream_t s);
 
+// dst[C, R] = transpose of src[R, C] (fp32): the tf32 tensor-core path takes K-major operands.
+te_status launch_transpose_f32(const float* src, int64_t R, int64_t C, float* dst, cudaStream_t s);
+
 // Tensor-core GEMM D[M, N] = epilogue(alpha * op(A) op(B)).
 enum Epilogue { EPI_BIAS = 0, EPI_BIAS_ACT = 1, EPI_BIAS_GATED = 2 };
 
@@ -116,5 +119,19 @@ int* device_status_ptr();
 te_status read_and_clear_device_status(int32_t* out);
 
 int num_sms();
+
+// Brackets one kernel launch with profiling events when te_profile_begin is active.
+class ProfileScope {
+ public:
+  ProfileScope(int kind, cudaStream_t stream);
+  ~ProfileScope();
+  ProfileScope(const ProfileScope&) = delete;
+  ProfileScope& operator=(const ProfileScope&) = delete;
+
+ private:
+  int kind_;
+  cudaStream_t stream_;
+  int slot_ = -1;
+};
 
 }  // namespace te

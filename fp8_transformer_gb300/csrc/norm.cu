@@ -258,6 +258,7 @@ te_status launch_bwd_dispatch(const NormBwdArgs& a, cudaStream_t s) {
 
 te_status launch_norm_fwd(const NormFwdArgs& a, cudaStream_t s) {
   if (a.M == 0) return TE_OK;
+  ProfileScope prof(TE_KERNEL_NORM_FWD, s);
   if (a.x_dtype == TE_BF16) return launch_fwd_dispatch<__nv_bfloat16>(a, s);
   if (a.x_dtype == TE_F32) return launch_fwd_dispatch<float>(a, s);
   return TE_ERR_UNSUPPORTED;
@@ -269,6 +270,7 @@ size_t norm_bwd_workspace(int64_t M, int64_t H) {
 
 te_status launch_norm_bwd(const NormBwdArgs& a, cudaStream_t s) {
   if (a.M == 0) return TE_OK;
+  ProfileScope prof(TE_KERNEL_NORM_BWD, s);
   if (a.dtype == TE_BF16) return launch_bwd_dispatch<__nv_bfloat16>(a, s);
   if (a.dtype == TE_F32) return launch_bwd_dispatch<float>(a, s);
   return TE_ERR_UNSUPPORTED;

@@ -255,6 +255,29 @@ te_status te_norm_bwd(const void* dz, const void* x, const float* mu, const floa
                       te_norm_type norm_type, int zero_centered_gamma, void* dx, float* dgamma,
                       float* dbeta, void* workspace, size_t ws_bytes, void* stream);
 
+/* ---------------------------------------------------------------------------------------
+ * Instrumentation (no counterpart on the pages; used by benchmarks).
+ * Between te_profile_begin and te_profile_end every kernel the library launches is bracketed
+ * by CUDA events recorded on the launching stream.  te_profile_end synchronizes those events
+ * and returns, per kernel kind, the summed device time (ms) and the number of launches.
+ * Arrays have TE_KERNEL_KINDS entries (either may be NULL).  At most `max_records` launches
+ * are timed (later ones are only counted).  Not thread-safe against concurrent calls.
+ */
+typedef enum {
+  TE_KERNEL_NORM_FWD = 0,
+  TE_KERNEL_QUANTIZE = 1,
+  TE_KERNEL_ACT_LU = 2,
+  TE_KERNEL_DACT_DBIAS = 3,
+  TE_KERNEL_GEMM = 4,        /* GEMM + bias epilogue */
+  TE_KERNEL_GEMM_ACT = 5,    /* GEMM + bias + activation (+ amax, E4M3) epilogue */
+  TE_KERNEL_NORM_BWD = 6,
+  TE_KERNEL_TRANSPOSE = 7,
+  TE_KERNEL_KINDS = 8
+} te_kernel_kind;
+
+te_status te_profile_begin(int32_t max_records);
+te_status te_profile_end(float* total_ms, int32_t* launches);
+
 #ifdef __cplusplus
 }
 #endif

@@ -141,19 +141,3 @@ def quantize(v32, scale) -> np.ndarray:
 def dequantize(codes, scale_inv) -> np.ndarray:
     """fp32(decode(code) * scale_inv), as float64."""
     return to_f32(e4m3_decode(codes).astype(np.float32) * np.float32(scale_inv))
-
-
-def e4m3_midpoint_distance(v32, scale) -> np.ndarray:
-    """Relative distance of fp32(v * scale) from the nearest E4M3 rounding boundary.
-
-    A GPU code that differs from the oracle's by one step is only acceptable where the
-    pre-cast value sits this close to a boundary that fp32 rounding-order differences can
-    move it across.  Boundaries are the midpoints between adjacent finite E4M3 values.
-    """
-    y = np.abs(np.asarray(v32, dtype=np.float32) * np.float32(scale)).astype(np.float64)
-    y = np.minimum(y, E4M3_MAX)
-    grid = np.unique(np.abs(e4m3_decode(np.arange(0, 0x7F))))
-    mids = (grid[:-1] + grid[1:]) / 2.0
-    idx = np.clip(np.searchsorted(mids, y), 1, len(mids) - 1)
-    d = np.minimum(np.abs(y - mids[idx - 1]), np.abs(y - mids[idx]))
-    return d / np.maximum(y, 2.0 ** -9)

@@ -72,7 +72,8 @@ def check_mlp(inp, got, ref, fp8, rows=None):
     # normalized operand
     if fp8:
         assert_e4m3_codes(codes(got["ln"])[sel], ln_ref.codes, pre32=ln_ref.pre,
-                          scale=ln_ref.scale, what="ln e4m3")
+                          scale=ln_ref.scale, rel=1e-5, abs_tol=1e-5 * rms(ln_ref.pre),
+                          what="ln e4m3")
     else:
         np.testing.assert_allclose(np64(got["ln"])[sel], ln_ref.value, rtol=2e-2,
                                    atol=1e-3 * rms(ln_ref.value))
@@ -150,7 +151,7 @@ def test_ln_dense_small(fp8):
                                  fp8={k: np.float32(v) for k, v in scales.items()} if fp8 else None)
     if fp8:
         assert_e4m3_codes(ln, ref["ln"].codes, pre32=ref["ln"].pre, scale=ref["ln"].scale,
-                          what="ln e4m3")
+                          rel=1e-5, abs_tol=1e-5 * rms(ref["ln"].pre), what="ln e4m3")
     a = ref["ln"].value * ref["ln"].inv()
     w = ref["kernel"].value * ref["kernel"].inv()
     assert_gemm_close(out, ref["out"].value, H, rms(a), rms(w), what="ln-dense out")

@@ -161,9 +161,3 @@ def test_quantize_dequantize_error_bound():
     big = np.abs(v) * s >= 2.0 ** -6
     rel = np.abs(back[big] - v[big]) / np.abs(v[big])
     assert rel.max() <= 2.0 ** -4 * (1 + 1e-6)
-
-
-def test_midpoint_distance_zero_on_ties():
-    s = np.float32(1.0)
-    assert nx.e4m3_midpoint_distance(np.array([1.0625], np.float32), s)[0] == 0.0
-    assert nx.e4m3_midpoint_distance(np.array([1.0], np.float32), s)[0] >= 0.03

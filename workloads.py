@@ -33,15 +33,15 @@ import torch
 
 WORKLOADS = {
     "tiny_ln_mlp": dict(M=64, H=128, F=512, norm="layernorm", act="gelu", eps=1e-6,
-                        dtype="f32", gated=False, bias=True, zero_centered_gamma=False),
+                        dtype="f32", gated=False, has_bias=True, zero_centered_gamma=False),
     "qkv_ln_dense": dict(M=16384, H=8192, N=24576, norm="layernorm", eps=1e-5,
-                         dtype="bf16", bias=True, zero_centered_gamma=False),
+                         dtype="bf16", has_bias=True, zero_centered_gamma=False),
     "gpt_ln_mlp": dict(M=16384, H=4096, F=16384, norm="layernorm", act="gelu", eps=1e-6,
-                       dtype="bf16", gated=False, bias=True, zero_centered_gamma=False),
+                       dtype="bf16", gated=False, has_bias=True, zero_centered_gamma=False),
     "llama_rms_mlp": dict(M=8192, H=4096, F=14336, norm="rmsnorm", act="swiglu", eps=1e-6,
-                          dtype="bf16", gated=True, bias=False, zero_centered_gamma=True),
+                          dtype="bf16", gated=True, has_bias=False, zero_centered_gamma=True),
     "gpt_ln_mlp_bwd": dict(M=16384, H=4096, F=16384, norm="layernorm", act="gelu", eps=1e-6,
-                           dtype="bf16", gated=False, bias=True, zero_centered_gamma=False),
+                           dtype="bf16", gated=False, has_bias=True, zero_centered_gamma=False),
 }
 
 _TORCH_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16}
