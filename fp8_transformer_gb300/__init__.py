@@ -6,7 +6,7 @@ quantize and dact+dbias kernels) behind the C ABI of include/te_gb300.h.  This p
 thin Python binding; the functions keep the C names.
 """
 
-from .binding import (ACT_TUPLES, ACT_TYPES, EXPORTED, KERNEL_KINDS, profile_begin, profile_end, NORM_TYPES, Quantizer, QuantizerSet,
+from .binding import (dact_dbias_noalloc_capacity, te_dact_dbias_quantize_noalloc, ACT_TUPLES, ACT_TYPES, EXPORTED, KERNEL_KINDS, profile_begin, profile_end, NORM_TYPES, Quantizer, QuantizerSet,
                       TEError, get_device_status, lib, lib_path, status_string, te_act_lu,
                       te_dact_dbias_quantize, te_gemm, te_layernorm_dense_fwd,
                       te_layernorm_mlp_fwd, te_norm_bwd, te_norm_fwd, te_quantize, version,
@@ -17,4 +17,5 @@ __all__ = ["Quantizer", "QuantizerSet", "TEError", "te_norm_fwd", "te_act_lu",
            "te_dact_dbias_quantize", "te_quantize", "te_gemm", "te_layernorm_dense_fwd",
            "te_layernorm_mlp_fwd", "te_norm_bwd", "lib", "lib_path", "version",
            "get_device_status", "status_string", "workspace_size", "EXPORTED", "ACT_TYPES",
-           "ACT_TUPLES", "NORM_TYPES", "KERNEL_KINDS", "profile_begin", "profile_end"]
+           "ACT_TUPLES", "NORM_TYPES", "KERNEL_KINDS", "profile_begin", "profile_end",
+           "te_dact_dbias_quantize_noalloc", "dact_dbias_noalloc_capacity"]

@@ -15,7 +15,8 @@ import torch
 
 from . import build as _build
 
-TE_OK, TE_ERR_INVALID_ARG, TE_ERR_UNSUPPORTED, TE_ERR_CUDA, TE_ERR_TIMEOUT, TE_ERR_WORKSPACE = range(6)
+(TE_OK, TE_ERR_INVALID_ARG, TE_ERR_UNSUPPORTED, TE_ERR_CUDA, TE_ERR_TIMEOUT, TE_ERR_WORKSPACE,
+ TE_ERR_TOO_LARGE) = range(7)
 TE_F32, TE_BF16, TE_E4M3 = 0, 1, 2
 TE_LAYERNORM, TE_RMSNORM = 0, 1
 TE_IDENTITY, TE_RELU, TE_GELU, TE_SILU, TE_SWIGLU = range(5)
@@ -36,7 +37,8 @@ _DTYPE = {torch.float32: TE_F32, torch.bfloat16: TE_BF16, torch.uint8: TE_E4M3,
 EXPORTED = ["te_status_string", "te_version", "te_get_device_status", "te_workspace_size",
             "te_norm_fwd", "te_act_lu", "te_dact_dbias_quantize", "te_quantize", "te_gemm",
             "te_layernorm_dense_fwd", "te_layernorm_mlp_fwd", "te_norm_bwd",
-            "te_profile_begin", "te_profile_end"]
+            "te_profile_begin", "te_profile_end", "te_dact_dbias_quantize_noalloc",
+            "te_dact_dbias_noalloc_capacity"]
 KERNEL_KINDS = ["norm_fwd", "quantize", "act_lu", "dact_dbias", "gemm", "gemm_act", "norm_bwd",
                 "transpose"]
 
@@ -90,6 +92,10 @@ _SIGS = {
     "te_norm_bwd": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, ctypes.c_int, _i64, _i64,
                                    ctypes.c_int, ctypes.c_int, _vp, _vp, _vp, _vp, _sz, _vp]),
     "te_profile_begin": (ctypes.c_int, [ctypes.c_int32]),
+    "te_dact_dbias_quantize_noalloc": (ctypes.c_int, [_vp, _vp, ctypes.c_int, _i64, _i64,
+                                                      ctypes.c_int, _QP, _vp, ctypes.c_int, _vp,
+                                                      _vp]),
+    "te_dact_dbias_noalloc_capacity": (_sz, []),
     "te_profile_end": (ctypes.c_int, [ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_int32)]),
 }
 
@@ -333,3 +339,19 @@ def profile_end() -> dict:
     cnt = (ctypes.c_int32 * n)()
     _check("te_profile_end", lib().te_profile_end(ms, cnt))
     return {k: (float(ms[i]), int(cnt[i])) for i, k in enumerate(KERNEL_KINDS)}
+
+
+def te_dact_dbias_quantize_noalloc(dy, x_preact, act, dx, dbias=None, q=None, stream=None):
+    """te_dact_dbias_quantize without a workspace: the bias reduction uses the library's fixed
+    device scratch (see include/te_gb300.h for its capacity and sharing rules)."""
+    M, N_in = dx.shape
+    st = lib().te_dact_dbias_quantize_noalloc(_ptr(dy), _ptr(x_preact), _dt(dy), M, N_in,
+                                              _act_id(act), _qp(q), _ptr(dx), _dt(dx),
+                                              _ptr(dbias), _stream(stream))
+    _check("te_dact_dbias_quantize_noalloc", st)
+    return dx
+
+
+def dact_dbias_noalloc_capacity() -> int:
+    """Floats of fixed device scratch behind te_dact_dbias_quantize_noalloc."""
+    return int(lib().te_dact_dbias_noalloc_capacity())

@@ -180,6 +180,8 @@ const char* te_status_string(te_status status) {
     case TE_ERR_CUDA: return "TE_ERR_CUDA: CUDA runtime error";
     case TE_ERR_TIMEOUT: return "TE_ERR_TIMEOUT: a device pipeline wait timed out";
     case TE_ERR_WORKSPACE: return "TE_ERR_WORKSPACE: workspace missing or too small";
+    case TE_ERR_TOO_LARGE:
+      return "TE_ERR_TOO_LARGE: problem exceeds the fixed scratch of the no-allocation entry point";
   }
   return "unknown te_status";
 }

@@ -41,7 +41,8 @@ typedef enum {
   TE_ERR_UNSUPPORTED = 2,  /* alignment or shape this build does not handle */
   TE_ERR_CUDA = 3,         /* a CUDA runtime call or kernel launch failed */
   TE_ERR_TIMEOUT = 4,      /* a device pipeline wait gave up (device status word only) */
-  TE_ERR_WORKSPACE = 5     /* workspace missing or smaller than te_workspace_size() */
+  TE_ERR_WORKSPACE = 5,    /* workspace missing or smaller than te_workspace_size() */
+  TE_ERR_TOO_LARGE = 6     /* problem exceeds the fixed scratch of te_dact_dbias_quantize_noalloc */
 } te_status;
 
 typedef enum { TE_F32 = 0, TE_BF16 = 1, TE_E4M3 = 2 } te_dtype;
@@ -277,6 +278,34 @@ typedef enum {
 
 te_status te_profile_begin(int32_t max_records);
 te_status te_profile_end(float* total_ms, int32_t* launches);
+
+/* ---------------------------------------------------------------------------------------
+ * te_dact_dbias_quantize_noalloc -- te_dact_dbias_quantize for callers that cannot allocate
+ * device memory at the call (no counterpart on the pages; an addition of this library).
+ *
+ * Who needs it: plugin hosts and runtimes that plan every device buffer ahead of time and give
+ * an operator no allocator, and latency-critical code that cannot afford cudaMalloc's
+ * device-wide synchronization.  Such callers cannot provide the workspace that
+ * te_dact_dbias_quantize's bias reduction needs.
+ *
+ * Same arguments, results and rules as te_dact_dbias_quantize, without workspace/ws_bytes.  The
+ * call allocates nothing: the bias reduction's partial sums live in one fixed device array of
+ * te_dact_dbias_noalloc_capacity() floats (8 MiB) that every GPU loading the library holds
+ * until the process exits.
+ *   - A reduction needing more than the capacity (ceil(M / 128) * N_in floats, counted only when
+ *     dbias is requested) returns TE_ERR_TOO_LARGE before launching.
+ *   - The first call on a device looks up the array's device address once for that device;
+ *     make that first call before any stream capture begins on the device.
+ *   - All calls on a device share the array: calls that overlap on the GPU race on it (order
+ *     them on one stream).  Nothing in it must start at zero; it keeps the last call's data.
+ */
+te_status te_dact_dbias_quantize_noalloc(const void* dy, const void* x_preact, te_dtype dtype,
+                                         int64_t M, int64_t N_in, te_act_type act,
+                                         const te_quantizer* q, void* dx, te_dtype dx_dtype,
+                                         float* dbias, void* stream);
+
+/* Floats of fixed scratch behind te_dact_dbias_quantize_noalloc. */
+size_t te_dact_dbias_noalloc_capacity(void);
 
 #ifdef __cplusplus
 }
