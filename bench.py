@@ -307,6 +307,78 @@ def run_ours(args, rank, world, local_rank):
     dact_bytes = Md * Nd * (2 + 2 + 1) + Nd * 4
     dact_step()
     ms_dact = max_over_ranks(statistics.mean(time_steps(dact_step, args.steps, flush)))
+    del dyd, hd, dxd, wsd
+    barrier()
+
+    # ---- the other workloads' hot paths: LN -> Dense (QKV) forward and the GPT MLP backward
+    extra = {}
+    dense = make_inputs("qkv_ln_dense", device=dev, seed=rank)
+    Mq, Hq, Nq = dense["M"], dense["H"], dense["N"]
+    qout = torch.empty(Mq, Nq, dtype=torch.bfloat16, device=dev)
+    qk_q = te.Quantizer(1.0, "current", dev)
+    kq = torch.empty(Hq, Nq, dtype=torch.uint8, device=dev)
+    te.te_quantize(dense["kernel"], qk_q, kq)
+    qx_d = te.Quantizer(1.0, "current", dev)
+    qs_d = te.QuantizerSet(x=qx_d, kernel1=qk_q)
+    dkw = dict(epsilon=dense["eps"])
+    te.te_layernorm_dense_fwd(dense["x"], kq, dense["gamma"], dense["beta"], dense["bias"], qout,
+                              quantizer_set=qs_d, **dkw)
+    torch.cuda.synchronize()
+    qx_d.mode = te.binding.TE_SCALING_DELAYED
+    dflops = 2.0 * Mq * Hq * Nq
+    for tag, fn in (("bf16", lambda: te.te_layernorm_dense_fwd(
+                        dense["x"], dense["kernel"], dense["gamma"], dense["beta"], dense["bias"],
+                        qout, **dkw)),
+                    ("fp8", lambda: te.te_layernorm_dense_fwd(
+                        dense["x"], kq, dense["gamma"], dense["beta"], dense["bias"], qout,
+                        quantizer_set=qs_d, **dkw))):
+        fn()
+        ms = max_over_ranks(statistics.mean(time_steps(fn, max(3, args.steps // 2), flush)))
+        extra[f"ln_dense_{tag}"] = {"TFLOP/s": dflops / (ms / 1e3) / 1e12, "ms": ms,
+                                    "workload": "qkv_ln_dense M=16384 H=8192 N=24576"}
+    del dense, qout, kq
+    bw = make_inputs("gpt_ln_mlp_bwd", device=dev, seed=rank)
+    Mb, Hb, Fb = bw["M"], bw["H"], bw["F"]
+    bt = {k: torch.empty(*sh, dtype=dt, device=dev) for k, sh, dt in (
+        ("out", (Mb, Hb), torch.bfloat16), ("h", (Mb, Fb), torch.bfloat16),
+        ("ln", (Mb, Hb), torch.uint8), ("lnb", (Mb, Hb), torch.bfloat16),
+        ("mu", (Mb,), torch.float32), ("rs", (Mb,), torch.float32),
+        ("dx", (Mb, Hb), torch.bfloat16), ("dg", (Hb,), torch.float32),
+        ("db", (Hb,), torch.float32), ("dw1", (Hb, Fb), torch.bfloat16),
+        ("dw2", (Fb, Hb), torch.bfloat16), ("db1", (Fb,), torch.float32),
+        ("db2", (Hb,), torch.float32))}
+    qs_b = te.QuantizerSet(x=te.Quantizer(1.0, "current", dev),
+                           kernel1=te.Quantizer(1.0, "current", dev),
+                           act=te.Quantizer(1.0, "current", dev),
+                           kernel2=te.Quantizer(1.0, "current", dev),
+                           grad=te.Quantizer(1.0, "current", dev))
+    bkw = dict(norm_type="layernorm", activation_type="gelu")
+    te.te_layernorm_mlp_fwd(bw["x"], bw["gamma"], bw["beta"], bw["w1"], bw["w2"], bw["b1"],
+                            bw["b2"], bt["out"], quantizer_set=qs_b, saved_h=bt["h"],
+                            saved_ln_out=bt["ln"], mu=bt["mu"], rsigma=bt["rs"], **bkw)
+    te.te_layernorm_mlp_fwd(bw["x"], bw["gamma"], bw["beta"], bw["w1"], bw["w2"], bw["b1"],
+                            bw["b2"], bt["out"], saved_ln_out=bt["lnb"], **bkw)
+    torch.cuda.synchronize()
+    bflops = 4 * 2.0 * Mb * Hb * Fb
+
+    def bwd(fp8):
+        te.te_layernorm_mlp_bwd(bw["dy"], bw["x"], bw["gamma"], bw["w1"], bw["w2"], bt["h"],
+                                bt["ln"] if fp8 else bt["lnb"], bt["mu"], bt["rs"], bt["dx"],
+                                bt["dg"], bt["dw1"], bt["dw2"], dbeta=bt["db"], dbias1=bt["db1"],
+                                dbias2=bt["db2"], quantizer_set=qs_b if fp8 else None, **bkw)
+
+    for tag, fp8 in (("bf16", False), ("fp8", True)):
+        bwd(fp8)
+        torch.cuda.synchronize()
+        te.profile_begin(64 * args.steps)
+        ms = max_over_ranks(statistics.mean(time_steps(lambda: bwd(fp8), max(3, args.steps // 2),
+                                                       flush)))
+        prof = te.profile_end()
+        extra[f"mlp_bwd_{tag}"] = {"TFLOP/s": bflops / (ms / 1e3) / 1e12, "ms": ms,
+                                   "workload": "gpt_ln_mlp_bwd M=16384 H=4096 F=16384 gelu",
+                                   "kernel_ms": {k: round(v[0] / max(v[1], 1), 4)
+                                                 for k, v in prof.items() if v[1]}}
+    del bw, bt
     barrier()
 
     if rank != 0:
@@ -341,6 +413,7 @@ def run_ours(args, rank, world, local_rank):
             "dact_dbias_quantize": {"shape": [Md, Nd], "GB/s": dact_bytes / (ms_dact / 1e3) / 1e9,
                                     "frac": dact_bytes / (ms_dact / 1e3) / 1e9 / peaks["hbm"],
                                     "ms": ms_dact, "bytes": dact_bytes}},
+        "other_workloads": extra,
         "clocks": clocks,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": x.numel() * 2,
                 "d2h_bytes_per_step": out.numel() * 2, "ms_per_step": ms_e2e},

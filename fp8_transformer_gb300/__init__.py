@@ -9,13 +9,13 @@ thin Python binding; the functions keep the C names.
 from .binding import (dact_dbias_noalloc_capacity, te_dact_dbias_quantize_noalloc, ACT_TUPLES, ACT_TYPES, EXPORTED, KERNEL_KINDS, profile_begin, profile_end, NORM_TYPES, Quantizer, QuantizerSet,
                       TEError, get_device_status, lib, lib_path, status_string, te_act_lu,
                       te_dact_dbias_quantize, te_gemm, te_layernorm_dense_fwd,
-                      te_layernorm_mlp_fwd, te_norm_bwd, te_norm_fwd, te_quantize, version,
+                      te_layernorm_mlp_fwd, te_layernorm_mlp_bwd, te_norm_bwd, te_norm_fwd, te_quantize, version,
                       workspace_size)
 from .binding import *  # noqa: F401,F403  (enum constants)
 
 __all__ = ["Quantizer", "QuantizerSet", "TEError", "te_norm_fwd", "te_act_lu",
            "te_dact_dbias_quantize", "te_quantize", "te_gemm", "te_layernorm_dense_fwd",
-           "te_layernorm_mlp_fwd", "te_norm_bwd", "lib", "lib_path", "version",
+           "te_layernorm_mlp_fwd", "te_layernorm_mlp_bwd", "te_norm_bwd", "lib", "lib_path", "version",
            "get_device_status", "status_string", "workspace_size", "EXPORTED", "ACT_TYPES",
            "ACT_TUPLES", "NORM_TYPES", "KERNEL_KINDS", "profile_begin", "profile_end",
            "te_dact_dbias_quantize_noalloc", "dact_dbias_noalloc_capacity"]

@@ -37,7 +37,8 @@ _DTYPE = {torch.float32: TE_F32, torch.bfloat16: TE_BF16, torch.uint8: TE_E4M3,
 EXPORTED = ["te_status_string", "te_version", "te_get_device_status", "te_workspace_size",
             "te_norm_fwd", "te_act_lu", "te_dact_dbias_quantize", "te_quantize", "te_gemm",
             "te_layernorm_dense_fwd", "te_layernorm_mlp_fwd", "te_norm_bwd",
-            "te_profile_begin", "te_profile_end", "te_dact_dbias_quantize_noalloc",
+            "te_profile_begin", "te_profile_end", "te_layernorm_mlp_bwd",
+            "te_dact_dbias_quantize_noalloc",
             "te_dact_dbias_noalloc_capacity"]
 KERNEL_KINDS = ["norm_fwd", "quantize", "act_lu", "dact_dbias", "gemm", "gemm_act", "norm_bwd",
                 "transpose"]
@@ -92,6 +93,10 @@ _SIGS = {
     "te_norm_bwd": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, ctypes.c_int, _i64, _i64,
                                    ctypes.c_int, ctypes.c_int, _vp, _vp, _vp, _vp, _sz, _vp]),
     "te_profile_begin": (ctypes.c_int, [ctypes.c_int32]),
+    "te_layernorm_mlp_bwd": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, ctypes.c_int, _vp, _vp, _vp,
+                                            _vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, _QSP,
+                                            _i64, _i64, _i64, ctypes.c_int, _vp, _vp, _vp, _vp,
+                                            _vp, _vp, _vp, _vp, _sz, _vp]),
     "te_dact_dbias_quantize_noalloc": (ctypes.c_int, [_vp, _vp, ctypes.c_int, _i64, _i64,
                                                       ctypes.c_int, _QP, _vp, ctypes.c_int, _vp,
                                                       _vp]),
@@ -312,6 +317,31 @@ def te_layernorm_mlp_fwd(x, gamma, beta, kernel1, kernel2, bias1, bias2, out,
                                     _stream(stream))
     _check("te_layernorm_mlp_fwd", st)
     return out
+
+
+def te_layernorm_mlp_bwd(dy, x, gamma, kernel1, kernel2, saved_h, saved_ln_out, mu, rsigma,
+                         dx, dgamma, dkernel1, dkernel2, dbeta=None, dbias1=None, dbias2=None,
+                         norm_type="layernorm", zero_centered_gamma=False,
+                         activation_type=("relu",), quantizer_set=None, workspace=None,
+                         stream=None):
+    M, H = x.shape
+    F = kernel2.shape[0]
+    act = _act_id(activation_type)
+    dt = _dt(x)
+    kd = _dt(kernel1)
+    if workspace is None:
+        workspace = _ws(workspace_size(TE_OP_LAYERNORM_MLP_BWD, M, H, F, dt,
+                                       quantizer_set is not None, kd, act), x.device)
+    qs = quantizer_set.c() if quantizer_set is not None else None
+    st = lib().te_layernorm_mlp_bwd(_ptr(dy), _ptr(x), _ptr(gamma), _ptr(kernel1), _ptr(kernel2),
+                                    kd, _ptr(saved_h), _ptr(saved_ln_out), _ptr(mu), _ptr(rsigma),
+                                    _norm_id(norm_type), int(bool(zero_centered_gamma)), act,
+                                    ctypes.byref(qs) if qs is not None else None, M, H, F, dt,
+                                    _ptr(dx), _ptr(dgamma), _ptr(dbeta), _ptr(dkernel1),
+                                    _ptr(dkernel2), _ptr(dbias1), _ptr(dbias2), _ptr(workspace),
+                                    workspace.numel(), _stream(stream))
+    _check("te_layernorm_mlp_bwd", st)
+    return dx
 
 
 def te_norm_bwd(dz, x, mu, rsigma, gamma, norm_type, zero_centered_gamma, dx, dgamma,

@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <utility>
 
 #include "kernels.h"
 #include "te_gb300.h"
@@ -93,7 +94,7 @@ struct FwdLayout {
   void* kq1 = nullptr;    // E4M3 copy of kernel1 / the dense kernel
   void* kq2 = nullptr;    // E4M3 copy of kernel2
   void* a2 = nullptr;     // activation output, GEMM2 operand
-  void* a2_hi = nullptr;  // activation output before current-scaling quantization
+  void* a2_hi = nullptr;  // fp32 activation output awaiting its current-scaling cast
   size_t bytes = 0;
 };
 
@@ -116,7 +117,7 @@ FwdLayout mlp_layout(void* ws, int64_t M, int64_t H, int64_t F, int dtype, bool 
   if (!have_saved_ln) L.ln = c.take(size_t(M) * H * (quant ? 1 : esize(dtype)));
   L.a2 = c.take(size_t(M) * F * (quant ? 1 : esize(dtype)));
   if (quant) {
-    L.a2_hi = c.take(size_t(M) * F * esize(dtype));
+    L.a2_hi = c.take(size_t(M) * F * 4);  // fp32: cast once, from the fp32 activation
     if (kernel_dtype != TE_E4M3) {
       L.kq1 = c.take(size_t(H) * F1);
       L.kq2 = c.take(size_t(F) * H);
@@ -125,6 +126,36 @@ FwdLayout mlp_layout(void* ws, int64_t M, int64_t H, int64_t F, int dtype, bool 
     L.kt1 = c.take(size_t(H) * F1 * 4);
     L.kt2 = c.take(size_t(F) * H * 4);
   }
+  L.bytes = c.used;
+  return L;
+}
+
+// Workspace of te_layernorm_mlp_bwd.  The three reductions run one after another on the
+// stream, so they share one partial-sum region.
+struct BwdLayout {
+  void* partials = nullptr;
+  void* a = nullptr;     // recomputed activation [M, F], dtype
+  void* da = nullptr;    // [M, F], dtype
+  void* dh = nullptr;    // [M, F'], E4M3 or dtype
+  void* dln = nullptr;   // [M, H], dtype
+  void* kq1 = nullptr;   // E4M3 kernel1 when quantized here
+  size_t bytes = 0;
+};
+
+BwdLayout bwd_layout(void* ws, int64_t M, int64_t H, int64_t F, int dtype, bool quant,
+                     int kernel_dtype, int act) {
+  Carver c(ws);
+  BwdLayout L;
+  const int64_t F1 = act == TE_SWIGLU ? 2 * F : F;
+  size_t part = dact_dbias_workspace(M, H);
+  if (dact_dbias_workspace(M, F1) > part) part = dact_dbias_workspace(M, F1);
+  if (norm_bwd_workspace(M, H) > part) part = norm_bwd_workspace(M, H);
+  L.partials = c.take(part);
+  L.a = c.take(size_t(M) * F * esize(dtype));
+  L.da = c.take(size_t(M) * F * esize(dtype));
+  L.dh = c.take(size_t(M) * F1 * (quant ? 1 : esize(dtype)));
+  L.dln = c.take(size_t(M) * H * esize(dtype));
+  if (quant && kernel_dtype != TE_E4M3) L.kq1 = c.take(size_t(H) * F1);
   L.bytes = c.used;
   return L;
 }
@@ -201,6 +232,8 @@ size_t te_workspace_size(te_op op, int64_t M, int64_t H, int64_t F_or_N, te_dtyp
       return dense_layout(nullptr, M, H, F_or_N, dtype, quantized != 0, kernel_dtype, false).bytes;
     case TE_OP_LAYERNORM_MLP_FWD:
       return mlp_layout(nullptr, M, H, F_or_N, dtype, quantized != 0, kernel_dtype, act, false).bytes;
+    case TE_OP_LAYERNORM_MLP_BWD:
+      return bwd_layout(nullptr, M, H, F_or_N, dtype, quantized != 0, kernel_dtype, act).bytes;
     default: return 0;
   }
 }
@@ -484,7 +517,7 @@ te_status te_layernorm_mlp_fwd(const void* x, const void* gamma, const void* bet
     g1.cast.amax_out = qset->act.amax;
     if (act_current) {
       g1.D = L.a2_hi;
-      g1.cast.out_dtype = dtype;
+      g1.cast.out_dtype = TE_F32;
     } else {
       g1.D = L.a2;
       g1.cast.out_dtype = TE_E4M3;
@@ -501,7 +534,7 @@ te_status te_layernorm_mlp_fwd(const void* x, const void* gamma, const void* bet
     // The amax is already known from GEMM1's epilogue: one cast pass.
     QuantizeArgs qa;
     qa.x = L.a2_hi;
-    qa.x_dtype = dtype;
+    qa.x_dtype = TE_F32;
     qa.n = M * F;
     qa.out = L.a2;
     qa.cast.out_dtype = TE_E4M3;
@@ -529,6 +562,195 @@ te_status te_layernorm_mlp_fwd(const void* x, const void* gamma, const void* bet
   g2.D = out;
   g2.cast.out_dtype = dtype;
   return launch_gemm(g2, s);
+}
+
+te_status te_layernorm_mlp_bwd(const void* dy, const void* x, const void* gamma,
+                               const void* kernel1, const void* kernel2, te_dtype kernel_dtype,
+                               const void* saved_h, const void* saved_ln_out, const float* mu,
+                               const float* rsigma, te_norm_type norm_type,
+                               int zero_centered_gamma, te_act_type act,
+                               const te_quantizer_set* qset, int64_t M, int64_t H, int64_t F,
+                               te_dtype dtype, void* dx, float* dgamma, float* dbeta,
+                               void* dkernel1, void* dkernel2, float* dbias1, float* dbias2,
+                               void* workspace, size_t ws_bytes, void* stream) {
+  if (M < 0 || H <= 0 || F <= 0 || dtype != TE_BF16 || act == TE_IDENTITY || !valid_act(act) ||
+      (norm_type != TE_LAYERNORM && norm_type != TE_RMSNORM))
+    return dtype == TE_F32 ? TE_ERR_UNSUPPORTED : TE_ERR_INVALID_ARG;
+  const bool quant = qset != nullptr;
+  if (quant) {
+    if (!enabled(&qset->grad) || !quantizer_ok(&qset->grad) || !qset->x.scale_inv ||
+        !quantizer_ok(&qset->kernel1))
+      return TE_ERR_INVALID_ARG;
+    if (kernel_dtype == TE_E4M3 ? !qset->kernel1.scale_inv
+                                : (kernel_dtype != dtype || !enabled(&qset->kernel1)))
+      return TE_ERR_INVALID_ARG;
+  } else if (kernel_dtype != dtype) {
+    return TE_ERR_INVALID_ARG;
+  }
+  if (!gamma || !dgamma || (M > 0 && (!dy || !x || !kernel1 || !kernel2 || !saved_h ||
+                                      !saved_ln_out || !rsigma || !dx || !dkernel1 || !dkernel2)) ||
+      (M > 0 && norm_type == TE_LAYERNORM && !mu))
+    return TE_ERR_INVALID_ARG;
+  if (H % 16 || F % 16 || H * int64_t(esize(dtype)) > 16384) return TE_ERR_UNSUPPORTED;
+  if (!aligned16(dy) || !aligned16(x) || !aligned16(gamma) || !aligned16(kernel1) ||
+      !aligned16(kernel2) || !aligned16(saved_h) || !aligned16(saved_ln_out) || !aligned16(dx) ||
+      !aligned16(dkernel1) || !aligned16(dkernel2) || !aligned16(workspace) || !aligned4(mu) ||
+      !aligned4(rsigma) || !aligned4(dgamma) || !aligned4(dbeta) || !aligned4(dbias1) ||
+      !aligned4(dbias2))
+    return TE_ERR_UNSUPPORTED;
+  cudaStream_t s = as_stream(stream);
+  const bool gated = act == TE_SWIGLU;
+  const int64_t F1 = gated ? 2 * F : F;
+  if (M == 0) {
+    // no tokens: every gradient is zero
+    const std::pair<void*, size_t> z[] = {{dgamma, size_t(H) * 4}, {dbeta, size_t(H) * 4},
+                                          {dbias1, size_t(F1) * 4}, {dbias2, size_t(H) * 4},
+                                          {dkernel1, size_t(H) * F1 * esize(dtype)},
+                                          {dkernel2, size_t(F) * H * esize(dtype)}};
+    for (const auto& e : z)
+      if (e.first && cudaMemsetAsync(e.first, 0, e.second, s) != cudaSuccess) return TE_ERR_CUDA;
+    return TE_OK;
+  }
+  BwdLayout L = bwd_layout(workspace, M, H, F, dtype, quant, kernel_dtype, act);
+  if (!workspace || ws_bytes < L.bytes) return TE_ERR_WORKSPACE;
+  float* partials = static_cast<float*>(L.partials);
+  te_status st;
+  // dbias2 = column sums of dy
+  if (dbias2) {
+    DactArgs d;
+    d.dy = dy;
+    d.dtype = dtype;
+    d.M = M;
+    d.N_in = H;
+    d.act = TE_IDENTITY;
+    d.dx = nullptr;
+    d.dbias = dbias2;
+    d.partials = partials;
+    st = launch_dact_dbias(d, s);
+    if (st != TE_OK) return st;
+  }
+  // recompute the activation output (what GEMM2 consumed, in dtype)
+  {
+    ActArgs aa;
+    aa.x = saved_h;
+    aa.x_dtype = dtype;
+    aa.M = M;
+    aa.N_in = F1;
+    aa.act = act;
+    aa.out = L.a;
+    aa.cast.out_dtype = dtype;
+    st = launch_act_lu(aa, s);
+    if (st != TE_OK) return st;
+  }
+  // dkernel2 = a^T dy   ([F, H], contraction over tokens)
+  {
+    GemmArgs g;
+    g.A = L.a;
+    g.B = dy;
+    g.ab_dtype = dtype;
+    g.a_kmajor = 0;
+    g.b_kmajor = 0;
+    g.M = F;
+    g.N = H;
+    g.K = M;
+    g.D = dkernel2;
+    g.cast.out_dtype = dtype;
+    st = launch_gemm(g, s);
+    if (st != TE_OK) return st;
+  }
+  // da = dy kernel2^T   ([M, F], contraction over H)
+  {
+    GemmArgs g;
+    g.A = dy;
+    g.B = kernel2;
+    g.ab_dtype = dtype;
+    g.a_kmajor = 1;
+    g.b_kmajor = 1;
+    g.M = M;
+    g.N = F;
+    g.K = H;
+    g.D = L.da;
+    g.cast.out_dtype = dtype;
+    st = launch_gemm(g, s);
+    if (st != TE_OK) return st;
+  }
+  // dH = da * act'(h), dbias1, quantized with the grad quantizer in FP8 mode
+  st = run_cast(quant ? &qset->grad : nullptr, quant ? TE_E4M3 : dtype, 0, s,
+                [&](const CastSpec& c) {
+                  DactArgs d;
+                  d.dy = L.da;
+                  d.x = saved_h;
+                  d.dtype = dtype;
+                  d.M = M;
+                  d.N_in = F1;
+                  d.act = act;
+                  d.dx = L.dh;
+                  const bool two_pass = quant && qset->grad.mode == TE_SCALING_CURRENT;
+                  d.dbias = (two_pass ? c.store == 0 : true) ? dbias1 : nullptr;
+                  d.partials = partials;
+                  d.cast = c;
+                  return launch_dact_dbias(d, s);
+                });
+  if (st != TE_OK) return st;
+  const void* w1 = kernel1;
+  if (quant && kernel_dtype != TE_E4M3) {
+    st = quantize_into(kernel1, dtype, H * F1, &qset->kernel1, L.kq1, s);
+    if (st != TE_OK) return st;
+    w1 = L.kq1;
+  }
+  // dln = dH kernel1^T   ([M, H], contraction over F')
+  {
+    GemmArgs g;
+    g.A = L.dh;
+    g.B = w1;
+    g.ab_dtype = quant ? TE_E4M3 : dtype;
+    g.a_kmajor = 1;
+    g.b_kmajor = 1;
+    g.M = M;
+    g.N = H;
+    g.K = F1;
+    g.a_scale_inv = quant ? qset->grad.scale_inv : nullptr;
+    g.b_scale_inv = quant ? qset->kernel1.scale_inv : nullptr;
+    g.D = L.dln;
+    g.cast.out_dtype = dtype;
+    st = launch_gemm(g, s);
+    if (st != TE_OK) return st;
+  }
+  // dkernel1 = ln^T dH   ([H, F'], contraction over tokens)
+  {
+    GemmArgs g;
+    g.A = saved_ln_out;
+    g.B = L.dh;
+    g.ab_dtype = quant ? TE_E4M3 : dtype;
+    g.a_kmajor = 0;
+    g.b_kmajor = 0;
+    g.M = H;
+    g.N = F1;
+    g.K = M;
+    g.a_scale_inv = quant ? qset->x.scale_inv : nullptr;
+    g.b_scale_inv = quant ? qset->grad.scale_inv : nullptr;
+    g.D = dkernel1;
+    g.cast.out_dtype = dtype;
+    st = launch_gemm(g, s);
+    if (st != TE_OK) return st;
+  }
+  // norm backward
+  NormBwdArgs nb;
+  nb.dz = L.dln;
+  nb.x = x;
+  nb.mu = mu;
+  nb.rsigma = rsigma;
+  nb.gamma = gamma;
+  nb.dtype = dtype;
+  nb.M = M;
+  nb.H = H;
+  nb.norm_type = norm_type;
+  nb.zero_centered_gamma = zero_centered_gamma;
+  nb.dx = dx;
+  nb.dgamma = dgamma;
+  nb.dbeta = norm_type == TE_LAYERNORM ? dbeta : nullptr;
+  nb.partials = partials;
+  return launch_norm_bwd(nb, s);
 }
 
 te_status te_norm_bwd(const void* dz, const void* x, const float* mu, const float* rsigma,

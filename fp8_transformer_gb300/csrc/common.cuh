@@ -84,6 +84,35 @@ __device__ __forceinline__ float dgelu(float h) {
   return sp + 2.0f * h * kGeluK0 * (1.0f + 3.0f * kGeluK1 * h * h) * sp * sn;
 }
 
+// Bandwidth-bound kernels evaluate the derivatives with the hardware exp2 / reciprocal
+// approximations (relative error ~1e-6), so that arithmetic stays under the memory time.
+__device__ __forceinline__ float fast_rcp(float x) { return __fdividef(1.0f, x); }
+
+__device__ __forceinline__ float silu_fast(float z) { return z * fast_rcp(1.0f + __expf(-z)); }
+
+__device__ __forceinline__ float dsilu_fast(float z) {
+  const float e = __expf(-fmaxf(z, -80.0f));
+  const float s = fast_rcp(1.0f + e);
+  return s * (1.0f + z * (e * s));
+}
+
+__device__ __forceinline__ float dgelu_fast(float h) {
+  const float u = gelu_u(h);
+  const float e = __expf(-2.0f * fmaxf(u, -40.0f));
+  const float sp = fast_rcp(1.0f + e);
+  const float sn = e * sp;
+  return sp + 2.0f * h * kGeluK0 * (1.0f + 3.0f * kGeluK1 * h * h) * sp * sn;
+}
+
+__device__ __forceinline__ float dact_fast(int act, float h) {
+  switch (act) {
+    case TE_RELU: return h > 0.0f ? 1.0f : 0.0f;
+    case TE_GELU: return dgelu_fast(h);
+    case TE_SILU: return dsilu_fast(h);
+    default: return 1.0f;
+  }
+}
+
 // Non-gated activation by id (TE_IDENTITY, TE_RELU, TE_GELU, TE_SILU).
 __device__ __forceinline__ float act_apply(int act, float h) {
   switch (act) {

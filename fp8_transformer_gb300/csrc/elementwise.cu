@@ -89,6 +89,8 @@ __global__ void __launch_bounds__(kEwThreads) act_lu_kernel(ActArgs a) {
 constexpr int kDactWarps = 8;
 constexpr int kDactRows = 128;  // rows per CTA (chunk)
 
+constexpr int kDactUnroll = 4;  // rows in flight per warp
+
 template <typename T>
 __global__ void __launch_bounds__(kDactWarps * 32) dact_dbias_kernel(DactArgs a) {
   using V = Vec16<T>;
@@ -98,6 +100,7 @@ __global__ void __launch_bounds__(kDactWarps * 32) dact_dbias_kernel(DactArgs a)
   const CastState cs = cast_begin(a.cast);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const bool gated = a.act == TE_SWIGLU;
+  const bool ident = a.act == TE_IDENTITY;
   const int64_t n_out = gated ? a.N_in / 2 : a.N_in;
   const int64_t col = (int64_t(blockIdx.x) * 32 + lane) * E;
   const bool valid = col < n_out;
@@ -107,41 +110,51 @@ __global__ void __launch_bounds__(kDactWarps * 32) dact_dbias_kernel(DactArgs a)
 #pragma unroll
   for (int e = 0; e < E; ++e) { acc1[e] = 0.0f; acc2[e] = 0.0f; }
   float amax = 0.0f;
+  const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
   if (valid) {
-    for (int64_t r = r0 + warp; r < r1; r += kDactWarps) {
-      float dy[E];
-      V::load(a.dy, r * n_out + col, dy);
-      if (gated) {
-        float g[E], l[E], dg[E], dl[E];
-        V::load(a.x, r * a.N_in + col, g);
-        V::load(a.x, r * a.N_in + n_out + col, l);
+    for (int64_t rb = r0 + warp; rb < r1; rb += kDactUnroll * kDactWarps) {
+      // issue every load of kDactUnroll rows before using any of them
+      uint4 rdy[kDactUnroll], rx[kDactUnroll], rl[kDactUnroll];
 #pragma unroll
-        for (int e = 0; e < E; ++e) {
-          dg[e] = dy[e] * l[e] * dsilu(g[e]);
-          dl[e] = dy[e] * act_silu(g[e]);
-          acc1[e] += dg[e];
-          acc2[e] += dl[e];
-          amax = fmaxf(amax, fmaxf(fabsf(dg[e]), fabsf(dl[e])));
-        }
-        if (cs.store) {
-          cast_store<E>(a.dx, r * a.N_in + col, dg, cs);
-          cast_store<E>(a.dx, r * a.N_in + n_out + col, dl, cs);
-        }
-      } else {
-        float h[E], d[E];
-        if (a.act != TE_IDENTITY) {
-          V::load(a.x, r * a.N_in + col, h);
+      for (int j = 0; j < kDactUnroll; ++j) {
+        const int64_t r = rb + int64_t(j) * kDactWarps;
+        const bool in = r < r1;
+        rdy[j] = in ? __ldg(reinterpret_cast<const uint4*>(static_cast<const T*>(a.dy) + r * n_out + col)) : zero;
+        rx[j] = (in && !ident) ? __ldg(reinterpret_cast<const uint4*>(static_cast<const T*>(a.x) + r * a.N_in + col)) : zero;
+        rl[j] = (in && gated) ? __ldg(reinterpret_cast<const uint4*>(static_cast<const T*>(a.x) + r * a.N_in + n_out + col)) : zero;
+      }
+#pragma unroll
+      for (int j = 0; j < kDactUnroll; ++j) {
+        const int64_t r = rb + int64_t(j) * kDactWarps;
+        if (r >= r1) break;
+        float dy[E], h[E];
+        V::unpack(rdy[j], dy);
+        V::unpack(rx[j], h);
+        if (gated) {
+          float l[E], dg[E], dl[E];
+          V::unpack(rl[j], l);
+#pragma unroll
+          for (int e = 0; e < E; ++e) {
+            dg[e] = dy[e] * l[e] * dsilu_fast(h[e]);
+            dl[e] = dy[e] * silu_fast(h[e]);
+            acc1[e] += dg[e];
+            acc2[e] += dl[e];
+            amax = fmaxf(amax, fmaxf(fabsf(dg[e]), fabsf(dl[e])));
+          }
+          if (cs.store) {
+            cast_store<E>(a.dx, r * a.N_in + col, dg, cs);
+            cast_store<E>(a.dx, r * a.N_in + n_out + col, dl, cs);
+          }
         } else {
+          float d[E];
 #pragma unroll
-          for (int e = 0; e < E; ++e) h[e] = 0.0f;
+          for (int e = 0; e < E; ++e) {
+            d[e] = ident ? dy[e] : dy[e] * dact_fast(a.act, h[e]);
+            acc1[e] += d[e];
+            amax = fmaxf(amax, fabsf(d[e]));
+          }
+          if (cs.store && a.dx) cast_store<E>(a.dx, r * a.N_in + col, d, cs);
         }
-#pragma unroll
-        for (int e = 0; e < E; ++e) {
-          d[e] = a.act == TE_IDENTITY ? dy[e] : dy[e] * dact_apply(a.act, h[e]);
-          acc1[e] += d[e];
-          amax = fmaxf(amax, fabsf(d[e]));
-        }
-        if (cs.store && a.dx) cast_store<E>(a.dx, r * a.N_in + col, d, cs);
       }
     }
   }
@@ -152,7 +165,7 @@ __global__ void __launch_bounds__(kDactWarps * 32) dact_dbias_kernel(DactArgs a)
       red[warp][1][lane * E + e] = acc2[e];
     }
     __syncthreads();
-    // 256 threads finish 2 * W column sums, each over the 8 warps in warp order.
+    // 256 threads finish the strip's column sums, each over the 8 warps in warp order.
     const int halves = gated ? 2 : 1;
     for (int t = threadIdx.x; t < halves * W; t += blockDim.x) {
       const int hsel = t / W, j = t % W;

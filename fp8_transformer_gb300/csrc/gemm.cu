@@ -28,6 +28,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "sync.cuh"
 
 namespace te {
 
@@ -43,8 +44,6 @@ constexpr int A_STAGE = BM * kRowBytes; // 16 KB
 constexpr int B_STAGE = BN * kRowBytes; // 32 KB
 constexpr int kThreads = 192;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
-constexpr uint64_t kDrainLimitNs = 200000000ull;   // 0.2 s
 constexpr int kGroupM = 8;              // m-tiles per raster group (L2 reuse of B)
 
 // Element kinds: 0 = bf16 (kind::f16), 1 = E4M3 (kind::f8f6f4), 2 = fp32 as tf32 (kind::tf32).
@@ -81,61 +80,6 @@ struct __align__(64) GemmParams {
 };
 
 // ------------------------------------------------------------------ PTX wrappers ----------
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-               : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-__device__ __forceinline__ uint64_t global_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
-// Waits for the phase of `bar` with parity `parity`.  Returns false, without waiting further,
-// when the CTA's abort flag is raised (check_abort) or the time limit passes; the latter
-// records TE_ERR_TIMEOUT and raises the flag.
-__device__ __noinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          uint64_t limit_ns, bool check_abort) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_ns();
-  for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 31) == 0) {
-      if (check_abort && *abort_flag) return false;
-      if (global_ns() - t0 > limit_ns) {
-        atomicCAS(&g_device_status, 0, int(TE_ERR_TIMEOUT));
-        *abort_flag = 1;
-        return false;
-      }
-    }
-  }
-}
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm, uint32_t bar,
                                             int c0, int c1) {
@@ -340,7 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         const int m0 = tl.m * BM;
         bool ok = true;
         for (int kb = 0; kb < g.num_kb; ++kb) {
-          if (!wait_bounded(smem_u32(&empty[stage]), phase ^ 1, abort_flag, kWaitLimitNs, true)) {
+          if (!wait_bounded(smem_u32(&empty[stage]), phase ^ 1, abort_flag, &g_device_status, kWaitLimitNs, true)) {
             ok = false;
             break;
           }
@@ -391,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       // Own copies still in flight complete before the CTA may exit.
       for (int s = 0; s < STAGES; ++s)
         if (issued & (1u << s))
-          wait_bounded(smem_u32(&full[s]), (last_parity >> s) & 1, abort_flag, kDrainLimitNs, false);
+          wait_bounded(smem_u32(&full[s]), (last_parity >> s) & 1, abort_flag, &g_device_status, kDrainLimitNs, false);
     }
   } else if (warp == 1) {
     // ----------------------------------------------------------- MMA issuer -------------
@@ -403,14 +347,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++local) {
         const int acc = local & 1;
         const uint32_t acc_phase = (local >> 1) & 1;
-        if (!wait_bounded(smem_u32(&tempty[acc]), acc_phase ^ 1, abort_flag, kWaitLimitNs, true)) {
+        if (!wait_bounded(smem_u32(&tempty[acc]), acc_phase ^ 1, abort_flag, &g_device_status, kWaitLimitNs, true)) {
           ok = false;
           break;
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + uint32_t(acc * BN);
         for (int kb = 0; kb < g.num_kb; ++kb) {
-          if (!wait_bounded(smem_u32(&full[stage]), phase, abort_flag, kWaitLimitNs, true)) {
+          if (!wait_bounded(smem_u32(&full[stage]), phase, abort_flag, &g_device_status, kWaitLimitNs, true)) {
             ok = false;
             break;
           }
@@ -438,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       }
       // Own MMAs complete before TMEM is released.
       umma_commit(smem_u32(drain));
-      wait_bounded(smem_u32(drain), 0, abort_flag, kDrainLimitNs, false);
+      wait_bounded(smem_u32(drain), 0, abort_flag, &g_device_status, kDrainLimitNs, false);
     }
   } else {
     // ----------------------------------------------------------- epilogue ---------------
@@ -457,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       const uint32_t acc_phase = (local >> 1) & 1;
       const uint32_t tb = smem_u32(&tfull[acc]);
       int ok = 1;
-      if (lane == 0) ok = wait_bounded(tb, acc_phase, abort_flag, kWaitLimitNs, true) ? 1 : 0;
+      if (lane == 0) ok = wait_bounded(tb, acc_phase, abort_flag, &g_device_status, kWaitLimitNs, true) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       // The phase has completed; every lane observes it before touching TMEM.
@@ -632,9 +576,15 @@ int num_sms() {
 }
 
 int* device_status_ptr() {
-  void* p = nullptr;
-  if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
-  return static_cast<int*>(p);
+  static int* cached[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (!cached[dev & 63]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
+    cached[dev & 63] = static_cast<int*>(p);
+  }
+  return cached[dev & 63];
 }
 
 te_status read_and_clear_device_status(int32_t* out) {

@@ -1,9 +1,10 @@
 // Row normalization kernels (LayerNorm / RMSNorm forward and backward).
 //
 // Forward (TransformerEngine JAX "LayerNorm MLP" page, Description step (1); "LayerNorm Dense"
-// page, Description): one warp per row, the row held in registers as 16-byte vectors, fp32
-// statistics, and the normalized row written once, directly in the consumer GEMM's operand
-// dtype (fp32, bf16 or E4M3) together with the per-tensor amax.
+// page, Description): one warp per row, rows streamed into a per-warp double buffer in shared
+// memory by the bulk-copy engine, fp32 statistics, and the normalized row written once,
+// directly in the consumer GEMM's operand dtype (fp32, bf16 or E4M3) with 16-byte stores,
+// together with the per-tensor amax.
 //
 // Backward (the norm's share of the backward pass, whose gradients cover every parameter): one CTA walks
 // a strided set of rows; each row's dx needs two row sums, reduced across the CTA; dgamma and
@@ -12,81 +13,114 @@
 #include "cast.cuh"
 #include "common.cuh"
 #include "kernels.h"
+#include "sync.cuh"
 
 namespace te {
 
 namespace {
 
-constexpr int kFwdWarps = 8;
+constexpr int kFwdMaxWarps = 8;
+constexpr size_t kFwdSmemBudget = 200 * 1024;  // row buffers per CTA
 
-template <typename T, int NV>
-__global__ void __launch_bounds__(kFwdWarps * 32) norm_fwd_kernel(NormFwdArgs a) {
+// One warp per row, persistent over rows.  Each warp owns two row buffers in shared memory:
+// while it normalizes row r from one buffer, the bulk-copy engine streams row r + stride into
+// the other, so every warp keeps a whole row in flight with few registers.
+template <typename T>
+__global__ void __launch_bounds__(kFwdMaxWarps * 32) norm_fwd_kernel(NormFwdArgs a, int* status,
+                                                                     uint32_t row_bytes) {
   using V = Vec16<T>;
   constexpr int E = V::N;
+  extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t row = int64_t(blockIdx.x) * kFwdWarps + warp;
+  const int nwarps = blockDim.x >> 5;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem) + 2 * warp;
+  uint8_t* bufs = smem + 256 + size_t(warp) * 2 * row_bytes;
+  if (lane == 0) {
+    mbar_init(smem_u32(&bars[0]), 1);
+    mbar_init(smem_u32(&bars[1]), 1);
+    mbar_init_fence();
+  }
+  __syncwarp();
   const CastState cs = cast_begin(a.cast);
+  const int nvec = int(a.H / E);
+  const float inv_h = 1.0f / float(a.H);
+  const bool ln = a.norm_type == TE_LAYERNORM;
+  const int64_t stride = int64_t(gridDim.x) * nwarps;
+  const char* xg = static_cast<const char*>(a.x);
+  int issued[2] = {0, 0}, waited[2] = {0, 0};  // lane 0's bookkeeping of its copies
   float amax = 0.0f;
-  if (row < a.M) {
-    const int nvec = int(a.H / E);
-    const T* xr = static_cast<const T*>(a.x) + row * a.H;
-    const uint4* xr16 = reinterpret_cast<const uint4*>(xr);
-    // The row stays in registers as raw 16-byte vectors and is unpacked on each pass.
-    uint4 raw[NV];
-#pragma unroll
-    for (int i = 0; i < NV; ++i) {
-      const int v = lane + i * 32;
-      raw[i] = v < nvec ? __ldg(xr16 + v) : make_uint4(0u, 0u, 0u, 0u);
+  int64_t row = int64_t(blockIdx.x) * nwarps + warp;
+  if (lane == 0 && row < a.M) {
+    mbar_expect_tx(smem_u32(&bars[0]), row_bytes);
+    bulk_load(smem_u32(bufs), xg + row * row_bytes, row_bytes, smem_u32(&bars[0]));
+    issued[0]++;
+  }
+  for (int i = 0; row < a.M; ++i, row += stride) {
+    const int st = i & 1;
+    const uint32_t par = uint32_t(i >> 1) & 1u;
+    const int64_t next = row + stride;
+    if (lane == 0 && next < a.M) {
+      // the other buffer was last read in the previous iteration (ordered by __syncwarp)
+      fence_proxy_async_smem();
+      mbar_expect_tx(smem_u32(&bars[st ^ 1]), row_bytes);
+      bulk_load(smem_u32(bufs + (st ^ 1) * row_bytes), xg + next * row_bytes, row_bytes,
+                smem_u32(&bars[st ^ 1]));
+      issued[st ^ 1]++;
     }
-    const float inv_h = 1.0f / float(a.H);
+    int ok = 1;
+    if (lane == 0) {
+      ok = wait_bounded(smem_u32(&bars[st]), par, nullptr, status, kWaitLimitNs, false) ? 1 : 0;
+      waited[st] += ok;
+    }
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (!ok) break;
+    while (!mbar_try_wait(smem_u32(&bars[st]), par)) {
+    }
+    __syncwarp();
+    const uint4* xs = reinterpret_cast<const uint4*>(bufs + st * row_bytes);
     float mean = 0.0f, rs;
-    if (a.norm_type == TE_LAYERNORM) {
-      float s = 0.0f;
-#pragma unroll
-      for (int i = 0; i < NV; ++i) {
+    if (ln) {
+      float s1 = 0.0f;
+#pragma unroll 4
+      for (int v = lane; v < nvec; v += 32) {
         float xv[E];
-        V::unpack(raw[i], xv);
+        V::unpack(xs[v], xv);
 #pragma unroll
-        for (int e = 0; e < E; ++e) s += xv[e];
+        for (int e = 0; e < E; ++e) s1 += xv[e];
       }
-      mean = warp_sum(s) * inv_h;
-      float ss = 0.0f;
+      mean = warp_sum(s1) * inv_h;
+      float s2 = 0.0f;
+#pragma unroll 4
+      for (int v = lane; v < nvec; v += 32) {
+        float xv[E];
+        V::unpack(xs[v], xv);
 #pragma unroll
-      for (int i = 0; i < NV; ++i) {
-        if (lane + i * 32 < nvec) {
-          float xv[E];
-          V::unpack(raw[i], xv);
-#pragma unroll
-          for (int e = 0; e < E; ++e) {
-            const float d = xv[e] - mean;
-            ss += d * d;
-          }
+        for (int e = 0; e < E; ++e) {
+          const float d = xv[e] - mean;
+          s2 += d * d;
         }
       }
-      rs = 1.0f / sqrtf(warp_sum(ss) * inv_h + a.eps);
+      rs = 1.0f / sqrtf(warp_sum(s2) * inv_h + a.eps);
     } else {
-      float ss = 0.0f;
-#pragma unroll
-      for (int i = 0; i < NV; ++i) {
+      float s2 = 0.0f;
+#pragma unroll 4
+      for (int v = lane; v < nvec; v += 32) {
         float xv[E];
-        V::unpack(raw[i], xv);
+        V::unpack(xs[v], xv);
 #pragma unroll
-        for (int e = 0; e < E; ++e) ss += xv[e] * xv[e];
+        for (int e = 0; e < E; ++e) s2 += xv[e] * xv[e];
       }
-      rs = 1.0f / sqrtf(warp_sum(ss) * inv_h + a.eps);
+      rs = 1.0f / sqrtf(warp_sum(s2) * inv_h + a.eps);
     }
     if (lane == 0) {
       if (a.mu) a.mu[row] = mean;
       if (a.rsigma) a.rsigma[row] = rs;
     }
-    const bool ln = a.norm_type == TE_LAYERNORM;
-#pragma unroll
-    for (int i = 0; i < NV; ++i) {
-      const int v = lane + i * 32;
-      if (v < nvec) {
+    if (cs.store || a.cast.amax_out) {
+#pragma unroll 2
+      for (int v = lane; v < nvec; v += 32) {
         float xv[E], g[E], b[E], y[E];
-        // Re-read from cache rather than keeping the packed row alive through this pass.
-        V::load(xr, int64_t(v) * E, xv);
+        V::unpack(xs[v], xv);
         V::load(a.gamma, int64_t(v) * E, g);
         if (ln && a.beta) {
           V::load(a.beta, int64_t(v) * E, b);
@@ -102,32 +136,44 @@ __global__ void __launch_bounds__(kFwdWarps * 32) norm_fwd_kernel(NormFwdArgs a)
         }
         if (cs.store) cast_store<E>(a.out, row * a.H + int64_t(v) * E, y, cs);
       }
-      // Keeps the next vector's gamma/beta loads from being hoisted above this store, which
-      // would hold every vector's parameters in registers at once.
-      asm volatile("" ::: "memory");
     }
+    __syncwarp();
   }
-  block_amax_commit(amax, a.cast.amax_out);
-}
-
-template <typename T, int NV>
-te_status launch_fwd_t(const NormFwdArgs& a, cudaStream_t s) {
-  const unsigned grid = unsigned(ceil_div(a.M, kFwdWarps));
-  norm_fwd_kernel<T, NV><<<grid, kFwdWarps * 32, 0, s>>>(a);
-  return cudaGetLastError() == cudaSuccess ? TE_OK : TE_ERR_CUDA;
+  // Copies still in flight land before the CTA may exit (only after a timeout).
+  if (lane == 0) {
+    for (int s2 = 0; s2 < 2; ++s2)
+      if (issued[s2] > waited[s2])
+        wait_bounded(smem_u32(&bars[s2]), uint32_t(waited[s2]) & 1u, nullptr, status,
+                     kDrainLimitNs, false);
+  }
+  amax = warp_max(amax);
+  if (lane == 0 && a.cast.amax_out) atomic_max_nonneg(a.cast.amax_out, amax);
 }
 
 template <typename T>
-te_status launch_fwd_dispatch(const NormFwdArgs& a, cudaStream_t s) {
-  constexpr int E = Vec16<T>::N;
-  const int64_t per_lane = ceil_div(a.H / E, 32);
-  if (per_lane <= 1) return launch_fwd_t<T, 1>(a, s);
-  if (per_lane <= 2) return launch_fwd_t<T, 2>(a, s);
-  if (per_lane <= 4) return launch_fwd_t<T, 4>(a, s);
-  if (per_lane <= 8) return launch_fwd_t<T, 8>(a, s);
-  if (per_lane <= 16) return launch_fwd_t<T, 16>(a, s);
-  if (per_lane <= 32) return launch_fwd_t<T, 32>(a, s);
-  return TE_ERR_UNSUPPORTED;
+te_status launch_fwd_t(const NormFwdArgs& a, cudaStream_t s) {
+  const uint32_t row_bytes = uint32_t(a.H * sizeof(T));
+  int warps = int(kFwdSmemBudget / (2 * size_t(row_bytes)));
+  if (warps < 1) return TE_ERR_UNSUPPORTED;
+  if (warps > kFwdMaxWarps) warps = kFwdMaxWarps;
+  const size_t smem = 256 + size_t(warps) * 2 * row_bytes;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (!attr_set[dev & 63]) {
+    if (cudaFuncSetAttribute(norm_fwd_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(256 + kFwdSmemBudget)) != cudaSuccess)
+      return TE_ERR_CUDA;
+    attr_set[dev & 63] = true;
+  }
+  int per_sm = int((227 * 1024) / smem);
+  if (per_sm < 1) per_sm = 1;
+  if (per_sm * warps > 64) per_sm = 64 / warps;
+  const int64_t needed = ceil_div(a.M, warps);
+  const int64_t cap = int64_t(num_sms()) * per_sm;
+  const unsigned grid = unsigned(needed < cap ? needed : cap);
+  norm_fwd_kernel<T><<<grid, warps * 32, smem, s>>>(a, device_status_ptr(), row_bytes);
+  return cudaGetLastError() == cudaSuccess ? TE_OK : TE_ERR_CUDA;
 }
 
 // ----------------------------------------------------------------------- backward --------
@@ -259,8 +305,8 @@ te_status launch_bwd_dispatch(const NormBwdArgs& a, cudaStream_t s) {
 te_status launch_norm_fwd(const NormFwdArgs& a, cudaStream_t s) {
   if (a.M == 0) return TE_OK;
   ProfileScope prof(TE_KERNEL_NORM_FWD, s);
-  if (a.x_dtype == TE_BF16) return launch_fwd_dispatch<__nv_bfloat16>(a, s);
-  if (a.x_dtype == TE_F32) return launch_fwd_dispatch<float>(a, s);
+  if (a.x_dtype == TE_BF16) return launch_fwd_t<__nv_bfloat16>(a, s);
+  if (a.x_dtype == TE_F32) return launch_fwd_t<float>(a, s);
   return TE_ERR_UNSUPPORTED;
 }
 

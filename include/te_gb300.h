@@ -237,6 +237,36 @@ te_status te_layernorm_mlp_fwd(const void* x, const void* gamma, const void* bet
                                void* stream);
 
 /* ---------------------------------------------------------------------------------------
+ * te_layernorm_mlp_bwd -- backward of te_layernorm_mlp_fwd (LayerNorm MLP page, Description:
+ * the backward pass yields the gradient of every parameter and uses the fused activation
+ * gradient + bias reduction + quantization step).
+ * Sequence (all on `stream`): dbias2 = column sums of dy; a = act(saved_h) recomputed in dtype;
+ * dkernel2 = a^T dy; da = dy kernel2^T; dH = da * act'(saved_h) with dbias1 = its fp32 column
+ * sums, stored E4M3 (qset->grad) or in dtype; dln = dH kernel1^T; dkernel1 = ln^T dH; then the
+ * norm backward gives dx, dgamma, dbeta.
+ *   dy [M, H], x [M, H], gamma [H], kernel2 [F, H], saved_h [M, F'] in dtype (F' = 2F for
+ *   TE_SWIGLU); kernel1 [H, F'] in kernel_dtype; mu, rsigma [M] from the forward.
+ *   saved_ln_out [M, H]: the forward's normalized output (E4M3 with qset, else dtype).
+ *   qset NULL: every GEMM in dtype.  Non-NULL (FP8): qset->grad must be enabled and quantizes dH;
+ *   qset->x.scale_inv dequantizes saved_ln_out; kernel1 is E4M3 (kernel_dtype TE_E4M3, factor in
+ *   qset->kernel1.scale_inv) or is quantized here with qset->kernel1.  dln and dkernel1 then run
+ *   as E4M3 x E4M3 GEMMs; dy, kernel2 and the recomputed activation stay in dtype.
+ *   Outputs: dx [M, H] dtype; dgamma [H] fp32; dbeta [H] fp32 or NULL (layernorm only);
+ *   dkernel1 [H, F'] and dkernel2 [F, H] in dtype; dbias1 [F'] and dbias2 [H] fp32 or NULL.
+ *   workspace: te_workspace_size(TE_OP_LAYERNORM_MLP_BWD, M, H, F, dtype, quantized,
+ *   kernel_dtype, act) bytes.  H and F multiples of 16.
+ */
+te_status te_layernorm_mlp_bwd(const void* dy, const void* x, const void* gamma,
+                               const void* kernel1, const void* kernel2, te_dtype kernel_dtype,
+                               const void* saved_h, const void* saved_ln_out, const float* mu,
+                               const float* rsigma, te_norm_type norm_type,
+                               int zero_centered_gamma, te_act_type act,
+                               const te_quantizer_set* qset, int64_t M, int64_t H, int64_t F,
+                               te_dtype dtype, void* dx, float* dgamma, float* dbeta,
+                               void* dkernel1, void* dkernel2, float* dbias1, float* dbias2,
+                               void* workspace, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------------------
  * te_norm_bwd -- gradients of te_norm_fwd (LayerNorm MLP page, Description: the backward pass
  * yields the gradient of every parameter; LayerNorm Dense page, Description: gradients of x,
  * gamma and beta).

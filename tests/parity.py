@@ -39,15 +39,23 @@ def rms(v) -> float:
     return float(np.sqrt(np.mean(v * v))) if v.size else 0.0
 
 
-def assert_gemm_close(got, ref, K, rms_a, rms_b, what="gemm", stored=None):
+def assert_gemm_close(got, ref, K, rms_a, rms_b, what="gemm", stored=None, fp8_operands=None):
     """``stored`` = "bf16" when both sides rounded the result to bf16: they may then land on
-    adjacent bf16 numbers, so one bf16 ulp of the stored value (2**-8 relative) is added."""
+    adjacent bf16 numbers, so one bf16 ulp of the stored value (2**-8 relative) is added.
+
+    ``fp8_operands`` = (A, B) dequantized [M, K] and [K, N] when both operands are E4M3 codes
+    that each side computed itself: by the E4M3 rule a code may sit one step (at most 1/8
+    relative) from the oracle's, so each output may also differ by one such step of one product
+    term, bounded by 2**-3 * max|A[i, :]| * max|B[:, j]|."""
     if stored is None:
         stored = "bf16" if isinstance(got, torch.Tensor) and got.dtype == torch.bfloat16 else "f32"
     got, ref = np64(got), np.asarray(ref, np.float64)
     tol = 2e-2 * math.sqrt(K) * rms_a * rms_b
     if stored == "bf16":
         tol = tol + 2.0 ** -8 * np.abs(ref)
+    if fp8_operands is not None:
+        a, b = (np.abs(np.asarray(t, np.float64)) for t in fp8_operands)
+        tol = tol + 2.0 ** -3 * a.max(axis=1)[:, None] * b.max(axis=0)[None, :]
     err = np.abs(got - ref)
     assert np.all(np.isfinite(got)), f"{what}: non-finite output"
     ratio = err / tol

