@@ -171,6 +171,69 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def bandwidth_kernels(args, dev, peaks):
+    """GB/s of the bandwidth-bound kernels alone (profiling aid): norm forward at the Llama
+    shape (bf16 and E4M3 out), and at the GPT backward shape the activation recompute, the
+    dact + dbias + quantize step and the norm backward.  --tokens scales the token count."""
+    import torch
+
+    import fp8_transformer_gb300 as te
+    from workloads import random_tensor
+
+    M = args.tokens or 8192
+    Mb = args.tokens or 16384
+    H, F = 4096, 16384
+    flush_buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = lambda: flush_buf.zero_()
+    res = {}
+
+    def run(name, fn, nbytes):
+        fn()
+        ms = statistics.mean(time_steps(fn, args.steps, flush))
+        gbs = nbytes / (ms / 1e3) / 1e9
+        res[name] = {"GB/s": gbs, "frac": gbs / peaks["hbm"], "ms": ms, "bytes": nbytes}
+
+    x = random_tensor((M, H), device=dev, seed=1)
+    g = random_tensor((H,), std=0.05, device=dev, seed=2)
+    b = torch.zeros(H, dtype=torch.bfloat16, device=dev)
+    y = torch.empty(M, H, dtype=torch.bfloat16, device=dev)
+    y8 = torch.empty(M, H, dtype=torch.uint8, device=dev)
+    mu = torch.empty(M, dtype=torch.float32, device=dev)
+    rs = torch.empty(M, dtype=torch.float32, device=dev)
+    q = te.Quantizer(32.0, "delayed", dev)
+    run("norm_fwd_bf16", lambda: te.te_norm_fwd(x, g, b, "rmsnorm", True, 1e-6, y, mu=mu,
+                                                rsigma=rs), M * H * 4 + M * 8)
+    run("norm_fwd_e4m3", lambda: te.te_norm_fwd(x, g, b, "rmsnorm", True, 1e-6, y8, q=q, mu=mu,
+                                                rsigma=rs), M * H * 3 + M * 8)
+    del x, y, y8, mu, rs
+    h = random_tensor((Mb, F), std=2.0, device=dev, seed=3)
+    da = random_tensor((Mb, F), device=dev, seed=4)
+    a = torch.empty(Mb, F, dtype=torch.bfloat16, device=dev)
+    run("act_lu_gelu_bf16", lambda: te.te_act_lu(h, "gelu", a), Mb * F * 4)
+    del a
+    dh = torch.empty(Mb, F, dtype=torch.uint8, device=dev)
+    db = torch.empty(F, dtype=torch.float32, device=dev)
+    ws = torch.empty(te.workspace_size(te.binding.TE_OP_DACT_DBIAS, Mb, 0, F), dtype=torch.uint8,
+                     device=dev)
+    qg = te.Quantizer(16.0, "delayed", dev)
+    run("dact_dbias_e4m3", lambda: te.te_dact_dbias_quantize(da, h, "gelu", dh, dbias=db, q=qg,
+                                                             workspace=ws), Mb * F * 5 + F * 4)
+    del h, da, dh, ws
+    xb = random_tensor((Mb, H), device=dev, seed=5)
+    dz = random_tensor((Mb, H), device=dev, seed=6)
+    mub = torch.zeros(Mb, dtype=torch.float32, device=dev)
+    rsb = torch.ones(Mb, dtype=torch.float32, device=dev)
+    dx = torch.empty(Mb, H, dtype=torch.bfloat16, device=dev)
+    dgm = torch.empty(H, dtype=torch.float32, device=dev)
+    dbt = torch.empty(H, dtype=torch.float32, device=dev)
+    wsn = torch.empty(te.workspace_size(te.binding.TE_OP_NORM_BWD, Mb, H, 0), dtype=torch.uint8,
+                      device=dev)
+    run("norm_bwd_bf16", lambda: te.te_norm_bwd(dz, xb, mub, rsb, g, "layernorm", False, dx, dgm,
+                                                dbt, workspace=wsn), Mb * H * 6 + Mb * 8)
+    return {"bandwidth_only": True, "tokens_norm": M, "tokens_bwd": Mb, "kernels": res,
+            "peak_hbm_gbs": peaks["hbm"]}
+
+
 def run_ours(args, rank, world, local_rank):
     import numpy as np
     import torch
@@ -183,6 +246,10 @@ def run_ours(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     te.lib()
     peaks = load_peaks()
+    if args.bandwidth_only:
+        if rank == 0:
+            print(json.dumps(bandwidth_kernels(args, dev, peaks)), flush=True)
+        return
     inp = make_inputs(WORKLOAD, device=dev, seed=rank, M=args.tokens)
     M, H, F = inp["M"], inp["H"], inp["F"]
     gated = inp["act"] == "swiglu"
@@ -443,6 +510,8 @@ def main():
                     help="override the token count (profiling runs on a smaller batch)")
     ap.add_argument("--kernels-only", action="store_true",
                     help="time the GPU steps only: no e2e, bandwidth kernels or CPU baseline")
+    ap.add_argument("--bandwidth-only", action="store_true",
+                    help="time only the bandwidth-bound kernels (profiling aid)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     world = int(os.environ.get("WORLD_SIZE", "1"))
