@@ -96,6 +96,16 @@ struct Vec16<__nv_bfloat16> {
   }
 };
 
+// 16-byte read-only global load kept in program order with the other volatile asm (so a loop
+// of these cannot all be hoisted ahead of the work that consumes them).
+__device__ __forceinline__ uint4 ldg16_ordered(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
 template <>
 struct Vec16<float> {
   static constexpr int N = 4;

@@ -104,6 +104,19 @@ __device__ __forceinline__ float dgelu_fast(float h) {
   return sp + 2.0f * h * kGeluK0 * (1.0f + 3.0f * kGeluK1 * h * h) * sp * sn;
 }
 
+__device__ __forceinline__ float gelu_fast(float h) {
+  return h * fast_rcp(1.0f + __expf(-2.0f * gelu_u(h)));
+}
+
+__device__ __forceinline__ float act_fast(int act, float h) {
+  switch (act) {
+    case TE_RELU: return act_relu(h);
+    case TE_GELU: return gelu_fast(h);
+    case TE_SILU: return silu_fast(h);
+    default: return h;
+  }
+}
+
 __device__ __forceinline__ float dact_fast(int act, float h) {
   switch (act) {
     case TE_RELU: return h > 0.0f ? 1.0f : 0.0f;

@@ -5,8 +5,9 @@
 //   and the kernel are quantized before the GEMM): 16-byte vectors, grid-stride, amax by one
 //   integer atomic per block.
 // * act_lu ("Activation" page, Description: the forward rule's activation primitive, optional
-//   FP8 round trip): elementwise; the gated pair reads its gate and linear halves from the two
-//   column halves of the same row.
+//   FP8 round trip): elementwise, several 16-byte vectors in flight per thread, exp and
+//   reciprocal on the hardware approximations; the gated pair reads its gate and linear halves
+//   from the two column halves of the same row.
 // * dact_dbias ("LayerNorm MLP" page, Description, backward: tex.quantize_dact_dbias): each CTA
 //   owns a strip of 32 x 16-byte column vectors and a chunk of rows; every thread keeps its
 //   columns' sums in registers, the 8 warps of the CTA are combined through shared memory in a
@@ -50,6 +51,8 @@ __global__ void __launch_bounds__(kEwThreads) quantize_kernel(QuantizeArgs a) {
 
 // ------------------------------------------------------------------ act_lu ----------------
 
+constexpr int kActUnroll = 4;  // vectors in flight per thread
+
 template <typename T>
 __global__ void __launch_bounds__(kEwThreads) act_lu_kernel(ActArgs a) {
   using V = Vec16<T>;
@@ -59,27 +62,43 @@ __global__ void __launch_bounds__(kEwThreads) act_lu_kernel(ActArgs a) {
   const int64_t n_out = gated ? a.N_in / 2 : a.N_in;
   const int64_t vec_per_row = n_out / E;
   const int64_t nvec = a.M * vec_per_row;
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  const T* x = static_cast<const T*>(a.x);
+  const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
   float amax = 0.0f;
-  for (int64_t v = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; v < nvec;
-       v += int64_t(gridDim.x) * blockDim.x) {
-    const int64_t r = v / vec_per_row;
-    const int64_t c = (v - r * vec_per_row) * E;
-    float y[E];
-    if (gated) {
-      float g[E], l[E];
-      V::load(a.x, r * a.N_in + c, g);
-      V::load(a.x, r * a.N_in + n_out + c, l);
+  for (int64_t v0 = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; v0 < nvec;
+       v0 += kActUnroll * stride) {
+    uint4 rg[kActUnroll], rl[kActUnroll];
 #pragma unroll
-      for (int e = 0; e < E; ++e) y[e] = act_silu(g[e]) * l[e];
-    } else {
-      float h[E];
-      V::load(a.x, r * a.N_in + c, h);
-#pragma unroll
-      for (int e = 0; e < E; ++e) y[e] = act_apply(a.act, h[e]);
+    for (int j = 0; j < kActUnroll; ++j) {
+      const int64_t v = v0 + j * stride;
+      const int64_t r = v / vec_per_row;
+      const int64_t c = (v - r * vec_per_row) * E;
+      const bool in = v < nvec;
+      rg[j] = in ? __ldg(reinterpret_cast<const uint4*>(x + r * a.N_in + c)) : zero;
+      rl[j] = (in && gated) ? __ldg(reinterpret_cast<const uint4*>(x + r * a.N_in + n_out + c)) : zero;
     }
 #pragma unroll
-    for (int e = 0; e < E; ++e) amax = fmaxf(amax, fabsf(y[e]));
-    if (cs.store) cast_store<E>(a.out, r * n_out + c, y, cs);
+    for (int j = 0; j < kActUnroll; ++j) {
+      const int64_t v = v0 + j * stride;
+      if (v >= nvec) break;
+      const int64_t r = v / vec_per_row;
+      const int64_t c = (v - r * vec_per_row) * E;
+      float h[E], y[E];
+      V::unpack(rg[j], h);
+      if (gated) {
+        float l[E];
+        V::unpack(rl[j], l);
+#pragma unroll
+        for (int e = 0; e < E; ++e) y[e] = silu_fast(h[e]) * l[e];
+      } else {
+#pragma unroll
+        for (int e = 0; e < E; ++e) y[e] = act_fast(a.act, h[e]);
+      }
+#pragma unroll
+      for (int e = 0; e < E; ++e) amax = fmaxf(amax, fabsf(y[e]));
+      if (cs.store) cast_store<E>(a.out, r * n_out + c, y, cs);
+    }
   }
   block_amax_commit(amax, a.cast.amax_out);
 }
@@ -89,10 +108,10 @@ __global__ void __launch_bounds__(kEwThreads) act_lu_kernel(ActArgs a) {
 constexpr int kDactWarps = 8;
 constexpr int kDactRows = 128;  // rows per CTA (chunk)
 
-constexpr int kDactUnroll = 4;  // rows in flight per warp
+constexpr int kDactUnroll = 2;  // rows in flight per warp (x 24 warps per SM)
 
 template <typename T>
-__global__ void __launch_bounds__(kDactWarps * 32) dact_dbias_kernel(DactArgs a) {
+__global__ void __launch_bounds__(kDactWarps * 32, 3) dact_dbias_kernel(DactArgs a) {
   using V = Vec16<T>;
   constexpr int E = V::N;
   constexpr int W = 32 * E;  // strip width in columns

@@ -6,10 +6,11 @@
 // directly in the consumer GEMM's operand dtype (fp32, bf16 or E4M3) with 16-byte stores,
 // together with the per-tensor amax.
 //
-// Backward (the norm's share of the backward pass, whose gradients cover every parameter): one CTA walks
-// a strided set of rows; each row's dx needs two row sums, reduced across the CTA; dgamma and
-// dbeta accumulate per thread in registers, are written as one partial row per CTA and summed
-// in a fixed order by a second kernel, so the result does not depend on timing.
+// Backward (the norm's share of the backward pass, whose gradients cover every parameter): one
+// CTA walks strided groups of four rows; each row's dx needs two row sums, reduced across the
+// CTA for the whole group at one barrier; dgamma and dbeta accumulate per thread in registers,
+// are written as one partial row per CTA and summed in a fixed order by a second kernel, so the
+// result does not depend on timing.
 #include "cast.cuh"
 #include "common.cuh"
 #include "kernels.h"
@@ -150,8 +151,120 @@ __global__ void __launch_bounds__(kFwdMaxWarps * 32) norm_fwd_kernel(NormFwdArgs
   if (lane == 0 && a.cast.amax_out) atomic_max_nonneg(a.cast.amax_out, amax);
 }
 
+// Rows of up to 8 KB: one warp per row with the row resident in registers as packed 16-byte
+// vectors, persistent over rows, 2+ CTAs per SM so that many rows are in flight per SM.
+// Statistics take one pass, shifted by the row's first element (mean = x0 + E[x - x0],
+// var = E[(x - x0)^2] - E[x - x0]^2), which avoids the cancellation of the unshifted form.
+template <typename T, int NV>
+__global__ void __launch_bounds__(256, 2) norm_fwd_reg_kernel(NormFwdArgs a) {
+  using V = Vec16<T>;
+  constexpr int E = V::N;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nwarps = blockDim.x >> 5;
+  const CastState cs = cast_begin(a.cast);
+  const int nvec = int(a.H / E);
+  const float inv_h = 1.0f / float(a.H);
+  const bool ln = a.norm_type == TE_LAYERNORM;
+  float amax = 0.0f;
+  for (int64_t row = int64_t(blockIdx.x) * nwarps + warp; row < a.M;
+       row += int64_t(gridDim.x) * nwarps) {
+    const T* xr = static_cast<const T*>(a.x) + row * a.H;
+    uint4 raw[NV];
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      const int v = lane + i * 32;
+      raw[i] = v < nvec ? __ldg(reinterpret_cast<const uint4*>(xr) + v) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    float x0 = 0.0f;
+    if (ln) {
+      float first[E];
+      V::unpack(raw[0], first);
+      x0 = __shfl_sync(0xffffffffu, first[0], 0);
+    }
+    float s1 = 0.0f, s2 = 0.0f;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      if (lane + i * 32 < nvec) {
+        float xv[E];
+        V::unpack(raw[i], xv);
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          const float d = xv[e] - x0;
+          s1 += d;
+          s2 += d * d;
+        }
+      }
+    }
+    s1 = warp_sum(s1) * inv_h;
+    s2 = warp_sum(s2) * inv_h;
+    const float mean = ln ? x0 + s1 : 0.0f;
+    const float var = ln ? fmaxf(s2 - s1 * s1, 0.0f) : s2;
+    const float rs = 1.0f / sqrtf(var + a.eps);
+    if (lane == 0) {
+      if (a.mu) a.mu[row] = mean;
+      if (a.rsigma) a.rsigma[row] = rs;
+    }
+    if (cs.store || a.cast.amax_out) {
+#pragma unroll
+      for (int i = 0; i < NV; ++i) {
+        const int v = lane + i * 32;
+        if (v < nvec) {
+          float xv[E], g[E], b[E], y[E];
+          V::unpack(raw[i], xv);
+          V::unpack(ldg16_ordered(static_cast<const T*>(a.gamma) + int64_t(v) * E), g);
+          if (ln && a.beta) {
+            V::unpack(ldg16_ordered(static_cast<const T*>(a.beta) + int64_t(v) * E), b);
+          } else {
+#pragma unroll
+            for (int e = 0; e < E; ++e) b[e] = 0.0f;
+          }
+#pragma unroll
+          for (int e = 0; e < E; ++e) {
+            const float gain = a.zero_centered_gamma ? 1.0f + g[e] : g[e];
+            y[e] = (xv[e] - mean) * rs * gain + b[e];
+            amax = fmaxf(amax, fabsf(y[e]));
+          }
+          if (cs.store) cast_store<E>(a.out, row * a.H + int64_t(v) * E, y, cs);
+        }
+      }
+    }
+  }
+  amax = warp_max(amax);
+  if (lane == 0 && a.cast.amax_out) atomic_max_nonneg(a.cast.amax_out, amax);
+}
+
+template <typename T>
+te_status launch_fwd_smem(const NormFwdArgs& a, cudaStream_t s);
+
+template <typename T, int NV>
+te_status launch_fwd_reg(const NormFwdArgs& a, cudaStream_t s) {
+  const int warps = 8;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, norm_fwd_reg_kernel<T, NV>,
+                                                    warps * 32, 0) != cudaSuccess || per_sm < 1)
+    per_sm = 1;
+  const int64_t needed = ceil_div(a.M, warps);
+  const int64_t cap = int64_t(num_sms()) * per_sm;
+  const unsigned grid = unsigned(needed < cap ? needed : cap);
+  norm_fwd_reg_kernel<T, NV><<<grid, warps * 32, 0, s>>>(a);
+  return cudaGetLastError() == cudaSuccess ? TE_OK : TE_ERR_CUDA;
+}
+
 template <typename T>
 te_status launch_fwd_t(const NormFwdArgs& a, cudaStream_t s) {
+  constexpr int E = Vec16<T>::N;
+  const int64_t per_lane = ceil_div(a.H / E, 32);
+  if (per_lane <= 1) return launch_fwd_reg<T, 1>(a, s);
+  if (per_lane <= 2) return launch_fwd_reg<T, 2>(a, s);
+  if (per_lane <= 4) return launch_fwd_reg<T, 4>(a, s);
+  if (per_lane <= 8) return launch_fwd_reg<T, 8>(a, s);
+  if (per_lane <= 16) return launch_fwd_reg<T, 16>(a, s);
+  return launch_fwd_smem<T>(a, s);
+}
+
+// Longer rows: streamed through per-warp shared-memory double buffers (norm_fwd_kernel).
+template <typename T>
+te_status launch_fwd_smem(const NormFwdArgs& a, cudaStream_t s) {
   const uint32_t row_bytes = uint32_t(a.H * sizeof(T));
   int warps = int(kFwdSmemBudget / (2 * size_t(row_bytes)));
   if (warps < 1) return TE_ERR_UNSUPPORTED;
@@ -180,73 +293,111 @@ te_status launch_fwd_t(const NormFwdArgs& a, cudaStream_t s) {
 
 constexpr int kBwdThreads = 256;
 constexpr int kBwdWarps = kBwdThreads / 32;
+constexpr int kBwdRows = 4;  // rows per CTA between two barriers, for rows of <= 4 KB
 
+// Rows per barrier for NV vectors per thread (the first pass holds the group's x and dz in
+// registers).
+__host__ __device__ constexpr int bwd_rows(int nv) { return nv >= 4 ? 2 : 4; }
+
+// One CTA per group of kBwdRows rows at a time (persistent over groups).  Each row's dx needs
+// two row sums; the CTA reduces the sums of all its rows with one barrier.  dgamma / dbeta
+// accumulate per thread in registers over every row the CTA visits.
 template <typename T, int NV>
-__global__ void __launch_bounds__(kBwdThreads) norm_bwd_kernel(NormBwdArgs a) {
+__global__ void __launch_bounds__(kBwdThreads, 2) norm_bwd_kernel(NormBwdArgs a) {
   using V = Vec16<T>;
   constexpr int E = V::N;
-  __shared__ float red[2][kBwdWarps][2];
+  constexpr int R = bwd_rows(NV);
+  __shared__ float red[2][kBwdWarps][R][2];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nvec = int(a.H / E);
   const float inv_h = 1.0f / float(a.H);
   const bool ln = a.norm_type == TE_LAYERNORM;
-  float g[NV][E], accg[NV][E], accb[NV][E];
+  const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+  uint4 graw[NV];
+  float accg[NV][E], accb[NV][E];
 #pragma unroll
   for (int i = 0; i < NV; ++i) {
     const int v = tid + i * kBwdThreads;
+    graw[i] = v < nvec ? __ldg(reinterpret_cast<const uint4*>(static_cast<const T*>(a.gamma)) + v) : zero;
 #pragma unroll
-    for (int e = 0; e < E; ++e) { accg[i][e] = 0.0f; accb[i][e] = 0.0f; g[i][e] = 0.0f; }
-    if (v < nvec) {
-      V::load(a.gamma, int64_t(v) * E, g[i]);
-      if (a.zero_centered_gamma)
-#pragma unroll
-        for (int e = 0; e < E; ++e) g[i][e] += 1.0f;
-    }
+    for (int e = 0; e < E; ++e) { accg[i][e] = 0.0f; accb[i][e] = 0.0f; }
   }
+  const float gshift = a.zero_centered_gamma ? 1.0f : 0.0f;
   int parity = 0;
-  for (int64_t row = blockIdx.x; row < a.M; row += gridDim.x, parity ^= 1) {
-    const float mu = ln ? a.mu[row] : 0.0f;
-    const float rs = a.rsigma[row];
-    float xh[NV][E], dz[NV][E];
-    float s1 = 0.0f, s2 = 0.0f;
+  for (int64_t r0 = int64_t(blockIdx.x) * R; r0 < a.M; r0 += int64_t(gridDim.x) * R, parity ^= 1) {
+    uint4 rx[R][NV], rdz[R][NV];
+    float mu[R], rs[R];
 #pragma unroll
-    for (int i = 0; i < NV; ++i) {
-      const int v = tid + i * kBwdThreads;
-      if (v < nvec) {
-        V::load(a.x, row * a.H + int64_t(v) * E, xh[i]);
-        V::load(a.dz, row * a.H + int64_t(v) * E, dz[i]);
+    for (int j = 0; j < R; ++j) {
+      const int64_t row = r0 + j;
+      const bool in = row < a.M;
+      mu[j] = (in && ln) ? a.mu[row] : 0.0f;
+      rs[j] = in ? a.rsigma[row] : 0.0f;
 #pragma unroll
-        for (int e = 0; e < E; ++e) {
-          xh[i][e] = (xh[i][e] - mu) * rs;
-          const float dyg = dz[i][e] * g[i][e];
-          s1 += dyg;
-          s2 += dyg * xh[i][e];
-        }
+      for (int i = 0; i < NV; ++i) {
+        const int v = tid + i * kBwdThreads;
+        const bool ok = in && v < nvec;
+        rx[j][i] = ok ? __ldg(reinterpret_cast<const uint4*>(static_cast<const T*>(a.x) + row * a.H) + v) : zero;
+        rdz[j][i] = ok ? __ldg(reinterpret_cast<const uint4*>(static_cast<const T*>(a.dz) + row * a.H) + v) : zero;
       }
     }
-    s1 = warp_sum(s1);
-    s2 = warp_sum(s2);
-    if (lane == 0) { red[parity][warp][0] = s1; red[parity][warp][1] = s2; }
-    __syncthreads();
-    s1 = 0.0f; s2 = 0.0f;
 #pragma unroll
-    for (int w = 0; w < kBwdWarps; ++w) { s1 += red[parity][w][0]; s2 += red[parity][w][1]; }
-    const float m1 = ln ? s1 * inv_h : 0.0f;
-    const float m2 = s2 * inv_h;
+    for (int j = 0; j < R; ++j) {
+      float s1 = 0.0f, s2 = 0.0f;
 #pragma unroll
-    for (int i = 0; i < NV; ++i) {
-      const int v = tid + i * kBwdThreads;
-      if (v < nvec) {
-        float dx[E];
+      for (int i = 0; i < NV; ++i) {
+        float xv[E], dz[E], g[E];
+        V::unpack(rx[j][i], xv);
+        V::unpack(rdz[j][i], dz);
+        V::unpack(graw[i], g);
 #pragma unroll
         for (int e = 0; e < E; ++e) {
-          dx[e] = rs * (dz[i][e] * g[i][e] - m1 - xh[i][e] * m2);
-          accg[i][e] += dz[i][e] * xh[i][e];
-          accb[i][e] += dz[i][e];
+          const float dyg = dz[e] * (g[e] + gshift);
+          s1 += dyg;
+          s2 += dyg * ((xv[e] - mu[j]) * rs[j]);
         }
-        CastState cs;
-        cs.out_dtype = a.dtype;
-        cast_store<E>(a.dx, row * a.H + int64_t(v) * E, dx, cs);
+      }
+      s1 = warp_sum(s1);
+      s2 = warp_sum(s2);
+      if (lane == 0) {
+        red[parity][warp][j][0] = s1;
+        red[parity][warp][j][1] = s2;
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < R; ++j) {
+      const int64_t row = r0 + j;
+      if (row >= a.M) break;
+      float s1 = 0.0f, s2 = 0.0f;
+#pragma unroll
+      for (int w = 0; w < kBwdWarps; ++w) {
+        s1 += red[parity][w][j][0];
+        s2 += red[parity][w][j][1];
+      }
+      const float m1 = ln ? s1 * inv_h : 0.0f;
+      const float m2 = s2 * inv_h;
+#pragma unroll
+      for (int i = 0; i < NV; ++i) {
+        const int v = tid + i * kBwdThreads;
+        if (v < nvec) {
+          // x and dz come again from cache (L1/L2): keeping the group's rows in registers
+          // across the barrier would spill.
+          float xv[E], dz[E], g[E], dx[E];
+          V::unpack(ldg16_ordered(static_cast<const T*>(a.x) + row * a.H + int64_t(v) * E), xv);
+          V::unpack(ldg16_ordered(static_cast<const T*>(a.dz) + row * a.H + int64_t(v) * E), dz);
+          V::unpack(graw[i], g);
+#pragma unroll
+          for (int e = 0; e < E; ++e) {
+            const float xh = (xv[e] - mu[j]) * rs[j];
+            dx[e] = rs[j] * (dz[e] * (g[e] + gshift) - m1 - xh * m2);
+            accg[i][e] += dz[e] * xh;
+            accb[i][e] += dz[e];
+          }
+          CastState cs;
+          cs.out_dtype = a.dtype;
+          cast_store<E>(a.dx, row * a.H + int64_t(v) * E, dx, cs);
+        }
       }
     }
   }
@@ -279,7 +430,12 @@ __global__ void norm_bwd_reduce_kernel(const float* partials, int chunks, int64_
   if (dbeta) dbeta[j] = sb;
 }
 
-int bwd_chunks(int64_t M) { return int(M < int64_t(num_sms()) * 4 ? M : int64_t(num_sms()) * 4); }
+int bwd_chunks(int64_t M) {
+  // enough row groups for the smallest group size (one row), capped at the resident CTAs
+  const int64_t groups = M;
+  const int64_t resident = int64_t(num_sms()) * 2;
+  return int(groups < resident ? groups : resident);
+}
 
 template <typename T, int NV>
 te_status launch_bwd_t(const NormBwdArgs& a, cudaStream_t s) {
