@@ -210,6 +210,10 @@ def bandwidth_kernels(args, dev, peaks):
     da = random_tensor((Mb, F), device=dev, seed=4)
     a = torch.empty(Mb, F, dtype=torch.bfloat16, device=dev)
     run("act_lu_gelu_bf16", lambda: te.te_act_lu(h, "gelu", a), Mb * F * 4)
+    # calibration points on the same tensors (library code, not part of this framework)
+    run("torch_copy_bf16", lambda: a.copy_(h), Mb * F * 4)
+    run("torch_gelu_tanh_bf16", lambda: torch.nn.functional.gelu(h, approximate="tanh"),
+        Mb * F * 4)
     del a
     dh = torch.empty(Mb, F, dtype=torch.uint8, device=dev)
     db = torch.empty(F, dtype=torch.float32, device=dev)

@@ -121,4 +121,34 @@ struct Vec16<float> {
   }
 };
 
+// A 16-byte vector of T as packed fp32 pairs (4 pairs of bf16, 2 pairs of fp32).  The bf16
+// expansion is volatile so that a packed row held in registers is re-expanded on each pass
+// instead of being kept expanded.
+template <typename T>
+struct Pairs;
+
+template <>
+struct Pairs<__nv_bfloat16> {
+  static constexpr int P = 4;
+  __device__ __forceinline__ static void get(const uint4& u, f32x2 (&p)[4]) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float lo, hi;
+      asm volatile("shl.b32 %0, %1, 16;" : "=f"(lo) : "r"(w[i]));
+      asm volatile("and.b32 %0, %1, 0xFFFF0000;" : "=f"(hi) : "r"(w[i]));
+      p[i] = f2(lo, hi);
+    }
+  }
+};
+
+template <>
+struct Pairs<float> {
+  static constexpr int P = 2;
+  __device__ __forceinline__ static void get(const uint4& u, f32x2 (&p)[2]) {
+    p[0] = f2(__uint_as_float(u.x), __uint_as_float(u.y));
+    p[1] = f2(__uint_as_float(u.z), __uint_as_float(u.w));
+  }
+};
+
 }  // namespace te

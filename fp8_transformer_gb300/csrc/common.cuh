@@ -48,6 +48,56 @@ __device__ __forceinline__ float2 unpack_e4m3x2(uint16_t v) {
   return __half22float2(h);
 }
 
+// ------------------------------------------------------------------ packed fp32 pairs -----
+// sm_100+ executes two IEEE fp32 operations per f32x2 instruction (round to nearest, no
+// flush-to-zero); the bandwidth-bound kernels run their arithmetic on such pairs.
+
+using f32x2 = unsigned long long;
+
+__device__ __forceinline__ f32x2 f2(float lo, float hi) {
+  f32x2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ f32x2 f2s(float v) { return f2(v, v); }
+__device__ __forceinline__ float f2lo(f32x2 v) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+  return lo;
+}
+__device__ __forceinline__ float f2hi(f32x2 v) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+  return hi;
+}
+__device__ __forceinline__ f32x2 add2(f32x2 a, f32x2 b) {
+  f32x2 r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ f32x2 sub2(f32x2 a, f32x2 b) {
+  f32x2 r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ f32x2 mul2(f32x2 a, f32x2 b) {
+  f32x2 r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ f32x2 fma2(f32x2 a, f32x2 b, f32x2 c) {
+  f32x2 r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+// bf16x2 word -> fp32 pair (exact).
+__device__ __forceinline__ f32x2 bf16x2_f2(uint32_t w) {
+  return f2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+__device__ __forceinline__ float absmax2(float m, f32x2 v) {
+  return fmaxf(m, fmaxf(fabsf(f2lo(v)), fabsf(f2hi(v))));
+}
+
 // ------------------------------------------------------------------ activations -----------
 // Written from their definitions, in fp32.  The tanh-form GELU uses the identity
 // 0.5 * (1 + tanh(u)) = 1 / (1 + exp(-2u)), which is the same function but avoids the
@@ -114,6 +164,92 @@ __device__ __forceinline__ float act_fast(int act, float h) {
     case TE_GELU: return gelu_fast(h);
     case TE_SILU: return silu_fast(h);
     default: return h;
+  }
+}
+
+// Pairwise versions for the bandwidth-bound kernels.  exp(x) = 2^(x log2 e) on the hardware
+// exp2 approximation, 1/x on the hardware reciprocal approximation; arguments are clamped so
+// that no exp2 result overflows where a product with it follows.
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ float ex2_approx(float x) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+__device__ __forceinline__ float rcp_approx(float x) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+__device__ __forceinline__ f32x2 ex2_2(f32x2 a) {
+  return f2(ex2_approx(f2lo(a)), ex2_approx(f2hi(a)));
+}
+__device__ __forceinline__ f32x2 rcp2(f32x2 a) {
+  return f2(rcp_approx(f2lo(a)), rcp_approx(f2hi(a)));
+}
+__device__ __forceinline__ f32x2 min2s(f32x2 a, float m) {
+  return f2(fminf(f2lo(a), m), fminf(f2hi(a), m));
+}
+
+// logistic s(z) = 1 / (1 + exp(-z)) and e = exp(-z), with z clamped at -80 inside exp.
+__device__ __forceinline__ void sigmoid2(f32x2 z, f32x2& s, f32x2& e) {
+  e = ex2_2(min2s(mul2(z, f2s(-kLog2e)), 80.0f * kLog2e));
+  s = rcp2(add2(e, f2s(1.0f)));
+}
+
+__device__ __forceinline__ f32x2 gelu2(f32x2 h) {
+  const f32x2 u = mul2(h, fma2(mul2(h, h), f2s(kGeluK0 * kGeluK1), f2s(kGeluK0)));
+  f32x2 s, e;
+  sigmoid2(add2(u, u), s, e);
+  return mul2(h, s);
+}
+
+// gelu'(h) = s + 2 h sqrt(2/pi) (1 + 3 * 0.044715 h^2) s (1 - s), s = logistic(2u).
+__device__ __forceinline__ f32x2 dgelu2(f32x2 h) {
+  const f32x2 hh = mul2(h, h);
+  const f32x2 u = mul2(h, fma2(hh, f2s(kGeluK0 * kGeluK1), f2s(kGeluK0)));
+  f32x2 s, e;
+  sigmoid2(add2(u, u), s, e);
+  const f32x2 sn = mul2(e, s);  // 1 - s
+  const f32x2 q = mul2(h, fma2(hh, f2s(6.0f * kGeluK0 * kGeluK1), f2s(2.0f * kGeluK0)));
+  return fma2(q, mul2(s, sn), s);
+}
+
+__device__ __forceinline__ f32x2 silu2(f32x2 z) {
+  f32x2 s, e;
+  sigmoid2(z, s, e);
+  return mul2(z, s);
+}
+
+// silu'(z) = s (1 + z (1 - s)).
+__device__ __forceinline__ f32x2 dsilu2(f32x2 z) {
+  f32x2 s, e;
+  sigmoid2(z, s, e);
+  return mul2(s, fma2(z, mul2(e, s), f2s(1.0f)));
+}
+
+__device__ __forceinline__ f32x2 relu2(f32x2 h) {
+  return f2(fmaxf(f2lo(h), 0.0f), fmaxf(f2hi(h), 0.0f));
+}
+__device__ __forceinline__ f32x2 drelu2(f32x2 h) {
+  return f2(f2lo(h) > 0.0f ? 1.0f : 0.0f, f2hi(h) > 0.0f ? 1.0f : 0.0f);
+}
+
+__device__ __forceinline__ f32x2 act2(int act, f32x2 h) {
+  switch (act) {
+    case TE_RELU: return relu2(h);
+    case TE_GELU: return gelu2(h);
+    case TE_SILU: return silu2(h);
+    default: return h;
+  }
+}
+__device__ __forceinline__ f32x2 dact2(int act, f32x2 h) {
+  switch (act) {
+    case TE_RELU: return drelu2(h);
+    case TE_GELU: return dgelu2(h);
+    case TE_SILU: return dsilu2(h);
+    default: return f2s(1.0f);
   }
 }
 

@@ -51,53 +51,55 @@ __global__ void __launch_bounds__(kEwThreads) quantize_kernel(QuantizeArgs a) {
 
 // ------------------------------------------------------------------ act_lu ----------------
 
-constexpr int kActUnroll = 4;  // vectors in flight per thread
+constexpr int kActWarps = 8;
+constexpr int kActRows = 32;    // rows per CTA
+constexpr int kActUnroll = 4;   // rows in flight per warp
 
+// Each CTA owns a strip of 32 x 16-byte output vectors (one per lane) and kActRows rows; its
+// warps take rows in turn, kActUnroll at a time, so every load is a 512-byte coalesced row
+// segment and no index needs a division.
 template <typename T>
-__global__ void __launch_bounds__(kEwThreads) act_lu_kernel(ActArgs a) {
+__global__ void __launch_bounds__(kActWarps * 32, 3) act_lu_kernel(ActArgs a) {
   using V = Vec16<T>;
+  using PR = Pairs<T>;
   constexpr int E = V::N;
   const CastState cs = cast_begin(a.cast);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const bool gated = a.act == TE_SWIGLU;
   const int64_t n_out = gated ? a.N_in / 2 : a.N_in;
-  const int64_t vec_per_row = n_out / E;
-  const int64_t nvec = a.M * vec_per_row;
-  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  const int64_t col = (int64_t(blockIdx.x) * 32 + lane) * E;
+  const int64_t r0 = int64_t(blockIdx.y) * kActRows;
+  const int64_t r1 = r0 + kActRows < a.M ? r0 + kActRows : a.M;
   const T* x = static_cast<const T*>(a.x);
   const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
   float amax = 0.0f;
-  for (int64_t v0 = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; v0 < nvec;
-       v0 += kActUnroll * stride) {
-    uint4 rg[kActUnroll], rl[kActUnroll];
+  if (col < n_out) {
+    for (int64_t rb = r0 + warp; rb < r1; rb += kActUnroll * kActWarps) {
+      uint4 rg[kActUnroll], rl[kActUnroll];
 #pragma unroll
-    for (int j = 0; j < kActUnroll; ++j) {
-      const int64_t v = v0 + j * stride;
-      const int64_t r = v / vec_per_row;
-      const int64_t c = (v - r * vec_per_row) * E;
-      const bool in = v < nvec;
-      rg[j] = in ? __ldg(reinterpret_cast<const uint4*>(x + r * a.N_in + c)) : zero;
-      rl[j] = (in && gated) ? __ldg(reinterpret_cast<const uint4*>(x + r * a.N_in + n_out + c)) : zero;
-    }
-#pragma unroll
-    for (int j = 0; j < kActUnroll; ++j) {
-      const int64_t v = v0 + j * stride;
-      if (v >= nvec) break;
-      const int64_t r = v / vec_per_row;
-      const int64_t c = (v - r * vec_per_row) * E;
-      float h[E], y[E];
-      V::unpack(rg[j], h);
-      if (gated) {
-        float l[E];
-        V::unpack(rl[j], l);
-#pragma unroll
-        for (int e = 0; e < E; ++e) y[e] = silu_fast(h[e]) * l[e];
-      } else {
-#pragma unroll
-        for (int e = 0; e < E; ++e) y[e] = act_fast(a.act, h[e]);
+      for (int j = 0; j < kActUnroll; ++j) {
+        const int64_t r = rb + int64_t(j) * kActWarps;
+        const bool in = r < r1;
+        rg[j] = in ? __ldg(reinterpret_cast<const uint4*>(x + r * a.N_in + col)) : zero;
+        rl[j] = (in && gated) ? __ldg(reinterpret_cast<const uint4*>(x + r * a.N_in + n_out + col)) : zero;
       }
 #pragma unroll
-      for (int e = 0; e < E; ++e) amax = fmaxf(amax, fabsf(y[e]));
-      if (cs.store) cast_store<E>(a.out, r * n_out + c, y, cs);
+      for (int j = 0; j < kActUnroll; ++j) {
+        const int64_t r = rb + int64_t(j) * kActWarps;
+        if (r >= r1) break;
+        f32x2 hp[PR::P], lp[PR::P];
+        PR::get(rg[j], hp);
+        if (gated) PR::get(rl[j], lp);
+        float y[E];
+#pragma unroll
+        for (int p = 0; p < PR::P; ++p) {
+          const f32x2 yy = gated ? mul2(silu2(hp[p]), lp[p]) : act2(a.act, hp[p]);
+          amax = absmax2(amax, yy);
+          y[2 * p] = f2lo(yy);
+          y[2 * p + 1] = f2hi(yy);
+        }
+        if (cs.store) cast_store<E>(a.out, r * n_out + col, y, cs);
+      }
     }
   }
   block_amax_commit(amax, a.cast.amax_out);
@@ -125,9 +127,11 @@ __global__ void __launch_bounds__(kDactWarps * 32, 3) dact_dbias_kernel(DactArgs
   const bool valid = col < n_out;
   const int64_t r0 = int64_t(blockIdx.y) * kDactRows;
   const int64_t r1 = r0 + kDactRows < a.M ? r0 + kDactRows : a.M;
-  float acc1[E], acc2[E];
+  using PR = Pairs<T>;
+  constexpr int P = PR::P;
+  f32x2 acc1[P], acc2[P];
 #pragma unroll
-  for (int e = 0; e < E; ++e) { acc1[e] = 0.0f; acc2[e] = 0.0f; }
+  for (int p = 0; p < P; ++p) { acc1[p] = f2s(0.0f); acc2[p] = f2s(0.0f); }
   float amax = 0.0f;
   const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
   if (valid) {
@@ -146,19 +150,28 @@ __global__ void __launch_bounds__(kDactWarps * 32, 3) dact_dbias_kernel(DactArgs
       for (int j = 0; j < kDactUnroll; ++j) {
         const int64_t r = rb + int64_t(j) * kDactWarps;
         if (r >= r1) break;
-        float dy[E], h[E];
-        V::unpack(rdy[j], dy);
-        V::unpack(rx[j], h);
+        f32x2 dyp[P], hp[P];
+        PR::get(rdy[j], dyp);
+        PR::get(rx[j], hp);
         if (gated) {
-          float l[E], dg[E], dl[E];
-          V::unpack(rl[j], l);
+          f32x2 lp[P];
+          PR::get(rl[j], lp);
+          float dg[E], dl[E];
 #pragma unroll
-          for (int e = 0; e < E; ++e) {
-            dg[e] = dy[e] * l[e] * dsilu_fast(h[e]);
-            dl[e] = dy[e] * silu_fast(h[e]);
-            acc1[e] += dg[e];
-            acc2[e] += dl[e];
-            amax = fmaxf(amax, fmaxf(fabsf(dg[e]), fabsf(dl[e])));
+          for (int p = 0; p < P; ++p) {
+            f32x2 sg, eg;
+            sigmoid2(hp[p], sg, eg);
+            // d_gate = dy * lin * silu'(gate), d_lin = dy * silu(gate)
+            const f32x2 dsil = mul2(sg, fma2(hp[p], mul2(eg, sg), f2s(1.0f)));
+            const f32x2 g2 = mul2(mul2(dyp[p], lp[p]), dsil);
+            const f32x2 l2 = mul2(dyp[p], mul2(hp[p], sg));
+            acc1[p] = add2(acc1[p], g2);
+            acc2[p] = add2(acc2[p], l2);
+            amax = absmax2(absmax2(amax, g2), l2);
+            dg[2 * p] = f2lo(g2);
+            dg[2 * p + 1] = f2hi(g2);
+            dl[2 * p] = f2lo(l2);
+            dl[2 * p + 1] = f2hi(l2);
           }
           if (cs.store) {
             cast_store<E>(a.dx, r * a.N_in + col, dg, cs);
@@ -167,10 +180,12 @@ __global__ void __launch_bounds__(kDactWarps * 32, 3) dact_dbias_kernel(DactArgs
         } else {
           float d[E];
 #pragma unroll
-          for (int e = 0; e < E; ++e) {
-            d[e] = ident ? dy[e] : dy[e] * dact_fast(a.act, h[e]);
-            acc1[e] += d[e];
-            amax = fmaxf(amax, fabsf(d[e]));
+          for (int p = 0; p < P; ++p) {
+            const f32x2 dd = ident ? dyp[p] : mul2(dyp[p], dact2(a.act, hp[p]));
+            acc1[p] = add2(acc1[p], dd);
+            amax = absmax2(amax, dd);
+            d[2 * p] = f2lo(dd);
+            d[2 * p + 1] = f2hi(dd);
           }
           if (cs.store && a.dx) cast_store<E>(a.dx, r * a.N_in + col, d, cs);
         }
@@ -179,9 +194,11 @@ __global__ void __launch_bounds__(kDactWarps * 32, 3) dact_dbias_kernel(DactArgs
   }
   if (a.dbias) {
 #pragma unroll
-    for (int e = 0; e < E; ++e) {
-      red[warp][0][lane * E + e] = acc1[e];
-      red[warp][1][lane * E + e] = acc2[e];
+    for (int p = 0; p < P; ++p) {
+      red[warp][0][lane * E + 2 * p] = f2lo(acc1[p]);
+      red[warp][0][lane * E + 2 * p + 1] = f2hi(acc1[p]);
+      red[warp][1][lane * E + 2 * p] = f2lo(acc2[p]);
+      red[warp][1][lane * E + 2 * p + 1] = f2hi(acc2[p]);
     }
     __syncthreads();
     // 256 threads finish the strip's column sums, each over the 8 warps in warp order.
@@ -263,10 +280,14 @@ te_status launch_quantize(const QuantizeArgs& a, cudaStream_t s) {
 te_status launch_act_lu(const ActArgs& a, cudaStream_t s) {
   ProfileScope prof(TE_KERNEL_ACT_LU, s);
   const int64_t n_out = a.act == TE_SWIGLU ? a.N_in / 2 : a.N_in;
+  if (a.M == 0) return TE_OK;
+  const int E = a.x_dtype == TE_BF16 ? 8 : 4;
+  if (ceil_div(a.M, kActRows) > 65535) return TE_ERR_UNSUPPORTED;
+  dim3 grid(unsigned(ceil_div(n_out, 32 * E)), unsigned(ceil_div(a.M, kActRows)));
   if (a.x_dtype == TE_BF16) {
-    act_lu_kernel<__nv_bfloat16><<<ew_grid(a.M * n_out / 8), kEwThreads, 0, s>>>(a);
+    act_lu_kernel<__nv_bfloat16><<<grid, kActWarps * 32, 0, s>>>(a);
   } else if (a.x_dtype == TE_F32) {
-    act_lu_kernel<float><<<ew_grid(a.M * n_out / 4), kEwThreads, 0, s>>>(a);
+    act_lu_kernel<float><<<grid, kActWarps * 32, 0, s>>>(a);
   } else {
     return TE_ERR_UNSUPPORTED;
   }

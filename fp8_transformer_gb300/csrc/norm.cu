@@ -152,19 +152,44 @@ __global__ void __launch_bounds__(kFwdMaxWarps * 32) norm_fwd_kernel(NormFwdArgs
 }
 
 // Rows of up to 8 KB: one warp per row with the row resident in registers as packed 16-byte
-// vectors, persistent over rows, 2+ CTAs per SM so that many rows are in flight per SM.
-// Statistics take one pass, shifted by the row's first element (mean = x0 + E[x - x0],
-// var = E[(x - x0)^2] - E[x - x0]^2), which avoids the cancellation of the unshifted form.
+// vectors, persistent over rows, 2+ CTAs per SM so that many rows are in flight per SM.  The
+// gain (gamma, or 1 + gamma) and beta are expanded to fp32 in shared memory once per CTA, and
+// the arithmetic runs on packed fp32 pairs.  Statistics take one pass, shifted by the row's
+// first element (mean = x0 + E[x - x0], var = E[(x - x0)^2] - E[x - x0]^2), which avoids the
+// cancellation of the unshifted form.
 template <typename T, int NV>
 __global__ void __launch_bounds__(256, 2) norm_fwd_reg_kernel(NormFwdArgs a) {
   using V = Vec16<T>;
+  using PR = Pairs<T>;
   constexpr int E = V::N;
+  constexpr int P = PR::P;
+  // gain (gamma, or 1 + gamma) and beta in fp32, laid out as float4 blocks so that the lanes of
+  // a warp, which own consecutive 16-byte input vectors, read consecutive float4s:
+  // element e of vector v sits in block (e / 4) * nvec + v, slot e % 4.
+  extern __shared__ float4 params[];
+  const int nvec = int(a.H / E);
+  constexpr int Q = E / 4;
+  float4* gain4 = params;
+  float4* beta4 = params + Q * nvec;
+  const bool ln = a.norm_type == TE_LAYERNORM;
+  {
+    const float shift = a.zero_centered_gamma ? 1.0f : 0.0f;
+    const T* g = static_cast<const T*>(a.gamma);
+    const T* b = static_cast<const T*>(a.beta);
+    float* gf = reinterpret_cast<float*>(gain4);
+    float* bf = reinterpret_cast<float*>(beta4);
+    for (int64_t j = threadIdx.x; j < a.H; j += blockDim.x) {
+      const int64_t v = j / E, e = j % E;
+      const int64_t slot = ((e / 4) * nvec + v) * 4 + (e % 4);
+      gf[slot] = float(g[j]) + shift;
+      bf[slot] = (ln && b) ? float(b[j]) : 0.0f;
+    }
+  }
+  __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nwarps = blockDim.x >> 5;
   const CastState cs = cast_begin(a.cast);
-  const int nvec = int(a.H / E);
   const float inv_h = 1.0f / float(a.H);
-  const bool ln = a.norm_type == TE_LAYERNORM;
   float amax = 0.0f;
   for (int64_t row = int64_t(blockIdx.x) * nwarps + warp; row < a.M;
        row += int64_t(gridDim.x) * nwarps) {
@@ -177,52 +202,58 @@ __global__ void __launch_bounds__(256, 2) norm_fwd_reg_kernel(NormFwdArgs a) {
     }
     float x0 = 0.0f;
     if (ln) {
-      float first[E];
-      V::unpack(raw[0], first);
-      x0 = __shfl_sync(0xffffffffu, first[0], 0);
+      f32x2 first[P];
+      PR::get(raw[0], first);
+      x0 = __shfl_sync(0xffffffffu, f2lo(first[0]), 0);
     }
-    float s1 = 0.0f, s2 = 0.0f;
+    const f32x2 x02 = f2s(x0);
+    f32x2 s1 = f2s(0.0f), s2 = f2s(0.0f);
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
       if (lane + i * 32 < nvec) {
-        float xv[E];
-        V::unpack(raw[i], xv);
+        f32x2 xp[P];
+        PR::get(raw[i], xp);
 #pragma unroll
-        for (int e = 0; e < E; ++e) {
-          const float d = xv[e] - x0;
-          s1 += d;
-          s2 += d * d;
+        for (int p = 0; p < P; ++p) {
+          const f32x2 d = sub2(xp[p], x02);
+          s1 = add2(s1, d);
+          s2 = fma2(d, d, s2);
         }
       }
     }
-    s1 = warp_sum(s1) * inv_h;
-    s2 = warp_sum(s2) * inv_h;
-    const float mean = ln ? x0 + s1 : 0.0f;
-    const float var = ln ? fmaxf(s2 - s1 * s1, 0.0f) : s2;
+    const float m1 = warp_sum(f2lo(s1) + f2hi(s1)) * inv_h;
+    const float m2 = warp_sum(f2lo(s2) + f2hi(s2)) * inv_h;
+    const float mean = ln ? x0 + m1 : 0.0f;
+    const float var = ln ? fmaxf(m2 - m1 * m1, 0.0f) : m2;
     const float rs = 1.0f / sqrtf(var + a.eps);
     if (lane == 0) {
       if (a.mu) a.mu[row] = mean;
       if (a.rsigma) a.rsigma[row] = rs;
     }
     if (cs.store || a.cast.amax_out) {
+      const f32x2 mean2 = f2s(mean), rs2 = f2s(rs);
 #pragma unroll
       for (int i = 0; i < NV; ++i) {
         const int v = lane + i * 32;
         if (v < nvec) {
-          float xv[E], g[E], b[E], y[E];
-          V::unpack(raw[i], xv);
-          V::unpack(ldg16_ordered(static_cast<const T*>(a.gamma) + int64_t(v) * E), g);
-          if (ln && a.beta) {
-            V::unpack(ldg16_ordered(static_cast<const T*>(a.beta) + int64_t(v) * E), b);
-          } else {
+          f32x2 xp[P], gp[P], bp[P];
+          PR::get(raw[i], xp);
 #pragma unroll
-            for (int e = 0; e < E; ++e) b[e] = 0.0f;
+          for (int q = 0; q < Q; ++q) {
+            const float4 g4 = gain4[q * nvec + v];
+            const float4 b4 = beta4[q * nvec + v];
+            gp[2 * q] = f2(g4.x, g4.y);
+            gp[2 * q + 1] = f2(g4.z, g4.w);
+            bp[2 * q] = f2(b4.x, b4.y);
+            bp[2 * q + 1] = f2(b4.z, b4.w);
           }
+          float y[E];
 #pragma unroll
-          for (int e = 0; e < E; ++e) {
-            const float gain = a.zero_centered_gamma ? 1.0f + g[e] : g[e];
-            y[e] = (xv[e] - mean) * rs * gain + b[e];
-            amax = fmaxf(amax, fabsf(y[e]));
+          for (int p = 0; p < P; ++p) {
+            const f32x2 yy = fma2(sub2(xp[p], mean2), mul2(gp[p], rs2), bp[p]);
+            amax = absmax2(amax, yy);
+            y[2 * p] = f2lo(yy);
+            y[2 * p + 1] = f2hi(yy);
           }
           if (cs.store) cast_store<E>(a.out, row * a.H + int64_t(v) * E, y, cs);
         }
@@ -239,14 +270,15 @@ te_status launch_fwd_smem(const NormFwdArgs& a, cudaStream_t s);
 template <typename T, int NV>
 te_status launch_fwd_reg(const NormFwdArgs& a, cudaStream_t s) {
   const int warps = 8;
+  const size_t smem = size_t(a.H) * 2 * sizeof(float);  // fp32 gain and beta
   int per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, norm_fwd_reg_kernel<T, NV>,
-                                                    warps * 32, 0) != cudaSuccess || per_sm < 1)
+                                                    warps * 32, smem) != cudaSuccess || per_sm < 1)
     per_sm = 1;
   const int64_t needed = ceil_div(a.M, warps);
   const int64_t cap = int64_t(num_sms()) * per_sm;
   const unsigned grid = unsigned(needed < cap ? needed : cap);
-  norm_fwd_reg_kernel<T, NV><<<grid, warps * 32, 0, s>>>(a);
+  norm_fwd_reg_kernel<T, NV><<<grid, warps * 32, smem, s>>>(a);
   return cudaGetLastError() == cudaSuccess ? TE_OK : TE_ERR_CUDA;
 }
 
