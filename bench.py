@@ -171,6 +171,36 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def cublas_calibration(M, H, F, gated, dev, steps, flush):
+    """cuBLAS (torch.matmul / torch._scaled_mm) on the two GEMM shapes of the step: context for
+    the tensor-core fractions, not part of this framework's path."""
+    import torch
+    F1 = 2 * F if gated else F
+    res = {}
+    a1 = torch.randn(M, H, device=dev, dtype=torch.bfloat16)
+    b1 = torch.randn(H, F1, device=dev, dtype=torch.bfloat16)
+    a2 = torch.randn(M, F, device=dev, dtype=torch.bfloat16)
+    b2 = torch.randn(F, H, device=dev, dtype=torch.bfloat16)
+    for name, a, b in (("gemm1_bf16", a1, b1), ("gemm2_bf16", a2, b2)):
+        fn = lambda: torch.matmul(a, b)
+        fn()
+        ms = statistics.mean(time_steps(fn, steps, flush))
+        res[name] = 2.0 * a.shape[0] * a.shape[1] * b.shape[1] / (ms / 1e3) / 1e12
+    try:
+        one = torch.ones((), device=dev)
+        for name, a, b in (("gemm1_fp8", a1, b1), ("gemm2_fp8", a2, b2)):
+            a8 = a.to(torch.float8_e4m3fn)
+            b8 = b.t().contiguous().to(torch.float8_e4m3fn).t()  # column-major second operand
+            fn = lambda: torch._scaled_mm(a8, b8, scale_a=one, scale_b=one,
+                                          out_dtype=torch.bfloat16)
+            fn()
+            ms = statistics.mean(time_steps(fn, steps, flush))
+            res[name] = 2.0 * a.shape[0] * a.shape[1] * b.shape[1] / (ms / 1e3) / 1e12
+    except Exception as e:  # pragma: no cover - depends on the installed torch
+        res["fp8_error"] = str(e)[:120]
+    return res
+
+
 def bandwidth_kernels(args, dev, peaks):
     """GB/s of the bandwidth-bound kernels alone (profiling aid): norm forward at the Llama
     shape (bf16 and E4M3 out), and at the GPT backward shape the activation recompute, the
@@ -334,10 +364,13 @@ def run_ours(args, rank, world, local_rank):
     launches = sum(n for _, n in prof_bf16.values())
     if args.kernels_only:
         if rank == 0:
-            print(json.dumps({"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
-                              "ms_per_step": ms_step, "fp8_ms_per_step": ms_step_fp8,
-                              "value_fp8": value_fp8, "tokens": M, "kernels_only": True,
-                              "profile_bf16": prof_bf16, "profile_fp8": prof_fp8}), flush=True)
+            line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+                    "ms_per_step": ms_step, "fp8_ms_per_step": ms_step_fp8,
+                    "value_fp8": value_fp8, "tokens": M, "kernels_only": True,
+                    "profile_bf16": prof_bf16, "profile_fp8": prof_fp8}
+            if args.calibrate:
+                line["cublas"] = cublas_calibration(M, H, F, gated, dev, args.steps, flush)
+            print(json.dumps(line), flush=True)
         return
 
     # ---- end to end through the public call: pinned host input -> device -> host output
@@ -516,6 +549,8 @@ def main():
                     help="time the GPU steps only: no e2e, bandwidth kernels or CPU baseline")
     ap.add_argument("--bandwidth-only", action="store_true",
                     help="time only the bandwidth-bound kernels (profiling aid)")
+    ap.add_argument("--calibrate", action="store_true",
+                    help="with --kernels-only: also time cuBLAS on the same GEMM shapes")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     world = int(os.environ.get("WORLD_SIZE", "1"))

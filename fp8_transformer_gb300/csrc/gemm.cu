@@ -42,9 +42,10 @@ constexpr int STAGES = 4;
 constexpr int kRowBytes = 128;          // bytes of K per tile row per stage
 constexpr int A_STAGE = BM * kRowBytes; // 16 KB
 constexpr int B_STAGE = BN * kRowBytes; // 32 KB
-constexpr int kThreads = 192;
+constexpr int kEpiWarps = 8;               // two warps per TMEM lane quadrant
+constexpr int kThreads = 32 * (2 + kEpiWarps);  // producer, MMA, epilogue warps
 constexpr uint32_t kTmemCols = 512;
-constexpr int kGroupM = 8;              // m-tiles per raster group (L2 reuse of B)
+constexpr int64_t kRasterL2Bytes = 48ll << 20;  // A rows a raster group may keep in L2
 
 // Element kinds: 0 = bf16 (kind::f16), 1 = E4M3 (kind::f8f6f4), 2 = fp32 as tf32 (kind::tf32).
 template <int KIND>
@@ -56,6 +57,7 @@ template <> struct Kind<2> { static constexpr int esize = 4; static constexpr ui
 struct GemmDev {
   int64_t M, N, K;
   int num_m, num_n, num_kb;
+  int group_m;      // m-tiles per raster group
   int gated;
   int64_t F;        // gated: column offset of the linear half in B
   int epilogue, act;
@@ -163,12 +165,13 @@ struct Tile {
   int m, n;
 };
 
-// Raster groups of kGroupM m-tiles: consecutive tiles share B columns within a group.
-__device__ __forceinline__ Tile tile_of(int t, int num_m, int num_n) {
-  const int group_size = kGroupM * num_n;
+// Raster groups of group_m m-tiles, m fastest: the tiles in flight share B columns, and a
+// group's A rows stay in L2 while the group sweeps every n column.
+__device__ __forceinline__ Tile tile_of(int t, int num_m, int num_n, int group_m) {
+  const int group_size = group_m * num_n;
   const int group = t / group_size;
-  const int first_m = group * kGroupM;
-  const int gm = min(num_m - first_m, kGroupM);
+  const int first_m = group * group_m;
+  const int gm = min(num_m - first_m, group_m);
   const int in_group = t - group * group_size;
   return Tile{first_m + in_group % gm, in_group / gm};
 }
@@ -208,6 +211,19 @@ __device__ __forceinline__ void store_seg(void* base, int64_t off, const float (
                           pack_e4m3x4(w[12] * scale, w[13] * scale, w[14] * scale, w[15] * scale));
       }
   }
+}
+
+// The bias values of columns j and j + 1 (j even) as an fp32 pair.
+__device__ __forceinline__ f32x2 load_bias_pair(const void* bias, int dtype, int64_t j) {
+  if (dtype == TE_BF16)
+    return bf16x2_f2(__ldg(reinterpret_cast<const uint32_t*>(static_cast<const uint16_t*>(bias) + j)));
+  const float2 w = __ldg(reinterpret_cast<const float2*>(static_cast<const float*>(bias) + j));
+  return f2(w.x, w.y);
+}
+
+// Rounds both halves of a pair to bf16 (round to nearest even) and back to fp32.
+__device__ __forceinline__ f32x2 round_bf16_2(f32x2 v) {
+  return bf16x2_f2(pack_bf16x2(f2lo(v), f2hi(v)));
 }
 
 __device__ __forceinline__ void round_to(float (&v)[32], int dtype) {
@@ -251,7 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(smem_u32(&tfull[a]), 1);
-      mbar_init(smem_u32(&tempty[a]), 128);
+      mbar_init(smem_u32(&tempty[a]), 32 * kEpiWarps);
     }
     mbar_init(smem_u32(drain), 1);
     *abort_flag = 0;
@@ -280,11 +296,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       int stage = 0;
       uint32_t phase = 0, issued = 0, last_parity = 0;
       for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
-        const Tile tl = tile_of(t, g.num_m, g.num_n);
+        const Tile tl = tile_of(t, g.num_m, g.num_n, g.group_m);
         const int m0 = tl.m * BM;
         bool ok = true;
         for (int kb = 0; kb < g.num_kb; ++kb) {
-          if (!wait_bounded(smem_u32(&empty[stage]), phase ^ 1, abort_flag, &g_device_status, kWaitLimitNs, true)) {
+          if (!mbar_try_wait(smem_u32(&empty[stage]), phase ^ 1) &&
+              !wait_bounded(smem_u32(&empty[stage]), phase ^ 1, abort_flag, &g_device_status, kWaitLimitNs, true)) {
             ok = false;
             break;
           }
@@ -354,7 +371,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + uint32_t(acc * BN);
         for (int kb = 0; kb < g.num_kb; ++kb) {
-          if (!wait_bounded(smem_u32(&full[stage]), phase, abort_flag, &g_device_status, kWaitLimitNs, true)) {
+          if (!mbar_try_wait(smem_u32(&full[stage]), phase) &&
+              !wait_bounded(smem_u32(&full[stage]), phase, abort_flag, &g_device_status, kWaitLimitNs, true)) {
             ok = false;
             break;
           }
@@ -386,14 +404,18 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     }
   } else {
     // ----------------------------------------------------------- epilogue ---------------
+    // Warp w reads the TMEM lanes of quadrant (w % 4) and one half of the tile's columns.
     const int quad = warp & 3;  // TMEM lanes [32 * quad, 32 * quad + 32)
+    const int half = (warp - 2) >> 2;
     const int row_in_tile = quad * 32 + lane;
     float alpha = 1.0f;
     if (g.a_scale_inv) alpha *= *g.a_scale_inv;
     if (g.b_scale_inv) alpha *= *g.b_scale_inv;
+    const f32x2 alpha2 = f2s(alpha);
     const float out_scale = (g.d_dtype == TE_E4M3 && g.out_scale) ? *g.out_scale : 1.0f;
     if (blockIdx.x == 0 && threadIdx.x == 64 && g.out_scale_inv) *g.out_scale_inv = 1.0f / out_scale;
     const int64_t ldd = g.gated ? g.F : g.N;
+    const bool round_h = g.h_dtype == TE_BF16;
     float amax = 0.0f;
     int local = 0;
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++local) {
@@ -409,14 +431,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       }
       __syncwarp();
       tc_fence_after();
-      const Tile tl = tile_of(t, g.num_m, g.num_n);
+      const Tile tl = tile_of(t, g.num_m, g.num_n, g.group_m);
       const int64_t row = int64_t(tl.m) * BM + row_in_tile;
       const bool row_ok = row < g.M;
       const uint32_t taddr = tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(acc * BN);
       if (!g.gated) {
         const int64_t n0 = int64_t(tl.n) * BN;
+        constexpr int kChunks = BN / 32 / 2;  // per warp
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
+        for (int c = half * kChunks; c < (half + 1) * kChunks; ++c) {
           const int64_t col0 = n0 + c * 32;
           if (col0 >= g.N) break;
           const int count = g.N - col0 >= 32 ? 32 : int(g.N - col0);
@@ -425,15 +448,21 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           tmem_ld_wait();
           float v[32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            v[i] = __uint_as_float(r[i]) * alpha;
-            if (g.bias && i < count) v[i] += load_bias(g.bias, g.bias_dtype, col0 + i);
+          for (int p = 0; p < 16; ++p) {
+            f32x2 x = mul2(f2(__uint_as_float(r[2 * p]), __uint_as_float(r[2 * p + 1])), alpha2);
+            if (g.bias && 2 * p < count) x = add2(x, load_bias_pair(g.bias, g.bias_dtype, col0 + 2 * p));
+            if (g.epilogue == EPI_BIAS_ACT && round_h) x = round_bf16_2(x);
+            v[2 * p] = f2lo(x);
+            v[2 * p + 1] = f2hi(x);
           }
           if (g.epilogue == EPI_BIAS_ACT) {
-            round_to(v, g.h_dtype);
             if (g.saved_h && row_ok) store_seg(g.saved_h, row * g.N + col0, v, count, g.h_dtype, 1.0f);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = act_apply(g.act, v[i]);
+            for (int p = 0; p < 16; ++p) {
+              const f32x2 y = act2(g.act, f2(v[2 * p], v[2 * p + 1]));
+              v[2 * p] = f2lo(y);
+              v[2 * p + 1] = f2hi(y);
+            }
           }
           if (row_ok) {
 #pragma unroll
@@ -444,8 +473,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         }
       } else {
         const int64_t n0 = int64_t(tl.n) * (BN / 2);
+        constexpr int kChunks = BN / 64 / 2;  // per warp
 #pragma unroll 1
-        for (int c = 0; c < BN / 64; ++c) {
+        for (int c = half * kChunks; c < (half + 1) * kChunks; ++c) {
           const int64_t col0 = n0 + c * 32;
           if (col0 >= g.F) break;
           const int count = g.F - col0 >= 32 ? 32 : int(g.F - col0);
@@ -455,22 +485,32 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           tmem_ld_wait();
           float vg[32], vl[32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            vg[i] = __uint_as_float(rg[i]) * alpha;
-            vl[i] = __uint_as_float(rl[i]) * alpha;
-            if (g.bias && i < count) {
-              vg[i] += load_bias(g.bias, g.bias_dtype, col0 + i);
-              vl[i] += load_bias(g.bias, g.bias_dtype, g.F + col0 + i);
+          for (int p = 0; p < 16; ++p) {
+            f32x2 xg = mul2(f2(__uint_as_float(rg[2 * p]), __uint_as_float(rg[2 * p + 1])), alpha2);
+            f32x2 xl = mul2(f2(__uint_as_float(rl[2 * p]), __uint_as_float(rl[2 * p + 1])), alpha2);
+            if (g.bias && 2 * p < count) {
+              xg = add2(xg, load_bias_pair(g.bias, g.bias_dtype, col0 + 2 * p));
+              xl = add2(xl, load_bias_pair(g.bias, g.bias_dtype, g.F + col0 + 2 * p));
             }
+            if (round_h) {
+              xg = round_bf16_2(xg);
+              xl = round_bf16_2(xl);
+            }
+            vg[2 * p] = f2lo(xg);
+            vg[2 * p + 1] = f2hi(xg);
+            vl[2 * p] = f2lo(xl);
+            vl[2 * p + 1] = f2hi(xl);
           }
-          round_to(vg, g.h_dtype);
-          round_to(vl, g.h_dtype);
           if (g.saved_h && row_ok) {
             store_seg(g.saved_h, row * g.N + col0, vg, count, g.h_dtype, 1.0f);
             store_seg(g.saved_h, row * g.N + g.F + col0, vl, count, g.h_dtype, 1.0f);
           }
 #pragma unroll
-          for (int i = 0; i < 32; ++i) vg[i] = act_silu(vg[i]) * vl[i];
+          for (int p = 0; p < 16; ++p) {
+            const f32x2 y = mul2(silu2(f2(vg[2 * p], vg[2 * p + 1])), f2(vl[2 * p], vl[2 * p + 1]));
+            vg[2 * p] = f2lo(y);
+            vg[2 * p + 1] = f2hi(y);
+          }
           if (row_ok) {
 #pragma unroll
             for (int i = 0; i < 32; ++i)
@@ -621,6 +661,12 @@ te_status launch_gemm(const GemmArgs& a, cudaStream_t s) {
   g.num_m = int(ceil_div(a.M, BM));
   g.num_n = int(gated ? ceil_div(a.N / 2, BN / 2) : ceil_div(a.N, BN));
   g.num_kb = int(ceil_div(a.K, epr));
+  {
+    const int64_t a_tile_bytes = int64_t(BM) * a.K * esize;
+    int64_t gm = kRasterL2Bytes / (a_tile_bytes > 0 ? a_tile_bytes : 1);
+    if (gm < 8) gm = 8;
+    g.group_m = int(gm < g.num_m ? gm : g.num_m);
+  }
   g.epilogue = a.epilogue;
   g.act = a.act;
   g.a_scale_inv = a.a_scale_inv;
