@@ -23,6 +23,7 @@
 // flight, the MMA thread waits for its own MMAs, and TMEM is freed before the CTA exits.
 #include <cuda.h>
 
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -36,12 +37,21 @@ __device__ int g_device_status;
 
 namespace {
 
-constexpr int BM = 128;                 // accumulator rows per tile (TMEM lanes)
+constexpr int BM = 128;                 // accumulator rows per CTA (TMEM lanes)
 constexpr int BN = 256;                 // accumulator columns per tile
-constexpr int STAGES = 4;
 constexpr int kRowBytes = 128;          // bytes of K per tile row per stage
-constexpr int A_STAGE = BM * kRowBytes; // 16 KB
-constexpr int B_STAGE = BN * kRowBytes; // 32 KB
+
+// CG = CTAs per MMA (tcgen05 cta_group).  CG == 2: a cluster of two CTAs on two SMs computes a
+// 256 x 256 tile; each CTA holds 128 rows of A and 128 columns of B, so each SM streams and
+// reads half of B per MMA.
+template <int CG>
+struct Cfg {
+  static constexpr int kBRows = BN / CG;                // B columns held per CTA
+  static constexpr int kStages = CG == 1 ? 4 : 6;
+  static constexpr int kAStage = BM * kRowBytes;        // 16 KB
+  static constexpr int kBStage = kBRows * kRowBytes;    // 32 KB or 16 KB
+  static constexpr size_t kSmem = size_t(kStages) * (kAStage + kBStage) + 1024 + 256;
+};
 constexpr int kEpiWarps = 8;               // two warps per TMEM lane quadrant
 constexpr int kThreads = 32 * (2 + kEpiWarps);  // producer, MMA, epilogue warps
 constexpr uint32_t kTmemCols = 512;
@@ -106,38 +116,109 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
 }
 
 // Instruction descriptor: fp32 accumulator, A/B format, operand majors, N >> 3, M >> 4.
-template <int KIND>
+template <int KIND, int CG>
 __host__ __device__ constexpr uint32_t instr_desc(int a_mn_major, int b_mn_major) {
   return (1u << 4) | (Kind<KIND>::fmt << 7) | (Kind<KIND>::fmt << 10) |
          (uint32_t(a_mn_major) << 15) | (uint32_t(b_mn_major) << 16) |
-         (uint32_t(BN >> 3) << 17) | (uint32_t(BM >> 4) << 24);
+         (uint32_t(BN >> 3) << 17) | (uint32_t((BM * CG) >> 4) << 24);
 }
 
-template <int KIND>
+#define TE_UMMA_ASM(CGS, KINDS)                                                          \
+  asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"                          \
+               "tcgen05.mma.cta_group::" CGS ".kind::" KINDS " [%0], %1, %2, %3, p;\n\t}" ::"r"( \
+                   d_tmem),                                                                \
+               "l"(a), "l"(b), "r"(idesc), "r"(accumulate))
+
+template <int KIND, int CG>
 __device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
                                      uint32_t accumulate) {
-  if constexpr (KIND == 0) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
-  } else if constexpr (KIND == 1) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
+  if constexpr (CG == 1) {
+    if constexpr (KIND == 0) TE_UMMA_ASM("1", "f16");
+    else if constexpr (KIND == 1) TE_UMMA_ASM("1", "f8f6f4");
+    else TE_UMMA_ASM("1", "tf32");
   } else {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
+    if constexpr (KIND == 0) TE_UMMA_ASM("2", "f16");
+    else if constexpr (KIND == 1) TE_UMMA_ASM("2", "f8f6f4");
+    else TE_UMMA_ASM("2", "tf32");
+  }
+}
+#undef TE_UMMA_ASM
+
+// Arrives on `bar` (this CTA) once every tcgen05.mma issued so far by this thread completed.
+template <int CG>
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  if constexpr (CG == 1)
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+  else
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+// Same, arriving on the barrier at this offset in every CTA of `mask` (cluster of two).
+__device__ __forceinline__ void umma_commit_mc(uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar),
+      "h"(mask)
+      : "memory");
+}
+
+template <int CG>
+__device__ __forceinline__ void tmem_alloc(uint32_t slot, uint32_t cols) {
+  if constexpr (CG == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot), "r"(cols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  } else {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot), "r"(cols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
   }
 }
 
-__device__ __forceinline__ void umma_commit(uint32_t bar) {
+template <int CG>
+__device__ __forceinline__ void tmem_dealloc(uint32_t base, uint32_t cols) {
+  if constexpr (CG == 1)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(base), "r"(cols)
+                 : "memory");
+  else
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(base), "r"(cols)
+                 : "memory");
+}
+
+// TMA load whose completion is signaled on an mbarrier that may sit in the peer CTA of the
+// pair (`bar` is a shared::cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* tm, uint32_t bar,
+                                                 int c0, int c1) {
   asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(bar), "r"(c0), "r"(c1)
       : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// shared::cluster address of the same shared-memory offset in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 // 32 lanes x 32 consecutive fp32 columns: thread t of the warp receives its TMEM lane's row.
@@ -235,12 +316,17 @@ __device__ __forceinline__ void round_to(float (&v)[32], int dtype) {
 
 // ------------------------------------------------------------------ the kernel ------------
 
-template <int KIND, bool A_KMAJOR, bool B_KMAJOR>
+template <int KIND, bool A_KMAJOR, bool B_KMAJOR, int CG>
 __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ GemmParams p) {
+  using C = Cfg<CG>;
+  constexpr int STAGES = C::kStages;
+  constexpr int A_STAGE = C::kAStage;
+  constexpr int B_STAGE = C::kBStage;
+  constexpr int BROWS = C::kBRows;
   constexpr int EPR = kRowBytes / Kind<KIND>::esize;  // K elements per 128-byte row
   constexpr int MMA_K_BYTES = 32;                     // K bytes consumed by one tcgen05.mma
   constexpr int MMA_K = MMA_K_BYTES / Kind<KIND>::esize;
-  constexpr uint32_t IDESC = instr_desc<KIND>(A_KMAJOR ? 0 : 1, B_KMAJOR ? 0 : 1);
+  constexpr uint32_t IDESC = instr_desc<KIND, CG>(A_KMAJOR ? 0 : 1, B_KMAJOR ? 0 : 1);
   const GemmDev& g = p.g;
 
   extern __shared__ uint8_t smem_raw[];
@@ -259,6 +345,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int num_tiles = g.num_m * g.num_n;
+  const uint32_t rank = CG == 1 ? 0u : cluster_rank();
+  const bool leader = rank == 0;
+  const int cluster_id = int(blockIdx.x) / CG;
+  const int num_clusters = int(gridDim.x) / CG;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -267,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(smem_u32(&tfull[a]), 1);
-      mbar_init(smem_u32(&tempty[a]), 32 * kEpiWarps);
+      mbar_init(smem_u32(&tempty[a]), 32 * kEpiWarps * CG);
     }
     mbar_init(smem_u32(drain), 1);
     *abort_flag = 0;
@@ -278,15 +368,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tmA)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tmB)) : "memory");
   }
-  if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     smem_u32(tmem_slot)),
-                 "r"(kTmemCols)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-  }
+  if (warp == 1) tmem_alloc<CG>(smem_u32(tmem_slot), kTmemCols);
   tc_fence_before();
   __syncthreads();
+  if constexpr (CG == 2) cluster_sync();  // the peer's barriers exist before anyone signals them
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -295,49 +380,46 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0, issued = 0, last_parity = 0;
-      for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+      bool ok = true;
+      for (int t = cluster_id; t < num_tiles && ok; t += num_clusters) {
         const Tile tl = tile_of(t, g.num_m, g.num_n, g.group_m);
-        const int m0 = tl.m * BM;
-        bool ok = true;
+        const int m0 = (tl.m * CG + int(rank)) * BM;
         for (int kb = 0; kb < g.num_kb; ++kb) {
           if (!mbar_try_wait(smem_u32(&empty[stage]), phase ^ 1) &&
               !wait_bounded(smem_u32(&empty[stage]), phase ^ 1, abort_flag, &g_device_status, kWaitLimitNs, true)) {
             ok = false;
             break;
           }
-          const uint32_t fb = smem_u32(&full[stage]);
-          mbar_expect_tx(fb, A_STAGE + B_STAGE);
+          // The pair's loads all complete on the leader's full barrier.
+          const uint32_t fb = CG == 1 ? smem_u32(&full[stage]) : map_to_rank(smem_u32(&full[stage]), 0);
+          if (leader) mbar_expect_tx(smem_u32(&full[stage]), CG * (A_STAGE + B_STAGE));
           const uint32_t a_dst = smem_u32(smA + stage * A_STAGE);
           const uint32_t b_dst = smem_u32(smB + stage * B_STAGE);
           const int k0 = kb * EPR;
+          auto load = [&](uint32_t dst, const CUtensorMap* tm, int c0, int c1) {
+            if constexpr (CG == 1) tma_load_2d(dst, tm, fb, c0, c1);
+            else tma_load_2d_pair(dst, tm, fb, c0, c1);
+          };
           if constexpr (A_KMAJOR) {
-            tma_load_2d(a_dst, &p.tmA, fb, k0, m0);
+            load(a_dst, &p.tmA, k0, m0);
           } else {
 #pragma unroll
-            for (int i = 0; i < BM / EPR; ++i)
-              tma_load_2d(a_dst + i * EPR * kRowBytes, &p.tmA, fb, m0 + i * EPR, k0);
+            for (int i = 0; i < BM / EPR; ++i) load(a_dst + i * EPR * kRowBytes, &p.tmA, m0 + i * EPR, k0);
           }
-          if (!g.gated) {
-            const int n0 = tl.n * BN;
+          // B columns held by this CTA: [n, n + BROWS) of the tile, or for a gated tile the gate
+          // half (rank 0 / first half) and the linear half (rank 1 / second half).
+          const int parts = (CG == 1 && g.gated) ? 2 : 1;
+#pragma unroll
+          for (int h = 0; h < parts; ++h) {
+            int c0;
+            if (!g.gated) c0 = tl.n * BN + int(rank) * BROWS;
+            else c0 = int((CG == 1 ? h : int(rank)) * g.F) + tl.n * (BN / 2);
+            const int cols = g.gated ? BN / 2 : BROWS;
+            const uint32_t dst = b_dst + h * (BN / 2) * kRowBytes;
             if constexpr (B_KMAJOR) {
-              tma_load_2d(b_dst, &p.tmB, fb, k0, n0);
+              load(dst, &p.tmB, k0, c0);
             } else {
-#pragma unroll
-              for (int i = 0; i < BN / EPR; ++i)
-                tma_load_2d(b_dst + i * EPR * kRowBytes, &p.tmB, fb, n0 + i * EPR, k0);
-            }
-          } else {
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const int c0 = int(h * g.F) + tl.n * (BN / 2);
-              const uint32_t dst = b_dst + h * (BN / 2) * kRowBytes;
-              if constexpr (B_KMAJOR) {
-                tma_load_2d(dst, &p.tmB, fb, k0, c0);
-              } else {
-#pragma unroll
-                for (int i = 0; i < (BN / 2) / EPR; ++i)
-                  tma_load_2d(dst + i * EPR * kRowBytes, &p.tmB, fb, c0 + i * EPR, k0);
-              }
+              for (int i = 0; i < cols / EPR; ++i) load(dst + i * EPR * kRowBytes, &p.tmB, c0 + i * EPR, k0);
             }
           }
           issued |= 1u << stage;
@@ -347,21 +429,28 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             phase ^= 1;
           }
         }
-        if (!ok) break;
       }
-      // Own copies still in flight complete before the CTA may exit.
-      for (int s = 0; s < STAGES; ++s)
-        if (issued & (1u << s))
-          wait_bounded(smem_u32(&full[s]), (last_parity >> s) & 1, abort_flag, &g_device_status, kDrainLimitNs, false);
+      if (leader) {
+        // Copies still in flight (the pair's) complete before the CTAs may exit.
+        for (int s = 0; s < STAGES; ++s)
+          if (issued & (1u << s))
+            wait_bounded(smem_u32(&full[s]), (last_parity >> s) & 1, abort_flag, &g_device_status, kDrainLimitNs, false);
+      } else if (!ok) {
+        // The peer cannot observe its copies' completion (they signal the leader): after an
+        // abort give copies in flight time to land before the final cluster barrier.
+        const uint64_t t0 = global_ns();
+        while (global_ns() - t0 < 100000ull) {
+        }
+      }
     }
   } else if (warp == 1) {
     // ----------------------------------------------------------- MMA issuer -------------
-    if (lane == 0) {
+    if (lane == 0 && leader) {
       int stage = 0;
       uint32_t phase = 0;
       int local = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++local) {
+      for (int t = cluster_id; t < num_tiles && ok; t += num_clusters, ++local) {
         const int acc = local & 1;
         const uint32_t acc_phase = (local >> 1) & 1;
         if (!wait_bounded(smem_u32(&tempty[acc]), acc_phase ^ 1, abort_flag, &g_device_status, kWaitLimitNs, true)) {
@@ -387,19 +476,21 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             const uint64_t bd =
                 B_KMAJOR ? smem_desc(b_base + j * MMA_K_BYTES, 16, 8 * kRowBytes)
                          : smem_desc(b_base + j * MMA_K * kRowBytes, EPR * kRowBytes, 8 * kRowBytes);
-            umma<KIND>(d_tmem, ad, bd, IDESC, (kb | j) != 0 ? 1u : 0u);
+            umma<KIND, CG>(d_tmem, ad, bd, IDESC, (kb | j) != 0 ? 1u : 0u);
           }
-          umma_commit(smem_u32(&empty[stage]));
+          if constexpr (CG == 1) umma_commit<1>(smem_u32(&empty[stage]));
+          else umma_commit_mc(smem_u32(&empty[stage]), 0x3);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1;
           }
         }
         if (!ok) break;
-        umma_commit(smem_u32(&tfull[acc]));
+        if constexpr (CG == 1) umma_commit<1>(smem_u32(&tfull[acc]));
+        else umma_commit_mc(smem_u32(&tfull[acc]), 0x3);
       }
       // Own MMAs complete before TMEM is released.
-      umma_commit(smem_u32(drain));
+      umma_commit<CG>(smem_u32(drain));
       wait_bounded(smem_u32(drain), 0, abort_flag, &g_device_status, kDrainLimitNs, false);
     }
   } else {
@@ -414,11 +505,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     const f32x2 alpha2 = f2s(alpha);
     const float out_scale = (g.d_dtype == TE_E4M3 && g.out_scale) ? *g.out_scale : 1.0f;
     if (blockIdx.x == 0 && threadIdx.x == 64 && g.out_scale_inv) *g.out_scale_inv = 1.0f / out_scale;
+    const uint32_t tempty_leader0 = CG == 1 ? smem_u32(&tempty[0]) : map_to_rank(smem_u32(&tempty[0]), 0);
+    const uint32_t tempty_leader1 = CG == 1 ? smem_u32(&tempty[1]) : map_to_rank(smem_u32(&tempty[1]), 0);
     const int64_t ldd = g.gated ? g.F : g.N;
     const bool round_h = g.h_dtype == TE_BF16;
     float amax = 0.0f;
     int local = 0;
-    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++local) {
+    for (int t = cluster_id; t < num_tiles; t += num_clusters, ++local) {
       const int acc = local & 1;
       const uint32_t acc_phase = (local >> 1) & 1;
       const uint32_t tb = smem_u32(&tfull[acc]);
@@ -432,7 +525,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       __syncwarp();
       tc_fence_after();
       const Tile tl = tile_of(t, g.num_m, g.num_n, g.group_m);
-      const int64_t row = int64_t(tl.m) * BM + row_in_tile;
+      const int64_t row = (int64_t(tl.m) * CG + rank) * BM + row_in_tile;
       const bool row_ok = row < g.M;
       const uint32_t taddr = tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(acc * BN);
       if (!g.gated) {
@@ -520,7 +613,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         }
       }
       tc_fence_before();
-      mbar_arrive(smem_u32(&tempty[acc]));
+      if constexpr (CG == 1) mbar_arrive(acc ? tempty_leader1 : tempty_leader0);
+      else mbar_arrive_cluster(acc ? tempty_leader1 : tempty_leader0);
     }
     amax = warp_max(amax);
     if (lane == 0 && g.amax_out) atomic_max_nonneg(g.amax_out, amax);
@@ -528,12 +622,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
 
   tc_fence_before();
   __syncthreads();
+  if constexpr (CG == 2) cluster_sync();  // no MMA of the pair still writes this CTA's TMEM
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
-                 "r"(kTmemCols)
-                 : "memory");
+    tmem_dealloc<CG>(tmem_base, kTmemCols);
   }
 }
 
@@ -576,29 +669,56 @@ bool make_tmap(CUtensorMap* tm, const void* ptr, int ab_dtype, uint64_t inner, u
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-constexpr size_t kSmemBytes = size_t(STAGES) * (A_STAGE + B_STAGE) + 1024 + 256;
-
-template <int KIND, bool AK, bool BK>
+template <int KIND, bool AK, bool BK, int CG>
 te_status launch_t(GemmParams& prm, int grid, cudaStream_t s) {
+  constexpr size_t smem = Cfg<CG>::kSmem;
   static bool attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (!attr_set[dev & 63]) {
-    if (cudaFuncSetAttribute(gemm_kernel<KIND, AK, BK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             int(kSmemBytes)) != cudaSuccess)
+    if (cudaFuncSetAttribute(gemm_kernel<KIND, AK, BK, CG>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
       return TE_ERR_CUDA;
     attr_set[dev & 63] = true;
   }
-  gemm_kernel<KIND, AK, BK><<<grid, kThreads, kSmemBytes, s>>>(prm);
+  if constexpr (CG == 1) {
+    gemm_kernel<KIND, AK, BK, 1><<<grid, kThreads, smem, s>>>(prm);
+  } else {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(grid));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, gemm_kernel<KIND, AK, BK, 2>, prm) != cudaSuccess) return TE_ERR_CUDA;
+  }
   return cudaGetLastError() == cudaSuccess ? TE_OK : TE_ERR_CUDA;
 }
 
-template <int KIND>
+template <int KIND, int CG>
 te_status launch_kind(GemmParams& prm, int grid, bool ak, bool bk, cudaStream_t s) {
-  if (ak && bk) return launch_t<KIND, true, true>(prm, grid, s);
-  if (ak && !bk) return launch_t<KIND, true, false>(prm, grid, s);
-  if (!ak && bk) return launch_t<KIND, false, true>(prm, grid, s);
-  return launch_t<KIND, false, false>(prm, grid, s);
+  if (ak && bk) return launch_t<KIND, true, true, CG>(prm, grid, s);
+  if (ak && !bk) return launch_t<KIND, true, false, CG>(prm, grid, s);
+  if (!ak && bk) return launch_t<KIND, false, true, CG>(prm, grid, s);
+  return launch_t<KIND, false, false, CG>(prm, grid, s);
+}
+
+// CTAs per MMA: pairs for bf16 / E4M3 problems taller than one tile.  TE_GEMM_CTA_GROUP=1 in
+// the environment forces single-CTA tiles (a diagnostic switch between two complete paths).
+int choose_cta_group(int kind, int64_t M) {
+  static int forced = -1;
+  if (forced < 0) {
+    const char* e = getenv("TE_GEMM_CTA_GROUP");
+    forced = (e && e[0] == '1') ? 1 : 0;
+  }
+  if (forced == 1 || kind == 2 || M <= BM) return 1;
+  return 2;
 }
 
 }  // namespace
@@ -643,13 +763,15 @@ te_status launch_gemm(const GemmArgs& a, cudaStream_t s) {
   const int esize = a.ab_dtype == TE_BF16 ? 2 : a.ab_dtype == TE_E4M3 ? 1 : 4;
   const uint32_t epr = uint32_t(kRowBytes / esize);
   const bool gated = a.epilogue == EPI_BIAS_GATED;
+  const int cg = choose_cta_group(kind, a.M);
   GemmParams prm;
   memset(&prm, 0, sizeof(prm));
-  // A: op(A) is [M, K].
+  // A: op(A) is [M, K]; each CTA loads 128 rows.
   bool ok = a.a_kmajor ? make_tmap(&prm.tmA, a.A, a.ab_dtype, a.K, a.M, epr, BM)
                        : make_tmap(&prm.tmA, a.A, a.ab_dtype, a.M, a.K, epr, epr);
-  // B: op(B) is [K, N].
-  ok = ok && (a.b_kmajor ? make_tmap(&prm.tmB, a.B, a.ab_dtype, a.K, a.N, epr, gated ? BN / 2 : BN)
+  // B: op(B) is [K, N]; a K-major box holds the B columns one CTA loads at a time.
+  const uint32_t b_rows = (gated || cg == 2) ? BN / 2 : BN;
+  ok = ok && (a.b_kmajor ? make_tmap(&prm.tmB, a.B, a.ab_dtype, a.K, a.N, epr, b_rows)
                          : make_tmap(&prm.tmB, a.B, a.ab_dtype, a.N, a.K, epr, epr));
   if (!ok) return TE_ERR_CUDA;
   GemmDev& g = prm.g;
@@ -658,13 +780,13 @@ te_status launch_gemm(const GemmArgs& a, cudaStream_t s) {
   g.K = a.K;
   g.gated = gated ? 1 : 0;
   g.F = gated ? a.N / 2 : 0;
-  g.num_m = int(ceil_div(a.M, BM));
+  g.num_m = int(ceil_div(a.M, int64_t(BM) * cg));
   g.num_n = int(gated ? ceil_div(a.N / 2, BN / 2) : ceil_div(a.N, BN));
   g.num_kb = int(ceil_div(a.K, epr));
   {
-    const int64_t a_tile_bytes = int64_t(BM) * a.K * esize;
+    const int64_t a_tile_bytes = int64_t(BM) * cg * a.K * esize;
     int64_t gm = kRasterL2Bytes / (a_tile_bytes > 0 ? a_tile_bytes : 1);
-    if (gm < 8) gm = 8;
+    if (gm < 4) gm = 4;
     g.group_m = int(gm < g.num_m ? gm : g.num_m);
   }
   g.epilogue = a.epilogue;
@@ -681,11 +803,16 @@ te_status launch_gemm(const GemmArgs& a, cudaStream_t s) {
   g.out_scale_inv = a.cast.scale_inv_out;
   g.amax_out = a.cast.amax_out;
   const int64_t tiles = int64_t(g.num_m) * g.num_n;
-  const int grid = int(tiles < num_sms() ? tiles : num_sms());
+  const int64_t slots = num_sms() / cg;
+  const int grid = int(tiles < slots ? tiles : slots) * cg;
   ProfileScope prof(a.epilogue == EPI_BIAS ? TE_KERNEL_GEMM : TE_KERNEL_GEMM_ACT, s);
-  if (kind == 0) return launch_kind<0>(prm, grid, a.a_kmajor, a.b_kmajor, s);
-  if (kind == 1) return launch_kind<1>(prm, grid, a.a_kmajor, a.b_kmajor, s);
-  return launch_kind<2>(prm, grid, a.a_kmajor, a.b_kmajor, s);
+  if (cg == 1) {
+    if (kind == 0) return launch_kind<0, 1>(prm, grid, a.a_kmajor, a.b_kmajor, s);
+    if (kind == 1) return launch_kind<1, 1>(prm, grid, a.a_kmajor, a.b_kmajor, s);
+    return launch_kind<2, 1>(prm, grid, a.a_kmajor, a.b_kmajor, s);
+  }
+  if (kind == 0) return launch_kind<0, 2>(prm, grid, a.a_kmajor, a.b_kmajor, s);
+  return launch_kind<1, 2>(prm, grid, a.a_kmajor, a.b_kmajor, s);
 }
 
 }  // namespace te
