@@ -35,9 +35,48 @@ ORACLE_ROWS_BASELINE = 256
 ORACLE_ROWS_REFERENCE = 32
 
 
+def reduce_max(v, world, device):
+    """Max of a per-rank float over all ranks (the slowest rank's step time)."""
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank, world, ms_per_step_max):
+    """Units all ranks processed per second, timed by the slowest rank."""
+    return world * units_per_rank / (ms_per_step_max / 1e3)
+
+
 def mlp_flops(M, H, F, gated):
     f1 = 2 * F if gated else F
     return 2.0 * M * H * f1 + 2.0 * M * F * H
+
+
+TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "gemm_pair_traffic_llama_full.md")
+
+
+def measured_traffic():
+    """DRAM bytes per GEMM1 launch from the committed ncu capture, or None when the kernel source
+    changed since the counters were taken (the capture records the source's sha256)."""
+    import hashlib
+    try:
+        fields = {}
+        with open(TRAFFIC_PROFILE) as f:
+            for line in f:
+                if ":" in line and not line.startswith(("|", "#", "`")):
+                    k, v = line.split(":", 1)
+                    fields[k.strip()] = v.strip()
+        src = os.path.join(ROOT, fields["source"])
+        with open(src, "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest() != fields["source sha256"]:
+                return None
+        return int(fields["traffic_bytes_per_launch"])
+    except Exception:
+        return None
 
 
 def load_peaks():
@@ -327,11 +366,7 @@ def run_ours(args, rank, world, local_rank):
             dist.barrier()
 
     def max_over_ranks(v):
-        if world == 1:
-            return v
-        t = torch.tensor([v], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return reduce_max(v, world, dev)
 
     for _ in range(args.warmup):
         flush()
@@ -359,8 +394,8 @@ def run_ours(args, rank, world, local_rank):
 
     ms_step = max_over_ranks(statistics.mean(ms_bf16))
     ms_step_fp8 = max_over_ranks(statistics.mean(ms_fp8))
-    value = world * flops / (ms_step / 1e3) / 1e12
-    value_fp8 = world * flops / (ms_step_fp8 / 1e3) / 1e12
+    value = whole_job_rate(flops, world, ms_step) / 1e12
+    value_fp8 = whole_job_rate(flops, world, ms_step_fp8) / 1e12
     launches = sum(n for _, n in prof_bf16.values())
     if args.kernels_only:
         if rank == 0:
@@ -525,7 +560,8 @@ def run_ours(args, rank, world, local_rank):
         "kernel_share": share,
         "roofline": {"kernel": "gemm_act (GEMM1 + SwiGLU epilogue, bf16)", "bound": "tensor",
                      "achieved": achieved, "peak": peaks["bf16"], "unit": "TFLOP/s",
-                     "frac": achieved / peaks["bf16"], "traffic": None,
+                     "frac": achieved / peaks["bf16"], "traffic": measured_traffic(),
+                     "traffic_unit": "bytes per launch (ncu, full-size capture)",
                      "peak_note": f"{peaks['source']} bf16 burst",
                      "fp8_achieved": achieved_fp8, "fp8_frac": achieved_fp8 / fp8_peak},
         "cpu_baseline": {"value": cpu_value, "unit": UNIT, "cores": cores_used(),
