@@ -1,18 +1,10 @@
-// Bandwidth-bound kernels of the block: per-tensor quantize, activation, and the backward's
-// fused activation-gradient + bias-reduction + quantize.
+// Bandwidth-bound kernels of the block that need no staging: the per-tensor quantize and the
+// fp32 transpose of the tf32 path.  (The activation and the backward's activation gradient +
+// bias reduction + quantize stream through TMA in stream.cu.)
 //
 // * quantize (TransformerEngine JAX "LayerNorm Dense" page, Description: the normalized output
 //   and the kernel are quantized before the GEMM): 16-byte vectors, grid-stride, amax by one
 //   integer atomic per block.
-// * act_lu ("Activation" page, Description: the forward rule's activation primitive, optional
-//   FP8 round trip): elementwise, several 16-byte vectors in flight per thread, exp and
-//   reciprocal on the hardware approximations; the gated pair reads its gate and linear halves
-//   from the two column halves of the same row.
-// * dact_dbias ("LayerNorm MLP" page, Description, backward: tex.quantize_dact_dbias): each CTA
-//   owns a strip of 32 x 16-byte column vectors and a chunk of rows; every thread keeps its
-//   columns' sums in registers, the 8 warps of the CTA are combined through shared memory in a
-//   fixed order, and one partial row per chunk goes to the workspace.  A second kernel adds the
-//   partial rows in chunk order, so dbias is deterministic.
 #include "cast.cuh"
 #include "common.cuh"
 #include "kernels.h"
@@ -47,193 +39,6 @@ __global__ void __launch_bounds__(kEwThreads) quantize_kernel(QuantizeArgs a) {
     if (cs.store) cast_store<E>(a.out, v * E, x, cs);
   }
   block_amax_commit(amax, a.cast.amax_out);
-}
-
-// ------------------------------------------------------------------ act_lu ----------------
-
-constexpr int kActWarps = 8;
-constexpr int kActRows = 32;    // rows per CTA
-constexpr int kActUnroll = 4;   // rows in flight per warp
-
-// Each CTA owns a strip of 32 x 16-byte output vectors (one per lane) and kActRows rows; its
-// warps take rows in turn, kActUnroll at a time, so every load is a 512-byte coalesced row
-// segment and no index needs a division.
-template <typename T>
-__global__ void __launch_bounds__(kActWarps * 32, 3) act_lu_kernel(ActArgs a) {
-  using V = Vec16<T>;
-  using PR = Pairs<T>;
-  constexpr int E = V::N;
-  const CastState cs = cast_begin(a.cast);
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const bool gated = a.act == TE_SWIGLU;
-  const int64_t n_out = gated ? a.N_in / 2 : a.N_in;
-  const int64_t col = (int64_t(blockIdx.x) * 32 + lane) * E;
-  const int64_t r0 = int64_t(blockIdx.y) * kActRows;
-  const int64_t r1 = r0 + kActRows < a.M ? r0 + kActRows : a.M;
-  const T* x = static_cast<const T*>(a.x);
-  const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
-  float amax = 0.0f;
-  if (col < n_out) {
-    for (int64_t rb = r0 + warp; rb < r1; rb += kActUnroll * kActWarps) {
-      uint4 rg[kActUnroll], rl[kActUnroll];
-#pragma unroll
-      for (int j = 0; j < kActUnroll; ++j) {
-        const int64_t r = rb + int64_t(j) * kActWarps;
-        const bool in = r < r1;
-        rg[j] = in ? __ldg(reinterpret_cast<const uint4*>(x + r * a.N_in + col)) : zero;
-        rl[j] = (in && gated) ? __ldg(reinterpret_cast<const uint4*>(x + r * a.N_in + n_out + col)) : zero;
-      }
-#pragma unroll
-      for (int j = 0; j < kActUnroll; ++j) {
-        const int64_t r = rb + int64_t(j) * kActWarps;
-        if (r >= r1) break;
-        f32x2 hp[PR::P], lp[PR::P];
-        PR::get(rg[j], hp);
-        if (gated) PR::get(rl[j], lp);
-        float y[E];
-#pragma unroll
-        for (int p = 0; p < PR::P; ++p) {
-          const f32x2 yy = gated ? mul2(silu2(hp[p]), lp[p]) : act2(a.act, hp[p]);
-          amax = absmax2(amax, yy);
-          y[2 * p] = f2lo(yy);
-          y[2 * p + 1] = f2hi(yy);
-        }
-        if (cs.store) cast_store<E>(a.out, r * n_out + col, y, cs);
-      }
-    }
-  }
-  block_amax_commit(amax, a.cast.amax_out);
-}
-
-// ------------------------------------------------------------------ dact + dbias ----------
-
-constexpr int kDactWarps = 8;
-constexpr int kDactRows = 128;  // rows per CTA (chunk)
-
-constexpr int kDactUnroll = 2;  // rows in flight per warp (x 24 warps per SM)
-
-template <typename T>
-__global__ void __launch_bounds__(kDactWarps * 32, 3) dact_dbias_kernel(DactArgs a) {
-  using V = Vec16<T>;
-  constexpr int E = V::N;
-  constexpr int W = 32 * E;  // strip width in columns
-  __shared__ float red[kDactWarps][2][W];
-  const CastState cs = cast_begin(a.cast);
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const bool gated = a.act == TE_SWIGLU;
-  const bool ident = a.act == TE_IDENTITY;
-  const int64_t n_out = gated ? a.N_in / 2 : a.N_in;
-  const int64_t col = (int64_t(blockIdx.x) * 32 + lane) * E;
-  const bool valid = col < n_out;
-  const int64_t r0 = int64_t(blockIdx.y) * kDactRows;
-  const int64_t r1 = r0 + kDactRows < a.M ? r0 + kDactRows : a.M;
-  using PR = Pairs<T>;
-  constexpr int P = PR::P;
-  f32x2 acc1[P], acc2[P];
-#pragma unroll
-  for (int p = 0; p < P; ++p) { acc1[p] = f2s(0.0f); acc2[p] = f2s(0.0f); }
-  float amax = 0.0f;
-  const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
-  if (valid) {
-    for (int64_t rb = r0 + warp; rb < r1; rb += kDactUnroll * kDactWarps) {
-      // issue every load of kDactUnroll rows before using any of them
-      uint4 rdy[kDactUnroll], rx[kDactUnroll], rl[kDactUnroll];
-#pragma unroll
-      for (int j = 0; j < kDactUnroll; ++j) {
-        const int64_t r = rb + int64_t(j) * kDactWarps;
-        const bool in = r < r1;
-        rdy[j] = in ? __ldg(reinterpret_cast<const uint4*>(static_cast<const T*>(a.dy) + r * n_out + col)) : zero;
-        rx[j] = (in && !ident) ? __ldg(reinterpret_cast<const uint4*>(static_cast<const T*>(a.x) + r * a.N_in + col)) : zero;
-        rl[j] = (in && gated) ? __ldg(reinterpret_cast<const uint4*>(static_cast<const T*>(a.x) + r * a.N_in + n_out + col)) : zero;
-      }
-#pragma unroll
-      for (int j = 0; j < kDactUnroll; ++j) {
-        const int64_t r = rb + int64_t(j) * kDactWarps;
-        if (r >= r1) break;
-        f32x2 dyp[P], hp[P];
-        PR::get(rdy[j], dyp);
-        PR::get(rx[j], hp);
-        if (gated) {
-          f32x2 lp[P];
-          PR::get(rl[j], lp);
-          float dg[E], dl[E];
-#pragma unroll
-          for (int p = 0; p < P; ++p) {
-            f32x2 sg, eg;
-            sigmoid2(hp[p], sg, eg);
-            // d_gate = dy * lin * silu'(gate), d_lin = dy * silu(gate)
-            const f32x2 dsil = mul2(sg, fma2(hp[p], mul2(eg, sg), f2s(1.0f)));
-            const f32x2 g2 = mul2(mul2(dyp[p], lp[p]), dsil);
-            const f32x2 l2 = mul2(dyp[p], mul2(hp[p], sg));
-            acc1[p] = add2(acc1[p], g2);
-            acc2[p] = add2(acc2[p], l2);
-            amax = absmax2(absmax2(amax, g2), l2);
-            dg[2 * p] = f2lo(g2);
-            dg[2 * p + 1] = f2hi(g2);
-            dl[2 * p] = f2lo(l2);
-            dl[2 * p + 1] = f2hi(l2);
-          }
-          if (cs.store) {
-            cast_store<E>(a.dx, r * a.N_in + col, dg, cs);
-            cast_store<E>(a.dx, r * a.N_in + n_out + col, dl, cs);
-          }
-        } else {
-          float d[E];
-#pragma unroll
-          for (int p = 0; p < P; ++p) {
-            const f32x2 dd = ident ? dyp[p] : mul2(dyp[p], dact2(a.act, hp[p]));
-            acc1[p] = add2(acc1[p], dd);
-            amax = absmax2(amax, dd);
-            d[2 * p] = f2lo(dd);
-            d[2 * p + 1] = f2hi(dd);
-          }
-          if (cs.store && a.dx) cast_store<E>(a.dx, r * a.N_in + col, d, cs);
-        }
-      }
-    }
-  }
-  if (a.dbias) {
-#pragma unroll
-    for (int p = 0; p < P; ++p) {
-      red[warp][0][lane * E + 2 * p] = f2lo(acc1[p]);
-      red[warp][0][lane * E + 2 * p + 1] = f2hi(acc1[p]);
-      red[warp][1][lane * E + 2 * p] = f2lo(acc2[p]);
-      red[warp][1][lane * E + 2 * p + 1] = f2hi(acc2[p]);
-    }
-    __syncthreads();
-    // 256 threads finish the strip's column sums, each over the 8 warps in warp order.
-    const int halves = gated ? 2 : 1;
-    for (int t = threadIdx.x; t < halves * W; t += blockDim.x) {
-      const int hsel = t / W, j = t % W;
-      float s = 0.0f;
-#pragma unroll
-      for (int w = 0; w < kDactWarps; ++w) s += red[w][hsel][j];
-      const int64_t c = int64_t(blockIdx.x) * W + j;
-      if (c < n_out) a.partials[int64_t(blockIdx.y) * a.N_in + hsel * n_out + c] = s;
-    }
-  }
-  block_amax_commit(amax, a.cast.amax_out);
-}
-
-__global__ void colsum_partials_kernel(const float* partials, int chunks, int64_t n, float* out) {
-  const int64_t j = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (j >= n) return;
-  float s = 0.0f;
-  for (int c = 0; c < chunks; ++c) s += partials[int64_t(c) * n + j];
-  out[j] = s;
-}
-
-template <typename T>
-te_status launch_dact_t(const DactArgs& a, cudaStream_t s) {
-  constexpr int E = Vec16<T>::N;
-  const int64_t n_out = a.act == TE_SWIGLU ? a.N_in / 2 : a.N_in;
-  const int chunks = int(ceil_div(a.M, kDactRows));
-  dim3 grid(unsigned(ceil_div(n_out, 32 * E)), unsigned(chunks));
-  dact_dbias_kernel<T><<<grid, kDactWarps * 32, 0, s>>>(a);
-  if (a.dbias)
-    colsum_partials_kernel<<<unsigned(ceil_div(a.N_in, 256)), 256, 0, s>>>(a.partials, chunks,
-                                                                          a.N_in, a.dbias);
-  return cudaGetLastError() == cudaSuccess ? TE_OK : TE_ERR_CUDA;
 }
 
 // ------------------------------------------------------------------ transpose -------------
@@ -275,35 +80,6 @@ te_status launch_quantize(const QuantizeArgs& a, cudaStream_t s) {
     return TE_ERR_UNSUPPORTED;
   }
   return cudaGetLastError() == cudaSuccess ? TE_OK : TE_ERR_CUDA;
-}
-
-te_status launch_act_lu(const ActArgs& a, cudaStream_t s) {
-  ProfileScope prof(TE_KERNEL_ACT_LU, s);
-  const int64_t n_out = a.act == TE_SWIGLU ? a.N_in / 2 : a.N_in;
-  if (a.M == 0) return TE_OK;
-  const int E = a.x_dtype == TE_BF16 ? 8 : 4;
-  if (ceil_div(a.M, kActRows) > 65535) return TE_ERR_UNSUPPORTED;
-  dim3 grid(unsigned(ceil_div(n_out, 32 * E)), unsigned(ceil_div(a.M, kActRows)));
-  if (a.x_dtype == TE_BF16) {
-    act_lu_kernel<__nv_bfloat16><<<grid, kActWarps * 32, 0, s>>>(a);
-  } else if (a.x_dtype == TE_F32) {
-    act_lu_kernel<float><<<grid, kActWarps * 32, 0, s>>>(a);
-  } else {
-    return TE_ERR_UNSUPPORTED;
-  }
-  return cudaGetLastError() == cudaSuccess ? TE_OK : TE_ERR_CUDA;
-}
-
-size_t dact_dbias_workspace(int64_t M, int64_t N_in) {
-  return size_t(ceil_div(M > 0 ? M : 1, kDactRows)) * size_t(N_in) * sizeof(float);
-}
-
-te_status launch_dact_dbias(const DactArgs& a, cudaStream_t s) {
-  if (a.M == 0) return TE_OK;
-  ProfileScope prof(TE_KERNEL_DACT_DBIAS, s);
-  if (a.dtype == TE_BF16) return launch_dact_t<__nv_bfloat16>(a, s);
-  if (a.dtype == TE_F32) return launch_dact_t<float>(a, s);
-  return TE_ERR_UNSUPPORTED;
 }
 
 }  // namespace te

@@ -93,15 +93,6 @@ struct __align__(64) GemmParams {
 
 // ------------------------------------------------------------------ PTX wrappers ----------
 
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm, uint32_t bar,
-                                            int c0, int c1) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(tm)), "r"(bar), "r"(c0), "r"(c1)
-      : "memory");
-}
-
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
@@ -632,43 +623,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
 
 // ------------------------------------------------------------------ host side -------------
 
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(f);
-  });
-  return fn;
-}
-
-// 2-D tensor map over a row-major [outer, inner] matrix, 128-byte swizzled boxes.
-bool make_tmap(CUtensorMap* tm, const void* ptr, int ab_dtype, uint64_t inner, uint64_t outer,
-               uint32_t box_inner, uint32_t box_outer) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  CUtensorMapDataType dt = ab_dtype == TE_BF16   ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                           : ab_dtype == TE_E4M3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
-                                                 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
-  const int esize = ab_dtype == TE_BF16 ? 2 : ab_dtype == TE_E4M3 ? 1 : 4;
-  cuuint64_t dims[2] = {inner, outer};
-  cuuint64_t strides[1] = {inner * esize};
-  cuuint32_t box[2] = {box_inner, box_outer};
-  cuuint32_t estr[2] = {1, 1};
-  return fn(tm, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int KIND, bool AK, bool BK, int CG>
 te_status launch_t(GemmParams& prm, int grid, cudaStream_t s) {
   constexpr size_t smem = Cfg<CG>::kSmem;
@@ -767,12 +721,12 @@ te_status launch_gemm(const GemmArgs& a, cudaStream_t s) {
   GemmParams prm;
   memset(&prm, 0, sizeof(prm));
   // A: op(A) is [M, K]; each CTA loads 128 rows.
-  bool ok = a.a_kmajor ? make_tmap(&prm.tmA, a.A, a.ab_dtype, a.K, a.M, epr, BM)
-                       : make_tmap(&prm.tmA, a.A, a.ab_dtype, a.M, a.K, epr, epr);
+  bool ok = a.a_kmajor ? make_tmap_2d(&prm.tmA, a.A, a.ab_dtype, a.K, a.M, epr, BM, true)
+                       : make_tmap_2d(&prm.tmA, a.A, a.ab_dtype, a.M, a.K, epr, epr, true);
   // B: op(B) is [K, N]; a K-major box holds the B columns one CTA loads at a time.
   const uint32_t b_rows = (gated || cg == 2) ? BN / 2 : BN;
-  ok = ok && (a.b_kmajor ? make_tmap(&prm.tmB, a.B, a.ab_dtype, a.K, a.N, epr, b_rows)
-                         : make_tmap(&prm.tmB, a.B, a.ab_dtype, a.N, a.K, epr, epr));
+  ok = ok && (a.b_kmajor ? make_tmap_2d(&prm.tmB, a.B, a.ab_dtype, a.K, a.N, epr, b_rows, true)
+                         : make_tmap_2d(&prm.tmB, a.B, a.ab_dtype, a.N, a.K, epr, epr, true));
   if (!ok) return TE_ERR_CUDA;
   GemmDev& g = prm.g;
   g.M = a.M;

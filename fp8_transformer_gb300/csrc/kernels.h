@@ -1,6 +1,7 @@
 // Internal launch interface between the C-ABI layer (api.cu) and the kernels.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -119,6 +120,11 @@ int* device_status_ptr();
 te_status read_and_clear_device_status(int32_t* out);
 
 int num_sms();
+
+// 2-D TMA tensor map over a row-major [outer, inner] matrix of dtype, boxes of
+// box_inner x box_outer elements, 128-byte swizzle or none, out-of-bounds reads zero.
+bool make_tmap_2d(CUtensorMap* tm, const void* ptr, int dtype, uint64_t inner, uint64_t outer,
+                  uint32_t box_inner, uint32_t box_outer, bool swizzle128);
 
 // Brackets one kernel launch with profiling events when te_profile_begin is active.
 class ProfileScope {
