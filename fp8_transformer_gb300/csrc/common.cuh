@@ -52,50 +52,23 @@ __device__ __forceinline__ float2 unpack_e4m3x2(uint16_t v) {
 // sm_100+ executes two IEEE fp32 operations per f32x2 instruction (round to nearest, no
 // flush-to-zero); the bandwidth-bound kernels run their arithmetic on such pairs.
 
-using f32x2 = unsigned long long;
+using f32x2 = float2;
 
-__device__ __forceinline__ f32x2 f2(float lo, float hi) {
-  f32x2 r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-  return r;
-}
-__device__ __forceinline__ f32x2 f2s(float v) { return f2(v, v); }
-__device__ __forceinline__ float f2lo(f32x2 v) {
-  float lo, hi;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-  return lo;
-}
-__device__ __forceinline__ float f2hi(f32x2 v) {
-  float lo, hi;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-  return hi;
-}
-__device__ __forceinline__ f32x2 add2(f32x2 a, f32x2 b) {
-  f32x2 r;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-__device__ __forceinline__ f32x2 sub2(f32x2 a, f32x2 b) {
-  f32x2 r;
-  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-__device__ __forceinline__ f32x2 mul2(f32x2 a, f32x2 b) {
-  f32x2 r;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-__device__ __forceinline__ f32x2 fma2(f32x2 a, f32x2 b, f32x2 c) {
-  f32x2 r;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-  return r;
-}
+__device__ __forceinline__ f32x2 f2(float lo, float hi) { return make_float2(lo, hi); }
+__device__ __forceinline__ f32x2 f2s(float v) { return make_float2(v, v); }
+__device__ __forceinline__ float f2lo(f32x2 v) { return v.x; }
+__device__ __forceinline__ float f2hi(f32x2 v) { return v.y; }
+__device__ __forceinline__ f32x2 add2(f32x2 a, f32x2 b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ f32x2 mul2(f32x2 a, f32x2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ f32x2 fma2(f32x2 a, f32x2 b, f32x2 c) { return __ffma2_rn(a, b, c); }
+// a - b, rounded once (b * -1 is exact).
+__device__ __forceinline__ f32x2 sub2(f32x2 a, f32x2 b) { return __ffma2_rn(b, f2s(-1.0f), a); }
 // bf16x2 word -> fp32 pair (exact).
 __device__ __forceinline__ f32x2 bf16x2_f2(uint32_t w) {
   return f2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
 }
 __device__ __forceinline__ float absmax2(float m, f32x2 v) {
-  return fmaxf(m, fmaxf(fabsf(f2lo(v)), fabsf(f2hi(v))));
+  return fmaxf(m, fmaxf(fabsf(v.x), fabsf(v.y)));
 }
 
 // ------------------------------------------------------------------ activations -----------

@@ -15,6 +15,7 @@
 // at the end of the item the 8 warps combine through shared memory in warp order and write one
 // partial row, and an ordered second kernel adds the partial rows, so dbias is deterministic.
 // Every wait (the ring and the end-of-item combine) is a bounded mbarrier wait.
+#include <cstdlib>
 #include <cstring>
 
 #include "cast.cuh"
@@ -300,9 +301,19 @@ __global__ void colsum_partials_kernel(const float* partials, int chunks, int64_
 
 }  // namespace
 
+bool use_tma_streams() {
+  static int v = -1;
+  if (v < 0) {
+    const char* e = getenv("TE_STREAM_TMA");
+    v = (e && e[0] == '1') ? 1 : 0;
+  }
+  return v == 1;
+}
+
 te_status launch_act_lu(const ActArgs& a, cudaStream_t s) {
   ProfileScope prof(TE_KERNEL_ACT_LU, s);
   if (a.x_dtype != TE_BF16 && a.x_dtype != TE_F32) return TE_ERR_UNSUPPORTED;
+  if (!use_tma_streams()) return launch_act_lu_reg(a, s);
   StreamParams p;
   memset(&p, 0, sizeof(p));
   p.dact = 0;
@@ -338,7 +349,7 @@ te_status launch_dact_dbias(const DactArgs& a, cudaStream_t s) {
   p.dbias = a.dbias;
   p.partials = a.partials;
   p.cast = a.cast;
-  te_status st = launch_stream(p, a.dtype, a.dy, a.x, s);
+  te_status st = use_tma_streams() ? launch_stream(p, a.dtype, a.dy, a.x, s) : launch_dact_reg(a, s);
   if (st != TE_OK || !a.dbias) return st;
   const int chunks = int(ceil_div(a.M, kItemRows));
   colsum_partials_kernel<<<unsigned(ceil_div(a.N_in, 256)), 256, 0, s>>>(a.partials, chunks,
