@@ -279,6 +279,8 @@ def bandwidth_kernels(args, dev, peaks):
     da = random_tensor((Mb, F), device=dev, seed=4)
     a = torch.empty(Mb, F, dtype=torch.bfloat16, device=dev)
     run("act_lu_gelu_bf16", lambda: te.te_act_lu(h, "gelu", a), Mb * F * 4)
+    run("act_lu_relu_bf16", lambda: te.te_act_lu(h, "relu", a), Mb * F * 4)
+    run("act_lu_silu_bf16", lambda: te.te_act_lu(h, "silu", a), Mb * F * 4)
     # calibration points on the same tensors (library code, not part of this framework)
     run("torch_copy_bf16", lambda: a.copy_(h), Mb * F * 4)
     run("torch_gelu_tanh_bf16", lambda: torch.nn.functional.gelu(h, approximate="tanh"),
@@ -291,6 +293,9 @@ def bandwidth_kernels(args, dev, peaks):
     qg = te.Quantizer(16.0, "delayed", dev)
     run("dact_dbias_e4m3", lambda: te.te_dact_dbias_quantize(da, h, "gelu", dh, dbias=db, q=qg,
                                                              workspace=ws), Mb * F * 5 + F * 4)
+    run("dact_relu_dbias_e4m3", lambda: te.te_dact_dbias_quantize(da, h, "relu", dh, dbias=db,
+                                                                  q=qg, workspace=ws),
+        Mb * F * 5 + F * 4)
     del h, da, dh, ws
     xb = random_tensor((Mb, H), device=dev, seed=5)
     dz = random_tensor((Mb, H), device=dev, seed=6)

@@ -40,27 +40,50 @@ __device__ __forceinline__ float fake_quant1(float v, float scale, float scale_i
   return d.x * scale_inv;
 }
 
+// Output kinds, chosen once per kernel (outside every per-element loop) so that each inner
+// loop is compiled for exactly one kind.
+enum OutKind : int {
+  OUT_F32 = 0,
+  OUT_BF16 = 1,
+  OUT_E4M3 = 2,
+  OUT_FAKE_F32 = 3,   // E4M3 round trip stored as fp32
+  OUT_FAKE_BF16 = 4,  // E4M3 round trip stored as bf16
+  OUT_NONE = 5        // amax pass of current scaling: nothing stored
+};
+
+__device__ __forceinline__ int out_kind(const CastState& cs) {
+  if (!cs.store) return OUT_NONE;
+  if (cs.out_dtype == TE_E4M3) return OUT_E4M3;
+  if (cs.fake_quant) return cs.out_dtype == TE_F32 ? OUT_FAKE_F32 : OUT_FAKE_BF16;
+  return cs.out_dtype == TE_F32 ? OUT_F32 : OUT_BF16;
+}
+
+template <int K>
+struct OutTag {
+  static constexpr int value = K;
+};
+
+// Calls f(OutTag<kind>{}) with the kind as a compile-time constant.
+template <class F>
+__device__ __forceinline__ void with_out(int kind, F&& f) {
+  switch (kind) {
+    case OUT_F32: f(OutTag<OUT_F32>{}); break;
+    case OUT_BF16: f(OutTag<OUT_BF16>{}); break;
+    case OUT_E4M3: f(OutTag<OUT_E4M3>{}); break;
+    case OUT_FAKE_F32: f(OutTag<OUT_FAKE_F32>{}); break;
+    case OUT_FAKE_BF16: f(OutTag<OUT_FAKE_BF16>{}); break;
+    default: f(OutTag<OUT_NONE>{}); break;
+  }
+}
+
 // Stores N (4 or 8) consecutive values at element index `idx` (a multiple of N) of `out`.
-template <int N>
-__device__ __forceinline__ void cast_store(void* out, int64_t idx, const float (&y)[N],
-                                           const CastState& cs) {
+template <int OUT, int N>
+__device__ __forceinline__ void store_out(void* out, int64_t idx, const float (&y)[N],
+                                          const CastState& cs) {
   static_assert(N == 4 || N == 8, "vector of 4 or 8");
-  float v[N];
-#pragma unroll
-  for (int i = 0; i < N; ++i) v[i] = cs.fake_quant ? fake_quant1(y[i], cs.scale, cs.scale_inv) : y[i];
-  if (cs.out_dtype == TE_F32) {
-    float4* p = reinterpret_cast<float4*>(static_cast<float*>(out) + idx);
-    p[0] = make_float4(v[0], v[1], v[2], v[3]);
-    if constexpr (N == 8) p[1] = make_float4(v[4], v[5], v[6], v[7]);
-  } else if (cs.out_dtype == TE_BF16) {
-    uint16_t* base = static_cast<uint16_t*>(out) + idx;
-    if constexpr (N == 8) {
-      *reinterpret_cast<uint4*>(base) = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
-                                                   pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
-    } else {
-      *reinterpret_cast<uint2*>(base) = make_uint2(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]));
-    }
-  } else {  // E4M3 codes
+  if constexpr (OUT == OUT_NONE) {
+    return;
+  } else if constexpr (OUT == OUT_E4M3) {
     const float s = cs.scale;
     uint8_t* base = static_cast<uint8_t*>(out) + idx;
     if constexpr (N == 8) {
@@ -68,6 +91,25 @@ __device__ __forceinline__ void cast_store(void* out, int64_t idx, const float (
                                                    pack_e4m3x4(y[4] * s, y[5] * s, y[6] * s, y[7] * s));
     } else {
       *reinterpret_cast<uint32_t*>(base) = pack_e4m3x4(y[0] * s, y[1] * s, y[2] * s, y[3] * s);
+    }
+  } else {
+    float v[N];
+#pragma unroll
+    for (int i = 0; i < N; ++i)
+      v[i] = (OUT == OUT_FAKE_F32 || OUT == OUT_FAKE_BF16) ? fake_quant1(y[i], cs.scale, cs.scale_inv)
+                                                          : y[i];
+    if constexpr (OUT == OUT_F32 || OUT == OUT_FAKE_F32) {
+      float4* p = reinterpret_cast<float4*>(static_cast<float*>(out) + idx);
+      p[0] = make_float4(v[0], v[1], v[2], v[3]);
+      if constexpr (N == 8) p[1] = make_float4(v[4], v[5], v[6], v[7]);
+    } else {
+      uint16_t* base = static_cast<uint16_t*>(out) + idx;
+      if constexpr (N == 8) {
+        *reinterpret_cast<uint4*>(base) = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
+                                                     pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
+      } else {
+        *reinterpret_cast<uint2*>(base) = make_uint2(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]));
+      }
     }
   }
 }

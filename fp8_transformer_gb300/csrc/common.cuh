@@ -171,28 +171,30 @@ __device__ __forceinline__ void sigmoid2(f32x2 z, f32x2& s, f32x2& e) {
   s = rcp2(add2(e, f2s(1.0f)));
 }
 
+// -2 u log2(e) with u = sqrt(2/pi) (h + 0.044715 h^3), as h (c1 + c2 h^2).
+constexpr float kGeluA1 = -2.0f * kLog2e * kGeluK0;
+constexpr float kGeluA2 = -2.0f * kLog2e * kGeluK0 * kGeluK1;
+
+// gelu(h) = h s(2u) = h / (1 + 2^(-2u log2 e)); an infinite exp2 gives the correct limit 0.
 __device__ __forceinline__ f32x2 gelu2(f32x2 h) {
-  const f32x2 u = mul2(h, fma2(mul2(h, h), f2s(kGeluK0 * kGeluK1), f2s(kGeluK0)));
-  f32x2 s, e;
-  sigmoid2(add2(u, u), s, e);
-  return mul2(h, s);
+  const f32x2 a = mul2(h, fma2(mul2(h, h), f2s(kGeluA2), f2s(kGeluA1)));
+  return mul2(h, rcp2(add2(ex2_2(a), f2s(1.0f))));
 }
 
-// gelu'(h) = s + 2 h sqrt(2/pi) (1 + 3 * 0.044715 h^2) s (1 - s), s = logistic(2u).
+// gelu'(h) = s + 2 h sqrt(2/pi) (1 + 3 * 0.044715 h^2) s (1 - s), s = logistic(2u),
+// 1 - s = e s with e = exp(-2u) (the exponent is clamped so e stays finite).
 __device__ __forceinline__ f32x2 dgelu2(f32x2 h) {
   const f32x2 hh = mul2(h, h);
-  const f32x2 u = mul2(h, fma2(hh, f2s(kGeluK0 * kGeluK1), f2s(kGeluK0)));
-  f32x2 s, e;
-  sigmoid2(add2(u, u), s, e);
-  const f32x2 sn = mul2(e, s);  // 1 - s
+  const f32x2 a = min2s(mul2(h, fma2(hh, f2s(kGeluA2), f2s(kGeluA1))), 80.0f * kLog2e);
+  const f32x2 e = ex2_2(a);
+  const f32x2 s = rcp2(add2(e, f2s(1.0f)));
   const f32x2 q = mul2(h, fma2(hh, f2s(6.0f * kGeluK0 * kGeluK1), f2s(2.0f * kGeluK0)));
-  return fma2(q, mul2(s, sn), s);
+  return fma2(q, mul2(s, mul2(e, s)), s);
 }
 
+// silu(z) = z / (1 + 2^(-z log2 e)); an infinite exp2 gives the correct limit 0.
 __device__ __forceinline__ f32x2 silu2(f32x2 z) {
-  f32x2 s, e;
-  sigmoid2(z, s, e);
-  return mul2(z, s);
+  return mul2(z, rcp2(add2(ex2_2(mul2(z, f2s(-kLog2e))), f2s(1.0f))));
 }
 
 // silu'(z) = s (1 + z (1 - s)).
@@ -207,6 +209,22 @@ __device__ __forceinline__ f32x2 relu2(f32x2 h) {
 }
 __device__ __forceinline__ f32x2 drelu2(f32x2 h) {
   return f2(f2lo(h) > 0.0f ? 1.0f : 0.0f, f2hi(h) > 0.0f ? 1.0f : 0.0f);
+}
+
+// Compile-time activation choice (the inner loops are instantiated per activation).
+template <int ACT>
+__device__ __forceinline__ f32x2 act2c(f32x2 h) {
+  if constexpr (ACT == TE_RELU) return relu2(h);
+  else if constexpr (ACT == TE_GELU) return gelu2(h);
+  else if constexpr (ACT == TE_SILU) return silu2(h);
+  else return h;
+}
+template <int ACT>
+__device__ __forceinline__ f32x2 dact2c(f32x2 h) {
+  if constexpr (ACT == TE_RELU) return drelu2(h);
+  else if constexpr (ACT == TE_GELU) return dgelu2(h);
+  else if constexpr (ACT == TE_SILU) return dsilu2(h);
+  else return f2s(1.0f);
 }
 
 __device__ __forceinline__ f32x2 act2(int act, f32x2 h) {

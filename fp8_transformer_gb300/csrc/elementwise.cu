@@ -1,10 +1,19 @@
-// Bandwidth-bound kernels of the block that need no staging: the per-tensor quantize and the
-// fp32 transpose of the tf32 path.  (The activation and the backward's activation gradient +
-// bias reduction + quantize stream through TMA in stream.cu.)
+// Bandwidth-bound kernels of the block: per-tensor quantize, activation, the backward's fused
+// activation gradient + bias reduction + quantize, and the fp32 transpose of the tf32 path.
 //
 // * quantize (TransformerEngine JAX "LayerNorm Dense" page, Description: the normalized output
 //   and the kernel are quantized before the GEMM): 16-byte vectors, grid-stride, amax by one
 //   integer atomic per block.
+// * act_lu ("Activation" page, Description: the forward rule's activation primitive, optional
+//   FP8 round trip) and dact_dbias ("LayerNorm MLP" page, Description, backward: the fused
+//   quantize / dact / dbias primitive).  Each CTA owns a strip of 32 x 16-byte column vectors
+//   (one per lane) and a chunk of rows; its warps take rows in turn with several rows of loads
+//   in flight, so every access is a 512-byte coalesced row segment and no index needs a
+//   division.  The activation and the output kind are compile-time choices of the inner loop,
+//   and the arithmetic runs on f32x2 pairs with the hardware exp2 / reciprocal.  For dbias
+//   every thread sums its columns over the chunk in registers, the 8 warps of the CTA combine
+//   through shared memory in warp order, one partial row per chunk goes to the workspace, and
+//   a second kernel adds the partial rows in chunk order, so dbias is deterministic.
 #include "cast.cuh"
 #include "common.cuh"
 #include "kernels.h"
@@ -30,72 +39,75 @@ __global__ void __launch_bounds__(kEwThreads) quantize_kernel(QuantizeArgs a) {
   const CastState cs = cast_begin(a.cast);
   const int64_t nvec = a.n / E;
   float amax = 0.0f;
-  for (int64_t v = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; v < nvec;
-       v += int64_t(gridDim.x) * blockDim.x) {
-    float x[E];
-    V::load(a.x, v * E, x);
+  with_out(out_kind(cs), [&](auto tag) {
+    constexpr int OUT = decltype(tag)::value;
+    for (int64_t v = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; v < nvec;
+         v += int64_t(gridDim.x) * blockDim.x) {
+      float x[E];
+      V::load(a.x, v * E, x);
 #pragma unroll
-    for (int e = 0; e < E; ++e) amax = fmaxf(amax, fabsf(x[e]));
-    if (cs.store) cast_store<E>(a.out, v * E, x, cs);
-  }
+      for (int e = 0; e < E; ++e) amax = fmaxf(amax, fabsf(x[e]));
+      store_out<OUT, E>(a.out, v * E, x, cs);
+    }
+  });
   block_amax_commit(amax, a.cast.amax_out);
 }
 
-// ------------------------------------------------------------------ register-resident -------
-// act_lu and dact_dbias with each warp's rows of loads held in registers (the default path;
-// the TMA-staged variants live in stream.cu).  Each CTA owns a strip of 32 x 16-byte column
-// vectors and a chunk of rows; warps take rows in turn with several rows of loads in flight.
+// ------------------------------------------------------------------ act_lu ----------------
 
 constexpr int kActWarps = 8;
 constexpr int kActRows = 32;    // rows per CTA
 constexpr int kActUnroll = 4;   // rows in flight per warp
 
-// Each CTA owns a strip of 32 x 16-byte output vectors (one per lane) and kActRows rows; its
-// warps take rows in turn, kActUnroll at a time, so every load is a 512-byte coalesced row
-// segment and no index needs a division.
-template <typename T>
+template <typename T, int ACT>
 __global__ void __launch_bounds__(kActWarps * 32, 3) act_lu_kernel(ActArgs a) {
-  using V = Vec16<T>;
   using PR = Pairs<T>;
-  constexpr int E = V::N;
+  constexpr int E = Vec16<T>::N;
+  constexpr bool kGated = ACT == TE_SWIGLU;
   const CastState cs = cast_begin(a.cast);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const bool gated = a.act == TE_SWIGLU;
-  const int64_t n_out = gated ? a.N_in / 2 : a.N_in;
+  const int64_t n_out = kGated ? a.N_in / 2 : a.N_in;
   const int64_t col = (int64_t(blockIdx.x) * 32 + lane) * E;
   const int64_t r0 = int64_t(blockIdx.y) * kActRows;
   const int64_t r1 = r0 + kActRows < a.M ? r0 + kActRows : a.M;
   const T* x = static_cast<const T*>(a.x);
   const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+  const bool want_amax = a.cast.amax_out != nullptr;
   float amax = 0.0f;
   if (col < n_out) {
-    for (int64_t rb = r0 + warp; rb < r1; rb += kActUnroll * kActWarps) {
-      uint4 rg[kActUnroll], rl[kActUnroll];
+    with_out(out_kind(cs), [&](auto tag) {
+      constexpr int OUT = decltype(tag)::value;
+      for (int64_t rb = r0 + warp; rb < r1; rb += kActUnroll * kActWarps) {
+        uint4 rg[kActUnroll], rl[kActUnroll];
 #pragma unroll
-      for (int j = 0; j < kActUnroll; ++j) {
-        const int64_t r = rb + int64_t(j) * kActWarps;
-        const bool in = r < r1;
-        rg[j] = in ? __ldg(reinterpret_cast<const uint4*>(x + r * a.N_in + col)) : zero;
-        rl[j] = (in && gated) ? __ldg(reinterpret_cast<const uint4*>(x + r * a.N_in + n_out + col)) : zero;
-      }
-#pragma unroll
-      for (int j = 0; j < kActUnroll; ++j) {
-        const int64_t r = rb + int64_t(j) * kActWarps;
-        if (r >= r1) break;
-        f32x2 hp[PR::P], lp[PR::P];
-        PR::get(rg[j], hp);
-        if (gated) PR::get(rl[j], lp);
-        float y[E];
-#pragma unroll
-        for (int p = 0; p < PR::P; ++p) {
-          const f32x2 yy = gated ? mul2(silu2(hp[p]), lp[p]) : act2(a.act, hp[p]);
-          amax = absmax2(amax, yy);
-          y[2 * p] = f2lo(yy);
-          y[2 * p + 1] = f2hi(yy);
+        for (int j = 0; j < kActUnroll; ++j) {
+          const int64_t r = rb + int64_t(j) * kActWarps;
+          const bool in = r < r1;
+          rg[j] = in ? __ldg(reinterpret_cast<const uint4*>(x + r * a.N_in + col)) : zero;
+          if constexpr (kGated)
+            rl[j] = in ? __ldg(reinterpret_cast<const uint4*>(x + r * a.N_in + n_out + col)) : zero;
         }
-        if (cs.store) cast_store<E>(a.out, r * n_out + col, y, cs);
+#pragma unroll
+        for (int j = 0; j < kActUnroll; ++j) {
+          const int64_t r = rb + int64_t(j) * kActWarps;
+          if (r >= r1) break;
+          f32x2 hp[PR::P], lp[PR::P];
+          PR::get(rg[j], hp);
+          if constexpr (kGated) PR::get(rl[j], lp);
+          float y[E];
+#pragma unroll
+          for (int p = 0; p < PR::P; ++p) {
+            f32x2 yy;
+            if constexpr (kGated) yy = mul2(silu2(hp[p]), lp[p]);
+            else yy = act2c<ACT>(hp[p]);
+            if (want_amax) amax = absmax2(amax, yy);
+            y[2 * p] = f2lo(yy);
+            y[2 * p + 1] = f2hi(yy);
+          }
+          store_out<OUT, E>(a.out, r * n_out + col, y, cs);
+        }
       }
-    }
+    });
   }
   block_amax_commit(amax, a.cast.amax_out);
 }
@@ -103,89 +115,92 @@ __global__ void __launch_bounds__(kActWarps * 32, 3) act_lu_kernel(ActArgs a) {
 // ------------------------------------------------------------------ dact + dbias ----------
 
 constexpr int kDactWarps = 8;
-constexpr int kDactRows = 128;  // rows per CTA (chunk)
+constexpr int kDactRows = 128;  // rows per CTA (chunk) = rows per dbias partial
+constexpr int kDactUnroll = 2;  // rows in flight per warp
 
-constexpr int kDactUnroll = 2;  // rows in flight per warp (x 24 warps per SM)
-
-template <typename T>
+template <typename T, int ACT>
 __global__ void __launch_bounds__(kDactWarps * 32, 3) dact_dbias_kernel(DactArgs a) {
-  using V = Vec16<T>;
-  constexpr int E = V::N;
+  using PR = Pairs<T>;
+  constexpr int E = Vec16<T>::N;
+  constexpr int P = PR::P;
   constexpr int W = 32 * E;  // strip width in columns
+  constexpr bool kGated = ACT == TE_SWIGLU;
+  constexpr bool kIdent = ACT == TE_IDENTITY;
   __shared__ float red[kDactWarps][2][W];
   const CastState cs = cast_begin(a.cast);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const bool gated = a.act == TE_SWIGLU;
-  const bool ident = a.act == TE_IDENTITY;
-  const int64_t n_out = gated ? a.N_in / 2 : a.N_in;
+  const int64_t n_out = kGated ? a.N_in / 2 : a.N_in;
   const int64_t col = (int64_t(blockIdx.x) * 32 + lane) * E;
-  const bool valid = col < n_out;
   const int64_t r0 = int64_t(blockIdx.y) * kDactRows;
   const int64_t r1 = r0 + kDactRows < a.M ? r0 + kDactRows : a.M;
-  using PR = Pairs<T>;
-  constexpr int P = PR::P;
   f32x2 acc1[P], acc2[P];
 #pragma unroll
   for (int p = 0; p < P; ++p) { acc1[p] = f2s(0.0f); acc2[p] = f2s(0.0f); }
   float amax = 0.0f;
+  const bool want_amax = a.cast.amax_out != nullptr;
   const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
-  if (valid) {
-    for (int64_t rb = r0 + warp; rb < r1; rb += kDactUnroll * kDactWarps) {
-      // issue every load of kDactUnroll rows before using any of them
-      uint4 rdy[kDactUnroll], rx[kDactUnroll], rl[kDactUnroll];
+  if (col < n_out) {
+    with_out(a.dx ? out_kind(cs) : int(OUT_NONE), [&](auto tag) {
+      constexpr int OUT = decltype(tag)::value;
+      for (int64_t rb = r0 + warp; rb < r1; rb += kDactUnroll * kDactWarps) {
+        // every load of kDactUnroll rows is issued before any of them is used
+        uint4 rdy[kDactUnroll], rx[kDactUnroll], rl[kDactUnroll];
 #pragma unroll
-      for (int j = 0; j < kDactUnroll; ++j) {
-        const int64_t r = rb + int64_t(j) * kDactWarps;
-        const bool in = r < r1;
-        rdy[j] = in ? __ldg(reinterpret_cast<const uint4*>(static_cast<const T*>(a.dy) + r * n_out + col)) : zero;
-        rx[j] = (in && !ident) ? __ldg(reinterpret_cast<const uint4*>(static_cast<const T*>(a.x) + r * a.N_in + col)) : zero;
-        rl[j] = (in && gated) ? __ldg(reinterpret_cast<const uint4*>(static_cast<const T*>(a.x) + r * a.N_in + n_out + col)) : zero;
-      }
+        for (int j = 0; j < kDactUnroll; ++j) {
+          const int64_t r = rb + int64_t(j) * kDactWarps;
+          const bool in = r < r1;
+          rdy[j] = in ? __ldg(reinterpret_cast<const uint4*>(static_cast<const T*>(a.dy) + r * n_out + col)) : zero;
+          if constexpr (!kIdent)
+            rx[j] = in ? __ldg(reinterpret_cast<const uint4*>(static_cast<const T*>(a.x) + r * a.N_in + col)) : zero;
+          if constexpr (kGated)
+            rl[j] = in ? __ldg(reinterpret_cast<const uint4*>(static_cast<const T*>(a.x) + r * a.N_in + n_out + col)) : zero;
+        }
 #pragma unroll
-      for (int j = 0; j < kDactUnroll; ++j) {
-        const int64_t r = rb + int64_t(j) * kDactWarps;
-        if (r >= r1) break;
-        f32x2 dyp[P], hp[P];
-        PR::get(rdy[j], dyp);
-        PR::get(rx[j], hp);
-        if (gated) {
-          f32x2 lp[P];
-          PR::get(rl[j], lp);
-          float dg[E], dl[E];
+        for (int j = 0; j < kDactUnroll; ++j) {
+          const int64_t r = rb + int64_t(j) * kDactWarps;
+          if (r >= r1) break;
+          f32x2 dyp[P], hp[P];
+          PR::get(rdy[j], dyp);
+          if constexpr (!kIdent) PR::get(rx[j], hp);
+          if constexpr (kGated) {
+            f32x2 lp[P];
+            PR::get(rl[j], lp);
+            float dg[E], dl[E];
 #pragma unroll
-          for (int p = 0; p < P; ++p) {
-            f32x2 sg, eg;
-            sigmoid2(hp[p], sg, eg);
-            // d_gate = dy * lin * silu'(gate), d_lin = dy * silu(gate)
-            const f32x2 dsil = mul2(sg, fma2(hp[p], mul2(eg, sg), f2s(1.0f)));
-            const f32x2 g2 = mul2(mul2(dyp[p], lp[p]), dsil);
-            const f32x2 l2 = mul2(dyp[p], mul2(hp[p], sg));
-            acc1[p] = add2(acc1[p], g2);
-            acc2[p] = add2(acc2[p], l2);
-            amax = absmax2(absmax2(amax, g2), l2);
-            dg[2 * p] = f2lo(g2);
-            dg[2 * p + 1] = f2hi(g2);
-            dl[2 * p] = f2lo(l2);
-            dl[2 * p + 1] = f2hi(l2);
+            for (int p = 0; p < P; ++p) {
+              f32x2 sg, eg;
+              sigmoid2(hp[p], sg, eg);
+              // d_gate = dy * lin * silu'(gate), d_lin = dy * silu(gate)
+              const f32x2 dsil = mul2(sg, fma2(hp[p], mul2(eg, sg), f2s(1.0f)));
+              const f32x2 g2 = mul2(mul2(dyp[p], lp[p]), dsil);
+              const f32x2 l2 = mul2(dyp[p], mul2(hp[p], sg));
+              acc1[p] = add2(acc1[p], g2);
+              acc2[p] = add2(acc2[p], l2);
+              if (want_amax) amax = absmax2(absmax2(amax, g2), l2);
+              dg[2 * p] = f2lo(g2);
+              dg[2 * p + 1] = f2hi(g2);
+              dl[2 * p] = f2lo(l2);
+              dl[2 * p + 1] = f2hi(l2);
+            }
+            store_out<OUT, E>(a.dx, r * a.N_in + col, dg, cs);
+            store_out<OUT, E>(a.dx, r * a.N_in + n_out + col, dl, cs);
+          } else {
+            float d[E];
+#pragma unroll
+            for (int p = 0; p < P; ++p) {
+              f32x2 dd;
+              if constexpr (kIdent) dd = dyp[p];
+              else dd = mul2(dyp[p], dact2c<ACT>(hp[p]));
+              acc1[p] = add2(acc1[p], dd);
+              if (want_amax) amax = absmax2(amax, dd);
+              d[2 * p] = f2lo(dd);
+              d[2 * p + 1] = f2hi(dd);
+            }
+            store_out<OUT, E>(a.dx, r * a.N_in + col, d, cs);
           }
-          if (cs.store) {
-            cast_store<E>(a.dx, r * a.N_in + col, dg, cs);
-            cast_store<E>(a.dx, r * a.N_in + n_out + col, dl, cs);
-          }
-        } else {
-          float d[E];
-#pragma unroll
-          for (int p = 0; p < P; ++p) {
-            const f32x2 dd = ident ? dyp[p] : mul2(dyp[p], dact2(a.act, hp[p]));
-            acc1[p] = add2(acc1[p], dd);
-            amax = absmax2(amax, dd);
-            d[2 * p] = f2lo(dd);
-            d[2 * p + 1] = f2hi(dd);
-          }
-          if (cs.store && a.dx) cast_store<E>(a.dx, r * a.N_in + col, d, cs);
         }
       }
-    }
+    });
   }
   if (a.dbias) {
 #pragma unroll
@@ -196,28 +211,26 @@ __global__ void __launch_bounds__(kDactWarps * 32, 3) dact_dbias_kernel(DactArgs
       red[warp][1][lane * E + 2 * p + 1] = f2hi(acc2[p]);
     }
     __syncthreads();
-    // 256 threads finish the strip's column sums, each over the 8 warps in warp order.
-    const int halves = gated ? 2 : 1;
+    // the CTA's threads finish the strip's column sums, each over the 8 warps in warp order
+    const int halves = kGated ? 2 : 1;
     for (int t = threadIdx.x; t < halves * W; t += blockDim.x) {
       const int hsel = t / W, j = t % W;
-      float s = 0.0f;
+      float sum = 0.0f;
 #pragma unroll
-      for (int w = 0; w < kDactWarps; ++w) s += red[w][hsel][j];
+      for (int w = 0; w < kDactWarps; ++w) sum += red[w][hsel][j];
       const int64_t c = int64_t(blockIdx.x) * W + j;
-      if (c < n_out) a.partials[int64_t(blockIdx.y) * a.N_in + hsel * n_out + c] = s;
+      if (c < n_out) a.partials[int64_t(blockIdx.y) * a.N_in + hsel * n_out + c] = sum;
     }
   }
   block_amax_commit(amax, a.cast.amax_out);
 }
 
-template <typename T>
-te_status launch_dact_t(const DactArgs& a, cudaStream_t s) {
-  constexpr int E = Vec16<T>::N;
-  const int64_t n_out = a.act == TE_SWIGLU ? a.N_in / 2 : a.N_in;
-  const int chunks = int(ceil_div(a.M, kDactRows));
-  dim3 grid(unsigned(ceil_div(n_out, 32 * E)), unsigned(chunks));
-  dact_dbias_kernel<T><<<grid, kDactWarps * 32, 0, s>>>(a);
-  return cudaGetLastError() == cudaSuccess ? TE_OK : TE_ERR_CUDA;
+__global__ void colsum_partials_kernel(const float* partials, int chunks, int64_t n, float* out) {
+  const int64_t j = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (j >= n) return;
+  float s = 0.0f;
+  for (int c = 0; c < chunks; ++c) s += partials[int64_t(c) * n + j];
+  out[j] = s;
 }
 
 // ------------------------------------------------------------------ transpose -------------
@@ -238,28 +251,63 @@ __global__ void __launch_bounds__(256) transpose_f32_kernel(const float* src, in
   }
 }
 
-}  // namespace
-
-te_status launch_act_lu_reg(const ActArgs& a, cudaStream_t s) {
-  const int64_t n_out = a.act == TE_SWIGLU ? a.N_in / 2 : a.N_in;
-  if (a.M == 0) return TE_OK;
-  const int E = a.x_dtype == TE_BF16 ? 8 : 4;
-  if (ceil_div(a.M, kActRows) > 65535) return TE_ERR_UNSUPPORTED;
-  dim3 grid(unsigned(ceil_div(n_out, 32 * E)), unsigned(ceil_div(a.M, kActRows)));
-  if (a.x_dtype == TE_BF16) {
-    act_lu_kernel<__nv_bfloat16><<<grid, kActWarps * 32, 0, s>>>(a);
-  } else if (a.x_dtype == TE_F32) {
-    act_lu_kernel<float><<<grid, kActWarps * 32, 0, s>>>(a);
-  } else {
-    return TE_ERR_UNSUPPORTED;
+template <typename T>
+te_status launch_act_t(const ActArgs& a, dim3 grid, cudaStream_t s) {
+  switch (a.act) {
+    case TE_RELU: act_lu_kernel<T, TE_RELU><<<grid, kActWarps * 32, 0, s>>>(a); break;
+    case TE_GELU: act_lu_kernel<T, TE_GELU><<<grid, kActWarps * 32, 0, s>>>(a); break;
+    case TE_SILU: act_lu_kernel<T, TE_SILU><<<grid, kActWarps * 32, 0, s>>>(a); break;
+    case TE_SWIGLU: act_lu_kernel<T, TE_SWIGLU><<<grid, kActWarps * 32, 0, s>>>(a); break;
+    default: act_lu_kernel<T, TE_IDENTITY><<<grid, kActWarps * 32, 0, s>>>(a); break;
   }
   return cudaGetLastError() == cudaSuccess ? TE_OK : TE_ERR_CUDA;
 }
 
-te_status launch_dact_reg(const DactArgs& a, cudaStream_t s) {
-  if (a.dtype == TE_BF16) return launch_dact_t<__nv_bfloat16>(a, s);
-  if (a.dtype == TE_F32) return launch_dact_t<float>(a, s);
+template <typename T>
+te_status launch_dact_t(const DactArgs& a, dim3 grid, cudaStream_t s) {
+  switch (a.act) {
+    case TE_RELU: dact_dbias_kernel<T, TE_RELU><<<grid, kDactWarps * 32, 0, s>>>(a); break;
+    case TE_GELU: dact_dbias_kernel<T, TE_GELU><<<grid, kDactWarps * 32, 0, s>>>(a); break;
+    case TE_SILU: dact_dbias_kernel<T, TE_SILU><<<grid, kDactWarps * 32, 0, s>>>(a); break;
+    case TE_SWIGLU: dact_dbias_kernel<T, TE_SWIGLU><<<grid, kDactWarps * 32, 0, s>>>(a); break;
+    default: dact_dbias_kernel<T, TE_IDENTITY><<<grid, kDactWarps * 32, 0, s>>>(a); break;
+  }
+  return cudaGetLastError() == cudaSuccess ? TE_OK : TE_ERR_CUDA;
+}
+
+}  // namespace
+
+te_status launch_act_lu(const ActArgs& a, cudaStream_t s) {
+  ProfileScope prof(TE_KERNEL_ACT_LU, s);
+  if (a.M == 0) return TE_OK;
+  const int64_t n_out = a.act == TE_SWIGLU ? a.N_in / 2 : a.N_in;
+  const int E = a.x_dtype == TE_BF16 ? 8 : 4;
+  if (ceil_div(a.M, kActRows) > 65535) return TE_ERR_UNSUPPORTED;
+  dim3 grid(unsigned(ceil_div(n_out, 32 * E)), unsigned(ceil_div(a.M, kActRows)));
+  if (a.x_dtype == TE_BF16) return launch_act_t<__nv_bfloat16>(a, grid, s);
+  if (a.x_dtype == TE_F32) return launch_act_t<float>(a, grid, s);
   return TE_ERR_UNSUPPORTED;
+}
+
+size_t dact_dbias_workspace(int64_t M, int64_t N_in) {
+  return size_t(ceil_div(M > 0 ? M : 1, kDactRows)) * size_t(N_in) * sizeof(float);
+}
+
+te_status launch_dact_dbias(const DactArgs& a, cudaStream_t s) {
+  if (a.M == 0) return TE_OK;
+  ProfileScope prof(TE_KERNEL_DACT_DBIAS, s);
+  const int64_t n_out = a.act == TE_SWIGLU ? a.N_in / 2 : a.N_in;
+  const int E = a.dtype == TE_BF16 ? 8 : 4;
+  const int chunks = int(ceil_div(a.M, kDactRows));
+  if (chunks > 65535) return TE_ERR_UNSUPPORTED;
+  dim3 grid(unsigned(ceil_div(n_out, 32 * E)), unsigned(chunks));
+  te_status st = a.dtype == TE_BF16 ? launch_dact_t<__nv_bfloat16>(a, grid, s)
+                 : a.dtype == TE_F32 ? launch_dact_t<float>(a, grid, s)
+                                     : TE_ERR_UNSUPPORTED;
+  if (st != TE_OK || !a.dbias) return st;
+  colsum_partials_kernel<<<unsigned(ceil_div(a.N_in, 256)), 256, 0, s>>>(a.partials, chunks,
+                                                                         a.N_in, a.dbias);
+  return cudaGetLastError() == cudaSuccess ? TE_OK : TE_ERR_CUDA;
 }
 
 te_status launch_transpose_f32(const float* src, int64_t R, int64_t C, float* dst, cudaStream_t s) {

@@ -78,11 +78,6 @@ struct DactArgs {
   CastSpec cast;
 };
 te_status launch_dact_dbias(const DactArgs& a, cudaStream_t s);
-// The two implementations behind launch_act_lu / launch_dact_dbias: register-resident rows
-// (default) and TMA-staged rows (TE_STREAM_TMA=1 in the environment).  launch_dact_reg leaves
-// the final ordered reduction of the partial rows to its caller.
-te_status launch_act_lu_reg(const ActArgs& a, cudaStream_t s);
-te_status launch_dact_reg(const DactArgs& a, cudaStream_t s);
 size_t dact_dbias_workspace(int64_t M, int64_t N_in);
 
 struct QuantizeArgs {

@@ -135,7 +135,9 @@ __global__ void __launch_bounds__(kFwdMaxWarps * 32) norm_fwd_kernel(NormFwdArgs
           y[e] = (xv[e] - mean) * rs * gain + b[e];
           amax = fmaxf(amax, fabsf(y[e]));
         }
-        if (cs.store) cast_store<E>(a.out, row * a.H + int64_t(v) * E, y, cs);
+        with_out(out_kind(cs), [&](auto tag) {
+          store_out<decltype(tag)::value, E>(a.out, row * a.H + int64_t(v) * E, y, cs);
+        });
       }
     }
     __syncwarp();
@@ -190,7 +192,10 @@ __global__ void __launch_bounds__(256, 2) norm_fwd_reg_kernel(NormFwdArgs a) {
   const int nwarps = blockDim.x >> 5;
   const CastState cs = cast_begin(a.cast);
   const float inv_h = 1.0f / float(a.H);
+  const bool want_amax = a.cast.amax_out != nullptr;
   float amax = 0.0f;
+  with_out(out_kind(cs), [&](auto tag) {
+  constexpr int OUT = decltype(tag)::value;
   for (int64_t row = int64_t(blockIdx.x) * nwarps + warp; row < a.M;
        row += int64_t(gridDim.x) * nwarps) {
     const T* xr = static_cast<const T*>(a.x) + row * a.H;
@@ -230,7 +235,7 @@ __global__ void __launch_bounds__(256, 2) norm_fwd_reg_kernel(NormFwdArgs a) {
       if (a.mu) a.mu[row] = mean;
       if (a.rsigma) a.rsigma[row] = rs;
     }
-    if (cs.store || a.cast.amax_out) {
+    if (OUT != OUT_NONE || want_amax) {
       const f32x2 mean2 = f2s(mean), rs2 = f2s(rs);
 #pragma unroll
       for (int i = 0; i < NV; ++i) {
@@ -251,15 +256,16 @@ __global__ void __launch_bounds__(256, 2) norm_fwd_reg_kernel(NormFwdArgs a) {
 #pragma unroll
           for (int p = 0; p < P; ++p) {
             const f32x2 yy = fma2(sub2(xp[p], mean2), mul2(gp[p], rs2), bp[p]);
-            amax = absmax2(amax, yy);
+            if (want_amax) amax = absmax2(amax, yy);
             y[2 * p] = f2lo(yy);
             y[2 * p + 1] = f2hi(yy);
           }
-          if (cs.store) cast_store<E>(a.out, row * a.H + int64_t(v) * E, y, cs);
+          store_out<OUT, E>(a.out, row * a.H + int64_t(v) * E, y, cs);
         }
       }
     }
   }
+  });
   amax = warp_max(amax);
   if (lane == 0 && a.cast.amax_out) atomic_max_nonneg(a.cast.amax_out, amax);
 }
@@ -426,9 +432,8 @@ __global__ void __launch_bounds__(kBwdThreads, 2) norm_bwd_kernel(NormBwdArgs a)
             accg[i][e] += dz[e] * xh;
             accb[i][e] += dz[e];
           }
-          CastState cs;
-          cs.out_dtype = a.dtype;
-          cast_store<E>(a.dx, row * a.H + int64_t(v) * E, dx, cs);
+          store_out<(E == 8 ? OUT_BF16 : OUT_F32), E>(a.dx, row * a.H + int64_t(v) * E, dx,
+                                                      CastState{});
         }
       }
     }
