@@ -76,6 +76,32 @@ __device__ __forceinline__ void with_out(int kind, F&& f) {
   }
 }
 
+template <bool B>
+struct BoolTag {
+  static constexpr bool value = B;
+};
+
+// Calls f(OutTag<kind>{}, BoolTag<amax>{}) with both as compile-time constants.  The kinds that
+// quantize or only measure always take the amax (their callers always ask for it); plain fp32 /
+// bf16 stores take it when `want_amax`.
+template <class F>
+__device__ __forceinline__ void with_out_amax(int kind, bool want_amax, F&& f) {
+  switch (kind) {
+    case OUT_F32:
+      if (want_amax) f(OutTag<OUT_F32>{}, BoolTag<true>{});
+      else f(OutTag<OUT_F32>{}, BoolTag<false>{});
+      break;
+    case OUT_BF16:
+      if (want_amax) f(OutTag<OUT_BF16>{}, BoolTag<true>{});
+      else f(OutTag<OUT_BF16>{}, BoolTag<false>{});
+      break;
+    case OUT_E4M3: f(OutTag<OUT_E4M3>{}, BoolTag<true>{}); break;
+    case OUT_FAKE_F32: f(OutTag<OUT_FAKE_F32>{}, BoolTag<true>{}); break;
+    case OUT_FAKE_BF16: f(OutTag<OUT_FAKE_BF16>{}, BoolTag<true>{}); break;
+    default: f(OutTag<OUT_NONE>{}, BoolTag<true>{}); break;
+  }
+}
+
 // Stores N (4 or 8) consecutive values at element index `idx` (a multiple of N) of `out`.
 template <int OUT, int N>
 __device__ __forceinline__ void store_out(void* out, int64_t idx, const float (&y)[N],
@@ -84,13 +110,19 @@ __device__ __forceinline__ void store_out(void* out, int64_t idx, const float (&
   if constexpr (OUT == OUT_NONE) {
     return;
   } else if constexpr (OUT == OUT_E4M3) {
-    const float s = cs.scale;
+    const f32x2 s2 = f2s(cs.scale);
+    uint32_t w[N / 4];
+#pragma unroll
+    for (int i = 0; i < N / 4; ++i) {
+      const f32x2 a = mul2(f2(y[4 * i], y[4 * i + 1]), s2);
+      const f32x2 b = mul2(f2(y[4 * i + 2], y[4 * i + 3]), s2);
+      w[i] = pack_e4m3x4(f2lo(a), f2hi(a), f2lo(b), f2hi(b));
+    }
     uint8_t* base = static_cast<uint8_t*>(out) + idx;
     if constexpr (N == 8) {
-      *reinterpret_cast<uint2*>(base) = make_uint2(pack_e4m3x4(y[0] * s, y[1] * s, y[2] * s, y[3] * s),
-                                                   pack_e4m3x4(y[4] * s, y[5] * s, y[6] * s, y[7] * s));
+      *reinterpret_cast<uint2*>(base) = make_uint2(w[0], w[1]);
     } else {
-      *reinterpret_cast<uint32_t*>(base) = pack_e4m3x4(y[0] * s, y[1] * s, y[2] * s, y[3] * s);
+      *reinterpret_cast<uint32_t*>(base) = w[0];
     }
   } else {
     float v[N];
@@ -163,9 +195,10 @@ struct Vec16<float> {
   }
 };
 
-// A 16-byte vector of T as packed fp32 pairs (4 pairs of bf16, 2 pairs of fp32).  The bf16
-// expansion is volatile so that a packed row held in registers is re-expanded on each pass
-// instead of being kept expanded.
+// A 16-byte vector of T as packed fp32 pairs (4 pairs of bf16, 2 pairs of fp32).  get() expands
+// bf16 with volatile moves, so that a packed row held in registers is re-expanded on each pass
+// instead of being kept expanded; cvt() is the plain expansion, free to be scheduled, for data
+// that is read from memory right before use.
 template <typename T>
 struct Pairs;
 
@@ -182,6 +215,11 @@ struct Pairs<__nv_bfloat16> {
       p[i] = f2(lo, hi);
     }
   }
+  __device__ __forceinline__ static void cvt(const uint4& u, f32x2 (&p)[4]) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) p[i] = f2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xFFFF0000u));
+  }
 };
 
 template <>
@@ -191,6 +229,7 @@ struct Pairs<float> {
     p[0] = f2(__uint_as_float(u.x), __uint_as_float(u.y));
     p[1] = f2(__uint_as_float(u.z), __uint_as_float(u.w));
   }
+  __device__ __forceinline__ static void cvt(const uint4& u, f32x2 (&p)[2]) { get(u, p); }
 };
 
 }  // namespace te

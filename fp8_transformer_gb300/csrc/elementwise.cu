@@ -73,10 +73,13 @@ __global__ void __launch_bounds__(kActWarps * 32, 3) act_lu_kernel(ActArgs a) {
   const T* x = static_cast<const T*>(a.x);
   const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
   const bool want_amax = a.cast.amax_out != nullptr;
-  float amax = 0.0f;
+  float am[PR::P];  // one running amax per pair position: no single long chain
+#pragma unroll
+  for (int p = 0; p < PR::P; ++p) am[p] = 0.0f;
   if (col < n_out) {
-    with_out(out_kind(cs), [&](auto tag) {
+    with_out_amax(out_kind(cs), want_amax, [&](auto tag, auto atag) {
       constexpr int OUT = decltype(tag)::value;
+      constexpr bool AMAX = decltype(atag)::value;
       for (int64_t rb = r0 + warp; rb < r1; rb += kActUnroll * kActWarps) {
         uint4 rg[kActUnroll], rl[kActUnroll];
 #pragma unroll
@@ -100,7 +103,7 @@ __global__ void __launch_bounds__(kActWarps * 32, 3) act_lu_kernel(ActArgs a) {
             f32x2 yy;
             if constexpr (kGated) yy = mul2(silu2(hp[p]), lp[p]);
             else yy = act2c<ACT>(hp[p]);
-            if (want_amax) amax = absmax2(amax, yy);
+            if (AMAX) am[p] = absmax2(am[p], yy);
             y[2 * p] = f2lo(yy);
             y[2 * p + 1] = f2hi(yy);
           }
@@ -109,6 +112,9 @@ __global__ void __launch_bounds__(kActWarps * 32, 3) act_lu_kernel(ActArgs a) {
       }
     });
   }
+  float amax = am[0];
+#pragma unroll
+  for (int p = 1; p < PR::P; ++p) amax = fmaxf(amax, am[p]);
   block_amax_commit(amax, a.cast.amax_out);
 }
 
@@ -136,12 +142,15 @@ __global__ void __launch_bounds__(kDactWarps * 32, 3) dact_dbias_kernel(DactArgs
   f32x2 acc1[P], acc2[P];
 #pragma unroll
   for (int p = 0; p < P; ++p) { acc1[p] = f2s(0.0f); acc2[p] = f2s(0.0f); }
-  float amax = 0.0f;
+  float am[P];  // one running amax per pair position: no single long chain
+#pragma unroll
+  for (int p = 0; p < P; ++p) am[p] = 0.0f;
   const bool want_amax = a.cast.amax_out != nullptr;
   const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
   if (col < n_out) {
-    with_out(a.dx ? out_kind(cs) : int(OUT_NONE), [&](auto tag) {
+    with_out_amax(a.dx ? out_kind(cs) : int(OUT_NONE), want_amax, [&](auto tag, auto atag) {
       constexpr int OUT = decltype(tag)::value;
+      constexpr bool AMAX = decltype(atag)::value;
       for (int64_t rb = r0 + warp; rb < r1; rb += kDactUnroll * kDactWarps) {
         // every load of kDactUnroll rows is issued before any of them is used
         uint4 rdy[kDactUnroll], rx[kDactUnroll], rl[kDactUnroll];
@@ -176,7 +185,7 @@ __global__ void __launch_bounds__(kDactWarps * 32, 3) dact_dbias_kernel(DactArgs
               const f32x2 l2 = mul2(dyp[p], mul2(hp[p], sg));
               acc1[p] = add2(acc1[p], g2);
               acc2[p] = add2(acc2[p], l2);
-              if (want_amax) amax = absmax2(absmax2(amax, g2), l2);
+              if (AMAX) am[p] = absmax2(absmax2(am[p], g2), l2);
               dg[2 * p] = f2lo(g2);
               dg[2 * p + 1] = f2hi(g2);
               dl[2 * p] = f2lo(l2);
@@ -192,7 +201,7 @@ __global__ void __launch_bounds__(kDactWarps * 32, 3) dact_dbias_kernel(DactArgs
               if constexpr (kIdent) dd = dyp[p];
               else dd = mul2(dyp[p], dact2c<ACT>(hp[p]));
               acc1[p] = add2(acc1[p], dd);
-              if (want_amax) amax = absmax2(amax, dd);
+              if (AMAX) am[p] = absmax2(am[p], dd);
               d[2 * p] = f2lo(dd);
               d[2 * p + 1] = f2hi(dd);
             }
@@ -222,6 +231,9 @@ __global__ void __launch_bounds__(kDactWarps * 32, 3) dact_dbias_kernel(DactArgs
       if (c < n_out) a.partials[int64_t(blockIdx.y) * a.N_in + hsel * n_out + c] = sum;
     }
   }
+  float amax = am[0];
+#pragma unroll
+  for (int p = 1; p < P; ++p) amax = fmaxf(amax, am[p]);
   block_amax_commit(amax, a.cast.amax_out);
 }
 

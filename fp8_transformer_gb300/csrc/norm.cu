@@ -1,16 +1,25 @@
 // Row normalization kernels (LayerNorm / RMSNorm forward and backward).
 //
 // Forward (TransformerEngine JAX "LayerNorm MLP" page, Description step (1); "LayerNorm Dense"
-// page, Description): one warp per row, rows streamed into a per-warp double buffer in shared
-// memory by the bulk-copy engine, fp32 statistics, and the normalized row written once,
-// directly in the consumer GEMM's operand dtype (fp32, bf16 or E4M3) with 16-byte stores,
-// together with the per-tensor amax.
+// page, Description): a CTA of a few warps normalizes one row at a time, persistent over rows
+// with a stride of the grid, with eight CTAs per SM.  Each thread loads its 16-byte vectors of
+// the row straight into registers and loads the next row's while it normalizes the current
+// one; the warps' row sums meet in shared memory at one barrier per row.  Statistics are fp32,
+// and the normalized row is written once, directly in the consumer GEMM's operand dtype (fp32,
+// bf16 or E4M3), together with the per-tensor amax.  (Staging rows through shared memory with
+// bulk copies, as the backward does, measured slower here: even with no arithmetic at all that
+// path reached about 77% of the copy bandwidth at the 8192 x 4096 shape.)
 //
-// Backward (the norm's share of the backward pass, whose gradients cover every parameter): one
-// CTA walks strided groups of four rows; each row's dx needs two row sums, reduced across the
-// CTA for the whole group at one barrier; dgamma and dbeta accumulate per thread in registers,
-// are written as one partial row per CTA and summed in a fixed order by a second kernel, so the
-// result does not depend on timing.
+// Backward (the norm's share of the backward pass, whose gradients cover every parameter):
+// rows of x and dz stream through a ring of shared-memory slots.  One producer warp issues bulk
+// copies (the TMA engine's contiguous form) of the CTA's rows into the ring as far ahead as
+// free slots allow, while a group of consumer warps works on rows already in shared memory;
+// each slot has a "full" mbarrier (completed by the copies' byte count) and an "empty" one
+// (completed by the warps that read it), and every wait on them is bounded.  The row is split
+// across the group's warps; the partial row sums of a few rows at a time meet in shared memory
+// at one named barrier.  dgamma and dbeta accumulate per thread in registers, are written as
+// one partial row per group and summed in a fixed order by a second kernel, so the result does
+// not depend on timing.
 #include "cast.cuh"
 #include "common.cuh"
 #include "kernels.h"
@@ -20,434 +29,563 @@ namespace te {
 
 namespace {
 
-constexpr int kFwdMaxWarps = 8;
-constexpr size_t kFwdSmemBudget = 200 * 1024;  // row buffers per CTA
+constexpr size_t kRingSmemMax = 224 * 1024;  // dynamic shared memory per CTA
+constexpr int kFwdGroupWarps = 4;            // forward: warps per CTA (one row at a time)
+constexpr int kFwdRowsCtasPerSm = 8;         // forward: register budget, CTAs per SM
+constexpr int kBwdGroupWarps = 8;            // backward: warps per row
+constexpr int kBwdGroups = 1;                // backward: rows in progress per CTA
+constexpr int kBwdRowsPerSync = 2;           // backward: rows per barrier of a group
+constexpr int kBwdMaxSlots = 16;
+static_assert(kBwdGroupWarps == 1 || kBwdGroups <= 14,
+              "groups of several warps use named barriers 1 .. groups");
 
-// One warp per row, persistent over rows.  Each warp owns two row buffers in shared memory:
-// while it normalizes row r from one buffer, the bulk-copy engine streams row r + stride into
-// the other, so every warp keeps a whole row in flight with few registers.
-template <typename T>
-__global__ void __launch_bounds__(kFwdMaxWarps * 32) norm_fwd_kernel(NormFwdArgs a, int* status,
-                                                                     uint32_t row_bytes) {
-  using V = Vec16<T>;
-  constexpr int E = V::N;
-  extern __shared__ __align__(128) uint8_t smem[];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nwarps = blockDim.x >> 5;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem) + 2 * warp;
-  uint8_t* bufs = smem + 256 + size_t(warp) * 2 * row_bytes;
-  if (lane == 0) {
-    mbar_init(smem_u32(&bars[0]), 1);
-    mbar_init(smem_u32(&bars[1]), 1);
-    mbar_init_fence();
-  }
-  __syncwarp();
-  const CastState cs = cast_begin(a.cast);
-  const int nvec = int(a.H / E);
-  const float inv_h = 1.0f / float(a.H);
-  const bool ln = a.norm_type == TE_LAYERNORM;
-  const int64_t stride = int64_t(gridDim.x) * nwarps;
-  const char* xg = static_cast<const char*>(a.x);
-  int issued[2] = {0, 0}, waited[2] = {0, 0};  // lane 0's bookkeeping of its copies
-  float amax = 0.0f;
-  int64_t row = int64_t(blockIdx.x) * nwarps + warp;
-  if (lane == 0 && row < a.M) {
-    mbar_expect_tx(smem_u32(&bars[0]), row_bytes);
-    bulk_load(smem_u32(bufs), xg + row * row_bytes, row_bytes, smem_u32(&bars[0]));
-    issued[0]++;
-  }
-  for (int i = 0; row < a.M; ++i, row += stride) {
-    const int st = i & 1;
-    const uint32_t par = uint32_t(i >> 1) & 1u;
-    const int64_t next = row + stride;
-    if (lane == 0 && next < a.M) {
-      // the other buffer was last read in the previous iteration (ordered by __syncwarp)
-      fence_proxy_async_smem();
-      mbar_expect_tx(smem_u32(&bars[st ^ 1]), row_bytes);
-      bulk_load(smem_u32(bufs + (st ^ 1) * row_bytes), xg + next * row_bytes, row_bytes,
-                smem_u32(&bars[st ^ 1]));
-      issued[st ^ 1]++;
-    }
-    int ok = 1;
-    if (lane == 0) {
-      ok = wait_bounded(smem_u32(&bars[st]), par, nullptr, status, kWaitLimitNs, false) ? 1 : 0;
-      waited[st] += ok;
-    }
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    if (!ok) break;
-    while (!mbar_try_wait(smem_u32(&bars[st]), par)) {
-    }
-    __syncwarp();
-    const uint4* xs = reinterpret_cast<const uint4*>(bufs + st * row_bytes);
-    float mean = 0.0f, rs;
-    if (ln) {
-      float s1 = 0.0f;
-#pragma unroll 4
-      for (int v = lane; v < nvec; v += 32) {
-        float xv[E];
-        V::unpack(xs[v], xv);
-#pragma unroll
-        for (int e = 0; e < E; ++e) s1 += xv[e];
-      }
-      mean = warp_sum(s1) * inv_h;
-      float s2 = 0.0f;
-#pragma unroll 4
-      for (int v = lane; v < nvec; v += 32) {
-        float xv[E];
-        V::unpack(xs[v], xv);
-#pragma unroll
-        for (int e = 0; e < E; ++e) {
-          const float d = xv[e] - mean;
-          s2 += d * d;
-        }
-      }
-      rs = 1.0f / sqrtf(warp_sum(s2) * inv_h + a.eps);
-    } else {
-      float s2 = 0.0f;
-#pragma unroll 4
-      for (int v = lane; v < nvec; v += 32) {
-        float xv[E];
-        V::unpack(xs[v], xv);
-#pragma unroll
-        for (int e = 0; e < E; ++e) s2 += xv[e] * xv[e];
-      }
-      rs = 1.0f / sqrtf(warp_sum(s2) * inv_h + a.eps);
-    }
-    if (lane == 0) {
-      if (a.mu) a.mu[row] = mean;
-      if (a.rsigma) a.rsigma[row] = rs;
-    }
-    if (cs.store || a.cast.amax_out) {
-#pragma unroll 2
-      for (int v = lane; v < nvec; v += 32) {
-        float xv[E], g[E], b[E], y[E];
-        V::unpack(xs[v], xv);
-        V::load(a.gamma, int64_t(v) * E, g);
-        if (ln && a.beta) {
-          V::load(a.beta, int64_t(v) * E, b);
-        } else {
-#pragma unroll
-          for (int e = 0; e < E; ++e) b[e] = 0.0f;
-        }
-#pragma unroll
-        for (int e = 0; e < E; ++e) {
-          const float gain = a.zero_centered_gamma ? 1.0f + g[e] : g[e];
-          y[e] = (xv[e] - mean) * rs * gain + b[e];
-          amax = fmaxf(amax, fabsf(y[e]));
-        }
-        with_out(out_kind(cs), [&](auto tag) {
-          store_out<decltype(tag)::value, E>(a.out, row * a.H + int64_t(v) * E, y, cs);
-        });
-      }
-    }
-    __syncwarp();
-  }
-  // Copies still in flight land before the CTA may exit (only after a timeout).
-  if (lane == 0) {
-    for (int s2 = 0; s2 < 2; ++s2)
-      if (issued[s2] > waited[s2])
-        wait_bounded(smem_u32(&bars[s2]), uint32_t(waited[s2]) & 1u, nullptr, status,
-                     kDrainLimitNs, false);
-  }
-  amax = warp_max(amax);
-  if (lane == 0 && a.cast.amax_out) atomic_max_nonneg(a.cast.amax_out, amax);
+// Barrier `id` among the `nthreads` threads of one group of consumer warps, returning whether
+// `pred` was true in any of them.
+__device__ __forceinline__ bool group_sync_or(bool pred, int id, int nthreads) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(uint32_t(pred)), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
 }
 
-// Rows of up to 8 KB: one warp per row with the row resident in registers as packed 16-byte
-// vectors, persistent over rows, 2+ CTAs per SM so that many rows are in flight per SM.  The
-// gain (gamma, or 1 + gamma) and beta are expanded to fp32 in shared memory once per CTA, and
-// the arithmetic runs on packed fp32 pairs.  Statistics take one pass, shifted by the row's
-// first element (mean = x0 + E[x - x0], var = E[(x - x0)^2] - E[x - x0]^2), which avoids the
-// cancellation of the unshifted form.
-template <typename T, int NV>
-__global__ void __launch_bounds__(256, 2) norm_fwd_reg_kernel(NormFwdArgs a) {
-  using V = Vec16<T>;
+// Bytes at the start of the dynamic shared memory: full / empty barriers, the abort flag.
+__host__ __device__ constexpr size_t ring_header_bytes(int slots) {
+  return (size_t(slots) * 16 + 16 + 127) / 128 * 128;
+}
+
+// The CTA's rows are blockIdx.x, blockIdx.x + gridDim.x, ...: its local rows 0 .. nloc - 1.
+__device__ __forceinline__ int64_t local_rows(int64_t M) {
+  const int64_t b = blockIdx.x, g = gridDim.x;
+  return M > b ? (M - b + g - 1) / g : 0;
+}
+
+__device__ __forceinline__ void ring_init(uint64_t* full, uint64_t* empty, int slots,
+                                          uint32_t empty_count, volatile int* abort_flag) {
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < slots; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), empty_count);
+    }
+    *abort_flag = 0;
+    mbar_init_fence();
+  }
+  __syncthreads();
+}
+
+// Producer (one thread): for every local row k, in order, copies that row of src0 (and of
+// src1, when given, right behind it) into slot slot_of(k), after waiting for the slot's
+// previous use to be released.  Slot uses come in order: with `cons` consumer rings of `spc`
+// slots each, row k goes to ring k % cons, slot (k / cons) % spc of it.  Before returning it
+// waits for its last copies to land, so that none is in flight when the CTA exits.
+__device__ void ring_produce(const char* src0, const char* src1, uint32_t row_bytes,
+                             int64_t nloc, int cons, int spc, uint8_t* ring, uint64_t* full,
+                             uint64_t* empty, volatile int* abort_flag, int* status) {
+  const uint32_t slot_bytes = src1 ? 2 * row_bytes : row_bytes;
+  const int64_t stride = int64_t(gridDim.x) * row_bytes;
+  int64_t off = int64_t(blockIdx.x) * row_bytes;
+  int w = 0, jj = 0;
+  uint32_t use = 0;
+  int64_t k = 0;
+  for (; k < nloc; ++k, off += stride) {
+    const int s = w * spc + jj;
+    if (use > 0 && !wait_bounded(smem_u32(&empty[s]), (use - 1) & 1u, abort_flag, status,
+                                 kWaitLimitNs, true))
+      break;
+    const uint32_t dst = smem_u32(ring + size_t(s) * slot_bytes);
+    mbar_expect_tx(smem_u32(&full[s]), slot_bytes);
+    bulk_load(dst, src0 + off, row_bytes, smem_u32(&full[s]));
+    if (src1) bulk_load(dst + row_bytes, src1 + off, row_bytes, smem_u32(&full[s]));
+    if (++w == cons) {
+      w = 0;
+      if (++jj == spc) { jj = 0; ++use; }
+    }
+  }
+  // the last copy issued into each slot: rows k - cons * spc .. k - 1
+  const uint64_t limit = *abort_flag ? kDrainLimitNs : kWaitLimitNs;
+  const int64_t per_round = int64_t(cons) * spc;
+  for (int64_t j = k > per_round ? k - per_round : 0; j < k; ++j) {
+    const int64_t q = j / cons;
+    const int s = int(j % cons) * spc + int(q % spc);
+    wait_bounded(smem_u32(&full[s]), uint32_t(q / spc) & 1u, nullptr, status, limit, false);
+  }
+}
+
+// A consumer warp's wait for use `use` of slot s: lane 0 waits (bounded) and the warp barrier
+// orders the other lanes' reads of the slot after its observation of the completed copy.
+// A parity wait tells the awaited phase only from the one before it, so a caller may wait
+// for use u only once the slot's use u - 1 has completed (every caller below waits for a slot
+// after it has itself consumed the slot's previous use).
+__device__ __forceinline__ bool ring_acquire(uint64_t* full, int s, uint32_t use,
+                                             volatile int* abort_flag, int* status) {
+  const int lane = threadIdx.x & 31;
+  int ok = 1;
+  if (lane == 0 && !mbar_try_wait(smem_u32(&full[s]), use & 1u))
+    ok = wait_bounded(smem_u32(&full[s]), use & 1u, abort_flag, status, kWaitLimitNs, true) ? 1 : 0;
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  __syncwarp();
+  return ok != 0;
+}
+
+// ----------------------------------------------------------------------- forward ---------
+
+// Forward without the ring: one row per CTA of kFwdGroupWarps warps at a time, persistent over
+// rows with a stride of the grid.  Each thread loads its NVL 16-byte vectors of the row straight
+// into registers, and loads the next row's while it normalizes the current one; many CTAs per
+// SM keep enough rows in flight.  The gain and beta sit in shared memory as fp32 float4 blocks
+// (the layout above); the warps' row sums meet in shared memory at one barrier per row.
+template <typename T, bool LN, int NVL, bool FULL>
+__global__ void __launch_bounds__(kFwdGroupWarps * 32, NVL >= 8 ? kFwdRowsCtasPerSm / 2 : kFwdRowsCtasPerSm)
+    norm_fwd_rows_kernel(NormFwdArgs a) {
   using PR = Pairs<T>;
-  constexpr int E = V::N;
+  constexpr int E = Vec16<T>::N;
   constexpr int P = PR::P;
-  // gain (gamma, or 1 + gamma) and beta in fp32, laid out as float4 blocks so that the lanes of
-  // a warp, which own consecutive 16-byte input vectors, read consecutive float4s:
-  // element e of vector v sits in block (e / 4) * nvec + v, slot e % 4.
-  extern __shared__ float4 params[];
-  const int nvec = int(a.H / E);
   constexpr int Q = E / 4;
-  float4* gain4 = params;
-  float4* beta4 = params + Q * nvec;
-  const bool ln = a.norm_type == TE_LAYERNORM;
+  constexpr int G = kFwdGroupWarps;
+  constexpr int GT = G * 32;
+  extern __shared__ __align__(16) float4 prm[];
+  __shared__ float2 red[2][G];
+  const int nvec = int(a.H / E);
+  float4* gain4 = prm;
+  float4* beta4 = prm + Q * nvec;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   {
     const float shift = a.zero_centered_gamma ? 1.0f : 0.0f;
     const T* g = static_cast<const T*>(a.gamma);
     const T* b = static_cast<const T*>(a.beta);
     float* gf = reinterpret_cast<float*>(gain4);
     float* bf = reinterpret_cast<float*>(beta4);
-    for (int64_t j = threadIdx.x; j < a.H; j += blockDim.x) {
+    for (int64_t j = tid; j < a.H; j += GT) {
       const int64_t v = j / E, e = j % E;
       const int64_t slot = ((e / 4) * nvec + v) * 4 + (e % 4);
       gf[slot] = float(g[j]) + shift;
-      bf[slot] = (ln && b) ? float(b[j]) : 0.0f;
+      if (LN) bf[slot] = b ? float(b[j]) : 0.0f;
     }
   }
-  __syncthreads();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nwarps = blockDim.x >> 5;
+  auto mine = [&](int v) { return FULL || v < nvec; };
+  const T* x = static_cast<const T*>(a.x);
+  const int64_t stride = gridDim.x;
+  auto load_row = [&](int64_t row, uint4 (&r)[NVL], float& first) {
+    const uint4* xr = reinterpret_cast<const uint4*>(x + row * a.H) + tid;
+#pragma unroll
+    for (int i = 0; i < NVL; ++i)
+      r[i] = mine(tid + GT * i) ? __ldg(xr + GT * i) : make_uint4(0u, 0u, 0u, 0u);
+    if (LN) first = float(x[row * a.H]);
+  };
+  uint4 bufa[NVL], bufb[NVL];
+  float x0a = 0.0f, x0b = 0.0f;
+  int64_t row = blockIdx.x;
+  if (row < a.M) load_row(row, bufa, x0a);
+  __syncthreads();  // gain / beta ready
   const CastState cs = cast_begin(a.cast);
   const float inv_h = 1.0f / float(a.H);
   const bool want_amax = a.cast.amax_out != nullptr;
-  float amax = 0.0f;
-  with_out(out_kind(cs), [&](auto tag) {
-  constexpr int OUT = decltype(tag)::value;
-  for (int64_t row = int64_t(blockIdx.x) * nwarps + warp; row < a.M;
-       row += int64_t(gridDim.x) * nwarps) {
-    const T* xr = static_cast<const T*>(a.x) + row * a.H;
-    uint4 raw[NV];
+  float am[P];
 #pragma unroll
-    for (int i = 0; i < NV; ++i) {
-      const int v = lane + i * 32;
-      raw[i] = v < nvec ? __ldg(reinterpret_cast<const uint4*>(xr) + v) : make_uint4(0u, 0u, 0u, 0u);
-    }
-    float x0 = 0.0f;
-    if (ln) {
-      f32x2 first[P];
-      PR::get(raw[0], first);
-      x0 = __shfl_sync(0xffffffffu, f2lo(first[0]), 0);
-    }
-    const f32x2 x02 = f2s(x0);
-    f32x2 s1 = f2s(0.0f), s2 = f2s(0.0f);
+  for (int p = 0; p < P; ++p) am[p] = 0.0f;
+  with_out_amax(out_kind(cs), want_amax, [&](auto tag, auto atag) {
+    constexpr int OUT = decltype(tag)::value;
+    constexpr bool AMAX = decltype(atag)::value;
+    // normalizes row `r` held in `cur` (its first element x0); `par` picks the reduction buffer
+    auto process = [&](int64_t r, const uint4 (&cur)[NVL], float x0, int par) {
+      f32x2 s1[P], s2[P];
 #pragma unroll
-    for (int i = 0; i < NV; ++i) {
-      if (lane + i * 32 < nvec) {
-        f32x2 xp[P];
-        PR::get(raw[i], xp);
+      for (int p = 0; p < P; ++p) { s1[p] = f2s(0.0f); s2[p] = f2s(0.0f); }
+      const f32x2 x02 = f2s(x0);
 #pragma unroll
-        for (int p = 0; p < P; ++p) {
-          const f32x2 d = sub2(xp[p], x02);
-          s1 = add2(s1, d);
-          s2 = fma2(d, d, s2);
-        }
-      }
-    }
-    const float m1 = warp_sum(f2lo(s1) + f2hi(s1)) * inv_h;
-    const float m2 = warp_sum(f2lo(s2) + f2hi(s2)) * inv_h;
-    const float mean = ln ? x0 + m1 : 0.0f;
-    const float var = ln ? fmaxf(m2 - m1 * m1, 0.0f) : m2;
-    const float rs = 1.0f / sqrtf(var + a.eps);
-    if (lane == 0) {
-      if (a.mu) a.mu[row] = mean;
-      if (a.rsigma) a.rsigma[row] = rs;
-    }
-    if (OUT != OUT_NONE || want_amax) {
-      const f32x2 mean2 = f2s(mean), rs2 = f2s(rs);
-#pragma unroll
-      for (int i = 0; i < NV; ++i) {
-        const int v = lane + i * 32;
-        if (v < nvec) {
-          f32x2 xp[P], gp[P], bp[P];
-          PR::get(raw[i], xp);
-#pragma unroll
-          for (int q = 0; q < Q; ++q) {
-            const float4 g4 = gain4[q * nvec + v];
-            const float4 b4 = beta4[q * nvec + v];
-            gp[2 * q] = f2(g4.x, g4.y);
-            gp[2 * q + 1] = f2(g4.z, g4.w);
-            bp[2 * q] = f2(b4.x, b4.y);
-            bp[2 * q + 1] = f2(b4.z, b4.w);
-          }
-          float y[E];
+      for (int i = 0; i < NVL; ++i) {
+        if (mine(tid + GT * i)) {
+          f32x2 xp[P];
+          PR::cvt(cur[i], xp);
 #pragma unroll
           for (int p = 0; p < P; ++p) {
-            const f32x2 yy = fma2(sub2(xp[p], mean2), mul2(gp[p], rs2), bp[p]);
-            if (want_amax) amax = absmax2(amax, yy);
-            y[2 * p] = f2lo(yy);
-            y[2 * p + 1] = f2hi(yy);
+            if (LN) {
+              const f32x2 d = sub2(xp[p], x02);
+              s1[p] = add2(s1[p], d);
+              s2[p] = fma2(d, d, s2[p]);
+            } else {
+              s2[p] = fma2(xp[p], xp[p], s2[p]);
+            }
           }
-          store_out<OUT, E>(a.out, row * a.H + int64_t(v) * E, y, cs);
         }
       }
+#pragma unroll
+      for (int p = 1; p < P; ++p) { s1[0] = add2(s1[0], s1[p]); s2[0] = add2(s2[0], s2[p]); }
+      float t1 = LN ? f2lo(s1[0]) + f2hi(s1[0]) : 0.0f;
+      float t2 = f2lo(s2[0]) + f2hi(s2[0]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        if (LN) t1 += __shfl_xor_sync(0xffffffffu, t1, o);
+        t2 += __shfl_xor_sync(0xffffffffu, t2, o);
+      }
+      if (lane == 0) red[par][warp] = make_float2(t1, t2);
+      __syncthreads();
+      t1 = 0.0f;
+      t2 = 0.0f;
+#pragma unroll
+      for (int w = 0; w < G; ++w) {  // warp order: the same bits in every thread
+        const float2 rr = red[par][w];
+        t1 += rr.x;
+        t2 += rr.y;
+      }
+      const float m1 = LN ? t1 * inv_h : 0.0f;
+      const float m2 = t2 * inv_h;
+      const float mean = LN ? x0 + m1 : 0.0f;
+      const float var = LN ? fmaxf(m2 - m1 * m1, 0.0f) : m2;
+      const float rs = rsqrtf(var + a.eps);
+      if (tid == 0) {
+        if (a.mu) a.mu[r] = mean;
+        if (a.rsigma) a.rsigma[r] = rs;
+      }
+      if (OUT != OUT_NONE || AMAX) {
+        const f32x2 mean2 = f2s(mean), rs2 = f2s(rs);
+        const int64_t base = r * a.H + int64_t(tid) * E;
+#pragma unroll
+        for (int i = 0; i < NVL; ++i) {
+          const int v = tid + GT * i;
+          if (mine(v)) {
+            f32x2 xp[P], gp[P], bp[P];
+            PR::cvt(cur[i], xp);
+#pragma unroll
+            for (int q = 0; q < Q; ++q) {
+              const float4 g4 = gain4[q * nvec + v];
+              gp[2 * q] = f2(g4.x, g4.y);
+              gp[2 * q + 1] = f2(g4.z, g4.w);
+              if (LN) {
+                const float4 b4 = beta4[q * nvec + v];
+                bp[2 * q] = f2(b4.x, b4.y);
+                bp[2 * q + 1] = f2(b4.z, b4.w);
+              }
+            }
+            float y[E];
+#pragma unroll
+            for (int p = 0; p < P; ++p) {
+              const f32x2 yy = LN ? fma2(sub2(xp[p], mean2), mul2(gp[p], rs2), bp[p])
+                                  : mul2(mul2(xp[p], rs2), gp[p]);
+              if (AMAX) am[p] = absmax2(am[p], yy);
+              y[2 * p] = f2lo(yy);
+              y[2 * p + 1] = f2hi(yy);
+            }
+            store_out<OUT, E>(a.out, base + int64_t(GT) * E * i, y, cs);
+          }
+        }
+      }
+    };
+    // two register buffers in turn: the next row loads while the current one is processed
+    for (int par = 0; row < a.M; par ^= 1) {
+      if (row + stride < a.M) load_row(row + stride, bufb, x0b);
+      process(row, bufa, x0a, par);
+      row += stride;
+      par ^= 1;
+      if (row >= a.M) break;
+      if (row + stride < a.M) load_row(row + stride, bufa, x0a);
+      process(row, bufb, x0b, par);
+      row += stride;
     }
-  }
   });
+  float amax = am[0];
+#pragma unroll
+  for (int p = 1; p < P; ++p) amax = fmaxf(amax, am[p]);
   amax = warp_max(amax);
   if (lane == 0 && a.cast.amax_out) atomic_max_nonneg(a.cast.amax_out, amax);
 }
 
-template <typename T>
-te_status launch_fwd_smem(const NormFwdArgs& a, cudaStream_t s);
+// Sets the kernel's dynamic shared memory limit once per device.
+template <typename K>
+te_status allow_ring_smem(K kernel, bool (&done)[64]) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return TE_ERR_CUDA;
+  if (!done[dev & 63]) {
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(kRingSmemMax)) != cudaSuccess)
+      return TE_ERR_CUDA;
+    done[dev & 63] = true;
+  }
+  return TE_OK;
+}
 
-template <typename T, int NV>
-te_status launch_fwd_reg(const NormFwdArgs& a, cudaStream_t s) {
-  const int warps = 8;
-  const size_t smem = size_t(a.H) * 2 * sizeof(float);  // fp32 gain and beta
+unsigned ring_grid(int64_t M) {
+  const int64_t sms = num_sms();
+  return unsigned(M < sms ? M : sms);
+}
+
+// Ring geometry for `slot_bytes`-byte slots after `fixed` bytes of other shared data: as many
+// slots as fit (at most max_slots), shared out as rings of at least `min_spc` slots (a multiple
+// of `mult`) among at most `max_groups` groups.  Returns false if not even one ring fits.
+bool ring_shape(size_t slot_bytes, size_t fixed, int max_slots, int max_groups, int min_spc,
+                int mult, int* groups, int* spc) {
+  int slots = max_slots;
+  while (slots > 0 && ring_header_bytes(slots) + fixed + size_t(slots) * slot_bytes > kRingSmemMax)
+    --slots;
+  int g = slots / min_spc < max_groups ? slots / min_spc : max_groups;
+  if (g < 1) return false;
+  int per = slots / g;
+  per -= per % mult;
+  if (per < mult) return false;
+  *groups = g;
+  *spc = per;
+  return true;
+}
+
+template <typename T, bool LN, int NVL, bool FULL>
+te_status launch_fwd_rows(const NormFwdArgs& a, cudaStream_t s) {
+  static bool attr_done[64] = {};
+  const size_t params = size_t(a.H) * (LN ? 2 : 1) * sizeof(float);
+  const te_status st = allow_ring_smem(norm_fwd_rows_kernel<T, LN, NVL, FULL>, attr_done);
+  if (st != TE_OK) return st;
   int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, norm_fwd_reg_kernel<T, NV>,
-                                                    warps * 32, smem) != cudaSuccess || per_sm < 1)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, norm_fwd_rows_kernel<T, LN, NVL, FULL>,
+                                                    kFwdGroupWarps * 32, params) != cudaSuccess ||
+      per_sm < 1)
     per_sm = 1;
-  const int64_t needed = ceil_div(a.M, warps);
   const int64_t cap = int64_t(num_sms()) * per_sm;
-  const unsigned grid = unsigned(needed < cap ? needed : cap);
-  norm_fwd_reg_kernel<T, NV><<<grid, warps * 32, smem, s>>>(a);
+  const unsigned grid = unsigned(a.M < cap ? a.M : cap);
+  norm_fwd_rows_kernel<T, LN, NVL, FULL><<<grid, kFwdGroupWarps * 32, params, s>>>(a);
   return cudaGetLastError() == cudaSuccess ? TE_OK : TE_ERR_CUDA;
+}
+
+template <typename T, int NVL>
+te_status launch_fwd_nvl(const NormFwdArgs& a, cudaStream_t s) {
+  // (the bounds-tested form throughout: without the tests the compiler holds more of the two
+  // row buffers live and spills)
+  return a.norm_type == TE_LAYERNORM ? launch_fwd_rows<T, true, NVL, false>(a, s)
+                                     : launch_fwd_rows<T, false, NVL, false>(a, s);
 }
 
 template <typename T>
 te_status launch_fwd_t(const NormFwdArgs& a, cudaStream_t s) {
   constexpr int E = Vec16<T>::N;
-  const int64_t per_lane = ceil_div(a.H / E, 32);
-  if (per_lane <= 1) return launch_fwd_reg<T, 1>(a, s);
-  if (per_lane <= 2) return launch_fwd_reg<T, 2>(a, s);
-  if (per_lane <= 4) return launch_fwd_reg<T, 4>(a, s);
-  if (per_lane <= 8) return launch_fwd_reg<T, 8>(a, s);
-  if (per_lane <= 16) return launch_fwd_reg<T, 16>(a, s);
-  return launch_fwd_smem<T>(a, s);
-}
-
-// Longer rows: streamed through per-warp shared-memory double buffers (norm_fwd_kernel).
-template <typename T>
-te_status launch_fwd_smem(const NormFwdArgs& a, cudaStream_t s) {
-  const uint32_t row_bytes = uint32_t(a.H * sizeof(T));
-  int warps = int(kFwdSmemBudget / (2 * size_t(row_bytes)));
-  if (warps < 1) return TE_ERR_UNSUPPORTED;
-  if (warps > kFwdMaxWarps) warps = kFwdMaxWarps;
-  const size_t smem = 256 + size_t(warps) * 2 * row_bytes;
-  static bool attr_set[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (!attr_set[dev & 63]) {
-    if (cudaFuncSetAttribute(norm_fwd_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             int(256 + kFwdSmemBudget)) != cudaSuccess)
-      return TE_ERR_CUDA;
-    attr_set[dev & 63] = true;
+  constexpr int GT = kFwdGroupWarps * 32;
+  // rows are at most 16 KB, i.e. 1024 vectors
+  constexpr int kMaxNVL = (1024 + GT - 1) / GT;
+  const int64_t per_thread = ceil_div(a.H / E, GT);
+  if (per_thread <= 1) return launch_fwd_nvl<T, 1>(a, s);
+  if (per_thread <= 2) return launch_fwd_nvl<T, 2>(a, s);
+  if (per_thread <= 4) return launch_fwd_nvl<T, 4>(a, s);
+  if constexpr (kMaxNVL > 4) {
+    if (per_thread <= 8) return launch_fwd_nvl<T, 8>(a, s);
   }
-  int per_sm = int((227 * 1024) / smem);
-  if (per_sm < 1) per_sm = 1;
-  if (per_sm * warps > 64) per_sm = 64 / warps;
-  const int64_t needed = ceil_div(a.M, warps);
-  const int64_t cap = int64_t(num_sms()) * per_sm;
-  const unsigned grid = unsigned(needed < cap ? needed : cap);
-  norm_fwd_kernel<T><<<grid, warps * 32, smem, s>>>(a, device_status_ptr(), row_bytes);
-  return cudaGetLastError() == cudaSuccess ? TE_OK : TE_ERR_CUDA;
+  if constexpr (kMaxNVL > 8) {
+    if (per_thread <= 16) return launch_fwd_nvl<T, 16>(a, s);
+  }
+  if constexpr (kMaxNVL > 16) {
+    if (per_thread <= 32) return launch_fwd_nvl<T, 32>(a, s);
+  }
+  return TE_ERR_UNSUPPORTED;
 }
 
 // ----------------------------------------------------------------------- backward --------
 
-constexpr int kBwdThreads = 256;
-constexpr int kBwdWarps = kBwdThreads / 32;
-constexpr int kBwdRows = 4;  // rows per CTA between two barriers, for rows of <= 4 KB
+// The consumer warps form groups of kBwdGroupWarps; group c takes local rows c, c + groups, ...
+// through its own ring of `spc` slots, kBwdRowsPerSync rows (consecutive slots of the ring) per
+// step.  Thread t of a group owns the 16-byte vectors t, t + 32 * kBwdGroupWarps, ... of each
+// row (NV of them), with its gamma vectors and dgamma / dbeta accumulators in registers; the
+// row sums of a step meet in shared memory at one barrier of the group, which also carries each
+// warp's "wait failed" flag so that the group's warps stop together.  A slot holds one row of x
+// followed by the same row of dz.  Each group writes one partial dgamma / dbeta row.
+// Rows per barrier step for NV vectors per thread (more rows per step hold more registers).
+__host__ __device__ constexpr int bwd_rows_per_sync(int nv) { return nv >= 4 ? 1 : kBwdRowsPerSync; }
 
-// Rows per barrier for NV vectors per thread (the first pass holds the group's x and dz in
-// registers).
-__host__ __device__ constexpr int bwd_rows(int nv) { return nv >= 4 ? 2 : 4; }
-
-// One CTA per group of kBwdRows rows at a time (persistent over groups).  Each row's dx needs
-// two row sums; the CTA reduces the sums of all its rows with one barrier.  dgamma / dbeta
-// accumulate per thread in registers over every row the CTA visits.
-template <typename T, int NV>
-__global__ void __launch_bounds__(kBwdThreads, 2) norm_bwd_kernel(NormBwdArgs a) {
-  using V = Vec16<T>;
-  constexpr int E = V::N;
-  constexpr int R = bwd_rows(NV);
-  __shared__ float red[2][kBwdWarps][R][2];
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+template <typename T, bool LN, int NV, bool FULL>
+__global__ void __launch_bounds__((kBwdGroups * kBwdGroupWarps + 1) * 32, 1)
+    norm_bwd_ring_kernel(NormBwdArgs a, int* status, int spc) {
+  using PR = Pairs<T>;
+  constexpr int E = Vec16<T>::N;
+  constexpr int P = PR::P;
+  constexpr int G = kBwdGroupWarps;
+  constexpr int GT = G * 32;
+  constexpr int RB = bwd_rows_per_sync(NV);
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ float2 red[kBwdGroups][2][RB][G];
+  const int groups = (int(blockDim.x >> 5) - 1) / G;  // the last warp produces
+  const int slots = groups * spc;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+  uint64_t* empty = full + slots;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + slots);
+  uint8_t* ring = smem + ring_header_bytes(slots);
   const int nvec = int(a.H / E);
+  const uint32_t row_bytes = uint32_t(a.H) * uint32_t(sizeof(T));
+  const int64_t nloc = local_rows(a.M);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  ring_init(full, empty, slots, G, abort_flag);
+
+  if (warp == groups * G) {
+    if (lane == 0)
+      ring_produce(static_cast<const char*>(a.x), static_cast<const char*>(a.dz), row_bytes, nloc,
+                   groups, spc, ring, full, empty, abort_flag, status);
+    return;
+  }
+
+  // FULL: every thread owns exactly NV vectors of every row (no bounds tests)
+  auto mine = [&](int v) { return FULL || v < nvec; };
+  const int grp = warp / G, wg = warp % G, gt = wg * 32 + lane;
   const float inv_h = 1.0f / float(a.H);
-  const bool ln = a.norm_type == TE_LAYERNORM;
-  const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
-  uint4 graw[NV];
-  float accg[NV][E], accb[NV][E];
+  const f32x2 gshift = f2s(a.zero_centered_gamma ? 1.0f : 0.0f);
+  f32x2 gp[NV][P], accg[NV][P], accb[NV][P];
 #pragma unroll
   for (int i = 0; i < NV; ++i) {
-    const int v = tid + i * kBwdThreads;
-    graw[i] = v < nvec ? __ldg(reinterpret_cast<const uint4*>(static_cast<const T*>(a.gamma)) + v) : zero;
+    const int v = gt + i * GT;
+    const uint4 graw = mine(v) ? __ldg(reinterpret_cast<const uint4*>(a.gamma) + v)
+                               : make_uint4(0u, 0u, 0u, 0u);
+    PR::cvt(graw, gp[i]);
 #pragma unroll
-    for (int e = 0; e < E; ++e) { accg[i][e] = 0.0f; accb[i][e] = 0.0f; }
+    for (int p = 0; p < P; ++p) {
+      gp[i][p] = add2(gp[i][p], gshift);
+      accg[i][p] = f2s(0.0f);
+      accb[i][p] = f2s(0.0f);
+    }
   }
-  const float gshift = a.zero_centered_gamma ? 1.0f : 0.0f;
-  int parity = 0;
-  for (int64_t r0 = int64_t(blockIdx.x) * R; r0 < a.M; r0 += int64_t(gridDim.x) * R, parity ^= 1) {
-    uint4 rx[R][NV], rdz[R][NV];
-    float mu[R], rs[R];
+  // The group's j-th row is local row grp + j * groups, i.e. global row
+  // blockIdx.x + (grp + j * groups) * gridDim.x: consecutive rows of the group are row_step apart.
+  const int64_t nmine = nloc > grp ? (nloc - grp + groups - 1) / groups : 0;
+  const int64_t row_step = int64_t(groups) * gridDim.x;
+  const int64_t row_first = int64_t(blockIdx.x) + int64_t(grp) * gridDim.x;
+  const uint32_t slot_bytes = 2 * row_bytes;
+  float mu_n[RB], rs_n[RB];
 #pragma unroll
-    for (int j = 0; j < R; ++j) {
-      const int64_t row = r0 + j;
-      const bool in = row < a.M;
-      mu[j] = (in && ln) ? a.mu[row] : 0.0f;
-      rs[j] = in ? a.rsigma[row] : 0.0f;
+  for (int j = 0; j < RB; ++j) {
+    const int64_t row = row_first + j * row_step;
+    mu_n[j] = (LN && j < nmine) ? a.mu[row] : 0.0f;
+    rs_n[j] = j < nmine ? a.rsigma[row] : 0.0f;
+  }
+  T* dx_first = static_cast<T*>(a.dx) + row_first * a.H + gt * E;
+  const int64_t dx_step = row_step * a.H;
+  int jj = 0;
+  uint32_t use = 0;
+  int64_t row0 = row_first;
+  T* dx0 = dx_first;
+  for (int64_t j0 = 0, it = 0; j0 < nmine;
+       j0 += RB, ++it, row0 += RB * row_step, dx0 += RB * dx_step) {
+    const int nr = nmine - j0 < RB ? int(nmine - j0) : RB;
+    f32x2 mu2[RB], rs2[RB];
 #pragma unroll
-      for (int i = 0; i < NV; ++i) {
-        const int v = tid + i * kBwdThreads;
-        const bool ok = in && v < nvec;
-        rx[j][i] = ok ? __ldg(reinterpret_cast<const uint4*>(static_cast<const T*>(a.x) + row * a.H) + v) : zero;
-        rdz[j][i] = ok ? __ldg(reinterpret_cast<const uint4*>(static_cast<const T*>(a.dz) + row * a.H) + v) : zero;
+    for (int j = 0; j < RB; ++j) {
+      mu2[j] = f2s(mu_n[j]);
+      rs2[j] = f2s(rs_n[j]);
+      if (j0 + RB + j < nmine) {  // the next step's statistics load while this step runs
+        const int64_t row = row0 + (RB + j) * row_step;
+        mu_n[j] = LN ? a.mu[row] : 0.0f;
+        rs_n[j] = a.rsigma[row];
       }
     }
+    const int s0 = grp * spc + jj;
+    const uint8_t* slot0 = ring + uint32_t(s0) * slot_bytes;
+    bool ok = true;
 #pragma unroll
-    for (int j = 0; j < R; ++j) {
-      float s1 = 0.0f, s2 = 0.0f;
+    for (int j = 0; j < RB; ++j)
+      if (j < nr && ok) ok = ring_acquire(full, s0 + j, use, abort_flag, status);
+    // pass 1: sum(dz * g) and sum(dz * g * xhat) over each row
+    float t1[RB], t2[RB];
 #pragma unroll
-      for (int i = 0; i < NV; ++i) {
-        float xv[E], dz[E], g[E];
-        V::unpack(rx[j][i], xv);
-        V::unpack(rdz[j][i], dz);
-        V::unpack(graw[i], g);
+    for (int j = 0; j < RB; ++j) {
+      f32x2 s1 = f2s(0.0f), s2 = f2s(0.0f);
+      if (ok && j < nr) {
+        const uint4* xs = reinterpret_cast<const uint4*>(slot0 + j * slot_bytes) + gt;
+        const uint4* dzs = xs + nvec;
 #pragma unroll
-        for (int e = 0; e < E; ++e) {
-          const float dyg = dz[e] * (g[e] + gshift);
-          s1 += dyg;
-          s2 += dyg * ((xv[e] - mu[j]) * rs[j]);
-        }
-      }
-      s1 = warp_sum(s1);
-      s2 = warp_sum(s2);
-      if (lane == 0) {
-        red[parity][warp][j][0] = s1;
-        red[parity][warp][j][1] = s2;
-      }
-    }
-    __syncthreads();
+        for (int i = 0; i < NV; ++i) {
+          if (mine(gt + i * GT)) {
+            f32x2 xp[P], dp[P];
+            PR::cvt(xs[i * GT], xp);
+            PR::cvt(dzs[i * GT], dp);
 #pragma unroll
-    for (int j = 0; j < R; ++j) {
-      const int64_t row = r0 + j;
-      if (row >= a.M) break;
-      float s1 = 0.0f, s2 = 0.0f;
-#pragma unroll
-      for (int w = 0; w < kBwdWarps; ++w) {
-        s1 += red[parity][w][j][0];
-        s2 += red[parity][w][j][1];
-      }
-      const float m1 = ln ? s1 * inv_h : 0.0f;
-      const float m2 = s2 * inv_h;
-#pragma unroll
-      for (int i = 0; i < NV; ++i) {
-        const int v = tid + i * kBwdThreads;
-        if (v < nvec) {
-          // x and dz come again from cache (L1/L2): keeping the group's rows in registers
-          // across the barrier would spill.
-          float xv[E], dz[E], g[E], dx[E];
-          V::unpack(ldg16_ordered(static_cast<const T*>(a.x) + row * a.H + int64_t(v) * E), xv);
-          V::unpack(ldg16_ordered(static_cast<const T*>(a.dz) + row * a.H + int64_t(v) * E), dz);
-          V::unpack(graw[i], g);
-#pragma unroll
-          for (int e = 0; e < E; ++e) {
-            const float xh = (xv[e] - mu[j]) * rs[j];
-            dx[e] = rs[j] * (dz[e] * (g[e] + gshift) - m1 - xh * m2);
-            accg[i][e] += dz[e] * xh;
-            accb[i][e] += dz[e];
+            for (int p = 0; p < P; ++p) {
+              const f32x2 xh = LN ? mul2(sub2(xp[p], mu2[j]), rs2[j]) : mul2(xp[p], rs2[j]);
+              const f32x2 dyg = mul2(dp[p], gp[i][p]);
+              if (LN) s1 = add2(s1, dyg);
+              s2 = fma2(dyg, xh, s2);
+            }
           }
-          store_out<(E == 8 ? OUT_BF16 : OUT_F32), E>(a.dx, row * a.H + int64_t(v) * E, dx,
-                                                      CastState{});
+        }
+      }
+      t1[j] = LN ? f2lo(s1) + f2hi(s1) : 0.0f;
+      t2[j] = f2lo(s2) + f2hi(s2);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+      for (int j = 0; j < RB; ++j) {
+        if (LN) t1[j] += __shfl_xor_sync(0xffffffffu, t1[j], o);
+        t2[j] += __shfl_xor_sync(0xffffffffu, t2[j], o);
+      }
+    }
+    const int par = int(it & 1);
+    if (lane == 0) {
+#pragma unroll
+      for (int j = 0; j < RB; ++j) red[grp][par][j][wg] = make_float2(t1[j], t2[j]);
+    }
+    if (group_sync_or(!ok, 1 + grp, GT)) break;
+    // the group's warps add their sums in warp order (the same bits in every thread)
+    f32x2 m1[RB], m2[RB];
+#pragma unroll
+    for (int j = 0; j < RB; ++j) {
+      float r1 = 0.0f, r2 = 0.0f;
+#pragma unroll
+      for (int w = 0; w < G; ++w) {
+        const float2 r = red[grp][par][j][w];
+        r1 += r.x;
+        r2 += r.y;
+      }
+      m1[j] = f2s(LN ? -r1 * inv_h : 0.0f);  // negated, for the fma below
+      m2[j] = f2s(-r2 * inv_h);
+    }
+    // pass 2: dx = rs * (dz * g - m1 - xhat * m2); dgamma += dz * xhat; dbeta += dz
+#pragma unroll
+    for (int j = 0; j < RB; ++j) {
+      if (j < nr) {
+        const uint4* xs = reinterpret_cast<const uint4*>(slot0 + j * slot_bytes) + gt;
+        const uint4* dzs = xs + nvec;
+        T* dxr = dx0 + j * dx_step;
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+          if (mine(gt + i * GT)) {
+            f32x2 xp[P], dp[P];
+            PR::cvt(xs[i * GT], xp);
+            PR::cvt(dzs[i * GT], dp);
+            float d[E];
+#pragma unroll
+            for (int p = 0; p < P; ++p) {
+              const f32x2 xh = LN ? mul2(sub2(xp[p], mu2[j]), rs2[j]) : mul2(xp[p], rs2[j]);
+              const f32x2 t = fma2(xh, m2[j], fma2(dp[p], gp[i][p], m1[j]));
+              const f32x2 dd = mul2(t, rs2[j]);
+              accg[i][p] = fma2(dp[p], xh, accg[i][p]);
+              if (LN) accb[i][p] = add2(accb[i][p], dp[p]);
+              d[2 * p] = f2lo(dd);
+              d[2 * p + 1] = f2hi(dd);
+            }
+            store_out<(E == 8 ? OUT_BF16 : OUT_F32), E>(dxr, int64_t(i) * GT * E, d, CastState{});
+          }
         }
       }
     }
+    __syncwarp();
+    if (lane == 0) {
+#pragma unroll
+      for (int j = 0; j < RB; ++j)
+        if (j < nr) mbar_arrive(smem_u32(&empty[s0 + j]));
+    }
+    jj += RB;
+    if (jj == spc) { jj = 0; ++use; }
   }
-  float* pg = a.partials + int64_t(blockIdx.x) * 2 * a.H;
+  float* pg = a.partials + (int64_t(blockIdx.x) * groups + grp) * 2 * a.H;
   float* pb = pg + a.H;
 #pragma unroll
   for (int i = 0; i < NV; ++i) {
-    const int v = tid + i * kBwdThreads;
-    if (v < nvec) {
+    const int v = gt + i * GT;
+    if (mine(v)) {
+      float4* g4 = reinterpret_cast<float4*>(pg + int64_t(v) * E);
+      float4* b4 = reinterpret_cast<float4*>(pb + int64_t(v) * E);
 #pragma unroll
-      for (int e = 0; e < E; ++e) {
-        pg[int64_t(v) * E + e] = accg[i][e];
-        pb[int64_t(v) * E + e] = accb[i][e];
+      for (int q = 0; q < P / 2; ++q) {
+        g4[q] = make_float4(f2lo(accg[i][2 * q]), f2hi(accg[i][2 * q]), f2lo(accg[i][2 * q + 1]),
+                            f2hi(accg[i][2 * q + 1]));
+        b4[q] = make_float4(f2lo(accb[i][2 * q]), f2hi(accb[i][2 * q]), f2lo(accb[i][2 * q + 1]),
+                            f2hi(accb[i][2 * q + 1]));
       }
     }
   }
@@ -467,29 +605,49 @@ __global__ void norm_bwd_reduce_kernel(const float* partials, int chunks, int64_
   if (dbeta) dbeta[j] = sb;
 }
 
-int bwd_chunks(int64_t M) {
-  // enough row groups for the smallest group size (one row), capped at the resident CTAs
-  const int64_t groups = M;
-  const int64_t resident = int64_t(num_sms()) * 2;
-  return int(groups < resident ? groups : resident);
+// Partial dgamma / dbeta rows: one per group of every CTA (groups = kBwdGroups at most).
+int bwd_chunks(int64_t M) { return int(ring_grid(M > 0 ? M : 1)) * kBwdGroups; }
+
+template <typename T, bool LN, int NV, bool FULL>
+te_status launch_bwd_t(const NormBwdArgs& a, cudaStream_t s) {
+  static bool attr_done[64] = {};
+  constexpr int RB = bwd_rows_per_sync(NV);
+  const size_t slot_bytes = size_t(a.H) * sizeof(T) * 2;
+  int groups = 0, spc = 0;
+  if (!ring_shape(slot_bytes, 0, kBwdMaxSlots, kBwdGroups, 2 * RB, RB, &groups, &spc))
+    return TE_ERR_UNSUPPORTED;
+  const size_t smem = ring_header_bytes(groups * spc) + size_t(groups * spc) * slot_bytes;
+  const te_status st = allow_ring_smem(norm_bwd_ring_kernel<T, LN, NV, FULL>, attr_done);
+  if (st != TE_OK) return st;
+  const unsigned grid = ring_grid(a.M);
+  norm_bwd_ring_kernel<T, LN, NV, FULL><<<grid, (groups * kBwdGroupWarps + 1) * 32, smem, s>>>(
+      a, device_status_ptr(), spc);
+  norm_bwd_reduce_kernel<<<unsigned(ceil_div(a.H, 256)), 256, 0, s>>>(
+      a.partials, int(grid) * groups, a.H, a.dgamma, a.dbeta);
+  return cudaGetLastError() == cudaSuccess ? TE_OK : TE_ERR_CUDA;
 }
 
 template <typename T, int NV>
-te_status launch_bwd_t(const NormBwdArgs& a, cudaStream_t s) {
-  const int chunks = bwd_chunks(a.M);
-  norm_bwd_kernel<T, NV><<<chunks, kBwdThreads, 0, s>>>(a);
-  norm_bwd_reduce_kernel<<<unsigned(ceil_div(a.H, 256)), 256, 0, s>>>(a.partials, chunks, a.H,
-                                                                       a.dgamma, a.dbeta);
-  return cudaGetLastError() == cudaSuccess ? TE_OK : TE_ERR_CUDA;
+te_status launch_bwd_nv(const NormBwdArgs& a, cudaStream_t s) {
+  const bool full = a.H / Vec16<T>::N == int64_t(NV) * kBwdGroupWarps * 32;
+  if (a.norm_type == TE_LAYERNORM)
+    return full ? launch_bwd_t<T, true, NV, true>(a, s) : launch_bwd_t<T, true, NV, false>(a, s);
+  return full ? launch_bwd_t<T, false, NV, true>(a, s) : launch_bwd_t<T, false, NV, false>(a, s);
 }
 
 template <typename T>
 te_status launch_bwd_dispatch(const NormBwdArgs& a, cudaStream_t s) {
   constexpr int E = Vec16<T>::N;
-  const int64_t per_thread = ceil_div(a.H / E, kBwdThreads);
-  if (per_thread <= 1) return launch_bwd_t<T, 1>(a, s);
-  if (per_thread <= 2) return launch_bwd_t<T, 2>(a, s);
-  if (per_thread <= 4) return launch_bwd_t<T, 4>(a, s);
+  // rows are at most 16 KB, i.e. 1024 vectors
+  constexpr int kMaxNV = (1024 + kBwdGroupWarps * 32 - 1) / (kBwdGroupWarps * 32);
+  const int64_t per_thread = ceil_div(a.H / E, kBwdGroupWarps * 32);
+  if (per_thread <= 1) return launch_bwd_nv<T, 1>(a, s);
+  if constexpr (kMaxNV >= 2) {
+    if (per_thread <= 2) return launch_bwd_nv<T, 2>(a, s);
+  }
+  if constexpr (kMaxNV >= 4) {
+    if (per_thread <= 4) return launch_bwd_nv<T, 4>(a, s);
+  }
   return TE_ERR_UNSUPPORTED;
 }
 
@@ -504,7 +662,7 @@ te_status launch_norm_fwd(const NormFwdArgs& a, cudaStream_t s) {
 }
 
 size_t norm_bwd_workspace(int64_t M, int64_t H) {
-  return size_t(bwd_chunks(M > 0 ? M : 1)) * 2 * size_t(H) * sizeof(float);
+  return size_t(bwd_chunks(M)) * 2 * size_t(H) * sizeof(float);
 }
 
 te_status launch_norm_bwd(const NormBwdArgs& a, cudaStream_t s) {

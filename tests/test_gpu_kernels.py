@@ -152,7 +152,8 @@ def test_dbias_deterministic():
 
 @pytest.mark.parametrize("norm", ["layernorm", "rmsnorm"])
 @pytest.mark.parametrize("M,H,dtype", [(1, 128, "f32"), (129, 136, "bf16"), (1000, 4096, "bf16"),
-                                       (70, 8192, "bf16"), (64, 128, "f32")])
+                                       (70, 8192, "bf16"), (64, 128, "f32"), (70, 4096, "f32"),
+                                       (9000, 1024, "bf16")])
 @pytest.mark.parametrize("zc", [False, True])
 def test_norm_fwd(norm, M, H, dtype, zc):
     x = rt((M, H), std=2.0, seed=11, dtype=dtype, mean=0.5)
@@ -208,21 +209,26 @@ def test_norm_scale_identity_outlier_rows():
 
 
 @pytest.mark.parametrize("norm", ["layernorm", "rmsnorm"])
-@pytest.mark.parametrize("M,H", [(1, 128), (300, 1032), (2000, 4096)])
-def test_norm_bwd(norm, M, H):
-    x = rt((M, H), std=2.0, seed=20)
-    gamma = rt((H,), 0.1, 21, mean=1.0)
-    dz = rt((M, H), seed=22)
+@pytest.mark.parametrize("M,H,dtype", [(1, 128, "bf16"), (300, 1032, "bf16"), (2000, 4096, "bf16"),
+                                       (5000, 2048, "bf16"), (64, 8192, "bf16"),
+                                       (300, 1032, "f32"), (70, 4096, "f32")])
+def test_norm_bwd(norm, M, H, dtype):
+    """Rows are dealt to CTAs round-robin and streamed through a ring of shared-memory slots;
+    the (5000, 2048) case passes through every slot of the ring more than twice."""
+    x = rt((M, H), std=2.0, seed=20, dtype=dtype)
+    gamma = rt((H,), 0.1, 21, mean=1.0, dtype=dtype)
+    dz = rt((M, H), seed=22, dtype=dtype)
     _, mu, rs = ob.norm_fwd(np64(x), np64(gamma), None if norm == "rmsnorm" else np.zeros(H),
                             norm, False, 1e-5)
     mu_t = torch.tensor(mu, dtype=torch.float32, device=DEV)
     rs_t = torch.tensor(rs, dtype=torch.float32, device=DEV)
-    dx = torch.empty(M, H, dtype=torch.bfloat16, device=DEV)
+    dx = torch.empty(M, H, dtype=TDT[dtype], device=DEV)
     dg = torch.empty(H, dtype=torch.float32, device=DEV)
     db = torch.empty(H, dtype=torch.float32, device=DEV)
     te.te_norm_bwd(dz, x, mu_t, rs_t, gamma, norm, False, dx, dg, db)
     rdx, rdg, rdb = ob.norm_bwd(np64(dz), np64(x), np64(mu_t), np64(rs_t), np64(gamma), norm, False)
-    assert_elementwise_close(dx, nx.bf16_round(nx.to_f32(rdx)), what="dx", abs_rms=2e-3)
+    want = nx.to_f32(rdx) if dtype == "f32" else nx.bf16_round(nx.to_f32(rdx))
+    assert_elementwise_close(dx, want, what="dx", abs_rms=2e-3)
     assert_reduction_close(dg, rdg, what="dgamma")
     if norm == "layernorm":
         assert_reduction_close(db, rdb, what="dbeta")
