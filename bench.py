@@ -40,7 +40,7 @@ def make_flush(dev):
     alone took a 64 MB copy from 97% to 76% of the copy bandwidth)."""
     import torch
     buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    words = buf.view(torch.int32)
+    words = buf.view(torch.float32)  # summed as is, with no widening copy
 
     def flush():
         buf.zero_()
@@ -75,8 +75,9 @@ TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "gemm_pair_traffic_llama_full.m
 
 
 def measured_traffic():
-    """DRAM bytes per GEMM1 launch from the committed ncu capture, or None when the kernel source
-    changed since the counters were taken (the capture records the source's sha256)."""
+    """DRAM bytes per GEMM1 launch from the committed ncu capture, or None when any source the
+    GEMM kernel is compiled from changed since the counters were taken (the capture records
+    the sha256 of those files, concatenated in the listed order)."""
     import hashlib
     try:
         fields = {}
@@ -85,13 +86,20 @@ def measured_traffic():
                 if ":" in line and not line.startswith(("|", "#", "`")):
                     k, v = line.split(":", 1)
                     fields[k.strip()] = v.strip()
-        src = os.path.join(ROOT, fields["source"])
-        with open(src, "rb") as f:
-            if hashlib.sha256(f.read()).hexdigest() != fields["source sha256"]:
-                return None
+        h = hashlib.sha256()
+        for rel in fields["sources"].split():
+            with open(os.path.join(ROOT, rel), "rb") as f:
+                h.update(f.read())
+        if h.hexdigest() != fields["sources sha256"]:
+            return None
         return int(fields["traffic_bytes_per_launch"])
     except Exception:
         return None
+
+
+GEMM_SOURCES = ["fp8_transformer_gb300/csrc/gemm.cu", "fp8_transformer_gb300/csrc/common.cuh",
+                "fp8_transformer_gb300/csrc/sync.cuh", "fp8_transformer_gb300/csrc/kernels.h",
+                "include/te_gb300.h"]
 
 
 def load_peaks():
