@@ -350,3 +350,37 @@ def layernorm_mlp_bwd(dy, x, gamma, beta, w1, w2, b1, b2, norm_type="layernorm",
                                  zero_centered_gamma)
     return dict(fwd=fwd, db2=db2, a_re=a_re, dW2=dW2, da=da, dh=dh, db1=db1, dln=dln, dW1=dW1,
                 dx=Stored(dx, dtype), dgamma=dgamma, dbeta=dbeta)
+
+
+def layernorm_dense_bwd(dy, x, gamma, beta, kernel, bias, norm_type="layernorm",
+                        zero_centered_gamma=False, eps=1e-6, dtype="bf16", fp8=None):
+    """Backward of ``layernorm_dense_fwd`` (LayerNorm Dense page, Description: the gradients of
+    x, the kernel, gamma, beta and the bias, with FP8 intermediate gradients).
+
+    Order: dbias = colsum(dy) over the unquantized dy; dy is the GEMM operand (E4M3 with the
+    ``grad`` scale, or its own amax, when ``fp8`` is given; else ``dtype``); dln = dy kernel^T;
+    dkernel = ln^T dy; then the norm backward gives dx, dgamma, dbeta.  In FP8 mode the GEMM
+    operands are dy, the forward's normalized output and the kernel, all E4M3.
+    ``fp8`` = None or a dict of fp32 scales ``x``, ``kernel`` and ``grad`` (None: own amax).
+    """
+    fwd = layernorm_dense_fwd(x, kernel, gamma, beta, bias, norm_type, zero_centered_gamma, eps,
+                              dtype, fp8=None if fp8 is None else
+                              {k: fp8.get(k) for k in ("x", "kernel")})
+    dy = _f64(dy)
+    xs, g = _f64(x), _f64(gamma)
+    dbias = colsum(dy)
+    if fp8 is None:
+        gy = Stored(dy, dtype)
+        dln = Stored(gemm(gy.value, fwd["kernel"].value.T), dtype)
+        dk = Stored(gemm(fwd["ln"].value.T, gy.value), dtype)
+    else:
+        gy = Stored(dy, "e4m3", fp8.get("grad"))
+        kq = fwd["kernel"]
+        dln = Stored(gemm(gy.value, kq.value.T, None, gemm_alpha(gy.scale_inv, kq.scale_inv)),
+                     dtype)
+        dk = Stored(gemm(fwd["ln"].value.T, gy.value, None,
+                         gemm_alpha(fwd["ln"].scale_inv, gy.scale_inv)), dtype)
+    dx, dgamma, dbeta = norm_bwd(dln.value, xs, fwd["mu"], fwd["rsigma"], g, norm_type,
+                                 zero_centered_gamma)
+    return dict(fwd=fwd, dbias=dbias, dy=gy, dln=dln, dkernel=dk, dx=Stored(dx, dtype),
+                dgamma=dgamma, dbeta=dbeta)

@@ -313,3 +313,67 @@ def test_fp8_current_scaling_uses_own_amax():
     s, si = nx.compute_scale(nx.amax_of(nx.to_f32(v)))
     assert st.scale == s and st.scale_inv == si
     assert np.abs(st.dequantized()).max() == pytest.approx(float(st.amax), rel=1e-6)
+
+
+@pytest.mark.parametrize("nt,zc", [("layernorm", False), ("rmsnorm", True)])
+def test_dense_bwd_finite_differences(nt, zc):
+    """LayerNorm Dense backward: every gradient against central differences of the plain
+    forward norm(x) @ kernel + bias (dtype f32 keeps the storage rounding far below the FD
+    tolerance)."""
+    r = rng(31)
+    M, H, N = 5, 8, 6
+    x = r.normal(size=(M, H)) + 0.3
+    g = (0.1 if zc else 1.0) * r.normal(size=H) * 0.3 + (0.0 if zc else 1.0)
+    b = 0.1 * r.normal(size=H)
+    k = 0.3 * r.normal(size=(H, N))
+    bias = 0.1 * r.normal(size=N)
+    G = r.normal(size=(M, N))
+    res = ob.layernorm_dense_bwd(G, x, g, b, k, bias, nt, zc, 1e-5, "f32")
+
+    def fwd(x, g, b, k, bias):
+        y, _, _ = ob.norm_fwd(x, g, b, nt, zc, 1e-5)
+        return y @ k + bias
+
+    params = dict(x=x, g=g, b=b, k=k, bias=bias)
+    grads = dict(x=res["dx"].value, g=res["dgamma"], b=res["dbeta"], k=res["dkernel"].value,
+                 bias=res["dbias"])
+    step = 1e-6
+    for name, p in params.items():
+        if nt == "rmsnorm" and name == "b":
+            assert grads["b"] is None
+            continue
+        fd = np.zeros_like(p)
+        for idx in np.ndindex(p.shape):
+            pp, pm = dict(params), dict(params)
+            pp[name] = p.copy()
+            pm[name] = p.copy()
+            pp[name][idx] += step
+            pm[name][idx] -= step
+            fd[idx] = ((fwd(**pp) - fwd(**pm)) * G).sum() / (2 * step)
+        np.testing.assert_allclose(grads[name], fd, rtol=2e-5, atol=2e-6, err_msg=name)
+
+
+def test_fp8_dense_bwd_matches_torch_float8_composition():
+    """The FP8 LayerNorm Dense backward GEMMs rebuilt with torch's float8 conversion and fp64
+    matmul, with fixed scales: dln = q(dy) q(kernel)^T and dkernel = q(ln)^T q(dy), each scaled
+    by the product of the two dequantization factors and rounded to bf16."""
+    r = rng(32)
+    M, H, N = 16, 32, 48
+    x = r.normal(size=(M, H)).astype(np.float32).astype(np.float64)
+    g = 1 + 0.1 * r.normal(size=H)
+    b = 0.1 * r.normal(size=H)
+    k = 0.02 * r.normal(size=(H, N))
+    dy = nx.bf16_round(r.normal(size=(M, N)))
+    s = dict(x=np.float32(64.0), kernel=np.float32(4096.0), grad=np.float32(32.0))
+    res = ob.layernorm_dense_bwd(dy, x, g, b, k, None, "layernorm", False, 1e-6, "bf16", fp8=s)
+    y, _, _ = ob.norm_fwd(x, g, b, "layernorm", False, 1e-6)
+    qx = _torch_fake_quant(nx.to_f32(y), s["x"])
+    qk = _torch_fake_quant(k, s["kernel"])
+    qdy = _torch_fake_quant(dy, s["grad"])
+    bf = lambda v: torch.tensor(v, dtype=torch.float32).to(torch.bfloat16).double().numpy()
+    a1 = float(np.float32(1 / s["grad"]) * np.float32(1 / s["kernel"]))
+    a2 = float(np.float32(1 / s["x"]) * np.float32(1 / s["grad"]))
+    np.testing.assert_array_equal(res["dy"].value, qdy)
+    np.testing.assert_array_equal(res["dln"].value, bf(qdy @ qk.T * a1))
+    np.testing.assert_array_equal(res["dkernel"].value, bf(qx.T @ qdy * a2))
+    np.testing.assert_allclose(res["dbias"], dy.sum(axis=0), rtol=1e-12)
