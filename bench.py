@@ -75,9 +75,9 @@ TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "gemm_pair_traffic_llama_full.m
 
 
 def measured_traffic():
-    """DRAM bytes per GEMM1 launch from the committed ncu capture, or None when any source the
-    GEMM kernel is compiled from changed since the counters were taken (the capture records
-    the sha256 of those files, concatenated in the listed order)."""
+    """DRAM bytes per GEMM1 launch from the committed ncu capture, or None when a file holding
+    the GEMM's device code or launch parameters (GEMM_SOURCES) changed since the counters were
+    taken (the capture records the sha256 of those files, concatenated in the listed order)."""
     import hashlib
     try:
         fields = {}
@@ -86,6 +86,8 @@ def measured_traffic():
                 if ":" in line and not line.startswith(("|", "#", "`")):
                     k, v = line.split(":", 1)
                     fields[k.strip()] = v.strip()
+        if fields["sources"].split() != GEMM_SOURCES:
+            return None
         h = hashlib.sha256()
         for rel in fields["sources"].split():
             with open(os.path.join(ROOT, rel), "rb") as f:
@@ -98,8 +100,7 @@ def measured_traffic():
 
 
 GEMM_SOURCES = ["fp8_transformer_gb300/csrc/gemm.cu", "fp8_transformer_gb300/csrc/common.cuh",
-                "fp8_transformer_gb300/csrc/sync.cuh", "fp8_transformer_gb300/csrc/kernels.h",
-                "include/te_gb300.h"]
+                "fp8_transformer_gb300/csrc/sync.cuh", "fp8_transformer_gb300/csrc/kernels.h"]
 
 
 def load_peaks():
@@ -340,7 +341,7 @@ def run_ours(args, rank, world, local_rank):
     import torch.distributed as dist
 
     import fp8_transformer_gb300 as te
-    from workloads import make_inputs
+    from workloads import make_inputs, random_tensor
 
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
@@ -475,7 +476,8 @@ def run_ours(args, rank, world, local_rank):
     del dyd, hd, dxd, wsd
     barrier()
 
-    # ---- the other workloads' hot paths: LN -> Dense (QKV) forward and the GPT MLP backward
+    # ---- the other workloads' hot paths: LN -> Dense (QKV) forward and backward, and the GPT
+    # MLP backward
     extra = {}
     dense = make_inputs("qkv_ln_dense", device=dev, seed=rank)
     Mq, Hq, Nq = dense["M"], dense["H"], dense["N"]
@@ -501,7 +503,39 @@ def run_ours(args, rank, world, local_rank):
         ms = max_over_ranks(statistics.mean(time_steps(fn, max(3, args.steps // 2), flush)))
         extra[f"ln_dense_{tag}"] = {"TFLOP/s": dflops / (ms / 1e3) / 1e12, "ms": ms,
                                     "workload": "qkv_ln_dense M=16384 H=8192 N=24576"}
-    del dense, qout, kq
+    # LN -> Dense backward: dbias (+ E4M3 cast of dy), dln = dy kernel^T, dkernel = ln^T dy,
+    # norm backward; the forward's saved normalized output, mu and rsigma feed it
+    dd = {k: torch.empty(*sh, dtype=dt, device=dev) for k, sh, dt in (
+        ("ln8", (Mq, Hq), torch.uint8), ("lnb", (Mq, Hq), torch.bfloat16),
+        ("mu", (Mq,), torch.float32), ("rs", (Mq,), torch.float32),
+        ("dx", (Mq, Hq), torch.bfloat16), ("dg", (Hq,), torch.float32),
+        ("db", (Hq,), torch.float32), ("dk", (Hq, Nq), torch.bfloat16),
+        ("dbias", (Nq,), torch.float32))}
+    dyq = random_tensor((Mq, Nq), device=dev, seed=100 + rank)
+    te.te_layernorm_dense_fwd(dense["x"], kq, dense["gamma"], dense["beta"], dense["bias"], qout,
+                              quantizer_set=qs_d, saved_ln_out=dd["ln8"], mu=dd["mu"],
+                              rsigma=dd["rs"], **dkw)
+    te.te_layernorm_dense_fwd(dense["x"], dense["kernel"], dense["gamma"], dense["beta"],
+                              dense["bias"], qout, saved_ln_out=dd["lnb"], **dkw)
+    qg_d = te.Quantizer(1.0, "current", dev)
+    qs_db = te.QuantizerSet(x=qx_d, kernel1=qk_q, grad=qg_d)
+
+    def dense_bwd(fp8):
+        te.te_layernorm_dense_bwd(dyq, dense["x"], dense["gamma"], kq if fp8 else dense["kernel"],
+                                  dd["ln8"] if fp8 else dd["lnb"], dd["mu"], dd["rs"], dd["dx"],
+                                  dd["dg"], dd["dk"], dbeta=dd["db"], dbias=dd["dbias"],
+                                  quantizer_set=qs_db if fp8 else None)
+
+    dense_bwd(True)  # calibrates the grad scale, then delayed scaling like the forward
+    torch.cuda.synchronize()
+    qg_d.mode = te.binding.TE_SCALING_DELAYED
+    for tag, fp8 in (("bf16", False), ("fp8", True)):
+        dense_bwd(fp8)
+        ms = max_over_ranks(statistics.mean(time_steps(lambda: dense_bwd(fp8),
+                                                       max(3, args.steps // 2), flush)))
+        extra[f"ln_dense_bwd_{tag}"] = {"TFLOP/s": 2 * dflops / (ms / 1e3) / 1e12, "ms": ms,
+                                        "workload": "qkv_ln_dense backward M=16384 H=8192 N=24576"}
+    del dense, qout, kq, dd, dyq
     bw = make_inputs("gpt_ln_mlp_bwd", device=dev, seed=rank)
     Mb, Hb, Fb = bw["M"], bw["H"], bw["F"]
     bt = {k: torch.empty(*sh, dtype=dt, device=dev) for k, sh, dt in (

@@ -22,7 +22,8 @@ TE_LAYERNORM, TE_RMSNORM = 0, 1
 TE_IDENTITY, TE_RELU, TE_GELU, TE_SILU, TE_SWIGLU = range(5)
 TE_SCALING_DELAYED, TE_SCALING_CURRENT = 0, 1
 (TE_OP_NORM_FWD, TE_OP_ACT_LU, TE_OP_DACT_DBIAS, TE_OP_LAYERNORM_DENSE_FWD,
- TE_OP_LAYERNORM_MLP_FWD, TE_OP_NORM_BWD, TE_OP_LAYERNORM_MLP_BWD) = range(7)
+ TE_OP_LAYERNORM_MLP_FWD, TE_OP_NORM_BWD, TE_OP_LAYERNORM_MLP_BWD,
+ TE_OP_LAYERNORM_DENSE_BWD) = range(8)
 
 NORM_TYPES = {"layernorm": TE_LAYERNORM, "rmsnorm": TE_RMSNORM}
 ACT_TYPES = {"identity": TE_IDENTITY, "relu": TE_RELU, "gelu": TE_GELU, "silu": TE_SILU,
@@ -38,6 +39,7 @@ EXPORTED = ["te_status_string", "te_version", "te_get_device_status", "te_worksp
             "te_norm_fwd", "te_act_lu", "te_dact_dbias_quantize", "te_quantize", "te_gemm",
             "te_layernorm_dense_fwd", "te_layernorm_mlp_fwd", "te_norm_bwd",
             "te_profile_begin", "te_profile_end", "te_layernorm_mlp_bwd",
+            "te_layernorm_dense_bwd",
             "te_dact_dbias_quantize_noalloc",
             "te_dact_dbias_noalloc_capacity"]
 KERNEL_KINDS = ["norm_fwd", "quantize", "act_lu", "dact_dbias", "gemm", "gemm_act", "norm_bwd",
@@ -97,6 +99,10 @@ _SIGS = {
                                             _vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, _QSP,
                                             _i64, _i64, _i64, ctypes.c_int, _vp, _vp, _vp, _vp,
                                             _vp, _vp, _vp, _vp, _sz, _vp]),
+    "te_layernorm_dense_bwd": (ctypes.c_int, [_vp, _vp, _vp, _vp, ctypes.c_int, _vp, _vp, _vp,
+                                              ctypes.c_int, ctypes.c_int, _QSP, _i64, _i64, _i64,
+                                              ctypes.c_int, _vp, _vp, _vp, _vp, _vp, _vp, _sz,
+                                              _vp]),
     "te_dact_dbias_quantize_noalloc": (ctypes.c_int, [_vp, _vp, ctypes.c_int, _i64, _i64,
                                                       ctypes.c_int, _QP, _vp, ctypes.c_int, _vp,
                                                       _vp]),
@@ -341,6 +347,28 @@ def te_layernorm_mlp_bwd(dy, x, gamma, kernel1, kernel2, saved_h, saved_ln_out, 
                                     _ptr(dkernel2), _ptr(dbias1), _ptr(dbias2), _ptr(workspace),
                                     workspace.numel(), _stream(stream))
     _check("te_layernorm_mlp_bwd", st)
+    return dx
+
+
+def te_layernorm_dense_bwd(dy, x, gamma, kernel, saved_ln_out, mu, rsigma, dx, dgamma, dkernel,
+                           dbeta=None, dbias=None, norm_type="layernorm", zero_centered_gamma=False,
+                           quantizer_set=None, workspace=None, stream=None):
+    M, H = x.shape
+    N = kernel.shape[1]
+    dt = _dt(x)
+    kd = _dt(kernel)
+    if workspace is None:
+        workspace = _ws(workspace_size(TE_OP_LAYERNORM_DENSE_BWD, M, H, N, dt,
+                                       quantizer_set is not None, kd), x.device)
+    qs = quantizer_set.c() if quantizer_set is not None else None
+    st = lib().te_layernorm_dense_bwd(_ptr(dy), _ptr(x), _ptr(gamma), _ptr(kernel), kd,
+                                      _ptr(saved_ln_out), _ptr(mu), _ptr(rsigma),
+                                      _norm_id(norm_type), int(bool(zero_centered_gamma)),
+                                      ctypes.byref(qs) if qs is not None else None, M, H, N, dt,
+                                      _ptr(dx), _ptr(dgamma), _ptr(dbeta), _ptr(dkernel),
+                                      _ptr(dbias), _ptr(workspace), workspace.numel(),
+                                      _stream(stream))
+    _check("te_layernorm_dense_bwd", st)
     return dx
 
 

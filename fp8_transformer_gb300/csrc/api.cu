@@ -160,6 +160,30 @@ BwdLayout bwd_layout(void* ws, int64_t M, int64_t H, int64_t F, int dtype, bool 
   return L;
 }
 
+// Workspace of te_layernorm_dense_bwd (reductions run one after another, so they share one
+// partials buffer).
+struct DenseBwdLayout {
+  void* partials = nullptr;
+  void* dyq = nullptr;  // E4M3 dy (FP8 mode)
+  void* kq = nullptr;   // E4M3 kernel when quantized here
+  void* dln = nullptr;  // [M, H], dtype
+  size_t bytes = 0;
+};
+
+DenseBwdLayout dense_bwd_layout(void* ws, int64_t M, int64_t H, int64_t N, int dtype, bool quant,
+                                int kernel_dtype) {
+  Carver c(ws);
+  DenseBwdLayout L;
+  size_t part = dact_dbias_workspace(M, N);
+  if (norm_bwd_workspace(M, H) > part) part = norm_bwd_workspace(M, H);
+  L.partials = c.take(part);
+  if (quant) L.dyq = c.take(size_t(M) * N);
+  if (quant && kernel_dtype != TE_E4M3) L.kq = c.take(size_t(H) * N);
+  L.dln = c.take(size_t(M) * H * esize(dtype));
+  L.bytes = c.used;
+  return L;
+}
+
 te_status norm_into(const void* x, int dtype, int64_t M, int64_t H, const void* gamma,
                     const void* beta, int norm_type, int zcg, float eps, const te_quantizer* q,
                     void* out, int out_dtype, float* mu, float* rsigma, cudaStream_t s) {
@@ -234,6 +258,8 @@ size_t te_workspace_size(te_op op, int64_t M, int64_t H, int64_t F_or_N, te_dtyp
       return mlp_layout(nullptr, M, H, F_or_N, dtype, quantized != 0, kernel_dtype, act, false).bytes;
     case TE_OP_LAYERNORM_MLP_BWD:
       return bwd_layout(nullptr, M, H, F_or_N, dtype, quantized != 0, kernel_dtype, act).bytes;
+    case TE_OP_LAYERNORM_DENSE_BWD:
+      return dense_bwd_layout(nullptr, M, H, F_or_N, dtype, quantized != 0, kernel_dtype).bytes;
     default: return 0;
   }
 }
@@ -735,6 +761,143 @@ te_status te_layernorm_mlp_bwd(const void* dy, const void* x, const void* gamma,
     if (st != TE_OK) return st;
   }
   // norm backward
+  NormBwdArgs nb;
+  nb.dz = L.dln;
+  nb.x = x;
+  nb.mu = mu;
+  nb.rsigma = rsigma;
+  nb.gamma = gamma;
+  nb.dtype = dtype;
+  nb.M = M;
+  nb.H = H;
+  nb.norm_type = norm_type;
+  nb.zero_centered_gamma = zero_centered_gamma;
+  nb.dx = dx;
+  nb.dgamma = dgamma;
+  nb.dbeta = norm_type == TE_LAYERNORM ? dbeta : nullptr;
+  nb.partials = partials;
+  return launch_norm_bwd(nb, s);
+}
+
+te_status te_layernorm_dense_bwd(const void* dy, const void* x, const void* gamma,
+                                 const void* kernel, te_dtype kernel_dtype,
+                                 const void* saved_ln_out, const float* mu, const float* rsigma,
+                                 te_norm_type norm_type, int zero_centered_gamma,
+                                 const te_quantizer_set* qset, int64_t M, int64_t H, int64_t N,
+                                 te_dtype dtype, void* dx, float* dgamma, float* dbeta,
+                                 void* dkernel, float* dbias, void* workspace, size_t ws_bytes,
+                                 void* stream) {
+  if (M < 0 || H <= 0 || N <= 0 || dtype != TE_BF16 ||
+      (norm_type != TE_LAYERNORM && norm_type != TE_RMSNORM))
+    return dtype == TE_F32 ? TE_ERR_UNSUPPORTED : TE_ERR_INVALID_ARG;
+  const bool quant = qset != nullptr;
+  if (quant) {
+    if (!enabled(&qset->grad) || !quantizer_ok(&qset->grad) || !qset->x.scale_inv ||
+        !quantizer_ok(&qset->kernel1))
+      return TE_ERR_INVALID_ARG;
+    if (kernel_dtype == TE_E4M3 ? !qset->kernel1.scale_inv
+                                : (kernel_dtype != dtype || !enabled(&qset->kernel1)))
+      return TE_ERR_INVALID_ARG;
+  } else if (kernel_dtype != dtype) {
+    return TE_ERR_INVALID_ARG;
+  }
+  if (!gamma || !dgamma || (M > 0 && (!dy || !x || !kernel || !saved_ln_out || !rsigma || !dx ||
+                                      !dkernel)) ||
+      (M > 0 && norm_type == TE_LAYERNORM && !mu))
+    return TE_ERR_INVALID_ARG;
+  if (H % 16 || N % 16 || H * int64_t(esize(dtype)) > 16384) return TE_ERR_UNSUPPORTED;
+  if (!aligned16(dy) || !aligned16(x) || !aligned16(gamma) || !aligned16(kernel) ||
+      !aligned16(saved_ln_out) || !aligned16(dx) || !aligned16(dkernel) || !aligned16(workspace) ||
+      !aligned4(mu) || !aligned4(rsigma) || !aligned4(dgamma) || !aligned4(dbeta) ||
+      !aligned4(dbias))
+    return TE_ERR_UNSUPPORTED;
+  cudaStream_t s = as_stream(stream);
+  if (M == 0) {
+    // no tokens: every gradient is zero
+    const std::pair<void*, size_t> z[] = {{dgamma, size_t(H) * 4}, {dbeta, size_t(H) * 4},
+                                          {dbias, size_t(N) * 4},
+                                          {dkernel, size_t(H) * N * esize(dtype)}};
+    for (const auto& e : z)
+      if (e.first && cudaMemsetAsync(e.first, 0, e.second, s) != cudaSuccess) return TE_ERR_CUDA;
+    return TE_OK;
+  }
+  DenseBwdLayout L = dense_bwd_layout(workspace, M, H, N, dtype, quant, kernel_dtype);
+  if (!workspace || ws_bytes < L.bytes) return TE_ERR_WORKSPACE;
+  float* partials = static_cast<float*>(L.partials);
+  te_status st;
+  // dbias = column sums of dy; in FP8 mode the same pass casts dy with the grad quantizer
+  if (quant) {
+    st = run_cast(&qset->grad, TE_E4M3, 0, s, [&](const CastSpec& c) {
+      DactArgs d;
+      d.dy = dy;
+      d.dtype = dtype;
+      d.M = M;
+      d.N_in = N;
+      d.act = TE_IDENTITY;
+      d.dx = L.dyq;
+      const bool two_pass = qset->grad.mode == TE_SCALING_CURRENT;
+      d.dbias = (two_pass ? c.store == 0 : true) ? dbias : nullptr;
+      d.partials = partials;
+      d.cast = c;
+      return launch_dact_dbias(d, s);
+    });
+    if (st != TE_OK) return st;
+  } else if (dbias) {
+    DactArgs d;
+    d.dy = dy;
+    d.dtype = dtype;
+    d.M = M;
+    d.N_in = N;
+    d.act = TE_IDENTITY;
+    d.dx = nullptr;
+    d.dbias = dbias;
+    d.partials = partials;
+    st = launch_dact_dbias(d, s);
+    if (st != TE_OK) return st;
+  }
+  const void* gy = quant ? L.dyq : dy;
+  const void* w = kernel;
+  if (quant && kernel_dtype != TE_E4M3) {
+    st = quantize_into(kernel, dtype, H * N, &qset->kernel1, L.kq, s);
+    if (st != TE_OK) return st;
+    w = L.kq;
+  }
+  // dln = dy kernel^T   ([M, H], contraction over N)
+  {
+    GemmArgs g;
+    g.A = gy;
+    g.B = w;
+    g.ab_dtype = quant ? TE_E4M3 : dtype;
+    g.a_kmajor = 1;
+    g.b_kmajor = 1;
+    g.M = M;
+    g.N = H;
+    g.K = N;
+    g.a_scale_inv = quant ? qset->grad.scale_inv : nullptr;
+    g.b_scale_inv = quant ? qset->kernel1.scale_inv : nullptr;
+    g.D = L.dln;
+    g.cast.out_dtype = dtype;
+    st = launch_gemm(g, s);
+    if (st != TE_OK) return st;
+  }
+  // dkernel = ln^T dy   ([H, N], contraction over tokens)
+  {
+    GemmArgs g;
+    g.A = saved_ln_out;
+    g.B = gy;
+    g.ab_dtype = quant ? TE_E4M3 : dtype;
+    g.a_kmajor = 0;
+    g.b_kmajor = 0;
+    g.M = H;
+    g.N = N;
+    g.K = M;
+    g.a_scale_inv = quant ? qset->x.scale_inv : nullptr;
+    g.b_scale_inv = quant ? qset->grad.scale_inv : nullptr;
+    g.D = dkernel;
+    g.cast.out_dtype = dtype;
+    st = launch_gemm(g, s);
+    if (st != TE_OK) return st;
+  }
   NormBwdArgs nb;
   nb.dz = L.dln;
   nb.x = x;

@@ -91,7 +91,8 @@ typedef enum {
   TE_OP_LAYERNORM_DENSE_FWD = 3,
   TE_OP_LAYERNORM_MLP_FWD = 4,
   TE_OP_NORM_BWD = 5,
-  TE_OP_LAYERNORM_MLP_BWD = 6
+  TE_OP_LAYERNORM_MLP_BWD = 6,
+  TE_OP_LAYERNORM_DENSE_BWD = 7
 } te_op;
 
 /* Human-readable name of a status code (static storage, never NULL). */
@@ -265,6 +266,37 @@ te_status te_layernorm_mlp_bwd(const void* dy, const void* x, const void* gamma,
                                te_dtype dtype, void* dx, float* dgamma, float* dbeta,
                                void* dkernel1, void* dkernel2, float* dbias1, float* dbias2,
                                void* workspace, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------------------
+ * te_layernorm_dense_bwd -- backward of te_layernorm_dense_fwd (LayerNorm Dense page,
+ * Description: the gradients of x, the kernel, gamma, beta and the bias, with FP8 intermediate
+ * gradients).
+ * Sequence (all on `stream`): dbias = fp32 column sums of dy, taken over the unquantized dy in
+ * the same pass that casts dy to E4M3 with qset->grad (FP8 mode); dln = dy kernel^T;
+ * dkernel = ln^T dy; then the norm backward gives dx, dgamma, dbeta.
+ *   dy [M, N], x [M, H], gamma [H] in dtype; kernel [H, N] in kernel_dtype; mu, rsigma [M]
+ *   from the forward (mu unused for rmsnorm).
+ *   saved_ln_out [M, H]: the forward's normalized output (E4M3 with qset, else dtype).
+ *   qset NULL: both GEMMs in dtype (kernel_dtype must equal dtype).  Non-NULL (FP8): qset->grad
+ *   must be enabled and quantizes dy; qset->x.scale_inv dequantizes saved_ln_out; the kernel is
+ *   E4M3 (kernel_dtype TE_E4M3, factor in qset->kernel1.scale_inv) or is quantized here with
+ *   qset->kernel1.  Both GEMMs then run as E4M3 x E4M3.
+ *   Outputs (caller-owned): dx [M, H] dtype; dgamma [H] fp32; dbeta [H] fp32 or NULL
+ *   (layernorm only); dkernel [H, N] dtype; dbias [N] fp32 or NULL.
+ *   workspace: te_workspace_size(TE_OP_LAYERNORM_DENSE_BWD, M, H, N, dtype, quantized,
+ *   kernel_dtype, 0) bytes, 16-byte aligned.  dtype TE_BF16; H and N multiples of 16, H at most
+ *   8192.  A NULL required pointer, a bad enum or a quantizer set without what FP8 mode needs
+ *   gives TE_ERR_INVALID_ARG; sizes or alignment outside these limits TE_ERR_UNSUPPORTED; a
+ *   missing or short workspace TE_ERR_WORKSPACE.  M = 0 zeroes every gradient.
+ */
+te_status te_layernorm_dense_bwd(const void* dy, const void* x, const void* gamma,
+                                 const void* kernel, te_dtype kernel_dtype,
+                                 const void* saved_ln_out, const float* mu, const float* rsigma,
+                                 te_norm_type norm_type, int zero_centered_gamma,
+                                 const te_quantizer_set* qset, int64_t M, int64_t H, int64_t N,
+                                 te_dtype dtype, void* dx, float* dgamma, float* dbeta,
+                                 void* dkernel, float* dbias, void* workspace, size_t ws_bytes,
+                                 void* stream);
 
 /* ---------------------------------------------------------------------------------------
  * te_norm_bwd -- gradients of te_norm_fwd (LayerNorm MLP page, Description: the backward pass
