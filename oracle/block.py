@@ -147,43 +147,43 @@ def d_silu(z):
     return s * (1.0 + z * (1.0 - s))
 
 
-GATED = {"swiglu": True, "relu": False, "gelu": False, "silu": False}
+# Gated pairs (Activation page, Usage Examples / activation_type tuples): (base, "linear")
+GATE_BASE = {"swiglu": "silu", "geglu": "gelu", "reglu": "relu"}
+GATED = {"swiglu": True, "geglu": True, "reglu": True, "relu": False, "gelu": False,
+         "silu": False}
+_BASE_FWD = {"relu": relu, "gelu": gelu, "silu": silu}
+_BASE_BWD = {"relu": d_relu, "gelu": d_gelu, "silu": d_silu}
 
 
 def act_fwd(h, act: str):
-    """Activation of h[M, N_in].  Gated "swiglu" = ("silu", "linear"): N_in = 2F, the first F
-    columns are the gate, the last F the linear factor; output silu(gate) * linear [M, F]."""
+    """Activation of h[M, N_in].  A gated type (base, "linear") -- "swiglu" = ("silu",
+    "linear"), "geglu" = ("gelu", "linear"), "reglu" = ("relu", "linear") -- has N_in = 2F: the
+    first F columns are the gate, the last F the linear factor; output base(gate) * linear
+    [M, F]."""
     h = np.asarray(h, dtype=np.float64)
-    if act == "relu":
-        return relu(h)
-    if act == "gelu":
-        return gelu(h)
-    if act == "silu":
-        return silu(h)
-    if act == "swiglu":
+    if act in _BASE_FWD:
+        return _BASE_FWD[act](h)
+    if act in GATE_BASE:
         F = h.shape[1] // 2
-        return silu(h[:, :F]) * h[:, F:]
+        return _BASE_FWD[GATE_BASE[act]](h[:, :F]) * h[:, F:]
     raise ValueError(act)
 
 
 def act_bwd(da, h, act: str):
     """Gradient w.r.t. the activation input h, given da = dL/d(act output).
 
-    Gated: d_gate = da * linear * silu'(gate), d_linear = da * silu(gate), concatenated
+    Gated: d_gate = da * linear * base'(gate), d_linear = da * base(gate), concatenated
     [d_gate | d_linear] like h.
     """
     da = np.asarray(da, dtype=np.float64)
     h = np.asarray(h, dtype=np.float64)
-    if act == "relu":
-        return da * d_relu(h)
-    if act == "gelu":
-        return da * d_gelu(h)
-    if act == "silu":
-        return da * d_silu(h)
-    if act == "swiglu":
+    if act in _BASE_BWD:
+        return da * _BASE_BWD[act](h)
+    if act in GATE_BASE:
         F = h.shape[1] // 2
         g, lin = h[:, :F], h[:, F:]
-        return np.concatenate([da * lin * d_silu(g), da * silu(g)], axis=1)
+        base = GATE_BASE[act]
+        return np.concatenate([da * lin * _BASE_BWD[base](g), da * _BASE_FWD[base](g)], axis=1)
     raise ValueError(act)
 
 

@@ -162,14 +162,20 @@ def test_activation_identities():
     lin = rng(10).normal(size=(5, 8))
     h = np.concatenate([gate, lin], axis=1)
     np.testing.assert_allclose(ob.act_fwd(h, "swiglu"), gate * sp.expit(gate) * lin, rtol=1e-13)
+    # ("gelu", "linear") and ("relu", "linear"): the gate half goes through the base function
+    h1 = np.concatenate([gate, np.ones_like(gate)], axis=1)
+    np.testing.assert_allclose(ob.act_fwd(h1, "geglu"), ob.gelu(gate), rtol=1e-15)
+    np.testing.assert_array_equal(ob.act_fwd(h, "reglu"), np.maximum(gate, 0.0) * lin)
+    swapped = np.concatenate([lin, gate], axis=1)
+    assert not np.allclose(ob.act_fwd(swapped, "geglu"), ob.act_fwd(h, "geglu"))
 
 
-@pytest.mark.parametrize("act", ["gelu", "silu", "relu", "swiglu"])
+@pytest.mark.parametrize("act", ["gelu", "silu", "relu", "swiglu", "geglu", "reglu"])
 def test_act_bwd_finite_differences(act):
     r = rng(11)
     h = r.normal(size=(4, 16)) * 2
     h[np.abs(h) < 1e-3] = 0.5  # keep away from relu's kink
-    n_out = 8 if act == "swiglu" else 16
+    n_out = 8 if ob.GATED[act] else 16
     da = r.normal(size=(4, n_out))
     got = ob.act_bwd(da, h, act)
     step = 1e-6
@@ -233,13 +239,14 @@ def _plain_forward(x, g, b, w1, w2, b1, b2, act, nt="layernorm"):
 
 
 @pytest.mark.parametrize("act,nt", [("gelu", "layernorm"), ("swiglu", "rmsnorm"),
-                                    ("relu", "layernorm")])
+                                    ("relu", "layernorm"), ("geglu", "layernorm"),
+                                    ("reglu", "rmsnorm")])
 def test_block_bwd_finite_differences(act, nt):
     """Every gradient of the composed backward against central differences of the forward.
 
     dtype f32 keeps the oracle's storage rounding at fp32, far below the FD tolerance."""
-    x, g, b, w1, w2, b1, b2 = _tiny_block(gated=(act == "swiglu"))
-    if act == "relu":
+    x, g, b, w1, w2, b1, b2 = _tiny_block(gated=ob.GATED[act])
+    if act in ("relu", "reglu"):
         w1 = w1 + 0.0
     G = rng(15).normal(size=(x.shape[0], w2.shape[1]))
     res = ob.layernorm_mlp_bwd(G, x, g, b, w1, w2, b1, b2, nt, False, 1e-5, act, "f32")
