@@ -19,7 +19,7 @@ from . import build as _build
  TE_ERR_TOO_LARGE) = range(7)
 TE_F32, TE_BF16, TE_E4M3 = 0, 1, 2
 TE_LAYERNORM, TE_RMSNORM = 0, 1
-TE_IDENTITY, TE_RELU, TE_GELU, TE_SILU, TE_SWIGLU = range(5)
+TE_IDENTITY, TE_RELU, TE_GELU, TE_SILU, TE_SWIGLU, TE_GEGLU, TE_REGLU = range(7)
 TE_SCALING_DELAYED, TE_SCALING_CURRENT = 0, 1
 (TE_OP_NORM_FWD, TE_OP_ACT_LU, TE_OP_DACT_DBIAS, TE_OP_LAYERNORM_DENSE_FWD,
  TE_OP_LAYERNORM_MLP_FWD, TE_OP_NORM_BWD, TE_OP_LAYERNORM_MLP_BWD,
@@ -27,10 +27,11 @@ TE_SCALING_DELAYED, TE_SCALING_CURRENT = 0, 1
 
 NORM_TYPES = {"layernorm": TE_LAYERNORM, "rmsnorm": TE_RMSNORM}
 ACT_TYPES = {"identity": TE_IDENTITY, "relu": TE_RELU, "gelu": TE_GELU, "silu": TE_SILU,
-             "swiglu": TE_SWIGLU}
+             "swiglu": TE_SWIGLU, "geglu": TE_GEGLU, "reglu": TE_REGLU}
 # the pages' activation_type tuples
 ACT_TUPLES = {("relu",): "relu", ("gelu",): "gelu", ("silu",): "silu",
-              ("silu", "linear"): "swiglu"}
+              ("silu", "linear"): "swiglu", ("gelu", "linear"): "geglu",
+              ("relu", "linear"): "reglu"}
 
 _DTYPE = {torch.float32: TE_F32, torch.bfloat16: TE_BF16, torch.uint8: TE_E4M3,
           torch.float8_e4m3fn: TE_E4M3}

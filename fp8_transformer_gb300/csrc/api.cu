@@ -18,7 +18,7 @@ bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0
 
 size_t esize(int dt) { return dt == TE_F32 ? 4 : dt == TE_BF16 ? 2 : 1; }
 bool is_act_dtype(int dt) { return dt == TE_F32 || dt == TE_BF16; }
-bool valid_act(int a) { return a >= TE_IDENTITY && a <= TE_SWIGLU; }
+bool valid_act(int a) { return a >= TE_IDENTITY && a <= TE_REGLU; }
 bool enabled(const te_quantizer* q) { return q != nullptr && q->scale != nullptr; }
 
 bool quantizer_ok(const te_quantizer* q) {
@@ -113,7 +113,7 @@ FwdLayout mlp_layout(void* ws, int64_t M, int64_t H, int64_t F, int dtype, bool 
                      int kernel_dtype, int act, bool have_saved_ln) {
   Carver c(ws);
   FwdLayout L;
-  const int64_t F1 = act == TE_SWIGLU ? 2 * F : F;
+  const int64_t F1 = is_gated(act) ? 2 * F : F;
   if (!have_saved_ln) L.ln = c.take(size_t(M) * H * (quant ? 1 : esize(dtype)));
   L.a2 = c.take(size_t(M) * F * (quant ? 1 : esize(dtype)));
   if (quant) {
@@ -146,7 +146,7 @@ BwdLayout bwd_layout(void* ws, int64_t M, int64_t H, int64_t F, int dtype, bool 
                      int kernel_dtype, int act) {
   Carver c(ws);
   BwdLayout L;
-  const int64_t F1 = act == TE_SWIGLU ? 2 * F : F;
+  const int64_t F1 = is_gated(act) ? 2 * F : F;
   size_t part = dact_dbias_workspace(M, H);
   if (dact_dbias_workspace(M, F1) > part) part = dact_dbias_workspace(M, F1);
   if (norm_bwd_workspace(M, H) > part) part = norm_bwd_workspace(M, H);
@@ -290,8 +290,8 @@ te_status te_act_lu(const void* x, te_dtype x_dtype, int64_t M, int64_t N_in, te
   if (M > 0 && (!x || !out)) return TE_ERR_INVALID_ARG;
   if (out_dtype == TE_E4M3 && !enabled(q)) return TE_ERR_INVALID_ARG;
   if (!quantizer_ok(q)) return TE_ERR_INVALID_ARG;
-  const int64_t n_out = act == TE_SWIGLU ? N_in / 2 : N_in;
-  if ((act == TE_SWIGLU && N_in % 2) || n_out % 8) return TE_ERR_UNSUPPORTED;
+  const int64_t n_out = is_gated(act) ? N_in / 2 : N_in;
+  if ((is_gated(act) && N_in % 2) || n_out % 8) return TE_ERR_UNSUPPORTED;
   if (!aligned16(x) || !aligned16(out)) return TE_ERR_UNSUPPORTED;
   if (M == 0) return TE_OK;
   const int fake = enabled(q) && out_dtype != TE_E4M3;
@@ -318,8 +318,8 @@ te_status te_dact_dbias_quantize(const void* dy, const void* x_preact, te_dtype 
   if (M > 0 && (!dy || (act != TE_IDENTITY && !x_preact) || !dx)) return TE_ERR_INVALID_ARG;
   if (dx_dtype == TE_E4M3 && !enabled(q)) return TE_ERR_INVALID_ARG;
   if (!quantizer_ok(q)) return TE_ERR_INVALID_ARG;
-  const int64_t n_out = act == TE_SWIGLU ? N_in / 2 : N_in;
-  if ((act == TE_SWIGLU && N_in % 2) || n_out % 8) return TE_ERR_UNSUPPORTED;
+  const int64_t n_out = is_gated(act) ? N_in / 2 : N_in;
+  if ((is_gated(act) && N_in % 2) || n_out % 8) return TE_ERR_UNSUPPORTED;
   if (!aligned16(dy) || !opt_aligned16(x_preact) || !aligned16(dx) || !aligned4(dbias))
     return TE_ERR_UNSUPPORTED;
   cudaStream_t s = as_stream(stream);
@@ -488,7 +488,7 @@ te_status te_layernorm_mlp_fwd(const void* x, const void* gamma, const void* bet
       !aligned4(mu) || !aligned4(rsigma))
     return TE_ERR_UNSUPPORTED;
   if (M == 0) return TE_OK;
-  const bool gated = act == TE_SWIGLU;
+  const bool gated = is_gated(act);
   const int64_t F1 = gated ? 2 * F : F;
   FwdLayout L = mlp_layout(workspace, M, H, F, dtype, quant, kernel_dtype, act,
                            saved_ln_out != nullptr);
@@ -625,7 +625,7 @@ te_status te_layernorm_mlp_bwd(const void* dy, const void* x, const void* gamma,
       !aligned4(dbias2))
     return TE_ERR_UNSUPPORTED;
   cudaStream_t s = as_stream(stream);
-  const bool gated = act == TE_SWIGLU;
+  const bool gated = is_gated(act);
   const int64_t F1 = gated ? 2 * F : F;
   if (M == 0) {
     // no tokens: every gradient is zero

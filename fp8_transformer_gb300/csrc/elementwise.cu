@@ -63,7 +63,8 @@ template <typename T, int ACT>
 __global__ void __launch_bounds__(kActWarps * 32, 3) act_lu_kernel(ActArgs a) {
   using PR = Pairs<T>;
   constexpr int E = Vec16<T>::N;
-  constexpr bool kGated = ACT == TE_SWIGLU;
+  constexpr bool kGated = is_gated(ACT);
+  constexpr int kBase = gate_act(ACT);  // the function of the gate half
   const CastState cs = cast_begin(a.cast);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t n_out = kGated ? a.N_in / 2 : a.N_in;
@@ -101,7 +102,7 @@ __global__ void __launch_bounds__(kActWarps * 32, 3) act_lu_kernel(ActArgs a) {
 #pragma unroll
           for (int p = 0; p < PR::P; ++p) {
             f32x2 yy;
-            if constexpr (kGated) yy = mul2(silu2(hp[p]), lp[p]);
+            if constexpr (kGated) yy = mul2(act2c<kBase>(hp[p]), lp[p]);
             else yy = act2c<ACT>(hp[p]);
             if (AMAX) am[p] = absmax2(am[p], yy);
             y[2 * p] = f2lo(yy);
@@ -130,7 +131,8 @@ __global__ void __launch_bounds__(kDactWarps * 32, 3) dact_dbias_kernel(DactArgs
   constexpr int E = Vec16<T>::N;
   constexpr int P = PR::P;
   constexpr int W = 32 * E;  // strip width in columns
-  constexpr bool kGated = ACT == TE_SWIGLU;
+  constexpr bool kGated = is_gated(ACT);
+  constexpr int kBase = gate_act(ACT);  // the function of the gate half
   constexpr bool kIdent = ACT == TE_IDENTITY;
   __shared__ float red[kDactWarps][2][W];
   const CastState cs = cast_begin(a.cast);
@@ -177,12 +179,19 @@ __global__ void __launch_bounds__(kDactWarps * 32, 3) dact_dbias_kernel(DactArgs
             float dg[E], dl[E];
 #pragma unroll
             for (int p = 0; p < P; ++p) {
-              f32x2 sg, eg;
-              sigmoid2(hp[p], sg, eg);
-              // d_gate = dy * lin * silu'(gate), d_lin = dy * silu(gate)
-              const f32x2 dsil = mul2(sg, fma2(hp[p], mul2(eg, sg), f2s(1.0f)));
-              const f32x2 g2 = mul2(mul2(dyp[p], lp[p]), dsil);
-              const f32x2 l2 = mul2(dyp[p], mul2(hp[p], sg));
+              // d_gate = dy * lin * base'(gate), d_lin = dy * base(gate)
+              f32x2 act_g, dact_g;
+              if constexpr (kBase == TE_SILU) {  // silu and silu' share one logistic
+                f32x2 sg, eg;
+                sigmoid2(hp[p], sg, eg);
+                dact_g = mul2(sg, fma2(hp[p], mul2(eg, sg), f2s(1.0f)));
+                act_g = mul2(hp[p], sg);
+              } else {
+                act_g = act2c<kBase>(hp[p]);
+                dact_g = dact2c<kBase>(hp[p]);
+              }
+              const f32x2 g2 = mul2(mul2(dyp[p], lp[p]), dact_g);
+              const f32x2 l2 = mul2(dyp[p], act_g);
               acc1[p] = add2(acc1[p], g2);
               acc2[p] = add2(acc2[p], l2);
               if (AMAX) am[p] = absmax2(absmax2(am[p], g2), l2);
@@ -270,6 +279,8 @@ te_status launch_act_t(const ActArgs& a, dim3 grid, cudaStream_t s) {
     case TE_GELU: act_lu_kernel<T, TE_GELU><<<grid, kActWarps * 32, 0, s>>>(a); break;
     case TE_SILU: act_lu_kernel<T, TE_SILU><<<grid, kActWarps * 32, 0, s>>>(a); break;
     case TE_SWIGLU: act_lu_kernel<T, TE_SWIGLU><<<grid, kActWarps * 32, 0, s>>>(a); break;
+    case TE_GEGLU: act_lu_kernel<T, TE_GEGLU><<<grid, kActWarps * 32, 0, s>>>(a); break;
+    case TE_REGLU: act_lu_kernel<T, TE_REGLU><<<grid, kActWarps * 32, 0, s>>>(a); break;
     default: act_lu_kernel<T, TE_IDENTITY><<<grid, kActWarps * 32, 0, s>>>(a); break;
   }
   return cudaGetLastError() == cudaSuccess ? TE_OK : TE_ERR_CUDA;
@@ -282,6 +293,8 @@ te_status launch_dact_t(const DactArgs& a, dim3 grid, cudaStream_t s) {
     case TE_GELU: dact_dbias_kernel<T, TE_GELU><<<grid, kDactWarps * 32, 0, s>>>(a); break;
     case TE_SILU: dact_dbias_kernel<T, TE_SILU><<<grid, kDactWarps * 32, 0, s>>>(a); break;
     case TE_SWIGLU: dact_dbias_kernel<T, TE_SWIGLU><<<grid, kDactWarps * 32, 0, s>>>(a); break;
+    case TE_GEGLU: dact_dbias_kernel<T, TE_GEGLU><<<grid, kDactWarps * 32, 0, s>>>(a); break;
+    case TE_REGLU: dact_dbias_kernel<T, TE_REGLU><<<grid, kDactWarps * 32, 0, s>>>(a); break;
     default: dact_dbias_kernel<T, TE_IDENTITY><<<grid, kDactWarps * 32, 0, s>>>(a); break;
   }
   return cudaGetLastError() == cudaSuccess ? TE_OK : TE_ERR_CUDA;
@@ -292,7 +305,7 @@ te_status launch_dact_t(const DactArgs& a, dim3 grid, cudaStream_t s) {
 te_status launch_act_lu(const ActArgs& a, cudaStream_t s) {
   ProfileScope prof(TE_KERNEL_ACT_LU, s);
   if (a.M == 0) return TE_OK;
-  const int64_t n_out = a.act == TE_SWIGLU ? a.N_in / 2 : a.N_in;
+  const int64_t n_out = is_gated(a.act) ? a.N_in / 2 : a.N_in;
   const int E = a.x_dtype == TE_BF16 ? 8 : 4;
   if (ceil_div(a.M, kActRows) > 65535) return TE_ERR_UNSUPPORTED;
   dim3 grid(unsigned(ceil_div(n_out, 32 * E)), unsigned(ceil_div(a.M, kActRows)));
@@ -308,7 +321,7 @@ size_t dact_dbias_workspace(int64_t M, int64_t N_in) {
 te_status launch_dact_dbias(const DactArgs& a, cudaStream_t s) {
   if (a.M == 0) return TE_OK;
   ProfileScope prof(TE_KERNEL_DACT_DBIAS, s);
-  const int64_t n_out = a.act == TE_SWIGLU ? a.N_in / 2 : a.N_in;
+  const int64_t n_out = is_gated(a.act) ? a.N_in / 2 : a.N_in;
   const int E = a.dtype == TE_BF16 ? 8 : 4;
   const int chunks = int(ceil_div(a.M, kDactRows));
   if (chunks > 65535) return TE_ERR_UNSUPPORTED;

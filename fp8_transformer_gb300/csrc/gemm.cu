@@ -5,16 +5,20 @@
 // (Description, forward steps (2) and (4)) and the one GEMM of the "LayerNorm Dense" page, with
 // the activation and FP8 cast of step (3) fused into the first GEMM's epilogue.
 //
-// Structure (one CTA per SM, persistent over output tiles of 128 x 256 accumulator columns):
+// Structure (persistent over output tiles; by default clusters of two CTAs on an SM pair
+// compute 256 x 256 tiles with tcgen05.mma.cta_group::2, one CTA per SM):
 //   warp 0     TMA producer: one elected thread fills a STAGES-deep ring of A/B tiles, each
-//              row of a tile 128 bytes of K in the 128-byte swizzled layout.
-//   warp 1     owns the TMEM allocation (512 columns = two 256-column fp32 accumulators) and
-//              issues tcgen05.mma from one thread; tcgen05.commit releases ring slots and
-//              hands a finished accumulator to the epilogue.
-//   warps 2-5  epilogue: tcgen05.ld 32 columns at a time, scale by the FP8 dequantization
-//              factor, add the bias, round the pre-activation, apply the activation (the gated
-//              pair's gate and linear halves sit in the two column halves of one accumulator
-//              tile), track amax, and store fp32 / bf16 / E4M3.
+//              row of a tile 128 bytes of K in the 128-byte swizzled layout (each CTA of a
+//              pair loads its own 128 rows of A and its half of the tile's B columns).
+//   warp 1     owns the TMEM allocation (512 columns = two 256-column fp32 accumulators) and,
+//              in the pair's even CTA, issues tcgen05.mma from one thread; tcgen05.commit
+//              releases ring slots (multicast to both CTAs) and hands a finished accumulator to
+//              the epilogue.
+//   warps 2-9  epilogue, two warps per TMEM lane quadrant: tcgen05.ld 32 columns at a time,
+//              scale by the FP8 dequantization factor, add the bias, round the pre-activation,
+//              apply the activation (a gated pair's gate and linear halves sit in the two
+//              column halves of one accumulator tile), track amax, and store fp32 / bf16 /
+//              E4M3.
 // The epilogue of tile i overlaps the MMAs of tile i + 1.
 //
 // Every mbarrier wait is bounded in time.  On expiry the waiting thread records
@@ -500,6 +504,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     const uint32_t tempty_leader1 = CG == 1 ? smem_u32(&tempty[1]) : map_to_rank(smem_u32(&tempty[1]), 0);
     const int64_t ldd = g.gated ? g.F : g.N;
     const bool round_h = g.h_dtype == TE_BF16;
+    const int gact = gate_act(g.act);  // a gated pair's function of its gate half
     float amax = 0.0f;
     int local = 0;
     for (int t = cluster_id; t < num_tiles; t += num_clusters, ++local) {
@@ -589,11 +594,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             store_seg(g.saved_h, row * g.N + col0, vg, count, g.h_dtype, 1.0f);
             store_seg(g.saved_h, row * g.N + g.F + col0, vl, count, g.h_dtype, 1.0f);
           }
+          if (gact == TE_SILU) {  // ("silu", "linear"): its own loop, without the switch
 #pragma unroll
-          for (int p = 0; p < 16; ++p) {
-            const f32x2 y = mul2(silu2(f2(vg[2 * p], vg[2 * p + 1])), f2(vl[2 * p], vl[2 * p + 1]));
-            vg[2 * p] = f2lo(y);
-            vg[2 * p + 1] = f2hi(y);
+            for (int p = 0; p < 16; ++p) {
+              const f32x2 y = mul2(silu2(f2(vg[2 * p], vg[2 * p + 1])), f2(vl[2 * p], vl[2 * p + 1]));
+              vg[2 * p] = f2lo(y);
+              vg[2 * p + 1] = f2hi(y);
+            }
+          } else {
+#pragma unroll
+            for (int p = 0; p < 16; ++p) {
+              const f32x2 y = mul2(act2(gact, f2(vg[2 * p], vg[2 * p + 1])), f2(vl[2 * p], vl[2 * p + 1]));
+              vg[2 * p] = f2lo(y);
+              vg[2 * p + 1] = f2hi(y);
+            }
           }
           if (row_ok) {
 #pragma unroll

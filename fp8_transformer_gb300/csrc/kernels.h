@@ -9,6 +9,14 @@
 
 namespace te {
 
+// Gated activations take [gate | linear] and apply their base function to the gate half.
+__host__ __device__ constexpr bool is_gated(int act) {
+  return act == TE_SWIGLU || act == TE_GEGLU || act == TE_REGLU;
+}
+__host__ __device__ constexpr int gate_act(int act) {
+  return act == TE_SWIGLU ? TE_SILU : act == TE_GEGLU ? TE_GELU : act == TE_REGLU ? TE_RELU : act;
+}
+
 // Output stage shared by the bandwidth-bound kernels: how fp32 results become the stored
 // tensor, and which scalars the kernel reads or writes.
 struct CastSpec {

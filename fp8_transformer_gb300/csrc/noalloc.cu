@@ -78,7 +78,7 @@ te_status te_dact_dbias_quantize_noalloc(const void* dy, const void* x_preact, t
                                          const te_quantizer* q, void* dx, te_dtype dx_dtype,
                                          float* dbias, void* stream) {
   if (M < 0 || N_in <= 0 || (dtype != TE_F32 && dtype != TE_BF16) || act < TE_IDENTITY ||
-      act > TE_SWIGLU || dx_dtype < TE_F32 || dx_dtype > TE_E4M3)
+      act > TE_REGLU || dx_dtype < TE_F32 || dx_dtype > TE_E4M3)
     return TE_ERR_INVALID_ARG;
   if (M > 0 && (!dy || (act != TE_IDENTITY && !x_preact) || !dx)) return TE_ERR_INVALID_ARG;
   if (dx_dtype == TE_E4M3 && !enabled(q)) return TE_ERR_INVALID_ARG;
@@ -86,8 +86,8 @@ te_status te_dact_dbias_quantize_noalloc(const void* dy, const void* x_preact, t
                      (q->mode == TE_SCALING_CURRENT && !q->amax) || !aligned4(q->scale) ||
                      !aligned4(q->scale_inv) || !aligned4(q->amax)))
     return TE_ERR_INVALID_ARG;
-  const int64_t n_out = act == TE_SWIGLU ? N_in / 2 : N_in;
-  if ((act == TE_SWIGLU && N_in % 2) || n_out % 8) return TE_ERR_UNSUPPORTED;
+  const int64_t n_out = is_gated(act) ? N_in / 2 : N_in;
+  if ((is_gated(act) && N_in % 2) || n_out % 8) return TE_ERR_UNSUPPORTED;
   if (!aligned16(dy) || !aligned16(x_preact) || !aligned16(dx) || !aligned4(dbias))
     return TE_ERR_UNSUPPORTED;
   if (dbias && M > 0 && dact_dbias_workspace(M, N_in) > kNoAllocPartials * sizeof(float))

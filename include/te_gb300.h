@@ -53,7 +53,19 @@ typedef enum { TE_LAYERNORM = 0, TE_RMSNORM = 1 } te_norm_type;
 /* activation_type (Activation page, I/O Contract): ("relu",), ("gelu",) (tanh form),
  * ("silu",), and the gated pair ("silu", "linear") = SwiGLU.  TE_IDENTITY passes values
  * through (used for the plain bias-gradient reduction). */
-typedef enum { TE_IDENTITY = 0, TE_RELU = 1, TE_GELU = 2, TE_SILU = 3, TE_SWIGLU = 4 } te_act_type;
+/* Activations (Activation page: activation_type tuples).  TE_SWIGLU = ("silu", "linear"),
+ * TE_GEGLU = ("gelu", "linear"), TE_REGLU = ("relu", "linear") are gated: their input has twice
+ * the output's columns, [gate | linear], and the output is base(gate) * linear.  "gelu" is the
+ * tanh form throughout. */
+typedef enum {
+  TE_IDENTITY = 0,
+  TE_RELU = 1,
+  TE_GELU = 2,
+  TE_SILU = 3,
+  TE_SWIGLU = 4,
+  TE_GEGLU = 5,
+  TE_REGLU = 6
+} te_act_type;
 
 /* How a quantizer obtains its scale.
  *   TE_SCALING_DELAYED: use *scale as given (e.g. from an earlier call's amax); one pass.
@@ -135,7 +147,7 @@ te_status te_norm_fwd(const void* x, te_dtype x_dtype, int64_t M, int64_t H, con
  * te_act_lu -- activation with optional FP8 quantization (Activation page, Description: the
  * forward rule runs the tex.act_lu primitive, quantizing when asked, and returns the values
  * dequantized).
- *   x      [M, N_in] in x_dtype (TE_F32 / TE_BF16).  For TE_SWIGLU, N_in = 2 * N_out and the
+ *   x      [M, N_in] in x_dtype (TE_F32 / TE_BF16).  For a gated type, N_in = 2 * N_out and the
  *          columns are [gate | linear]: out = silu(x[:, :N_out]) * x[:, N_out:].
  *   out    [M, N_out] in out_dtype.
  *   q      NULL: out = act(x) rounded to out_dtype (TE_F32 / TE_BF16).
@@ -217,7 +229,7 @@ te_status te_layernorm_dense_fwd(const void* x, const void* kernel, te_dtype ker
  * page, Description steps (1)-(4); Signature: layernorm_mlp(x, gamma, beta, kernels, biases,
  * norm_type, zero_centered_gamma, epsilon, ..., activation_type, quantizer_set)).
  *   dtype       activation dtype of x, gamma, beta, biases, out (TE_F32 or TE_BF16).
- *   x [M, H]; kernel1 [H, F'] with F' = 2F for TE_SWIGLU (columns [gate | linear]) else F;
+ *   x [M, H]; kernel1 [H, F'] with F' = 2F for a gated act (columns [gate | linear]) else F;
  *   kernel2 [F, H]; bias1 [F'] or NULL; bias2 [H] or NULL; out [M, H].
  *   GEMM1's output plus bias1 is rounded to dtype before the activation; the activation and
  *   the FP8 casts are fused into GEMM1's epilogue, bias2 into GEMM2's.
@@ -246,7 +258,7 @@ te_status te_layernorm_mlp_fwd(const void* x, const void* gamma, const void* bet
  * sums, stored E4M3 (qset->grad) or in dtype; dln = dH kernel1^T; dkernel1 = ln^T dH; then the
  * norm backward gives dx, dgamma, dbeta.
  *   dy [M, H], x [M, H], gamma [H], kernel2 [F, H], saved_h [M, F'] in dtype (F' = 2F for
- *   TE_SWIGLU); kernel1 [H, F'] in kernel_dtype; mu, rsigma [M] from the forward.
+ *   a gated act); kernel1 [H, F'] in kernel_dtype; mu, rsigma [M] from the forward.
  *   saved_ln_out [M, H]: the forward's normalized output (E4M3 with qset, else dtype).
  *   qset NULL: every GEMM in dtype.  Non-NULL (FP8): qset->grad must be enabled and quantizes dH;
  *   qset->x.scale_inv dequantizes saved_ln_out; kernel1 is E4M3 (kernel_dtype TE_E4M3, factor in

@@ -27,7 +27,7 @@ SCALES = dict(x=32.0, w1=2048.0, act=16.0, w2=2048.0, grad=64.0)
 
 def run_gpu(inp, fp8):
     M, H, F = inp["M"], inp["H"], inp["F"]
-    gated = inp["act"] == "swiglu"
+    gated = ob.GATED[inp["act"]]
     F1 = 2 * F if gated else F
     dt = torch.bfloat16
     qs = None
@@ -109,6 +109,18 @@ def _inputs(name, shape):
 @pytest.mark.parametrize("fp8", [False, True])
 def test_mlp_backward_small(name, shape, fp8):
     inp = _inputs(name, shape)
+    g = run_gpu(inp, fp8)
+    ref = run_oracle(inp, fp8)
+    check(inp, g, ref)
+
+
+@pytest.mark.parametrize("act", ["geglu", "reglu"])
+@pytest.mark.parametrize("fp8", [False, True])
+def test_mlp_backward_other_gated(act, fp8):
+    """("gelu", "linear") and ("relu", "linear"): the recomputed activation, the gated
+    dact + dbias (+ E4M3) step and the rest of the backward."""
+    inp = _inputs("llama_rms_mlp", dict(M=256, H=512, F=528))
+    inp["act"] = act
     g = run_gpu(inp, fp8)
     ref = run_oracle(inp, fp8)
     check(inp, g, ref)

@@ -37,7 +37,7 @@ def _fp8_oracle_scales(scales):
 
 def run_mlp(inp, fp8=False, scales=MLP_SCALES, mode="delayed", rows=None):
     M, H, F = inp["M"], inp["H"], inp["F"]
-    gated = inp["act"] == "swiglu"
+    gated = ob.GATED[inp["act"]]
     dt = inp["x"].dtype
     out = torch.empty(M, H, dtype=dt, device=DEV)
     saved_h = torch.empty(M, 2 * F if gated else F, dtype=dt, device=DEV)
@@ -107,6 +107,18 @@ def test_mlp_small(name, shape):
     got = run_mlp(inp)
     ref = oracle_mlp(inp)
     check_mlp(inp, got, ref, fp8=False)
+
+
+@pytest.mark.parametrize("act", ["geglu", "reglu"])
+@pytest.mark.parametrize("fp8", [False, True])
+def test_mlp_small_other_gated(act, fp8):
+    """("gelu", "linear") and ("relu", "linear") through GEMM1's gated epilogue, on the Llama
+    workload's tensors (W1 holds [gate | linear] columns)."""
+    inp = make_inputs("llama_rms_mlp", device=DEV, M=300, H=512, F=784)
+    inp["act"] = act
+    got = run_mlp(inp, fp8=fp8)
+    ref = oracle_mlp(inp, fp8=fp8)
+    check_mlp(inp, got, ref, fp8=fp8)
 
 
 @pytest.mark.parametrize("name,shape", SMALL[1:])

@@ -57,25 +57,25 @@ def test_quantize_saturates_and_keeps_sign():
 # ------------------------------------------------------------------ activation -------------
 
 
-@pytest.mark.parametrize("act", ["relu", "gelu", "silu", "swiglu"])
+@pytest.mark.parametrize("act", ["relu", "gelu", "silu", "swiglu", "geglu", "reglu"])
 @pytest.mark.parametrize("M,N", [(1, 16), (300, 1040)])
 def test_act_lu_bf16(act, M, N):
     x = rt((M, N), std=2.0, seed=3)
-    n_out = N // 2 if act == "swiglu" else N
+    n_out = N // 2 if ob.GATED[act] else N
     out = torch.empty(M, n_out, dtype=torch.bfloat16, device=DEV)
     te.te_act_lu(x, act, out)
     ref = ob.act_fwd(np64(x), act)
     assert_elementwise_close(out, nx.bf16_round(nx.to_f32(ref)), what=act)
-    if act == "relu":  # exact arithmetic: bit-exact
+    if act in ("relu", "reglu"):  # exact arithmetic (one rounding): bit-exact
         assert np.array_equal(np64(out), nx.bf16_round(ref))
 
 
-@pytest.mark.parametrize("act", ["gelu", "swiglu"])
+@pytest.mark.parametrize("act", ["gelu", "swiglu", "geglu"])
 @pytest.mark.parametrize("mode", ["delayed", "current"])
 def test_act_lu_e4m3_and_dequantized(act, mode):
     M, N = 257, 2048
     x = rt((M, N), std=2.0, seed=4)
-    n_out = N // 2 if act == "swiglu" else N
+    n_out = N // 2 if ob.GATED[act] else N
     q = te.Quantizer(scale=64.0, mode=mode)
     out = torch.empty(M, n_out, dtype=torch.uint8, device=DEV)
     te.te_act_lu(x, act, out, q=q)
@@ -101,10 +101,10 @@ def test_act_lu_e4m3_and_dequantized(act, mode):
 # ------------------------------------------------------------------ dact + dbias -----------
 
 
-@pytest.mark.parametrize("act", ["gelu", "relu", "silu", "swiglu", "identity"])
+@pytest.mark.parametrize("act", ["gelu", "relu", "silu", "swiglu", "geglu", "reglu", "identity"])
 @pytest.mark.parametrize("M,N_in", [(1, 16), (300, 528), (1000, 4096)])
 def test_dact_dbias_bf16(act, M, N_in):
-    n_out = N_in // 2 if act == "swiglu" else N_in
+    n_out = N_in // 2 if ob.GATED.get(act, False) else N_in
     dy = rt((M, n_out), seed=5)
     h = rt((M, N_in), std=2.0, seed=6)
     dx = torch.empty(M, N_in, dtype=torch.bfloat16, device=DEV)
