@@ -42,7 +42,7 @@ EXPORTED = ["te_status_string", "te_version", "te_get_device_status", "te_worksp
             "te_profile_begin", "te_profile_end", "te_layernorm_mlp_bwd",
             "te_layernorm_dense_bwd",
             "te_dact_dbias_quantize_noalloc",
-            "te_dact_dbias_noalloc_capacity"]
+            "te_dact_dbias_noalloc_capacity", "te_selftest_wait_timeout"]
 KERNEL_KINDS = ["norm_fwd", "quantize", "act_lu", "dact_dbias", "gemm", "gemm_act", "norm_bwd",
                 "transpose"]
 
@@ -100,6 +100,7 @@ _SIGS = {
                                             _vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, _QSP,
                                             _i64, _i64, _i64, ctypes.c_int, _vp, _vp, _vp, _vp,
                                             _vp, _vp, _vp, _vp, _sz, _vp]),
+    "te_selftest_wait_timeout": (ctypes.c_int, [_i64, _vp]),
     "te_layernorm_dense_bwd": (ctypes.c_int, [_vp, _vp, _vp, _vp, ctypes.c_int, _vp, _vp, _vp,
                                               ctypes.c_int, ctypes.c_int, _QSP, _i64, _i64, _i64,
                                               ctypes.c_int, _vp, _vp, _vp, _vp, _vp, _vp, _sz,
@@ -203,6 +204,12 @@ def get_device_status() -> int:
     v = ctypes.c_int32(0)
     _check("te_get_device_status", lib().te_get_device_status(ctypes.byref(v)))
     return v.value
+
+
+def selftest_wait_timeout(limit_us: int = 20000, stream=None):
+    """Launch the library's bounded-wait self-test: a wait that nothing completes gives up after
+    limit_us and records TE_ERR_TIMEOUT, which get_device_status() then returns."""
+    _check("te_selftest_wait_timeout", lib().te_selftest_wait_timeout(int(limit_us), _stream(stream)))
 
 
 def workspace_size(op, M, H, F_or_N, dtype=TE_BF16, quantized=False, kernel_dtype=None,

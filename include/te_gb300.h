@@ -117,6 +117,14 @@ int te_version(void);
  * *device_status receives TE_OK, or the te_status a kernel recorded (e.g. TE_ERR_TIMEOUT). */
 te_status te_get_device_status(int32_t* device_status);
 
+/* Self-test of the failure reporting (no counterpart on the pages).  Launches on `stream` one
+ * kernel whose single waiting thread waits `limit_us` microseconds (1 .. 1000000) on an
+ * mbarrier that nothing completes -- the bounded wait every pipeline of this library uses --
+ * so that the wait gives up and records TE_ERR_TIMEOUT in the device status word.  The kernel
+ * then exits normally; nothing faults and the context stays usable.  Returns
+ * TE_ERR_INVALID_ARG for a limit outside the range. */
+te_status te_selftest_wait_timeout(int64_t limit_us, void* stream);
+
 /* Bytes of workspace a call needs.  dims = {M, H, F or N}; `dtype` is the activation dtype,
  * `quantized` is nonzero when a quantizer set is passed, `kernel_dtype` the weights' storage
  * dtype.  Unused dims may be 0.  Returns 0 for operations that need none. */

@@ -65,3 +65,10 @@ def test_invalid_arguments_rejected_before_launch():
                        b.TE_BF16, None) == b.TE_ERR_UNSUPPORTED
     assert lib.te_gemm(18, 0, 32, 0, b.TE_BF16, 16, 32, 16, None, None, None, b.TE_F32, 64,
                        b.TE_BF16, None) == b.TE_ERR_UNSUPPORTED
+
+
+def test_selftest_limit_checked_on_the_host():
+    lib = te.lib()
+    b = te.binding
+    for bad in (0, -5, 1000001):
+        assert lib.te_selftest_wait_timeout(bad, None) == b.TE_ERR_INVALID_ARG
