@@ -12,8 +12,8 @@ from .binding import (ACT_TUPLES, ACT_TYPES, EXPORTED, KERNEL_KINDS, NORM_TYPES,
                       te_act_lu,
                       te_dact_dbias_quantize, te_dact_dbias_quantize_noalloc, te_gemm,
                       te_layernorm_dense_bwd, te_layernorm_dense_fwd, te_layernorm_mlp_bwd,
-                      te_layernorm_mlp_fwd, te_norm_bwd, te_norm_fwd, te_quantize, version,
-                      workspace_size)
+                      te_layernorm_mlp_fwd, te_layernorm_mlp_fwd_host, te_norm_bwd, te_norm_fwd,
+                      te_quantize, version, workspace_size)
 from .binding import *  # noqa: F401,F403  (enum constants)
 
 __all__ = ["Quantizer", "QuantizerSet", "TEError", "te_norm_fwd", "te_act_lu",
@@ -23,4 +23,4 @@ __all__ = ["Quantizer", "QuantizerSet", "TEError", "te_norm_fwd", "te_act_lu",
            "get_device_status", "status_string", "workspace_size", "EXPORTED", "ACT_TYPES",
            "ACT_TUPLES", "NORM_TYPES", "KERNEL_KINDS", "profile_begin", "profile_end",
            "te_dact_dbias_quantize_noalloc", "dact_dbias_noalloc_capacity",
-           "selftest_wait_timeout"]
+           "selftest_wait_timeout", "te_layernorm_mlp_fwd_host"]

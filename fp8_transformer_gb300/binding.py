@@ -23,7 +23,7 @@ TE_IDENTITY, TE_RELU, TE_GELU, TE_SILU, TE_SWIGLU, TE_GEGLU, TE_REGLU = range(7)
 TE_SCALING_DELAYED, TE_SCALING_CURRENT = 0, 1
 (TE_OP_NORM_FWD, TE_OP_ACT_LU, TE_OP_DACT_DBIAS, TE_OP_LAYERNORM_DENSE_FWD,
  TE_OP_LAYERNORM_MLP_FWD, TE_OP_NORM_BWD, TE_OP_LAYERNORM_MLP_BWD,
- TE_OP_LAYERNORM_DENSE_BWD) = range(8)
+ TE_OP_LAYERNORM_DENSE_BWD, TE_OP_LAYERNORM_MLP_FWD_HOST) = range(9)
 
 NORM_TYPES = {"layernorm": TE_LAYERNORM, "rmsnorm": TE_RMSNORM}
 ACT_TYPES = {"identity": TE_IDENTITY, "relu": TE_RELU, "gelu": TE_GELU, "silu": TE_SILU,
@@ -42,7 +42,8 @@ EXPORTED = ["te_status_string", "te_version", "te_get_device_status", "te_worksp
             "te_profile_begin", "te_profile_end", "te_layernorm_mlp_bwd",
             "te_layernorm_dense_bwd",
             "te_dact_dbias_quantize_noalloc",
-            "te_dact_dbias_noalloc_capacity", "te_selftest_wait_timeout"]
+            "te_dact_dbias_noalloc_capacity", "te_selftest_wait_timeout",
+            "te_layernorm_mlp_fwd_host"]
 KERNEL_KINDS = ["norm_fwd", "quantize", "act_lu", "dact_dbias", "gemm", "gemm_act", "norm_bwd",
                 "transpose"]
 
@@ -101,6 +102,10 @@ _SIGS = {
                                             _i64, _i64, _i64, ctypes.c_int, _vp, _vp, _vp, _vp,
                                             _vp, _vp, _vp, _vp, _sz, _vp]),
     "te_selftest_wait_timeout": (ctypes.c_int, [_i64, _vp]),
+    "te_layernorm_mlp_fwd_host": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_int,
+                                                 ctypes.c_int, ctypes.c_float, ctypes.c_int, _i64,
+                                                 _i64, _i64, ctypes.c_int, _vp, ctypes.c_int, _vp,
+                                                 _sz, _vp]),
     "te_layernorm_dense_bwd": (ctypes.c_int, [_vp, _vp, _vp, _vp, ctypes.c_int, _vp, _vp, _vp,
                                               ctypes.c_int, ctypes.c_int, _QSP, _i64, _i64, _i64,
                                               ctypes.c_int, _vp, _vp, _vp, _vp, _vp, _vp, _sz,
@@ -140,6 +145,15 @@ def _check(fn: str, status: int):
     if status != TE_OK:
         msg = lib().te_status_string(status).decode()
         raise TEError(fn, status, msg)
+
+
+def _host_ptr(t):
+    """Host tensor for the host-buffer entry points (pinned memory lets the copies overlap)."""
+    if t.is_cuda:
+        raise ValueError("this argument is a host buffer")
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return t.data_ptr()
 
 
 def _ptr(t):
@@ -331,6 +345,28 @@ def te_layernorm_mlp_fwd(x, gamma, beta, kernel1, kernel2, bias1, bias2, out,
                                     _stream(stream))
     _check("te_layernorm_mlp_fwd", st)
     return out
+
+
+def te_layernorm_mlp_fwd_host(x_host, gamma, beta, kernel1, kernel2, bias1, bias2, out_host,
+                              norm_type="layernorm", zero_centered_gamma=False, epsilon=1e-6,
+                              activation_type=("relu",), chunks=4, workspace=None, stream=None):
+    """te_layernorm_mlp_fwd with x and out in (pinned) host memory, copies overlapped with the
+    compute of other row slices; the weights are device tensors."""
+    M, H = x_host.shape
+    F = kernel2.shape[0]
+    act = _act_id(activation_type)
+    dt = _dt(x_host)
+    if workspace is None:
+        workspace = _ws(workspace_size(TE_OP_LAYERNORM_MLP_FWD_HOST, M, H, F, dt, False, dt, act),
+                        kernel1.device)
+    st = lib().te_layernorm_mlp_fwd_host(_host_ptr(x_host), _ptr(gamma), _ptr(beta), _ptr(kernel1),
+                                         _ptr(kernel2), _ptr(bias1), _ptr(bias2),
+                                         _norm_id(norm_type), int(bool(zero_centered_gamma)),
+                                         float(epsilon), act, M, H, F, dt, _host_ptr(out_host),
+                                         int(chunks), _ptr(workspace), workspace.numel(),
+                                         _stream(stream))
+    _check("te_layernorm_mlp_fwd_host", st)
+    return out_host
 
 
 def te_layernorm_mlp_bwd(dy, x, gamma, kernel1, kernel2, saved_h, saved_ln_out, mu, rsigma,

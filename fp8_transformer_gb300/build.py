@@ -20,7 +20,7 @@ BUILD_DIR = os.path.join(HERE, "_build")
 LIB_NAME = "libte_gb300.so"
 LIB_PATH = os.path.join(HERE, LIB_NAME)
 SOURCES = ["api.cu", "norm.cu", "elementwise.cu", "gemm.cu", "tmap.cu", "profile.cu", "noalloc.cu",
-           "selftest.cu"]
+           "selftest.cu", "host_pipeline.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -258,6 +258,8 @@ size_t te_workspace_size(te_op op, int64_t M, int64_t H, int64_t F_or_N, te_dtyp
       return mlp_layout(nullptr, M, H, F_or_N, dtype, quantized != 0, kernel_dtype, act, false).bytes;
     case TE_OP_LAYERNORM_MLP_BWD:
       return bwd_layout(nullptr, M, H, F_or_N, dtype, quantized != 0, kernel_dtype, act).bytes;
+    case TE_OP_LAYERNORM_MLP_FWD_HOST:
+      return host_fwd_workspace(M, H, F_or_N, dtype, act);
     case TE_OP_LAYERNORM_DENSE_BWD:
       return dense_bwd_layout(nullptr, M, H, F_or_N, dtype, quantized != 0, kernel_dtype).bytes;
     default: return 0;

@@ -62,6 +62,9 @@ struct NormBwdArgs {
   float* partials = nullptr; // workspace: [chunks, 2, H]
 };
 te_status launch_norm_bwd(const NormBwdArgs& a, cudaStream_t s);
+
+// Workspace of te_layernorm_mlp_fwd_host: device staging of x and out plus one forward's.
+size_t host_fwd_workspace(int64_t M, int64_t H, int64_t F, int dtype, int act);
 size_t norm_bwd_workspace(int64_t M, int64_t H);
 
 struct ActArgs {

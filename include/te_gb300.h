@@ -104,7 +104,8 @@ typedef enum {
   TE_OP_LAYERNORM_MLP_FWD = 4,
   TE_OP_NORM_BWD = 5,
   TE_OP_LAYERNORM_MLP_BWD = 6,
-  TE_OP_LAYERNORM_DENSE_BWD = 7
+  TE_OP_LAYERNORM_DENSE_BWD = 7,
+  TE_OP_LAYERNORM_MLP_FWD_HOST = 8
 } te_op;
 
 /* Human-readable name of a status code (static storage, never NULL). */
@@ -256,6 +257,34 @@ te_status te_layernorm_mlp_fwd(const void* x, const void* gamma, const void* bet
                                te_dtype dtype, void* out, void* saved_h, void* saved_ln_out,
                                float* mu, float* rsigma, void* workspace, size_t ws_bytes,
                                void* stream);
+
+/* ---------------------------------------------------------------------------------------
+ * te_layernorm_mlp_fwd_host -- te_layernorm_mlp_fwd (LayerNorm MLP page, Description steps
+ * (1)-(4)) with the activations in HOST memory: x_host [M, H] and out_host [M, H] are host
+ * pointers (pinned -- cudaHostAlloc or cudaHostRegister -- for the copies to overlap); gamma,
+ * beta, the kernels and the biases are device pointers as in te_layernorm_mlp_fwd.  No quantizer
+ * set (a per-tensor FP8 scale needs every row before the cast) and no saved tensors.
+ *   The rows are cut into at most `chunks` (1 .. 16) slices: the first and the last small (their
+ *   copies are the ones no compute hides), the middle ones seven times larger, all but the last
+ *   a multiple of 256 rows.  All host -> device copies are issued on a copy-in stream, each
+ *   slice's forward runs on `stream` once
+ *   its rows have landed, and its output returns on a copy-out stream as soon as it is
+ *   computed; two such streams are created per device on first use and kept.  The copies start
+ *   after the work already queued on `stream`, and `stream` waits for the last copy out before
+ *   anything queued after the call, so the call is asynchronous and ordered like the others.
+ *   Concurrent calls on one device from several host threads are not supported.
+ *   workspace: te_workspace_size(TE_OP_LAYERNORM_MLP_FWD_HOST, M, H, F, dtype, 0, dtype, act)
+ *   bytes, 256-byte aligned (device staging of x and out, and one forward's workspace).
+ *   dtype TE_BF16 or TE_F32; the kernels in dtype.  Errors as for te_layernorm_mlp_fwd, plus
+ *   TE_ERR_INVALID_ARG for `chunks` outside 1 .. 16.
+ */
+te_status te_layernorm_mlp_fwd_host(const void* x_host, const void* gamma, const void* beta,
+                                    const void* kernel1, const void* kernel2, const void* bias1,
+                                    const void* bias2, te_norm_type norm_type,
+                                    int zero_centered_gamma, float epsilon, te_act_type act,
+                                    int64_t M, int64_t H, int64_t F, te_dtype dtype,
+                                    void* out_host, int chunks, void* workspace, size_t ws_bytes,
+                                    void* stream);
 
 /* ---------------------------------------------------------------------------------------
  * te_layernorm_mlp_bwd -- backward of te_layernorm_mlp_fwd (LayerNorm MLP page, Description:
