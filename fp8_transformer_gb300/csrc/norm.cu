@@ -479,11 +479,18 @@ __global__ void __launch_bounds__((kBwdGroups * kBwdGroupWarps + 1) * 32, 1)
 #pragma unroll
     for (int j = 0; j < RB; ++j)
       if (j < nr && ok) ok = ring_acquire(full, s0 + j, use, abort_flag, status);
-    // pass 1: sum(dz * g) and sum(dz * g * xhat) over each row
+    // pass 1, over the rows in shared memory: the two row sums sum(dz * g) and
+    // sum(dz * g * xhat), and the column sums dgamma += dz * xhat, dbeta += dz (which do not
+    // depend on the row sums); xhat and dz * g stay in registers for pass 2
     float t1[RB], t2[RB];
+    f32x2 xk[RB][NV][P], gk[RB][NV][P];
 #pragma unroll
     for (int j = 0; j < RB; ++j) {
       f32x2 s1 = f2s(0.0f), s2 = f2s(0.0f);
+#pragma unroll
+      for (int i = 0; i < NV; ++i)
+#pragma unroll
+        for (int p = 0; p < P; ++p) { xk[j][i][p] = f2s(0.0f); gk[j][i][p] = f2s(0.0f); }
       if (ok && j < nr) {
         const uint4* xs = reinterpret_cast<const uint4*>(slot0 + j * slot_bytes) + gt;
         const uint4* dzs = xs + nvec;
@@ -499,12 +506,23 @@ __global__ void __launch_bounds__((kBwdGroups * kBwdGroupWarps + 1) * 32, 1)
               const f32x2 dyg = mul2(dp[p], gp[i][p]);
               if (LN) s1 = add2(s1, dyg);
               s2 = fma2(dyg, xh, s2);
+              accg[i][p] = fma2(dp[p], xh, accg[i][p]);
+              if (LN) accb[i][p] = add2(accb[i][p], dp[p]);
+              xk[j][i][p] = xh;
+              gk[j][i][p] = dyg;
             }
           }
         }
       }
       t1[j] = LN ? f2lo(s1) + f2hi(s1) : 0.0f;
       t2[j] = f2lo(s2) + f2hi(s2);
+    }
+    // the slots are no longer read: the producer may refill them while the sums meet
+    __syncwarp();
+    if (lane == 0 && ok) {
+#pragma unroll
+      for (int j = 0; j < RB; ++j)
+        if (j < nr) mbar_arrive(smem_u32(&empty[s0 + j]));
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -520,8 +538,10 @@ __global__ void __launch_bounds__((kBwdGroups * kBwdGroupWarps + 1) * 32, 1)
       for (int j = 0; j < RB; ++j) red[grp][par][j][wg] = make_float2(t1[j], t2[j]);
     }
     if (group_sync_or(!ok, 1 + grp, GT)) break;
-    // the group's warps add their sums in warp order (the same bits in every thread)
-    f32x2 m1[RB], m2[RB];
+    // the group's warps add their sums in warp order (the same bits in every thread);
+    // dx = rs * (dz * g - mean(dz * g) - xhat * mean(dz * g * xhat))
+    //    = (dz * g) * rs + c1 + xhat * c2,  c1 = -rs * mean(dz * g), c2 = -rs * mean(dz * g * xhat)
+    f32x2 c1[RB], c2[RB];
 #pragma unroll
     for (int j = 0; j < RB; ++j) {
       float r1 = 0.0f, r2 = 0.0f;
@@ -531,30 +551,22 @@ __global__ void __launch_bounds__((kBwdGroups * kBwdGroupWarps + 1) * 32, 1)
         r1 += r.x;
         r2 += r.y;
       }
-      m1[j] = f2s(LN ? -r1 * inv_h : 0.0f);  // negated, for the fma below
-      m2[j] = f2s(-r2 * inv_h);
+      const float rs = f2lo(rs2[j]);
+      c1[j] = f2s(LN ? -rs * (r1 * inv_h) : 0.0f);
+      c2[j] = f2s(-rs * (r2 * inv_h));
     }
-    // pass 2: dx = rs * (dz * g - m1 - xhat * m2); dgamma += dz * xhat; dbeta += dz
+    // pass 2, from registers
 #pragma unroll
     for (int j = 0; j < RB; ++j) {
       if (j < nr) {
-        const uint4* xs = reinterpret_cast<const uint4*>(slot0 + j * slot_bytes) + gt;
-        const uint4* dzs = xs + nvec;
         T* dxr = dx0 + j * dx_step;
 #pragma unroll
         for (int i = 0; i < NV; ++i) {
           if (mine(gt + i * GT)) {
-            f32x2 xp[P], dp[P];
-            PR::cvt(xs[i * GT], xp);
-            PR::cvt(dzs[i * GT], dp);
             float d[E];
 #pragma unroll
             for (int p = 0; p < P; ++p) {
-              const f32x2 xh = LN ? mul2(sub2(xp[p], mu2[j]), rs2[j]) : mul2(xp[p], rs2[j]);
-              const f32x2 t = fma2(xh, m2[j], fma2(dp[p], gp[i][p], m1[j]));
-              const f32x2 dd = mul2(t, rs2[j]);
-              accg[i][p] = fma2(dp[p], xh, accg[i][p]);
-              if (LN) accb[i][p] = add2(accb[i][p], dp[p]);
+              const f32x2 dd = fma2(xk[j][i][p], c2[j], fma2(gk[j][i][p], rs2[j], c1[j]));
               d[2 * p] = f2lo(dd);
               d[2 * p + 1] = f2hi(dd);
             }
@@ -562,12 +574,6 @@ __global__ void __launch_bounds__((kBwdGroups * kBwdGroupWarps + 1) * 32, 1)
           }
         }
       }
-    }
-    __syncwarp();
-    if (lane == 0) {
-#pragma unroll
-      for (int j = 0; j < RB; ++j)
-        if (j < nr) mbar_arrive(smem_u32(&empty[s0 + j]));
     }
     jj += RB;
     if (jj == spc) { jj = 0; ++use; }
