@@ -336,6 +336,35 @@ def bandwidth_kernels(args, dev, peaks):
             "peak_hbm_gbs": peaks["hbm"]}
 
 
+def single_gemm(args, dev, peaks):
+    """Profiling aid: one bf16 te_gemm shape, op(A)[M, K] op(B)[K, N] with the given transposes
+    (--gemm M,N,K,a_trans,b_trans), timed with CUDA events next to cuBLAS (torch.matmul) on the
+    same operands."""
+    import torch
+
+    import fp8_transformer_gb300 as te
+
+    M, N, K, at, bt = (int(v) for v in args.gemm.split(","))
+    g = torch.Generator(device=dev).manual_seed(0)
+    rnd = lambda *shape: (torch.randn(*shape, generator=g, device=dev) * 0.02).to(torch.bfloat16)
+    A = rnd(K, M) if at else rnd(M, K)
+    B = rnd(N, K) if bt else rnd(K, N)
+    out = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+    flush = make_flush(dev)
+    flops = 2.0 * M * N * K
+    ours = lambda: te.te_gemm(A, B, out, a_trans=bool(at), b_trans=bool(bt))
+    opA, opB = (A.t() if at else A), (B.t() if bt else B)
+    lib = lambda: torch.matmul(opA, opB, out=out)
+    res = {"gemm": [M, N, K, at, bt], "dtype": "bf16"}
+    for name, fn in (("te_gemm", ours), ("cublas", lib)):
+        for _ in range(args.warmup):
+            fn()
+        ms = statistics.mean(time_steps(fn, args.steps, flush))
+        res[name] = {"ms": ms, "TFLOP/s": flops / (ms / 1e3) / 1e12,
+                     "frac": flops / (ms / 1e3) / 1e12 / peaks["bf16"]}
+    return res
+
+
 def run_ours(args, rank, world, local_rank):
     import numpy as np
     import torch
@@ -351,6 +380,10 @@ def run_ours(args, rank, world, local_rank):
     if args.bandwidth_only:
         if rank == 0:
             print(json.dumps(bandwidth_kernels(args, dev, peaks)), flush=True)
+        return
+    if args.gemm:
+        if rank == 0:
+            print(json.dumps(single_gemm(args, dev, peaks)), flush=True)
         return
     inp = make_inputs(WORKLOAD, device=dev, seed=rank, M=args.tokens)
     M, H, F = inp["M"], inp["H"], inp["F"]
@@ -657,6 +690,8 @@ def main():
                     help="time only the bandwidth-bound kernels (profiling aid)")
     ap.add_argument("--calibrate", action="store_true",
                     help="with --kernels-only: also time cuBLAS on the same GEMM shapes")
+    ap.add_argument("--gemm", default=None, metavar="M,N,K,a_trans,b_trans",
+                    help="time one bf16 te_gemm shape next to cuBLAS (profiling aid)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     world = int(os.environ.get("WORLD_SIZE", "1"))
