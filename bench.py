@@ -573,10 +573,15 @@ def run_ours(args, rank, world, local_rank):
     qg_d.mode = te.binding.TE_SCALING_DELAYED
     for tag, fp8 in (("bf16", False), ("fp8", True)):
         dense_bwd(fp8)
+        torch.cuda.synchronize()
+        te.profile_begin(64 * args.steps)
         ms = max_over_ranks(statistics.mean(time_steps(lambda: dense_bwd(fp8),
                                                        max(3, args.steps // 2), flush)))
+        prof = te.profile_end()
         extra[f"ln_dense_bwd_{tag}"] = {"TFLOP/s": 2 * dflops / (ms / 1e3) / 1e12, "ms": ms,
-                                        "workload": "qkv_ln_dense backward M=16384 H=8192 N=24576"}
+                                        "workload": "qkv_ln_dense backward M=16384 H=8192 N=24576",
+                                        "kernel_ms": {k: round(v[0] / max(v[1], 1), 4)
+                                                      for k, v in prof.items() if v[1]}}
     del dense, qout, kq, dd, dyq
     bw = make_inputs("gpt_ln_mlp_bwd", device=dev, seed=rank)
     Mb, Hb, Fb = bw["M"], bw["H"], bw["F"]

@@ -400,6 +400,9 @@ __global__ void __launch_bounds__((kBwdGroups * kBwdGroupWarps + 1) * 32, 1)
   constexpr int G = kBwdGroupWarps;
   constexpr int GT = G * 32;
   constexpr int RB = bwd_rows_per_sync(NV);
+  // xhat and dz * g of the step's rows stay in registers for pass 2 when few enough; otherwise
+  // pass 2 reads the slots again (and they are released after it)
+  constexpr bool KEEP = NV <= 2;
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ float2 red[kBwdGroups][2][RB][G];
   const int groups = (int(blockDim.x >> 5) - 1) / G;  // the last warp produces
@@ -483,14 +486,17 @@ __global__ void __launch_bounds__((kBwdGroups * kBwdGroupWarps + 1) * 32, 1)
     // sum(dz * g * xhat), and the column sums dgamma += dz * xhat, dbeta += dz (which do not
     // depend on the row sums); xhat and dz * g stay in registers for pass 2
     float t1[RB], t2[RB];
-    f32x2 xk[RB][NV][P], gk[RB][NV][P];
+    constexpr int KR = KEEP ? RB : 1, KV = KEEP ? NV : 1;
+    f32x2 xk[KR][KV][P], gk[KR][KV][P];
 #pragma unroll
     for (int j = 0; j < RB; ++j) {
       f32x2 s1 = f2s(0.0f), s2 = f2s(0.0f);
+      if constexpr (KEEP) {
 #pragma unroll
-      for (int i = 0; i < NV; ++i)
+        for (int i = 0; i < NV; ++i)
 #pragma unroll
-        for (int p = 0; p < P; ++p) { xk[j][i][p] = f2s(0.0f); gk[j][i][p] = f2s(0.0f); }
+          for (int p = 0; p < P; ++p) { xk[j][i][p] = f2s(0.0f); gk[j][i][p] = f2s(0.0f); }
+      }
       if (ok && j < nr) {
         const uint4* xs = reinterpret_cast<const uint4*>(slot0 + j * slot_bytes) + gt;
         const uint4* dzs = xs + nvec;
@@ -508,8 +514,10 @@ __global__ void __launch_bounds__((kBwdGroups * kBwdGroupWarps + 1) * 32, 1)
               s2 = fma2(dyg, xh, s2);
               accg[i][p] = fma2(dp[p], xh, accg[i][p]);
               if (LN) accb[i][p] = add2(accb[i][p], dp[p]);
-              xk[j][i][p] = xh;
-              gk[j][i][p] = dyg;
+              if constexpr (KEEP) {
+                xk[j][i][p] = xh;
+                gk[j][i][p] = dyg;
+              }
             }
           }
         }
@@ -517,12 +525,14 @@ __global__ void __launch_bounds__((kBwdGroups * kBwdGroupWarps + 1) * 32, 1)
       t1[j] = LN ? f2lo(s1) + f2hi(s1) : 0.0f;
       t2[j] = f2lo(s2) + f2hi(s2);
     }
-    // the slots are no longer read: the producer may refill them while the sums meet
-    __syncwarp();
-    if (lane == 0 && ok) {
+    if constexpr (KEEP) {
+      // the slots are no longer read: the producer may refill them while the sums meet
+      __syncwarp();
+      if (lane == 0 && ok) {
 #pragma unroll
-      for (int j = 0; j < RB; ++j)
-        if (j < nr) mbar_arrive(smem_u32(&empty[s0 + j]));
+        for (int j = 0; j < RB; ++j)
+          if (j < nr) mbar_arrive(smem_u32(&empty[s0 + j]));
+      }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -555,24 +565,48 @@ __global__ void __launch_bounds__((kBwdGroups * kBwdGroupWarps + 1) * 32, 1)
       c1[j] = f2s(LN ? -rs * (r1 * inv_h) : 0.0f);
       c2[j] = f2s(-rs * (r2 * inv_h));
     }
-    // pass 2, from registers
+    // pass 2, from registers (or from the slots again)
 #pragma unroll
     for (int j = 0; j < RB; ++j) {
       if (j < nr) {
         T* dxr = dx0 + j * dx_step;
+        const uint4* xs = reinterpret_cast<const uint4*>(slot0 + j * slot_bytes) + gt;
+        const uint4* dzs = xs + nvec;
 #pragma unroll
         for (int i = 0; i < NV; ++i) {
           if (mine(gt + i * GT)) {
+            f32x2 xh[P], dyg[P];
+            if constexpr (KEEP) {
+#pragma unroll
+              for (int p = 0; p < P; ++p) { xh[p] = xk[j][i][p]; dyg[p] = gk[j][i][p]; }
+            } else {
+              f32x2 xp[P], dp[P];
+              PR::cvt(xs[i * GT], xp);
+              PR::cvt(dzs[i * GT], dp);
+#pragma unroll
+              for (int p = 0; p < P; ++p) {
+                xh[p] = LN ? mul2(sub2(xp[p], mu2[j]), rs2[j]) : mul2(xp[p], rs2[j]);
+                dyg[p] = mul2(dp[p], gp[i][p]);
+              }
+            }
             float d[E];
 #pragma unroll
             for (int p = 0; p < P; ++p) {
-              const f32x2 dd = fma2(xk[j][i][p], c2[j], fma2(gk[j][i][p], rs2[j], c1[j]));
+              const f32x2 dd = fma2(xh[p], c2[j], fma2(dyg[p], rs2[j], c1[j]));
               d[2 * p] = f2lo(dd);
               d[2 * p + 1] = f2hi(dd);
             }
             store_out<(E == 8 ? OUT_BF16 : OUT_F32), E>(dxr, int64_t(i) * GT * E, d, CastState{});
           }
         }
+      }
+    }
+    if constexpr (!KEEP) {
+      __syncwarp();
+      if (lane == 0) {
+#pragma unroll
+        for (int j = 0; j < RB; ++j)
+          if (j < nr) mbar_arrive(smem_u32(&empty[s0 + j]));
       }
     }
     jj += RB;
