@@ -82,7 +82,8 @@ __global__ void __launch_bounds__(kActWarps * 32, 3) act_lu_kernel(ActArgs a) {
       constexpr int OUT = decltype(tag)::value;
       constexpr bool AMAX = decltype(atag)::value;
       for (int64_t rb = r0 + warp; rb < r1; rb += kActUnroll * kActWarps) {
-        uint4 rg[kActUnroll], rl[kActUnroll];
+        uint4 rg[kActUnroll], rl[kActUnroll];  // rl: the linear halves (gated types only)
+        (void)rl;
 #pragma unroll
         for (int j = 0; j < kActUnroll; ++j) {
           const int64_t r = rb + int64_t(j) * kActWarps;
@@ -96,6 +97,7 @@ __global__ void __launch_bounds__(kActWarps * 32, 3) act_lu_kernel(ActArgs a) {
           const int64_t r = rb + int64_t(j) * kActWarps;
           if (r >= r1) break;
           f32x2 hp[PR::P], lp[PR::P];
+          (void)lp;
           PR::get(rg[j], hp);
           if constexpr (kGated) PR::get(rl[j], lp);
           float y[E];
@@ -155,7 +157,9 @@ __global__ void __launch_bounds__(kDactWarps * 32, 3) dact_dbias_kernel(DactArgs
       constexpr bool AMAX = decltype(atag)::value;
       for (int64_t rb = r0 + warp; rb < r1; rb += kDactUnroll * kDactWarps) {
         // every load of kDactUnroll rows is issued before any of them is used
-        uint4 rdy[kDactUnroll], rx[kDactUnroll], rl[kDactUnroll];
+        uint4 rdy[kDactUnroll], rx[kDactUnroll], rl[kDactUnroll];  // rx, rl unused by some types
+        (void)rx;
+        (void)rl;
 #pragma unroll
         for (int j = 0; j < kDactUnroll; ++j) {
           const int64_t r = rb + int64_t(j) * kDactWarps;
@@ -171,6 +175,7 @@ __global__ void __launch_bounds__(kDactWarps * 32, 3) dact_dbias_kernel(DactArgs
           const int64_t r = rb + int64_t(j) * kDactWarps;
           if (r >= r1) break;
           f32x2 dyp[P], hp[P];
+          (void)hp;
           PR::get(rdy[j], dyp);
           if constexpr (!kIdent) PR::get(rx[j], hp);
           if constexpr (kGated) {

@@ -89,7 +89,7 @@ struct GemmDev {
   int* status;
 };
 
-struct __align__(64) GemmParams {
+struct GemmParams {  // aligned like its tensor maps
   CUtensorMap tmA;
   CUtensorMap tmB;
   GemmDev g;
@@ -254,12 +254,6 @@ __device__ __forceinline__ Tile tile_of(int t, int num_m, int num_n, int group_m
 
 // ------------------------------------------------------------------ epilogue stores -------
 
-__device__ __forceinline__ float load_bias(const void* bias, int dtype, int64_t j) {
-  if (dtype == TE_BF16) return __bfloat162float(static_cast<const __nv_bfloat16*>(bias)[j]);
-  return static_cast<const float*>(bias)[j];
-}
-
-// Stores `count` (16 or 32) values of one row segment starting at element `off`.
 __device__ __forceinline__ void store_seg(void* base, int64_t off, const float (&v)[32],
                                           int count, int dtype, float scale) {
   if (dtype == TE_F32) {
@@ -300,13 +294,6 @@ __device__ __forceinline__ f32x2 load_bias_pair(const void* bias, int dtype, int
 // Rounds both halves of a pair to bf16 (round to nearest even) and back to fp32.
 __device__ __forceinline__ f32x2 round_bf16_2(f32x2 v) {
   return bf16x2_f2(pack_bf16x2(f2lo(v), f2hi(v)));
-}
-
-__device__ __forceinline__ void round_to(float (&v)[32], int dtype) {
-  if (dtype == TE_BF16) {
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = round_bf16(v[i]);
-  }
 }
 
 // ------------------------------------------------------------------ the kernel ------------
