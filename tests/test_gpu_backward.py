@@ -25,16 +25,22 @@ DEV = "cuda"
 SCALES = dict(x=32.0, w1=2048.0, act=16.0, w2=2048.0, grad=64.0)
 
 
-def run_gpu(inp, fp8):
+def run_gpu(inp, fp8, mode="delayed", keep=None):
+    """GPU forward + backward; `keep` (a dict) receives the quantizer set."""
     M, H, F = inp["M"], inp["H"], inp["F"]
     gated = ob.GATED[inp["act"]]
     F1 = 2 * F if gated else F
     dt = torch.bfloat16
     qs = None
-    if fp8:
+    if fp8 and mode == "delayed":
         qs = te.QuantizerSet(x=te.Quantizer(SCALES["x"]), kernel1=te.Quantizer(SCALES["w1"]),
                              act=te.Quantizer(SCALES["act"]), kernel2=te.Quantizer(SCALES["w2"]),
                              grad=te.Quantizer(SCALES["grad"]))
+    elif fp8:
+        qs = te.QuantizerSet(**{k: te.Quantizer(mode="current")
+                                for k in ("x", "kernel1", "act", "kernel2", "grad")})
+    if keep is not None:
+        keep["qs"] = qs
     out = torch.empty(M, H, dtype=dt, device=DEV)
     h = torch.empty(M, F1, dtype=dt, device=DEV)
     ln = torch.empty(M, H, dtype=torch.uint8 if fp8 else dt, device=DEV)
@@ -59,12 +65,12 @@ def run_gpu(inp, fp8):
     return g
 
 
-def run_oracle(inp, fp8, rows=None):
+def run_oracle(inp, fp8, scales=None):
     f = lambda k: None if inp.get(k) is None else np64(inp[k])
+    sc = scales if scales is not None else {k: np.float32(v) for k, v in SCALES.items()}
     return ob.layernorm_mlp_bwd(f("dy"), f("x"), f("gamma"), f("beta"), f("w1"), f("w2"),
                                 f("b1"), f("b2"), inp["norm"], inp["zero_centered_gamma"],
-                                inp["eps"], inp["act"], "bf16",
-                                fp8={k: np.float32(v) for k, v in SCALES.items()} if fp8 else None)
+                                inp["eps"], inp["act"], "bf16", fp8=sc if fp8 else None)
 
 
 def close(got, ref, what, rel=2e-2):
@@ -111,6 +117,33 @@ def test_mlp_backward_small(name, shape, fp8):
     inp = _inputs(name, shape)
     g = run_gpu(inp, fp8)
     ref = run_oracle(inp, fp8)
+    check(inp, g, ref)
+
+
+@pytest.mark.parametrize("name,shape", CASES)
+def test_mlp_backward_fp8_current_scaling(name, shape):
+    """Every quantizer in current scaling: the forward's casts and the backward's dH cast each
+    take a separate amax pass (the dbias reduction runs in dH's amax pass).  The normalized
+    output, the activation output and dH are computed by each side itself, so the oracle
+    quantizes them with the GPU's scales, after checking that each scale is the recipe's
+    function of the GPU's amax and that the amaxes agree; the weights' scales come from
+    identical inputs and must be identical."""
+    inp = _inputs(name, shape)
+    keep = {}
+    g = run_gpu(inp, True, mode="current", keep=keep)
+    qs = keep["qs"]
+    gpu_scale = {}
+    for name_q, q in (("x", qs.x), ("act", qs.act), ("grad", qs.grad)):
+        amax = np.float32(q.amax.item())
+        assert np.float32(q.scale.item()) == nx.compute_scale(amax)[0], name_q
+        gpu_scale[name_q] = np.float32(q.scale.item())
+    ref = run_oracle(inp, True, scales=dict(x=gpu_scale["x"], w1=None, act=gpu_scale["act"],
+                                            w2=None, grad=gpu_scale["grad"]))
+    assert np.float32(qs.kernel1.scale.item()) == ref["fwd"]["w1"].scale
+    assert np.float32(qs.kernel2.scale.item()) == ref["fwd"]["w2"].scale
+    assert abs(qs.x.amax.item() - float(ref["fwd"]["ln"].amax)) <= 1e-5 * float(ref["fwd"]["ln"].amax)
+    assert abs(qs.act.amax.item() - float(ref["fwd"]["a"].amax)) <= 2e-2 * float(ref["fwd"]["a"].amax)
+    assert abs(qs.grad.amax.item() - float(ref["dh"].amax)) <= 2e-2 * float(ref["dh"].amax)
     check(inp, g, ref)
 
 
