@@ -268,7 +268,8 @@ def cublas_calibration(M, H, F, gated, dev, steps, flush):
 def bandwidth_kernels(args, dev, peaks):
     """GB/s of the bandwidth-bound kernels alone (profiling aid): norm forward at the Llama
     shape (bf16 and E4M3 out), and at the GPT backward shape the activation recompute, the
-    dact + dbias + quantize step and the norm backward.  --tokens scales the token count."""
+    dact + dbias + quantize step and the norm backward (LayerNorm and RMSNorm; LayerNorm also
+    at the QKV projection's hidden size 8192).  --tokens scales the token count."""
     import torch
 
     import fp8_transformer_gb300 as te
@@ -332,6 +333,21 @@ def bandwidth_kernels(args, dev, peaks):
                       device=dev)
     run("norm_bwd_bf16", lambda: te.te_norm_bwd(dz, xb, mub, rsb, g, "layernorm", False, dx, dgm,
                                                 dbt, workspace=wsn), Mb * H * 6 + Mb * 8)
+    run("norm_bwd_rms_bf16", lambda: te.te_norm_bwd(dz, xb, mub, rsb, g, "rmsnorm", False, dx,
+                                                    dgm, dbt, workspace=wsn), Mb * H * 6 + Mb * 4)
+    del xb, dz, dx, wsn
+    H2 = 2 * H  # the QKV projection's hidden size
+    xb = random_tensor((Mb, H2), device=dev, seed=5)
+    dz = random_tensor((Mb, H2), device=dev, seed=6)
+    dx = torch.empty(Mb, H2, dtype=torch.bfloat16, device=dev)
+    g2 = random_tensor((H2,), std=0.05, device=dev, seed=2)
+    dgm = torch.empty(H2, dtype=torch.float32, device=dev)
+    dbt = torch.empty(H2, dtype=torch.float32, device=dev)
+    wsn = torch.empty(te.workspace_size(te.binding.TE_OP_NORM_BWD, Mb, H2, 0), dtype=torch.uint8,
+                      device=dev)
+    run("norm_bwd_bf16_h8192", lambda: te.te_norm_bwd(dz, xb, mub, rsb, g2, "layernorm", False,
+                                                      dx, dgm, dbt, workspace=wsn),
+        Mb * H2 * 6 + Mb * 8)
     return {"bandwidth_only": True, "tokens_norm": M, "tokens_bwd": Mb, "kernels": res,
             "peak_hbm_gbs": peaks["hbm"]}
 

@@ -11,15 +11,15 @@
 // path reached about 77% of the copy bandwidth at the 8192 x 4096 shape.)
 //
 // Backward (the norm's share of the backward pass, whose gradients cover every parameter):
-// rows of x and dz stream through a ring of shared-memory slots.  One producer warp issues bulk
-// copies (the TMA engine's contiguous form) of the CTA's rows into the ring as far ahead as
-// free slots allow, while a group of consumer warps works on rows already in shared memory;
-// each slot has a "full" mbarrier (completed by the copies' byte count) and an "empty" one
-// (completed by the warps that read it), and every wait on them is bounded.  The row is split
-// across the group's warps; the partial row sums of a few rows at a time meet in shared memory
-// at one named barrier.  dgamma and dbeta accumulate per thread in registers, are written as
-// one partial row per group and summed in a fixed order by a second kernel, so the result does
-// not depend on timing.
+// rows of x and dz stream through a ring of shared-memory slots, filled by bulk copies (the
+// TMA engine's contiguous form) as far ahead as the ring allows, while the CTA's warps work on
+// rows already in shared memory.  Each slot has a "full" mbarrier (completed by the copies'
+// byte count) and an "empty" one (completed by the warps that read it), and every wait on them
+// is bounded; there is no producer warp: the last warp to release a slot issues its refill.
+// The row is split across the warps; the partial row sums of a few rows at a time meet in
+// shared memory at one named barrier.  dgamma and dbeta accumulate per thread in registers, are
+// written as one partial row per CTA and summed in a fixed order by a second kernel, so the
+// result does not depend on timing.
 #include "cast.cuh"
 #include "common.cuh"
 #include "kernels.h"
@@ -32,12 +32,9 @@ namespace {
 constexpr size_t kRingSmemMax = 224 * 1024;  // dynamic shared memory per CTA
 constexpr int kFwdGroupWarps = 4;            // forward: warps per CTA (one row at a time)
 constexpr int kFwdRowsCtasPerSm = 8;         // forward: register budget, CTAs per SM
-constexpr int kBwdGroupWarps = 8;            // backward: warps per row
-constexpr int kBwdGroups = 1;                // backward: rows in progress per CTA
-constexpr int kBwdRowsPerSync = 2;           // backward: rows per barrier of a group
+constexpr int kBwdWarps = 8;                 // backward: warps per CTA, all sharing each row
+constexpr int kBwdRowsPerSync = 4;           // backward: rows per barrier (at most)
 constexpr int kBwdMaxSlots = 16;
-static_assert(kBwdGroupWarps == 1 || kBwdGroups <= 14,
-              "groups of several warps use named barriers 1 .. groups");
 
 // Barrier `id` among the `nthreads` threads of one group of consumer warps, returning whether
 // `pred` was true in any of them.
@@ -78,42 +75,15 @@ __device__ __forceinline__ void ring_init(uint64_t* full, uint64_t* empty, int s
   __syncthreads();
 }
 
-// Producer (one thread): for every local row k, in order, copies that row of src0 (and of
-// src1, when given, right behind it) into slot slot_of(k), after waiting for the slot's
-// previous use to be released.  Slot uses come in order: with `cons` consumer rings of `spc`
-// slots each, row k goes to ring k % cons, slot (k / cons) % spc of it.  Before returning it
-// waits for its last copies to land, so that none is in flight when the CTA exits.
-__device__ void ring_produce(const char* src0, const char* src1, uint32_t row_bytes,
-                             int64_t nloc, int cons, int spc, uint8_t* ring, uint64_t* full,
-                             uint64_t* empty, volatile int* abort_flag, int* status) {
-  const uint32_t slot_bytes = src1 ? 2 * row_bytes : row_bytes;
-  const int64_t stride = int64_t(gridDim.x) * row_bytes;
-  int64_t off = int64_t(blockIdx.x) * row_bytes;
-  int w = 0, jj = 0;
-  uint32_t use = 0;
-  int64_t k = 0;
-  for (; k < nloc; ++k, off += stride) {
-    const int s = w * spc + jj;
-    if (use > 0 && !wait_bounded(smem_u32(&empty[s]), (use - 1) & 1u, abort_flag, status,
-                                 kWaitLimitNs, true))
-      break;
-    const uint32_t dst = smem_u32(ring + size_t(s) * slot_bytes);
-    mbar_expect_tx(smem_u32(&full[s]), slot_bytes);
-    bulk_load(dst, src0 + off, row_bytes, smem_u32(&full[s]));
-    if (src1) bulk_load(dst + row_bytes, src1 + off, row_bytes, smem_u32(&full[s]));
-    if (++w == cons) {
-      w = 0;
-      if (++jj == spc) { jj = 0; ++use; }
-    }
-  }
-  // the last copy issued into each slot: rows k - cons * spc .. k - 1
-  const uint64_t limit = *abort_flag ? kDrainLimitNs : kWaitLimitNs;
-  const int64_t per_round = int64_t(cons) * spc;
-  for (int64_t j = k > per_round ? k - per_round : 0; j < k; ++j) {
-    const int64_t q = j / cons;
-    const int s = int(j % cons) * spc + int(q % spc);
-    wait_bounded(smem_u32(&full[s]), uint32_t(q / spc) & 1u, nullptr, status, limit, false);
-  }
+// Copies local row k of src0 and the same row of src1 (one behind the other) into slot s,
+// completing on the slot's full barrier.
+__device__ __forceinline__ void ring_issue(const char* src0, const char* src1, uint32_t row_bytes,
+                                           int64_t k, int s, uint8_t* ring, uint64_t* full) {
+  const int64_t off = (int64_t(blockIdx.x) + k * gridDim.x) * row_bytes;
+  const uint32_t dst = smem_u32(ring + size_t(s) * 2 * row_bytes);
+  mbar_expect_tx(smem_u32(&full[s]), 2 * row_bytes);
+  bulk_load(dst, src0 + off, row_bytes, smem_u32(&full[s]));
+  bulk_load(dst + row_bytes, src1 + off, row_bytes, smem_u32(&full[s]));
 }
 
 // A consumer warp's wait for use `use` of slot s: lane 0 waits (bounded) and the warp barrier
@@ -381,52 +351,54 @@ te_status launch_fwd_t(const NormFwdArgs& a, cudaStream_t s) {
 
 // ----------------------------------------------------------------------- backward --------
 
-// The consumer warps form groups of kBwdGroupWarps; group c takes local rows c, c + groups, ...
-// through its own ring of `spc` slots, kBwdRowsPerSync rows (consecutive slots of the ring) per
-// step.  Thread t of a group owns the 16-byte vectors t, t + 32 * kBwdGroupWarps, ... of each
-// row (NV of them), with its gamma vectors and dgamma / dbeta accumulators in registers; the
-// row sums of a step meet in shared memory at one barrier of the group, which also carries each
-// warp's "wait failed" flag so that the group's warps stop together.  A slot holds one row of x
-// followed by the same row of dz.  Each group writes one partial dgamma / dbeta row.
-// Rows per barrier step for NV vectors per thread (more rows per step hold more registers).
+// All kBwdWarps warps of a CTA share each of its rows: thread t owns the 16-byte vectors t,
+// t + 32 * kBwdWarps, ... of the row (NV of them), with its gamma vectors and dgamma / dbeta
+// accumulators in registers.  The CTA's rows (local rows 0, 1, ...) go round a ring of `spc`
+// slots, each holding one row of x followed by the same row of dz; RB consecutive rows form a
+// step, whose row sums meet in shared memory at one named barrier, which also carries each
+// warp's "wait failed" flag so that the warps stop together.  There is no producer warp: after
+// its first pass over a slot each warp arrives on the slot's empty barrier, and after the
+// step's barrier one warp waits for those (which acquires the others' reads) and issues the
+// bulk copies of the rows `spc` rows ahead into the slots.  With no ninth warp a thread may
+// hold up to 255 registers, enough to keep xhat and dz * g of the step's rows for the second
+// pass instead of reading and converting the slot again.
 __host__ __device__ constexpr int bwd_rows_per_sync(int nv) { return nv >= 4 ? 1 : kBwdRowsPerSync; }
 
 template <typename T, bool LN, int NV, bool FULL>
-__global__ void __launch_bounds__((kBwdGroups * kBwdGroupWarps + 1) * 32, 1)
+__global__ void __launch_bounds__(kBwdWarps * 32, 1)
     norm_bwd_ring_kernel(NormBwdArgs a, int* status, int spc) {
   using PR = Pairs<T>;
   constexpr int E = Vec16<T>::N;
   constexpr int P = PR::P;
-  constexpr int G = kBwdGroupWarps;
+  constexpr int G = kBwdWarps;
   constexpr int GT = G * 32;
   constexpr int RB = bwd_rows_per_sync(NV);
-  // xhat and dz * g of the step's rows stay in registers for pass 2 when few enough; otherwise
-  // pass 2 reads the slots again (and they are released after it)
-  constexpr bool KEEP = NV <= 2;
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ float2 red[kBwdGroups][2][RB][G];
-  const int groups = (int(blockDim.x >> 5) - 1) / G;  // the last warp produces
-  const int slots = groups * spc;
+  __shared__ float2 red[2][RB][G];
+  __shared__ int last_use[kBwdMaxSlots];  // the latest use issued into each slot
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
-  uint64_t* empty = full + slots;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + slots);
-  uint8_t* ring = smem + ring_header_bytes(slots);
+  uint64_t* empty = full + spc;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + spc);
+  uint8_t* ring = smem + ring_header_bytes(spc);
+  const char* xsrc = static_cast<const char*>(a.x);
+  const char* dzsrc = static_cast<const char*>(a.dz);
   const int nvec = int(a.H / E);
   const uint32_t row_bytes = uint32_t(a.H) * uint32_t(sizeof(T));
+  const uint32_t slot_bytes = 2 * row_bytes;
   const int64_t nloc = local_rows(a.M);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  ring_init(full, empty, slots, G, abort_flag);
-
-  if (warp == groups * G) {
-    if (lane == 0)
-      ring_produce(static_cast<const char*>(a.x), static_cast<const char*>(a.dz), row_bytes, nloc,
-                   groups, spc, ring, full, empty, abort_flag, status);
-    return;
+  if (threadIdx.x < spc) last_use[threadIdx.x] = -1;
+  ring_init(full, empty, spc, G, abort_flag);
+  if (threadIdx.x == 0) {  // the first use of every slot (the barriers' init is fenced)
+    for (int k = 0; k < spc && k < nloc; ++k) {
+      ring_issue(xsrc, dzsrc, row_bytes, k, k, ring, full);
+      last_use[k] = 0;
+    }
   }
 
   // FULL: every thread owns exactly NV vectors of every row (no bounds tests)
   auto mine = [&](int v) { return FULL || v < nvec; };
-  const int grp = warp / G, wg = warp % G, gt = wg * 32 + lane;
+  const int gt = threadIdx.x;
   const float inv_h = 1.0f / float(a.H);
   const f32x2 gshift = f2s(a.zero_centered_gamma ? 1.0f : 0.0f);
   f32x2 gp[NV][P], accg[NV][P], accb[NV][P];
@@ -443,42 +415,37 @@ __global__ void __launch_bounds__((kBwdGroups * kBwdGroupWarps + 1) * 32, 1)
       accb[i][p] = f2s(0.0f);
     }
   }
-  // The group's j-th row is local row grp + j * groups, i.e. global row
-  // blockIdx.x + (grp + j * groups) * gridDim.x: consecutive rows of the group are row_step apart.
-  const int64_t nmine = nloc > grp ? (nloc - grp + groups - 1) / groups : 0;
-  const int64_t row_step = int64_t(groups) * gridDim.x;
-  const int64_t row_first = int64_t(blockIdx.x) + int64_t(grp) * gridDim.x;
-  const uint32_t slot_bytes = 2 * row_bytes;
+  // local row k is global row blockIdx.x + k * gridDim.x
+  const int64_t row_step = gridDim.x;
   float mu_n[RB], rs_n[RB];
 #pragma unroll
   for (int j = 0; j < RB; ++j) {
-    const int64_t row = row_first + j * row_step;
-    mu_n[j] = (LN && j < nmine) ? a.mu[row] : 0.0f;
-    rs_n[j] = j < nmine ? a.rsigma[row] : 0.0f;
+    const int64_t row = blockIdx.x + j * row_step;
+    mu_n[j] = (LN && j < nloc) ? a.mu[row] : 0.0f;
+    rs_n[j] = j < nloc ? a.rsigma[row] : 0.0f;
   }
-  T* dx_first = static_cast<T*>(a.dx) + row_first * a.H + gt * E;
   const int64_t dx_step = row_step * a.H;
   int jj = 0;
   uint32_t use = 0;
-  int64_t row0 = row_first;
-  T* dx0 = dx_first;
-  for (int64_t j0 = 0, it = 0; j0 < nmine;
+  int64_t row0 = blockIdx.x;
+  T* dx0 = static_cast<T*>(a.dx) + row0 * a.H + gt * E;
+  bool ok = true;
+  for (int64_t j0 = 0, it = 0; j0 < nloc;
        j0 += RB, ++it, row0 += RB * row_step, dx0 += RB * dx_step) {
-    const int nr = nmine - j0 < RB ? int(nmine - j0) : RB;
+    const int nr = nloc - j0 < RB ? int(nloc - j0) : RB;
     f32x2 mu2[RB], rs2[RB];
 #pragma unroll
     for (int j = 0; j < RB; ++j) {
       mu2[j] = f2s(mu_n[j]);
       rs2[j] = f2s(rs_n[j]);
-      if (j0 + RB + j < nmine) {  // the next step's statistics load while this step runs
+      if (j0 + RB + j < nloc) {  // the next step's statistics load while this step runs
         const int64_t row = row0 + (RB + j) * row_step;
         mu_n[j] = LN ? a.mu[row] : 0.0f;
         rs_n[j] = a.rsigma[row];
       }
     }
-    const int s0 = grp * spc + jj;
+    const int s0 = jj;  // the step's rows are in slots s0 .. s0 + nr - 1 (spc is a multiple of RB)
     const uint8_t* slot0 = ring + uint32_t(s0) * slot_bytes;
-    bool ok = true;
 #pragma unroll
     for (int j = 0; j < RB; ++j)
       if (j < nr && ok) ok = ring_acquire(full, s0 + j, use, abort_flag, status);
@@ -486,17 +453,14 @@ __global__ void __launch_bounds__((kBwdGroups * kBwdGroupWarps + 1) * 32, 1)
     // sum(dz * g * xhat), and the column sums dgamma += dz * xhat, dbeta += dz (which do not
     // depend on the row sums); xhat and dz * g stay in registers for pass 2
     float t1[RB], t2[RB];
-    constexpr int KR = KEEP ? RB : 1, KV = KEEP ? NV : 1;
-    f32x2 xk[KR][KV][P], gk[KR][KV][P];
+    f32x2 xk[RB][NV][P], gk[RB][NV][P];
 #pragma unroll
     for (int j = 0; j < RB; ++j) {
       f32x2 s1 = f2s(0.0f), s2 = f2s(0.0f);
-      if constexpr (KEEP) {
 #pragma unroll
-        for (int i = 0; i < NV; ++i)
+      for (int i = 0; i < NV; ++i)
 #pragma unroll
-          for (int p = 0; p < P; ++p) { xk[j][i][p] = f2s(0.0f); gk[j][i][p] = f2s(0.0f); }
-      }
+        for (int p = 0; p < P; ++p) { xk[j][i][p] = f2s(0.0f); gk[j][i][p] = f2s(0.0f); }
       if (ok && j < nr) {
         const uint4* xs = reinterpret_cast<const uint4*>(slot0 + j * slot_bytes) + gt;
         const uint4* dzs = xs + nvec;
@@ -514,10 +478,8 @@ __global__ void __launch_bounds__((kBwdGroups * kBwdGroupWarps + 1) * 32, 1)
               s2 = fma2(dyg, xh, s2);
               accg[i][p] = fma2(dp[p], xh, accg[i][p]);
               if (LN) accb[i][p] = add2(accb[i][p], dp[p]);
-              if constexpr (KEEP) {
-                xk[j][i][p] = xh;
-                gk[j][i][p] = dyg;
-              }
+              xk[j][i][p] = xh;
+              gk[j][i][p] = dyg;
             }
           }
         }
@@ -525,14 +487,12 @@ __global__ void __launch_bounds__((kBwdGroups * kBwdGroupWarps + 1) * 32, 1)
       t1[j] = LN ? f2lo(s1) + f2hi(s1) : 0.0f;
       t2[j] = f2lo(s2) + f2hi(s2);
     }
-    if constexpr (KEEP) {
-      // the slots are no longer read: the producer may refill them while the sums meet
-      __syncwarp();
-      if (lane == 0 && ok) {
+    // the slots are no longer read
+    __syncwarp();
+    if (lane == 0 && ok) {
 #pragma unroll
-        for (int j = 0; j < RB; ++j)
-          if (j < nr) mbar_arrive(smem_u32(&empty[s0 + j]));
-      }
+      for (int j = 0; j < RB; ++j)
+        if (j < nr) mbar_arrive(smem_u32(&empty[s0 + j]));
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -545,54 +505,49 @@ __global__ void __launch_bounds__((kBwdGroups * kBwdGroupWarps + 1) * 32, 1)
     const int par = int(it & 1);
     if (lane == 0) {
 #pragma unroll
-      for (int j = 0; j < RB; ++j) red[grp][par][j][wg] = make_float2(t1[j], t2[j]);
+      for (int j = 0; j < RB; ++j) red[par][j][warp] = make_float2(t1[j], t2[j]);
     }
-    if (group_sync_or(!ok, 1 + grp, GT)) break;
-    // the group's warps add their sums in warp order (the same bits in every thread);
+    if (group_sync_or(!ok, 1, GT)) break;
+    // Every warp has released the step's slots before the barrier: each slot is refilled with
+    // the row spc ahead by one warp (a different one for each row, in turn), which waits on the
+    // slot's empty barrier to acquire the other warps' reads.  (A failed wait has raised the
+    // abort flag: the next acquire of every warp gives up.)
+#pragma unroll
+    for (int j = 0; j < RB; ++j) {
+      const int s = s0 + j;
+      const int64_t next = j0 + j + spc;
+      if (warp == int((it * RB + j) % G) && lane == 0 && j < nr && next < nloc &&
+          (mbar_try_wait(smem_u32(&empty[s]), use & 1u) ||
+           wait_bounded(smem_u32(&empty[s]), use & 1u, abort_flag, status, kWaitLimitNs, true))) {
+        ring_issue(xsrc, dzsrc, row_bytes, next, s, ring, full);
+        last_use[s] = int(use) + 1;
+      }
+    }
+    // the warps add their sums in warp order (the same bits in every thread);
     // dx = rs * (dz * g - mean(dz * g) - xhat * mean(dz * g * xhat))
     //    = (dz * g) * rs + c1 + xhat * c2,  c1 = -rs * mean(dz * g), c2 = -rs * mean(dz * g * xhat)
-    f32x2 c1[RB], c2[RB];
 #pragma unroll
     for (int j = 0; j < RB; ++j) {
       float r1 = 0.0f, r2 = 0.0f;
 #pragma unroll
       for (int w = 0; w < G; ++w) {
-        const float2 r = red[grp][par][j][w];
+        const float2 r = red[par][j][w];
         r1 += r.x;
         r2 += r.y;
       }
       const float rs = f2lo(rs2[j]);
-      c1[j] = f2s(LN ? -rs * (r1 * inv_h) : 0.0f);
-      c2[j] = f2s(-rs * (r2 * inv_h));
-    }
-    // pass 2, from registers (or from the slots again)
-#pragma unroll
-    for (int j = 0; j < RB; ++j) {
+      const f32x2 c1 = f2s(LN ? -rs * (r1 * inv_h) : 0.0f);
+      const f32x2 c2 = f2s(-rs * (r2 * inv_h));
+      // pass 2, from registers
       if (j < nr) {
         T* dxr = dx0 + j * dx_step;
-        const uint4* xs = reinterpret_cast<const uint4*>(slot0 + j * slot_bytes) + gt;
-        const uint4* dzs = xs + nvec;
 #pragma unroll
         for (int i = 0; i < NV; ++i) {
           if (mine(gt + i * GT)) {
-            f32x2 xh[P], dyg[P];
-            if constexpr (KEEP) {
-#pragma unroll
-              for (int p = 0; p < P; ++p) { xh[p] = xk[j][i][p]; dyg[p] = gk[j][i][p]; }
-            } else {
-              f32x2 xp[P], dp[P];
-              PR::cvt(xs[i * GT], xp);
-              PR::cvt(dzs[i * GT], dp);
-#pragma unroll
-              for (int p = 0; p < P; ++p) {
-                xh[p] = LN ? mul2(sub2(xp[p], mu2[j]), rs2[j]) : mul2(xp[p], rs2[j]);
-                dyg[p] = mul2(dp[p], gp[i][p]);
-              }
-            }
             float d[E];
 #pragma unroll
             for (int p = 0; p < P; ++p) {
-              const f32x2 dd = fma2(xh[p], c2[j], fma2(dyg[p], rs2[j], c1[j]));
+              const f32x2 dd = fma2(xk[j][i][p], c2, fma2(gk[j][i][p], rs2[j], c1));
               d[2 * p] = f2lo(dd);
               d[2 * p + 1] = f2hi(dd);
             }
@@ -601,18 +556,19 @@ __global__ void __launch_bounds__((kBwdGroups * kBwdGroupWarps + 1) * 32, 1)
         }
       }
     }
-    if constexpr (!KEEP) {
-      __syncwarp();
-      if (lane == 0) {
-#pragma unroll
-        for (int j = 0; j < RB; ++j)
-          if (j < nr) mbar_arrive(smem_u32(&empty[s0 + j]));
-      }
-    }
     jj += RB;
     if (jj == spc) { jj = 0; ++use; }
   }
-  float* pg = a.partials + (int64_t(blockIdx.x) * groups + grp) * 2 * a.H;
+  // After a failed wait, copies issued but never consumed may still be in flight: wait for
+  // them (briefly) before the CTA exits.  Without a failure every issued row was consumed.
+  __syncthreads();
+  if (threadIdx.x == 0 && *abort_flag) {
+    for (int s = 0; s < spc; ++s)
+      if (last_use[s] >= 0)
+        wait_bounded(smem_u32(&full[s]), uint32_t(last_use[s]) & 1u, nullptr, status,
+                     kDrainLimitNs, false);
+  }
+  float* pg = a.partials + int64_t(blockIdx.x) * 2 * a.H;
   float* pb = pg + a.H;
 #pragma unroll
   for (int i = 0; i < NV; ++i) {
@@ -631,22 +587,48 @@ __global__ void __launch_bounds__((kBwdGroups * kBwdGroupWarps + 1) * 32, 1)
   }
 }
 
-// dgamma[j] = sum_c partials[c][0][j], dbeta[j] = sum_c partials[c][1][j], in chunk order.
-__global__ void norm_bwd_reduce_kernel(const float* partials, int chunks, int64_t H,
-                                       float* dgamma, float* dbeta) {
-  const int64_t j = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (j >= H) return;
-  float sg = 0.0f, sb = 0.0f;
-  for (int c = 0; c < chunks; ++c) {
-    sg += partials[int64_t(c) * 2 * H + j];
-    sb += partials[int64_t(c) * 2 * H + H + j];
+// dgamma[j] = sum_c partials[c][0][j], dbeta[j] = sum_c partials[c][1][j].  A CTA takes 128
+// columns, 4 per thread of a warp (16-byte loads); its 16 warps take the chunks c = w, w + 16,
+// ... each in chunk order, and then the warps' sums are added in warp order: the same order for
+// every column and every run.  (One thread per column looping over all chunks made a chain of
+// about 150 dependent loads, longer than the ring kernel's own tail.)
+constexpr int kRedWarps = 16;
+__global__ void __launch_bounds__(kRedWarps * 32) norm_bwd_reduce_kernel(const float* partials,
+                                                                         int chunks, int64_t H,
+                                                                         float* dgamma,
+                                                                         float* dbeta) {
+  __shared__ float4 sg[kRedWarps][32], sb[kRedWarps][32];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int64_t j = int64_t(blockIdx.x) * 128 + lane * 4;  // H is a multiple of 8
+  float4 ag = make_float4(0.0f, 0.0f, 0.0f, 0.0f), ab = ag;
+  if (j < H) {
+#pragma unroll 4
+    for (int c = w; c < chunks; c += kRedWarps) {
+      const float* row = partials + int64_t(c) * 2 * H + j;
+      const float4 g = *reinterpret_cast<const float4*>(row);
+      const float4 b = *reinterpret_cast<const float4*>(row + H);
+      ag.x += g.x; ag.y += g.y; ag.z += g.z; ag.w += g.w;
+      ab.x += b.x; ab.y += b.y; ab.z += b.z; ab.w += b.w;
+    }
   }
-  dgamma[j] = sg;
-  if (dbeta) dbeta[j] = sb;
+  sg[w][lane] = ag;
+  sb[w][lane] = ab;
+  __syncthreads();
+  if (w == 0 && j < H) {
+    float4 tg = sg[0][lane], tb = sb[0][lane];
+#pragma unroll
+    for (int v = 1; v < kRedWarps; ++v) {
+      const float4 g = sg[v][lane], b = sb[v][lane];
+      tg.x += g.x; tg.y += g.y; tg.z += g.z; tg.w += g.w;
+      tb.x += b.x; tb.y += b.y; tb.z += b.z; tb.w += b.w;
+    }
+    dgamma[j] = tg.x; dgamma[j + 1] = tg.y; dgamma[j + 2] = tg.z; dgamma[j + 3] = tg.w;
+    if (dbeta) { dbeta[j] = tb.x; dbeta[j + 1] = tb.y; dbeta[j + 2] = tb.z; dbeta[j + 3] = tb.w; }
+  }
 }
 
-// Partial dgamma / dbeta rows: one per group of every CTA (groups = kBwdGroups at most).
-int bwd_chunks(int64_t M) { return int(ring_grid(M > 0 ? M : 1)) * kBwdGroups; }
+// Partial dgamma / dbeta rows: one per CTA.
+int bwd_chunks(int64_t M) { return int(ring_grid(M > 0 ? M : 1)); }
 
 template <typename T, bool LN, int NV, bool FULL>
 te_status launch_bwd_t(const NormBwdArgs& a, cudaStream_t s) {
@@ -654,22 +636,22 @@ te_status launch_bwd_t(const NormBwdArgs& a, cudaStream_t s) {
   constexpr int RB = bwd_rows_per_sync(NV);
   const size_t slot_bytes = size_t(a.H) * sizeof(T) * 2;
   int groups = 0, spc = 0;
-  if (!ring_shape(slot_bytes, 0, kBwdMaxSlots, kBwdGroups, 2 * RB, RB, &groups, &spc))
+  if (!ring_shape(slot_bytes, 0, kBwdMaxSlots, 1, 2 * RB, RB, &groups, &spc))
     return TE_ERR_UNSUPPORTED;
-  const size_t smem = ring_header_bytes(groups * spc) + size_t(groups * spc) * slot_bytes;
+  const size_t smem = ring_header_bytes(spc) + size_t(spc) * slot_bytes;
   const te_status st = allow_ring_smem(norm_bwd_ring_kernel<T, LN, NV, FULL>, attr_done);
   if (st != TE_OK) return st;
   const unsigned grid = ring_grid(a.M);
-  norm_bwd_ring_kernel<T, LN, NV, FULL><<<grid, (groups * kBwdGroupWarps + 1) * 32, smem, s>>>(
+  norm_bwd_ring_kernel<T, LN, NV, FULL><<<grid, kBwdWarps * 32, smem, s>>>(
       a, device_status_ptr(), spc);
-  norm_bwd_reduce_kernel<<<unsigned(ceil_div(a.H, 256)), 256, 0, s>>>(
-      a.partials, int(grid) * groups, a.H, a.dgamma, a.dbeta);
+  norm_bwd_reduce_kernel<<<unsigned(ceil_div(a.H, 128)), kRedWarps * 32, 0, s>>>(
+      a.partials, int(grid), a.H, a.dgamma, a.dbeta);
   return cudaGetLastError() == cudaSuccess ? TE_OK : TE_ERR_CUDA;
 }
 
 template <typename T, int NV>
 te_status launch_bwd_nv(const NormBwdArgs& a, cudaStream_t s) {
-  const bool full = a.H / Vec16<T>::N == int64_t(NV) * kBwdGroupWarps * 32;
+  const bool full = a.H / Vec16<T>::N == int64_t(NV) * kBwdWarps * 32;
   if (a.norm_type == TE_LAYERNORM)
     return full ? launch_bwd_t<T, true, NV, true>(a, s) : launch_bwd_t<T, true, NV, false>(a, s);
   return full ? launch_bwd_t<T, false, NV, true>(a, s) : launch_bwd_t<T, false, NV, false>(a, s);
@@ -679,8 +661,8 @@ template <typename T>
 te_status launch_bwd_dispatch(const NormBwdArgs& a, cudaStream_t s) {
   constexpr int E = Vec16<T>::N;
   // rows are at most 16 KB, i.e. 1024 vectors
-  constexpr int kMaxNV = (1024 + kBwdGroupWarps * 32 - 1) / (kBwdGroupWarps * 32);
-  const int64_t per_thread = ceil_div(a.H / E, kBwdGroupWarps * 32);
+  constexpr int kMaxNV = (1024 + kBwdWarps * 32 - 1) / (kBwdWarps * 32);
+  const int64_t per_thread = ceil_div(a.H / E, kBwdWarps * 32);
   if (per_thread <= 1) return launch_bwd_nv<T, 1>(a, s);
   if constexpr (kMaxNV >= 2) {
     if (per_thread <= 2) return launch_bwd_nv<T, 2>(a, s);
