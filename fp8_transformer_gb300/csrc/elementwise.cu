@@ -125,10 +125,13 @@ __global__ void __launch_bounds__(kActWarps * 32, 3) act_lu_kernel(ActArgs a) {
 
 constexpr int kDactWarps = 8;
 constexpr int kDactRows = 128;  // rows per CTA (chunk) = rows per dbias partial
-constexpr int kDactUnroll = 2;  // rows in flight per warp
+constexpr int kDactUnroll = 2;  // rows in flight per warp (twice that when only dy is read)
 
+// (three CTAs per SM; two for a gated pair, whose third input row per load would not fit the
+// register budget of three)
 template <typename T, int ACT>
-__global__ void __launch_bounds__(kDactWarps * 32, 3) dact_dbias_kernel(DactArgs a) {
+__global__ void __launch_bounds__(kDactWarps * 32, is_gated(ACT) ? 2 : 3)
+    dact_dbias_kernel(DactArgs a) {
   using PR = Pairs<T>;
   constexpr int E = Vec16<T>::N;
   constexpr int P = PR::P;
@@ -136,6 +139,9 @@ __global__ void __launch_bounds__(kDactWarps * 32, 3) dact_dbias_kernel(DactArgs
   constexpr bool kGated = is_gated(ACT);
   constexpr int kBase = gate_act(ACT);  // the function of the gate half
   constexpr bool kIdent = ACT == TE_IDENTITY;
+  // rows whose loads are in flight at once per warp: with the identity only dy is read, so
+  // twice as many rows keep as many bytes in flight
+  constexpr int U = kIdent ? 2 * kDactUnroll : kDactUnroll;
   __shared__ float red[kDactWarps][2][W];
   const CastState cs = cast_begin(a.cast);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -155,13 +161,13 @@ __global__ void __launch_bounds__(kDactWarps * 32, 3) dact_dbias_kernel(DactArgs
     with_out_amax(a.dx ? out_kind(cs) : int(OUT_NONE), want_amax, [&](auto tag, auto atag) {
       constexpr int OUT = decltype(tag)::value;
       constexpr bool AMAX = decltype(atag)::value;
-      for (int64_t rb = r0 + warp; rb < r1; rb += kDactUnroll * kDactWarps) {
-        // every load of kDactUnroll rows is issued before any of them is used
-        uint4 rdy[kDactUnroll], rx[kDactUnroll], rl[kDactUnroll];  // rx, rl unused by some types
+      for (int64_t rb = r0 + warp; rb < r1; rb += U * kDactWarps) {
+        // every load of U rows is issued before any of them is used
+        uint4 rdy[U], rx[U], rl[U];  // rx, rl unused by some types
         (void)rx;
         (void)rl;
 #pragma unroll
-        for (int j = 0; j < kDactUnroll; ++j) {
+        for (int j = 0; j < U; ++j) {
           const int64_t r = rb + int64_t(j) * kDactWarps;
           const bool in = r < r1;
           rdy[j] = in ? __ldg(reinterpret_cast<const uint4*>(static_cast<const T*>(a.dy) + r * n_out + col)) : zero;
@@ -171,7 +177,7 @@ __global__ void __launch_bounds__(kDactWarps * 32, 3) dact_dbias_kernel(DactArgs
             rl[j] = in ? __ldg(reinterpret_cast<const uint4*>(static_cast<const T*>(a.x) + r * a.N_in + n_out + col)) : zero;
         }
 #pragma unroll
-        for (int j = 0; j < kDactUnroll; ++j) {
+        for (int j = 0; j < U; ++j) {
           const int64_t r = rb + int64_t(j) * kDactWarps;
           if (r >= r1) break;
           f32x2 dyp[P], hp[P];
@@ -251,12 +257,36 @@ __global__ void __launch_bounds__(kDactWarps * 32, 3) dact_dbias_kernel(DactArgs
   block_amax_commit(amax, a.cast.amax_out);
 }
 
-__global__ void colsum_partials_kernel(const float* partials, int chunks, int64_t n, float* out) {
-  const int64_t j = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (j >= n) return;
-  float s = 0.0f;
-  for (int c = 0; c < chunks; ++c) s += partials[int64_t(c) * n + j];
-  out[j] = s;
+// out[j] = sum_c partials[c][j] (n a multiple of 4), summed in the same order for every column
+// and every run: a CTA takes 128 columns, 4 per thread of a warp (16-byte loads); its warps take
+// the chunks c = w, w + kColsumWarps, ... each in chunk order, and the warps' sums are then
+// added in warp order.  (One thread per column looping over every chunk was a chain of ~128
+// dependent loads.)
+constexpr int kColsumWarps = 16;
+__global__ void __launch_bounds__(kColsumWarps * 32)
+    colsum_partials_kernel(const float* partials, int chunks, int64_t n, float* out) {
+  __shared__ float4 sums[kColsumWarps][32];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int64_t j = int64_t(blockIdx.x) * 128 + lane * 4;
+  float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  if (j < n) {
+#pragma unroll 4
+    for (int c = w; c < chunks; c += kColsumWarps) {
+      const float4 v = __ldg(reinterpret_cast<const float4*>(partials + int64_t(c) * n + j));
+      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+    }
+  }
+  sums[w][lane] = acc;
+  __syncthreads();
+  if (w == 0 && j < n) {
+    float4 t = sums[0][lane];
+#pragma unroll
+    for (int v = 1; v < kColsumWarps; ++v) {
+      const float4 u = sums[v][lane];
+      t.x += u.x; t.y += u.y; t.z += u.z; t.w += u.w;
+    }
+    out[j] = t.x; out[j + 1] = t.y; out[j + 2] = t.z; out[j + 3] = t.w;
+  }
 }
 
 // ------------------------------------------------------------------ transpose -------------
@@ -335,8 +365,8 @@ te_status launch_dact_dbias(const DactArgs& a, cudaStream_t s) {
                  : a.dtype == TE_F32 ? launch_dact_t<float>(a, grid, s)
                                      : TE_ERR_UNSUPPORTED;
   if (st != TE_OK || !a.dbias) return st;
-  colsum_partials_kernel<<<unsigned(ceil_div(a.N_in, 256)), 256, 0, s>>>(a.partials, chunks,
-                                                                         a.N_in, a.dbias);
+  colsum_partials_kernel<<<unsigned(ceil_div(a.N_in, 128)), kColsumWarps * 32, 0, s>>>(
+      a.partials, chunks, a.N_in, a.dbias);
   return cudaGetLastError() == cudaSuccess ? TE_OK : TE_ERR_CUDA;
 }
 
