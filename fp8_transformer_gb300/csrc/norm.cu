@@ -1,11 +1,12 @@
 // Row normalization kernels (LayerNorm / RMSNorm forward and backward).
 //
 // Forward (TransformerEngine JAX "LayerNorm MLP" page, Description step (1); "LayerNorm Dense"
-// page, Description): a CTA of a few warps normalizes one row at a time, persistent over rows
-// with a stride of the grid, with eight CTAs per SM.  Each thread loads its 16-byte vectors of
-// the row straight into registers and loads the next row's while it normalizes the current
-// one; the warps' row sums meet in shared memory at one barrier per row.  Statistics are fp32,
-// and the normalized row is written once, directly in the consumer GEMM's operand dtype (fp32,
+// page, Description): rows of 4, 8 or 16 16-byte vectors per lane of a warp (H = 1024, 2048 or
+// 4096 in bf16) take one row per warp, whose sums meet by shuffles alone; other widths take a
+// CTA of a few warps per row, persistent over rows with a stride of the grid, eight CTAs per
+// SM, each thread loading the next row's vectors while it normalizes the current one, the
+// warps' row sums meeting in shared memory at one barrier per row.  Statistics are fp32, and
+// the normalized row is written once, directly in the consumer GEMM's operand dtype (fp32,
 // bf16 or E4M3), together with the per-tensor amax.  (Staging rows through shared memory with
 // bulk copies, as the backward does, measured slower here: even with no arithmetic at all that
 // path reached about 77% of the copy bandwidth at the 8192 x 4096 shape.)
@@ -265,6 +266,139 @@ __global__ void __launch_bounds__(kFwdGroupWarps * 32, NVL >= 8 ? kFwdRowsCtasPe
   if (lane == 0 && a.cast.amax_out) atomic_max_nonneg(a.cast.amax_out, amax);
 }
 
+// Forward with one row per warp, for rows of exactly NVW x 32 vectors: the row's sums meet by
+// shuffles within the warp, with no barrier between warps; the CTA's kFwdWarpRowWarps warps
+// share the gain / beta table in shared memory (the layout above).  Each lane holds its NVW
+// vectors of one row at a time; the many warps per SM keep rows in flight.
+constexpr int kFwdWarpRowWarps = 4;
+template <typename T, bool LN, int NVW>
+__global__ void __launch_bounds__(kFwdWarpRowWarps * 32, NVW * Vec16<T>::N >= 128 ? 3 : 4)
+    norm_fwd_warp_kernel(NormFwdArgs a) {
+  using PR = Pairs<T>;
+  constexpr int E = Vec16<T>::N;
+  constexpr int P = PR::P;
+  constexpr int Q = E / 4;
+  constexpr int nvec = NVW * 32;
+  extern __shared__ __align__(16) float4 prm[];
+  float4* gain4 = prm;
+  float4* beta4 = prm + Q * nvec;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  {
+    const float shift = a.zero_centered_gamma ? 1.0f : 0.0f;
+    const T* g = static_cast<const T*>(a.gamma);
+    const T* b = static_cast<const T*>(a.beta);
+    float* gf = reinterpret_cast<float*>(gain4);
+    float* bf = reinterpret_cast<float*>(beta4);
+    for (int64_t j = tid; j < a.H; j += blockDim.x) {
+      const int64_t v = j / E, e = j % E;
+      const int64_t slot = ((e / 4) * nvec + v) * 4 + (e % 4);
+      gf[slot] = float(g[j]) + shift;
+      if (LN) bf[slot] = b ? float(b[j]) : 0.0f;
+    }
+  }
+  __syncthreads();  // gain / beta ready
+  const T* x = static_cast<const T*>(a.x);
+  const CastState cs = cast_begin(a.cast);
+  const float inv_h = 1.0f / float(a.H);
+  const bool want_amax = a.cast.amax_out != nullptr;
+  float am[P];
+#pragma unroll
+  for (int p = 0; p < P; ++p) am[p] = 0.0f;
+  with_out_amax(out_kind(cs), want_amax, [&](auto tag, auto atag) {
+    constexpr int OUT = decltype(tag)::value;
+    constexpr bool AMAX = decltype(atag)::value;
+    const int64_t step = int64_t(gridDim.x) * kFwdWarpRowWarps;
+    for (int64_t r = int64_t(blockIdx.x) * kFwdWarpRowWarps + warp; r < a.M; r += step) {
+      const uint4* xr = reinterpret_cast<const uint4*>(x + r * a.H) + lane;
+      uint4 cur[NVW];
+#pragma unroll
+      for (int i = 0; i < NVW; ++i) cur[i] = __ldg(xr + 32 * i);
+      // the row's first element, subtracted before the sums (shifted variance), from lane 0
+      float x0 = 0.0f;
+      if (LN) {
+        f32x2 first[P];
+        PR::cvt(cur[0], first);
+        x0 = __shfl_sync(0xffffffffu, f2lo(first[0]), 0);
+      }
+      const f32x2 x02 = f2s(x0);
+      f32x2 s1[P], s2[P];
+#pragma unroll
+      for (int p = 0; p < P; ++p) { s1[p] = f2s(0.0f); s2[p] = f2s(0.0f); }
+#pragma unroll
+      for (int i = 0; i < NVW; ++i) {
+        f32x2 xp[P];
+        PR::cvt(cur[i], xp);
+#pragma unroll
+        for (int p = 0; p < P; ++p) {
+          if (LN) {
+            const f32x2 d = sub2(xp[p], x02);
+            s1[p] = add2(s1[p], d);
+            s2[p] = fma2(d, d, s2[p]);
+          } else {
+            s2[p] = fma2(xp[p], xp[p], s2[p]);
+          }
+        }
+      }
+#pragma unroll
+      for (int p = 1; p < P; ++p) { s1[0] = add2(s1[0], s1[p]); s2[0] = add2(s2[0], s2[p]); }
+      float t1 = LN ? f2lo(s1[0]) + f2hi(s1[0]) : 0.0f;
+      float t2 = f2lo(s2[0]) + f2hi(s2[0]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        if (LN) t1 += __shfl_xor_sync(0xffffffffu, t1, o);
+        t2 += __shfl_xor_sync(0xffffffffu, t2, o);
+      }
+      const float m1 = LN ? t1 * inv_h : 0.0f;
+      const float m2 = t2 * inv_h;
+      const float mean = LN ? x0 + m1 : 0.0f;
+      const float var = LN ? fmaxf(m2 - m1 * m1, 0.0f) : m2;
+      const float rs = rsqrtf(var + a.eps);
+      if (lane == 0) {
+        if (a.mu) a.mu[r] = mean;
+        if (a.rsigma) a.rsigma[r] = rs;
+      }
+      if (OUT != OUT_NONE || AMAX) {
+        const f32x2 mean2 = f2s(mean), rs2 = f2s(rs);
+        const int64_t base = r * a.H + int64_t(lane) * E;
+#pragma unroll
+        for (int i = 0; i < NVW; ++i) {
+          const int v = lane + 32 * i;
+          f32x2 xp[P], gp[P], bp[P];
+          PR::get(cur[i], xp);  // converted again here rather than kept from the sums
+#pragma unroll
+          for (int q = 0; q < Q; ++q) {
+            const float4 g4 = gain4[q * nvec + v];
+            gp[2 * q] = f2(g4.x, g4.y);
+            gp[2 * q + 1] = f2(g4.z, g4.w);
+            if (LN) {
+              const float4 b4 = beta4[q * nvec + v];
+              bp[2 * q] = f2(b4.x, b4.y);
+              bp[2 * q + 1] = f2(b4.z, b4.w);
+            }
+          }
+          float y[E];
+#pragma unroll
+          for (int p = 0; p < P; ++p) {
+            const f32x2 yy = LN ? fma2(sub2(xp[p], mean2), mul2(gp[p], rs2), bp[p])
+                                : mul2(mul2(xp[p], rs2), gp[p]);
+            if (AMAX) am[p] = absmax2(am[p], yy);
+            y[2 * p] = f2lo(yy);
+            y[2 * p + 1] = f2hi(yy);
+          }
+          store_out<OUT, E>(a.out, base + int64_t(32) * E * i, y, cs);
+          // one vector's gain / beta loads at a time: hoisting all of them spills
+          asm volatile("" ::: "memory");
+        }
+      }
+    }
+  });
+  float amax = am[0];
+#pragma unroll
+  for (int p = 1; p < P; ++p) amax = fmaxf(amax, am[p]);
+  amax = warp_max(amax);
+  if (lane == 0 && a.cast.amax_out) atomic_max_nonneg(a.cast.amax_out, amax);
+}
+
 // Sets the kernel's dynamic shared memory limit once per device.
 template <typename K>
 te_status allow_ring_smem(K kernel, bool (&done)[64]) {
@@ -319,6 +453,30 @@ te_status launch_fwd_rows(const NormFwdArgs& a, cudaStream_t s) {
   return cudaGetLastError() == cudaSuccess ? TE_OK : TE_ERR_CUDA;
 }
 
+template <typename T, bool LN, int NVW>
+te_status launch_fwd_warp(const NormFwdArgs& a, cudaStream_t s) {
+  static bool attr_done[64] = {};
+  const size_t params = size_t(a.H) * (LN ? 2 : 1) * sizeof(float);
+  const te_status st = allow_ring_smem(norm_fwd_warp_kernel<T, LN, NVW>, attr_done);
+  if (st != TE_OK) return st;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, norm_fwd_warp_kernel<T, LN, NVW>,
+                                                    kFwdWarpRowWarps * 32, params) != cudaSuccess ||
+      per_sm < 1)
+    per_sm = 1;
+  const int64_t cap = int64_t(num_sms()) * per_sm;
+  const int64_t ctas = ceil_div(a.M, kFwdWarpRowWarps);
+  const unsigned grid = unsigned(ctas < cap ? ctas : cap);
+  norm_fwd_warp_kernel<T, LN, NVW><<<grid, kFwdWarpRowWarps * 32, params, s>>>(a);
+  return cudaGetLastError() == cudaSuccess ? TE_OK : TE_ERR_CUDA;
+}
+
+template <typename T, int NVW>
+te_status launch_fwd_nvw(const NormFwdArgs& a, cudaStream_t s) {
+  return a.norm_type == TE_LAYERNORM ? launch_fwd_warp<T, true, NVW>(a, s)
+                                     : launch_fwd_warp<T, false, NVW>(a, s);
+}
+
 template <typename T, int NVL>
 te_status launch_fwd_nvl(const NormFwdArgs& a, cudaStream_t s) {
   // (the bounds-tested form throughout: without the tests the compiler holds more of the two
@@ -333,6 +491,13 @@ te_status launch_fwd_t(const NormFwdArgs& a, cudaStream_t s) {
   constexpr int GT = kFwdGroupWarps * 32;
   // rows are at most 16 KB, i.e. 1024 vectors
   constexpr int kMaxNVL = (1024 + GT - 1) / GT;
+  // rows of 4, 8 or 16 vectors per lane of one warp: one row per warp
+  const int64_t nvec = a.H / E;
+  if (nvec % 32 == 0) {
+    if (nvec == 4 * 32) return launch_fwd_nvw<T, 4>(a, s);
+    if (nvec == 8 * 32) return launch_fwd_nvw<T, 8>(a, s);
+    if (nvec == 16 * 32) return launch_fwd_nvw<T, 16>(a, s);
+  }
   const int64_t per_thread = ceil_div(a.H / E, GT);
   if (per_thread <= 1) return launch_fwd_nvl<T, 1>(a, s);
   if (per_thread <= 2) return launch_fwd_nvl<T, 2>(a, s);
