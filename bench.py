@@ -283,7 +283,9 @@ def bandwidth_kernels(args, dev, peaks):
     res = {}
 
     def run(name, fn, nbytes):
-        fn()
+        for _ in range(max(1, args.warmup)):
+            flush()
+            fn()
         ms = statistics.mean(time_steps(fn, args.steps, flush))
         gbs = nbytes / (ms / 1e3) / 1e9
         res[name] = {"GB/s": gbs, "frac": gbs / peaks["hbm"], "ms": ms, "bytes": nbytes}
