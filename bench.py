@@ -555,6 +555,24 @@ def run_ours(args, rank, world, local_rank):
     dact_step()
     ms_dact = max_over_ranks(statistics.mean(time_steps(dact_step, args.steps, flush)))
     del dyd, hd, dxd, wsd
+    # the norm backward at the GPT workload's shape (LayerNorm, 16384 x 4096)
+    Mn, Hn = 16384, 4096
+    xn = torch.randn(Mn, Hn, device=dev, dtype=torch.bfloat16)
+    dzn = torch.randn(Mn, Hn, device=dev, dtype=torch.bfloat16)
+    mun = torch.zeros(Mn, device=dev, dtype=torch.float32)
+    rsn = torch.ones(Mn, device=dev, dtype=torch.float32)
+    gn = torch.ones(Hn, device=dev, dtype=torch.bfloat16)
+    dxn = torch.empty(Mn, Hn, device=dev, dtype=torch.bfloat16)
+    dgn = torch.empty(Hn, device=dev, dtype=torch.float32)
+    dbn = torch.empty(Hn, device=dev, dtype=torch.float32)
+    wsn = torch.empty(te.workspace_size(te.binding.TE_OP_NORM_BWD, Mn, Hn, 0), dtype=torch.uint8,
+                      device=dev)
+    nbwd_step = lambda: te.te_norm_bwd(dzn, xn, mun, rsn, gn, "layernorm", False, dxn, dgn,
+                                       dbeta=dbn, workspace=wsn)
+    nbwd_bytes = Mn * Hn * (2 + 2 + 2) + Mn * 8
+    nbwd_step()
+    ms_nbwd = max_over_ranks(statistics.mean(time_steps(nbwd_step, args.steps, flush)))
+    del xn, dzn, dxn, wsn
     barrier()
 
     # ---- the other workloads' hot paths: LN -> Dense (QKV) forward and backward, and the GPT
@@ -696,6 +714,9 @@ def run_ours(args, rank, world, local_rank):
             "norm_fwd": {"shape": [M, H], "GB/s": norm_bytes / (ms_norm / 1e3) / 1e9,
                          "frac": norm_bytes / (ms_norm / 1e3) / 1e9 / peaks["hbm"],
                          "ms": ms_norm, "bytes": norm_bytes},
+            "norm_bwd": {"shape": [Mn, Hn], "GB/s": nbwd_bytes / (ms_nbwd / 1e3) / 1e9,
+                         "frac": nbwd_bytes / (ms_nbwd / 1e3) / 1e9 / peaks["hbm"],
+                         "ms": ms_nbwd, "bytes": nbwd_bytes},
             "dact_dbias_quantize": {"shape": [Md, Nd], "GB/s": dact_bytes / (ms_dact / 1e3) / 1e9,
                                     "frac": dact_bytes / (ms_dact / 1e3) / 1e9 / peaks["hbm"],
                                     "ms": ms_dact, "bytes": dact_bytes}},

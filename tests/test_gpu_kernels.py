@@ -153,9 +153,12 @@ def test_dbias_deterministic():
 @pytest.mark.parametrize("norm", ["layernorm", "rmsnorm"])
 @pytest.mark.parametrize("M,H,dtype", [(1, 128, "f32"), (129, 136, "bf16"), (1000, 4096, "bf16"),
                                        (70, 8192, "bf16"), (64, 128, "f32"), (70, 4096, "f32"),
-                                       (9000, 1024, "bf16")])
+                                       (9000, 1024, "bf16"), (301, 2048, "bf16"),
+                                       (257, 2048, "f32"), (33, 512, "f32")])
 @pytest.mark.parametrize("zc", [False, True])
 def test_norm_fwd(norm, M, H, dtype, zc):
+    """Widths of 4, 8 or 16 vectors per lane of a warp (1024 / 2048 / 4096 bf16, 512 / 1024 /
+    2048 fp32) take one row per warp; the others a CTA of four warps per row."""
     x = rt((M, H), std=2.0, seed=11, dtype=dtype, mean=0.5)
     gamma = rt((H,), std=0.1, seed=12, dtype=dtype, mean=0.0 if zc else 1.0)
     beta = rt((H,), std=0.1, seed=13, dtype=dtype)
