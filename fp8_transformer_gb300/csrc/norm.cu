@@ -418,22 +418,14 @@ unsigned ring_grid(int64_t M) {
   return unsigned(M < sms ? M : sms);
 }
 
-// Ring geometry for `slot_bytes`-byte slots after `fixed` bytes of other shared data: as many
-// slots as fit (at most max_slots), shared out as rings of at least `min_spc` slots (a multiple
-// of `mult`) among at most `max_groups` groups.  Returns false if not even one ring fits.
-bool ring_shape(size_t slot_bytes, size_t fixed, int max_slots, int max_groups, int min_spc,
-                int mult, int* groups, int* spc) {
+// Ring size for `slot_bytes`-byte slots: as many as fit the shared memory (at most
+// max_slots), rounded down to a multiple of `mult`; 0 if fewer than `min_slots` fit.
+int ring_slots(size_t slot_bytes, int max_slots, int min_slots, int mult) {
   int slots = max_slots;
-  while (slots > 0 && ring_header_bytes(slots) + fixed + size_t(slots) * slot_bytes > kRingSmemMax)
+  while (slots > 0 && ring_header_bytes(slots) + size_t(slots) * slot_bytes > kRingSmemMax)
     --slots;
-  int g = slots / min_spc < max_groups ? slots / min_spc : max_groups;
-  if (g < 1) return false;
-  int per = slots / g;
-  per -= per % mult;
-  if (per < mult) return false;
-  *groups = g;
-  *spc = per;
-  return true;
+  slots -= slots % mult;
+  return slots >= min_slots ? slots : 0;
 }
 
 template <typename T, bool LN, int NVL, bool FULL>
@@ -800,9 +792,9 @@ te_status launch_bwd_t(const NormBwdArgs& a, cudaStream_t s) {
   static bool attr_done[64] = {};
   constexpr int RB = bwd_rows_per_sync(NV);
   const size_t slot_bytes = size_t(a.H) * sizeof(T) * 2;
-  int groups = 0, spc = 0;
-  if (!ring_shape(slot_bytes, 0, kBwdMaxSlots, 1, 2 * RB, RB, &groups, &spc))
-    return TE_ERR_UNSUPPORTED;
+  // a step holds RB slots; a second step's worth lets the refills run ahead
+  const int spc = ring_slots(slot_bytes, kBwdMaxSlots, 2 * RB, RB);
+  if (spc == 0) return TE_ERR_UNSUPPORTED;
   const size_t smem = ring_header_bytes(spc) + size_t(spc) * slot_bytes;
   const te_status st = allow_ring_smem(norm_bwd_ring_kernel<T, LN, NV, FULL>, attr_done);
   if (st != TE_OK) return st;
