@@ -237,6 +237,27 @@ def test_norm_bwd(norm, M, H, dtype):
         assert_reduction_close(db, rdb, what="dbeta")
 
 
+def test_norm_bwd_large_mean():
+    """LayerNorm rows whose mean is 64 standard deviations from zero: the kernel forms xhat as
+    x * rs - mu * rs, so the rounding of mu * rs must stay below the tolerances."""
+    M, H = 600, 4096
+    x = rt((M, H), std=1.0, seed=23, mean=64.0)
+    gamma = rt((H,), 0.1, 24, mean=1.0)
+    dz = rt((M, H), seed=25)
+    _, mu, rs = ob.norm_fwd(np64(x), np64(gamma), np.zeros(H), "layernorm", False, 1e-5)
+    mu_t = torch.tensor(mu, dtype=torch.float32, device=DEV)
+    rs_t = torch.tensor(rs, dtype=torch.float32, device=DEV)
+    dx = torch.empty(M, H, dtype=torch.bfloat16, device=DEV)
+    dg = torch.empty(H, dtype=torch.float32, device=DEV)
+    db = torch.empty(H, dtype=torch.float32, device=DEV)
+    te.te_norm_bwd(dz, x, mu_t, rs_t, gamma, "layernorm", False, dx, dg, db)
+    rdx, rdg, rdb = ob.norm_bwd(np64(dz), np64(x), np64(mu_t), np64(rs_t), np64(gamma),
+                                "layernorm", False)
+    assert_elementwise_close(dx, nx.bf16_round(nx.to_f32(rdx)), what="dx", abs_rms=2e-3)
+    assert_reduction_close(dg, rdg, what="dgamma")
+    assert_reduction_close(db, rdb, what="dbeta")
+
+
 # ------------------------------------------------------------------ GEMM -------------------
 
 
