@@ -72,3 +72,36 @@ def test_selftest_limit_checked_on_the_host():
     b = te.binding
     for bad in (0, -5, 1000001):
         assert lib.te_selftest_wait_timeout(bad, None) == b.TE_ERR_INVALID_ARG
+
+
+def test_backward_and_host_forward_arguments_checked_on_the_host():
+    """The whole-block entry points refuse bad arguments before any CUDA call (fake, aligned,
+    never dereferenced addresses stand in for device buffers)."""
+    lib = te.lib()
+    b = te.binding
+    P = 4096  # a 16-byte aligned stand-in address; nothing reads it
+
+    def mlp_bwd(dtype=b.TE_BF16, act=b.TE_GELU, H=512, F=784, gamma=P):
+        return lib.te_layernorm_mlp_bwd(P, P, gamma, P, P, dtype, P, P, P, P, b.TE_LAYERNORM, 0,
+                                        act, None, 64, H, F, dtype, P, P, P, P, P, P, P, P,
+                                        1 << 20, None)
+    assert mlp_bwd(dtype=b.TE_F32) == b.TE_ERR_UNSUPPORTED       # bf16 only
+    assert mlp_bwd(act=b.TE_IDENTITY) == b.TE_ERR_INVALID_ARG    # the MLP needs an activation
+    assert mlp_bwd(gamma=None) == b.TE_ERR_INVALID_ARG
+    assert mlp_bwd(H=520) == b.TE_ERR_UNSUPPORTED                # H not a multiple of 16
+
+    def dense_bwd(dtype=b.TE_BF16, N=784, gamma=P):
+        return lib.te_layernorm_dense_bwd(P, P, gamma, P, dtype, P, P, P, b.TE_LAYERNORM, 0, None,
+                                          64, 512, N, dtype, P, P, P, P, P, P, 1 << 20, None)
+    assert dense_bwd(dtype=b.TE_F32) == b.TE_ERR_UNSUPPORTED
+    assert dense_bwd(gamma=None) == b.TE_ERR_INVALID_ARG
+    assert dense_bwd(N=792) == b.TE_ERR_UNSUPPORTED              # N not a multiple of 16
+
+    def host_fwd(M=64, chunks=4, dtype=b.TE_BF16):
+        return lib.te_layernorm_mlp_fwd_host(P, P, P, P, P, None, None, b.TE_RMSNORM, 1, 1e-6,
+                                             b.TE_SWIGLU, M, 512, 784, dtype, P, chunks, P,
+                                             1 << 20, None)
+    assert host_fwd(chunks=0) == b.TE_ERR_INVALID_ARG
+    assert host_fwd(chunks=17) == b.TE_ERR_INVALID_ARG           # at most 16 row slices
+    assert host_fwd(dtype=b.TE_E4M3) == b.TE_ERR_INVALID_ARG     # activations bf16 or fp32
+    assert host_fwd(M=0) == b.TE_OK                              # no rows: nothing to do
