@@ -25,12 +25,14 @@ def test_whole_job_rate_uses_every_rank_and_the_slowest_time():
 
 
 def test_peaks_measured_file_and_fallback(tmp_path, monkeypatch):
+    # a peaks file as the pod writes it is read as is
+    (tmp_path / "MEASURED_PEAKS.json").write_text(json.dumps(
+        {"hbm_gbs": 6671.5, "bf16_tflops": 1941.1, "bf16_tflops_sustained": 1730.3}))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     p = bench.load_peaks()
-    with open(os.path.join(bench.ROOT, "MEASURED_PEAKS.json")) as f:
-        raw = json.load(f)
-    assert p["source"] == "measured"
-    assert p["hbm"] == float(raw["hbm_gbs"]) and p["bf16"] == float(raw["bf16_tflops"])
-    monkeypatch.setattr(bench, "ROOT", str(tmp_path))  # no peaks file there
+    assert p == dict(hbm=6671.5, bf16=1941.1, bf16_sustained=1730.3, source="measured")
+    # without one, the fallback figures
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path / "empty"))
     q = bench.load_peaks()
     assert q["source"] == "fallback" and q["hbm"] == 6800.0 and q["bf16"] == 1900.0
 
