@@ -384,3 +384,68 @@ def test_fp8_dense_bwd_matches_torch_float8_composition():
     np.testing.assert_array_equal(res["dln"].value, bf(qdy @ qk.T * a1))
     np.testing.assert_array_equal(res["dkernel"].value, bf(qx.T @ qdy * a2))
     np.testing.assert_allclose(res["dbias"], dy.sum(axis=0), rtol=1e-12)
+
+
+@pytest.mark.parametrize("act", ["gelu", "swiglu"])
+def test_fp8_mlp_bwd_matches_torch_float8_composition(act):
+    """The FP8 branch of the MLP backward rebuilt from torch: float8_e4m3fn conversion for the
+    quantized operands, autograd through torch's tanh-form gelu / silu for the activation
+    gradient and through torch's layer_norm for the norm backward, fp64 matmul for the GEMMs,
+    all with fixed scales.  It fixes which tensor each step reads: dbias1 sums the unquantized
+    fp32 dH; dH is cast with the grad scale alone; dln = q(dH) q(W1)^T and dW1 = q(ln)^T q(dH),
+    each scaled by the product of its two operands' dequantization factors; dW2 and da use the
+    bf16 recomputed activation, dy and bf16 W2."""
+    r = rng(33)
+    M, H, Fd = 16, 32, 24
+    gated = ob.GATED[act]
+    F1 = 2 * Fd if gated else Fd
+    x = r.normal(size=(M, H)).astype(np.float32).astype(np.float64)
+    g = 1 + 0.1 * r.normal(size=H)
+    b = 0.1 * r.normal(size=H)
+    w1 = nx.bf16_round(0.05 * r.normal(size=(H, F1)))
+    w2 = nx.bf16_round(0.05 * r.normal(size=(Fd, H)))
+    b1 = nx.bf16_round(0.02 * r.normal(size=F1))
+    dy = nx.bf16_round(r.normal(size=(M, H)))
+    s = dict(x=np.float32(32.0), w1=np.float32(2048.0), act=np.float32(16.0),
+             w2=np.float32(2048.0), grad=np.float32(256.0))
+    res = ob.layernorm_mlp_bwd(dy, x, g, b, w1, w2, b1, None, "layernorm", False, 1e-6, act,
+                               "bf16", fp8=s)
+    bf = lambda v: torch.tensor(v, dtype=torch.float32).to(torch.bfloat16).double().numpy()
+    inv = lambda k: float(np.float32(1) / s[k])
+    # forward operands: E4M3 normalized output and W1, bf16 GEMM1 output
+    xt = torch.tensor(x, requires_grad=True)
+    gt = torch.tensor(g, requires_grad=True)
+    bt = torch.tensor(b, requires_grad=True)
+    y = F.layer_norm(xt, (H,), gt, bt, eps=1e-6)
+    qx = _torch_fake_quant(nx.to_f32(y.detach().numpy()), s["x"])
+    qw1 = _torch_fake_quant(w1, s["w1"])
+    h = bf(qx @ qw1 * float(np.float32(inv("x")) * np.float32(inv("w1"))) + b1)
+    np.testing.assert_array_equal(res["fwd"]["h"].value, h)
+
+    def act_t(ht):
+        if not gated:
+            return F.gelu(ht, approximate="tanh")
+        return F.silu(ht[:, :Fd]) * ht[:, Fd:]
+
+    ht = torch.tensor(h, requires_grad=True)
+    a = act_t(ht)
+    a_re = bf(a.detach().numpy())
+    np.testing.assert_array_equal(res["a_re"].value, a_re)
+    np.testing.assert_array_equal(res["dW2"].value, bf(a_re.T @ dy))
+    da = bf(dy @ w2.T)
+    np.testing.assert_array_equal(res["da"].value, da)
+    a.backward(torch.tensor(da))
+    dh32 = nx.to_f32(ht.grad.numpy())
+    np.testing.assert_allclose(res["db1"], dh32.sum(axis=0), rtol=1e-12, atol=1e-12)
+    qdh = _torch_fake_quant(dh32, s["grad"])
+    np.testing.assert_array_equal(res["dh"].value, qdh)
+    assert res["dh"].scale == s["grad"]
+    dln = bf(qdh @ qw1.T * float(np.float32(inv("grad")) * np.float32(inv("w1"))))
+    np.testing.assert_array_equal(res["dln"].value, dln)
+    dw1 = bf(qx.T @ qdh * float(np.float32(inv("x")) * np.float32(inv("grad"))))
+    np.testing.assert_array_equal(res["dW1"].value, dw1)
+    y.backward(torch.tensor(dln))
+    np.testing.assert_allclose(res["dx"].value, bf(xt.grad.numpy()), rtol=2.0 ** -8, atol=1e-12)
+    np.testing.assert_allclose(res["dgamma"], gt.grad.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(res["dbeta"], bt.grad.numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(res["db2"], dy.sum(axis=0), rtol=1e-12)
