@@ -313,74 +313,107 @@ def layernorm_mlp_fwd(x, gamma, beta, w1, w2, b1, b2, norm_type="layernorm",
 def layernorm_mlp_bwd(dy, x, gamma, beta, w1, w2, b1, b2, norm_type="layernorm",
                       zero_centered_gamma=False, eps=1e-6, act="gelu", dtype="bf16",
                       fp8=None):
-    """Backward of ``layernorm_mlp_fwd`` (LayerNorm MLP page, Description, backward pass).
+    """Backward of ``layernorm_mlp_fwd`` (LayerNorm MLP page, Description, backward pass):
+    the forward pass, then ``layernorm_mlp_bwd_from_saved`` on what it saves.
 
-    Order: db2 = colsum(dy); a = act(h) recomputed; dW2 = a^T dy; da = dy W2^T;
-    dh = da * act'(h) (fp32), db1 = colsum(dh), dh stored (E4M3 with its own scale when
-    ``fp8`` is given, else ``dtype``); dln = dh W1^T; dW1 = ln^T dh; then the norm backward
-    gives dx, dgamma, dbeta.  In FP8 mode only dh, the forward's normalized output and W1
-    are E4M3 operands; dy, W2 and the recomputed activation stay in ``dtype``.
-    ``fp8`` may carry a fixed ``grad`` scale for dh (else dh's own amax).
+    ``fp8`` = None or a dict of fp32 scales ``x``, ``w1``, ``act``, ``w2`` (forward) and ``grad``
+    (dh); None entries take the tensor's own amax.  Returns the backward's dict plus ``fwd``.
     """
     fwd = layernorm_mlp_fwd(x, gamma, beta, w1, w2, b1, b2, norm_type, zero_centered_gamma,
                             eps, act, dtype, fp8=None if fp8 is None else
                             {k: fp8.get(k) for k in ("x", "w1", "act", "w2")})
-    dy = _f64(dy)
+    ln = fwd["ln"]
+    res = layernorm_mlp_bwd_from_saved(dy, x, gamma, w1, w2, fwd["h"].value, ln.value, ln.inv(),
+                                       fwd["mu"], fwd["rsigma"], norm_type, zero_centered_gamma,
+                                       act, dtype, fp8)
+    res["fwd"] = fwd
+    return res
+
+
+def layernorm_mlp_bwd_from_saved(dy, x, gamma, w1, w2, h, ln, ln_scale_inv, mu, rsigma,
+                                 norm_type="layernorm", zero_centered_gamma=False, act="gelu",
+                                 dtype="bf16", fp8=None):
+    """The MLP backward given what the forward saved (LayerNorm MLP page, Description, backward
+    pass): h = GEMM1 output + bias (the activation input), ln = the normalized output as stored
+    (decoded E4M3 codes, dequantized by ``ln_scale_inv``, or ``dtype`` values), mu, rsigma.
+
+    Order: db2 = colsum(dy); a = act(h) recomputed; dW2 = a^T dy; da = dy W2^T;
+    dh = da * act'(h) (fp32), db1 = colsum(dh), dh stored (E4M3 with its own scale when
+    ``fp8`` is given, else ``dtype``); dln = dh W1^T; dW1 = ln^T dh; then the norm backward
+    gives dx, dgamma, dbeta.  In FP8 mode only dh, ln and W1 are E4M3 operands (W1 cast with
+    ``fp8["w1"]``, dh with ``fp8["grad"]``; None = the tensor's own amax); dy, W2 and the
+    recomputed activation stay in ``dtype``.
+    """
+    dy, h, ln = _f64(dy), _f64(h), _f64(ln)
     xs, g = _f64(x), _f64(gamma)
     db2 = colsum(dy)
-    a_re = Stored(act_fwd(fwd["h"].value, act), dtype)
+    a_re = Stored(act_fwd(h, act), dtype)
     dW2 = Stored(gemm(a_re.value.T, dy), dtype)
     w2s = Stored(_f64(w2), dtype)
     da = Stored(gemm(dy, w2s.value.T), dtype)
-    dh64 = act_bwd(da.value, fwd["h"].value, act)
+    dh64 = act_bwd(da.value, h, act)
     dh32 = to_f32(dh64)
     db1 = colsum(dh32)
     if fp8 is None:
         dh = Stored(dh32, dtype)
         w1s = Stored(_f64(w1), dtype)
         dln = Stored(gemm(dh.value, w1s.value.T), dtype)
-        dW1 = Stored(gemm(fwd["ln"].value.T, dh.value), dtype)
+        dW1 = Stored(gemm(ln.T, dh.value), dtype)
     else:
         dh = Stored(dh32, "e4m3", fp8.get("grad"))
-        w1q = fwd["w1"]
-        dln = Stored(gemm(dh.value, w1q.value.T, None, gemm_alpha(dh.scale_inv, w1q.scale_inv)), dtype)
-        dW1 = Stored(gemm(fwd["ln"].value.T, dh.value, None,
-                          gemm_alpha(fwd["ln"].scale_inv, dh.scale_inv)), dtype)
-    dx, dgamma, dbeta = norm_bwd(dln.value, xs, fwd["mu"], fwd["rsigma"], g, norm_type,
-                                 zero_centered_gamma)
-    return dict(fwd=fwd, db2=db2, a_re=a_re, dW2=dW2, da=da, dh=dh, db1=db1, dln=dln, dW1=dW1,
+        w1q = Stored(_f64(w1), "e4m3", fp8.get("w1"))
+        dln = Stored(gemm(dh.value, w1q.value.T, None, gemm_alpha(dh.scale_inv, w1q.scale_inv)),
+                     dtype)
+        dW1 = Stored(gemm(ln.T, dh.value, None, gemm_alpha(ln_scale_inv, dh.scale_inv)), dtype)
+    dx, dgamma, dbeta = norm_bwd(dln.value, xs, mu, rsigma, g, norm_type, zero_centered_gamma)
+    return dict(db2=db2, a_re=a_re, dW2=dW2, da=da, dh=dh, db1=db1, dln=dln, dW1=dW1,
                 dx=Stored(dx, dtype), dgamma=dgamma, dbeta=dbeta)
 
 
 def layernorm_dense_bwd(dy, x, gamma, beta, kernel, bias, norm_type="layernorm",
                         zero_centered_gamma=False, eps=1e-6, dtype="bf16", fp8=None):
-    """Backward of ``layernorm_dense_fwd`` (LayerNorm Dense page, Description: the gradients of
-    x, the kernel, gamma, beta and the bias, with FP8 intermediate gradients).
+    """Backward of ``layernorm_dense_fwd``: the forward pass, then
+    ``layernorm_dense_bwd_from_saved`` on what it saves.  ``fp8`` = None or a dict of fp32
+    scales ``x``, ``kernel`` and ``grad`` (None: the tensor's own amax).  Returns the
+    backward's dict plus ``fwd``."""
+    fwd = layernorm_dense_fwd(x, kernel, gamma, beta, bias, norm_type, zero_centered_gamma, eps,
+                              dtype, fp8=None if fp8 is None else
+                              {k: fp8.get(k) for k in ("x", "kernel")})
+    ln = fwd["ln"]
+    res = layernorm_dense_bwd_from_saved(dy, x, gamma, kernel, ln.value, ln.inv(), fwd["mu"],
+                                         fwd["rsigma"], norm_type, zero_centered_gamma, dtype,
+                                         fp8)
+    res["fwd"] = fwd
+    return res
+
+
+def layernorm_dense_bwd_from_saved(dy, x, gamma, kernel, ln, ln_scale_inv, mu, rsigma,
+                                   norm_type="layernorm", zero_centered_gamma=False,
+                                   dtype="bf16", fp8=None):
+    """The LayerNorm Dense backward given what the forward saved (LayerNorm Dense page,
+    Description: the gradients of x, the kernel, gamma, beta and the bias, with FP8
+    intermediate gradients): ln = the normalized output as stored (decoded E4M3 codes,
+    dequantized by ``ln_scale_inv``, or ``dtype`` values), mu, rsigma.
 
     Order: dbias = colsum(dy) over the unquantized dy; dy is the GEMM operand (E4M3 with the
     ``grad`` scale, or its own amax, when ``fp8`` is given; else ``dtype``); dln = dy kernel^T;
     dkernel = ln^T dy; then the norm backward gives dx, dgamma, dbeta.  In FP8 mode the GEMM
-    operands are dy, the forward's normalized output and the kernel, all E4M3.
-    ``fp8`` = None or a dict of fp32 scales ``x``, ``kernel`` and ``grad`` (None: own amax).
+    operands are dy, ln and the kernel (cast with ``fp8["kernel"]``), all E4M3.
     """
-    fwd = layernorm_dense_fwd(x, kernel, gamma, beta, bias, norm_type, zero_centered_gamma, eps,
-                              dtype, fp8=None if fp8 is None else
-                              {k: fp8.get(k) for k in ("x", "kernel")})
-    dy = _f64(dy)
+    dy, ln = _f64(dy), _f64(ln)
     xs, g = _f64(x), _f64(gamma)
     dbias = colsum(dy)
     if fp8 is None:
         gy = Stored(dy, dtype)
-        dln = Stored(gemm(gy.value, fwd["kernel"].value.T), dtype)
-        dk = Stored(gemm(fwd["ln"].value.T, gy.value), dtype)
+        ks = Stored(_f64(kernel), dtype)
+        dln = Stored(gemm(gy.value, ks.value.T), dtype)
+        dk = Stored(gemm(ln.T, gy.value), dtype)
     else:
         gy = Stored(dy, "e4m3", fp8.get("grad"))
-        kq = fwd["kernel"]
+        kq = Stored(_f64(kernel), "e4m3", fp8.get("kernel"))
         dln = Stored(gemm(gy.value, kq.value.T, None, gemm_alpha(gy.scale_inv, kq.scale_inv)),
                      dtype)
-        dk = Stored(gemm(fwd["ln"].value.T, gy.value, None,
-                         gemm_alpha(fwd["ln"].scale_inv, gy.scale_inv)), dtype)
-    dx, dgamma, dbeta = norm_bwd(dln.value, xs, fwd["mu"], fwd["rsigma"], g, norm_type,
-                                 zero_centered_gamma)
-    return dict(fwd=fwd, dbias=dbias, dy=gy, dln=dln, dkernel=dk, dx=Stored(dx, dtype),
-                dgamma=dgamma, dbeta=dbeta)
+        dk = Stored(gemm(ln.T, gy.value, None, gemm_alpha(ln_scale_inv, gy.scale_inv)), dtype)
+    dx, dgamma, dbeta = norm_bwd(dln.value, xs, mu, rsigma, g, norm_type, zero_centered_gamma)
+    return dict(dbias=dbias, dy=gy, dln=dln, dkernel=dk, dx=Stored(dx, dtype), dgamma=dgamma,
+                dbeta=dbeta)
