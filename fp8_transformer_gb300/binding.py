@@ -93,14 +93,14 @@ _SIGS = {
     "te_layernorm_mlp_fwd": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, ctypes.c_int, _vp, _vp,
                                             ctypes.c_int, ctypes.c_int, _f, ctypes.c_int, _QSP,
                                             _i64, _i64, _i64, ctypes.c_int, _vp, _vp, _vp, _vp,
-                                            _vp, _vp, _sz, _vp]),
+                                            _vp, _vp, _vp, _sz, _vp]),
     "te_norm_bwd": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, ctypes.c_int, _i64, _i64,
                                    ctypes.c_int, ctypes.c_int, _vp, _vp, _vp, _vp, _sz, _vp]),
     "te_profile_begin": (ctypes.c_int, [ctypes.c_int32]),
     "te_layernorm_mlp_bwd": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, ctypes.c_int, _vp, _vp, _vp,
                                             _vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, _QSP,
                                             _i64, _i64, _i64, ctypes.c_int, _vp, _vp, _vp, _vp,
-                                            _vp, _vp, _vp, _vp, _sz, _vp]),
+                                            _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "te_selftest_wait_timeout": (ctypes.c_int, [_i64, _vp]),
     "te_layernorm_mlp_fwd_host": (ctypes.c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_int,
                                                  ctypes.c_int, ctypes.c_float, ctypes.c_int, _i64,
@@ -325,7 +325,8 @@ def te_layernorm_dense_fwd(x, kernel, gamma, beta, bias, out, norm_type="layerno
 def te_layernorm_mlp_fwd(x, gamma, beta, kernel1, kernel2, bias1, bias2, out,
                          norm_type="layernorm", zero_centered_gamma=False, epsilon=1e-6,
                          activation_type=("relu",), quantizer_set=None, saved_h=None,
-                         saved_ln_out=None, mu=None, rsigma=None, workspace=None, stream=None):
+                         saved_ln_out=None, mu=None, rsigma=None, workspace=None, stream=None,
+                         saved_act=None):
     M, H = x.shape
     F = kernel2.shape[0]
     act = _act_id(activation_type)
@@ -340,9 +341,9 @@ def te_layernorm_mlp_fwd(x, gamma, beta, kernel1, kernel2, bias1, bias2, out,
                                     _norm_id(norm_type), int(bool(zero_centered_gamma)),
                                     float(epsilon), act,
                                     ctypes.byref(qs) if qs is not None else None, M, H, F, dt,
-                                    _ptr(out), _ptr(saved_h), _ptr(saved_ln_out), _ptr(mu),
-                                    _ptr(rsigma), _ptr(workspace), workspace.numel(),
-                                    _stream(stream))
+                                    _ptr(out), _ptr(saved_h), _ptr(saved_act),
+                                    _ptr(saved_ln_out), _ptr(mu), _ptr(rsigma), _ptr(workspace),
+                                    workspace.numel(), _stream(stream))
     _check("te_layernorm_mlp_fwd", st)
     return out
 
@@ -373,7 +374,7 @@ def te_layernorm_mlp_bwd(dy, x, gamma, kernel1, kernel2, saved_h, saved_ln_out, 
                          dx, dgamma, dkernel1, dkernel2, dbeta=None, dbias1=None, dbias2=None,
                          norm_type="layernorm", zero_centered_gamma=False,
                          activation_type=("relu",), quantizer_set=None, workspace=None,
-                         stream=None):
+                         stream=None, saved_dh=None):
     M, H = x.shape
     F = kernel2.shape[0]
     act = _act_id(activation_type)
@@ -388,8 +389,8 @@ def te_layernorm_mlp_bwd(dy, x, gamma, kernel1, kernel2, saved_h, saved_ln_out, 
                                     _norm_id(norm_type), int(bool(zero_centered_gamma)), act,
                                     ctypes.byref(qs) if qs is not None else None, M, H, F, dt,
                                     _ptr(dx), _ptr(dgamma), _ptr(dbeta), _ptr(dkernel1),
-                                    _ptr(dkernel2), _ptr(dbias1), _ptr(dbias2), _ptr(workspace),
-                                    workspace.numel(), _stream(stream))
+                                    _ptr(dkernel2), _ptr(dbias1), _ptr(dbias2), _ptr(saved_dh),
+                                    _ptr(workspace), workspace.numel(), _stream(stream))
     _check("te_layernorm_mlp_bwd", st)
     return dx
 

@@ -241,7 +241,7 @@ const char* te_status_string(te_status status) {
   return "unknown te_status";
 }
 
-int te_version(void) { return 100; }
+int te_version(void) { return 200; }
 
 te_status te_get_device_status(int32_t* device_status) {
   return read_and_clear_device_status(device_status);
@@ -464,9 +464,9 @@ te_status te_layernorm_mlp_fwd(const void* x, const void* gamma, const void* bet
                                const void* bias1, const void* bias2, te_norm_type norm_type,
                                int zero_centered_gamma, float epsilon, te_act_type act,
                                const te_quantizer_set* qset, int64_t M, int64_t H, int64_t F,
-                               te_dtype dtype, void* out, void* saved_h, void* saved_ln_out,
-                               float* mu, float* rsigma, void* workspace, size_t ws_bytes,
-                               void* stream) {
+                               te_dtype dtype, void* out, void* saved_h, void* saved_act,
+                               void* saved_ln_out, float* mu, float* rsigma, void* workspace,
+                               size_t ws_bytes, void* stream) {
   if (M < 0 || H <= 0 || F <= 0 || !is_act_dtype(dtype) || act == TE_IDENTITY ||
       !valid_act(act) || (norm_type != TE_LAYERNORM && norm_type != TE_RMSNORM))
     return TE_ERR_INVALID_ARG;
@@ -486,8 +486,8 @@ te_status te_layernorm_mlp_fwd(const void* x, const void* gamma, const void* bet
   if (H % 16 || F % 16 || H * int64_t(esize(dtype)) > 16384) return TE_ERR_UNSUPPORTED;
   if (!aligned16(x) || !aligned16(gamma) || !opt_aligned16(beta) || !aligned16(kernel1) ||
       !aligned16(kernel2) || !opt_aligned16(bias1) || !opt_aligned16(bias2) || !aligned16(out) ||
-      !opt_aligned16(saved_h) || !opt_aligned16(saved_ln_out) || !aligned16(workspace) ||
-      !aligned4(mu) || !aligned4(rsigma))
+      !opt_aligned16(saved_h) || !opt_aligned16(saved_act) || !opt_aligned16(saved_ln_out) ||
+      !aligned16(workspace) || !aligned4(mu) || !aligned4(rsigma))
     return TE_ERR_UNSUPPORTED;
   if (M == 0) return TE_OK;
   const bool gated = is_gated(act);
@@ -497,6 +497,7 @@ te_status te_layernorm_mlp_fwd(const void* x, const void* gamma, const void* bet
   if (!workspace || ws_bytes < L.bytes) return TE_ERR_WORKSPACE;
   cudaStream_t s = as_stream(stream);
   void* ln = saved_ln_out ? saved_ln_out : L.ln;
+  void* a2 = saved_act ? saved_act : L.a2;  // GEMM2's A operand
   // (1) normalization, written once in GEMM1's operand dtype
   te_status st = norm_into(x, dtype, M, H, gamma, beta, norm_type, zero_centered_gamma, epsilon,
                            quant ? &qset->x : nullptr, ln, quant ? TE_E4M3 : dtype, mu, rsigma, s);
@@ -547,13 +548,13 @@ te_status te_layernorm_mlp_fwd(const void* x, const void* gamma, const void* bet
       g1.D = L.a2_hi;
       g1.cast.out_dtype = TE_F32;
     } else {
-      g1.D = L.a2;
+      g1.D = a2;
       g1.cast.out_dtype = TE_E4M3;
       g1.cast.scale = qset->act.scale;
       g1.cast.scale_inv_out = qset->act.scale_inv;
     }
   } else {
-    g1.D = L.a2;
+    g1.D = a2;
     g1.cast.out_dtype = dtype;
   }
   st = launch_gemm(g1, s);
@@ -564,7 +565,7 @@ te_status te_layernorm_mlp_fwd(const void* x, const void* gamma, const void* bet
     qa.x = L.a2_hi;
     qa.x_dtype = TE_F32;
     qa.n = M * F;
-    qa.out = L.a2;
+    qa.out = a2;
     qa.cast.out_dtype = TE_E4M3;
     qa.cast.amax_in = qset->act.amax;
     qa.cast.scale_out = qset->act.scale;
@@ -574,7 +575,7 @@ te_status te_layernorm_mlp_fwd(const void* x, const void* gamma, const void* bet
   }
   // (4) GEMM2 + bias2
   GemmArgs g2;
-  g2.A = L.a2;
+  g2.A = a2;
   g2.B = w2;
   g2.ab_dtype = quant ? TE_E4M3 : dtype;
   g2.a_kmajor = 1;
@@ -600,7 +601,7 @@ te_status te_layernorm_mlp_bwd(const void* dy, const void* x, const void* gamma,
                                const te_quantizer_set* qset, int64_t M, int64_t H, int64_t F,
                                te_dtype dtype, void* dx, float* dgamma, float* dbeta,
                                void* dkernel1, void* dkernel2, float* dbias1, float* dbias2,
-                               void* workspace, size_t ws_bytes, void* stream) {
+                               void* saved_dh, void* workspace, size_t ws_bytes, void* stream) {
   if (M < 0 || H <= 0 || F <= 0 || dtype != TE_BF16 || act == TE_IDENTITY || !valid_act(act) ||
       (norm_type != TE_LAYERNORM && norm_type != TE_RMSNORM))
     return dtype == TE_F32 ? TE_ERR_UNSUPPORTED : TE_ERR_INVALID_ARG;
@@ -624,7 +625,7 @@ te_status te_layernorm_mlp_bwd(const void* dy, const void* x, const void* gamma,
       !aligned16(kernel2) || !aligned16(saved_h) || !aligned16(saved_ln_out) || !aligned16(dx) ||
       !aligned16(dkernel1) || !aligned16(dkernel2) || !aligned16(workspace) || !aligned4(mu) ||
       !aligned4(rsigma) || !aligned4(dgamma) || !aligned4(dbeta) || !aligned4(dbias1) ||
-      !aligned4(dbias2))
+      !aligned4(dbias2) || !opt_aligned16(saved_dh))
     return TE_ERR_UNSUPPORTED;
   cudaStream_t s = as_stream(stream);
   const bool gated = is_gated(act);
@@ -642,6 +643,7 @@ te_status te_layernorm_mlp_bwd(const void* dy, const void* x, const void* gamma,
   BwdLayout L = bwd_layout(workspace, M, H, F, dtype, quant, kernel_dtype, act);
   if (!workspace || ws_bytes < L.bytes) return TE_ERR_WORKSPACE;
   float* partials = static_cast<float*>(L.partials);
+  void* dh = saved_dh ? saved_dh : L.dh;  // the dgrad / wgrad GEMMs' operand
   te_status st;
   // dbias2 = column sums of dy
   if (dbias2) {
@@ -712,7 +714,7 @@ te_status te_layernorm_mlp_bwd(const void* dy, const void* x, const void* gamma,
                   d.M = M;
                   d.N_in = F1;
                   d.act = act;
-                  d.dx = L.dh;
+                  d.dx = dh;
                   const bool two_pass = quant && qset->grad.mode == TE_SCALING_CURRENT;
                   d.dbias = (two_pass ? c.store == 0 : true) ? dbias1 : nullptr;
                   d.partials = partials;
@@ -729,7 +731,7 @@ te_status te_layernorm_mlp_bwd(const void* dy, const void* x, const void* gamma,
   // dln = dH kernel1^T   ([M, H], contraction over F')
   {
     GemmArgs g;
-    g.A = L.dh;
+    g.A = dh;
     g.B = w1;
     g.ab_dtype = quant ? TE_E4M3 : dtype;
     g.a_kmajor = 1;
@@ -748,7 +750,7 @@ te_status te_layernorm_mlp_bwd(const void* dy, const void* x, const void* gamma,
   {
     GemmArgs g;
     g.A = saved_ln_out;
-    g.B = L.dh;
+    g.B = dh;
     g.ab_dtype = quant ? TE_E4M3 : dtype;
     g.a_kmajor = 0;
     g.b_kmajor = 0;

@@ -627,15 +627,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
 template <int KIND, bool AK, bool BK, int CG>
 te_status launch_t(GemmParams& prm, int grid, cudaStream_t s) {
   constexpr size_t smem = Cfg<CG>::kSmem;
-  static bool attr_set[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (!attr_set[dev & 63]) {
-    if (cudaFuncSetAttribute(gemm_kernel<KIND, AK, BK, CG>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
-      return TE_ERR_CUDA;
-    attr_set[dev & 63] = true;
-  }
+  static PerDevice<bool> attr_set;
+  bool ok = false;
+  if (!attr_set.get(&ok, [](bool* v) {
+        *v = cudaFuncSetAttribute(gemm_kernel<KIND, AK, BK, CG>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  int(smem)) == cudaSuccess;
+        return *v;
+      }))
+    return TE_ERR_CUDA;
   if constexpr (CG == 1) {
     gemm_kernel<KIND, AK, BK, 1><<<grid, kThreads, smem, s>>>(prm);
   } else {
@@ -679,27 +679,32 @@ int choose_cta_group(int kind, int64_t M) {
 }  // namespace
 
 int num_sms() {
-  static int cached[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (!cached[dev & 63]) {
-    int n = 0;
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    cached[dev & 63] = n > 0 ? n : 1;
-  }
-  return cached[dev & 63];
+  static PerDevice<int> cached;
+  int n = 1;
+  if (!cached.get(&n, [](int* v) {
+        int dev = 0, count = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            count < 1)
+          return false;
+        *v = count;
+        return true;
+      }))
+    return 1;
+  return n;
 }
 
 int* device_status_ptr() {
-  static int* cached[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (!cached[dev & 63]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
-    cached[dev & 63] = static_cast<int*>(p);
-  }
-  return cached[dev & 63];
+  static PerDevice<int*> cached;
+  int* p = nullptr;
+  if (!cached.get(&p, [](int** v) {
+        void* addr = nullptr;
+        if (cudaGetSymbolAddress(&addr, g_device_status) != cudaSuccess || !addr) return false;
+        *v = static_cast<int*>(addr);
+        return true;
+      }))
+    return nullptr;
+  return p;
 }
 
 te_status read_and_clear_device_status(int32_t* out) {

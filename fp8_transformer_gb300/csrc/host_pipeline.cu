@@ -132,7 +132,7 @@ extern "C" te_status te_layernorm_mlp_fwd_host(
     if (cudaStreamWaitEvent(s, p->landed[c], 0) != cudaSuccess) return TE_ERR_CUDA;
     st = te_layernorm_mlp_fwd(x_dev + r0 * row_bytes, gamma, beta, kernel1, kernel2, dtype, bias1,
                               bias2, norm_type, zero_centered_gamma, epsilon, act, nullptr, m, H, F,
-                              dtype, out_dev + r0 * row_bytes, nullptr, nullptr, nullptr, nullptr,
+                              dtype, out_dev + r0 * row_bytes, nullptr, nullptr, nullptr, nullptr, nullptr,
                               fwd_ws, fwd_bytes, stream);
     if (st != TE_OK) return st;
     if (cudaEventRecord(p->computed[c], s) != cudaSuccess ||

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "te_gb300.h"
 
 namespace te {
@@ -131,6 +133,34 @@ int* device_status_ptr();
 te_status read_and_clear_device_status(int32_t* out);
 
 int num_sms();
+
+// A value set up once per device and shared by every host thread: get() runs make(&value) for
+// the current device the first time (make returns false on failure, and is then retried on the
+// next call) and returns the cached value afterwards.  Devices numbered kMaxDevices or above
+// are set up on every call, uncached.
+constexpr int kMaxDevices = 64;
+template <typename T>
+class PerDevice {
+ public:
+  template <class Make>
+  bool get(T* out, Make&& make) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    if (dev < 0 || dev >= kMaxDevices) return make(out);
+    std::lock_guard<std::mutex> lock(mu_);
+    if (!have_[dev]) {
+      if (!make(&value_[dev])) return false;
+      have_[dev] = true;
+    }
+    *out = value_[dev];
+    return true;
+  }
+
+ private:
+  std::mutex mu_;
+  T value_[kMaxDevices] = {};
+  bool have_[kMaxDevices] = {};
+};
 
 // 2-D TMA tensor map over a row-major [outer, inner] matrix of dtype, boxes of
 // box_inner x box_outer elements, 128-byte swizzle or none, out-of-bounds reads zero.

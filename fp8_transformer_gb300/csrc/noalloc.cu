@@ -29,7 +29,6 @@ namespace te {
 namespace {
 
 constexpr size_t kNoAllocPartials = size_t(2) << 20;  // floats: 8 MiB
-constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) float g_noalloc_partials[kNoAllocPartials];
 

@@ -401,16 +401,15 @@ __global__ void __launch_bounds__(kFwdWarpRowWarps * 32, NVW * Vec16<T>::N >= 12
 
 // Sets the kernel's dynamic shared memory limit once per device.
 template <typename K>
-te_status allow_ring_smem(K kernel, bool (&done)[64]) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return TE_ERR_CUDA;
-  if (!done[dev & 63]) {
-    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             int(kRingSmemMax)) != cudaSuccess)
-      return TE_ERR_CUDA;
-    done[dev & 63] = true;
-  }
-  return TE_OK;
+te_status allow_ring_smem(K kernel, PerDevice<bool>& done) {
+  bool ok = false;
+  return done.get(&ok, [&](bool* v) {
+           *v = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     int(kRingSmemMax)) == cudaSuccess;
+           return *v;
+         })
+             ? TE_OK
+             : TE_ERR_CUDA;
 }
 
 unsigned ring_grid(int64_t M) {
@@ -430,7 +429,7 @@ int ring_slots(size_t slot_bytes, int max_slots, int min_slots, int mult) {
 
 template <typename T, bool LN, int NVL, bool FULL>
 te_status launch_fwd_rows(const NormFwdArgs& a, cudaStream_t s) {
-  static bool attr_done[64] = {};
+  static PerDevice<bool> attr_done;
   const size_t params = size_t(a.H) * (LN ? 2 : 1) * sizeof(float);
   const te_status st = allow_ring_smem(norm_fwd_rows_kernel<T, LN, NVL, FULL>, attr_done);
   if (st != TE_OK) return st;
@@ -447,7 +446,7 @@ te_status launch_fwd_rows(const NormFwdArgs& a, cudaStream_t s) {
 
 template <typename T, bool LN, int NVW>
 te_status launch_fwd_warp(const NormFwdArgs& a, cudaStream_t s) {
-  static bool attr_done[64] = {};
+  static PerDevice<bool> attr_done;
   const size_t params = size_t(a.H) * (LN ? 2 : 1) * sizeof(float);
   const te_status st = allow_ring_smem(norm_fwd_warp_kernel<T, LN, NVW>, attr_done);
   if (st != TE_OK) return st;
@@ -792,7 +791,7 @@ int bwd_chunks(int64_t M) { return int(ring_grid(M > 0 ? M : 1)); }
 
 template <typename T, bool LN, int NV, bool FULL>
 te_status launch_bwd_t(const NormBwdArgs& a, cudaStream_t s) {
-  static bool attr_done[64] = {};
+  static PerDevice<bool> attr_done;
   constexpr int RB = bwd_rows_per_sync(NV);
   const size_t slot_bytes = size_t(a.H) * sizeof(T) * 2;
   // a step holds RB slots; a second step's worth lets the refills run ahead

@@ -246,6 +246,9 @@ te_status te_layernorm_dense_fwd(const void* x, const void* kernel, te_dtype ker
  *         means both kernels are pre-quantized (their scale_inv fields hold the factors),
  *         kernel_dtype == dtype means they are quantized in this call.
  *   saved_h      [M, F'] in dtype or NULL: GEMM1 output + bias1 (the activation input).
+ *   saved_act    [M, F] (E4M3 codes with qset, else dtype) or NULL: the activation output as
+ *                GEMM2 reads it.  When given, GEMM1's epilogue writes it there instead of into
+ *                the workspace (the workspace size does not change).
  *   saved_ln_out [M, H] (E4M3 with qset, else dtype) or NULL.
  *   mu, rsigma   [M] fp32 or NULL.
  */
@@ -254,9 +257,9 @@ te_status te_layernorm_mlp_fwd(const void* x, const void* gamma, const void* bet
                                const void* bias1, const void* bias2, te_norm_type norm_type,
                                int zero_centered_gamma, float epsilon, te_act_type act,
                                const te_quantizer_set* qset, int64_t M, int64_t H, int64_t F,
-                               te_dtype dtype, void* out, void* saved_h, void* saved_ln_out,
-                               float* mu, float* rsigma, void* workspace, size_t ws_bytes,
-                               void* stream);
+                               te_dtype dtype, void* out, void* saved_h, void* saved_act,
+                               void* saved_ln_out, float* mu, float* rsigma, void* workspace,
+                               size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------------------
  * te_layernorm_mlp_fwd_host -- te_layernorm_mlp_fwd (LayerNorm MLP page, Description steps
@@ -303,6 +306,8 @@ te_status te_layernorm_mlp_fwd_host(const void* x_host, const void* gamma, const
  *   as E4M3 x E4M3 GEMMs; dy, kernel2 and the recomputed activation stay in dtype.
  *   Outputs: dx [M, H] dtype; dgamma [H] fp32; dbeta [H] fp32 or NULL (layernorm only);
  *   dkernel1 [H, F'] and dkernel2 [F, H] in dtype; dbias1 [F'] and dbias2 [H] fp32 or NULL.
+ *   saved_dh [M, F'] or NULL: when given, dH is written there (E4M3 codes with qset, else dtype)
+ *   instead of into the workspace, as the dln and dkernel1 GEMMs read it.
  *   workspace: te_workspace_size(TE_OP_LAYERNORM_MLP_BWD, M, H, F, dtype, quantized,
  *   kernel_dtype, act) bytes.  H and F multiples of 16.
  */
@@ -314,7 +319,7 @@ te_status te_layernorm_mlp_bwd(const void* dy, const void* x, const void* gamma,
                                const te_quantizer_set* qset, int64_t M, int64_t H, int64_t F,
                                te_dtype dtype, void* dx, float* dgamma, float* dbeta,
                                void* dkernel1, void* dkernel2, float* dbias1, float* dbias2,
-                               void* workspace, size_t ws_bytes, void* stream);
+                               void* saved_dh, void* workspace, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------------------
  * te_layernorm_dense_bwd -- backward of te_layernorm_dense_fwd (LayerNorm Dense page,

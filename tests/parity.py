@@ -125,6 +125,8 @@ def assert_e4m3_codes(got, want_codes, pre32=None, scale=None, rel=1e-5, abs_tol
     assert steps.max() <= 1, f"{what}: codes differ by up to {int(steps.max())} steps"
     v = np.asarray(pre32, np.float64)[diff]
     dist = boundary_distance(v, scale)
+    if np.ndim(abs_tol):  # a window per element
+        abs_tol = np.broadcast_to(np.asarray(abs_tol, np.float64), np.shape(pre32))[diff]
     allowed = (rel * np.abs(v) + abs_tol) * float(scale)
     far = dist > allowed
     assert not far.any(), (f"{what}: {int(far.sum())} of {n} flips farther from a rounding "
@@ -136,3 +138,95 @@ def assert_e4m3_codes(got, want_codes, pre32=None, scale=None, rel=1e-5, abs_tol
 
 def to_dev(t, device="cuda"):
     return t.to(device).contiguous()
+
+
+# ---------------------------------------------------------------------- error windows ------
+#
+# A value the GPU computes in fp32 differs from the oracle's float64 value by at most a known
+# bound w (its fp32 error window).  Where it is then rounded (to bf16, or to an E4M3 code), the
+# two roundings can differ only if the interval [v - w, v + w] straddles a rounding midpoint,
+# and then only by the jump between the two rounded ends.  A consumer that is linear in such
+# values inherits the jumps through the absolute values of its coefficients.  These windows let
+# the tests compare each step of a chain with the oracle's step at the pages' tight rules,
+# adding exactly what the rounding of an fp32 intermediate can explain.
+
+# |fp32 GEMM result - exact| <= ACC_REL * sum_k |a_k b_k| for the library's tensor-core GEMMs
+# (bf16 and E4M3 operands, fp32 accumulation); tests/test_gpu_kernels.py measures it.
+ACC_REL = 2.0 ** -18
+
+
+def gemm_window(a, b, alpha=1.0):
+    """fp32 accumulation window of alpha * (a @ b): ACC_REL * |alpha| * (|a| @ |b|)."""
+    return ACC_REL * abs(float(alpha)) * (np.abs(np.asarray(a, np.float64)) @
+                                          np.abs(np.asarray(b, np.float64)))
+
+
+def bf16_jump(v64, w) -> np.ndarray:
+    """How far the bf16 rounding of a value known to within +-w of v64 can move from
+    bf16(v64): 0 where [v - w, v + w] rounds to one bf16 number."""
+    v = np.asarray(v64, np.float64)
+    lo, hi, mid = nx.bf16_round(v - w), nx.bf16_round(v + w), nx.bf16_round(v)
+    return np.maximum(np.abs(hi - mid), np.abs(mid - lo))
+
+
+def assert_in_window(got, ref64, w, what, stored="f32", rel=1e-4, max_frac=None):
+    """``got`` against the float64 reference ``ref64`` known to within +-w (array or scalar).
+
+    stored="bf16": got must be a bf16 rounding of a value in [ref - w, ref + w] (rounding is
+    monotonic, so bf16(ref - w) <= got <= bf16(ref + w)); ``max_frac`` bounds the fraction of
+    elements that differ from bf16(ref) at all.
+    stored="f32" (an fp32 reduction): |got - ref| <= rel * max(|ref|, rms(ref)) + w, the 1e-4
+    reduction rule plus the window its inputs carry.
+    """
+    got, ref = np64(got), np.asarray(ref64, np.float64)
+    w = np.broadcast_to(np.asarray(w, np.float64), ref.shape)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    if stored == "bf16":
+        lo, hi = nx.bf16_round(ref - w), nx.bf16_round(ref + w)
+        bad = (got < lo) | (got > hi)
+        assert not bad.any(), (f"{what}: {int(bad.sum())} of {bad.size} outside the window; first "
+                               f"got {got[bad][:3]} ref {ref[bad][:3]} w {w[bad][:3]}")
+        if max_frac is not None:
+            moved = got != nx.bf16_round(ref)
+            assert moved.mean() <= max_frac, f"{what}: {int(moved.sum())} of {moved.size} moved"
+        return
+    scale = np.maximum(np.abs(ref), rms(ref))
+    err = np.abs(got - ref)
+    tol = rel * scale + w
+    bad = err > tol
+    assert not bad.any(), (f"{what}: {int(bad.sum())} of {bad.size} out of tolerance; worst "
+                           f"{float((err / tol).max()):.3f}x")
+
+
+# ---------------------------------------------------------------------- guard bands --------
+
+GUARD_BYTE = 0xA5
+
+
+class Guarded:
+    """An output tensor with guard bands on both sides: ``t`` is a contiguous view into a larger
+    byte buffer whose first and last ``rows`` rows' worth of bytes (at least 4 KiB) hold
+    GUARD_BYTE.  ``check()`` asserts that no byte of either band changed, so that a store past
+    a tile edge of a ragged shape into neighbouring memory fails the test."""
+
+    def __init__(self, shape, dtype, device="cuda", rows=256):
+        esz = torch.tensor([], dtype=dtype).element_size()
+        n = 1
+        for d in shape:
+            n *= int(d)
+        row = int(shape[-1]) * esz if len(shape) else esz
+        g = max(4096, rows * row)
+        self.g = (g + 255) // 256 * 256
+        self.nbytes = n * esz
+        self.raw = torch.full((self.nbytes + 2 * self.g,), GUARD_BYTE, dtype=torch.uint8,
+                              device=device)
+        self.t = self.raw[self.g:self.g + self.nbytes].view(dtype).view(*shape)
+
+    def check(self, what="output"):
+        torch.cuda.synchronize()
+        lo = self.raw[:self.g]
+        hi = self.raw[self.g + self.nbytes:]
+        nlo = int((lo != GUARD_BYTE).sum().item())
+        nhi = int((hi != GUARD_BYTE).sum().item())
+        assert nlo == 0 and nhi == 0, (f"{what}: {nlo} bytes before and {nhi} bytes after the "
+                                       f"tensor were overwritten")

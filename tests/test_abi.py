@@ -38,7 +38,7 @@ def test_library_exports_every_declared_symbol():
 
 
 def test_host_only_calls():
-    assert te.version() == 100
+    assert te.version() == 200
     assert te.status_string(0) == "TE_OK"
     assert "timed out" in te.status_string(4)
     b = te.binding
@@ -81,14 +81,22 @@ def test_backward_and_host_forward_arguments_checked_on_the_host():
     b = te.binding
     P = 4096  # a 16-byte aligned stand-in address; nothing reads it
 
-    def mlp_bwd(dtype=b.TE_BF16, act=b.TE_GELU, H=512, F=784, gamma=P):
+    def mlp_bwd(dtype=b.TE_BF16, act=b.TE_GELU, H=512, F=784, gamma=P, saved_dh=None):
         return lib.te_layernorm_mlp_bwd(P, P, gamma, P, P, dtype, P, P, P, P, b.TE_LAYERNORM, 0,
                                         act, None, 64, H, F, dtype, P, P, P, P, P, P, P, P,
-                                        1 << 20, None)
+                                        saved_dh, 1 << 20, None)
     assert mlp_bwd(dtype=b.TE_F32) == b.TE_ERR_UNSUPPORTED       # bf16 only
     assert mlp_bwd(act=b.TE_IDENTITY) == b.TE_ERR_INVALID_ARG    # the MLP needs an activation
     assert mlp_bwd(gamma=None) == b.TE_ERR_INVALID_ARG
     assert mlp_bwd(H=520) == b.TE_ERR_UNSUPPORTED                # H not a multiple of 16
+    assert mlp_bwd(saved_dh=P + 8) == b.TE_ERR_UNSUPPORTED       # optional output misaligned
+
+    def mlp_fwd(saved_act=None, act=b.TE_SWIGLU):
+        return lib.te_layernorm_mlp_fwd(P, P, P, P, P, b.TE_BF16, None, None, b.TE_RMSNORM, 1,
+                                        1e-6, act, None, 64, 512, 784, b.TE_BF16, P, None,
+                                        saved_act, None, None, None, P, 1 << 30, None)
+    assert mlp_fwd(saved_act=P + 8) == b.TE_ERR_UNSUPPORTED
+    assert mlp_fwd(act=b.TE_IDENTITY) == b.TE_ERR_INVALID_ARG
 
     def dense_bwd(dtype=b.TE_BF16, N=784, gamma=P):
         return lib.te_layernorm_dense_bwd(P, P, gamma, P, dtype, P, P, P, b.TE_LAYERNORM, 0, None,

@@ -1,13 +1,12 @@
 """Backward of the LayerNorm-MLP block (te_layernorm_mlp_bwd) against the oracle.
 
 The GPU runs its own forward (te_layernorm_mlp_fwd, keeping h, the normalized output, mu and
-rsigma) and then the backward; the oracle runs its own forward and backward from the same x,
-weights and upstream gradient.  Every gradient is compared:
-
-* weight gradients (contraction over tokens) and the pre-norm gradient by the GEMM rule
-  (2e-2 of the expected magnitude, plus one bf16 ulp of the stored value);
-* bias and gain gradients, whose inputs carry that GEMM error, to 2e-2 of their magnitude;
-* dbias2 = column sums of dy (identical inputs on both sides) to the 1e-4 reduction rule.
+rsigma) and then the backward, with dH kept through ``saved_dh``.  The saved tensors are the
+backward call's inputs, so the oracle's steps start from them and each output is held to the
+pages' rules step by step (``steps``): fp32 reductions to 1e-4, E4M3 codes and amax exact up to
+the rounding of the step's own fp32 arithmetic, bf16 values up to the rounding of an fp32
+intermediate, each plus only the window that the rounding of the chain's fp32 intermediates
+can explain.
 """
 
 import numpy as np
@@ -17,7 +16,9 @@ import torch
 import fp8_transformer_gb300 as te
 from oracle import block as ob
 from oracle import numerics as nx
-from parity import assert_gemm_close, assert_reduction_close, np64, rms
+from parity import ACC_REL, Guarded, assert_in_window, bf16_jump, codes, np64
+from steps import (ACT_REL, SCALE_REL, check_dact, check_mlp_bwd, check_norm_dx,
+                   check_norm_params, gemm_ref)
 from workloads import make_inputs
 
 pytestmark = pytest.mark.gpu
@@ -25,8 +26,8 @@ DEV = "cuda"
 SCALES = dict(x=32.0, w1=2048.0, act=16.0, w2=2048.0, grad=64.0)
 
 
-def run_gpu(inp, fp8, mode="delayed", keep=None):
-    """GPU forward + backward; `keep` (a dict) receives the quantizer set."""
+def run_gpu(inp, fp8, mode="delayed"):
+    """GPU forward + backward; returns the saved tensors, the gradients, dH and the quantizers."""
     M, H, F = inp["M"], inp["H"], inp["F"]
     gated = ob.GATED[inp["act"]]
     F1 = 2 * F if gated else F
@@ -39,64 +40,31 @@ def run_gpu(inp, fp8, mode="delayed", keep=None):
     elif fp8:
         qs = te.QuantizerSet(**{k: te.Quantizer(mode="current")
                                 for k in ("x", "kernel1", "act", "kernel2", "grad")})
-    if keep is not None:
-        keep["qs"] = qs
     out = torch.empty(M, H, dtype=dt, device=DEV)
-    h = torch.empty(M, F1, dtype=dt, device=DEV)
-    ln = torch.empty(M, H, dtype=torch.uint8 if fp8 else dt, device=DEV)
-    mu = torch.empty(M, dtype=torch.float32, device=DEV)
-    rs = torch.empty(M, dtype=torch.float32, device=DEV)
+    g = dict(qs=qs, h=torch.empty(M, F1, dtype=dt, device=DEV),
+             ln=torch.empty(M, H, dtype=torch.uint8 if fp8 else dt, device=DEV),
+             mu=torch.empty(M, dtype=torch.float32, device=DEV),
+             rs=torch.empty(M, dtype=torch.float32, device=DEV))
     kw = dict(norm_type=inp["norm"], zero_centered_gamma=inp["zero_centered_gamma"],
               activation_type=inp["act"], quantizer_set=qs)
     te.te_layernorm_mlp_fwd(inp["x"], inp["gamma"], inp["beta"], inp["w1"], inp["w2"],
-                            inp.get("b1"), inp.get("b2"), out, epsilon=inp["eps"], saved_h=h,
-                            saved_ln_out=ln, mu=mu, rsigma=rs, **kw)
-    g = dict(dx=torch.empty(M, H, dtype=dt, device=DEV),
-             dgamma=torch.empty(H, dtype=torch.float32, device=DEV),
-             dbeta=torch.empty(H, dtype=torch.float32, device=DEV),
-             dw1=torch.empty(H, F1, dtype=dt, device=DEV),
-             dw2=torch.empty(F, H, dtype=dt, device=DEV),
-             db1=torch.empty(F1, dtype=torch.float32, device=DEV),
-             db2=torch.empty(H, dtype=torch.float32, device=DEV))
-    te.te_layernorm_mlp_bwd(inp["dy"], inp["x"], inp["gamma"], inp["w1"], inp["w2"], h, ln, mu, rs,
-                            g["dx"], g["dgamma"], g["dw1"], g["dw2"], dbeta=g["dbeta"],
-                            dbias1=g["db1"], dbias2=g["db2"], **kw)
-    torch.cuda.synchronize()
+                            inp.get("b1"), inp.get("b2"), out, epsilon=inp["eps"], saved_h=g["h"],
+                            saved_ln_out=g["ln"], mu=g["mu"], rsigma=g["rs"], **kw)
+    guards = dict(dx=Guarded((M, H), dt), dgamma=Guarded((H,), torch.float32),
+                  dbeta=Guarded((H,), torch.float32), dw1=Guarded((H, F1), dt),
+                  dw2=Guarded((F, H), dt), db1=Guarded((F1,), torch.float32),
+                  db2=Guarded((H,), torch.float32),
+                  dh=Guarded((M, F1), torch.uint8 if fp8 else dt))
+    g.update({k: gb.t for k, gb in guards.items()})
+    te.te_layernorm_mlp_bwd(inp["dy"], inp["x"], inp["gamma"], inp["w1"], inp["w2"], g["h"],
+                            g["ln"], g["mu"], g["rs"], g["dx"], g["dgamma"], g["dw1"], g["dw2"],
+                            dbeta=g["dbeta"], dbias1=g["db1"], dbias2=g["db2"],
+                            saved_dh=g["dh"], **kw)
+    for k, gb in guards.items():
+        gb.check(k)
+    if inp["norm"] != "layernorm":
+        g["dbeta"] = None
     return g
-
-
-def run_oracle(inp, fp8, scales=None):
-    f = lambda k: None if inp.get(k) is None else np64(inp[k])
-    sc = scales if scales is not None else {k: np.float32(v) for k, v in SCALES.items()}
-    return ob.layernorm_mlp_bwd(f("dy"), f("x"), f("gamma"), f("beta"), f("w1"), f("w2"),
-                                f("b1"), f("b2"), inp["norm"], inp["zero_centered_gamma"],
-                                inp["eps"], inp["act"], "bf16", fp8=sc if fp8 else None)
-
-
-def close(got, ref, what, rel=2e-2):
-    got, ref = np64(got), np.asarray(ref, np.float64)
-    tol = rel * np.maximum(np.abs(ref), rms(ref)) + 2.0 ** -8 * np.abs(ref)
-    bad = np.abs(got - ref) > tol
-    assert not bad.any(), (f"{what}: {int(bad.sum())} of {bad.size} outside; worst "
-                           f"{float((np.abs(got - ref) / tol).max()):.2f}x")
-
-
-def check(inp, g, ref):
-    M = inp["M"]
-    fwd = ref["fwd"]
-    assert_reduction_close(g["db2"], ref["db2"], what="dbias2")
-    a = ref["a_re"].value
-    assert_gemm_close(g["dw2"], ref["dW2"].value, M, rms(a), rms(np64(inp["dy"])), what="dW2")
-    ln = fwd["ln"].value * fwd["ln"].inv()
-    dh = ref["dh"].value * ref["dh"].inv()
-    fp8 = ref["dh"].dtype == "e4m3"
-    assert_gemm_close(g["dw1"], ref["dW1"].value, M, rms(ln), rms(dh), what="dW1",
-                      fp8_operands=(ln.T, dh) if fp8 else None)
-    close(g["db1"], ref["db1"], "dbias1")
-    close(g["dx"], ref["dx"].value, "dx", rel=4e-2)
-    close(g["dgamma"], ref["dgamma"], "dgamma")
-    if inp["norm"] == "layernorm":
-        close(g["dbeta"], ref["dbeta"], "dbeta")
 
 
 CASES = [("gpt_ln_mlp_bwd", dict(M=300, H=512, F=784)),
@@ -116,35 +84,26 @@ def _inputs(name, shape):
 def test_mlp_backward_small(name, shape, fp8):
     inp = _inputs(name, shape)
     g = run_gpu(inp, fp8)
-    ref = run_oracle(inp, fp8)
-    check(inp, g, ref)
+    check_mlp_bwd(inp, g, fp8)
+    if fp8:  # delayed scaling: the given scales are used as they are
+        assert g["qs"].grad.scale.item() == SCALES["grad"]
 
 
 @pytest.mark.parametrize("name,shape", CASES)
 def test_mlp_backward_fp8_current_scaling(name, shape):
     """Every quantizer in current scaling: the forward's casts and the backward's dH cast each
-    take a separate amax pass (the dbias reduction runs in dH's amax pass).  The normalized
-    output, the activation output and dH are computed by each side itself, so the oracle
-    quantizes them with the GPU's scales, after checking that each scale is the recipe's
-    function of the GPU's amax and that the amaxes agree; the weights' scales come from
-    identical inputs and must be identical."""
+    take a separate amax pass (the dbias reduction runs in dH's amax pass).  Each scale must be
+    the recipe's function of the GPU's amax; the weights' amaxes come from identical inputs and
+    must be identical; dH's amax is held by the step check."""
     inp = _inputs(name, shape)
-    keep = {}
-    g = run_gpu(inp, True, mode="current", keep=keep)
-    qs = keep["qs"]
-    gpu_scale = {}
-    for name_q, q in (("x", qs.x), ("act", qs.act), ("grad", qs.grad)):
+    g = run_gpu(inp, True, mode="current")
+    qs = g["qs"]
+    for name_q, q in (("x", qs.x), ("act", qs.act), ("grad", qs.grad), ("kernel1", qs.kernel1)):
         amax = np.float32(q.amax.item())
         assert np.float32(q.scale.item()) == nx.compute_scale(amax)[0], name_q
-        gpu_scale[name_q] = np.float32(q.scale.item())
-    ref = run_oracle(inp, True, scales=dict(x=gpu_scale["x"], w1=None, act=gpu_scale["act"],
-                                            w2=None, grad=gpu_scale["grad"]))
-    assert np.float32(qs.kernel1.scale.item()) == ref["fwd"]["w1"].scale
-    assert np.float32(qs.kernel2.scale.item()) == ref["fwd"]["w2"].scale
-    assert abs(qs.x.amax.item() - float(ref["fwd"]["ln"].amax)) <= 1e-5 * float(ref["fwd"]["ln"].amax)
-    assert abs(qs.act.amax.item() - float(ref["fwd"]["a"].amax)) <= 2e-2 * float(ref["fwd"]["a"].amax)
-    assert abs(qs.grad.amax.item() - float(ref["dh"].amax)) <= 2e-2 * float(ref["dh"].amax)
-    check(inp, g, ref)
+    w1 = nx.bf16_round(np64(inp["w1"]))
+    assert np.float32(qs.kernel1.amax.item()) == nx.amax_of(w1)
+    check_mlp_bwd(inp, g, True)
 
 
 @pytest.mark.parametrize("act", ["geglu", "reglu"])
@@ -155,47 +114,87 @@ def test_mlp_backward_other_gated(act, fp8):
     inp = _inputs("llama_rms_mlp", dict(M=256, H=512, F=528))
     inp["act"] = act
     g = run_gpu(inp, fp8)
-    ref = run_oracle(inp, fp8)
-    check(inp, g, ref)
+    check_mlp_bwd(inp, g, fp8)
 
 
-def test_mlp_backward_full_size_sampled():
-    """The full GPT backward (16384 tokens, 4096 -> 16384 -> 4096, gelu), bf16.  The oracle
-    recomputes, from its own primitives and in float64, what a sample of outputs depends on:
-    rows of dx (row-local), rows of dW2 (one GEMM1 column each), columns of dW1 and dbias1 (one
-    dA column each), and all of dbias2."""
+def _cols(t, idx):
+    """Columns idx of a device tensor, on the host as float64 (E4M3: the codes)."""
+    sel = t[:, torch.as_tensor(idx, device=t.device)]
+    return codes(sel) if t.dtype == torch.uint8 else np64(sel)
+
+
+def _decoded_rows_matmul(t, b, chunk=2048):
+    """decode(t) @ b and |decode(t)| @ |b| for an E4M3 (or bf16) device tensor t, in row chunks
+    so that the float64 copy of t never exists whole on the host."""
+    out, absout = [], []
+    for r0 in range(0, t.shape[0], chunk):
+        part = t[r0:r0 + chunk]
+        v = nx.e4m3_decode(codes(part)) if t.dtype == torch.uint8 else np64(part)
+        out.append(v @ b)
+        absout.append(np.abs(v) @ np.abs(b))
+    return np.concatenate(out), np.concatenate(absout)
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_mlp_backward_full_size_sampled(fp8):
+    """The full GPT backward (16384 tokens, 4096 -> 16384 -> 4096, gelu), bf16 and with dH in
+    E4M3 (delayed scaling), in the launch configuration the benchmark times.  The oracle's steps
+    run from the backward's inputs on a sample: all of dbias2, rows of dx (row-local), columns f
+    of the hidden layer (dH[:, f], dbias1[f], dW1[:, f], dW2[f, :]) and columns of dgamma and
+    dbeta (which need dln over every token)."""
     inp = make_inputs("gpt_ln_mlp_bwd", device=DEV)
-    g = run_gpu(inp, fp8=False)
-    for k, v in g.items():
-        assert torch.isfinite(v.float()).all(), k
+    g = run_gpu(inp, fp8)
+    for k in ("dx", "dgamma", "dbeta", "dw1", "dw2", "db1", "db2"):
+        assert torch.isfinite(g[k].float()).all(), k
     M, H, F = inp["M"], inp["H"], inp["F"]
-    f64 = lambda k: np64(inp[k])
-    x, gamma, beta, w1, w2, b1, b2, dy = (f64(k) for k in ("x", "gamma", "beta", "w1", "w2", "b1",
-                                                           "b2", "dy"))
-    bf = lambda v: nx.bf16_round(nx.to_f32(v))
-    assert_reduction_close(g["db2"], ob.colsum(dy), what="dbias2")
-    # normalized operand of every token (needed by the column samples)
-    y, mu, rs = ob.norm_fwd(x, gamma, beta, "layernorm", False, inp["eps"])
-    ln = bf(y)
+    qs = g["qs"]
     rng = np.random.default_rng(11)
-    # rows of dx: everything row-local
-    rows = np.sort(rng.choice(M, 12, replace=False))
-    h_r = bf(ob.gemm(ln[rows], w1, b1))
-    da_r = bf(ob.gemm(dy[rows], w2.T))
-    dh_r = bf(ob.act_bwd(da_r, h_r, "gelu"))
-    dln_r = bf(ob.gemm(dh_r, w1.T))
-    dx_r, _, _ = ob.norm_bwd(dln_r, x[rows], mu[rows], rs[rows], gamma, "layernorm", False)
-    close(np64(g["dx"])[rows], bf(dx_r), "dx rows", rel=4e-2)
-    # columns f of the hidden layer: dW2[f, :], dW1[:, f], dbias1[f]
+    rows = np.sort(rng.choice(M, 8, replace=False))
+    rows[-1] = M - 1
     feats = np.sort(rng.choice(F, 6, replace=False))
-    h_c = bf(ln @ w1[:, feats] + b1[feats])            # [M, 6]
-    a_c = bf(ob.act_fwd(h_c, "gelu"))
-    dw2_ref = bf(a_c.T @ dy)                           # [6, H]
-    assert_gemm_close(np64(g["dw2"])[feats], dw2_ref, M, rms(a_c), rms(dy), what="dW2 rows",
-                      stored="bf16")
-    da_c = bf(dy @ w2[feats].T)                        # [M, 6]
-    dh_c = nx.to_f32(ob.act_bwd(da_c, h_c, "gelu"))
-    close(np64(g["db1"])[feats], dh_c.sum(axis=0), "dbias1 sampled")
-    dw1_ref = bf(ln.T @ bf(dh_c))                      # [H, 6]
-    assert_gemm_close(np64(g["dw1"])[:, feats], dw1_ref, M, rms(ln), rms(dh_c),
-                      what="dW1 columns", stored="bf16")
+    feats[-1] = F - 1
+    hcols = np.sort(rng.choice(H, 6, replace=False))
+    f64 = lambda k: np64(inp[k])
+    dy, x, gamma, w1, w2 = f64("dy"), f64("x"), f64("gamma"), f64("w1"), f64("w2")
+    mu, rs = np64(g["mu"]), np64(g["rs"])
+    assert_in_window(g["db2"], ob.colsum(dy), 0.0, "dbias2")
+    # columns f of the hidden layer
+    h_c = _cols(g["h"], feats)                                     # [M, 6]
+    a64 = ob.act_fwd(h_c, "gelu")
+    J_a = bf16_jump(a64, ACT_REL * np.abs(a64))
+    a = nx.bf16_round(a64)
+    dw2, w_dw2 = gemm_ref(a.T, dy)
+    assert_in_window(np64(g["dw2"])[feats], dw2, w_dw2 + J_a.T @ np.abs(dy), "dW2 rows",
+                     stored="bf16")
+    w2b = nx.bf16_round(w2)
+    da64, w_da = gemm_ref(dy, w2b[feats].T)                        # [M, 6]
+    g_scale = np.float32(qs.grad.scale.item()) if fp8 else None
+    dh_c = _cols(g["dh"], feats)
+    check_dact(dh_c if fp8 else dh_c.astype(np.float64), np64(g["db1"])[feats], da64, w_da,
+               h_c, "gelu", q_scale=g_scale, what="dH columns")
+    if fp8:
+        dh_cv = nx.e4m3_decode(dh_c)
+        ln_v = nx.e4m3_decode(codes(g["ln"]))
+        a_w1 = float(np.float32(qs.x.scale_inv.item()) * np.float32(qs.grad.scale_inv.item()))
+        w1q = nx.e4m3_decode(nx.quantize(nx.bf16_round(w1), np.float32(qs.kernel1.scale.item())))
+        a_dln = float(np.float32(qs.grad.scale_inv.item()) * np.float32(qs.kernel1.scale_inv.item()))
+        # the amax of dH covers at least the sampled columns' values
+        pre_max = np.abs(nx.to_f32(ob.act_bwd(nx.bf16_round(da64), h_c, "gelu"))).max()
+        assert qs.grad.amax.item() >= pre_max * (1 - 1e-4)
+    else:
+        dh_cv, ln_v = dh_c, np64(g["ln"])
+        w1q, a_w1, a_dln = nx.bf16_round(w1), 1.0, 1.0
+    dw1, w_dw1 = gemm_ref(ln_v.T, dh_cv, a_w1)                     # [H, 6]
+    assert_in_window(np64(g["dw1"])[:, feats], dw1, w_dw1, "dW1 columns", stored="bf16")
+    # rows of dx: dln of those rows from the GPU's dH
+    dh_r = g["dh"][torch.as_tensor(rows, device=DEV)]
+    dh_rv = nx.e4m3_decode(codes(dh_r)) if fp8 else np64(dh_r)
+    dln_r, w_dln_r = gemm_ref(dh_rv, w1q.T, a_dln)
+    check_norm_dx(np64(g["dx"])[rows], dln_r, w_dln_r, x[rows], mu[rows], rs[rows], gamma,
+                  "layernorm", False, what="dx rows")
+    # columns of dgamma / dbeta: dln[:, hcols] over every token
+    dln_c, abs_c = _decoded_rows_matmul(g["dh"], w1q[hcols].T)
+    dln_c = dln_c * a_dln
+    w_dln_c = ACC_REL * abs(a_dln) * abs_c + SCALE_REL * np.abs(dln_c)
+    check_norm_params(np64(g["dgamma"])[hcols], np64(g["dbeta"])[hcols], dln_c, w_dln_c,
+                      x[:, hcols], mu, rs, "layernorm", what="norm columns")

@@ -12,8 +12,8 @@ import torch
 import fp8_transformer_gb300 as te
 from oracle import block as ob
 from oracle import numerics as nx
-from parity import (assert_e4m3_codes, assert_elementwise_close, assert_gemm_close,
-                    assert_reduction_close, codes, np64, rms)
+from parity import (ACC_REL, Guarded, assert_e4m3_codes, assert_elementwise_close,
+                    assert_gemm_close, assert_reduction_close, codes, np64, rms)
 from workloads import random_tensor
 
 pytestmark = pytest.mark.gpu
@@ -34,9 +34,10 @@ def rt(shape, std=1.0, seed=0, dtype="bf16", mean=0.0):
 def test_quantize_bit_exact(M, N, dtype, mode):
     x = rt((M, N), std=3.0, seed=M + N, dtype=dtype)
     q = te.Quantizer(scale=17.0, mode=mode)
-    out = torch.empty(M, N, dtype=torch.uint8, device=DEV)
+    gout = Guarded((M, N), torch.uint8)
+    out = gout.t
     te.te_quantize(x, q, out)
-    torch.cuda.synchronize()
+    gout.check("quantize")
     xv = np64(x)
     amax = nx.amax_of(xv)
     assert q.amax.item() == amax  # order-free max: bit-exact
@@ -54,6 +55,109 @@ def test_quantize_saturates_and_keeps_sign():
     assert_e4m3_codes(out, nx.quantize(np64(x), np.float32(1.0)), what="saturate")
 
 
+def _nan_code(c):
+    return (np.asarray(c) & 0x7F) == 0x7F
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("mode", ["delayed", "current"])
+def test_quantize_nan_inf(dtype, mode):
+    """NaN encodes as an E4M3 NaN code (either sign) and is ignored by the amax; +-inf
+    saturates to +-448 and makes the amax infinite, which current scaling turns into scale 1."""
+    vals = [float("nan"), float("inf"), float("-inf"), 0.0, -0.0, 1.5, -3.25, 1000.0,
+            -1000.0, 2.0 ** -10, float("nan"), 7.0, -0.5, 0.25, 448.0, -464.0]
+    x = torch.tensor([vals], dtype=TDT[dtype], device=DEV)
+    q = te.Quantizer(scale=2.0, mode=mode)
+    out = torch.empty(1, 16, dtype=torch.uint8, device=DEV)
+    te.te_quantize(x, q, out)
+    torch.cuda.synchronize()
+    xv = np64(x)
+    assert q.amax.item() == float("inf")
+    scale = np.float32(2.0) if mode == "delayed" else np.float32(1.0)
+    assert q.scale.item() == scale and q.scale_inv.item() == 1.0 / scale
+    got, want = codes(out), nx.quantize(xv, scale).astype(np.int64)
+    nan = np.isnan(xv)
+    assert _nan_code(got[nan]).all()
+    assert np.array_equal(got[~nan], want[~nan])
+    assert got[0, 1] == 0x7E and got[0, 2] == 0xFE  # +-inf -> +-448
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_quantize_nan_and_zero_amax_current_scaling(dtype):
+    """Current scaling: NaN does not enter the amax (scale from the finite values); an all-zero
+    tensor has amax 0, which gives scale 1 and all-zero codes."""
+    x = rt((8, 64), std=3.0, seed=41, dtype=dtype)
+    x[3, 5] = float("nan")
+    q = te.Quantizer(mode="current")
+    out = torch.empty(8, 64, dtype=torch.uint8, device=DEV)
+    te.te_quantize(x, q, out)
+    torch.cuda.synchronize()
+    xv = np64(x)
+    amax = nx.amax_of(xv)
+    assert np.isfinite(amax) and q.amax.item() == amax
+    scale = nx.compute_scale(amax)[0]
+    assert q.scale.item() == scale
+    got, want = codes(out), nx.quantize(xv, scale).astype(np.int64)
+    assert _nan_code(got[3, 5])
+    got[3, 5] = want[3, 5] = 0
+    assert np.array_equal(got, want)
+    z = torch.zeros(8, 64, dtype=TDT[dtype], device=DEV)
+    qz = te.Quantizer(scale=5.0, mode="current")
+    te.te_quantize(z, qz, out)
+    torch.cuda.synchronize()
+    assert qz.amax.item() == 0.0 and qz.scale.item() == 1.0 and qz.scale_inv.item() == 1.0
+    assert int(out.count_nonzero().item()) == 0
+
+
+def test_norm_e4m3_zero_rows_and_all_zero_current_scaling():
+    """RMSNorm of all-zero rows is zero; a tensor of only such rows has amax 0 -> scale 1 under
+    current scaling.  LayerNorm of a constant row is beta exactly."""
+    M, H = 70, 1024
+    x = torch.zeros(M, H, dtype=torch.bfloat16, device=DEV)
+    gamma = rt((H,), 0.1, 42, mean=1.0)
+    q = te.Quantizer(scale=3.0, mode="current")
+    out = torch.full((M, H), 0x55, dtype=torch.uint8, device=DEV)
+    te.te_norm_fwd(x, gamma, None, "rmsnorm", False, 1e-6, out, q=q)
+    torch.cuda.synchronize()
+    assert q.amax.item() == 0.0 and q.scale.item() == 1.0
+    assert int(out.count_nonzero().item()) == 0
+    x[5].fill_(3.0)  # a constant LayerNorm row: y = beta
+    beta = rt((H,), 0.1, 43)
+    q2 = te.Quantizer(scale=64.0)
+    te.te_norm_fwd(x, gamma, beta, "layernorm", False, 1e-6, out, q=q2)
+    torch.cuda.synchronize()
+    want = nx.quantize(np64(beta)[None, :].repeat(M, 0), np.float32(64.0))
+    assert_e4m3_codes(out, want, what="constant rows")
+    assert q2.amax.item() == nx.amax_of(np64(beta))
+
+
+def test_dact_dbias_nan_zero_current_scaling():
+    """dact + dbias + E4M3 in current scaling: an all-zero dy gives dx codes 0, dbias 0 and
+    scale 1; a NaN in dy becomes a NaN code, a NaN in its dbias column, and stays out of the
+    amax."""
+    M, N = 300, 528
+    h = rt((M, N), std=2.0, seed=44)
+    dy = torch.zeros(M, N, dtype=torch.bfloat16, device=DEV)
+    dx = torch.full((M, N), 0x55, dtype=torch.uint8, device=DEV)
+    db = torch.full((N,), 1.0, dtype=torch.float32, device=DEV)
+    q = te.Quantizer(scale=9.0, mode="current")
+    te.te_dact_dbias_quantize(dy, h, "gelu", dx, dbias=db, q=q)
+    torch.cuda.synchronize()
+    assert q.amax.item() == 0.0 and q.scale.item() == 1.0
+    assert int(dx.count_nonzero().item()) == 0 and int(db.count_nonzero().item()) == 0
+    dy = rt((M, N), seed=45)
+    dy[7, 11] = float("nan")
+    te.te_dact_dbias_quantize(dy, h, "gelu", dx, dbias=db, q=q)
+    torch.cuda.synchronize()
+    pre = nx.to_f32(ob.act_bwd(np64(dy), np64(h), "gelu"))
+    amax = nx.amax_of(pre)
+    assert np.isfinite(q.amax.item()) and abs(q.amax.item() - amax) <= 1e-6 * amax
+    got = codes(dx)
+    assert _nan_code(got[7, 11])
+    dbv = np64(db)
+    assert np.isnan(dbv[11]) and np.isfinite(np.delete(dbv, 11)).all()
+
+
 # ------------------------------------------------------------------ activation -------------
 
 
@@ -62,8 +166,10 @@ def test_quantize_saturates_and_keeps_sign():
 def test_act_lu_bf16(act, M, N):
     x = rt((M, N), std=2.0, seed=3)
     n_out = N // 2 if ob.GATED[act] else N
-    out = torch.empty(M, n_out, dtype=torch.bfloat16, device=DEV)
+    gout = Guarded((M, n_out), torch.bfloat16)
+    out = gout.t
     te.te_act_lu(x, act, out)
+    gout.check(act)
     ref = ob.act_fwd(np64(x), act)
     assert_elementwise_close(out, nx.bf16_round(nx.to_f32(ref)), what=act)
     if act in ("relu", "reglu"):  # exact arithmetic (one rounding): bit-exact
@@ -107,9 +213,11 @@ def test_dact_dbias_bf16(act, M, N_in):
     n_out = N_in // 2 if ob.GATED.get(act, False) else N_in
     dy = rt((M, n_out), seed=5)
     h = rt((M, N_in), std=2.0, seed=6)
-    dx = torch.empty(M, N_in, dtype=torch.bfloat16, device=DEV)
-    db = torch.empty(N_in, dtype=torch.float32, device=DEV)
+    gdx, gdb = Guarded((M, N_in), torch.bfloat16), Guarded((N_in,), torch.float32)
+    dx, db = gdx.t, gdb.t
     te.te_dact_dbias_quantize(dy, h, act, dx, dbias=db)
+    gdx.check("dx")
+    gdb.check("dbias")
     ref = np64(dy) if act == "identity" else ob.act_bwd(np64(dy), np64(h), act)
     assert_elementwise_close(dx, nx.bf16_round(nx.to_f32(ref)), what=f"d{act}")
     assert_reduction_close(db, ob.colsum(nx.to_f32(ref)), what=f"dbias {act}")
@@ -162,11 +270,13 @@ def test_norm_fwd(norm, M, H, dtype, zc):
     x = rt((M, H), std=2.0, seed=11, dtype=dtype, mean=0.5)
     gamma = rt((H,), std=0.1, seed=12, dtype=dtype, mean=0.0 if zc else 1.0)
     beta = rt((H,), std=0.1, seed=13, dtype=dtype)
-    out = torch.empty(M, H, dtype=TDT[dtype], device=DEV)
-    mu = torch.empty(M, dtype=torch.float32, device=DEV)
-    rs = torch.empty(M, dtype=torch.float32, device=DEV)
+    gout = Guarded((M, H), TDT[dtype])
+    gmu, grs = Guarded((M,), torch.float32), Guarded((M,), torch.float32)
+    out, mu, rs = gout.t, gmu.t, grs.t
     q = te.Quantizer()
     te.te_norm_fwd(x, gamma, beta, norm, zc, 1e-5, out, q=q, mu=mu, rsigma=rs)
+    for gb, name in ((gout, "y"), (gmu, "mu"), (grs, "rsigma")):
+        gb.check(name)
     y, m_ref, r_ref = ob.norm_fwd(np64(x), np64(gamma), np64(beta), norm, zc, 1e-5)
     want = nx.to_f32(y) if dtype == "f32" else nx.bf16_round(nx.to_f32(y))
     assert_elementwise_close(out, want, what=f"{norm} y")
@@ -182,10 +292,11 @@ def test_norm_fwd_e4m3(mode):
     M, H = 1000, 4096
     x = rt((M, H), seed=14)
     gamma, beta = rt((H,), 0.1, 15, mean=1.0), rt((H,), 0.1, 16)
-    out = torch.empty(M, H, dtype=torch.uint8, device=DEV)
+    gout = Guarded((M, H), torch.uint8)
+    out = gout.t
     q = te.Quantizer(scale=64.0, mode=mode)
     te.te_norm_fwd(x, gamma, beta, "layernorm", False, 1e-5, out, q=q)
-    torch.cuda.synchronize()
+    gout.check("norm e4m3")
     y, _, _ = ob.norm_fwd(np64(x), np64(gamma), np64(beta), "layernorm", False, 1e-5)
     pre = nx.to_f32(y)
     gpu_scale = np.float32(q.scale.item())
@@ -270,8 +381,10 @@ def test_gemm_bf16_layouts(a_trans, b_trans, M, N, K):
     A = rt((K, M) if a_trans else (M, K), seed=23)
     B = rt((N, K) if b_trans else (K, N), seed=24)
     bias = rt((N,), 0.5, 25)
-    out = torch.empty(M, N, dtype=torch.bfloat16, device=DEV)
+    gout = Guarded((M, N), torch.bfloat16)
+    out = gout.t
     te.te_gemm(A, B, out, a_trans=a_trans, b_trans=b_trans, bias=bias)
+    gout.check("gemm")
     a = np64(A).T if a_trans else np64(A)
     b = np64(B).T if b_trans else np64(B)
     ref = ob.gemm(a, b, np64(bias))
@@ -299,6 +412,40 @@ def test_gemm_e4m3(a_trans, b_trans):
     assert_gemm_close(out, ref, K, rms(a) / 64, rms(b) / 128, what="gemm e4m3")
     err = np.abs(np64(out) - ref).max()
     assert err <= 1e-4 * np.abs(ref).max() + 1e-6
+
+
+@pytest.mark.parametrize("kind", ["bf16", "e4m3"])
+@pytest.mark.parametrize("a_trans,b_trans", [(False, False), (False, True), (True, False)])
+@pytest.mark.parametrize("K", [512, 4096, 16384])
+def test_gemm_accumulation_window(kind, a_trans, b_trans, K):
+    """The fp32 accumulation error of the tensor-core GEMMs against the exact (float64) sum,
+    relative to sum_k |a_k b_k|, stays within parity.ACC_REL: the window the step-by-step
+    backward checks allow a bf16 GEMM output to round across a midpoint.  Output in fp32, so
+    nothing but the accumulation is measured."""
+    M, N = 256, 272
+    A = rt((K, M) if a_trans else (M, K), std=1.0, seed=K + 1, dtype="f32")
+    B = rt((N, K) if b_trans else (K, N), std=1.0, seed=K + 2, dtype="f32")
+    if kind == "bf16":
+        A, B = A.to(torch.bfloat16), B.to(torch.bfloat16)
+        a, b = np64(A), np64(B)
+        sa = sb = None
+        alpha = 1.0
+    else:
+        A = (A * 64).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8)
+        B = (B * 64).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8)
+        a, b = nx.e4m3_decode(codes(A)), nx.e4m3_decode(codes(B))
+        sa = torch.tensor([1 / 64.0], device=DEV)
+        sb = torch.tensor([1 / 64.0], device=DEV)
+        alpha = ob.gemm_alpha(1 / 64.0, 1 / 64.0)
+    out = torch.empty(M, N, dtype=torch.float32, device=DEV)
+    te.te_gemm(A, B, out, a_trans=a_trans, b_trans=b_trans, a_scale_inv=sa, b_scale_inv=sb)
+    a = a.T if a_trans else a
+    b = b.T if b_trans else b
+    ref = ob.gemm(a, b, None, alpha)
+    absdot = np.abs(a) @ np.abs(b) * abs(alpha)
+    ratio = float((np.abs(np64(out) - ref) / absdot).max())
+    print(f"accumulation error / sum|ab|: {ratio:.3e} ({kind}, K={K})")
+    assert ratio <= ACC_REL, f"{ratio:.3e} > ACC_REL {ACC_REL:.3e}"
 
 
 def test_gemm_tf32_k_major():
