@@ -38,6 +38,7 @@ from __future__ import annotations
 import math
 
 import numpy as np
+from scipy.special import expit
 
 from .numerics import (amax_of, bf16_round, compute_scale, dequantize, e4m3_decode,
                        quantize, to_f32)
@@ -117,9 +118,17 @@ def relu(h):
     return np.maximum(h, 0.0)
 
 
+def _half_one_plus_tanh(u):
+    """0.5 (1 + tanh(u)), evaluated as the logistic function of 2u (the same number: 1 + tanh(u)
+    = 2 / (1 + exp(-2u))), which keeps its relative accuracy where 1 + tanh(u) would cancel
+    (u below about -5, where float64 tanh(u) rounds to within a few ulps of -1)."""
+    return expit(2.0 * np.asarray(u, dtype=np.float64))
+
+
 def gelu(h):
+    """Tanh-form GELU 0.5 h (1 + tanh(sqrt(2/pi) (h + 0.044715 h^3)))."""
     h = np.asarray(h, dtype=np.float64)
-    return 0.5 * h * (1.0 + np.tanh(SQRT_2_OVER_PI * (h + GELU_CUBIC * h ** 3)))
+    return h * _half_one_plus_tanh(SQRT_2_OVER_PI * (h + GELU_CUBIC * h ** 3))
 
 
 def silu(z):
@@ -134,10 +143,13 @@ def d_relu(h):
 
 def d_gelu(h):
     """Derivative of the tanh-form gelu: with u = sqrt(2/pi)(h + 0.044715 h^3), t = tanh(u),
-    gelu' = 0.5 (1 + t) + 0.5 h (1 - t^2) sqrt(2/pi) (1 + 3 * 0.044715 h^2)."""
+    gelu' = 0.5 (1 + t) + 0.5 h (1 - t^2) sqrt(2/pi) (1 + 3 * 0.044715 h^2).
+    0.5 (1 + t) and 1 - t^2 = 4 * [0.5 (1 + t)] * [0.5 (1 - t)] are taken through the logistic
+    function (see _half_one_plus_tanh), so neither cancels in the tails."""
     h = np.asarray(h, dtype=np.float64)
-    t = np.tanh(SQRT_2_OVER_PI * (h + GELU_CUBIC * h ** 3))
-    return 0.5 * (1.0 + t) + 0.5 * h * (1.0 - t * t) * SQRT_2_OVER_PI * (1.0 + 3.0 * GELU_CUBIC * h * h)
+    u = SQRT_2_OVER_PI * (h + GELU_CUBIC * h ** 3)
+    p, m = _half_one_plus_tanh(u), _half_one_plus_tanh(-u)
+    return p + 2.0 * h * p * m * SQRT_2_OVER_PI * (1.0 + 3.0 * GELU_CUBIC * h * h)
 
 
 def d_silu(z):

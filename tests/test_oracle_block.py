@@ -149,6 +149,24 @@ def test_gelu_tanh_form_close_to_erf_form():
     assert err.max() > 1e-5  # and it is the tanh form, not the exact one
 
 
+@pytest.mark.parametrize("h", [-12.0, -9.5, -6.875, -4.0, -1.5, -0.75, -1e-3, 0.0, 2e-3, 0.5,
+                               1.0, 3.0, 6.875, 11.0])
+def test_gelu_and_derivative_against_high_precision(h):
+    """The tanh form and its derivative evaluated with 200 significant digits (mpmath) from the
+    definition as written, 0.5 h (1 + tanh(u)): the oracle keeps 1e-13 relative accuracy in the
+    far tails, where a float64 evaluation of 1 + tanh(u) itself would cancel."""
+    mp = pytest.importorskip("mpmath")
+    mp.mp.dps = 200
+    hm = mp.mpf(h)
+    c = mp.sqrt(2 / mp.pi)
+    u = c * (hm + mp.mpf("0.044715") * hm ** 3)
+    t = mp.tanh(u)
+    g = hm / 2 * (1 + t)
+    dg = (1 + t) / 2 + hm / 2 * (1 - t * t) * c * (1 + 3 * mp.mpf("0.044715") * hm * hm)
+    assert ob.gelu(np.array([h]))[0] == pytest.approx(float(g), rel=1e-13, abs=1e-300)
+    assert ob.d_gelu(np.array([h]))[0] == pytest.approx(float(dg), rel=1e-12, abs=1e-300)
+
+
 def test_activation_identities():
     x = np.linspace(-10, 10, 4001)
     np.testing.assert_allclose(ob.gelu(x) - ob.gelu(-x), x, atol=1e-12)
