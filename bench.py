@@ -32,6 +32,7 @@ WORKLOAD = "llama_rms_mlp"
 METRIC = "fused LN-MLP fwd TFLOP/s (bf16, FP8) & % tensor peak; norm/dact GB/s % HBM"
 UNIT = "TFLOP/s"
 FLUSH_BYTES = 512 << 20  # > 129 MB L2
+HBM_NOMINAL_GBS = 7900.0  # GB300 HBM3e datasheet figure, for context beside the measured copy
 E2E_CHUNKS = 4  # row slices of the host-buffer forward (copies overlap the other slices' compute)
 
 
@@ -73,7 +74,7 @@ def mlp_flops(M, H, F, gated):
     return 2.0 * M * H * f1 + 2.0 * M * F * H
 
 
-TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "gemm_pair_traffic_llama_full.md")
+TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "gemm_pair_traffic_llama_full.json")
 
 
 def measured_traffic():
@@ -82,21 +83,17 @@ def measured_traffic():
     taken (the capture records the sha256 of those files, concatenated in the listed order)."""
     import hashlib
     try:
-        fields = {}
         with open(TRAFFIC_PROFILE) as f:
-            for line in f:
-                if ":" in line and not line.startswith(("|", "#", "`")):
-                    k, v = line.split(":", 1)
-                    fields[k.strip()] = v.strip()
-        if fields["sources"].split() != GEMM_SOURCES:
+            rec = json.load(f)
+        if rec["sources"] != GEMM_SOURCES:
             return None
         h = hashlib.sha256()
-        for rel in fields["sources"].split():
+        for rel in rec["sources"]:
             with open(os.path.join(ROOT, rel), "rb") as f:
                 h.update(f.read())
-        if h.hexdigest() != fields["sources sha256"]:
+        if h.hexdigest() != rec["sources_sha256"]:
             return None
-        return int(fields["traffic_bytes_per_launch"])
+        return int(rec["traffic_bytes_per_launch"])
     except Exception:
         return None
 
@@ -266,6 +263,33 @@ def cublas_calibration(M, H, F, gated, dev, steps, flush):
     return res
 
 
+def fp8_peak_measured(dev, flush):
+    """Dense E4M3 tensor throughput of cuBLASLt (torch._scaled_mm, 8192^3, bf16 out), best of
+    10 CUDA-event timed calls with L2 flushed between them: the FP8 roofline denominator,
+    measured once after every timed region of the bench.  None if torch cannot run it."""
+    import torch
+    try:
+        n = 8192
+        a = torch.randn(n, n, device=dev).to(torch.float8_e4m3fn)
+        b = torch.randn(n, n, device=dev).to(torch.float8_e4m3fn).t()  # column-major operand
+        one = torch.ones((), device=dev)
+        fn = lambda: torch._scaled_mm(a, b, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+        for _ in range(3):
+            fn()
+        best = min(time_steps(fn, 10, flush))
+        return 2.0 * n ** 3 / (best / 1e3) / 1e12
+    except Exception:  # pragma: no cover - depends on the installed torch
+        return None
+
+
+def bw_entry(shape, nbytes, ms, peaks):
+    """GB/s of one bandwidth-bound kernel and its fraction of the measured copy bandwidth
+    (`frac`) and of the datasheet figure (`frac_nominal`)."""
+    gbs = nbytes / (ms / 1e3) / 1e9
+    return {"shape": list(shape), "GB/s": gbs, "frac": gbs / peaks["hbm"],
+            "frac_nominal": gbs / HBM_NOMINAL_GBS, "ms": ms, "bytes": nbytes}
+
+
 def bandwidth_kernels(args, dev, peaks):
     """GB/s of the bandwidth-bound kernels alone (profiling aid): norm forward at the Llama
     shape (bf16 and E4M3 out), and at the GPT backward shape the activation recompute, the
@@ -287,8 +311,7 @@ def bandwidth_kernels(args, dev, peaks):
             flush()
             fn()
         ms = statistics.mean(time_steps(fn, args.steps, flush))
-        gbs = nbytes / (ms / 1e3) / 1e9
-        res[name] = {"GB/s": gbs, "frac": gbs / peaks["hbm"], "ms": ms, "bytes": nbytes}
+        res[name] = bw_entry([], nbytes, ms, peaks)
 
     x = random_tensor((M, H), device=dev, seed=1)
     g = random_tensor((H,), std=0.05, device=dev, seed=2)
@@ -532,15 +555,48 @@ def run_ours(args, rank, world, local_rank):
     ms_e2e = max_over_ranks(statistics.mean(time_steps(step_e2e, args.steps, flush)))
     e2e_value = world * flops / (ms_e2e / 1e3) / 1e12
 
-    # ---- bandwidth-bound kernels: norm (this workload's shape) and dact+dbias+quantize
+    # ---- bandwidth-bound kernels: the norm forward at this workload's shape (bf16 and E4M3
+    # out) and at the GPT / QKV shapes (LayerNorm, bf16 and E4M3 out), dact+dbias+quantize and
+    # the norm backward
+    bwk = {}
+
+    def time_bw(name, fn, shape, nbytes):
+        for _ in range(args.warmup):
+            flush()
+            fn()
+        ms_k = max_over_ranks(statistics.mean(time_steps(fn, args.steps, flush)))
+        bwk[name] = bw_entry(shape, nbytes, ms_k, peaks)
+
     mu = torch.empty(M, dtype=torch.float32, device=dev)
     rs = torch.empty(M, dtype=torch.float32, device=dev)
     ln_out = torch.empty(M, H, dtype=torch.bfloat16, device=dev)
-    norm_step = lambda: te.te_norm_fwd(x, gamma, beta, inp["norm"], True, inp["eps"], ln_out,
-                                       mu=mu, rsigma=rs)
-    norm_bytes = M * H * (2 + 2) + H * 2 + M * 8
-    norm_step()
-    ms_norm = max_over_ranks(statistics.mean(time_steps(norm_step, args.steps, flush)))
+    ln_out8 = torch.empty(M, H, dtype=torch.uint8, device=dev)
+    qn = te.Quantizer(float(qx.scale.item()), "delayed", dev)
+    time_bw("norm_fwd", lambda: te.te_norm_fwd(x, gamma, beta, inp["norm"], True, inp["eps"],
+                                               ln_out, mu=mu, rsigma=rs),
+            (M, H), M * H * (2 + 2) + H * 2 + M * 8)
+    time_bw("norm_fwd_e4m3", lambda: te.te_norm_fwd(x, gamma, beta, inp["norm"], True,
+                                                    inp["eps"], ln_out8, q=qn, mu=mu, rsigma=rs),
+            (M, H), M * H * (2 + 1) + H * 2 + M * 8)
+    del ln_out, ln_out8
+    for tag, (Mn_, Hn_) in (("gpt", (16384, 4096)), ("qkv", (16384, 8192))):
+        xg = random_tensor((Mn_, Hn_), device=dev, seed=7)
+        gg = random_tensor((Hn_,), std=0.1, mean=1.0, device=dev, seed=8)
+        bg = random_tensor((Hn_,), std=0.1, device=dev, seed=9)
+        mug = torch.empty(Mn_, dtype=torch.float32, device=dev)
+        rsg = torch.empty(Mn_, dtype=torch.float32, device=dev)
+        yb = torch.empty(Mn_, Hn_, dtype=torch.bfloat16, device=dev)
+        y8 = torch.empty(Mn_, Hn_, dtype=torch.uint8, device=dev)
+        qg8 = te.Quantizer(32.0, "delayed", dev)
+        if tag == "gpt":
+            time_bw("norm_fwd_gpt", lambda: te.te_norm_fwd(xg, gg, bg, "layernorm", False, 1e-6,
+                                                           yb, mu=mug, rsigma=rsg),
+                    (Mn_, Hn_), Mn_ * Hn_ * 4 + Hn_ * 4 + Mn_ * 8)
+        time_bw(f"norm_fwd_{tag}_e4m3", lambda: te.te_norm_fwd(xg, gg, bg, "layernorm", False,
+                                                               1e-6, y8, q=qg8, mu=mug,
+                                                               rsigma=rsg),
+                (Mn_, Hn_), Mn_ * Hn_ * 3 + Hn_ * 4 + Mn_ * 8)
+        del xg, yb, y8
     Md, Nd = 16384, 16384  # the GPT workload's activation gradient
     dyd = torch.randn(Md, Nd, device=dev, dtype=torch.bfloat16)
     hd = torch.randn(Md, Nd, device=dev, dtype=torch.bfloat16)
@@ -551,9 +607,7 @@ def run_ours(args, rank, world, local_rank):
                       device=dev)
     dact_step = lambda: te.te_dact_dbias_quantize(dyd, hd, "gelu", dxd, dbias=dbd, q=qd,
                                                   workspace=wsd)
-    dact_bytes = Md * Nd * (2 + 2 + 1) + Nd * 4
-    dact_step()
-    ms_dact = max_over_ranks(statistics.mean(time_steps(dact_step, args.steps, flush)))
+    time_bw("dact_dbias_quantize", dact_step, (Md, Nd), Md * Nd * (2 + 2 + 1) + Nd * 4)
     del dyd, hd, dxd, wsd
     # the norm backward at the GPT workload's shape (LayerNorm, 16384 x 4096)
     Mn, Hn = 16384, 4096
@@ -569,9 +623,7 @@ def run_ours(args, rank, world, local_rank):
                       device=dev)
     nbwd_step = lambda: te.te_norm_bwd(dzn, xn, mun, rsn, gn, "layernorm", False, dxn, dgn,
                                        dbeta=dbn, workspace=wsn)
-    nbwd_bytes = Mn * Hn * (2 + 2 + 2) + Mn * 8
-    nbwd_step()
-    ms_nbwd = max_over_ranks(statistics.mean(time_steps(nbwd_step, args.steps, flush)))
+    time_bw("norm_bwd", nbwd_step, (Mn, Hn), Mn * Hn * (2 + 2 + 2) + Mn * 8)
     del xn, dzn, dxn, wsn
     barrier()
 
@@ -640,6 +692,48 @@ def run_ours(args, rank, world, local_rank):
                                         "kernel_ms": {k: round(v[0] / max(v[1], 1), 4)
                                                       for k, v in prof.items() if v[1]}}
     del dense, qout, kq, dd, dyq
+    # GPT LayerNorm-MLP forward (gelu, biases): bf16, and FP8 in the steady state (E4M3 weights
+    # cached, x / activation scales from a calibration call, then delayed)
+    gpt = make_inputs("gpt_ln_mlp", device=dev, seed=rank)
+    Mg, Hg, Fg = gpt["M"], gpt["H"], gpt["F"]
+    gout = torch.empty(Mg, Hg, dtype=torch.bfloat16, device=dev)
+    gflops = mlp_flops(Mg, Hg, Fg, False)
+    gq1, gq2 = te.Quantizer(1.0, "current", dev), te.Quantizer(1.0, "current", dev)
+    gw1q = torch.empty_like(gpt["w1"], dtype=torch.uint8)
+    gw2q = torch.empty_like(gpt["w2"], dtype=torch.uint8)
+    te.te_quantize(gpt["w1"], gq1, gw1q)
+    te.te_quantize(gpt["w2"], gq2, gw2q)
+    gqs = te.QuantizerSet(x=te.Quantizer(1.0, "current", dev), kernel1=gq1,
+                          act=te.Quantizer(1.0, "current", dev), kernel2=gq2)
+    gkw = dict(norm_type="layernorm", epsilon=gpt["eps"], activation_type="gelu")
+    te.te_layernorm_mlp_fwd(gpt["x"], gpt["gamma"], gpt["beta"], gw1q, gw2q, gpt["b1"], gpt["b2"],
+                            gout, quantizer_set=gqs, **gkw)
+    torch.cuda.synchronize()
+    gqs.x.mode = gqs.act.mode = te.binding.TE_SCALING_DELAYED
+    for tag, fn, fp8 in (
+            ("bf16", lambda: te.te_layernorm_mlp_fwd(gpt["x"], gpt["gamma"], gpt["beta"],
+                                                     gpt["w1"], gpt["w2"], gpt["b1"], gpt["b2"],
+                                                     gout, **gkw), False),
+            ("fp8", lambda: te.te_layernorm_mlp_fwd(gpt["x"], gpt["gamma"], gpt["beta"], gw1q,
+                                                    gw2q, gpt["b1"], gpt["b2"], gout,
+                                                    quantizer_set=gqs, **gkw), True)):
+        for _ in range(args.warmup):
+            flush()
+            fn()
+        torch.cuda.synchronize()
+        te.profile_begin(64 * args.steps)
+        ms = max_over_ranks(statistics.mean(time_steps(fn, args.steps, flush)))
+        prof = te.profile_end()
+        g1_ms_, g1_n_ = prof["gemm_act"]
+        nf_ms_, nf_n_ = prof["norm_fwd"]
+        nf_bytes = Mg * Hg * (2 + (1 if fp8 else 2)) + Hg * 4 + Mg * 8
+        extra[f"gpt_mlp_fwd_{tag}"] = {
+            "TFLOP/s": gflops / (ms / 1e3) / 1e12, "ms": ms,
+            "workload": "gpt_ln_mlp M=16384 H=4096 F=16384 layernorm gelu, biases",
+            "gemm1_TFLOP/s": 2.0 * Mg * Hg * Fg / (g1_ms_ / max(g1_n_, 1) / 1e3) / 1e12,
+            "norm_fwd_GB/s": nf_bytes / (nf_ms_ / max(nf_n_, 1) / 1e3) / 1e9,
+            "kernel_ms": {k: round(v[0] / max(v[1], 1), 4) for k, v in prof.items() if v[1]}}
+    del gpt, gout, gw1q, gw2q
     bw = make_inputs("gpt_ln_mlp_bwd", device=dev, seed=rank)
     Mb, Hb, Fb = bw["M"], bw["H"], bw["F"]
     bt = {k: torch.empty(*sh, dtype=dt, device=dev) for k, sh, dt in (
@@ -692,7 +786,20 @@ def run_ours(args, rank, world, local_rank):
     achieved = gemm1_flops / (g1_avg / 1e3) / 1e12
     g1f_ms, g1f_n = prof_fp8["gemm_act"]
     achieved_fp8 = gemm1_flops / (g1f_ms / max(g1f_n, 1) / 1e3) / 1e12
-    fp8_peak = 2.0 * peaks["bf16"]  # nominal fp8 : bf16 dense ratio 4.5 : 2.25
+    fp8_meas = fp8_peak_measured(dev, flush)
+    if fp8_meas is not None:
+        fp8_peak, fp8_note = fp8_meas, ("measured: torch._scaled_mm (cuBLASLt) E4M3 8192^3, "
+                                        "best of 10, after the timed regions")
+    else:
+        fp8_peak = 2.0 * peaks["bf16"]  # nominal fp8 : bf16 dense ratio 4.5 : 2.25
+        fp8_note = f"{peaks['source']} bf16 burst x nominal 2"
+    for tag in ("bf16", "fp8"):
+        e = extra.get(f"gpt_mlp_fwd_{tag}")
+        if e:
+            pk = peaks["bf16"] if tag == "bf16" else fp8_peak
+            e["frac"] = e["TFLOP/s"] / pk
+            e["gemm1_frac"] = e["gemm1_TFLOP/s"] / pk
+            e["norm_fwd_frac"] = e["norm_fwd_GB/s"] / peaks["hbm"]
     cpu_flops, cpu_times = oracle_baseline(inp, ORACLE_ROWS_BASELINE)
     cpu_value = cpu_flops / cpu_times[0] / 1e12
     share = {k: round(v[0] / max(sum(t for t, _ in prof_bf16.values()), 1e-9), 4)
@@ -708,18 +815,11 @@ def run_ours(args, rank, world, local_rank):
         "tensor_frac_bf16": value / world / peaks["bf16"],
         "fp8": {"value": value_fp8, "unit": UNIT, "ms_per_step": ms_step_fp8,
                 "frac": value_fp8 / world / fp8_peak,
-                "peak": fp8_peak, "peak_note": f"{peaks['source']} bf16 burst x nominal 2",
+                "peak": fp8_peak, "peak_note": fp8_note,
                 "scaling": "delayed (steady state), E4M3 weights cached", "other_modes": fp8_modes},
-        "bandwidth_kernels": {
-            "norm_fwd": {"shape": [M, H], "GB/s": norm_bytes / (ms_norm / 1e3) / 1e9,
-                         "frac": norm_bytes / (ms_norm / 1e3) / 1e9 / peaks["hbm"],
-                         "ms": ms_norm, "bytes": norm_bytes},
-            "norm_bwd": {"shape": [Mn, Hn], "GB/s": nbwd_bytes / (ms_nbwd / 1e3) / 1e9,
-                         "frac": nbwd_bytes / (ms_nbwd / 1e3) / 1e9 / peaks["hbm"],
-                         "ms": ms_nbwd, "bytes": nbwd_bytes},
-            "dact_dbias_quantize": {"shape": [Md, Nd], "GB/s": dact_bytes / (ms_dact / 1e3) / 1e9,
-                                    "frac": dact_bytes / (ms_dact / 1e3) / 1e9 / peaks["hbm"],
-                                    "ms": ms_dact, "bytes": dact_bytes}},
+        "bandwidth_kernels": dict(bwk, peak_note=f"frac: of the {peaks['source']} copy "
+                                  f"bandwidth {peaks['hbm']} GB/s; frac_nominal: of "
+                                  f"{HBM_NOMINAL_GBS:.0f} GB/s"),
         "other_workloads": extra,
         "clocks": clocks,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": x.numel() * 2,

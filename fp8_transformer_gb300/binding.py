@@ -43,7 +43,7 @@ EXPORTED = ["te_status_string", "te_version", "te_get_device_status", "te_worksp
             "te_layernorm_dense_bwd",
             "te_dact_dbias_quantize_noalloc",
             "te_dact_dbias_noalloc_capacity", "te_selftest_wait_timeout",
-            "te_layernorm_mlp_fwd_host"]
+            "te_layernorm_mlp_fwd_host", "te_update_scales"]
 KERNEL_KINDS = ["norm_fwd", "quantize", "act_lu", "dact_dbias", "gemm", "gemm_act", "norm_bwd",
                 "transpose"]
 
@@ -115,6 +115,7 @@ _SIGS = {
                                                       _vp]),
     "te_dact_dbias_noalloc_capacity": (_sz, []),
     "te_profile_end": (ctypes.c_int, [ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_int32)]),
+    "te_update_scales": (ctypes.c_int, [_QP, ctypes.c_int, _vp]),
 }
 
 
@@ -442,6 +443,14 @@ def profile_end() -> dict:
     cnt = (ctypes.c_int32 * n)()
     _check("te_profile_end", lib().te_profile_end(ms, cnt))
     return {k: (float(ms[i]), int(cnt[i])) for i, k in enumerate(KERNEL_KINDS)}
+
+
+def te_update_scales(quantizers, stream=None):
+    """scale = 448 / amax and scale_inv = 1 / scale on the device for every given quantizer
+    (the delayed-scaling update between calls, e.g. after an amax all-reduce)."""
+    qs = [q for q in quantizers if q is not None]
+    arr = (_Quantizer * max(len(qs), 1))(*(q.c() for q in qs))
+    _check("te_update_scales", lib().te_update_scales(arr, len(qs), _stream(stream)))
 
 
 def te_dact_dbias_quantize_noalloc(dy, x_preact, act, dx, dbias=None, q=None, stream=None):

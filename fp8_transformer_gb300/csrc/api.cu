@@ -349,6 +349,22 @@ te_status te_dact_dbias_quantize(const void* dy, const void* x_preact, te_dtype 
   });
 }
 
+te_status te_update_scales(const te_quantizer* qs, int n, void* stream) {
+  if (n < 0 || n > kMaxScaleUpdates || (n > 0 && !qs)) return TE_ERR_INVALID_ARG;
+  ScaleUpdateArgs a;
+  for (int i = 0; i < n; ++i) {
+    if (!enabled(&qs[i])) continue;  // a disabled quantizer has nothing to update
+    if (!qs[i].amax || !aligned4(qs[i].amax) || !aligned4(qs[i].scale) ||
+        !aligned4(qs[i].scale_inv))
+      return TE_ERR_INVALID_ARG;
+    a.amax[a.n] = qs[i].amax;
+    a.scale[a.n] = qs[i].scale;
+    a.scale_inv[a.n] = qs[i].scale_inv;
+    ++a.n;
+  }
+  return launch_update_scales(a, as_stream(stream));
+}
+
 te_status te_quantize(const void* x, te_dtype x_dtype, int64_t M, int64_t N,
                       const te_quantizer* q, void* out, void* stream) {
   if (M < 0 || N <= 0 || !is_act_dtype(x_dtype) || !enabled(q)) return TE_ERR_INVALID_ARG;

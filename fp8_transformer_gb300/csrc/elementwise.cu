@@ -391,4 +391,20 @@ te_status launch_quantize(const QuantizeArgs& a, cudaStream_t s) {
   return cudaGetLastError() == cudaSuccess ? TE_OK : TE_ERR_CUDA;
 }
 
+// ------------------------------------------------------------------ scale update ---------
+
+__global__ void update_scales_kernel(ScaleUpdateArgs a) {
+  const int i = threadIdx.x;
+  if (i >= a.n) return;
+  const float s = scale_from_amax(*a.amax[i]);
+  *a.scale[i] = s;
+  if (a.scale_inv[i]) *a.scale_inv[i] = 1.0f / s;
+}
+
+te_status launch_update_scales(const ScaleUpdateArgs& a, cudaStream_t s) {
+  if (a.n <= 0) return TE_OK;
+  update_scales_kernel<<<1, 32, 0, s>>>(a);
+  return cudaGetLastError() == cudaSuccess ? TE_OK : TE_ERR_CUDA;
+}
+
 }  // namespace te

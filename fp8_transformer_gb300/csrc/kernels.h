@@ -45,6 +45,7 @@ struct NormFwdArgs {
   float* mu = nullptr;
   float* rsigma = nullptr;
   CastSpec cast;
+  int prefetch = 0;  // rows ahead of the current one each warp asks L2 to fetch (set at launch)
 };
 te_status launch_norm_fwd(const NormFwdArgs& a, cudaStream_t s);
 
@@ -104,6 +105,17 @@ te_status launch_quantize(const QuantizeArgs& a, cudaStream_t s);
 
 // dst[C, R] = transpose of src[R, C] (fp32): the tf32 tensor-core path takes K-major operands.
 te_status launch_transpose_f32(const float* src, int64_t R, int64_t C, float* dst, cudaStream_t s);
+
+// scale = 448 / amax (the recipe's exceptions included), scale_inv = 1 / scale, for up to
+// kMaxScaleUpdates quantizers in one launch.
+constexpr int kMaxScaleUpdates = 16;
+struct ScaleUpdateArgs {
+  int n = 0;
+  const float* amax[kMaxScaleUpdates] = {};
+  float* scale[kMaxScaleUpdates] = {};
+  float* scale_inv[kMaxScaleUpdates] = {};
+};
+te_status launch_update_scales(const ScaleUpdateArgs& a, cudaStream_t s);
 
 // Tensor-core GEMM D[M, N] = epilogue(alpha * op(A) op(B)).
 enum Epilogue { EPI_BIAS = 0, EPI_BIAS_ACT = 1, EPI_BIAS_GATED = 2 };

@@ -21,6 +21,8 @@
 // shared memory at one named barrier.  dgamma and dbeta accumulate per thread in registers, are
 // written as one partial row per CTA and summed in a fixed order by a second kernel, so the
 // result does not depend on timing.
+#include <cstdlib>
+
 #include "cast.cuh"
 #include "common.cuh"
 #include "kernels.h"
@@ -247,13 +249,24 @@ __global__ void __launch_bounds__(kFwdGroupWarps * 32, NVL >= 8 ? kFwdRowsCtasPe
         }
       }
     };
-    // two register buffers in turn: the next row loads while the current one is processed
+    // two register buffers in turn: the next row loads while the current one is processed;
+    // the rows after it are asked into L2 by one thread
+    const uint32_t row_bytes = uint32_t(a.H) * uint32_t(sizeof(T));
+    auto prefetch_ahead = [&](int64_t r) {
+      if (tid == 0 && a.prefetch > 0 && r + (a.prefetch + 1) * stride < a.M)
+        bulk_prefetch_l2(x + (r + (a.prefetch + 1) * stride) * a.H, row_bytes);
+    };
+    if (tid == 0)
+      for (int k = 2; k <= a.prefetch && row + k * stride < a.M; ++k)
+        bulk_prefetch_l2(x + (row + k * stride) * a.H, row_bytes);
     for (int par = 0; row < a.M; par ^= 1) {
+      prefetch_ahead(row);
       if (row + stride < a.M) load_row(row + stride, bufb, x0b);
       process(row, bufa, x0a, par);
       row += stride;
       par ^= 1;
       if (row >= a.M) break;
+      prefetch_ahead(row);
       if (row + stride < a.M) load_row(row + stride, bufa, x0a);
       process(row, bufb, x0b, par);
       row += stride;
@@ -308,7 +321,15 @@ __global__ void __launch_bounds__(kFwdWarpRowWarps * 32, NVW * Vec16<T>::N >= 12
     constexpr int OUT = decltype(tag)::value;
     constexpr bool AMAX = decltype(atag)::value;
     const int64_t step = int64_t(gridDim.x) * kFwdWarpRowWarps;
-    for (int64_t r = int64_t(blockIdx.x) * kFwdWarpRowWarps + warp; r < a.M; r += step) {
+    const int64_t r0 = int64_t(blockIdx.x) * kFwdWarpRowWarps + warp;
+    const uint32_t row_bytes = uint32_t(a.H) * uint32_t(sizeof(T));
+    // rows r0 + step .. r0 + (prefetch - 1) step now; row r + prefetch step with row r below
+    if (lane == 0)
+      for (int k = 1; k < a.prefetch && r0 + k * step < a.M; ++k)
+        bulk_prefetch_l2(x + (r0 + k * step) * a.H, row_bytes);
+    for (int64_t r = r0; r < a.M; r += step) {
+      if (lane == 0 && a.prefetch > 0 && r + a.prefetch * step < a.M)
+        bulk_prefetch_l2(x + (r + a.prefetch * step) * a.H, row_bytes);
       const uint4* xr = reinterpret_cast<const uint4*>(x + r * a.H) + lane;
       uint4 cur[NVW];
 #pragma unroll
@@ -834,11 +855,25 @@ te_status launch_bwd_dispatch(const NormBwdArgs& a, cudaStream_t s) {
 
 }  // namespace
 
+// Rows ahead of its current row that each warp (or row group) of the forward asks L2 to fetch.
+// TE_NORM_FWD_PREFETCH (0 .. 8) in the environment overrides the default, for measurements.
+int fwd_prefetch_rows() {
+  static const int rows = [] {
+    const char* e = getenv("TE_NORM_FWD_PREFETCH");
+    if (!e) return 2;
+    const int v = atoi(e);
+    return v < 0 ? 0 : v > 8 ? 8 : v;
+  }();
+  return rows;
+}
+
 te_status launch_norm_fwd(const NormFwdArgs& a, cudaStream_t s) {
   if (a.M == 0) return TE_OK;
   ProfileScope prof(TE_KERNEL_NORM_FWD, s);
-  if (a.x_dtype == TE_BF16) return launch_fwd_t<__nv_bfloat16>(a, s);
-  if (a.x_dtype == TE_F32) return launch_fwd_t<float>(a, s);
+  NormFwdArgs b = a;
+  b.prefetch = fwd_prefetch_rows();
+  if (b.x_dtype == TE_BF16) return launch_fwd_t<__nv_bfloat16>(b, s);
+  if (b.x_dtype == TE_F32) return launch_fwd_t<float>(b, s);
   return TE_ERR_UNSUPPORTED;
 }
 

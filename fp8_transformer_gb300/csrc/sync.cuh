@@ -83,6 +83,12 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
       : "memory");
 }
 
+// Asks the bulk-copy engine to bring `bytes` of global memory at `src` into L2 (no data returns
+// to the SM, nothing to wait for).  src and bytes must be multiples of 16.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // One 2-D TMA tile load into this CTA's shared memory, completing on `bar` (this CTA).
 // c0 is the inner (contiguous) coordinate in elements, c1 the row.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, uint32_t bar, int c0,

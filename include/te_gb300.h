@@ -197,6 +197,18 @@ te_status te_quantize(const void* x, te_dtype x_dtype, int64_t M, int64_t N,
                       const te_quantizer* q, void* out, void* stream);
 
 /* ---------------------------------------------------------------------------------------
+ * te_update_scales -- the delayed-scaling step between two calls: for each enabled quantizer
+ * of qs[0 .. n-1] (a host array of n <= 16 structs; disabled ones, scale == NULL, are skipped),
+ * *scale = 448 / *amax (1 if the amax is 0 or not finite, FLT_MAX if the quotient overflows)
+ * and *scale_inv = 1 / *scale, on the device, in one launch on `stream`.  (The FP8 recipe the
+ * pages leave open, read as per-tensor scaling from the amax; no page section defines this
+ * step by name.)  Data-parallel callers reduce every rank's amax with MAX first, so that all
+ * ranks derive the same scales.  An enabled quantizer needs an amax; NULL or misaligned
+ * pointers and n outside 0 .. 16 give TE_ERR_INVALID_ARG.
+ */
+te_status te_update_scales(const te_quantizer* qs, int n, void* stream);
+
+/* ---------------------------------------------------------------------------------------
  * te_gemm -- D = alpha * op(A) @ op(B) + bias on the tensor cores (LayerNorm MLP page,
  * Description, forward steps (2) and (4): the tex.gemm primitive with a bias).
  *   op(A) is [M, K]: A stored [M, K] (a_trans = 0) or [K, M] (a_trans = 1).

@@ -38,11 +38,9 @@ def test_peaks_measured_file_and_fallback(tmp_path, monkeypatch):
 
 
 def _profile(tmp_path, sources, digest, traffic=123456):
-    path = tmp_path / "traffic.md"
-    path.write_text("# capture\n\n| a | b |\n|---|---|\n\n"
-                    f"traffic_bytes_per_launch: {traffic}\n"
-                    f"sources: {' '.join(sources)}\n"
-                    f"sources sha256: {digest}\n")
+    path = tmp_path / "traffic.json"
+    path.write_text(json.dumps({"traffic_bytes_per_launch": traffic, "sources": list(sources),
+                                "sources_sha256": digest}))
     return str(path)
 
 
@@ -65,5 +63,5 @@ def test_traffic_kept_only_while_the_gemm_sources_match(tmp_path, monkeypatch):
     monkeypatch.setattr(bench, "TRAFFIC_PROFILE", _profile(tmp_path, src[:2], _digest(src[:2])))
     assert bench.measured_traffic() is None
     # and a missing capture
-    monkeypatch.setattr(bench, "TRAFFIC_PROFILE", str(tmp_path / "absent.md"))
+    monkeypatch.setattr(bench, "TRAFFIC_PROFILE", str(tmp_path / "absent.json"))
     assert bench.measured_traffic() is None

@@ -16,7 +16,8 @@ import torch
 import fp8_transformer_gb300 as te
 from oracle import block as ob
 from oracle import numerics as nx
-from parity import ACC_REL, Guarded, assert_in_window, bf16_jump, codes, np64
+from parity import (ACC_REL, Guarded, assert_in_window, bf16_jump, codes, decode, np64,
+                    quantize_fast)
 from steps import (ACT_REL, SCALE_REL, check_dact, check_mlp_bwd, check_norm_dx,
                    check_norm_params, gemm_ref)
 from workloads import make_inputs
@@ -129,7 +130,7 @@ def _decoded_rows_matmul(t, b, chunk=2048):
     out, absout = [], []
     for r0 in range(0, t.shape[0], chunk):
         part = t[r0:r0 + chunk]
-        v = nx.e4m3_decode(codes(part)) if t.dtype == torch.uint8 else np64(part)
+        v = decode(codes(part)) if t.dtype == torch.uint8 else np64(part)
         out.append(v @ b)
         absout.append(np.abs(v) @ np.abs(b))
     return np.concatenate(out), np.concatenate(absout)
@@ -173,10 +174,10 @@ def test_mlp_backward_full_size_sampled(fp8):
     check_dact(dh_c if fp8 else dh_c.astype(np.float64), np64(g["db1"])[feats], da64, w_da,
                h_c, "gelu", q_scale=g_scale, what="dH columns")
     if fp8:
-        dh_cv = nx.e4m3_decode(dh_c)
-        ln_v = nx.e4m3_decode(codes(g["ln"]))
+        dh_cv = decode(dh_c)
+        ln_v = decode(codes(g["ln"]))
         a_w1 = float(np.float32(qs.x.scale_inv.item()) * np.float32(qs.grad.scale_inv.item()))
-        w1q = nx.e4m3_decode(nx.quantize(nx.bf16_round(w1), np.float32(qs.kernel1.scale.item())))
+        w1q = decode(quantize_fast(w1, np.float32(qs.kernel1.scale.item())))
         a_dln = float(np.float32(qs.grad.scale_inv.item()) * np.float32(qs.kernel1.scale_inv.item()))
         # the amax of dH covers at least the sampled columns' values
         pre_max = np.abs(nx.to_f32(ob.act_bwd(nx.bf16_round(da64), h_c, "gelu"))).max()
@@ -188,7 +189,7 @@ def test_mlp_backward_full_size_sampled(fp8):
     assert_in_window(np64(g["dw1"])[:, feats], dw1, w_dw1, "dW1 columns", stored="bf16")
     # rows of dx: dln of those rows from the GPU's dH
     dh_r = g["dh"][torch.as_tensor(rows, device=DEV)]
-    dh_rv = nx.e4m3_decode(codes(dh_r)) if fp8 else np64(dh_r)
+    dh_rv = decode(codes(dh_r)) if fp8 else np64(dh_r)
     dln_r, w_dln_r = gemm_ref(dh_rv, w1q.T, a_dln)
     check_norm_dx(np64(g["dx"])[rows], dln_r, w_dln_r, x[rows], mu[rows], rs[rows], gamma,
                   "layernorm", False, what="dx rows")
