@@ -448,8 +448,24 @@ int ring_slots(size_t slot_bytes, int max_slots, int min_slots, int mult) {
   return slots >= min_slots ? slots : 0;
 }
 
+// Rows ahead of its current row that a warp (or a row group) of the forward asks L2 to fetch:
+// `fallback` unless TE_NORM_FWD_PREFETCH (0 .. 8) in the environment says otherwise (a switch
+// for measurements).  The row-group kernel gains from one row ahead (its next row is already
+// loading into registers); the one-row-per-warp kernel measured no gain.
+int fwd_prefetch_rows(int fallback) {
+  static const int env = [] {
+    const char* e = getenv("TE_NORM_FWD_PREFETCH");
+    if (!e) return -1;
+    const int v = atoi(e);
+    return v < 0 ? 0 : v > 8 ? 8 : v;
+  }();
+  return env >= 0 ? env : fallback;
+}
+
 template <typename T, bool LN, int NVL, bool FULL>
-te_status launch_fwd_rows(const NormFwdArgs& a, cudaStream_t s) {
+te_status launch_fwd_rows(const NormFwdArgs& a_in, cudaStream_t s) {
+  NormFwdArgs a = a_in;
+  a.prefetch = fwd_prefetch_rows(1);
   static PerDevice<bool> attr_done;
   const size_t params = size_t(a.H) * (LN ? 2 : 1) * sizeof(float);
   const te_status st = allow_ring_smem(norm_fwd_rows_kernel<T, LN, NVL, FULL>, attr_done);
@@ -466,7 +482,9 @@ te_status launch_fwd_rows(const NormFwdArgs& a, cudaStream_t s) {
 }
 
 template <typename T, bool LN, int NVW>
-te_status launch_fwd_warp(const NormFwdArgs& a, cudaStream_t s) {
+te_status launch_fwd_warp(const NormFwdArgs& a_in, cudaStream_t s) {
+  NormFwdArgs a = a_in;
+  a.prefetch = fwd_prefetch_rows(0);
   static PerDevice<bool> attr_done;
   const size_t params = size_t(a.H) * (LN ? 2 : 1) * sizeof(float);
   const te_status st = allow_ring_smem(norm_fwd_warp_kernel<T, LN, NVW>, attr_done);
@@ -855,25 +873,11 @@ te_status launch_bwd_dispatch(const NormBwdArgs& a, cudaStream_t s) {
 
 }  // namespace
 
-// Rows ahead of its current row that each warp (or row group) of the forward asks L2 to fetch.
-// TE_NORM_FWD_PREFETCH (0 .. 8) in the environment overrides the default, for measurements.
-int fwd_prefetch_rows() {
-  static const int rows = [] {
-    const char* e = getenv("TE_NORM_FWD_PREFETCH");
-    if (!e) return 2;
-    const int v = atoi(e);
-    return v < 0 ? 0 : v > 8 ? 8 : v;
-  }();
-  return rows;
-}
-
 te_status launch_norm_fwd(const NormFwdArgs& a, cudaStream_t s) {
   if (a.M == 0) return TE_OK;
   ProfileScope prof(TE_KERNEL_NORM_FWD, s);
-  NormFwdArgs b = a;
-  b.prefetch = fwd_prefetch_rows();
-  if (b.x_dtype == TE_BF16) return launch_fwd_t<__nv_bfloat16>(b, s);
-  if (b.x_dtype == TE_F32) return launch_fwd_t<float>(b, s);
+  if (a.x_dtype == TE_BF16) return launch_fwd_t<__nv_bfloat16>(a, s);
+  if (a.x_dtype == TE_F32) return launch_fwd_t<float>(a, s);
   return TE_ERR_UNSUPPORTED;
 }
 
