@@ -427,22 +427,25 @@ def run_ours(args, rank, world, local_rank):
         if rank == 0:
             print(json.dumps(single_gemm(args, dev, peaks)), flush=True)
         return
-    inp = make_inputs(WORKLOAD, device=dev, seed=rank, M=args.tokens)
+    workload = args.workload if args.kernels_only else WORKLOAD
+    inp = make_inputs(workload, device=dev, seed=rank, M=args.tokens)
     M, H, F = inp["M"], inp["H"], inp["F"]
     gated = inp["act"] == "swiglu"
+    b1, b2 = inp.get("b1"), inp.get("b2")
     flops = mlp_flops(M, H, F, gated)
     gemm1_flops = 2.0 * M * H * (2 * F if gated else F)
     x, gamma, beta, w1, w2 = (inp[k] for k in ("x", "gamma", "beta", "w1", "w2"))
     out = torch.empty(M, H, dtype=torch.bfloat16, device=dev)
     ws = torch.empty(te.workspace_size(te.binding.TE_OP_LAYERNORM_MLP_FWD, M, H, F,
                                        te.binding.TE_BF16, True, te.binding.TE_BF16,
-                                       te.binding.TE_SWIGLU), dtype=torch.uint8, device=dev)
+                                       te.binding.ACT_TYPES[inp["act"]]), dtype=torch.uint8,
+                     device=dev)
     flush = make_flush(dev)
     common = dict(norm_type=inp["norm"], zero_centered_gamma=inp["zero_centered_gamma"],
-                  epsilon=inp["eps"], activation_type=("silu", "linear"), workspace=ws)
+                  epsilon=inp["eps"], activation_type=inp["act"], workspace=ws)
 
     def step_bf16(xx=x, oo=out):
-        te.te_layernorm_mlp_fwd(xx, gamma, beta, w1, w2, None, None, oo, **common)
+        te.te_layernorm_mlp_fwd(xx, gamma, beta, w1, w2, b1, b2, oo, **common)
 
     # FP8 steady state: weights cached in E4M3 with their own scales; x / act scales from a
     # calibration call in current-scaling mode (delayed scaling with a history of one).
@@ -453,14 +456,14 @@ def run_ours(args, rank, world, local_rank):
     te.te_quantize(w2, qw2, w2q)
     qx, qa = te.Quantizer(1.0, "current", dev), te.Quantizer(1.0, "current", dev)
     calib = te.QuantizerSet(x=qx, kernel1=qw1, act=qa, kernel2=qw2)
-    te.te_layernorm_mlp_fwd(x, gamma, beta, w1q, w2q, None, None, out, quantizer_set=calib,
+    te.te_layernorm_mlp_fwd(x, gamma, beta, w1q, w2q, b1, b2, out, quantizer_set=calib,
                             **common)
     torch.cuda.synchronize()
     qx.mode = qa.mode = te.binding.TE_SCALING_DELAYED
     qs = te.QuantizerSet(x=qx, kernel1=qw1, act=qa, kernel2=qw2)
 
     def step_fp8():
-        te.te_layernorm_mlp_fwd(x, gamma, beta, w1q, w2q, None, None, out, quantizer_set=qs,
+        te.te_layernorm_mlp_fwd(x, gamma, beta, w1q, w2q, b1, b2, out, quantizer_set=qs,
                                 **common)
 
     def barrier():
@@ -522,7 +525,7 @@ def run_ours(args, rank, world, local_rank):
     fp8_modes = {}
     for tag, wa, wb, qset in (("current_scaling", w1q, w2q, qs_cur),
                               ("weight_cast_per_call", w1, w2, qs_wcast)):
-        fn = lambda: te.te_layernorm_mlp_fwd(x, gamma, beta, wa, wb, None, None, out,
+        fn = lambda: te.te_layernorm_mlp_fwd(x, gamma, beta, wa, wb, b1, b2, out,
                                              quantizer_set=qset, **common)
         for _ in range(args.warmup):
             flush()
@@ -854,6 +857,8 @@ def main():
                     help="time the GPU steps only: no e2e, bandwidth kernels or CPU baseline")
     ap.add_argument("--bandwidth-only", action="store_true",
                     help="time only the bandwidth-bound kernels (profiling aid)")
+    ap.add_argument("--workload", default=WORKLOAD, choices=[WORKLOAD, "gpt_ln_mlp"],
+                    help="with --kernels-only: the forward workload to time (profiling aid)")
     ap.add_argument("--calibrate", action="store_true",
                     help="with --kernels-only: also time cuBLAS on the same GEMM shapes")
     ap.add_argument("--gemm", default=None, metavar="M,N,K,a_trans,b_trans",

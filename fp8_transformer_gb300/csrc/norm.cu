@@ -420,6 +420,195 @@ __global__ void __launch_bounds__(kFwdWarpRowWarps * 32, NVW * Vec16<T>::N >= 12
   if (lane == 0 && a.cast.amax_out) atomic_max_nonneg(a.cast.amax_out, amax);
 }
 
+// Forward for rows of exactly NVW x 32 vectors with the rows staged in shared memory: one CTA
+// of kFwdRingWarps warps per SM, each warp working through its own rows (rows r0, r0 + step,
+// ... with step = all warps of the grid) one at a time, its sums meeting by shuffles, while the
+// bulk copies of its next `slots - 1` rows are in flight into its own shared-memory slots.  The
+// loads in flight no longer live in registers, so every SM keeps kFwdRingWarps x slots rows
+// (about 190 KB) requested from memory at all times; each row is read from its slot twice (for
+// the sums, then for the output).  Each slot has one "full" mbarrier completed by the copy's
+// byte count; the warp that consumes a slot refills it, so no "empty" barrier is needed, and
+// every wait is bounded.
+constexpr int kFwdRingWarps = 12;
+constexpr int kFwdRingMaxSlots = 4;
+constexpr size_t kFwdRingSmemMax = 232448;  // the largest dynamic shared memory of one CTA
+
+__host__ __device__ constexpr size_t fwd_ring_header(int slots) {
+  return (size_t(kFwdRingWarps) * slots * 8 + 16 + 127) / 128 * 128;
+}
+
+template <typename T, bool LN, int NVW>
+__global__ void __launch_bounds__(kFwdRingWarps * 32, 1)
+    norm_fwd_ring_kernel(NormFwdArgs a, int* status, int slots) {
+  using PR = Pairs<T>;
+  constexpr int E = Vec16<T>::N;
+  constexpr int P = PR::P;
+  constexpr int Q = E / 4;
+  constexpr int nvec = NVW * 32;
+  constexpr uint32_t row_bytes = uint32_t(nvec) * 16u;
+  extern __shared__ __align__(128) uint8_t smem[];
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(full + kFwdRingWarps * slots);
+  float4* gain4 = reinterpret_cast<float4*>(smem + fwd_ring_header(slots));
+  float4* beta4 = gain4 + Q * nvec;
+  uint8_t* ring = reinterpret_cast<uint8_t*>(gain4 + (LN ? 2 : 1) * Q * nvec);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    for (int i = 0; i < kFwdRingWarps * slots; ++i) mbar_init(smem_u32(&full[i]), 1);
+    *abort_flag = 0;
+    mbar_init_fence();
+  }
+  {
+    const float shift = a.zero_centered_gamma ? 1.0f : 0.0f;
+    const T* g = static_cast<const T*>(a.gamma);
+    const T* b = static_cast<const T*>(a.beta);
+    float* gf = reinterpret_cast<float*>(gain4);
+    float* bf = reinterpret_cast<float*>(beta4);
+    for (int64_t j = tid; j < a.H; j += blockDim.x) {
+      const int64_t v = j / E, e = j % E;
+      const int64_t slot = ((e / 4) * nvec + v) * 4 + (e % 4);
+      gf[slot] = float(g[j]) + shift;
+      if (LN) bf[slot] = b ? float(b[j]) : 0.0f;
+    }
+  }
+  __syncthreads();  // barriers, gain / beta ready
+  const char* xb = static_cast<const char*>(a.x);
+  uint8_t* mine = ring + size_t(warp) * slots * row_bytes;
+  uint64_t* mfull = full + warp * slots;
+  const int64_t step = int64_t(gridDim.x) * kFwdRingWarps;
+  const int64_t r0 = int64_t(blockIdx.x) * kFwdRingWarps + warp;
+  // the warp's row k (row r0 + k step) goes to slot k % slots, use k / slots of that slot
+  auto issue = [&](int64_t k) {
+    const int sl = int(k % slots);
+    mbar_expect_tx(smem_u32(&mfull[sl]), row_bytes);
+    bulk_load(smem_u32(mine + size_t(sl) * row_bytes), xb + (r0 + k * step) * row_bytes,
+              row_bytes, smem_u32(&mfull[sl]));
+  };
+  if (lane == 0)
+    for (int k = 0; k < slots && r0 + k * step < a.M; ++k) issue(k);
+  const CastState cs = cast_begin(a.cast);
+  const float inv_h = 1.0f / float(a.H);
+  const bool want_amax = a.cast.amax_out != nullptr;
+  float am[P];
+#pragma unroll
+  for (int p = 0; p < P; ++p) am[p] = 0.0f;
+  int64_t k = 0;
+  bool failed = false;
+  with_out_amax(out_kind(cs), want_amax, [&](auto tag, auto atag) {
+    constexpr int OUT = decltype(tag)::value;
+    constexpr bool AMAX = decltype(atag)::value;
+    for (int64_t r = r0; r < a.M; r += step, ++k) {
+      const int sl = int(k % slots);
+      const uint32_t par = uint32_t(k / slots) & 1u;
+      const uint32_t bar = smem_u32(&mfull[sl]);
+      int ok = 1;
+      if (lane == 0 && !mbar_try_wait(bar, par))
+        ok = wait_bounded(bar, par, abort_flag, status, kWaitLimitNs, true) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) {
+        failed = true;
+        break;
+      }
+      // the phase has completed: every lane observes it before reading the slot
+      while (!mbar_try_wait(bar, par)) {
+      }
+      const uint4* row = reinterpret_cast<const uint4*>(mine + size_t(sl) * row_bytes) + lane;
+      // the row's first element, subtracted before the sums (shifted variance)
+      float x0 = 0.0f;
+      if (LN) {
+        f32x2 first[P];
+        PR::cvt(reinterpret_cast<const uint4*>(mine + size_t(sl) * row_bytes)[0], first);
+        x0 = f2lo(first[0]);
+      }
+      const f32x2 x02 = f2s(x0);
+      f32x2 s1[P], s2[P];
+#pragma unroll
+      for (int p = 0; p < P; ++p) { s1[p] = f2s(0.0f); s2[p] = f2s(0.0f); }
+#pragma unroll
+      for (int i = 0; i < NVW; ++i) {
+        f32x2 xp[P];
+        PR::cvt(row[32 * i], xp);
+#pragma unroll
+        for (int p = 0; p < P; ++p) {
+          if (LN) {
+            const f32x2 d = sub2(xp[p], x02);
+            s1[p] = add2(s1[p], d);
+            s2[p] = fma2(d, d, s2[p]);
+          } else {
+            s2[p] = fma2(xp[p], xp[p], s2[p]);
+          }
+        }
+      }
+#pragma unroll
+      for (int p = 1; p < P; ++p) { s1[0] = add2(s1[0], s1[p]); s2[0] = add2(s2[0], s2[p]); }
+      float t1 = LN ? f2lo(s1[0]) + f2hi(s1[0]) : 0.0f;
+      float t2 = f2lo(s2[0]) + f2hi(s2[0]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        if (LN) t1 += __shfl_xor_sync(0xffffffffu, t1, o);
+        t2 += __shfl_xor_sync(0xffffffffu, t2, o);
+      }
+      const float m1 = LN ? t1 * inv_h : 0.0f;
+      const float m2 = t2 * inv_h;
+      const float mean = LN ? x0 + m1 : 0.0f;
+      const float var = LN ? fmaxf(m2 - m1 * m1, 0.0f) : m2;
+      const float rs = rsqrtf(var + a.eps);
+      if (lane == 0) {
+        if (a.mu) a.mu[r] = mean;
+        if (a.rsigma) a.rsigma[r] = rs;
+      }
+      if (OUT != OUT_NONE || AMAX) {
+        const f32x2 mean2 = f2s(mean), rs2 = f2s(rs);
+        const int64_t base = r * a.H + int64_t(lane) * E;
+#pragma unroll 4
+        for (int i = 0; i < NVW; ++i) {
+          const int v = lane + 32 * i;
+          f32x2 xp[P], gp[P], bp[P];
+          PR::cvt(row[32 * i], xp);
+#pragma unroll
+          for (int q = 0; q < Q; ++q) {
+            const float4 g4 = gain4[q * nvec + v];
+            gp[2 * q] = f2(g4.x, g4.y);
+            gp[2 * q + 1] = f2(g4.z, g4.w);
+            if (LN) {
+              const float4 b4 = beta4[q * nvec + v];
+              bp[2 * q] = f2(b4.x, b4.y);
+              bp[2 * q + 1] = f2(b4.z, b4.w);
+            }
+          }
+          float y[E];
+#pragma unroll
+          for (int p = 0; p < P; ++p) {
+            const f32x2 yy = LN ? fma2(sub2(xp[p], mean2), mul2(gp[p], rs2), bp[p])
+                                : mul2(mul2(xp[p], rs2), gp[p]);
+            if (AMAX) am[p] = absmax2(am[p], yy);
+            y[2 * p] = f2lo(yy);
+            y[2 * p + 1] = f2hi(yy);
+          }
+          store_out<OUT, E>(a.out, base + int64_t(32) * E * i, y, cs);
+        }
+      }
+      // every lane has read the slot: refill it with the row `slots` ahead
+      __syncwarp();
+      if (lane == 0 && r + slots * step < a.M) {
+        fence_proxy_async_smem();
+        issue(k + slots);
+      }
+    }
+  });
+  if (failed && lane == 0) {
+    // after a failed wait, the copies this warp still has in flight land before the CTA exits
+    for (int64_t j = k; j < k + slots && r0 + j * step < a.M; ++j)
+      wait_bounded(smem_u32(&mfull[int(j % slots)]), uint32_t(j / slots) & 1u, abort_flag, status,
+                   kDrainLimitNs, false);
+  }
+  float amax = am[0];
+#pragma unroll
+  for (int p = 1; p < P; ++p) amax = fmaxf(amax, am[p]);
+  amax = warp_max(amax);
+  if (lane == 0 && a.cast.amax_out) atomic_max_nonneg(a.cast.amax_out, amax);
+}
+
 // Sets the kernel's dynamic shared memory limit once per device.
 template <typename K>
 te_status allow_ring_smem(K kernel, PerDevice<bool>& done) {
@@ -501,10 +690,52 @@ te_status launch_fwd_warp(const NormFwdArgs& a_in, cudaStream_t s) {
   return cudaGetLastError() == cudaSuccess ? TE_OK : TE_ERR_CUDA;
 }
 
+// Ring slots per warp for the staged forward: as many as fit (at most kFwdRingMaxSlots), or 0
+// when fewer than two do.
+int fwd_ring_slots(size_t row_bytes, size_t table_bytes) {
+  for (int slots = kFwdRingMaxSlots; slots >= 2; --slots)
+    if (fwd_ring_header(slots) + table_bytes + size_t(kFwdRingWarps) * slots * row_bytes <=
+        kFwdRingSmemMax)
+      return slots;
+  return 0;
+}
+
+template <typename T, bool LN, int NVW>
+te_status launch_fwd_ring(const NormFwdArgs& a, int slots, cudaStream_t s) {
+  static PerDevice<bool> attr_done;
+  bool ok = false;
+  if (!attr_done.get(&ok, [](bool* v) {
+        *v = cudaFuncSetAttribute(norm_fwd_ring_kernel<T, LN, NVW>,
+                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  int(kFwdRingSmemMax)) == cudaSuccess;
+        return *v;
+      }))
+    return TE_ERR_CUDA;
+  constexpr size_t row_bytes = size_t(NVW) * 32 * 16;
+  const size_t smem = fwd_ring_header(slots) + size_t(a.H) * (LN ? 2 : 1) * sizeof(float) +
+                      size_t(kFwdRingWarps) * slots * row_bytes;
+  const int64_t ctas = ceil_div(a.M, kFwdRingWarps);
+  const int64_t sms = num_sms();
+  const unsigned grid = unsigned(ctas < sms ? ctas : sms);
+  norm_fwd_ring_kernel<T, LN, NVW><<<grid, kFwdRingWarps * 32, smem, s>>>(a, device_status_ptr(),
+                                                                          slots);
+  return cudaGetLastError() == cudaSuccess ? TE_OK : TE_ERR_CUDA;
+}
+
+// One row per warp: rows staged in shared memory (the default), or loaded straight into
+// registers when TE_NORM_FWD_KERNEL=warp is set in the environment (a switch between two
+// complete kernels, for measurements) or when two ring slots per warp do not fit.
 template <typename T, int NVW>
 te_status launch_fwd_nvw(const NormFwdArgs& a, cudaStream_t s) {
-  return a.norm_type == TE_LAYERNORM ? launch_fwd_warp<T, true, NVW>(a, s)
-                                     : launch_fwd_warp<T, false, NVW>(a, s);
+  static const bool use_warp = [] {
+    const char* e = getenv("TE_NORM_FWD_KERNEL");
+    return e && e[0] == 'w';
+  }();
+  const bool ln = a.norm_type == TE_LAYERNORM;
+  const int slots = fwd_ring_slots(size_t(NVW) * 32 * 16, size_t(a.H) * (ln ? 2 : 1) * 4);
+  if (!use_warp && slots >= 2)
+    return ln ? launch_fwd_ring<T, true, NVW>(a, slots, s) : launch_fwd_ring<T, false, NVW>(a, slots, s);
+  return ln ? launch_fwd_warp<T, true, NVW>(a, s) : launch_fwd_warp<T, false, NVW>(a, s);
 }
 
 template <typename T, int NVL>

@@ -56,11 +56,20 @@ def xhat_err(x, mu, rs, norm):
     return NORM_REL * (np.abs(x) + m) * rs[:, None]
 
 
-def check_norm_dx(g_dx, dln64, w_dln, x, mu, rs, gamma, norm, zc, what="dx", stored="bf16"):
-    """dx of whole rows against the oracle's norm backward of bf16(dln64), where the GPU's dln
-    may sit one bf16 step away wherever dln64 +- w_dln straddles a midpoint."""
-    J = bf16_jump(dln64, w_dln)
-    dln = nx.bf16_round(dln64)
+def _stored_dln(dln64, w_dln, dln_dtype):
+    """The upstream gradient as the norm backward reads it, and how far the GPU's copy may sit
+    from it: a bf16 GEMM output may be one bf16 step away wherever dln64 +- w_dln straddles a
+    midpoint; an input given in fp32 (or bf16) is identical on both sides."""
+    if dln_dtype == "gemm_bf16":
+        return nx.bf16_round(dln64), bf16_jump(dln64, w_dln)
+    return np.asarray(dln64, np.float64), np.zeros(np.shape(dln64))
+
+
+def check_norm_dx(g_dx, dln64, w_dln, x, mu, rs, gamma, norm, zc, what="dx", stored="bf16",
+                  dln_dtype="gemm_bf16"):
+    """dx of whole rows against the oracle's norm backward of the upstream gradient (see
+    _stored_dln), stored as ``stored``."""
+    dln, J = _stored_dln(dln64, w_dln, dln_dtype)
     dx, _, _ = ob.norm_bwd(dln, x, mu, rs, gamma, norm, zc)
     g = ob.applied_gain(gamma, zc)[None, :]
     xh = xhat_of(x, mu, rs, norm)
@@ -85,11 +94,11 @@ def check_norm_dx(g_dx, dln64, w_dln, x, mu, rs, gamma, norm, zc, what="dx", sto
         assert not bad.any(), f"{what}: {int(bad.sum())} of {bad.size} outside the window"
 
 
-def check_norm_params(g_dgamma, g_dbeta, dln64, w_dln, x, mu, rs, norm, what="norm"):
+def check_norm_params(g_dgamma, g_dbeta, dln64, w_dln, x, mu, rs, norm, what="norm",
+                      dln_dtype="gemm_bf16"):
     """dgamma = sum_i dln * xhat and dbeta = sum_i dln over all rows, for the columns given
     (x, dln64, w_dln hold those columns of every row)."""
-    J = bf16_jump(dln64, w_dln)
-    dln = nx.bf16_round(dln64)
+    dln, J = _stored_dln(dln64, w_dln, dln_dtype)
     xh = xhat_of(x, mu, rs, norm)
     xerr = xhat_err(x, mu, rs, norm)
     assert_in_window(g_dgamma, (dln * xh).sum(axis=0),

@@ -345,8 +345,10 @@ def test_norm_bwd(norm, M, H, dtype):
     # identical inputs: dx within the fp32 window of the norm backward's arithmetic, the column
     # sums to the 1e-4 reduction rule plus that window
     args = (np64(x), np64(mu_t), np64(rs_t))
-    check_norm_dx(dx, np64(dz), 0.0, *args, np64(gamma), norm, False, stored=dtype)
-    check_norm_params(dg, db if norm == "layernorm" else None, np64(dz), 0.0, *args, norm)
+    check_norm_dx(dx, np64(dz), 0.0, *args, np64(gamma), norm, False, stored=dtype,
+                  dln_dtype=dtype)
+    check_norm_params(dg, db if norm == "layernorm" else None, np64(dz), 0.0, *args, norm,
+                      dln_dtype=dtype)
 
 
 def test_norm_bwd_large_mean():
@@ -364,8 +366,8 @@ def test_norm_bwd_large_mean():
     db = torch.empty(H, dtype=torch.float32, device=DEV)
     te.te_norm_bwd(dz, x, mu_t, rs_t, gamma, "layernorm", False, dx, dg, db)
     args = (np64(x), np64(mu_t), np64(rs_t))
-    check_norm_dx(dx, np64(dz), 0.0, *args, np64(gamma), "layernorm", False)
-    check_norm_params(dg, db, np64(dz), 0.0, *args, "layernorm")
+    check_norm_dx(dx, np64(dz), 0.0, *args, np64(gamma), "layernorm", False, dln_dtype="bf16")
+    check_norm_params(dg, db, np64(dz), 0.0, *args, "layernorm", dln_dtype="bf16")
 
 
 # ------------------------------------------------------------------ GEMM -------------------
