@@ -291,6 +291,60 @@ __device__ __forceinline__ f32x2 load_bias_pair(const void* bias, int dtype, int
   return f2(w.x, w.y);
 }
 
+// The bias of columns col0 .. col0 + 31 as fp32 pairs (zero past `count`, or without a bias).
+__device__ __forceinline__ void load_bias_chunk(const void* bias, int dtype, int64_t col0,
+                                                int count, f32x2 (&b)[16]) {
+#pragma unroll
+  for (int p = 0; p < 16; ++p)
+    b[p] = (bias && 2 * p < count) ? load_bias_pair(bias, dtype, col0 + 2 * p) : f2s(0.0f);
+}
+
+// The activation applied to a chunk of 32 values, one inner loop per activation (a switch
+// per chunk, none per element, so that the compiler interleaves the 16 independent pairs).
+template <int ACT>
+__device__ __forceinline__ void act_chunk_t(float (&v)[32]) {
+#pragma unroll
+  for (int p = 0; p < 16; ++p) {
+    const f32x2 y = act2c<ACT>(f2(v[2 * p], v[2 * p + 1]));
+    v[2 * p] = f2lo(y);
+    v[2 * p + 1] = f2hi(y);
+  }
+}
+__device__ __forceinline__ void act_chunk(int act, float (&v)[32]) {
+  switch (act) {
+    case TE_RELU: act_chunk_t<TE_RELU>(v); break;
+    case TE_GELU: act_chunk_t<TE_GELU>(v); break;
+    case TE_SILU: act_chunk_t<TE_SILU>(v); break;
+    default: break;
+  }
+}
+
+// A gated pair's output base(gate) * linear into vg, the base function a compile-time choice.
+template <int ACT>
+__device__ __forceinline__ void gated_chunk_t(float (&vg)[32], const float (&vl)[32]) {
+#pragma unroll
+  for (int p = 0; p < 16; ++p) {
+    const f32x2 y = mul2(act2c<ACT>(f2(vg[2 * p], vg[2 * p + 1])), f2(vl[2 * p], vl[2 * p + 1]));
+    vg[2 * p] = f2lo(y);
+    vg[2 * p + 1] = f2hi(y);
+  }
+}
+__device__ __forceinline__ void gated_chunk(int base_act, float (&vg)[32], const float (&vl)[32]) {
+  switch (base_act) {
+    case TE_RELU: gated_chunk_t<TE_RELU>(vg, vl); break;
+    case TE_GELU: gated_chunk_t<TE_GELU>(vg, vl); break;
+    default: gated_chunk_t<TE_SILU>(vg, vl); break;
+  }
+}
+
+// Running max of |v| over the first `count` values of a chunk.
+__device__ __forceinline__ float chunk_amax(float m, const float (&v)[32], int count) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i)
+    if (i < count) m = fmaxf(m, fabsf(v[i]));
+  return m;
+}
+
 // Rounds both halves of a pair to bf16 (round to nearest even) and back to fp32.
 __device__ __forceinline__ f32x2 round_bf16_2(f32x2 v) {
   return bf16x2_f2(pack_bf16x2(f2lo(v), f2hi(v)));
@@ -521,29 +575,23 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           const int count = g.N - col0 >= 32 ? 32 : int(g.N - col0);
           uint32_t r[32];
           tmem_ld32(taddr + c * 32, r);
+          f32x2 bz[16];  // the chunk's bias, loaded while the accumulator columns arrive
+          load_bias_chunk(g.bias, g.bias_dtype, col0, count, bz);
           tmem_ld_wait();
           float v[32];
 #pragma unroll
           for (int p = 0; p < 16; ++p) {
-            f32x2 x = mul2(f2(__uint_as_float(r[2 * p]), __uint_as_float(r[2 * p + 1])), alpha2);
-            if (g.bias && 2 * p < count) x = add2(x, load_bias_pair(g.bias, g.bias_dtype, col0 + 2 * p));
+            f32x2 x = fma2(f2(__uint_as_float(r[2 * p]), __uint_as_float(r[2 * p + 1])), alpha2, bz[p]);
             if (g.epilogue == EPI_BIAS_ACT && round_h) x = round_bf16_2(x);
             v[2 * p] = f2lo(x);
             v[2 * p + 1] = f2hi(x);
           }
           if (g.epilogue == EPI_BIAS_ACT) {
             if (g.saved_h && row_ok) store_seg(g.saved_h, row * g.N + col0, v, count, g.h_dtype, 1.0f);
-#pragma unroll
-            for (int p = 0; p < 16; ++p) {
-              const f32x2 y = act2(g.act, f2(v[2 * p], v[2 * p + 1]));
-              v[2 * p] = f2lo(y);
-              v[2 * p + 1] = f2hi(y);
-            }
+            act_chunk(g.act, v);
           }
           if (row_ok) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (i < count) amax = fmaxf(amax, fabsf(v[i]));
+            amax = chunk_amax(amax, v, count);
             store_seg(g.D, row * ldd + col0, v, count, g.d_dtype, out_scale);
           }
         }
@@ -558,16 +606,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           uint32_t rg[32], rl[32];
           tmem_ld32(taddr + c * 32, rg);
           tmem_ld32(taddr + BN / 2 + c * 32, rl);
+          f32x2 bg[16], bl[16];
+          load_bias_chunk(g.bias, g.bias_dtype, col0, count, bg);
+          load_bias_chunk(g.bias, g.bias_dtype, g.F + col0, count, bl);
           tmem_ld_wait();
           float vg[32], vl[32];
 #pragma unroll
           for (int p = 0; p < 16; ++p) {
-            f32x2 xg = mul2(f2(__uint_as_float(rg[2 * p]), __uint_as_float(rg[2 * p + 1])), alpha2);
-            f32x2 xl = mul2(f2(__uint_as_float(rl[2 * p]), __uint_as_float(rl[2 * p + 1])), alpha2);
-            if (g.bias && 2 * p < count) {
-              xg = add2(xg, load_bias_pair(g.bias, g.bias_dtype, col0 + 2 * p));
-              xl = add2(xl, load_bias_pair(g.bias, g.bias_dtype, g.F + col0 + 2 * p));
-            }
+            f32x2 xg = fma2(f2(__uint_as_float(rg[2 * p]), __uint_as_float(rg[2 * p + 1])), alpha2, bg[p]);
+            f32x2 xl = fma2(f2(__uint_as_float(rl[2 * p]), __uint_as_float(rl[2 * p + 1])), alpha2, bl[p]);
             if (round_h) {
               xg = round_bf16_2(xg);
               xl = round_bf16_2(xl);
@@ -581,25 +628,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             store_seg(g.saved_h, row * g.N + col0, vg, count, g.h_dtype, 1.0f);
             store_seg(g.saved_h, row * g.N + g.F + col0, vl, count, g.h_dtype, 1.0f);
           }
-          if (gact == TE_SILU) {  // ("silu", "linear"): its own loop, without the switch
-#pragma unroll
-            for (int p = 0; p < 16; ++p) {
-              const f32x2 y = mul2(silu2(f2(vg[2 * p], vg[2 * p + 1])), f2(vl[2 * p], vl[2 * p + 1]));
-              vg[2 * p] = f2lo(y);
-              vg[2 * p + 1] = f2hi(y);
-            }
-          } else {
-#pragma unroll
-            for (int p = 0; p < 16; ++p) {
-              const f32x2 y = mul2(act2(gact, f2(vg[2 * p], vg[2 * p + 1])), f2(vl[2 * p], vl[2 * p + 1]));
-              vg[2 * p] = f2lo(y);
-              vg[2 * p + 1] = f2hi(y);
-            }
-          }
+          gated_chunk(gact, vg, vl);
           if (row_ok) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (i < count) amax = fmaxf(amax, fabsf(vg[i]));
+            amax = chunk_amax(amax, vg, count);
             store_seg(g.D, row * ldd + col0, vg, count, g.d_dtype, out_scale);
           }
         }
