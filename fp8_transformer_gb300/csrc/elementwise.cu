@@ -143,6 +143,8 @@ __global__ void __launch_bounds__(kDactWarps * 32, is_gated(ACT) ? 2 : 3)
   // twice as many rows keep as many bytes in flight
   constexpr int U = kIdent ? 2 * kDactUnroll : kDactUnroll;
   __shared__ float red[kDactWarps][2][W];
+  // the column-sum kernel that follows may launch now: it waits for this grid's completion
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const CastState cs = cast_begin(a.cast);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t n_out = kGated ? a.N_in / 2 : a.N_in;
@@ -266,6 +268,8 @@ constexpr int kColsumWarps = 16;
 __global__ void __launch_bounds__(kColsumWarps * 32)
     colsum_partials_kernel(const float* partials, int chunks, int64_t n, float* out) {
   __shared__ float4 sums[kColsumWarps][32];
+  // launched as a programmatic dependent of the dact kernel: wait for that grid's partials
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int64_t j = int64_t(blockIdx.x) * 128 + lane * 4;
   float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
@@ -365,9 +369,9 @@ te_status launch_dact_dbias(const DactArgs& a, cudaStream_t s) {
                  : a.dtype == TE_F32 ? launch_dact_t<float>(a, grid, s)
                                      : TE_ERR_UNSUPPORTED;
   if (st != TE_OK || !a.dbias) return st;
-  colsum_partials_kernel<<<unsigned(ceil_div(a.N_in, 128)), kColsumWarps * 32, 0, s>>>(
-      a.partials, chunks, a.N_in, a.dbias);
-  return cudaGetLastError() == cudaSuccess ? TE_OK : TE_ERR_CUDA;
+  return launch_dependent(colsum_partials_kernel, dim3(unsigned(ceil_div(a.N_in, 128))),
+                          dim3(kColsumWarps * 32), s, static_cast<const float*>(a.partials),
+                          chunks, int64_t(a.N_in), a.dbias);
 }
 
 te_status launch_transpose_f32(const float* src, int64_t R, int64_t C, float* dst, cudaStream_t s) {

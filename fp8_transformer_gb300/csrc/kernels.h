@@ -6,6 +6,7 @@
 #include <stdint.h>
 
 #include <mutex>
+#include <utility>
 
 #include "te_gb300.h"
 
@@ -145,6 +146,27 @@ int* device_status_ptr();
 te_status read_and_clear_device_status(int32_t* out);
 
 int num_sms();
+
+// Launches `kernel` as a programmatic dependent of the work queued before it on `s`: its launch
+// may overlap the previous kernel's tail once every CTA of that kernel has executed
+// griddepcontrol.launch_dependents (or exited), and the kernel itself executes
+// griddepcontrol.wait before it reads anything the previous kernel wrote.
+template <typename... KArgs, typename... Args>
+te_status launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, cudaStream_t s,
+                           Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...) == cudaSuccess ? TE_OK
+                                                                                     : TE_ERR_CUDA;
+}
 
 // A value set up once per device and shared by every host thread: get() runs make(&value) for
 // the current device the first time (make returns false on failure, and is then retried on the

@@ -321,15 +321,7 @@ __global__ void __launch_bounds__(kFwdWarpRowWarps * 32, NVW * Vec16<T>::N >= 12
     constexpr int OUT = decltype(tag)::value;
     constexpr bool AMAX = decltype(atag)::value;
     const int64_t step = int64_t(gridDim.x) * kFwdWarpRowWarps;
-    const int64_t r0 = int64_t(blockIdx.x) * kFwdWarpRowWarps + warp;
-    const uint32_t row_bytes = uint32_t(a.H) * uint32_t(sizeof(T));
-    // rows r0 + step .. r0 + (prefetch - 1) step now; row r + prefetch step with row r below
-    if (lane == 0)
-      for (int k = 1; k < a.prefetch && r0 + k * step < a.M; ++k)
-        bulk_prefetch_l2(x + (r0 + k * step) * a.H, row_bytes);
-    for (int64_t r = r0; r < a.M; r += step) {
-      if (lane == 0 && a.prefetch > 0 && r + a.prefetch * step < a.M)
-        bulk_prefetch_l2(x + (r + a.prefetch * step) * a.H, row_bytes);
+    for (int64_t r = int64_t(blockIdx.x) * kFwdWarpRowWarps + warp; r < a.M; r += step) {
       const uint4* xr = reinterpret_cast<const uint4*>(x + r * a.H) + lane;
       uint4 cur[NVW];
 #pragma unroll
@@ -453,10 +445,27 @@ __global__ void __launch_bounds__(kFwdRingWarps * 32, 1)
   float4* beta4 = gain4 + Q * nvec;
   uint8_t* ring = reinterpret_cast<uint8_t*>(gain4 + (LN ? 2 : 1) * Q * nvec);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const char* xb = static_cast<const char*>(a.x);
+  const int64_t step = int64_t(gridDim.x) * kFwdRingWarps;
+  // warp w's row k (row w0 + k step, w0 = blockIdx.x * kFwdRingWarps + w) goes to its slot
+  // k % slots, use k / slots of that slot
+  auto issue = [&](int w, int64_t k) {
+    const int64_t row = int64_t(blockIdx.x) * kFwdRingWarps + w + k * step;
+    const int sl = int(k % slots);
+    uint64_t* bar = full + w * slots + sl;
+    mbar_expect_tx(smem_u32(bar), row_bytes);
+    bulk_load(smem_u32(ring + (size_t(w) * slots + sl) * row_bytes), xb + row * row_bytes,
+              row_bytes, smem_u32(bar));
+  };
   if (tid == 0) {
     for (int i = 0; i < kFwdRingWarps * slots; ++i) mbar_init(smem_u32(&full[i]), 1);
     *abort_flag = 0;
     mbar_init_fence();
+    // every warp's first rows are requested before the gain table is built, so that the table's
+    // loads overlap the rows' instead of preceding them
+    for (int w = 0; w < kFwdRingWarps; ++w)
+      for (int k = 0; k < slots && int64_t(blockIdx.x) * kFwdRingWarps + w + k * step < a.M; ++k)
+        issue(w, k);
   }
   {
     const float shift = a.zero_centered_gamma ? 1.0f : 0.0f;
@@ -472,20 +481,9 @@ __global__ void __launch_bounds__(kFwdRingWarps * 32, 1)
     }
   }
   __syncthreads();  // barriers, gain / beta ready
-  const char* xb = static_cast<const char*>(a.x);
   uint8_t* mine = ring + size_t(warp) * slots * row_bytes;
   uint64_t* mfull = full + warp * slots;
-  const int64_t step = int64_t(gridDim.x) * kFwdRingWarps;
   const int64_t r0 = int64_t(blockIdx.x) * kFwdRingWarps + warp;
-  // the warp's row k (row r0 + k step) goes to slot k % slots, use k / slots of that slot
-  auto issue = [&](int64_t k) {
-    const int sl = int(k % slots);
-    mbar_expect_tx(smem_u32(&mfull[sl]), row_bytes);
-    bulk_load(smem_u32(mine + size_t(sl) * row_bytes), xb + (r0 + k * step) * row_bytes,
-              row_bytes, smem_u32(&mfull[sl]));
-  };
-  if (lane == 0)
-    for (int k = 0; k < slots && r0 + k * step < a.M; ++k) issue(k);
   const CastState cs = cast_begin(a.cast);
   const float inv_h = 1.0f / float(a.H);
   const bool want_amax = a.cast.amax_out != nullptr;
@@ -513,12 +511,22 @@ __global__ void __launch_bounds__(kFwdRingWarps * 32, 1)
       while (!mbar_try_wait(bar, par)) {
       }
       const uint4* row = reinterpret_cast<const uint4*>(mine + size_t(sl) * row_bytes) + lane;
+      uint4 cur[NVW];
+#pragma unroll
+      for (int i = 0; i < NVW; ++i) cur[i] = row[32 * i];
       // the row's first element, subtracted before the sums (shifted variance)
       float x0 = 0.0f;
       if (LN) {
         f32x2 first[P];
         PR::cvt(reinterpret_cast<const uint4*>(mine + size_t(sl) * row_bytes)[0], first);
         x0 = f2lo(first[0]);
+      }
+      // the row is in registers: every lane has read the slot, which is refilled with the row
+      // `slots` ahead before this row's arithmetic
+      __syncwarp();
+      if (lane == 0 && r + slots * step < a.M) {
+        fence_proxy_async_smem();
+        issue(warp, k + slots);
       }
       const f32x2 x02 = f2s(x0);
       f32x2 s1[P], s2[P];
@@ -527,7 +535,7 @@ __global__ void __launch_bounds__(kFwdRingWarps * 32, 1)
 #pragma unroll
       for (int i = 0; i < NVW; ++i) {
         f32x2 xp[P];
-        PR::cvt(row[32 * i], xp);
+        PR::cvt(cur[i], xp);
 #pragma unroll
         for (int p = 0; p < P; ++p) {
           if (LN) {
@@ -560,11 +568,11 @@ __global__ void __launch_bounds__(kFwdRingWarps * 32, 1)
       if (OUT != OUT_NONE || AMAX) {
         const f32x2 mean2 = f2s(mean), rs2 = f2s(rs);
         const int64_t base = r * a.H + int64_t(lane) * E;
-#pragma unroll 4
+#pragma unroll
         for (int i = 0; i < NVW; ++i) {
           const int v = lane + 32 * i;
           f32x2 xp[P], gp[P], bp[P];
-          PR::cvt(row[32 * i], xp);
+          PR::get(cur[i], xp);  // converted again here rather than kept from the sums
 #pragma unroll
           for (int q = 0; q < Q; ++q) {
             const float4 g4 = gain4[q * nvec + v];
@@ -586,13 +594,9 @@ __global__ void __launch_bounds__(kFwdRingWarps * 32, 1)
             y[2 * p + 1] = f2hi(yy);
           }
           store_out<OUT, E>(a.out, base + int64_t(32) * E * i, y, cs);
+          // one vector's gain / beta loads at a time: hoisting all of them spills
+          asm volatile("" ::: "memory");
         }
-      }
-      // every lane has read the slot: refill it with the row `slots` ahead
-      __syncwarp();
-      if (lane == 0 && r + slots * step < a.M) {
-        fence_proxy_async_smem();
-        issue(k + slots);
       }
     }
   });
@@ -671,9 +675,7 @@ te_status launch_fwd_rows(const NormFwdArgs& a_in, cudaStream_t s) {
 }
 
 template <typename T, bool LN, int NVW>
-te_status launch_fwd_warp(const NormFwdArgs& a_in, cudaStream_t s) {
-  NormFwdArgs a = a_in;
-  a.prefetch = fwd_prefetch_rows(0);
+te_status launch_fwd_warp(const NormFwdArgs& a, cudaStream_t s) {
   static PerDevice<bool> attr_done;
   const size_t params = size_t(a.H) * (LN ? 2 : 1) * sizeof(float);
   const te_status st = allow_ring_smem(norm_fwd_warp_kernel<T, LN, NVW>, attr_done);
@@ -722,18 +724,26 @@ te_status launch_fwd_ring(const NormFwdArgs& a, int slots, cudaStream_t s) {
   return cudaGetLastError() == cudaSuccess ? TE_OK : TE_ERR_CUDA;
 }
 
-// One row per warp: rows staged in shared memory (the default), or loaded straight into
-// registers when TE_NORM_FWD_KERNEL=warp is set in the environment (a switch between two
-// complete kernels, for measurements) or when two ring slots per warp do not fit.
+// One row per warp.  Rows of 16 vectors per lane are staged in shared memory when every warp
+// of the grid gets at least kFwdRingMinRows of them: the staged kernel streams faster but starts
+// slower (measured on 4096-wide bf16 rows: 85% against 82% of the copy bandwidth at 16384 rows,
+// 75% against 80% at 8192 rows; slower at every shorter width).  Other rows are loaded straight
+// into registers.  TE_NORM_FWD_KERNEL=warp or =ring in the environment forces one kernel (a
+// switch between two complete kernels, for measurements); a row too long for two ring slots per
+// warp always takes the register kernel.
+constexpr int64_t kFwdRingMinRows = 6;
+
 template <typename T, int NVW>
 te_status launch_fwd_nvw(const NormFwdArgs& a, cudaStream_t s) {
-  static const bool use_warp = [] {
+  static const int forced = [] {
     const char* e = getenv("TE_NORM_FWD_KERNEL");
-    return e && e[0] == 'w';
+    return !e ? 0 : e[0] == 'w' ? 1 : e[0] == 'r' ? 2 : 0;
   }();
   const bool ln = a.norm_type == TE_LAYERNORM;
   const int slots = fwd_ring_slots(size_t(NVW) * 32 * 16, size_t(a.H) * (ln ? 2 : 1) * 4);
-  if (!use_warp && slots >= 2)
+  const bool long_run = a.M >= kFwdRingMinRows * kFwdRingWarps * num_sms();
+  const bool ring = forced == 2 || (forced == 0 && NVW == 16 && long_run);
+  if (ring && slots >= 2)
     return ln ? launch_fwd_ring<T, true, NVW>(a, slots, s) : launch_fwd_ring<T, false, NVW>(a, slots, s);
   return ln ? launch_fwd_warp<T, true, NVW>(a, s) : launch_fwd_warp<T, false, NVW>(a, s);
 }
@@ -815,6 +825,8 @@ __global__ void __launch_bounds__(kBwdWarps * 32, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x < spc) last_use[threadIdx.x] = -1;
   ring_init(full, empty, spc, G, abort_flag);
+  // the column-sum kernel that follows may launch now: it waits for this grid's completion
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (threadIdx.x == 0) {  // the first use of every slot (the barriers' init is fenced)
     for (int k = 0; k < spc && k < nloc; ++k) {
       ring_issue(xsrc, dzsrc, row_bytes, k, k, ring, full);
@@ -1027,6 +1039,9 @@ __global__ void __launch_bounds__(kRedWarps * 32) norm_bwd_reduce_kernel(const f
                                                                          float* dgamma,
                                                                          float* dbeta) {
   __shared__ float4 sg[kRedWarps][32], sb[kRedWarps][32];
+  // launched as a programmatic dependent of the ring kernel: wait here until that grid has
+  // completed and its partial sums are visible (a no-op for an ordinary launch)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int64_t j = int64_t(blockIdx.x) * 128 + lane * 4;  // H is a multiple of 8
   float4 ag = make_float4(0.0f, 0.0f, 0.0f, 0.0f), ab = ag;
@@ -1073,9 +1088,12 @@ te_status launch_bwd_t(const NormBwdArgs& a, cudaStream_t s) {
   const unsigned grid = ring_grid(a.M);
   norm_bwd_ring_kernel<T, LN, NV, FULL><<<grid, kBwdWarps * 32, smem, s>>>(
       a, device_status_ptr(), spc);
-  norm_bwd_reduce_kernel<<<unsigned(ceil_div(a.H, 128)), kRedWarps * 32, 0, s>>>(
-      a.partials, int(grid), a.H, a.dgamma, a.dbeta);
-  return cudaGetLastError() == cudaSuccess ? TE_OK : TE_ERR_CUDA;
+  if (cudaGetLastError() != cudaSuccess) return TE_ERR_CUDA;
+  // the column sums: their launch overlaps the ring kernel's tail (griddepcontrol.wait in the
+  // kernel orders them after the whole ring grid)
+  return launch_dependent(norm_bwd_reduce_kernel, dim3(unsigned(ceil_div(a.H, 128))),
+                          dim3(kRedWarps * 32), s, static_cast<const float*>(a.partials),
+                          int(grid), int64_t(a.H), a.dgamma, a.dbeta);
 }
 
 template <typename T, int NV>
