@@ -289,6 +289,37 @@ def test_norm_fwd(norm, M, H, dtype, zc):
     assert abs(q.amax.item() - nx.amax_of(nx.to_f32(y))) <= 1e-5 * nx.amax_of(nx.to_f32(y))
 
 
+@pytest.mark.parametrize("norm,zc", [("layernorm", False), ("rmsnorm", True)])
+@pytest.mark.parametrize("H,dtype", [(4096, "bf16"), (2048, "f32")])
+@pytest.mark.parametrize("out_kind", ["same", "e4m3"])
+def test_norm_fwd_long_runs(norm, zc, H, dtype, out_kind):
+    """Enough rows (12000, a ragged number of rows per warp) for the staged kernel of rows of 16
+    vectors per lane: y (or its E4M3 codes), mu, rsigma and amax, with guard bands."""
+    M = 12000
+    x = rt((M, H), std=1.5, seed=51, dtype=dtype, mean=0.25)
+    gamma = rt((H,), std=0.1, seed=52, dtype=dtype, mean=0.0 if zc else 1.0)
+    beta = rt((H,), std=0.1, seed=53, dtype=dtype)
+    odt = torch.uint8 if out_kind == "e4m3" else TDT[dtype]
+    gout, gmu, grs = Guarded((M, H), odt), Guarded((M,), torch.float32), Guarded((M,), torch.float32)
+    q = te.Quantizer(scale=16.0)
+    te.te_norm_fwd(x, gamma, beta, norm, zc, 1e-5, gout.t, q=q, mu=gmu.t, rsigma=grs.t)
+    for gb, name in ((gout, "y"), (gmu, "mu"), (grs, "rsigma")):
+        gb.check(name)
+    y, m_ref, r_ref = ob.norm_fwd(np64(x), np64(gamma), np64(beta), norm, zc, 1e-5)
+    pre = nx.to_f32(y)
+    if out_kind == "e4m3":
+        assert_e4m3_codes(gout.t, nx.quantize(pre, np.float32(16.0)), pre32=pre,
+                          scale=np.float32(16.0), rel=1e-5, abs_tol=1e-5 * rms(pre),
+                          what="norm e4m3")
+    else:
+        want = pre if dtype == "f32" else nx.bf16_round(pre)
+        assert_elementwise_close(gout.t, want, what=f"{norm} y")
+    assert_reduction_close(grs.t, r_ref, what="rsigma")
+    if norm == "layernorm":
+        assert_reduction_close(gmu.t, m_ref, what="mu")
+    assert abs(q.amax.item() - nx.amax_of(pre)) <= 1e-5 * nx.amax_of(pre)
+
+
 @pytest.mark.parametrize("mode", ["delayed", "current"])
 def test_norm_fwd_e4m3(mode):
     M, H = 1000, 4096
