@@ -34,6 +34,8 @@ unsigned ew_grid(int64_t vectors) {
 
 template <typename T>
 __global__ void __launch_bounds__(kEwThreads) quantize_kernel(QuantizeArgs a) {
+  // the kernel after this one may launch its setup now (it waits for this grid's completion)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   using V = Vec16<T>;
   constexpr int E = V::N;
   const CastState cs = cast_begin(a.cast);
@@ -61,6 +63,8 @@ constexpr int kActUnroll = 4;   // rows in flight per warp
 
 template <typename T, int ACT>
 __global__ void __launch_bounds__(kActWarps * 32, 3) act_lu_kernel(ActArgs a) {
+  // the kernel after this one may launch its setup now (it waits for this grid's completion)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   using PR = Pairs<T>;
   constexpr int E = Vec16<T>::N;
   constexpr bool kGated = is_gated(ACT);

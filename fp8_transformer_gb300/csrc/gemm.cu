@@ -364,6 +364,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   constexpr int MMA_K = MMA_K_BYTES / Kind<KIND>::esize;
   constexpr uint32_t IDESC = instr_desc<KIND, CG>(A_KMAJOR ? 0 : 1, B_KMAJOR ? 0 : 1);
   const GemmDev& g = p.g;
+  // the kernel after this one may launch its setup now (it waits for this grid's completion)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -410,6 +412,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   if constexpr (CG == 2) cluster_sync();  // the peer's barriers exist before anyone signals them
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // Launched as a programmatic dependent of the kernel before it: the setup above overlapped
+  // that kernel's tail; nothing it writes (the A operand, the scales) is read before this wait.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   if (warp == 0) {
     // ----------------------------------------------------------- TMA producer -----------
@@ -667,23 +672,23 @@ te_status launch_t(GemmParams& prm, int grid, cudaStream_t s) {
         return *v;
       }))
     return TE_ERR_CUDA;
-  if constexpr (CG == 1) {
-    gemm_kernel<KIND, AK, BK, 1><<<grid, kThreads, smem, s>>>(prm);
-  } else {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(unsigned(grid));
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, gemm_kernel<KIND, AK, BK, 2>, prm) != cudaSuccess) return TE_ERR_CUDA;
-  }
+  // a programmatic dependent launch (the kernel waits for its predecessor after its setup),
+  // in clusters of two CTAs for the SM-pair form
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(grid));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = CG;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = CG == 1 ? 1 : 2;
+  if (cudaLaunchKernelEx(&cfg, gemm_kernel<KIND, AK, BK, CG>, prm) != cudaSuccess) return TE_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? TE_OK : TE_ERR_CUDA;
 }
 

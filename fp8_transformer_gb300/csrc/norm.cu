@@ -115,6 +115,8 @@ __device__ __forceinline__ bool ring_acquire(uint64_t* full, int s, uint32_t use
 template <typename T, bool LN, int NVL, bool FULL>
 __global__ void __launch_bounds__(kFwdGroupWarps * 32, NVL >= 8 ? kFwdRowsCtasPerSm / 2 : kFwdRowsCtasPerSm)
     norm_fwd_rows_kernel(NormFwdArgs a) {
+  // the kernel after this one may launch its setup now (it waits for this grid's completion)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   using PR = Pairs<T>;
   constexpr int E = Vec16<T>::N;
   constexpr int P = PR::P;
@@ -287,6 +289,8 @@ constexpr int kFwdWarpRowWarps = 4;
 template <typename T, bool LN, int NVW>
 __global__ void __launch_bounds__(kFwdWarpRowWarps * 32, NVW * Vec16<T>::N >= 128 ? 3 : 4)
     norm_fwd_warp_kernel(NormFwdArgs a) {
+  // the kernel after this one may launch its setup now (it waits for this grid's completion)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   using PR = Pairs<T>;
   constexpr int E = Vec16<T>::N;
   constexpr int P = PR::P;
@@ -432,6 +436,8 @@ __host__ __device__ constexpr size_t fwd_ring_header(int slots) {
 template <typename T, bool LN, int NVW>
 __global__ void __launch_bounds__(kFwdRingWarps * 32, 1)
     norm_fwd_ring_kernel(NormFwdArgs a, int* status, int slots) {
+  // the kernel after this one may launch its setup now (it waits for this grid's completion)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   using PR = Pairs<T>;
   constexpr int E = Vec16<T>::N;
   constexpr int P = PR::P;
