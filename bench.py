@@ -326,6 +326,19 @@ def bandwidth_kernels(args, dev, peaks):
     run("norm_fwd_e4m3", lambda: te.te_norm_fwd(x, g, b, "rmsnorm", True, 1e-6, y8, q=q, mu=mu,
                                                 rsigma=rs), M * H * 3 + M * 8)
     del x, y, y8, mu, rs
+    # the GPT workload's LayerNorm (16384 rows: the staged ring kernel)
+    xg = random_tensor((Mb, H), device=dev, seed=7)
+    gg = random_tensor((H,), std=0.1, mean=1.0, device=dev, seed=8)
+    bg = random_tensor((H,), std=0.1, device=dev, seed=9)
+    yg = torch.empty(Mb, H, dtype=torch.bfloat16, device=dev)
+    yg8 = torch.empty(Mb, H, dtype=torch.uint8, device=dev)
+    mug = torch.empty(Mb, dtype=torch.float32, device=dev)
+    rsg = torch.empty(Mb, dtype=torch.float32, device=dev)
+    run("norm_fwd_gpt_bf16", lambda: te.te_norm_fwd(xg, gg, bg, "layernorm", False, 1e-6, yg,
+                                                    mu=mug, rsigma=rsg), Mb * H * 4 + Mb * 8)
+    run("norm_fwd_gpt_e4m3", lambda: te.te_norm_fwd(xg, gg, bg, "layernorm", False, 1e-6, yg8,
+                                                    q=q, mu=mug, rsigma=rsg), Mb * H * 3 + Mb * 8)
+    del xg, yg, yg8, mug, rsg
     h = random_tensor((Mb, F), std=2.0, device=dev, seed=3)
     da = random_tensor((Mb, F), device=dev, seed=4)
     a = torch.empty(Mb, F, dtype=torch.bfloat16, device=dev)
