@@ -186,6 +186,14 @@ class Quantizer:
         self.amax = torch.zeros(1, dtype=torch.float32, device=device)
         self.mode = TE_SCALING_CURRENT if mode == "current" else TE_SCALING_DELAYED
 
+    @classmethod
+    def from_tensors(cls, scale, scale_inv, amax, mode="delayed"):
+        """A quantizer over caller-owned one-element fp32 tensors (e.g. views into a bank)."""
+        q = cls.__new__(cls)
+        q.scale, q.scale_inv, q.amax = scale, scale_inv, amax
+        q.mode = TE_SCALING_CURRENT if mode == "current" else TE_SCALING_DELAYED
+        return q
+
     def c(self) -> _Quantizer:
         return _Quantizer(self.scale.data_ptr(), self.scale_inv.data_ptr(), self.amax.data_ptr(),
                           self.mode)

@@ -796,6 +796,10 @@ te_status te_layernorm_mlp_bwd(const void* dy, const void* x, const void* gamma,
   nb.dgamma = dgamma;
   nb.dbeta = norm_type == TE_LAYERNORM ? dbeta : nullptr;
   nb.partials = partials;
+  // RMSNorm has no shift: the gradient of an (ignored) beta is zero
+  if (norm_type == TE_RMSNORM && dbeta &&
+      cudaMemsetAsync(dbeta, 0, size_t(H) * sizeof(float), s) != cudaSuccess)
+    return TE_ERR_CUDA;
   return launch_norm_bwd(nb, s);
 }
 
@@ -933,6 +937,10 @@ te_status te_layernorm_dense_bwd(const void* dy, const void* x, const void* gamm
   nb.dgamma = dgamma;
   nb.dbeta = norm_type == TE_LAYERNORM ? dbeta : nullptr;
   nb.partials = partials;
+  // RMSNorm has no shift: the gradient of an (ignored) beta is zero
+  if (norm_type == TE_RMSNORM && dbeta &&
+      cudaMemsetAsync(dbeta, 0, size_t(H) * sizeof(float), s) != cudaSuccess)
+    return TE_ERR_CUDA;
   return launch_norm_bwd(nb, s);
 }
 

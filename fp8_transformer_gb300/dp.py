@@ -42,12 +42,10 @@ class QuantizerBank:
         self.amax = torch.zeros(len(NAMES), dtype=torch.float32, device=device)
         self.quantizers = {}
         for i, n in enumerate(NAMES):
-            q = Quantizer.__new__(Quantizer)
-            q.scale = self.scale[i:i + 1]
-            q.scale_inv = self.scale_inv[i:i + 1]
-            q.amax = self.amax[i:i + 1]
-            q.mode = Quantizer(1.0, modes.get(n, "delayed"), device="cpu").mode
-            self.quantizers[n] = q
+            self.quantizers[n] = Quantizer.from_tensors(self.scale[i:i + 1],
+                                                        self.scale_inv[i:i + 1],
+                                                        self.amax[i:i + 1],
+                                                        modes.get(n, "delayed"))
 
     def quantizer_set(self) -> QuantizerSet:
         return QuantizerSet(**self.quantizers)
@@ -92,12 +90,9 @@ def layernorm_mlp_bwd_dp(dy, x, gamma, kernel1, kernel2, saved_h, saved_ln_out, 
                          activation_type=("relu",), quantizer_set=None, group=None, stream=None):
     """te_layernorm_mlp_bwd on this rank's tokens, writing the parameter gradients into
     ``buckets``, then their sum over the ranks.  dx stays local (it belongs to this rank's
-    tokens).  RMSNorm leaves ``buckets.dbeta`` at zero."""
-    if norm_type == "rmsnorm" or norm_type == 1:
-        buckets.dbeta.zero_()
+    tokens).  RMSNorm writes zeros into ``buckets.dbeta`` (beta is unused)."""
     te_layernorm_mlp_bwd(dy, x, gamma, kernel1, kernel2, saved_h, saved_ln_out, mu, rsigma, dx,
-                         buckets.dgamma, buckets.dkernel1, buckets.dkernel2,
-                         dbeta=None if norm_type in ("rmsnorm", 1) else buckets.dbeta,
+                         buckets.dgamma, buckets.dkernel1, buckets.dkernel2, dbeta=buckets.dbeta,
                          dbias1=buckets.dbias1, dbias2=buckets.dbias2, norm_type=norm_type,
                          zero_centered_gamma=zero_centered_gamma,
                          activation_type=activation_type, quantizer_set=quantizer_set,

@@ -316,8 +316,9 @@ te_status te_layernorm_mlp_fwd_host(const void* x_host, const void* gamma, const
  *   qset->x.scale_inv dequantizes saved_ln_out; kernel1 is E4M3 (kernel_dtype TE_E4M3, factor in
  *   qset->kernel1.scale_inv) or is quantized here with qset->kernel1.  dln and dkernel1 then run
  *   as E4M3 x E4M3 GEMMs; dy, kernel2 and the recomputed activation stay in dtype.
- *   Outputs: dx [M, H] dtype; dgamma [H] fp32; dbeta [H] fp32 or NULL (layernorm only);
- *   dkernel1 [H, F'] and dkernel2 [F, H] in dtype; dbias1 [F'] and dbias2 [H] fp32 or NULL.
+ *   Outputs: dx [M, H] dtype; dgamma [H] fp32; dbeta [H] fp32 or NULL (rmsnorm: written
+ *   with zeros, the gradient of the unused beta); dkernel1 [H, F'] and dkernel2 [F, H] in
+ *   dtype; dbias1 [F'] and dbias2 [H] fp32 or NULL.
  *   saved_dh [M, F'] or NULL: when given, dH is written there (E4M3 codes with qset, else dtype)
  *   instead of into the workspace, as the dln and dkernel1 GEMMs read it.
  *   workspace: te_workspace_size(TE_OP_LAYERNORM_MLP_BWD, M, H, F, dtype, quantized,
@@ -348,7 +349,7 @@ te_status te_layernorm_mlp_bwd(const void* dy, const void* x, const void* gamma,
  *   E4M3 (kernel_dtype TE_E4M3, factor in qset->kernel1.scale_inv) or is quantized here with
  *   qset->kernel1.  Both GEMMs then run as E4M3 x E4M3.
  *   Outputs (caller-owned): dx [M, H] dtype; dgamma [H] fp32; dbeta [H] fp32 or NULL
- *   (layernorm only); dkernel [H, N] dtype; dbias [N] fp32 or NULL.
+ *   (rmsnorm: written with zeros); dkernel [H, N] dtype; dbias [N] fp32 or NULL.
  *   workspace: te_workspace_size(TE_OP_LAYERNORM_DENSE_BWD, M, H, N, dtype, quantized,
  *   kernel_dtype, 0) bytes, 16-byte aligned.  dtype TE_BF16; H and N multiples of 16, H at most
  *   8192.  A NULL required pointer, a bad enum or a quantizer set without what FP8 mode needs
