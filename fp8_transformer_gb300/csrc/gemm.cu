@@ -271,14 +271,18 @@ __device__ __forceinline__ void store_seg(void* base, int64_t off, const float (
                           pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
   } else {
     uint4* p = reinterpret_cast<uint4*>(static_cast<uint8_t*>(base) + off);
+    const f32x2 s2 = f2s(scale);
 #pragma unroll
     for (int i = 0; i < 2; ++i)
       if (i * 16 < count) {
-        const float* w = v + 16 * i;
-        p[i] = make_uint4(pack_e4m3x4(w[0] * scale, w[1] * scale, w[2] * scale, w[3] * scale),
-                          pack_e4m3x4(w[4] * scale, w[5] * scale, w[6] * scale, w[7] * scale),
-                          pack_e4m3x4(w[8] * scale, w[9] * scale, w[10] * scale, w[11] * scale),
-                          pack_e4m3x4(w[12] * scale, w[13] * scale, w[14] * scale, w[15] * scale));
+        uint32_t w4[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {  // fp32(v * scale) on pairs, then the E4M3 codes
+          const float* w = v + 16 * i + 4 * q;
+          const f32x2 a = mul2(f2(w[0], w[1]), s2), b = mul2(f2(w[2], w[3]), s2);
+          w4[q] = pack_e4m3x4(f2lo(a), f2hi(a), f2lo(b), f2hi(b));
+        }
+        p[i] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
       }
   }
 }
@@ -337,8 +341,19 @@ __device__ __forceinline__ void gated_chunk(int base_act, float (&vg)[32], const
   }
 }
 
-// Running max of |v| over the first `count` values of a chunk.
+// Running max of |v| over the first `count` values of a chunk; a full chunk by a tree of
+// depth 5 rather than a chain of 32 (the max ignores NaN and is the same in any order).
 __device__ __forceinline__ float chunk_amax(float m, const float (&v)[32], int count) {
+  if (count == 32) {
+    float t[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) t[i] = fmaxf(fabsf(v[2 * i]), fabsf(v[2 * i + 1]));
+#pragma unroll
+    for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+      for (int i = 0; i < w; ++i) t[i] = fmaxf(t[i], t[i + w]);
+    return fmaxf(m, t[0]);
+  }
 #pragma unroll
   for (int i = 0; i < 32; ++i)
     if (i < count) m = fmaxf(m, fabsf(v[i]));
@@ -596,7 +611,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             act_chunk(g.act, v);
           }
           if (row_ok) {
-            amax = chunk_amax(amax, v, count);
+            if (g.amax_out) amax = chunk_amax(amax, v, count);
             store_seg(g.D, row * ldd + col0, v, count, g.d_dtype, out_scale);
           }
         }
@@ -635,7 +650,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
           }
           gated_chunk(gact, vg, vl);
           if (row_ok) {
-            amax = chunk_amax(amax, vg, count);
+            if (g.amax_out) amax = chunk_amax(amax, vg, count);
             store_seg(g.D, row * ldd + col0, vg, count, g.d_dtype, out_scale);
           }
         }
