@@ -407,7 +407,9 @@ def single_gemm(args, dev, peaks):
     out = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
     flush = make_flush(dev)
     flops = 2.0 * M * N * K
-    ours = lambda: te.te_gemm(A, B, out, a_trans=bool(at), b_trans=bool(bt))
+    nws = te.workspace_size(te.binding.TE_OP_GEMM, M, K, N, te.binding.TE_BF16)
+    ws = torch.empty(max(nws, 1), dtype=torch.uint8, device=dev)
+    ours = lambda: te.te_gemm(A, B, out, a_trans=bool(at), b_trans=bool(bt), workspace=ws)
     opA, opB = (A.t() if at else A), (B.t() if bt else B)
     lib = lambda: torch.matmul(opA, opB, out=out)
     res = {"gemm": [M, N, K, at, bt], "dtype": "bf16"}

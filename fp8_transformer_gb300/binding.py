@@ -23,7 +23,7 @@ TE_IDENTITY, TE_RELU, TE_GELU, TE_SILU, TE_SWIGLU, TE_GEGLU, TE_REGLU = range(7)
 TE_SCALING_DELAYED, TE_SCALING_CURRENT = 0, 1
 (TE_OP_NORM_FWD, TE_OP_ACT_LU, TE_OP_DACT_DBIAS, TE_OP_LAYERNORM_DENSE_FWD,
  TE_OP_LAYERNORM_MLP_FWD, TE_OP_NORM_BWD, TE_OP_LAYERNORM_MLP_BWD,
- TE_OP_LAYERNORM_DENSE_BWD, TE_OP_LAYERNORM_MLP_FWD_HOST) = range(9)
+ TE_OP_LAYERNORM_DENSE_BWD, TE_OP_LAYERNORM_MLP_FWD_HOST, TE_OP_GEMM) = range(10)
 
 NORM_TYPES = {"layernorm": TE_LAYERNORM, "rmsnorm": TE_RMSNORM}
 ACT_TYPES = {"identity": TE_IDENTITY, "relu": TE_RELU, "gelu": TE_GELU, "silu": TE_SILU,
@@ -85,7 +85,8 @@ _SIGS = {
                                               _QP, _vp, ctypes.c_int, _vp, _vp, _sz, _vp]),
     "te_quantize": (ctypes.c_int, [_vp, ctypes.c_int, _i64, _i64, _QP, _vp, _vp]),
     "te_gemm": (ctypes.c_int, [_vp, ctypes.c_int, _vp, ctypes.c_int, ctypes.c_int, _i64, _i64,
-                               _i64, _vp, _vp, _vp, ctypes.c_int, _vp, ctypes.c_int, _vp]),
+                               _i64, _vp, _vp, _vp, ctypes.c_int, _vp, ctypes.c_int, _vp, _sz,
+                               _vp]),
     "te_layernorm_dense_fwd": (ctypes.c_int, [_vp, _vp, ctypes.c_int, _vp, _vp, _vp,
                                               ctypes.c_int, ctypes.c_int, _f, _QSP, _i64, _i64,
                                               _i64, ctypes.c_int, _vp, _vp, _vp, _vp, _vp, _sz,
@@ -298,13 +299,18 @@ def te_quantize(x, q, out, stream=None):
 
 
 def te_gemm(A, B, out, a_trans=False, b_trans=False, a_scale_inv=None, b_scale_inv=None,
-            bias=None, stream=None):
+            bias=None, workspace=None, split_k=True, stream=None):
+    """split_k=False passes no workspace: no tile is split along K."""
     M = A.shape[1] if a_trans else A.shape[0]
     K = A.shape[0] if a_trans else A.shape[1]
     N = B.shape[0] if b_trans else B.shape[1]
+    if workspace is None and split_k:
+        n = workspace_size(TE_OP_GEMM, M, K, N, _dt(A))
+        workspace = _ws(n, A.device) if n > 0 else None
     st = lib().te_gemm(_ptr(A), int(bool(a_trans)), _ptr(B), int(bool(b_trans)), _dt(A), M, N, K,
                        _ptr(a_scale_inv), _ptr(b_scale_inv), _ptr(bias),
                        _dt(bias) if bias is not None else TE_F32, _ptr(out), _dt(out),
+                       _ptr(workspace), 0 if workspace is None else workspace.numel(),
                        _stream(stream))
     _check("te_gemm", st)
     return out

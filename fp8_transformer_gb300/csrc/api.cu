@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <initializer_list>
 #include <utility>
 
 #include "kernels.h"
@@ -44,6 +45,31 @@ struct Carver {
     return p;
   }
 };
+
+// The scratch for splitting GEMM tails along K (launch_gemm) is carved last: a workspace that
+// stops short of it still serves the call, with no tile split.  The GEMMs of one call run one
+// after another on its stream, so they share the region, sized for the largest.
+struct SplitScratch {
+  size_t offset = 0;  // where the region starts in the workspace
+  size_t required = 0;  // workspace bytes the call needs (everything before the region)
+};
+
+SplitScratch carve_split(Carver& c, std::initializer_list<size_t> needs) {
+  SplitScratch r;
+  r.required = c.used;
+  r.offset = c.used;
+  size_t most = 0;
+  for (size_t n : needs) most = n > most ? n : most;
+  if (most) c.take(most);
+  return r;
+}
+
+void give_split(GemmArgs& g, const SplitScratch& sc, void* ws, size_t ws_bytes) {
+  if (ws && ws_bytes > sc.offset) {
+    g.split_ws = static_cast<uint8_t*>(ws) + sc.offset;
+    g.split_ws_bytes = ws_bytes - sc.offset;
+  }
+}
 
 cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
 
@@ -95,6 +121,7 @@ struct FwdLayout {
   void* kq2 = nullptr;    // E4M3 copy of kernel2
   void* a2 = nullptr;     // activation output, GEMM2 operand
   void* a2_hi = nullptr;  // fp32 activation output awaiting its current-scaling cast
+  SplitScratch split;
   size_t bytes = 0;
 };
 
@@ -105,6 +132,7 @@ FwdLayout dense_layout(void* ws, int64_t M, int64_t H, int64_t N, int dtype, boo
   if (!have_saved_ln) L.ln = c.take(size_t(M) * H * (quant ? 1 : esize(dtype)));
   if (quant && kernel_dtype != TE_E4M3) L.kq1 = c.take(size_t(H) * N);
   if (!quant && dtype == TE_F32) L.kt1 = c.take(size_t(H) * N * 4);
+  L.split = carve_split(c, {gemm_split_workspace(M, N, H, quant ? TE_E4M3 : dtype, EPI_BIAS)});
   L.bytes = c.used;
   return L;
 }
@@ -126,6 +154,9 @@ FwdLayout mlp_layout(void* ws, int64_t M, int64_t H, int64_t F, int dtype, bool 
     L.kt1 = c.take(size_t(H) * F1 * 4);
     L.kt2 = c.take(size_t(F) * H * 4);
   }
+  const int gd = quant ? TE_E4M3 : dtype;
+  L.split = carve_split(c, {gemm_split_workspace(M, F1, H, gd, is_gated(act) ? EPI_BIAS_GATED : EPI_BIAS_ACT),
+                            gemm_split_workspace(M, H, F, gd, EPI_BIAS)});
   L.bytes = c.used;
   return L;
 }
@@ -139,6 +170,7 @@ struct BwdLayout {
   void* dh = nullptr;    // [M, F'], E4M3 or dtype
   void* dln = nullptr;   // [M, H], dtype
   void* kq1 = nullptr;   // E4M3 kernel1 when quantized here
+  SplitScratch split;
   size_t bytes = 0;
 };
 
@@ -156,6 +188,11 @@ BwdLayout bwd_layout(void* ws, int64_t M, int64_t H, int64_t F, int dtype, bool 
   L.dh = c.take(size_t(M) * F1 * (quant ? 1 : esize(dtype)));
   L.dln = c.take(size_t(M) * H * esize(dtype));
   if (quant && kernel_dtype != TE_E4M3) L.kq1 = c.take(size_t(H) * F1);
+  const int gd = quant ? TE_E4M3 : dtype;
+  L.split = carve_split(c, {gemm_split_workspace(F, H, M, dtype, EPI_BIAS),
+                            gemm_split_workspace(M, F, H, dtype, EPI_BIAS),
+                            gemm_split_workspace(M, H, F1, gd, EPI_BIAS),
+                            gemm_split_workspace(H, F1, M, gd, EPI_BIAS)});
   L.bytes = c.used;
   return L;
 }
@@ -167,6 +204,7 @@ struct DenseBwdLayout {
   void* dyq = nullptr;  // E4M3 dy (FP8 mode)
   void* kq = nullptr;   // E4M3 kernel when quantized here
   void* dln = nullptr;  // [M, H], dtype
+  SplitScratch split;
   size_t bytes = 0;
 };
 
@@ -180,6 +218,9 @@ DenseBwdLayout dense_bwd_layout(void* ws, int64_t M, int64_t H, int64_t N, int d
   if (quant) L.dyq = c.take(size_t(M) * N);
   if (quant && kernel_dtype != TE_E4M3) L.kq = c.take(size_t(H) * N);
   L.dln = c.take(size_t(M) * H * esize(dtype));
+  const int gd = quant ? TE_E4M3 : dtype;
+  L.split = carve_split(c, {gemm_split_workspace(M, H, N, gd, EPI_BIAS),
+                            gemm_split_workspace(H, N, M, gd, EPI_BIAS)});
   L.bytes = c.used;
   return L;
 }
@@ -260,6 +301,8 @@ size_t te_workspace_size(te_op op, int64_t M, int64_t H, int64_t F_or_N, te_dtyp
       return bwd_layout(nullptr, M, H, F_or_N, dtype, quantized != 0, kernel_dtype, act).bytes;
     case TE_OP_LAYERNORM_MLP_FWD_HOST:
       return host_fwd_workspace(M, H, F_or_N, dtype, act);
+    case TE_OP_GEMM:  // dims = {M, K, N}
+      return gemm_split_workspace(M, F_or_N, H, dtype, EPI_BIAS);
     case TE_OP_LAYERNORM_DENSE_BWD:
       return dense_bwd_layout(nullptr, M, H, F_or_N, dtype, quantized != 0, kernel_dtype).bytes;
     default: return 0;
@@ -378,7 +421,7 @@ te_status te_quantize(const void* x, te_dtype x_dtype, int64_t M, int64_t N,
 te_status te_gemm(const void* A, int a_trans, const void* B, int b_trans, te_dtype ab_dtype,
                   int64_t M, int64_t N, int64_t K, const float* a_scale_inv,
                   const float* b_scale_inv, const void* bias, te_dtype bias_dtype, void* D,
-                  te_dtype d_dtype, void* stream) {
+                  te_dtype d_dtype, void* workspace, size_t ws_bytes, void* stream) {
   if (M < 0 || N <= 0 || K <= 0 || ab_dtype < TE_F32 || ab_dtype > TE_E4M3 ||
       !is_act_dtype(d_dtype) || (bias && !is_act_dtype(bias_dtype)))
     return TE_ERR_INVALID_ARG;
@@ -388,10 +431,12 @@ te_status te_gemm(const void* A, int a_trans, const void* B, int b_trans, te_dty
   // fp32 operands run as tf32, which the tensor cores take K-major only.
   if (ab_dtype == TE_F32 && (a_trans || !b_trans)) return TE_ERR_UNSUPPORTED;
   if (!aligned16(A) || !aligned16(B) || !aligned16(D) || !opt_aligned16(bias) ||
-      !aligned4(a_scale_inv) || !aligned4(b_scale_inv))
+      !aligned4(a_scale_inv) || !aligned4(b_scale_inv) || !aligned16(workspace))
     return TE_ERR_UNSUPPORTED;
   if (M == 0) return TE_OK;
   GemmArgs g;
+  g.split_ws = workspace;
+  g.split_ws_bytes = workspace ? ws_bytes : 0;
   g.A = A;
   g.B = B;
   g.ab_dtype = ab_dtype;
@@ -437,7 +482,7 @@ te_status te_layernorm_dense_fwd(const void* x, const void* kernel, te_dtype ker
     return TE_ERR_UNSUPPORTED;
   if (M == 0) return TE_OK;
   FwdLayout L = dense_layout(workspace, M, H, N, dtype, quant, kernel_dtype, saved_ln_out != nullptr);
-  if (L.bytes > 0 && (!workspace || ws_bytes < L.bytes)) return TE_ERR_WORKSPACE;
+  if (L.split.required > 0 && (!workspace || ws_bytes < L.split.required)) return TE_ERR_WORKSPACE;
   cudaStream_t s = as_stream(stream);
   void* ln = saved_ln_out ? saved_ln_out : L.ln;
   const int ln_dtype = quant ? TE_E4M3 : dtype;
@@ -472,6 +517,7 @@ te_status te_layernorm_dense_fwd(const void* x, const void* kernel, te_dtype ker
   g.bias_dtype = dtype;
   g.D = out;
   g.cast.out_dtype = dtype;
+  give_split(g, L.split, workspace, ws_bytes);
   return launch_gemm(g, s);
 }
 
@@ -510,7 +556,7 @@ te_status te_layernorm_mlp_fwd(const void* x, const void* gamma, const void* bet
   const int64_t F1 = gated ? 2 * F : F;
   FwdLayout L = mlp_layout(workspace, M, H, F, dtype, quant, kernel_dtype, act,
                            saved_ln_out != nullptr);
-  if (!workspace || ws_bytes < L.bytes) return TE_ERR_WORKSPACE;
+  if (!workspace || ws_bytes < L.split.required) return TE_ERR_WORKSPACE;
   cudaStream_t s = as_stream(stream);
   void* ln = saved_ln_out ? saved_ln_out : L.ln;
   void* a2 = saved_act ? saved_act : L.a2;  // GEMM2's A operand
@@ -573,6 +619,7 @@ te_status te_layernorm_mlp_fwd(const void* x, const void* gamma, const void* bet
     g1.D = a2;
     g1.cast.out_dtype = dtype;
   }
+  give_split(g1, L.split, workspace, ws_bytes);
   st = launch_gemm(g1, s);
   if (st != TE_OK) return st;
   if (act_current) {
@@ -606,6 +653,7 @@ te_status te_layernorm_mlp_fwd(const void* x, const void* gamma, const void* bet
   g2.bias_dtype = dtype;
   g2.D = out;
   g2.cast.out_dtype = dtype;
+  give_split(g2, L.split, workspace, ws_bytes);
   return launch_gemm(g2, s);
 }
 
@@ -657,7 +705,7 @@ te_status te_layernorm_mlp_bwd(const void* dy, const void* x, const void* gamma,
     return TE_OK;
   }
   BwdLayout L = bwd_layout(workspace, M, H, F, dtype, quant, kernel_dtype, act);
-  if (!workspace || ws_bytes < L.bytes) return TE_ERR_WORKSPACE;
+  if (!workspace || ws_bytes < L.split.required) return TE_ERR_WORKSPACE;
   float* partials = static_cast<float*>(L.partials);
   void* dh = saved_dh ? saved_dh : L.dh;  // the dgrad / wgrad GEMMs' operand
   te_status st;
@@ -701,6 +749,7 @@ te_status te_layernorm_mlp_bwd(const void* dy, const void* x, const void* gamma,
     g.K = M;
     g.D = dkernel2;
     g.cast.out_dtype = dtype;
+    give_split(g, L.split, workspace, ws_bytes);
     st = launch_gemm(g, s);
     if (st != TE_OK) return st;
   }
@@ -717,6 +766,7 @@ te_status te_layernorm_mlp_bwd(const void* dy, const void* x, const void* gamma,
     g.K = H;
     g.D = L.da;
     g.cast.out_dtype = dtype;
+    give_split(g, L.split, workspace, ws_bytes);
     st = launch_gemm(g, s);
     if (st != TE_OK) return st;
   }
@@ -759,6 +809,7 @@ te_status te_layernorm_mlp_bwd(const void* dy, const void* x, const void* gamma,
     g.b_scale_inv = quant ? qset->kernel1.scale_inv : nullptr;
     g.D = L.dln;
     g.cast.out_dtype = dtype;
+    give_split(g, L.split, workspace, ws_bytes);
     st = launch_gemm(g, s);
     if (st != TE_OK) return st;
   }
@@ -777,6 +828,7 @@ te_status te_layernorm_mlp_bwd(const void* dy, const void* x, const void* gamma,
     g.b_scale_inv = quant ? qset->grad.scale_inv : nullptr;
     g.D = dkernel1;
     g.cast.out_dtype = dtype;
+    give_split(g, L.split, workspace, ws_bytes);
     st = launch_gemm(g, s);
     if (st != TE_OK) return st;
   }
@@ -846,7 +898,7 @@ te_status te_layernorm_dense_bwd(const void* dy, const void* x, const void* gamm
     return TE_OK;
   }
   DenseBwdLayout L = dense_bwd_layout(workspace, M, H, N, dtype, quant, kernel_dtype);
-  if (!workspace || ws_bytes < L.bytes) return TE_ERR_WORKSPACE;
+  if (!workspace || ws_bytes < L.split.required) return TE_ERR_WORKSPACE;
   float* partials = static_cast<float*>(L.partials);
   te_status st;
   // dbias = column sums of dy; in FP8 mode the same pass casts dy with the grad quantizer
@@ -901,6 +953,7 @@ te_status te_layernorm_dense_bwd(const void* dy, const void* x, const void* gamm
     g.b_scale_inv = quant ? qset->kernel1.scale_inv : nullptr;
     g.D = L.dln;
     g.cast.out_dtype = dtype;
+    give_split(g, L.split, workspace, ws_bytes);
     st = launch_gemm(g, s);
     if (st != TE_OK) return st;
   }
@@ -919,6 +972,7 @@ te_status te_layernorm_dense_bwd(const void* dy, const void* x, const void* gamm
     g.b_scale_inv = quant ? qset->grad.scale_inv : nullptr;
     g.D = dkernel;
     g.cast.out_dtype = dtype;
+    give_split(g, L.split, workspace, ws_bytes);
     st = launch_gemm(g, s);
     if (st != TE_OK) return st;
   }

@@ -21,12 +21,18 @@
 //              E4M3.
 // The epilogue of tile i overlaps the MMAs of tile i + 1.
 //
+// When the tiles do not fill the last wave of SM pairs, and the caller gives scratch memory, the
+// tiles of that wave are split along K into chunks computed by different pairs: every chunk
+// stores its raw fp32 accumulator, and the pair whose chunk is counted in last sums them in
+// chunk order (so the result is the same whichever pair finishes last) and runs the epilogue.
+//
 // Every mbarrier wait is bounded in time.  On expiry the waiting thread records
 // TE_ERR_TIMEOUT in the device status word and raises a CTA-wide abort flag; every role
 // then leaves its loop, the producer waits (again bounded) for its own TMA copies still in
 // flight, the MMA thread waits for its own MMAs, and TMEM is freed before the CTA exits.
 #include <cuda.h>
 
+#include <cstdint>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -87,6 +93,15 @@ struct GemmDev {
   float* out_scale_inv;
   float* amax_out;
   int* status;
+  // The tiles after the first `full_tiles` (the last, partial wave) are split along K into
+  // `split` chunks of `kb_chunk` k-blocks; chunks 0 .. split-2 leave their raw accumulators in
+  // `partials` and count themselves in `flags` (zeroed before the launch); the last chunk's
+  // CTA adds them to its own and runs the epilogue.
+  int full_tiles;
+  int split;
+  int kb_chunk;
+  float* partials;  // [remaining tiles][split - 1][CG][BM][BN]
+  int* flags;       // [remaining tiles][CG]
 };
 
 struct GemmParams {  // aligned like its tensor maps
@@ -235,6 +250,31 @@ __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// Stores 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};"
+      ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]),
+        "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]),
+        "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]),
+        "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+        "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// TMEM column of the k-th (of 4) 32-column group an epilogue warp of column half `half` reads:
+// one half of the tile, or for a gated tile the matching quarter of each of its two halves.
+__device__ __forceinline__ int epilogue_column(int k, int half, int gated) {
+  if (!gated) return (half * 4 + k) * 32;
+  return (k >> 1) * (BN / 2) + (half * 2 + (k & 1)) * 32;
+}
+
 // ------------------------------------------------------------------ tile order ------------
 
 struct Tile {
@@ -250,6 +290,87 @@ __device__ __forceinline__ Tile tile_of(int t, int num_m, int num_n, int group_m
   const int gm = min(num_m - first_m, group_m);
   const int in_group = t - group * group_size;
   return Tile{first_m + in_group % gm, in_group / gm};
+}
+
+// A cluster's unit of work: tile `tile`, k-blocks [kb0, kb1), and which K chunk of a split
+// tile it is (-1: the whole tile).  Items [0, full_tiles) are whole tiles in raster order; the
+// rest are the remaining tiles' chunks, chunk-minor, so a tile's last chunk comes after its
+// other chunks in every cluster's sequence.
+struct Item {
+  int tile, kb0, kb1, chunk;
+};
+
+__device__ __forceinline__ Item item_of(int it, const GemmDev& g) {
+  if (it < g.full_tiles) return Item{it, 0, g.num_kb, -1};
+  const int u = it - g.full_tiles;
+  const int c = u % g.split;
+  const int kb0 = c * g.kb_chunk;
+  const int kb1 = kb0 + g.kb_chunk < g.num_kb ? kb0 + g.kb_chunk : g.num_kb;
+  return Item{g.full_tiles + u / g.split, kb0, kb1, g.split > 1 ? c : -1};
+}
+
+// Counts a split tile's chunks in at GPU scope: releases this chunk's partial, acquires the
+// earlier ones', returns how many chunks had arrived before.
+__device__ __forceinline__ int atom_add_acq_rel(int* p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
+// A K chunk's raw accumulator (one CTA's 128 x 256 fp32) in 4-column groups with the 128 rows
+// contiguous, so the 32 rows of a warp's access are one 512-byte run.
+__device__ __forceinline__ size_t partial_index(int col, int row) {
+  return (size_t(col >> 2) * BM + row) * 4;
+}
+
+__device__ __forceinline__ void store_partial(float* base, int col, int row, const uint32_t (&r)[32]) {
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    __stcg(reinterpret_cast<float4*>(base + partial_index(col + 4 * j, row)),
+           make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                       __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3])));
+}
+
+// r (this chunk's accumulator, columns [col, col + 32) of one row) becomes the sum of all the
+// tile's chunks, added in chunk order so that the result does not depend on which chunk ran last.
+template <int CG>
+__device__ __forceinline__ void add_chunks(uint32_t (&r)[32], const float* slot0, int own, int split,
+                                           int col, int row) {
+  constexpr size_t kChunkStride = size_t(CG) * BM * BN;  // from one chunk's partials to the next's
+  float t[32];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    float4 p;
+    if (own == 0) {
+      p = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                      __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+    } else {
+      p = __ldcg(reinterpret_cast<const float4*>(slot0 + partial_index(col + 4 * j, row)));
+    }
+    t[4 * j] = p.x;
+    t[4 * j + 1] = p.y;
+    t[4 * j + 2] = p.z;
+    t[4 * j + 3] = p.w;
+  }
+#pragma unroll 1
+  for (int c = 1; c < split; ++c) {
+    if (c == own) {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) t[i] += __uint_as_float(r[i]);
+    } else {
+      const float* b = slot0 + size_t(c) * kChunkStride;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float4 p = __ldcg(reinterpret_cast<const float4*>(b + partial_index(col + 4 * j, row)));
+        t[4 * j] += p.x;
+        t[4 * j + 1] += p.y;
+        t[4 * j + 2] += p.z;
+        t[4 * j + 3] += p.w;
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(t[i]);
 }
 
 // ------------------------------------------------------------------ epilogue stores -------
@@ -393,11 +514,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
   uint64_t* tfull = bars + 2 * STAGES;
   uint64_t* tempty = tfull + 2;
   uint64_t* drain = tempty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* epi_bar = drain + 1;  // barrier of the epilogue warps (split tiles)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(epi_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* split_arrival = abort_flag + 1;  // [2]: a split chunk's arrival number
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int num_tiles = g.num_m * g.num_n;
+  const int num_items = g.full_tiles + (num_tiles - g.full_tiles) * g.split;
   const uint32_t rank = CG == 1 ? 0u : cluster_rank();
   const bool leader = rank == 0;
   const int cluster_id = int(blockIdx.x) / CG;
@@ -413,6 +537,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       mbar_init(smem_u32(&tempty[a]), 32 * kEpiWarps * CG);
     }
     mbar_init(smem_u32(drain), 1);
+    mbar_init(smem_u32(epi_bar), 32 * kEpiWarps);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -437,10 +562,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       int stage = 0;
       uint32_t phase = 0, issued = 0, last_parity = 0;
       bool ok = true;
-      for (int t = cluster_id; t < num_tiles && ok; t += num_clusters) {
-        const Tile tl = tile_of(t, g.num_m, g.num_n, g.group_m);
+      for (int it = cluster_id; it < num_items && ok; it += num_clusters) {
+        const Item w = item_of(it, g);
+        const Tile tl = tile_of(w.tile, g.num_m, g.num_n, g.group_m);
         const int m0 = (tl.m * CG + int(rank)) * BM;
-        for (int kb = 0; kb < g.num_kb; ++kb) {
+        for (int kb = w.kb0; kb < w.kb1; ++kb) {
           if (!mbar_try_wait(smem_u32(&empty[stage]), phase ^ 1) &&
               !wait_bounded(smem_u32(&empty[stage]), phase ^ 1, abort_flag, &g_device_status, kWaitLimitNs, true)) {
             ok = false;
@@ -506,7 +632,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       uint32_t phase = 0;
       int local = 0;
       bool ok = true;
-      for (int t = cluster_id; t < num_tiles && ok; t += num_clusters, ++local) {
+      for (int it = cluster_id; it < num_items && ok; it += num_clusters, ++local) {
+        const Item w = item_of(it, g);
         const int acc = local & 1;
         const uint32_t acc_phase = (local >> 1) & 1;
         if (!wait_bounded(smem_u32(&tempty[acc]), acc_phase ^ 1, abort_flag, &g_device_status, kWaitLimitNs, true)) {
@@ -515,7 +642,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + uint32_t(acc * BN);
-        for (int kb = 0; kb < g.num_kb; ++kb) {
+        for (int kb = w.kb0; kb < w.kb1; ++kb) {
           if (!mbar_try_wait(smem_u32(&full[stage]), phase) &&
               !wait_bounded(smem_u32(&full[stage]), phase, abort_flag, &g_device_status, kWaitLimitNs, true)) {
             ok = false;
@@ -532,7 +659,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             const uint64_t bd =
                 B_KMAJOR ? smem_desc(b_base + j * MMA_K_BYTES, 16, 8 * kRowBytes)
                          : smem_desc(b_base + j * MMA_K * kRowBytes, EPR * kRowBytes, 8 * kRowBytes);
-            umma<KIND, CG>(d_tmem, ad, bd, IDESC, (kb | j) != 0 ? 1u : 0u);
+            umma<KIND, CG>(d_tmem, ad, bd, IDESC, (kb != w.kb0 || j != 0) ? 1u : 0u);
           }
           if constexpr (CG == 1) umma_commit<1>(smem_u32(&empty[stage]));
           else umma_commit_mc(smem_u32(&empty[stage]), 0x3);
@@ -568,7 +695,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     const int gact = gate_act(g.act);  // a gated pair's function of its gate half
     float amax = 0.0f;
     int local = 0;
-    for (int t = cluster_id; t < num_tiles; t += num_clusters, ++local) {
+    uint32_t epi_phase = 0;
+    // All epilogue warps meet (bounded like every other wait).
+    auto epi_sync = [&]() -> bool {
+      mbar_arrive(smem_u32(epi_bar));
+      const bool r = wait_bounded(smem_u32(epi_bar), epi_phase, abort_flag, &g_device_status, kWaitLimitNs, true);
+      epi_phase ^= 1;
+      return r;
+    };
+    for (int it = cluster_id; it < num_items; it += num_clusters, ++local) {
+      const Item w = item_of(it, g);
       const int acc = local & 1;
       const uint32_t acc_phase = (local >> 1) & 1;
       const uint32_t tb = smem_u32(&tfull[acc]);
@@ -581,11 +717,45 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       }
       __syncwarp();
       tc_fence_after();
-      const Tile tl = tile_of(t, g.num_m, g.num_n, g.group_m);
+      const Tile tl = tile_of(w.tile, g.num_m, g.num_n, g.group_m);
       const int64_t row = (int64_t(tl.m) * CG + rank) * BM + row_in_tile;
       const bool row_ok = row < g.M;
       const uint32_t taddr = tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(acc * BN);
-      if (!g.gated) {
+      // A K chunk of a split tile: every chunk stores its raw accumulator; the one counted in
+      // last adds the others' to its own in TMEM, in chunk order, and runs the epilogue.
+      bool epilogue = true;
+      if (w.chunk >= 0) {
+        const int u = w.tile - g.full_tiles;
+        float* slot0 = g.partials + (size_t(u) * g.split * CG + rank) * (BM * BN);
+        float* mine = slot0 + size_t(w.chunk) * CG * (BM * BN);
+#pragma unroll 1
+        for (int k = 0; k < 4; ++k) {
+          const int col = epilogue_column(k, half, g.gated);
+          uint32_t r[32];
+          tmem_ld32(taddr + col, r);
+          tmem_ld_wait();
+          store_partial(mine, col, row_in_tile, r);
+        }
+        __threadfence();
+        if (!epi_sync()) break;
+        if (warp == 2 && lane == 0) split_arrival[local & 1] = atom_add_acq_rel(g.flags + u * CG + rank, 1);
+        if (!epi_sync()) break;
+        epilogue = split_arrival[local & 1] == g.split - 1;
+        if (epilogue) {
+          __threadfence();
+#pragma unroll 1
+          for (int k = 0; k < 4; ++k) {  // the columns this warp's epilogue reads back
+            const int col = epilogue_column(k, half, g.gated);
+            uint32_t r[32];
+            tmem_ld32(taddr + col, r);
+            tmem_ld_wait();
+            add_chunks<CG>(r, slot0, w.chunk, g.split, col, row_in_tile);
+            tmem_st32(taddr + col, r);
+          }
+          tmem_st_wait();
+        }
+      }
+      if (epilogue && !g.gated) {
         const int64_t n0 = int64_t(tl.n) * BN;
         constexpr int kChunks = BN / 32 / 2;  // per warp
 #pragma unroll 1
@@ -615,7 +785,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             store_seg(g.D, row * ldd + col0, v, count, g.d_dtype, out_scale);
           }
         }
-      } else {
+      } else if (epilogue) {
         const int64_t n0 = int64_t(tl.n) * (BN / 2);
         constexpr int kChunks = BN / 64 / 2;  // per warp
 #pragma unroll 1
@@ -727,6 +897,73 @@ int choose_cta_group(int kind, int64_t M) {
   return 2;
 }
 
+// Tile grid of one GEMM.
+struct Geometry {
+  int kind, esize, cg, num_m, num_n, num_kb;
+};
+
+Geometry geometry(int ab_dtype, int64_t M, int64_t N, int64_t K, bool gated) {
+  Geometry q;
+  q.kind = ab_dtype == TE_BF16 ? 0 : ab_dtype == TE_E4M3 ? 1 : 2;
+  q.esize = ab_dtype == TE_BF16 ? 2 : ab_dtype == TE_E4M3 ? 1 : 4;
+  q.cg = choose_cta_group(q.kind, M);
+  q.num_m = int(ceil_div(M, int64_t(BM) * q.cg));
+  q.num_n = int(gated ? ceil_div(N / 2, BN / 2) : ceil_div(N, BN));
+  q.num_kb = int(ceil_div(K, int64_t(kRowBytes / q.esize)));
+  return q;
+}
+
+// K split of the tiles left over after the last whole wave.  A tile keeps its SM pair busy for
+// about num_kb k-block times (about a third of a microsecond each, for every operand type).
+// Splitting pays only while all chunks run at once, in one wave: spread over several waves, the
+// chunks of one tile re-read their operands in different waves and lose more than they gain.
+// Measured on GB300, storing a chunk's partial and summing the partials cost about 24 k-block
+// times per chunk.  The plan takes the split that finishes the leftover tiles soonest, within
+// the workspace given.  TE_GEMM_SPLIT_K=0 in the environment turns splitting off (a diagnostic
+// switch between two complete paths).
+constexpr int kSplitCostKb = 24;
+constexpr int kMinChunkKb = 4;
+
+struct SplitPlan {
+  int64_t full_tiles = 0;
+  int split = 1;
+  int kb_chunk = 0;
+  size_t partial_bytes = 0;
+  size_t flag_bytes = 0;
+};
+
+bool split_enabled() {
+  const char* e = getenv("TE_GEMM_SPLIT_K");
+  return !(e && e[0] == '0');
+}
+
+SplitPlan plan_split(int64_t tiles, int64_t clusters, int num_kb, int cg, size_t budget) {
+  SplitPlan best;
+  best.full_tiles = tiles;
+  best.kb_chunk = num_kb;
+  if (clusters < 1 || tiles < 1) return best;
+  const int64_t full = tiles / clusters * clusters;
+  const int64_t rest = tiles - full;
+  if (rest == 0) return best;
+  int64_t best_cost = num_kb;  // unsplit: one round of whole tiles
+  for (int sp : {2, 3, 4, 6, 8}) {
+    const int kbc = (num_kb + sp - 1) / sp;
+    if (kbc < kMinChunkKb || int64_t(sp - 1) * kbc >= num_kb) continue;  // every chunk non-empty
+    if (rest * sp > clusters) break;  // more than one wave of chunks
+    const int64_t cost = kbc + int64_t(kSplitCostKb) * sp;
+    const size_t pb = size_t(rest) * sp * cg * BM * BN * sizeof(float);
+    const size_t fb = (size_t(rest) * cg * sizeof(int) + 255) / 256 * 256;
+    if (cost >= best_cost || pb + fb > budget) continue;
+    best_cost = cost;
+    best.full_tiles = full;
+    best.split = sp;
+    best.kb_chunk = kbc;
+    best.partial_bytes = pb;
+    best.flag_bytes = fb;
+  }
+  return best;
+}
+
 }  // namespace
 
 int num_sms() {
@@ -768,13 +1005,21 @@ te_status read_and_clear_device_status(int32_t* out) {
   return TE_OK;
 }
 
+size_t gemm_split_workspace(int64_t M, int64_t N, int64_t K, int ab_dtype, int epilogue) {
+  if (M <= 0 || N <= 0 || K <= 0) return 0;
+  const Geometry q = geometry(ab_dtype, M, N, K, epilogue == EPI_BIAS_GATED);
+  const SplitPlan sp = plan_split(int64_t(q.num_m) * q.num_n, num_sms() / q.cg, q.num_kb, q.cg, SIZE_MAX);
+  return sp.partial_bytes + sp.flag_bytes;
+}
+
 te_status launch_gemm(const GemmArgs& a, cudaStream_t s) {
   if (a.M == 0 || a.N == 0) return TE_OK;
-  const int kind = a.ab_dtype == TE_BF16 ? 0 : a.ab_dtype == TE_E4M3 ? 1 : 2;
-  const int esize = a.ab_dtype == TE_BF16 ? 2 : a.ab_dtype == TE_E4M3 ? 1 : 4;
-  const uint32_t epr = uint32_t(kRowBytes / esize);
   const bool gated = a.epilogue == EPI_BIAS_GATED;
-  const int cg = choose_cta_group(kind, a.M);
+  const Geometry q = geometry(a.ab_dtype, a.M, a.N, a.K, gated);
+  const int kind = q.kind;
+  const int esize = q.esize;
+  const uint32_t epr = uint32_t(kRowBytes / esize);
+  const int cg = q.cg;
   GemmParams prm;
   memset(&prm, 0, sizeof(prm));
   // A: op(A) is [M, K]; each CTA loads 128 rows.
@@ -791,9 +1036,9 @@ te_status launch_gemm(const GemmArgs& a, cudaStream_t s) {
   g.K = a.K;
   g.gated = gated ? 1 : 0;
   g.F = gated ? a.N / 2 : 0;
-  g.num_m = int(ceil_div(a.M, int64_t(BM) * cg));
-  g.num_n = int(gated ? ceil_div(a.N / 2, BN / 2) : ceil_div(a.N, BN));
-  g.num_kb = int(ceil_div(a.K, epr));
+  g.num_m = q.num_m;
+  g.num_n = q.num_n;
+  g.num_kb = q.num_kb;
   {
     const int64_t a_tile_bytes = int64_t(BM) * cg * a.K * esize;
     int64_t gm = kRasterL2Bytes / (a_tile_bytes > 0 ? a_tile_bytes : 1);
@@ -815,7 +1060,20 @@ te_status launch_gemm(const GemmArgs& a, cudaStream_t s) {
   g.amax_out = a.cast.amax_out;
   const int64_t tiles = int64_t(g.num_m) * g.num_n;
   const int64_t slots = num_sms() / cg;
-  const int grid = int(tiles < slots ? tiles : slots) * cg;
+  SplitPlan sp;
+  sp.full_tiles = tiles;
+  sp.kb_chunk = g.num_kb;
+  if (a.split_ws && split_enabled()) sp = plan_split(tiles, slots, g.num_kb, cg, a.split_ws_bytes);
+  g.full_tiles = int(sp.full_tiles);
+  g.split = sp.split;
+  g.kb_chunk = sp.kb_chunk;
+  if (sp.split > 1) {
+    g.partials = static_cast<float*>(a.split_ws);
+    g.flags = reinterpret_cast<int*>(static_cast<char*>(a.split_ws) + sp.partial_bytes);
+    if (cudaMemsetAsync(g.flags, 0, sp.flag_bytes, s) != cudaSuccess) return TE_ERR_CUDA;
+  }
+  const int64_t items = sp.full_tiles + (tiles - sp.full_tiles) * sp.split;
+  const int grid = int(items < slots ? items : slots) * cg;
   ProfileScope prof(a.epilogue == EPI_BIAS ? TE_KERNEL_GEMM : TE_KERNEL_GEMM_ACT, s);
   if (cg == 1) {
     if (kind == 0) return launch_kind<0, 1>(prm, grid, a.a_kmajor, a.b_kmajor, s);

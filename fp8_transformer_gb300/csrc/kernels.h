@@ -138,8 +138,14 @@ struct GemmArgs {
   void* saved_h = nullptr;      // [M, N] pre-activation, h_dtype
   void* D = nullptr;            // [M, N] or [M, N/2] gated
   CastSpec cast;                // output stage of D (amax / E4M3 of the activation)
+  // Optional scratch (256-byte aligned) for splitting the last wave's tiles along K; without it
+  // no tile is split.
+  void* split_ws = nullptr;
+  size_t split_ws_bytes = 0;
 };
 te_status launch_gemm(const GemmArgs& g, cudaStream_t s);
+// Bytes of split_ws that launch_gemm would use for this GEMM on the current device (0: none).
+size_t gemm_split_workspace(int64_t M, int64_t N, int64_t K, int ab_dtype, int epilogue);
 
 // Device status word (TE_OK or the first failure a kernel recorded).
 int* device_status_ptr();

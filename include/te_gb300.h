@@ -105,7 +105,8 @@ typedef enum {
   TE_OP_NORM_BWD = 5,
   TE_OP_LAYERNORM_MLP_BWD = 6,
   TE_OP_LAYERNORM_DENSE_BWD = 7,
-  TE_OP_LAYERNORM_MLP_FWD_HOST = 8
+  TE_OP_LAYERNORM_MLP_FWD_HOST = 8,
+  TE_OP_GEMM = 9 /* dims = {M, K, N}, dtype = the operands' dtype */
 } te_op;
 
 /* Human-readable name of a status code (static storage, never NULL). */
@@ -128,7 +129,10 @@ te_status te_selftest_wait_timeout(int64_t limit_us, void* stream);
 
 /* Bytes of workspace a call needs.  dims = {M, H, F or N}; `dtype` is the activation dtype,
  * `quantized` is nonzero when a quantizer set is passed, `kernel_dtype` the weights' storage
- * dtype.  Unused dims may be 0.  Returns 0 for operations that need none. */
+ * dtype.  Unused dims may be 0.  Returns 0 for operations that need none.
+ * The size includes, at its end, scratch for splitting the GEMMs' last partial wave of tiles
+ * along K; it depends on the current device's SM count (none without a device).  A workspace
+ * that stops short of that scratch is accepted: the call then splits no tile. */
 size_t te_workspace_size(te_op op, int64_t M, int64_t H, int64_t F_or_N, te_dtype dtype,
                          int quantized, te_dtype kernel_dtype, te_act_type act);
 
@@ -217,12 +221,17 @@ te_status te_update_scales(const te_quantizer* qs, int n, void* stream);
  *   a_scale_inv, b_scale_inv  device fp32 scalars or NULL (= 1); alpha is their product.
  *   bias          [N] in bias_dtype (TE_F32 / TE_BF16) or NULL.
  *   D             [M, N] in d_dtype (TE_F32 / TE_BF16).
+ *   workspace     NULL, or te_workspace_size(TE_OP_GEMM, M, K, N, ab_dtype, ...) bytes,
+ *                 16-byte aligned: with it, the tiles of the last partial wave are split along
+ *                 K over the idle SM pairs (their fp32 partial sums added in a fixed order, so
+ *                 repeated calls give identical results; the rounding differs from the unsplit
+ *                 sum within fp32 accumulation error).
  * M >= 1; N and K multiples of 16.
  */
 te_status te_gemm(const void* A, int a_trans, const void* B, int b_trans, te_dtype ab_dtype,
                   int64_t M, int64_t N, int64_t K, const float* a_scale_inv,
                   const float* b_scale_inv, const void* bias, te_dtype bias_dtype, void* D,
-                  te_dtype d_dtype, void* stream);
+                  te_dtype d_dtype, void* workspace, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------------------
  * te_layernorm_dense_fwd -- out = norm(x) @ kernel + bias (LayerNorm Dense page, Description

@@ -62,9 +62,12 @@ def test_invalid_arguments_rejected_before_launch():
     # misaligned pointers and row lengths that are not whole 16-byte vectors
     assert lib.te_quantize(8, b.TE_BF16, 1, 12, None, 16, None) == b.TE_ERR_INVALID_ARG
     assert lib.te_gemm(16, 0, 32, 0, b.TE_BF16, 16, 24, 16, None, None, None, b.TE_F32, 64,
-                       b.TE_BF16, None) == b.TE_ERR_UNSUPPORTED
+                       b.TE_BF16, None, 0, None) == b.TE_ERR_UNSUPPORTED
     assert lib.te_gemm(18, 0, 32, 0, b.TE_BF16, 16, 32, 16, None, None, None, b.TE_F32, 64,
-                       b.TE_BF16, None) == b.TE_ERR_UNSUPPORTED
+                       b.TE_BF16, None, 0, None) == b.TE_ERR_UNSUPPORTED
+    # a misaligned split-K workspace
+    assert lib.te_gemm(16, 0, 32, 0, b.TE_BF16, 16, 32, 16, None, None, None, b.TE_F32, 64,
+                       b.TE_BF16, 72, 4096, None) == b.TE_ERR_UNSUPPORTED
 
 
 def test_selftest_limit_checked_on_the_host():

@@ -153,6 +153,21 @@ def test_mlp_small_other_gated(act, fp8):
     check_mlp(inp, got, ref, fp8=fp8)
 
 
+@pytest.mark.parametrize("shape", [dict(M=300, H=8192, F=784), dict(M=300, H=512, F=16384)])
+@pytest.mark.parametrize("fp8", [False, True])
+def test_mlp_split_k(shape, fp8):
+    """Few tiles and a long contraction, so the library splits GEMM1 (the gated SwiGLU epilogue,
+    K = H = 8192; bf16 only: E4M3 k-blocks are twice as deep, too few to split) or GEMM2 (K = F =
+    16384) along K: element by element against the oracle, and bit-identical on a second call."""
+    inp = make_inputs("llama_rms_mlp", device=DEV, **shape)
+    got = run_mlp(inp, fp8=fp8)
+    again = run_mlp(inp, fp8=fp8)
+    for k in ("out", "h", "act"):
+        assert torch.equal(got[k], again[k]), k
+    ref = oracle_mlp(inp, fp8=fp8)
+    check_mlp(inp, got, ref, fp8=fp8)
+
+
 @pytest.mark.parametrize("name,shape", SMALL[1:])
 def test_mlp_small_fp8(name, shape):
     inp = make_inputs(name, device=DEV, **shape)

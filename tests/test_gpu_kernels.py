@@ -448,6 +448,54 @@ def test_gemm_e4m3(a_trans, b_trans):
 
 @pytest.mark.parametrize("kind", ["bf16", "e4m3"])
 @pytest.mark.parametrize("a_trans,b_trans", [(False, False), (False, True), (True, False)])
+@pytest.mark.parametrize("M,N,K", [(300, 528, 16400), (1040, 272, 16384), (256, 256, 16384)])
+def test_gemm_split_k(kind, a_trans, b_trans, M, N, K):
+    """Tiles split along K (fewer tiles than SM pairs, long K; a ragged last k-block at
+    K = 16400, ragged M and N): against the oracle, against the unsplit GEMM within the fp32
+    accumulation window, bit-identical on repeated calls (the partial sums are added in chunk
+    order), and nothing written outside the output or the workspace."""
+    if a_trans and M % 16:
+        M += 16 - M % 16
+    A = rt((K, M) if a_trans else (M, K), std=1.0, seed=M + 31, dtype="f32")
+    B = rt((N, K) if b_trans else (K, N), std=1.0, seed=N + 32, dtype="f32")
+    bias = rt((N,), 0.5, 33)
+    if kind == "bf16":
+        A, B = A.to(torch.bfloat16), B.to(torch.bfloat16)
+        a, b = np64(A), np64(B)
+        sa = sb = None
+        alpha = 1.0
+        ab = te.binding.TE_BF16
+    else:
+        A = (A * 64).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8)
+        B = (B * 64).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8)
+        a, b = nx.e4m3_decode(codes(A)), nx.e4m3_decode(codes(B))
+        sa = torch.tensor([1 / 64.0], device=DEV)
+        sb = torch.tensor([1 / 64.0], device=DEV)
+        alpha = ob.gemm_alpha(1 / 64.0, 1 / 64.0)
+        ab = te.binding.TE_E4M3
+    nws = te.workspace_size(te.binding.TE_OP_GEMM, M, K, N, ab)
+    assert nws > 0, "these shapes leave SM pairs idle: the library should split them"
+    ws = Guarded((nws,), torch.uint8)
+    outs = []
+    for split in (True, True, False):
+        g = Guarded((M, N), torch.float32)
+        te.te_gemm(A, B, g.t, a_trans=a_trans, b_trans=b_trans, a_scale_inv=sa, b_scale_inv=sb,
+                   bias=bias, workspace=ws.t if split else None, split_k=split)
+        g.check("split-K gemm out")
+        outs.append(np64(g.t))
+    ws.check("split-K workspace")
+    assert np.array_equal(outs[0], outs[1]), "split-K result differs between two calls"
+    a = a.T if a_trans else a
+    b = b.T if b_trans else b
+    ref = ob.gemm(a, b, np64(bias), alpha)
+    absdot = np.abs(a) @ np.abs(b) * abs(alpha)
+    for got, what in ((outs[0], "split"), (outs[2], "unsplit")):
+        ratio = float((np.abs(got - ref) / absdot).max())
+        assert ratio <= ACC_REL, f"{what}: {ratio:.3e} > ACC_REL {ACC_REL:.3e}"
+
+
+@pytest.mark.parametrize("kind", ["bf16", "e4m3"])
+@pytest.mark.parametrize("a_trans,b_trans", [(False, False), (False, True), (True, False)])
 @pytest.mark.parametrize("K", [512, 4096, 16384])
 def test_gemm_accumulation_window(kind, a_trans, b_trans, K):
     """The fp32 accumulation error of the tensor-core GEMMs against the exact (float64) sum,
