@@ -577,13 +577,33 @@ def run_ours(args, rank, world, local_rank):
     # out) and at the GPT / QKV shapes (LayerNorm, bf16 and E4M3 out), dact+dbias+quantize and
     # the norm backward
     bwk = {}
+    probe_buf = {}
 
-    def time_bw(name, fn, shape, nbytes):
+    def stream_ref(nbytes, ratio):
+        """GB/s of the library's streaming reference kernel moving the same bytes in the same
+        read:write ratio (te_stream_probe), timed like the kernel."""
+        w = nbytes // (ratio + 1) // 16 * 16
+        for key, need in (("src", w * ratio), ("dst", w)):
+            if key not in probe_buf or probe_buf[key].numel() < need:
+                probe_buf.pop(key, None)
+                probe_buf[key] = torch.ones(need, dtype=torch.uint8, device=dev)
+        fn = lambda: te.stream_probe(probe_buf["src"], probe_buf["dst"], write_bytes=w,
+                                     ratio=ratio)
+        for _ in range(args.warmup):
+            flush()
+            fn()
+        ms_p = max_over_ranks(statistics.mean(time_steps(fn, args.steps, flush)))
+        return w * (ratio + 1) / (ms_p / 1e3) / 1e9
+
+    def time_bw(name, fn, shape, nbytes, ratio):
         for _ in range(args.warmup):
             flush()
             fn()
         ms_k = max_over_ranks(statistics.mean(time_steps(fn, args.steps, flush)))
         bwk[name] = bw_entry(shape, nbytes, ms_k, peaks)
+        ref = stream_ref(nbytes, ratio)
+        bwk[name]["stream_ref"] = {"GB/s": ref, "reads_per_write": ratio,
+                                   "frac_of_stream": bwk[name]["GB/s"] / ref}
 
     mu = torch.empty(M, dtype=torch.float32, device=dev)
     rs = torch.empty(M, dtype=torch.float32, device=dev)
@@ -592,10 +612,10 @@ def run_ours(args, rank, world, local_rank):
     qn = te.Quantizer(float(qx.scale.item()), "delayed", dev)
     time_bw("norm_fwd", lambda: te.te_norm_fwd(x, gamma, beta, inp["norm"], True, inp["eps"],
                                                ln_out, mu=mu, rsigma=rs),
-            (M, H), M * H * (2 + 2) + H * 2 + M * 8)
+            (M, H), M * H * (2 + 2) + H * 2 + M * 8, 1)
     time_bw("norm_fwd_e4m3", lambda: te.te_norm_fwd(x, gamma, beta, inp["norm"], True,
                                                     inp["eps"], ln_out8, q=qn, mu=mu, rsigma=rs),
-            (M, H), M * H * (2 + 1) + H * 2 + M * 8)
+            (M, H), M * H * (2 + 1) + H * 2 + M * 8, 2)
     del ln_out, ln_out8
     for tag, (Mn_, Hn_) in (("gpt", (16384, 4096)), ("qkv", (16384, 8192))):
         xg = random_tensor((Mn_, Hn_), device=dev, seed=7)
@@ -609,11 +629,11 @@ def run_ours(args, rank, world, local_rank):
         if tag == "gpt":
             time_bw("norm_fwd_gpt", lambda: te.te_norm_fwd(xg, gg, bg, "layernorm", False, 1e-6,
                                                            yb, mu=mug, rsigma=rsg),
-                    (Mn_, Hn_), Mn_ * Hn_ * 4 + Hn_ * 4 + Mn_ * 8)
+                    (Mn_, Hn_), Mn_ * Hn_ * 4 + Hn_ * 4 + Mn_ * 8, 1)
         time_bw(f"norm_fwd_{tag}_e4m3", lambda: te.te_norm_fwd(xg, gg, bg, "layernorm", False,
                                                                1e-6, y8, q=qg8, mu=mug,
                                                                rsigma=rsg),
-                (Mn_, Hn_), Mn_ * Hn_ * 3 + Hn_ * 4 + Mn_ * 8)
+                (Mn_, Hn_), Mn_ * Hn_ * 3 + Hn_ * 4 + Mn_ * 8, 2)
         del xg, yb, y8
     Md, Nd = 16384, 16384  # the GPT workload's activation gradient
     dyd = torch.randn(Md, Nd, device=dev, dtype=torch.bfloat16)
@@ -625,7 +645,7 @@ def run_ours(args, rank, world, local_rank):
                       device=dev)
     dact_step = lambda: te.te_dact_dbias_quantize(dyd, hd, "gelu", dxd, dbias=dbd, q=qd,
                                                   workspace=wsd)
-    time_bw("dact_dbias_quantize", dact_step, (Md, Nd), Md * Nd * (2 + 2 + 1) + Nd * 4)
+    time_bw("dact_dbias_quantize", dact_step, (Md, Nd), Md * Nd * (2 + 2 + 1) + Nd * 4, 4)
     del dyd, hd, dxd, wsd
     # the norm backward at the GPT workload's shape (LayerNorm, 16384 x 4096)
     Mn, Hn = 16384, 4096
@@ -641,8 +661,9 @@ def run_ours(args, rank, world, local_rank):
                       device=dev)
     nbwd_step = lambda: te.te_norm_bwd(dzn, xn, mun, rsn, gn, "layernorm", False, dxn, dgn,
                                        dbeta=dbn, workspace=wsn)
-    time_bw("norm_bwd", nbwd_step, (Mn, Hn), Mn * Hn * (2 + 2 + 2) + Mn * 8)
+    time_bw("norm_bwd", nbwd_step, (Mn, Hn), Mn * Hn * (2 + 2 + 2) + Mn * 8, 2)
     del xn, dzn, dxn, wsn
+    probe_buf.clear()
     barrier()
 
     # ---- the other workloads' hot paths: LN -> Dense (QKV) forward and backward, and the GPT

@@ -9,7 +9,7 @@ include/te_gb300.h.  This package is its thin Python binding; the functions keep
 from .binding import (ACT_TUPLES, ACT_TYPES, EXPORTED, KERNEL_KINDS, NORM_TYPES, Quantizer,
                       QuantizerSet, TEError, dact_dbias_noalloc_capacity, get_device_status, lib,
                       lib_path, profile_begin, profile_end, selftest_wait_timeout, status_string,
-                      te_act_lu,
+                      stream_probe, te_act_lu,
                       te_dact_dbias_quantize, te_dact_dbias_quantize_noalloc, te_gemm,
                       te_layernorm_dense_bwd, te_layernorm_dense_fwd, te_layernorm_mlp_bwd,
                       te_layernorm_mlp_fwd, te_layernorm_mlp_fwd_host, te_norm_bwd, te_norm_fwd,
@@ -23,4 +23,4 @@ __all__ = ["Quantizer", "QuantizerSet", "TEError", "te_norm_fwd", "te_act_lu",
            "get_device_status", "status_string", "workspace_size", "EXPORTED", "ACT_TYPES",
            "ACT_TUPLES", "NORM_TYPES", "KERNEL_KINDS", "profile_begin", "profile_end",
            "te_dact_dbias_quantize_noalloc", "dact_dbias_noalloc_capacity",
-           "selftest_wait_timeout", "te_layernorm_mlp_fwd_host"]
+           "selftest_wait_timeout", "te_layernorm_mlp_fwd_host", "stream_probe"]

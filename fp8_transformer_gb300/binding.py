@@ -43,7 +43,7 @@ EXPORTED = ["te_status_string", "te_version", "te_get_device_status", "te_worksp
             "te_layernorm_dense_bwd",
             "te_dact_dbias_quantize_noalloc",
             "te_dact_dbias_noalloc_capacity", "te_selftest_wait_timeout",
-            "te_layernorm_mlp_fwd_host", "te_update_scales"]
+            "te_layernorm_mlp_fwd_host", "te_update_scales", "te_stream_probe"]
 KERNEL_KINDS = ["norm_fwd", "quantize", "act_lu", "dact_dbias", "gemm", "gemm_act", "norm_bwd",
                 "transpose"]
 
@@ -117,6 +117,7 @@ _SIGS = {
     "te_dact_dbias_noalloc_capacity": (_sz, []),
     "te_profile_end": (ctypes.c_int, [ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_int32)]),
     "te_update_scales": (ctypes.c_int, [_QP, ctypes.c_int, _vp]),
+    "te_stream_probe": (ctypes.c_int, [_vp, _vp, _sz, ctypes.c_int, _sz, _vp]),
 }
 
 
@@ -448,6 +449,13 @@ def te_norm_bwd(dz, x, mu, rsigma, gamma, norm_type, zero_centered_gamma, dx, dg
 def profile_begin(max_records: int = 4096):
     """Start timing every library kernel launch with CUDA events on its launching stream."""
     _check("te_profile_begin", lib().te_profile_begin(int(max_records)))
+
+
+def stream_probe(src, dst=None, write_bytes=0, ratio=1, read_only_bytes=0, stream=None):
+    """One launch of the library's streaming reference kernel (te_stream_probe)."""
+    _check("te_stream_probe", lib().te_stream_probe(_ptr(src), _ptr(dst), int(write_bytes),
+                                                     int(ratio), int(read_only_bytes),
+                                                     _stream(stream)))
 
 
 def profile_end() -> dict:

@@ -153,6 +153,11 @@ te_status read_and_clear_device_status(int32_t* out);
 
 int num_sms();
 
+// The streaming reference of te_stream_probe (n_out 16-byte vectors written, each from `ratio`
+// read; n_out = 0: n_read vectors read only).
+te_status launch_stream_probe(const uint4* src, uint4* dst, size_t n_out, int ratio,
+                              size_t n_read, cudaStream_t s);
+
 // Launches `kernel` as a programmatic dependent of the work queued before it on `s`: its launch
 // may overlap the previous kernel's tail once every CTA of that kernel has executed
 // griddepcontrol.launch_dependents (or exited), and the kernel itself executes

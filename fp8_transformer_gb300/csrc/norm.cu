@@ -35,7 +35,7 @@ namespace {
 constexpr size_t kRingSmemMax = 224 * 1024;  // dynamic shared memory per CTA
 constexpr int kFwdGroupWarps = 4;            // forward: warps per CTA (one row at a time)
 constexpr int kFwdRowsCtasPerSm = 8;         // forward: register budget, CTAs per SM
-constexpr int kBwdWarps = 8;                 // backward: warps per CTA, all sharing each row
+constexpr int kBwdWarps = 8;                 // backward: warps per SM, in one or two CTAs
 constexpr int kBwdRowsPerSync = 4;           // backward: rows per barrier (at most)
 constexpr int kBwdMaxSlots = 16;
 
@@ -284,10 +284,14 @@ __global__ void __launch_bounds__(kFwdGroupWarps * 32, NVL >= 8 ? kFwdRowsCtasPe
 // Forward with one row per warp, for rows of exactly NVW x 32 vectors: the row's sums meet by
 // shuffles within the warp, with no barrier between warps; the CTA's kFwdWarpRowWarps warps
 // share the gain / beta table in shared memory (the layout above).  Each lane holds its NVW
-// vectors of one row at a time; the many warps per SM keep rows in flight.
+// vectors of one row (PIPE: of two rows, the next one loading while the current one is worked
+// on); the many warps per SM keep rows in flight.
 constexpr int kFwdWarpRowWarps = 4;
-template <typename T, bool LN, int NVW>
-__global__ void __launch_bounds__(kFwdWarpRowWarps * 32, NVW * Vec16<T>::N >= 128 ? 3 : 4)
+__host__ __device__ constexpr int fwd_warp_ctas(int elems_per_lane, bool pipe) {
+  return pipe ? (elems_per_lane >= 128 ? 2 : 3) : (elems_per_lane >= 128 ? 3 : 4);
+}
+template <typename T, bool LN, int NVW, bool PIPE>
+__global__ void __launch_bounds__(kFwdWarpRowWarps * 32, fwd_warp_ctas(NVW * Vec16<T>::N, PIPE))
     norm_fwd_warp_kernel(NormFwdArgs a) {
   // the kernel after this one may launch its setup now (it waits for this grid's completion)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -325,11 +329,28 @@ __global__ void __launch_bounds__(kFwdWarpRowWarps * 32, NVW * Vec16<T>::N >= 12
     constexpr int OUT = decltype(tag)::value;
     constexpr bool AMAX = decltype(atag)::value;
     const int64_t step = int64_t(gridDim.x) * kFwdWarpRowWarps;
-    for (int64_t r = int64_t(blockIdx.x) * kFwdWarpRowWarps + warp; r < a.M; r += step) {
-      const uint4* xr = reinterpret_cast<const uint4*>(x + r * a.H) + lane;
-      uint4 cur[NVW];
+    const int64_t r_first = int64_t(blockIdx.x) * kFwdWarpRowWarps + warp;
+    uint4 cur[NVW];
+    if (PIPE && r_first < a.M) {
+      const uint4* xr = reinterpret_cast<const uint4*>(x + r_first * a.H) + lane;
 #pragma unroll
       for (int i = 0; i < NVW; ++i) cur[i] = __ldg(xr + 32 * i);
+    }
+    for (int64_t r = r_first; r < a.M; r += step) {
+      // PIPE: the warp's next row is requested before this row's arithmetic, so that a row's
+      // loads are always in flight
+      uint4 nxt[NVW];
+      if (PIPE) {
+        if (r + step < a.M) {
+          const uint4* xn = reinterpret_cast<const uint4*>(x + (r + step) * a.H) + lane;
+#pragma unroll
+          for (int i = 0; i < NVW; ++i) nxt[i] = __ldg(xn + 32 * i);
+        }
+      } else {
+        const uint4* xr = reinterpret_cast<const uint4*>(x + r * a.H) + lane;
+#pragma unroll
+        for (int i = 0; i < NVW; ++i) cur[i] = __ldg(xr + 32 * i);
+      }
       // the row's first element, subtracted before the sums (shifted variance), from lane 0
       float x0 = 0.0f;
       if (LN) {
@@ -406,6 +427,10 @@ __global__ void __launch_bounds__(kFwdWarpRowWarps * 32, NVW * Vec16<T>::N >= 12
           // one vector's gain / beta loads at a time: hoisting all of them spills
           asm volatile("" ::: "memory");
         }
+      }
+      if (PIPE) {
+#pragma unroll
+        for (int i = 0; i < NVW; ++i) cur[i] = nxt[i];
       }
     }
   });
@@ -619,13 +644,18 @@ __global__ void __launch_bounds__(kFwdRingWarps * 32, 1)
   if (lane == 0 && a.cast.amax_out) atomic_max_nonneg(a.cast.amax_out, amax);
 }
 
-// Sets the kernel's dynamic shared memory limit once per device.
+// Sets the kernel's dynamic shared memory limit once per device; `max_carveout` also asks for
+// the largest shared-memory share of the SM's L1 (for two large-ring CTAs per SM; the forward
+// kernels, which read through L1, measured slower with it).
 template <typename K>
-te_status allow_ring_smem(K kernel, PerDevice<bool>& done) {
+te_status allow_ring_smem(K kernel, PerDevice<bool>& done, bool max_carveout = false) {
   bool ok = false;
   return done.get(&ok, [&](bool* v) {
            *v = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     int(kRingSmemMax)) == cudaSuccess;
+                                     int(kRingSmemMax)) == cudaSuccess &&
+                (!max_carveout ||
+                 cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                      int(cudaSharedmemCarveoutMaxShared)) == cudaSuccess);
            return *v;
          })
              ? TE_OK
@@ -639,9 +669,10 @@ unsigned ring_grid(int64_t M) {
 
 // Ring size for `slot_bytes`-byte slots: as many as fit the shared memory (at most
 // max_slots), rounded down to a multiple of `mult`; 0 if fewer than `min_slots` fit.
-int ring_slots(size_t slot_bytes, int max_slots, int min_slots, int mult) {
+int ring_slots(size_t slot_bytes, int max_slots, int min_slots, int mult,
+               size_t max_bytes = kRingSmemMax) {
   int slots = max_slots;
-  while (slots > 0 && ring_header_bytes(slots) + size_t(slots) * slot_bytes > kRingSmemMax)
+  while (slots > 0 && ring_header_bytes(slots) + size_t(slots) * slot_bytes > max_bytes)
     --slots;
   slots -= slots % mult;
   return slots >= min_slots ? slots : 0;
@@ -680,21 +711,21 @@ te_status launch_fwd_rows(const NormFwdArgs& a_in, cudaStream_t s) {
   return cudaGetLastError() == cudaSuccess ? TE_OK : TE_ERR_CUDA;
 }
 
-template <typename T, bool LN, int NVW>
+template <typename T, bool LN, int NVW, bool PIPE>
 te_status launch_fwd_warp(const NormFwdArgs& a, cudaStream_t s) {
   static PerDevice<bool> attr_done;
   const size_t params = size_t(a.H) * (LN ? 2 : 1) * sizeof(float);
-  const te_status st = allow_ring_smem(norm_fwd_warp_kernel<T, LN, NVW>, attr_done);
+  const te_status st = allow_ring_smem(norm_fwd_warp_kernel<T, LN, NVW, PIPE>, attr_done);
   if (st != TE_OK) return st;
   int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, norm_fwd_warp_kernel<T, LN, NVW>,
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, norm_fwd_warp_kernel<T, LN, NVW, PIPE>,
                                                     kFwdWarpRowWarps * 32, params) != cudaSuccess ||
       per_sm < 1)
     per_sm = 1;
   const int64_t cap = int64_t(num_sms()) * per_sm;
   const int64_t ctas = ceil_div(a.M, kFwdWarpRowWarps);
   const unsigned grid = unsigned(ctas < cap ? ctas : cap);
-  norm_fwd_warp_kernel<T, LN, NVW><<<grid, kFwdWarpRowWarps * 32, params, s>>>(a);
+  norm_fwd_warp_kernel<T, LN, NVW, PIPE><<<grid, kFwdWarpRowWarps * 32, params, s>>>(a);
   return cudaGetLastError() == cudaSuccess ? TE_OK : TE_ERR_CUDA;
 }
 
@@ -734,24 +765,30 @@ te_status launch_fwd_ring(const NormFwdArgs& a, int slots, cudaStream_t s) {
 // of the grid gets at least kFwdRingMinRows of them: the staged kernel streams faster but starts
 // slower (measured on 4096-wide bf16 rows: 85% against 82% of the copy bandwidth at 16384 rows,
 // 75% against 80% at 8192 rows; slower at every shorter width).  Other rows are loaded straight
-// into registers.  TE_NORM_FWD_KERNEL=warp or =ring in the environment forces one kernel (a
-// switch between two complete kernels, for measurements); a row too long for two ring slots per
-// warp always takes the register kernel.
+// into registers, each warp requesting its next row before the current row's arithmetic (with
+// two rows in registers, fewer warps fit an SM; measured against one row at a time: equal with
+// bf16 output and 1% faster with E4M3 at 8192 x 4096, 3% faster at 8192 x 2048).
+// TE_NORM_FWD_KERNEL=warp (one row at a time), =pipe or =ring in the environment forces one
+// kernel (a switch between complete kernels, for measurements); a row too long for two ring
+// slots per warp always takes a register kernel.
 constexpr int64_t kFwdRingMinRows = 6;
 
 template <typename T, int NVW>
 te_status launch_fwd_nvw(const NormFwdArgs& a, cudaStream_t s) {
   static const int forced = [] {
     const char* e = getenv("TE_NORM_FWD_KERNEL");
-    return !e ? 0 : e[0] == 'w' ? 1 : e[0] == 'r' ? 2 : 0;
+    return !e ? 0 : e[0] == 'w' ? 1 : e[0] == 'r' ? 2 : e[0] == 'p' ? 3 : 0;
   }();
   const bool ln = a.norm_type == TE_LAYERNORM;
   const int slots = fwd_ring_slots(size_t(NVW) * 32 * 16, size_t(a.H) * (ln ? 2 : 1) * 4);
   const bool long_run = a.M >= kFwdRingMinRows * kFwdRingWarps * num_sms();
   const bool ring = forced == 2 || (forced == 0 && NVW == 16 && long_run);
+  // (forced == 3: the pipelined register kernel, also for long runs)
   if (ring && slots >= 2)
     return ln ? launch_fwd_ring<T, true, NVW>(a, slots, s) : launch_fwd_ring<T, false, NVW>(a, slots, s);
-  return ln ? launch_fwd_warp<T, true, NVW>(a, s) : launch_fwd_warp<T, false, NVW>(a, s);
+  if (forced == 1)
+    return ln ? launch_fwd_warp<T, true, NVW, false>(a, s) : launch_fwd_warp<T, false, NVW, false>(a, s);
+  return ln ? launch_fwd_warp<T, true, NVW, true>(a, s) : launch_fwd_warp<T, false, NVW, true>(a, s);
 }
 
 template <typename T, int NVL>
@@ -793,8 +830,8 @@ te_status launch_fwd_t(const NormFwdArgs& a, cudaStream_t s) {
 
 // ----------------------------------------------------------------------- backward --------
 
-// All kBwdWarps warps of a CTA share each of its rows: thread t owns the 16-byte vectors t,
-// t + 32 * kBwdWarps, ... of the row (NV of them), with its gamma vectors and dgamma / dbeta
+// All G warps of a CTA share each of its rows: thread t owns the 16-byte vectors t,
+// t + 32 * G, ... of the row (NV of them), with its gamma vectors and dgamma / dbeta
 // accumulators in registers.  The CTA's rows (local rows 0, 1, ...) go round a ring of `spc`
 // slots, each holding one row of x followed by the same row of dz; RB consecutive rows form a
 // step, whose row sums meet in shared memory at one named barrier, which also carries each
@@ -806,13 +843,12 @@ te_status launch_fwd_t(const NormFwdArgs& a, cudaStream_t s) {
 // pass instead of reading and converting the slot again.
 __host__ __device__ constexpr int bwd_rows_per_sync(int nv) { return nv >= 4 ? 1 : kBwdRowsPerSync; }
 
-template <typename T, bool LN, int NV, bool FULL>
-__global__ void __launch_bounds__(kBwdWarps * 32, 1)
+template <typename T, bool LN, int NV, bool FULL, int G>
+__global__ void __launch_bounds__(G * 32, kBwdWarps / G)
     norm_bwd_ring_kernel(NormBwdArgs a, int* status, int spc) {
   using PR = Pairs<T>;
   constexpr int E = Vec16<T>::N;
   constexpr int P = PR::P;
-  constexpr int G = kBwdWarps;
   constexpr int GT = G * 32;
   constexpr int RB = bwd_rows_per_sync(NV);
   extern __shared__ __align__(128) uint8_t smem[];
@@ -1077,22 +1113,33 @@ __global__ void __launch_bounds__(kRedWarps * 32) norm_bwd_reduce_kernel(const f
   }
 }
 
-// Partial dgamma / dbeta rows: one per CTA.
-int bwd_chunks(int64_t M) { return int(ring_grid(M > 0 ? M : 1)); }
+// CTAs of the backward on one SM: kBwdWarps / G.  Each takes an equal share of the SM's shared
+// memory for its ring.
+constexpr size_t kBwdSmPerSm = 227 * 1024;  // dynamic shared memory all CTAs of an SM may hold
 
-template <typename T, bool LN, int NV, bool FULL>
+int64_t bwd_grid(int64_t M, int ctas_per_sm) {
+  const int64_t n = int64_t(num_sms()) * ctas_per_sm;
+  return M < n ? (M > 0 ? M : 1) : n;
+}
+
+// Partial dgamma / dbeta rows: one per CTA (at most two CTAs per SM).
+int bwd_chunks(int64_t M) { return int(bwd_grid(M, 2)); }
+
+template <typename T, bool LN, int NV, bool FULL, int G>
 te_status launch_bwd_t(const NormBwdArgs& a, cudaStream_t s) {
   static PerDevice<bool> attr_done;
   constexpr int RB = bwd_rows_per_sync(NV);
+  constexpr int kCtas = kBwdWarps / G;
   const size_t slot_bytes = size_t(a.H) * sizeof(T) * 2;
   // a step holds RB slots; a second step's worth lets the refills run ahead
-  const int spc = ring_slots(slot_bytes, kBwdMaxSlots, 2 * RB, RB);
+  const size_t cap = kCtas == 1 ? kRingSmemMax : kBwdSmPerSm / kCtas - 1024;
+  const int spc = ring_slots(slot_bytes, kBwdMaxSlots, 2 * RB, RB, cap);
   if (spc == 0) return TE_ERR_UNSUPPORTED;
   const size_t smem = ring_header_bytes(spc) + size_t(spc) * slot_bytes;
-  const te_status st = allow_ring_smem(norm_bwd_ring_kernel<T, LN, NV, FULL>, attr_done);
+  const te_status st = allow_ring_smem(norm_bwd_ring_kernel<T, LN, NV, FULL, G>, attr_done, kCtas > 1);
   if (st != TE_OK) return st;
-  const unsigned grid = ring_grid(a.M);
-  norm_bwd_ring_kernel<T, LN, NV, FULL><<<grid, kBwdWarps * 32, smem, s>>>(
+  const unsigned grid = unsigned(bwd_grid(a.M, kCtas));
+  norm_bwd_ring_kernel<T, LN, NV, FULL, G><<<grid, G * 32, smem, s>>>(
       a, device_status_ptr(), spc);
   if (cudaGetLastError() != cudaSuccess) return TE_ERR_CUDA;
   // the column sums: their launch overlaps the ring kernel's tail (griddepcontrol.wait in the
@@ -1102,27 +1149,34 @@ te_status launch_bwd_t(const NormBwdArgs& a, cudaStream_t s) {
                           int(grid), int64_t(a.H), a.dgamma, a.dbeta);
 }
 
-template <typename T, int NV>
+template <typename T, int NV, int G>
 te_status launch_bwd_nv(const NormBwdArgs& a, cudaStream_t s) {
-  const bool full = a.H / Vec16<T>::N == int64_t(NV) * kBwdWarps * 32;
+  const bool full = a.H / Vec16<T>::N == int64_t(NV) * G * 32;
   if (a.norm_type == TE_LAYERNORM)
-    return full ? launch_bwd_t<T, true, NV, true>(a, s) : launch_bwd_t<T, true, NV, false>(a, s);
-  return full ? launch_bwd_t<T, false, NV, true>(a, s) : launch_bwd_t<T, false, NV, false>(a, s);
+    return full ? launch_bwd_t<T, true, NV, true, G>(a, s) : launch_bwd_t<T, true, NV, false, G>(a, s);
+  return full ? launch_bwd_t<T, false, NV, true, G>(a, s) : launch_bwd_t<T, false, NV, false, G>(a, s);
 }
 
+// Rows of up to 512 vectors (8 KB) go to two CTAs of 4 warps per SM, each thread holding up to
+// 4 vectors of a row; longer rows (up to 1024 vectors, 16 KB) to one CTA of 8 warps.  Four
+// vectors per thread per row keep the per-row barrier and ring bookkeeping small against the
+// row's arithmetic, and two CTAs keep two rows in work per SM: LayerNorm at 16384 x 4096 went
+// from 78% to 84% of the measured copy bandwidth, at 16384 x 2048 / 1024 by a third / a half.
+// RMSNorm rows of 257 .. 512 vectors (less arithmetic per element) measured 1% faster with one
+// CTA of 8 warps and keep it.
 template <typename T>
 te_status launch_bwd_dispatch(const NormBwdArgs& a, cudaStream_t s) {
   constexpr int E = Vec16<T>::N;
-  // rows are at most 16 KB, i.e. 1024 vectors
-  constexpr int kMaxNV = (1024 + kBwdWarps * 32 - 1) / (kBwdWarps * 32);
-  const int64_t per_thread = ceil_div(a.H / E, kBwdWarps * 32);
-  if (per_thread <= 1) return launch_bwd_nv<T, 1>(a, s);
-  if constexpr (kMaxNV >= 2) {
-    if (per_thread <= 2) return launch_bwd_nv<T, 2>(a, s);
+  const int64_t nvec = a.H / E;
+  const int64_t two_cta_max = a.norm_type == TE_LAYERNORM ? 4 * 4 * 32 : 2 * 4 * 32;
+  if (nvec <= two_cta_max) {
+    const int64_t per_thread = ceil_div(nvec, int64_t(4 * 32));
+    if (per_thread <= 1) return launch_bwd_nv<T, 1, 4>(a, s);
+    if (per_thread <= 2) return launch_bwd_nv<T, 2, 4>(a, s);
+    return launch_bwd_nv<T, 4, 4>(a, s);
   }
-  if constexpr (kMaxNV >= 4) {
-    if (per_thread <= 4) return launch_bwd_nv<T, 4>(a, s);
-  }
+  if (nvec <= 2 * kBwdWarps * 32) return launch_bwd_nv<T, 2, kBwdWarps>(a, s);
+  if (nvec <= 4 * kBwdWarps * 32) return launch_bwd_nv<T, 4, kBwdWarps>(a, s);
   return TE_ERR_UNSUPPORTED;
 }
 

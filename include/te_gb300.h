@@ -417,6 +417,17 @@ typedef enum {
 te_status te_profile_begin(int32_t max_records);
 te_status te_profile_end(float* total_ms, int32_t* launches);
 
+/* Streaming reference (no counterpart on the pages; used by benchmarks).  One launch of a plain
+ * kernel that moves a bandwidth-bound kernel's traffic with no arithmetic: it reads
+ * `ratio` x `write_bytes` bytes from `src` and writes `write_bytes` bytes to `dst`, each
+ * 16-byte vector of dst from the next `ratio` vectors of src; write_bytes = 0 reads
+ * `read_only_bytes` from src and writes nothing.  Its time is the floor a kernel with the same
+ * traffic, size and access order can reach, below the bandwidth of a long copy for short
+ * kernels.  src, dst 16-byte aligned, byte counts multiples of 16, ratio 1 .. 8; otherwise
+ * TE_ERR_INVALID_ARG. */
+te_status te_stream_probe(const void* src, void* dst, size_t write_bytes, int ratio,
+                          size_t read_only_bytes, void* stream);
+
 /* ---------------------------------------------------------------------------------------
  * te_dact_dbias_quantize_noalloc -- te_dact_dbias_quantize for callers that cannot allocate
  * device memory at the call (no counterpart on the pages; an addition of this library).

@@ -65,6 +65,10 @@ def test_invalid_arguments_rejected_before_launch():
                        b.TE_BF16, None, 0, None) == b.TE_ERR_UNSUPPORTED
     assert lib.te_gemm(18, 0, 32, 0, b.TE_BF16, 16, 32, 16, None, None, None, b.TE_F32, 64,
                        b.TE_BF16, None, 0, None) == b.TE_ERR_UNSUPPORTED
+    # the streaming reference: bad ratio, misaligned pointer, byte count not a multiple of 16
+    assert lib.te_stream_probe(16, 32, 64, 0, 0, None) == b.TE_ERR_INVALID_ARG
+    assert lib.te_stream_probe(16, 40, 64, 2, 0, None) == b.TE_ERR_INVALID_ARG
+    assert lib.te_stream_probe(16, 32, 0, 1, 24, None) == b.TE_ERR_INVALID_ARG
     # a misaligned split-K workspace
     assert lib.te_gemm(16, 0, 32, 0, b.TE_BF16, 16, 32, 16, None, None, None, b.TE_F32, 64,
                        b.TE_BF16, 72, 4096, None) == b.TE_ERR_UNSUPPORTED
