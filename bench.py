@@ -339,6 +339,20 @@ def bandwidth_kernels(args, dev, peaks):
     run("norm_fwd_gpt_e4m3", lambda: te.te_norm_fwd(xg, gg, bg, "layernorm", False, 1e-6, yg8,
                                                     q=q, mu=mug, rsigma=rsg), Mb * H * 3 + Mb * 8)
     del xg, yg, yg8, mug, rsg
+    # the QKV workload's LayerNorm (16384 x 8192: the 8-warp row-sharing kernel)
+    Hq = 8192
+    xq = random_tensor((Mb, Hq), device=dev, seed=10)
+    gq = random_tensor((Hq,), std=0.1, mean=1.0, device=dev, seed=11)
+    bq = random_tensor((Hq,), std=0.1, device=dev, seed=12)
+    yq = torch.empty(Mb, Hq, dtype=torch.bfloat16, device=dev)
+    yq8 = torch.empty(Mb, Hq, dtype=torch.uint8, device=dev)
+    muq = torch.empty(Mb, dtype=torch.float32, device=dev)
+    rsq = torch.empty(Mb, dtype=torch.float32, device=dev)
+    run("norm_fwd_qkv_bf16", lambda: te.te_norm_fwd(xq, gq, bq, "layernorm", False, 1e-5, yq,
+                                                    mu=muq, rsigma=rsq), Mb * Hq * 4 + Mb * 8)
+    run("norm_fwd_qkv_e4m3", lambda: te.te_norm_fwd(xq, gq, bq, "layernorm", False, 1e-5, yq8,
+                                                    q=q, mu=muq, rsigma=rsq), Mb * Hq * 3 + Mb * 8)
+    del xq, yq, yq8, muq, rsq
     h = random_tensor((Mb, F), std=2.0, device=dev, seed=3)
     da = random_tensor((Mb, F), device=dev, seed=4)
     a = torch.empty(Mb, F, dtype=torch.bfloat16, device=dev)
@@ -626,10 +640,9 @@ def run_ours(args, rank, world, local_rank):
         yb = torch.empty(Mn_, Hn_, dtype=torch.bfloat16, device=dev)
         y8 = torch.empty(Mn_, Hn_, dtype=torch.uint8, device=dev)
         qg8 = te.Quantizer(32.0, "delayed", dev)
-        if tag == "gpt":
-            time_bw("norm_fwd_gpt", lambda: te.te_norm_fwd(xg, gg, bg, "layernorm", False, 1e-6,
-                                                           yb, mu=mug, rsigma=rsg),
-                    (Mn_, Hn_), Mn_ * Hn_ * 4 + Hn_ * 4 + Mn_ * 8, 1)
+        time_bw(f"norm_fwd_{tag}", lambda: te.te_norm_fwd(xg, gg, bg, "layernorm", False, 1e-6,
+                                                          yb, mu=mug, rsigma=rsg),
+                (Mn_, Hn_), Mn_ * Hn_ * 4 + Hn_ * 4 + Mn_ * 8, 1)
         time_bw(f"norm_fwd_{tag}_e4m3", lambda: te.te_norm_fwd(xg, gg, bg, "layernorm", False,
                                                                1e-6, y8, q=qg8, mu=mug,
                                                                rsigma=rsg),

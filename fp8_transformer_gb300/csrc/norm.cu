@@ -662,11 +662,6 @@ te_status allow_ring_smem(K kernel, PerDevice<bool>& done, bool max_carveout = f
              : TE_ERR_CUDA;
 }
 
-unsigned ring_grid(int64_t M) {
-  const int64_t sms = num_sms();
-  return unsigned(M < sms ? M : sms);
-}
-
 // Ring size for `slot_bytes`-byte slots: as many as fit the shared memory (at most
 // max_slots), rounded down to a multiple of `mult`; 0 if fewer than `min_slots` fit.
 int ring_slots(size_t slot_bytes, int max_slots, int min_slots, int mult,
@@ -729,6 +724,232 @@ te_status launch_fwd_warp(const NormFwdArgs& a, cudaStream_t s) {
   return cudaGetLastError() == cudaSuccess ? TE_OK : TE_ERR_CUDA;
 }
 
+// Forward for long rows (exactly kFwdCtaWarps x 32 x NV 16-byte vectors: H = 8192 bf16 with
+// NV = 4): the 8 warps of one CTA per SM share each row, as in the backward.  The
+// CTA's rows (blockIdx.x, blockIdx.x + gridDim.x, ...) arrive by cp.async.bulk in a ring of
+// `spc` shared-memory slots of one row each (12 at 16 KB), so that up to 12 rows per SM are in
+// flight without occupying registers.  The CTA works on RB rows at a time: each thread takes
+// its NV vectors of each of them into registers and releases their slots; its gain and beta
+// vectors stay in registers for the whole kernel.  The warps' partial sums of the RB rows meet
+// at one named barrier (double-buffered, and carrying a failed wait so that the warps stop
+// together); after it one warp per row, in turn, waits for the slot's release and refills it
+// with the row `spc` ahead.  Every wait is bounded.
+constexpr int kFwdCtaWarps = 8;
+constexpr int kFwdCtaVecs = 1024 / (kFwdCtaWarps * 32);  // vectors per thread per row
+constexpr int kFwdCtaMaxSlots = 16;
+constexpr int kFwdCtaRows = 2;  // rows per barrier (measured: 1 and 4 slower; 16 warps slower)
+
+template <typename T, bool LN, int NV, int G>
+__global__ void __launch_bounds__(G * 32, 1)
+    norm_fwd_cta_kernel(NormFwdArgs a, int* status, int spc) {
+  // the kernel after this one may launch its setup now (it waits for this grid's completion)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  using PR = Pairs<T>;
+  constexpr int E = Vec16<T>::N;
+  constexpr int P = PR::P;
+  constexpr int GT = G * 32;
+  constexpr int RB = kFwdCtaRows;
+  constexpr uint32_t row_bytes = uint32_t(GT * NV) * 16u;
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ float2 red[2][RB][G];
+  __shared__ int last_use[kFwdCtaMaxSlots];  // the latest use issued into each slot
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+  uint64_t* empty = full + spc;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + spc);
+  uint8_t* ring = smem + ring_header_bytes(spc);
+  const char* xb = static_cast<const char*>(a.x);
+  const int64_t nloc = local_rows(a.M);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // local row k -> slot sl: its copy completes on full[sl]
+  auto issue = [&](int64_t k, int sl) {
+    const int64_t row = int64_t(blockIdx.x) + k * gridDim.x;
+    mbar_expect_tx(smem_u32(&full[sl]), row_bytes);
+    bulk_load(smem_u32(ring + size_t(sl) * row_bytes), xb + row * row_bytes, row_bytes,
+              smem_u32(&full[sl]));
+  };
+  if (tid < spc) last_use[tid] = -1;
+  ring_init(full, empty, spc, G, abort_flag);
+  if (tid == 0) {  // the first use of every slot (the barriers' init is fenced)
+    for (int k = 0; k < spc && k < nloc; ++k) {
+      issue(k, k);
+      last_use[k] = 0;
+    }
+  }
+  // this thread's gain (and beta) vectors, as fp32 pairs, while the first rows load
+  f32x2 gp[NV][P], bp[NV][P];
+  {
+    const f32x2 shift = f2s(a.zero_centered_gamma ? 1.0f : 0.0f);
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      const int v = tid + i * GT;
+      PR::cvt(__ldg(reinterpret_cast<const uint4*>(a.gamma) + v), gp[i]);
+      if (LN && a.beta) PR::cvt(__ldg(reinterpret_cast<const uint4*>(a.beta) + v), bp[i]);
+#pragma unroll
+      for (int p = 0; p < P; ++p) {
+        gp[i][p] = add2(gp[i][p], shift);
+        if (!LN || !a.beta) bp[i][p] = f2s(0.0f);
+      }
+    }
+  }
+  const CastState cs = cast_begin(a.cast);
+  const float inv_h = 1.0f / float(a.H);
+  const bool want_amax = a.cast.amax_out != nullptr;
+  float am[P];
+#pragma unroll
+  for (int p = 0; p < P; ++p) am[p] = 0.0f;
+  with_out_amax(out_kind(cs), want_amax, [&](auto tag, auto atag) {
+    constexpr int OUT = decltype(tag)::value;
+    constexpr bool AMAX = decltype(atag)::value;
+    int s0 = 0;  // the step's rows are in slots s0 .. s0 + nr - 1 (spc is a multiple of RB)
+    uint32_t use = 0;
+    for (int64_t j0 = 0, it = 0; j0 < nloc; j0 += RB, ++it) {
+      const int nr = nloc - j0 < RB ? int(nloc - j0) : RB;
+      bool ok = true;
+#pragma unroll
+      for (int r = 0; r < RB; ++r)
+        if (r < nr && ok) ok = ring_acquire(full, s0 + r, use, abort_flag, status);
+      uint4 cur[RB][NV];
+      float x0[RB];
+#pragma unroll
+      for (int r = 0; r < RB; ++r) {
+        x0[r] = 0.0f;
+#pragma unroll
+        for (int i = 0; i < NV; ++i) cur[r][i] = make_uint4(0u, 0u, 0u, 0u);
+        if (ok && r < nr) {
+          const uint4* src = reinterpret_cast<const uint4*>(ring + size_t(s0 + r) * row_bytes);
+#pragma unroll
+          for (int i = 0; i < NV; ++i) cur[r][i] = src[tid + i * GT];
+          if (LN) {  // the row's first element, subtracted before the sums (shifted variance)
+            f32x2 first[P];
+            PR::cvt(src[0], first);
+            x0[r] = f2lo(first[0]);
+          }
+        }
+      }
+      // the rows are in registers: their slots may be refilled
+      __syncwarp();
+      if (lane == 0 && ok) {
+#pragma unroll
+        for (int r = 0; r < RB; ++r)
+          if (r < nr) mbar_arrive(smem_u32(&empty[s0 + r]));
+      }
+      float t1[RB], t2[RB];
+#pragma unroll
+      for (int r = 0; r < RB; ++r) {
+        const f32x2 x02 = f2s(x0[r]);
+        f32x2 s1[P], s2[P];
+#pragma unroll
+        for (int p = 0; p < P; ++p) { s1[p] = f2s(0.0f); s2[p] = f2s(0.0f); }
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+          f32x2 xp[P];
+          PR::cvt(cur[r][i], xp);
+#pragma unroll
+          for (int p = 0; p < P; ++p) {
+            if (LN) {
+              const f32x2 d = sub2(xp[p], x02);
+              s1[p] = add2(s1[p], d);
+              s2[p] = fma2(d, d, s2[p]);
+            } else {
+              s2[p] = fma2(xp[p], xp[p], s2[p]);
+            }
+          }
+        }
+#pragma unroll
+        for (int p = 1; p < P; ++p) { s1[0] = add2(s1[0], s1[p]); s2[0] = add2(s2[0], s2[p]); }
+        t1[r] = LN ? f2lo(s1[0]) + f2hi(s1[0]) : 0.0f;
+        t2[r] = f2lo(s2[0]) + f2hi(s2[0]);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+        for (int r = 0; r < RB; ++r) {
+          if (LN) t1[r] += __shfl_xor_sync(0xffffffffu, t1[r], o);
+          t2[r] += __shfl_xor_sync(0xffffffffu, t2[r], o);
+        }
+      }
+      const int par = int(it & 1);
+      if (lane == 0) {
+#pragma unroll
+        for (int r = 0; r < RB; ++r) red[par][r][warp] = make_float2(t1[r], t2[r]);
+      }
+      if (group_sync_or(!ok, 1, GT)) break;
+      // every warp has released the step's slots: one warp per slot, in turn, refills it with
+      // the row spc ahead (its wait on the slot's empty barrier acquires the other warps' reads)
+#pragma unroll
+      for (int r = 0; r < RB; ++r) {
+        const int sl = s0 + r;
+        if (warp == int((j0 + r) % G) && lane == 0 && r < nr && j0 + r + spc < nloc &&
+            (mbar_try_wait(smem_u32(&empty[sl]), use & 1u) ||
+             wait_bounded(smem_u32(&empty[sl]), use & 1u, abort_flag, status, kWaitLimitNs, true))) {
+          fence_proxy_async_smem();
+          issue(j0 + r + spc, sl);
+          last_use[sl] = int(use) + 1;
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < RB; ++r) {
+        if (r >= nr) break;
+        // the warps' sums in warp order (the same bits in every thread)
+        float r1 = 0.0f, r2 = 0.0f;
+#pragma unroll
+        for (int w = 0; w < G; ++w) {
+          const float2 v = red[par][r][w];
+          r1 += v.x;
+          r2 += v.y;
+        }
+        const int64_t row = int64_t(blockIdx.x) + (j0 + r) * gridDim.x;
+        const float m1 = LN ? r1 * inv_h : 0.0f;
+        const float m2 = r2 * inv_h;
+        const float mean = LN ? x0[r] + m1 : 0.0f;
+        const float var = LN ? fmaxf(m2 - m1 * m1, 0.0f) : m2;
+        const float rs = rsqrtf(var + a.eps);
+        if (tid == 0) {
+          if (a.mu) a.mu[row] = mean;
+          if (a.rsigma) a.rsigma[row] = rs;
+        }
+        if (OUT != OUT_NONE || AMAX) {
+          const f32x2 mean2 = f2s(mean), rs2 = f2s(rs);
+#pragma unroll
+          for (int i = 0; i < NV; ++i) {
+            f32x2 xp[P];
+            PR::get(cur[r][i], xp);
+            float y[E];
+#pragma unroll
+            for (int p = 0; p < P; ++p) {
+              const f32x2 yy = LN ? fma2(sub2(xp[p], mean2), mul2(gp[i][p], rs2), bp[i][p])
+                                  : mul2(mul2(xp[p], rs2), gp[i][p]);
+              if (AMAX) am[p] = absmax2(am[p], yy);
+              y[2 * p] = f2lo(yy);
+              y[2 * p + 1] = f2hi(yy);
+            }
+            store_out<OUT, E>(a.out, row * a.H + int64_t(tid + i * GT) * E, y, cs);
+          }
+        }
+      }
+      s0 += RB;
+      if (s0 == spc) {
+        s0 = 0;
+        ++use;
+      }
+    }
+  });
+  // After a failed wait, copies issued but never consumed may still be in flight: wait for them
+  // (briefly) before the CTA exits.  Without a failure every issued row was consumed.
+  __syncthreads();
+  if (tid == 0 && *abort_flag) {
+    for (int k = 0; k < spc; ++k)
+      if (last_use[k] >= 0)
+        wait_bounded(smem_u32(&full[k]), uint32_t(last_use[k]) & 1u, nullptr, status,
+                     kDrainLimitNs, false);
+  }
+  float amax = am[0];
+#pragma unroll
+  for (int p = 1; p < P; ++p) amax = fmaxf(amax, am[p]);
+  amax = warp_max(amax);
+  if (lane == 0 && a.cast.amax_out) atomic_max_nonneg(a.cast.amax_out, amax);
+}
+
 // Ring slots per warp for the staged forward: as many as fit (at most kFwdRingMaxSlots), or 0
 // when fewer than two do.
 int fwd_ring_slots(size_t row_bytes, size_t table_bytes) {
@@ -758,6 +979,22 @@ te_status launch_fwd_ring(const NormFwdArgs& a, int slots, cudaStream_t s) {
   const unsigned grid = unsigned(ctas < sms ? ctas : sms);
   norm_fwd_ring_kernel<T, LN, NVW><<<grid, kFwdRingWarps * 32, smem, s>>>(a, device_status_ptr(),
                                                                           slots);
+  return cudaGetLastError() == cudaSuccess ? TE_OK : TE_ERR_CUDA;
+}
+
+template <typename T, bool LN, int NV, int G>
+te_status launch_fwd_cta(const NormFwdArgs& a, cudaStream_t s) {
+  static PerDevice<bool> attr_done;
+  constexpr size_t row_bytes = size_t(G) * 32 * NV * 16;
+  // a step holds kFwdCtaRows slots; a second step's worth lets the refills run ahead
+  const int spc = ring_slots(row_bytes, kFwdCtaMaxSlots, 2 * kFwdCtaRows, kFwdCtaRows);
+  if (spc == 0) return TE_ERR_UNSUPPORTED;
+  const te_status st = allow_ring_smem(norm_fwd_cta_kernel<T, LN, NV, G>, attr_done);
+  if (st != TE_OK) return st;
+  const size_t smem = ring_header_bytes(spc) + size_t(spc) * row_bytes;
+  const int64_t sms = num_sms();
+  const unsigned grid = unsigned(a.M < sms ? a.M : sms);
+  norm_fwd_cta_kernel<T, LN, NV, G><<<grid, G * 32, smem, s>>>(a, device_status_ptr(), spc);
   return cudaGetLastError() == cudaSuccess ? TE_OK : TE_ERR_CUDA;
 }
 
@@ -812,6 +1049,18 @@ te_status launch_fwd_t(const NormFwdArgs& a, cudaStream_t s) {
     if (nvec == 8 * 32) return launch_fwd_nvw<T, 8>(a, s);
     if (nvec == 16 * 32) return launch_fwd_nvw<T, 16>(a, s);
   }
+  // bf16 rows of 1024 vectors (H = 8192): shared by the 8 warps of one CTA per SM, staged in a
+  // ring (measured against the register kernel below at 16384 / 8192 rows: bf16 output +15% /
+  // +28%, E4M3 output +8% / +19%; fp32 rows of 4096 measured slower that way and stay there).
+  // TE_NORM_FWD_LONG=rows in the environment forces the register kernel (a switch between two
+  // complete kernels, for measurements).
+  static const bool long_rows = [] {
+    const char* e = getenv("TE_NORM_FWD_LONG");
+    return !(e && e[0] == 'r');
+  }();
+  if (sizeof(T) == 2 && long_rows && nvec == int64_t(kFwdCtaWarps) * 32 * kFwdCtaVecs)
+    return a.norm_type == TE_LAYERNORM ? launch_fwd_cta<T, true, kFwdCtaVecs, kFwdCtaWarps>(a, s)
+                                       : launch_fwd_cta<T, false, kFwdCtaVecs, kFwdCtaWarps>(a, s);
   const int64_t per_thread = ceil_div(a.H / E, GT);
   if (per_thread <= 1) return launch_fwd_nvl<T, 1>(a, s);
   if (per_thread <= 2) return launch_fwd_nvl<T, 2>(a, s);

@@ -268,7 +268,8 @@ def test_dbias_deterministic():
 @pytest.mark.parametrize("zc", [False, True])
 def test_norm_fwd(norm, M, H, dtype, zc):
     """Widths of 4, 8 or 16 vectors per lane of a warp (1024 / 2048 / 4096 bf16, 512 / 1024 /
-    2048 fp32) take one row per warp; the others a CTA of four warps per row."""
+    2048 fp32) take one row per warp; bf16 rows of 8192 the eight warps of a CTA with a ring of
+    staged rows; the others a CTA of four warps per row."""
     x = rt((M, H), std=2.0, seed=11, dtype=dtype, mean=0.5)
     gamma = rt((H,), std=0.1, seed=12, dtype=dtype, mean=0.0 if zc else 1.0)
     beta = rt((H,), std=0.1, seed=13, dtype=dtype)
@@ -290,11 +291,13 @@ def test_norm_fwd(norm, M, H, dtype, zc):
 
 
 @pytest.mark.parametrize("norm,zc", [("layernorm", False), ("rmsnorm", True)])
-@pytest.mark.parametrize("H,dtype", [(4096, "bf16"), (2048, "f32")])
+@pytest.mark.parametrize("H,dtype", [(4096, "bf16"), (2048, "f32"), (8192, "bf16"), (4096, "f32")])
 @pytest.mark.parametrize("out_kind", ["same", "e4m3"])
 def test_norm_fwd_long_runs(norm, zc, H, dtype, out_kind):
-    """Enough rows (12000, a ragged number of rows per warp) for the staged kernel of rows of 16
-    vectors per lane: y (or its E4M3 codes), mu, rsigma and amax, with guard bands."""
+    """Enough rows (12000, a ragged number of rows per warp or CTA) for the staged kernels: rows
+    of 16 vectors per lane (a ring per warp) and bf16 rows of 8192 (a ring per CTA, which wraps
+    six times; fp32 rows of 4096 take the four-warp row kernel): y (or its E4M3 codes), mu,
+    rsigma and amax, with guard bands."""
     M = 12000
     x = rt((M, H), std=1.5, seed=51, dtype=dtype, mean=0.25)
     gamma = rt((H,), std=0.1, seed=52, dtype=dtype, mean=0.0 if zc else 1.0)
