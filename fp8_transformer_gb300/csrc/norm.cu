@@ -737,10 +737,12 @@ te_status launch_fwd_warp(const NormFwdArgs& a, cudaStream_t s) {
 constexpr int kFwdCtaWarps = 8;
 constexpr int kFwdCtaVecs = 1024 / (kFwdCtaWarps * 32);  // vectors per thread per row
 constexpr int kFwdCtaMaxSlots = 16;
-constexpr int kFwdCtaRows = 2;  // rows per barrier (measured: 1 and 4 slower; 16 warps slower)
+constexpr int kFwdCtaRows = 2;  // rows per barrier (measured: 1 and 4 slower; 16 warps slower;
+                                // for 4096-wide rows two CTAs of 4 warps per SM measured 10-20%
+                                // slower than one row per warp)
 
 template <typename T, bool LN, int NV, int G>
-__global__ void __launch_bounds__(G * 32, 1)
+__global__ void __launch_bounds__(G * 32, G < 8 ? 8 / G : 1)
     norm_fwd_cta_kernel(NormFwdArgs a, int* status, int spc) {
   // the kernel after this one may launch its setup now (it waits for this grid's completion)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -986,14 +988,16 @@ template <typename T, bool LN, int NV, int G>
 te_status launch_fwd_cta(const NormFwdArgs& a, cudaStream_t s) {
   static PerDevice<bool> attr_done;
   constexpr size_t row_bytes = size_t(G) * 32 * NV * 16;
+  constexpr int kCtas = G < 8 ? 8 / G : 1;  // CTAs per SM, sharing its shared memory
+  const size_t cap = kCtas == 1 ? kRingSmemMax : size_t(227 * 1024) / kCtas - 1024;
   // a step holds kFwdCtaRows slots; a second step's worth lets the refills run ahead
-  const int spc = ring_slots(row_bytes, kFwdCtaMaxSlots, 2 * kFwdCtaRows, kFwdCtaRows);
+  const int spc = ring_slots(row_bytes, kFwdCtaMaxSlots, 2 * kFwdCtaRows, kFwdCtaRows, cap);
   if (spc == 0) return TE_ERR_UNSUPPORTED;
-  const te_status st = allow_ring_smem(norm_fwd_cta_kernel<T, LN, NV, G>, attr_done);
+  const te_status st = allow_ring_smem(norm_fwd_cta_kernel<T, LN, NV, G>, attr_done, kCtas > 1);
   if (st != TE_OK) return st;
   const size_t smem = ring_header_bytes(spc) + size_t(spc) * row_bytes;
-  const int64_t sms = num_sms();
-  const unsigned grid = unsigned(a.M < sms ? a.M : sms);
+  const int64_t n = int64_t(num_sms()) * kCtas;
+  const unsigned grid = unsigned(a.M < n ? a.M : n);
   norm_fwd_cta_kernel<T, LN, NV, G><<<grid, G * 32, smem, s>>>(a, device_status_ptr(), spc);
   return cudaGetLastError() == cudaSuccess ? TE_OK : TE_ERR_CUDA;
 }
@@ -1058,9 +1062,11 @@ te_status launch_fwd_t(const NormFwdArgs& a, cudaStream_t s) {
     const char* e = getenv("TE_NORM_FWD_LONG");
     return !(e && e[0] == 'r');
   }();
-  if (sizeof(T) == 2 && long_rows && nvec == int64_t(kFwdCtaWarps) * 32 * kFwdCtaVecs)
-    return a.norm_type == TE_LAYERNORM ? launch_fwd_cta<T, true, kFwdCtaVecs, kFwdCtaWarps>(a, s)
-                                       : launch_fwd_cta<T, false, kFwdCtaVecs, kFwdCtaWarps>(a, s);
+  if constexpr (sizeof(T) == 2) {
+    if (long_rows && nvec == int64_t(kFwdCtaWarps) * 32 * kFwdCtaVecs)
+      return a.norm_type == TE_LAYERNORM ? launch_fwd_cta<T, true, kFwdCtaVecs, kFwdCtaWarps>(a, s)
+                                         : launch_fwd_cta<T, false, kFwdCtaVecs, kFwdCtaWarps>(a, s);
+  }
   const int64_t per_thread = ceil_div(a.H / E, GT);
   if (per_thread <= 1) return launch_fwd_nvl<T, 1>(a, s);
   if (per_thread <= 2) return launch_fwd_nvl<T, 2>(a, s);
