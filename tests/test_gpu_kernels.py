@@ -497,6 +497,40 @@ def test_gemm_split_k(kind, a_trans, b_trans, M, N, K):
         assert ratio <= ACC_REL, f"{what}: {ratio:.3e} > ACC_REL {ACC_REL:.3e}"
 
 
+@pytest.mark.parametrize("kind,M,N,K", [("bf16", 100, 528, 16384), ("tf32", 200, 256, 8192)])
+def test_gemm_split_k_single_cta_tiles(kind, M, N, K):
+    """The split along K with single-CTA tiles (128 x 256: M <= 128, and the tf32 path, which
+    always runs them): against the oracle within the accumulation window, repeatable to the
+    bit, and nothing written outside the output or the workspace."""
+    if kind == "bf16":
+        A = rt((M, K), seed=61)
+        B = rt((N, K), seed=62)
+        ab = te.binding.TE_BF16
+    else:
+        A = rt((M, K), seed=61, dtype="f32")
+        B = rt((N, K), seed=62, dtype="f32")
+        ab = te.binding.TE_F32
+    nws = te.workspace_size(te.binding.TE_OP_GEMM, M, K, N, ab)
+    assert nws > 0, "these shapes leave SM pairs idle: the library should split them"
+    ws = Guarded((nws,), torch.uint8)
+    outs = []
+    for _ in range(2):
+        g = Guarded((M, N), torch.float32)
+        te.te_gemm(A, B, g.t, b_trans=True, workspace=ws.t)
+        g.check("split-K gemm out")
+        outs.append(np64(g.t))
+    ws.check("split-K workspace")
+    assert np.array_equal(outs[0], outs[1])
+    a, b = np64(A), np64(B).T
+    ref = ob.gemm(a, b, None)
+    absdot = np.abs(a) @ np.abs(b)
+    if kind == "bf16":
+        ratio = float((np.abs(outs[0] - ref) / absdot).max())
+        assert ratio <= ACC_REL, f"{ratio:.3e} > ACC_REL {ACC_REL:.3e}"
+    else:  # tf32 operands: held to the bf16 rule of the fp32 workload
+        assert_gemm_close(outs[0], ref, K, rms(a), rms(b), what="split-K tf32", stored="f32")
+
+
 @pytest.mark.parametrize("kind", ["bf16", "e4m3"])
 @pytest.mark.parametrize("a_trans,b_trans", [(False, False), (False, True), (True, False)])
 @pytest.mark.parametrize("K", [512, 4096, 16384])
