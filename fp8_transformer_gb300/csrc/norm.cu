@@ -2,14 +2,15 @@
 //
 // Forward (TransformerEngine JAX "LayerNorm MLP" page, Description step (1); "LayerNorm Dense"
 // page, Description): rows of 4, 8 or 16 16-byte vectors per lane of a warp (H = 1024, 2048 or
-// 4096 in bf16) take one row per warp, whose sums meet by shuffles alone; other widths take a
-// CTA of a few warps per row, persistent over rows with a stride of the grid, eight CTAs per
-// SM, each thread loading the next row's vectors while it normalizes the current one, the
-// warps' row sums meeting in shared memory at one barrier per row.  Statistics are fp32, and
-// the normalized row is written once, directly in the consumer GEMM's operand dtype (fp32,
-// bf16 or E4M3), together with the per-tensor amax.  (Staging rows through shared memory with
-// bulk copies, as the backward does, measured slower here: even with no arithmetic at all that
-// path reached about 77% of the copy bandwidth at the 8192 x 4096 shape.)
+// 4096 in bf16) take one row per warp, whose sums meet by shuffles alone, each warp loading its
+// next row while it works on the current one (long runs of 4096-wide rows stage the rows in
+// per-warp bulk-copy rings instead); bf16 rows of 8192 are shared by the 8 warps of one CTA per
+// SM, staged in a 12-row bulk-copy ring; other widths take a CTA of a few warps per row,
+// persistent over rows with a stride of the grid, eight CTAs per SM, each thread loading the
+// next row's vectors while it normalizes the current one, the warps' row sums meeting in shared
+// memory at one barrier per row.  Statistics are fp32, and the normalized row is written once,
+// directly in the consumer GEMM's operand dtype (fp32, bf16 or E4M3), together with the
+// per-tensor amax.
 //
 // Backward (the norm's share of the backward pass, whose gradients cover every parameter):
 // rows of x and dz stream through a ring of shared-memory slots, filled by bulk copies (the
@@ -17,8 +18,9 @@
 // rows already in shared memory.  Each slot has a "full" mbarrier (completed by the copies'
 // byte count) and an "empty" one (completed by the warps that read it), and every wait on them
 // is bounded; there is no producer warp: the last warp to release a slot issues its refill.
-// The row is split across the warps; the partial row sums of a few rows at a time meet in
-// shared memory at one named barrier.  dgamma and dbeta accumulate per thread in registers, are
+// The row is split across the warps of a CTA (one CTA of 8 warps per SM, or two of 4 for rows
+// up to 8 KB); the partial row sums of a few rows at a time meet in shared memory at one named
+// barrier.  dgamma and dbeta accumulate per thread in registers, are
 // written as one partial row per CTA and summed in a fixed order by a second kernel, so the
 // result does not depend on timing.
 #include <cstdlib>
