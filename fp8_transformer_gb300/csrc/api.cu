@@ -560,9 +560,18 @@ te_status te_layernorm_mlp_fwd(const void* x, const void* gamma, const void* bet
   cudaStream_t s = as_stream(stream);
   void* ln = saved_ln_out ? saved_ln_out : L.ln;
   void* a2 = saved_act ? saved_act : L.a2;  // GEMM2's A operand
+  // The activation's amax (GEMM1's epilogue accumulates into it) is zeroed before the norm rather
+  // than between the norm and GEMM1, where the memset would keep GEMM1 from launching as the
+  // norm's programmatic dependent; unless it shares storage with an amax written before GEMM1.
+  const bool act_zero_first =
+      quant && qset->act.amax && qset->act.amax != qset->x.amax &&
+      (kernel_dtype == TE_E4M3 ||
+       (qset->act.amax != qset->kernel1.amax && qset->act.amax != qset->kernel2.amax));
+  te_status st = act_zero_first ? zero_scalar(qset->act.amax, s) : TE_OK;
+  if (st != TE_OK) return st;
   // (1) normalization, written once in GEMM1's operand dtype
-  te_status st = norm_into(x, dtype, M, H, gamma, beta, norm_type, zero_centered_gamma, epsilon,
-                           quant ? &qset->x : nullptr, ln, quant ? TE_E4M3 : dtype, mu, rsigma, s);
+  st = norm_into(x, dtype, M, H, gamma, beta, norm_type, zero_centered_gamma, epsilon,
+                 quant ? &qset->x : nullptr, ln, quant ? TE_E4M3 : dtype, mu, rsigma, s);
   if (st != TE_OK) return st;
   const void* w1 = kernel1;
   const void* w2 = kernel2;
@@ -603,8 +612,10 @@ te_status te_layernorm_mlp_fwd(const void* x, const void* gamma, const void* bet
   g1.saved_h = saved_h;
   const bool act_current = quant && qset->act.mode == TE_SCALING_CURRENT;
   if (quant) {
-    st = zero_scalar(qset->act.amax, s);
-    if (st != TE_OK) return st;
+    if (!act_zero_first) {
+      st = zero_scalar(qset->act.amax, s);
+      if (st != TE_OK) return st;
+    }
     g1.cast.amax_out = qset->act.amax;
     if (act_current) {
       g1.D = L.a2_hi;
