@@ -168,6 +168,55 @@ def test_mlp_split_k(shape, fp8):
     check_mlp(inp, got, ref, fp8=fp8)
 
 
+def test_mlp_workspace_without_split_room():
+    """A workspace that stops short of the split scratch at its end is accepted: the call
+    splits fewer or no tiles along K and gives the same result within the GEMM windows."""
+    inp = make_inputs("llama_rms_mlp", device=DEV, M=300, H=512, F=16384)
+    M, H, F = inp["M"], inp["H"], inp["F"]
+    b = te.binding
+    full = te.workspace_size(b.TE_OP_LAYERNORM_MLP_FWD, M, H, F, b.TE_BF16, False, b.TE_BF16,
+                             b.TE_SWIGLU)
+    outs = []
+    for nbytes in (full, full - 16):
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
+        out = torch.empty(M, H, dtype=torch.bfloat16, device=DEV)
+        te.te_layernorm_mlp_fwd(inp["x"], inp["gamma"], inp["beta"], inp["w1"], inp["w2"], None,
+                                None, out, norm_type=inp["norm"],
+                                zero_centered_gamma=inp["zero_centered_gamma"],
+                                epsilon=inp["eps"], activation_type=inp["act"], workspace=ws)
+        outs.append(out)
+    ref = oracle_mlp(inp)
+    a2 = ref["a"].value * ref["a"].inv()
+    w2 = ref["w2"].value * ref["w2"].inv()
+    for out in outs:
+        assert_gemm_close(np64(out), ref["out"].value, F, rms(a2), rms(w2), what="out",
+                          stored="bf16")
+
+
+def test_mlp_fp8_act_amax_sharing_storage_with_x():
+    """The activation's amax is zeroed before the norm only when it has storage of its own; a
+    quantizer set whose x and act amax share one scalar still ends with the activation's amax
+    (the value an unshared act quantizer reports), the norm's amax having been overwritten."""
+    inp = make_inputs("llama_rms_mlp", device=DEV, M=300, H=512, F=784)
+    plain = run_mlp(inp, fp8=True)
+    shared = torch.zeros(1, dtype=torch.float32, device=DEV)
+    qx = te.Quantizer(MLP_SCALES["x"])
+    qa = te.Quantizer(MLP_SCALES["act"])
+    qs = te.QuantizerSet(
+        x=te.Quantizer.from_tensors(qx.scale, qx.scale_inv, shared),
+        kernel1=te.Quantizer(MLP_SCALES["w1"]),
+        act=te.Quantizer.from_tensors(qa.scale, qa.scale_inv, shared),
+        kernel2=te.Quantizer(MLP_SCALES["w2"]))
+    out = torch.empty(inp["M"], inp["H"], dtype=torch.bfloat16, device=DEV)
+    te.te_layernorm_mlp_fwd(inp["x"], inp["gamma"], inp["beta"], inp["w1"], inp["w2"], None, None,
+                            out, norm_type=inp["norm"],
+                            zero_centered_gamma=inp["zero_centered_gamma"], epsilon=inp["eps"],
+                            activation_type=inp["act"], quantizer_set=qs)
+    torch.cuda.synchronize()
+    assert torch.equal(out, plain["out"])
+    assert shared.item() == plain["qs"].act.amax.item()
+
+
 @pytest.mark.parametrize("name,shape", SMALL[1:])
 def test_mlp_small_fp8(name, shape):
     inp = make_inputs(name, device=DEV, **shape)
