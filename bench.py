@@ -326,7 +326,7 @@ def bandwidth_kernels(args, dev, peaks):
     run("norm_fwd_e4m3", lambda: te.te_norm_fwd(x, g, b, "rmsnorm", True, 1e-6, y8, q=q, mu=mu,
                                                 rsigma=rs), M * H * 3 + M * 8)
     del x, y, y8, mu, rs
-    # the GPT workload's LayerNorm (16384 rows: the staged ring kernel)
+    # the GPT workload's LayerNorm (16384 rows, one row per warp)
     xg = random_tensor((Mb, H), device=dev, seed=7)
     gg = random_tensor((H,), std=0.1, mean=1.0, device=dev, seed=8)
     bg = random_tensor((H,), std=0.1, device=dev, seed=9)

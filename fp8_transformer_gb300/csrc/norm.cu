@@ -3,14 +3,13 @@
 // Forward (TransformerEngine JAX "LayerNorm MLP" page, Description step (1); "LayerNorm Dense"
 // page, Description): rows of 4, 8 or 16 16-byte vectors per lane of a warp (H = 1024, 2048 or
 // 4096 in bf16) take one row per warp, whose sums meet by shuffles alone, each warp loading its
-// next row while it works on the current one (long runs of 4096-wide rows stage the rows in
-// per-warp bulk-copy rings instead); bf16 rows of 8192 are shared by the 8 warps of one CTA per
-// SM, staged in a 12-row bulk-copy ring; other widths take a CTA of a few warps per row,
-// persistent over rows with a stride of the grid, eight CTAs per SM, each thread loading the
-// next row's vectors while it normalizes the current one, the warps' row sums meeting in shared
-// memory at one barrier per row.  Statistics are fp32, and the normalized row is written once,
-// directly in the consumer GEMM's operand dtype (fp32, bf16 or E4M3), together with the
-// per-tensor amax.
+// next row while it works on the current one; bf16 rows of 8192 are shared by the 8 warps of
+// one CTA per SM, staged in a 12-row bulk-copy ring; other widths take a CTA of a few warps per
+// row, persistent over rows with a stride of the grid, eight CTAs per SM, each thread loading
+// the next row's vectors while it normalizes the current one, the warps' row sums meeting in
+// shared memory at one barrier per row.  Every form requests its first row before it builds
+// its table of gains.  Statistics are fp32, and the normalized row is written once, directly in
+// the consumer GEMM's operand dtype (fp32, bf16 or E4M3), together with the per-tensor amax.
 //
 // Backward (the norm's share of the backward pass, whose gradients cover every parameter):
 // rows of x and dz stream through a ring of shared-memory slots, filled by bulk copies (the
@@ -109,11 +108,49 @@ __device__ __forceinline__ bool ring_acquire(uint64_t* full, int s, uint32_t use
 
 // ----------------------------------------------------------------------- forward ---------
 
+// The forward's gain (gamma, plus one when zero-centered) and beta tables in shared memory, as
+// fp32: elements 4q .. 4q + 3 of the row's 16-byte vector v sit in float4 q * nvec + v, so a
+// lane that owns vector v reads its gains as Q float4s, each warp's reads contiguous.  Filled
+// with 16-byte loads of gamma and beta (both 16-byte aligned, the row a whole number of
+// vectors) by the CTA's NT threads; with the row's vector count NVEC known at compile time (a
+// multiple of NT), every thread's loads are issued back to back.
+template <typename T, bool LN, int NT, int NVEC = 0>
+__device__ __forceinline__ void fill_gain_table(float4* gain4, float4* beta4, int nvec,
+                                                const NormFwdArgs& a, int tid) {
+  static_assert(NVEC % NT == 0, "a compile-time row length is a whole number of passes");
+  using PR = Pairs<T>;
+  constexpr int P = PR::P;
+  constexpr int Q = Vec16<T>::N / 4;
+  const float shift = a.zero_centered_gamma ? 1.0f : 0.0f;
+  const uint4* g = static_cast<const uint4*>(a.gamma);
+  const uint4* b = static_cast<const uint4*>(a.beta);
+  auto one = [&](int v) {
+    f32x2 gp[P], bp[P];
+    PR::cvt(__ldg(g + v), gp);
+    if (LN && b) PR::cvt(__ldg(b + v), bp);
+#pragma unroll
+    for (int q = 0; q < Q; ++q) {
+      gain4[q * nvec + v] = make_float4(f2lo(gp[2 * q]) + shift, f2hi(gp[2 * q]) + shift,
+                                        f2lo(gp[2 * q + 1]) + shift, f2hi(gp[2 * q + 1]) + shift);
+      if (LN)
+        beta4[q * nvec + v] = b ? make_float4(f2lo(bp[2 * q]), f2hi(bp[2 * q]),
+                                              f2lo(bp[2 * q + 1]), f2hi(bp[2 * q + 1]))
+                                : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    }
+  };
+  if constexpr (NVEC > 0) {
+#pragma unroll
+    for (int i = 0; i < NVEC / NT; ++i) one(tid + i * NT);
+  } else {
+    for (int v = tid; v < nvec; v += NT) one(v);
+  }
+}
+
 // Forward without the ring: one row per CTA of kFwdGroupWarps warps at a time, persistent over
 // rows with a stride of the grid.  Each thread loads its NVL 16-byte vectors of the row straight
 // into registers, and loads the next row's while it normalizes the current one; many CTAs per
 // SM keep enough rows in flight.  The gain and beta sit in shared memory as fp32 float4 blocks
-// (the layout above); the warps' row sums meet in shared memory at one barrier per row.
+// (fill_gain_table's layout); the warps' row sums meet in shared memory at one barrier per row.
 template <typename T, bool LN, int NVL, bool FULL>
 __global__ void __launch_bounds__(kFwdGroupWarps * 32, NVL >= 8 ? kFwdRowsCtasPerSm / 2 : kFwdRowsCtasPerSm)
     norm_fwd_rows_kernel(NormFwdArgs a) {
@@ -131,19 +168,6 @@ __global__ void __launch_bounds__(kFwdGroupWarps * 32, NVL >= 8 ? kFwdRowsCtasPe
   float4* gain4 = prm;
   float4* beta4 = prm + Q * nvec;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  {
-    const float shift = a.zero_centered_gamma ? 1.0f : 0.0f;
-    const T* g = static_cast<const T*>(a.gamma);
-    const T* b = static_cast<const T*>(a.beta);
-    float* gf = reinterpret_cast<float*>(gain4);
-    float* bf = reinterpret_cast<float*>(beta4);
-    for (int64_t j = tid; j < a.H; j += GT) {
-      const int64_t v = j / E, e = j % E;
-      const int64_t slot = ((e / 4) * nvec + v) * 4 + (e % 4);
-      gf[slot] = float(g[j]) + shift;
-      if (LN) bf[slot] = b ? float(b[j]) : 0.0f;
-    }
-  }
   auto mine = [&](int v) { return FULL || v < nvec; };
   const T* x = static_cast<const T*>(a.x);
   const int64_t stride = gridDim.x;
@@ -157,7 +181,10 @@ __global__ void __launch_bounds__(kFwdGroupWarps * 32, NVL >= 8 ? kFwdRowsCtasPe
   uint4 bufa[NVL], bufb[NVL];
   float x0a = 0.0f, x0b = 0.0f;
   int64_t row = blockIdx.x;
+  // the first row is requested before the gain table is built, so that the table's loads
+  // overlap the row's
   if (row < a.M) load_row(row, bufa, x0a);
+  fill_gain_table<T, LN, GT>(gain4, beta4, nvec, a, tid);
   __syncthreads();  // gain / beta ready
   const CastState cs = cast_begin(a.cast);
   const float inv_h = 1.0f / float(a.H);
@@ -285,9 +312,9 @@ __global__ void __launch_bounds__(kFwdGroupWarps * 32, NVL >= 8 ? kFwdRowsCtasPe
 
 // Forward with one row per warp, for rows of exactly NVW x 32 vectors: the row's sums meet by
 // shuffles within the warp, with no barrier between warps; the CTA's kFwdWarpRowWarps warps
-// share the gain / beta table in shared memory (the layout above).  Each lane holds its NVW
-// vectors of one row (PIPE: of two rows, the next one loading while the current one is worked
-// on); the many warps per SM keep rows in flight.
+// share the gain / beta table in shared memory (fill_gain_table's layout).  Each lane holds its
+// NVW vectors of one row (PIPE: of two rows, the next one loading while the current one is
+// worked on); the many warps per SM keep rows in flight.
 constexpr int kFwdWarpRowWarps = 4;
 __host__ __device__ constexpr int fwd_warp_ctas(int elems_per_lane, bool pipe) {
   return pipe ? (elems_per_lane >= 128 ? 2 : 3) : (elems_per_lane >= 128 ? 3 : 4);
@@ -306,21 +333,19 @@ __global__ void __launch_bounds__(kFwdWarpRowWarps * 32, fwd_warp_ctas(NVW * Vec
   float4* gain4 = prm;
   float4* beta4 = prm + Q * nvec;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  {
-    const float shift = a.zero_centered_gamma ? 1.0f : 0.0f;
-    const T* g = static_cast<const T*>(a.gamma);
-    const T* b = static_cast<const T*>(a.beta);
-    float* gf = reinterpret_cast<float*>(gain4);
-    float* bf = reinterpret_cast<float*>(beta4);
-    for (int64_t j = tid; j < a.H; j += blockDim.x) {
-      const int64_t v = j / E, e = j % E;
-      const int64_t slot = ((e / 4) * nvec + v) * 4 + (e % 4);
-      gf[slot] = float(g[j]) + shift;
-      if (LN) bf[slot] = b ? float(b[j]) : 0.0f;
-    }
-  }
-  __syncthreads();  // gain / beta ready
   const T* x = static_cast<const T*>(a.x);
+  const int64_t step = int64_t(gridDim.x) * kFwdWarpRowWarps;
+  const int64_t r_first = int64_t(blockIdx.x) * kFwdWarpRowWarps + warp;
+  // PIPE: the warp's first row is requested before the gain table is built, so that the
+  // table's loads overlap the row's
+  uint4 cur[NVW];
+  if (PIPE && r_first < a.M) {
+    const uint4* xr = reinterpret_cast<const uint4*>(x + r_first * a.H) + lane;
+#pragma unroll
+    for (int i = 0; i < NVW; ++i) cur[i] = __ldg(xr + 32 * i);
+  }
+  fill_gain_table<T, LN, kFwdWarpRowWarps * 32, nvec>(gain4, beta4, nvec, a, tid);
+  __syncthreads();  // gain / beta ready
   const CastState cs = cast_begin(a.cast);
   const float inv_h = 1.0f / float(a.H);
   const bool want_amax = a.cast.amax_out != nullptr;
@@ -330,14 +355,6 @@ __global__ void __launch_bounds__(kFwdWarpRowWarps * 32, fwd_warp_ctas(NVW * Vec
   with_out_amax(out_kind(cs), want_amax, [&](auto tag, auto atag) {
     constexpr int OUT = decltype(tag)::value;
     constexpr bool AMAX = decltype(atag)::value;
-    const int64_t step = int64_t(gridDim.x) * kFwdWarpRowWarps;
-    const int64_t r_first = int64_t(blockIdx.x) * kFwdWarpRowWarps + warp;
-    uint4 cur[NVW];
-    if (PIPE && r_first < a.M) {
-      const uint4* xr = reinterpret_cast<const uint4*>(x + r_first * a.H) + lane;
-#pragma unroll
-      for (int i = 0; i < NVW; ++i) cur[i] = __ldg(xr + 32 * i);
-    }
     for (int64_t r = r_first; r < a.M; r += step) {
       // PIPE: the warp's next row is requested before this row's arithmetic, so that a row's
       // loads are always in flight
@@ -436,209 +453,6 @@ __global__ void __launch_bounds__(kFwdWarpRowWarps * 32, fwd_warp_ctas(NVW * Vec
       }
     }
   });
-  float amax = am[0];
-#pragma unroll
-  for (int p = 1; p < P; ++p) amax = fmaxf(amax, am[p]);
-  amax = warp_max(amax);
-  if (lane == 0 && a.cast.amax_out) atomic_max_nonneg(a.cast.amax_out, amax);
-}
-
-// Forward for rows of exactly NVW x 32 vectors with the rows staged in shared memory: one CTA
-// of kFwdRingWarps warps per SM, each warp working through its own rows (rows r0, r0 + step,
-// ... with step = all warps of the grid) one at a time, its sums meeting by shuffles, while the
-// bulk copies of its next `slots - 1` rows are in flight into its own shared-memory slots.  The
-// loads in flight no longer live in registers, so every SM keeps kFwdRingWarps x slots rows
-// (about 190 KB) requested from memory at all times; each row is read from its slot twice (for
-// the sums, then for the output).  Each slot has one "full" mbarrier completed by the copy's
-// byte count; the warp that consumes a slot refills it, so no "empty" barrier is needed, and
-// every wait is bounded.
-constexpr int kFwdRingWarps = 12;
-constexpr int kFwdRingMaxSlots = 4;
-constexpr size_t kFwdRingSmemMax = 232448;  // the largest dynamic shared memory of one CTA
-
-__host__ __device__ constexpr size_t fwd_ring_header(int slots) {
-  return (size_t(kFwdRingWarps) * slots * 8 + 16 + 127) / 128 * 128;
-}
-
-template <typename T, bool LN, int NVW>
-__global__ void __launch_bounds__(kFwdRingWarps * 32, 1)
-    norm_fwd_ring_kernel(NormFwdArgs a, int* status, int slots) {
-  // the kernel after this one may launch its setup now (it waits for this grid's completion)
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  using PR = Pairs<T>;
-  constexpr int E = Vec16<T>::N;
-  constexpr int P = PR::P;
-  constexpr int Q = E / 4;
-  constexpr int nvec = NVW * 32;
-  constexpr uint32_t row_bytes = uint32_t(nvec) * 16u;
-  extern __shared__ __align__(128) uint8_t smem[];
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(full + kFwdRingWarps * slots);
-  float4* gain4 = reinterpret_cast<float4*>(smem + fwd_ring_header(slots));
-  float4* beta4 = gain4 + Q * nvec;
-  uint8_t* ring = reinterpret_cast<uint8_t*>(gain4 + (LN ? 2 : 1) * Q * nvec);
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const char* xb = static_cast<const char*>(a.x);
-  const int64_t step = int64_t(gridDim.x) * kFwdRingWarps;
-  // warp w's row k (row w0 + k step, w0 = blockIdx.x * kFwdRingWarps + w) goes to its slot
-  // k % slots, use k / slots of that slot
-  auto issue = [&](int w, int64_t k) {
-    const int64_t row = int64_t(blockIdx.x) * kFwdRingWarps + w + k * step;
-    const int sl = int(k % slots);
-    uint64_t* bar = full + w * slots + sl;
-    mbar_expect_tx(smem_u32(bar), row_bytes);
-    bulk_load(smem_u32(ring + (size_t(w) * slots + sl) * row_bytes), xb + row * row_bytes,
-              row_bytes, smem_u32(bar));
-  };
-  if (tid == 0) {
-    for (int i = 0; i < kFwdRingWarps * slots; ++i) mbar_init(smem_u32(&full[i]), 1);
-    *abort_flag = 0;
-    mbar_init_fence();
-    // every warp's first rows are requested before the gain table is built, so that the table's
-    // loads overlap the rows' instead of preceding them
-    for (int w = 0; w < kFwdRingWarps; ++w)
-      for (int k = 0; k < slots && int64_t(blockIdx.x) * kFwdRingWarps + w + k * step < a.M; ++k)
-        issue(w, k);
-  }
-  {
-    const float shift = a.zero_centered_gamma ? 1.0f : 0.0f;
-    const T* g = static_cast<const T*>(a.gamma);
-    const T* b = static_cast<const T*>(a.beta);
-    float* gf = reinterpret_cast<float*>(gain4);
-    float* bf = reinterpret_cast<float*>(beta4);
-    for (int64_t j = tid; j < a.H; j += blockDim.x) {
-      const int64_t v = j / E, e = j % E;
-      const int64_t slot = ((e / 4) * nvec + v) * 4 + (e % 4);
-      gf[slot] = float(g[j]) + shift;
-      if (LN) bf[slot] = b ? float(b[j]) : 0.0f;
-    }
-  }
-  __syncthreads();  // barriers, gain / beta ready
-  uint8_t* mine = ring + size_t(warp) * slots * row_bytes;
-  uint64_t* mfull = full + warp * slots;
-  const int64_t r0 = int64_t(blockIdx.x) * kFwdRingWarps + warp;
-  const CastState cs = cast_begin(a.cast);
-  const float inv_h = 1.0f / float(a.H);
-  const bool want_amax = a.cast.amax_out != nullptr;
-  float am[P];
-#pragma unroll
-  for (int p = 0; p < P; ++p) am[p] = 0.0f;
-  int64_t k = 0;
-  bool failed = false;
-  with_out_amax(out_kind(cs), want_amax, [&](auto tag, auto atag) {
-    constexpr int OUT = decltype(tag)::value;
-    constexpr bool AMAX = decltype(atag)::value;
-    for (int64_t r = r0; r < a.M; r += step, ++k) {
-      const int sl = int(k % slots);
-      const uint32_t par = uint32_t(k / slots) & 1u;
-      const uint32_t bar = smem_u32(&mfull[sl]);
-      int ok = 1;
-      if (lane == 0 && !mbar_try_wait(bar, par))
-        ok = wait_bounded(bar, par, abort_flag, status, kWaitLimitNs, true) ? 1 : 0;
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) {
-        failed = true;
-        break;
-      }
-      // the phase has completed: every lane observes it before reading the slot
-      while (!mbar_try_wait(bar, par)) {
-      }
-      const uint4* row = reinterpret_cast<const uint4*>(mine + size_t(sl) * row_bytes) + lane;
-      uint4 cur[NVW];
-#pragma unroll
-      for (int i = 0; i < NVW; ++i) cur[i] = row[32 * i];
-      // the row's first element, subtracted before the sums (shifted variance)
-      float x0 = 0.0f;
-      if (LN) {
-        f32x2 first[P];
-        PR::cvt(reinterpret_cast<const uint4*>(mine + size_t(sl) * row_bytes)[0], first);
-        x0 = f2lo(first[0]);
-      }
-      // the row is in registers: every lane has read the slot, which is refilled with the row
-      // `slots` ahead before this row's arithmetic
-      __syncwarp();
-      if (lane == 0 && r + slots * step < a.M) {
-        fence_proxy_async_smem();
-        issue(warp, k + slots);
-      }
-      const f32x2 x02 = f2s(x0);
-      f32x2 s1[P], s2[P];
-#pragma unroll
-      for (int p = 0; p < P; ++p) { s1[p] = f2s(0.0f); s2[p] = f2s(0.0f); }
-#pragma unroll
-      for (int i = 0; i < NVW; ++i) {
-        f32x2 xp[P];
-        PR::cvt(cur[i], xp);
-#pragma unroll
-        for (int p = 0; p < P; ++p) {
-          if (LN) {
-            const f32x2 d = sub2(xp[p], x02);
-            s1[p] = add2(s1[p], d);
-            s2[p] = fma2(d, d, s2[p]);
-          } else {
-            s2[p] = fma2(xp[p], xp[p], s2[p]);
-          }
-        }
-      }
-#pragma unroll
-      for (int p = 1; p < P; ++p) { s1[0] = add2(s1[0], s1[p]); s2[0] = add2(s2[0], s2[p]); }
-      float t1 = LN ? f2lo(s1[0]) + f2hi(s1[0]) : 0.0f;
-      float t2 = f2lo(s2[0]) + f2hi(s2[0]);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        if (LN) t1 += __shfl_xor_sync(0xffffffffu, t1, o);
-        t2 += __shfl_xor_sync(0xffffffffu, t2, o);
-      }
-      const float m1 = LN ? t1 * inv_h : 0.0f;
-      const float m2 = t2 * inv_h;
-      const float mean = LN ? x0 + m1 : 0.0f;
-      const float var = LN ? fmaxf(m2 - m1 * m1, 0.0f) : m2;
-      const float rs = rsqrtf(var + a.eps);
-      if (lane == 0) {
-        if (a.mu) a.mu[r] = mean;
-        if (a.rsigma) a.rsigma[r] = rs;
-      }
-      if (OUT != OUT_NONE || AMAX) {
-        const f32x2 mean2 = f2s(mean), rs2 = f2s(rs);
-        const int64_t base = r * a.H + int64_t(lane) * E;
-#pragma unroll
-        for (int i = 0; i < NVW; ++i) {
-          const int v = lane + 32 * i;
-          f32x2 xp[P], gp[P], bp[P];
-          PR::get(cur[i], xp);  // converted again here rather than kept from the sums
-#pragma unroll
-          for (int q = 0; q < Q; ++q) {
-            const float4 g4 = gain4[q * nvec + v];
-            gp[2 * q] = f2(g4.x, g4.y);
-            gp[2 * q + 1] = f2(g4.z, g4.w);
-            if (LN) {
-              const float4 b4 = beta4[q * nvec + v];
-              bp[2 * q] = f2(b4.x, b4.y);
-              bp[2 * q + 1] = f2(b4.z, b4.w);
-            }
-          }
-          float y[E];
-#pragma unroll
-          for (int p = 0; p < P; ++p) {
-            const f32x2 yy = LN ? fma2(sub2(xp[p], mean2), mul2(gp[p], rs2), bp[p])
-                                : mul2(mul2(xp[p], rs2), gp[p]);
-            if (AMAX) am[p] = absmax2(am[p], yy);
-            y[2 * p] = f2lo(yy);
-            y[2 * p + 1] = f2hi(yy);
-          }
-          store_out<OUT, E>(a.out, base + int64_t(32) * E * i, y, cs);
-          // one vector's gain / beta loads at a time: hoisting all of them spills
-          asm volatile("" ::: "memory");
-        }
-      }
-    }
-  });
-  if (failed && lane == 0) {
-    // after a failed wait, the copies this warp still has in flight land before the CTA exits
-    for (int64_t j = k; j < k + slots && r0 + j * step < a.M; ++j)
-      wait_bounded(smem_u32(&mfull[int(j % slots)]), uint32_t(j / slots) & 1u, abort_flag, status,
-                   kDrainLimitNs, false);
-  }
   float amax = am[0];
 #pragma unroll
   for (int p = 1; p < P; ++p) amax = fmaxf(amax, am[p]);
@@ -954,38 +768,6 @@ __global__ void __launch_bounds__(G * 32, G < 8 ? 8 / G : 1)
   if (lane == 0 && a.cast.amax_out) atomic_max_nonneg(a.cast.amax_out, amax);
 }
 
-// Ring slots per warp for the staged forward: as many as fit (at most kFwdRingMaxSlots), or 0
-// when fewer than two do.
-int fwd_ring_slots(size_t row_bytes, size_t table_bytes) {
-  for (int slots = kFwdRingMaxSlots; slots >= 2; --slots)
-    if (fwd_ring_header(slots) + table_bytes + size_t(kFwdRingWarps) * slots * row_bytes <=
-        kFwdRingSmemMax)
-      return slots;
-  return 0;
-}
-
-template <typename T, bool LN, int NVW>
-te_status launch_fwd_ring(const NormFwdArgs& a, int slots, cudaStream_t s) {
-  static PerDevice<bool> attr_done;
-  bool ok = false;
-  if (!attr_done.get(&ok, [](bool* v) {
-        *v = cudaFuncSetAttribute(norm_fwd_ring_kernel<T, LN, NVW>,
-                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  int(kFwdRingSmemMax)) == cudaSuccess;
-        return *v;
-      }))
-    return TE_ERR_CUDA;
-  constexpr size_t row_bytes = size_t(NVW) * 32 * 16;
-  const size_t smem = fwd_ring_header(slots) + size_t(a.H) * (LN ? 2 : 1) * sizeof(float) +
-                      size_t(kFwdRingWarps) * slots * row_bytes;
-  const int64_t ctas = ceil_div(a.M, kFwdRingWarps);
-  const int64_t sms = num_sms();
-  const unsigned grid = unsigned(ctas < sms ? ctas : sms);
-  norm_fwd_ring_kernel<T, LN, NVW><<<grid, kFwdRingWarps * 32, smem, s>>>(a, device_status_ptr(),
-                                                                          slots);
-  return cudaGetLastError() == cudaSuccess ? TE_OK : TE_ERR_CUDA;
-}
-
 template <typename T, bool LN, int NV, int G>
 te_status launch_fwd_cta(const NormFwdArgs& a, cudaStream_t s) {
   static PerDevice<bool> attr_done;
@@ -1004,32 +786,19 @@ te_status launch_fwd_cta(const NormFwdArgs& a, cudaStream_t s) {
   return cudaGetLastError() == cudaSuccess ? TE_OK : TE_ERR_CUDA;
 }
 
-// One row per warp.  Rows of 16 vectors per lane are staged in shared memory when every warp
-// of the grid gets at least kFwdRingMinRows of them: the staged kernel streams faster but starts
-// slower (measured on 4096-wide bf16 rows: 85% against 82% of the copy bandwidth at 16384 rows,
-// 75% against 80% at 8192 rows; slower at every shorter width).  Other rows are loaded straight
-// into registers, each warp requesting its next row before the current row's arithmetic (with
-// two rows in registers, fewer warps fit an SM; measured against one row at a time: equal with
-// bf16 output and 1% faster with E4M3 at 8192 x 4096, 3% faster at 8192 x 2048).
-// TE_NORM_FWD_KERNEL=warp (one row at a time), =pipe or =ring in the environment forces one
-// kernel (a switch between complete kernels, for measurements); a row too long for two ring
-// slots per warp always takes a register kernel.
-constexpr int64_t kFwdRingMinRows = 6;
-
+// One row per warp, loaded straight into registers, each warp requesting its next row before
+// the current row's arithmetic (with two rows in registers fewer warps fit an SM; measured
+// against one row at a time: equal with bf16 output and 1% faster with E4M3 at 8192 x 4096, 3%
+// faster at 8192 x 2048).  TE_NORM_FWD_KERNEL=warp in the environment forces the one-row-at-a-
+// time form (a switch between complete kernels, for measurements).
 template <typename T, int NVW>
 te_status launch_fwd_nvw(const NormFwdArgs& a, cudaStream_t s) {
-  static const int forced = [] {
+  static const bool one_row = [] {
     const char* e = getenv("TE_NORM_FWD_KERNEL");
-    return !e ? 0 : e[0] == 'w' ? 1 : e[0] == 'r' ? 2 : e[0] == 'p' ? 3 : 0;
+    return e && e[0] == 'w';
   }();
   const bool ln = a.norm_type == TE_LAYERNORM;
-  const int slots = fwd_ring_slots(size_t(NVW) * 32 * 16, size_t(a.H) * (ln ? 2 : 1) * 4);
-  const bool long_run = a.M >= kFwdRingMinRows * kFwdRingWarps * num_sms();
-  const bool ring = forced == 2 || (forced == 0 && NVW == 16 && long_run);
-  // (forced == 3: the pipelined register kernel, also for long runs)
-  if (ring && slots >= 2)
-    return ln ? launch_fwd_ring<T, true, NVW>(a, slots, s) : launch_fwd_ring<T, false, NVW>(a, slots, s);
-  if (forced == 1)
+  if (one_row)
     return ln ? launch_fwd_warp<T, true, NVW, false>(a, s) : launch_fwd_warp<T, false, NVW, false>(a, s);
   return ln ? launch_fwd_warp<T, true, NVW, true>(a, s) : launch_fwd_warp<T, false, NVW, true>(a, s);
 }

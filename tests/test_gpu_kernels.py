@@ -294,10 +294,10 @@ def test_norm_fwd(norm, M, H, dtype, zc):
 @pytest.mark.parametrize("H,dtype", [(4096, "bf16"), (2048, "f32"), (8192, "bf16"), (4096, "f32")])
 @pytest.mark.parametrize("out_kind", ["same", "e4m3"])
 def test_norm_fwd_long_runs(norm, zc, H, dtype, out_kind):
-    """Enough rows (12000, a ragged number of rows per warp or CTA) for the staged kernels: rows
-    of 16 vectors per lane (a ring per warp) and bf16 rows of 8192 (a ring per CTA, which wraps
-    six times; fp32 rows of 4096 take the four-warp row kernel): y (or its E4M3 codes), mu,
-    rsigma and amax, with guard bands."""
+    """Long runs (12000 rows, a ragged number of rows per warp or CTA): rows of 16 vectors per
+    lane (one row per warp, each warp working through about ten rows with the next one in
+    flight), bf16 rows of 8192 (a ring per CTA, which wraps six times) and fp32 rows of 4096 (the
+    four-warp row kernel): y (or its E4M3 codes), mu, rsigma and amax, with guard bands."""
     M = 12000
     x = rt((M, H), std=1.5, seed=51, dtype=dtype, mean=0.25)
     gamma = rt((H,), std=0.1, seed=52, dtype=dtype, mean=0.0 if zc else 1.0)
