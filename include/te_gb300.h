@@ -141,7 +141,8 @@ size_t te_workspace_size(te_op op, int64_t M, int64_t H, int64_t F_or_N, te_dtyp
  * step (1), the tex.normalization_fwd primitive; I/O Contract: norm_type, zero_centered_gamma,
  * epsilon).
  *   x      [M, H] in x_dtype (TE_F32 or TE_BF16); gamma, beta [H] in x_dtype.
- *   layernorm: y = (x - mean) / sqrt(var + epsilon) * g + beta, var the population variance.
+ *   layernorm: y = (x - mean) / sqrt(var + epsilon) * g + beta, var the population variance;
+ *              a NULL beta is taken as zero.
  *   rmsnorm:   y = x / sqrt(mean(x^2) + epsilon) * g; beta is ignored and may be NULL.
  *   g = gamma, or 1 + gamma when zero_centered_gamma != 0.  All arithmetic is fp32.
  *   out    [M, H] in out_dtype: TE_F32, TE_BF16, or TE_E4M3 (then q is required).

@@ -290,6 +290,22 @@ def test_norm_fwd(norm, M, H, dtype, zc):
     assert abs(q.amax.item() - nx.amax_of(nx.to_f32(y))) <= 1e-5 * nx.amax_of(nx.to_f32(y))
 
 
+@pytest.mark.parametrize("M,H,dtype", [(1000, 4096, "bf16"), (300, 1024, "f32"), (70, 8192, "bf16"),
+                                       (129, 136, "bf16"), (65, 4096, "f32")])
+def test_layernorm_fwd_without_beta(M, H, dtype):
+    """A NULL beta is a zero beta, in every kernel form (one row per warp: 4096 bf16 and 1024
+    fp32; the eight-warp row-sharing kernel: 8192 bf16; the four-warp row kernel: 136 bf16 and
+    4096 fp32)."""
+    x = rt((M, H), std=1.5, seed=61, dtype=dtype, mean=-0.5)
+    gamma = rt((H,), std=0.1, seed=62, dtype=dtype, mean=1.0)
+    gout = Guarded((M, H), TDT[dtype])
+    te.te_norm_fwd(x, gamma, None, "layernorm", False, 1e-5, gout.t)
+    gout.check("y")
+    y, _, _ = ob.norm_fwd(np64(x), np64(gamma), np.zeros(H), "layernorm", False, 1e-5)
+    want = nx.to_f32(y) if dtype == "f32" else nx.bf16_round(nx.to_f32(y))
+    assert_elementwise_close(gout.t, want, what="layernorm y without beta")
+
+
 @pytest.mark.parametrize("norm,zc", [("layernorm", False), ("rmsnorm", True)])
 @pytest.mark.parametrize("H,dtype", [(4096, "bf16"), (2048, "f32"), (8192, "bf16"), (4096, "f32")])
 @pytest.mark.parametrize("out_kind", ["same", "e4m3"])
