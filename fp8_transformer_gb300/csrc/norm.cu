@@ -553,11 +553,14 @@ te_status launch_fwd_warp(const NormFwdArgs& a, cudaStream_t s) {
 constexpr int kFwdCtaWarps = 8;
 constexpr int kFwdCtaVecs = 1024 / (kFwdCtaWarps * 32);  // vectors per thread per row
 constexpr int kFwdCtaMaxSlots = 16;
-constexpr int kFwdCtaRows = 2;  // rows per barrier (measured: 1 and 4 slower; 16 warps slower;
-                                // for 4096-wide rows two CTAs of 4 warps per SM measured 10-20%
-                                // slower than one row per warp)
+// Rows per barrier: 2, and 4 with E4M3 output, whose longer chain of dependent arithmetic per
+// row gains from the wider step (measured at 16384 x 8192: bf16 output 7% slower with 4 rows,
+// E4M3 output 2% faster; 1 row slower for both; 16 warps slower; for 4096-wide rows two CTAs of
+// 4 warps per SM measured 10-30% slower than one row per warp).
+constexpr int kFwdCtaRows = 2;
+constexpr int kFwdCtaRowsE4M3 = 4;
 
-template <typename T, bool LN, int NV, int G>
+template <typename T, bool LN, int NV, int G, int RB>
 __global__ void __launch_bounds__(G * 32, G < 8 ? 8 / G : 1)
     norm_fwd_cta_kernel(NormFwdArgs a, int* status, int spc) {
   // the kernel after this one may launch its setup now (it waits for this grid's completion)
@@ -566,7 +569,6 @@ __global__ void __launch_bounds__(G * 32, G < 8 ? 8 / G : 1)
   constexpr int E = Vec16<T>::N;
   constexpr int P = PR::P;
   constexpr int GT = G * 32;
-  constexpr int RB = kFwdCtaRows;
   constexpr uint32_t row_bytes = uint32_t(GT * NV) * 16u;
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ float2 red[2][RB][G];
@@ -768,22 +770,30 @@ __global__ void __launch_bounds__(G * 32, G < 8 ? 8 / G : 1)
   if (lane == 0 && a.cast.amax_out) atomic_max_nonneg(a.cast.amax_out, amax);
 }
 
-template <typename T, bool LN, int NV, int G>
-te_status launch_fwd_cta(const NormFwdArgs& a, cudaStream_t s) {
+template <typename T, bool LN, int NV, int G, int RB>
+te_status launch_fwd_cta_rb(const NormFwdArgs& a, cudaStream_t s) {
   static PerDevice<bool> attr_done;
   constexpr size_t row_bytes = size_t(G) * 32 * NV * 16;
   constexpr int kCtas = G < 8 ? 8 / G : 1;  // CTAs per SM, sharing its shared memory
   const size_t cap = kCtas == 1 ? kRingSmemMax : size_t(227 * 1024) / kCtas - 1024;
-  // a step holds kFwdCtaRows slots; a second step's worth lets the refills run ahead
-  const int spc = ring_slots(row_bytes, kFwdCtaMaxSlots, 2 * kFwdCtaRows, kFwdCtaRows, cap);
+  // a step holds RB slots; a second step's worth lets the refills run ahead
+  const int spc = ring_slots(row_bytes, kFwdCtaMaxSlots, 2 * RB, RB, cap);
   if (spc == 0) return TE_ERR_UNSUPPORTED;
-  const te_status st = allow_ring_smem(norm_fwd_cta_kernel<T, LN, NV, G>, attr_done, kCtas > 1);
+  const te_status st =
+      allow_ring_smem(norm_fwd_cta_kernel<T, LN, NV, G, RB>, attr_done, kCtas > 1);
   if (st != TE_OK) return st;
   const size_t smem = ring_header_bytes(spc) + size_t(spc) * row_bytes;
   const int64_t n = int64_t(num_sms()) * kCtas;
   const unsigned grid = unsigned(a.M < n ? a.M : n);
-  norm_fwd_cta_kernel<T, LN, NV, G><<<grid, G * 32, smem, s>>>(a, device_status_ptr(), spc);
+  norm_fwd_cta_kernel<T, LN, NV, G, RB><<<grid, G * 32, smem, s>>>(a, device_status_ptr(), spc);
   return cudaGetLastError() == cudaSuccess ? TE_OK : TE_ERR_CUDA;
+}
+
+template <typename T, bool LN, int NV, int G>
+te_status launch_fwd_cta(const NormFwdArgs& a, cudaStream_t s) {
+  return a.cast.out_dtype == TE_E4M3 && a.cast.store
+             ? launch_fwd_cta_rb<T, LN, NV, G, kFwdCtaRowsE4M3>(a, s)
+             : launch_fwd_cta_rb<T, LN, NV, G, kFwdCtaRows>(a, s);
 }
 
 // One row per warp, loaded straight into registers, each warp requesting its next row before

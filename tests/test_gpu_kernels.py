@@ -339,6 +339,30 @@ def test_norm_fwd_long_runs(norm, zc, H, dtype, out_kind):
     assert abs(q.amax.item() - nx.amax_of(pre)) <= 1e-5 * nx.amax_of(pre)
 
 
+@pytest.mark.parametrize("M", [70, 300, 457])
+def test_norm_fwd_e4m3_8192_partial_steps(M):
+    """8192-wide bf16 rows with E4M3 output: the row-sharing kernel then works on four rows per
+    barrier, and these row counts leave CTAs with fewer rows than one step (and a partial last
+    step): codes, mu, rsigma and amax, with guard bands."""
+    H = 8192
+    x = rt((M, H), std=1.5, seed=71, mean=0.25)
+    gamma = rt((H,), std=0.1, seed=72, mean=1.0)
+    beta = rt((H,), std=0.1, seed=73)
+    gout, gmu, grs = Guarded((M, H), torch.uint8), Guarded((M,), torch.float32), Guarded((M,), torch.float32)
+    q = te.Quantizer(scale=16.0)
+    te.te_norm_fwd(x, gamma, beta, "layernorm", False, 1e-5, gout.t, q=q, mu=gmu.t, rsigma=grs.t)
+    for gb, name in ((gout, "y"), (gmu, "mu"), (grs, "rsigma")):
+        gb.check(name)
+    y, m_ref, r_ref = ob.norm_fwd(np64(x), np64(gamma), np64(beta), "layernorm", False, 1e-5)
+    pre = nx.to_f32(y)
+    assert_e4m3_codes(gout.t, nx.quantize(pre, np.float32(16.0)), pre32=pre,
+                      scale=np.float32(16.0), rel=1e-5, abs_tol=1e-5 * rms(pre),
+                      what="norm e4m3 8192")
+    assert_reduction_close(grs.t, r_ref, what="rsigma")
+    assert_reduction_close(gmu.t, m_ref, what="mu")
+    assert abs(q.amax.item() - nx.amax_of(pre)) <= 1e-5 * nx.amax_of(pre)
+
+
 @pytest.mark.parametrize("mode", ["delayed", "current"])
 def test_norm_fwd_e4m3(mode):
     M, H = 1000, 4096
