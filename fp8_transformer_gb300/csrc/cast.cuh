@@ -51,11 +51,15 @@ enum OutKind : int {
   OUT_NONE = 5        // amax pass of current scaling: nothing stored
 };
 
+__host__ __device__ __forceinline__ int out_kind_of(int store, int out_dtype, int fake_quant) {
+  if (!store) return OUT_NONE;
+  if (out_dtype == TE_E4M3) return OUT_E4M3;
+  if (fake_quant) return out_dtype == TE_F32 ? OUT_FAKE_F32 : OUT_FAKE_BF16;
+  return out_dtype == TE_F32 ? OUT_F32 : OUT_BF16;
+}
+
 __device__ __forceinline__ int out_kind(const CastState& cs) {
-  if (!cs.store) return OUT_NONE;
-  if (cs.out_dtype == TE_E4M3) return OUT_E4M3;
-  if (cs.fake_quant) return cs.out_dtype == TE_F32 ? OUT_FAKE_F32 : OUT_FAKE_BF16;
-  return cs.out_dtype == TE_F32 ? OUT_F32 : OUT_BF16;
+  return out_kind_of(cs.store, cs.out_dtype, cs.fake_quant);
 }
 
 template <int K>
@@ -81,11 +85,13 @@ struct BoolTag {
   static constexpr bool value = B;
 };
 
-// Calls f(OutTag<kind>{}, BoolTag<amax>{}) with both as compile-time constants.  The kinds that
-// quantize or only measure always take the amax (their callers always ask for it); plain fp32 /
-// bf16 stores take it when `want_amax`.
+// Calls f(OutTag<kind>{}, BoolTag<amax>{}) with both as compile-time constants (inside a kernel,
+// or on the host to pick a kernel compiled for one kind).  The kinds that quantize or only
+// measure always take the amax (their callers always ask for it); plain fp32 / bf16 stores take
+// it when `want_amax`.
+#pragma nv_exec_check_disable
 template <class F>
-__device__ __forceinline__ void with_out_amax(int kind, bool want_amax, F&& f) {
+__host__ __device__ __forceinline__ void with_out_amax(int kind, bool want_amax, F&& f) {
   switch (kind) {
     case OUT_F32:
       if (want_amax) f(OutTag<OUT_F32>{}, BoolTag<true>{});
